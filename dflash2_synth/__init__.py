@@ -1,0 +1,203 @@
+"""Seeded synthetic inputs for the DFlash2 draft step.
+
+This module only draws random numbers and converts storage formats.  It
+holds none of the method's arithmetic and imports neither the oracle nor the
+CUDA library; both the tests and ``bench.py`` take their inputs from here.
+
+Recipe (per workload, seed = 1000 + workload index):
+  * matrices ~ N(0, 0.02), norm gains ~ 1 + N(0, 0.1);
+  * target-layer taps ~ N(0, 1), each row divided by its RMS for the bf16
+    workloads (plain N(0, 1) for the tiny fp32 one);
+  * bf16 workloads round every drawn value to bfloat16 (nearest, ties to
+    even) before either side sees it, so both sides read identical values.
+Each tensor has its own PCG64 stream keyed by (seed, tensor name).
+"""
+
+import hashlib
+
+import numpy as np
+
+# ---------------------------------------------------------------------------
+# workloads (shapes from the pages' targets: a tiny fp32 case, an 8B-class
+# Qwen3 shape at batch 1 and batch 32, a 27B-class shape, a 30B-A3B-class
+# shape with fp8 weights)
+# ---------------------------------------------------------------------------
+
+_COMMON = dict(n_taps=3, conv_kernel_size=2, conv_group_size=32, page_size=16,
+               rms_eps=1e-6, rope_theta=1.0e6, input_embedding_scale=1.0,
+               output_multiplier=1.0, final_logit_softcap=0.0)
+
+WORKLOADS = {
+    "tiny_fp32": dict(_COMMON, index=0, dtype="f32", hidden=256, n_q_heads=4,
+                      n_kv_heads=4, head_dim=64, intermediate=1024, vocab=4096,
+                      n_layers=1, block_size=8, top_k=4, selector_rank=16,
+                      batch=1, context=128),
+    "qwen3_8b_b1": dict(_COMMON, index=1, dtype="bf16", hidden=4096, n_q_heads=32,
+                        n_kv_heads=8, head_dim=128, intermediate=12288,
+                        vocab=151936, n_layers=1, block_size=8, top_k=16,
+                        selector_rank=64, batch=1, context=2048),
+    "qwen3_8b_b32_paged": dict(_COMMON, index=2, dtype="bf16", hidden=4096,
+                               n_q_heads=32, n_kv_heads=8, head_dim=128,
+                               intermediate=12288, vocab=151936, n_layers=1,
+                               block_size=8, top_k=16, selector_rank=64,
+                               batch=32, context=(512, 4096), accept_p=0.7),
+    "qwen3_27b_b8": dict(_COMMON, index=3, dtype="bf16", hidden=5120, n_q_heads=40,
+                         n_kv_heads=8, head_dim=128, intermediate=17408,
+                         vocab=151936, n_layers=1, block_size=16, top_k=16,
+                         selector_rank=64, batch=8, context=8192),
+}
+
+
+def config_of(name, **over):
+    """Model/config dict of a workload (mask token = vocab - 1)."""
+    c = dict(WORKLOADS[name])
+    c.update(over)
+    c["mask_token_id"] = c["vocab"] - 1
+    return c
+
+
+# ---------------------------------------------------------------------------
+# format conversion (storage only)
+# ---------------------------------------------------------------------------
+
+def to_bf16_bits(x):
+    """float32 array -> uint16 bfloat16 bit patterns, nearest-even rounding."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    return ((u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(bits):
+    """uint16 bfloat16 bit patterns -> float32 values (exact)."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+class Tensor:
+    """A drawn tensor: exact float32 values plus, for bf16, its bit patterns."""
+
+    __slots__ = ("values", "bits")
+
+    def __init__(self, values, bits=None):
+        self.values = values
+        self.bits = bits
+
+    @property
+    def shape(self):
+        return self.values.shape
+
+
+def _rng(seed, name):
+    h = int.from_bytes(hashlib.sha256(name.encode()).digest()[:8], "little")
+    return np.random.Generator(np.random.PCG64([seed, h]))
+
+
+def _draw(seed, name, shape, std, dtype, mean=0.0):
+    x = _rng(seed, name).standard_normal(size=shape, dtype=np.float32)
+    if std != 1.0:
+        x *= np.float32(std)
+    if mean != 0.0:
+        x += np.float32(mean)
+    if dtype == "bf16":
+        bits = to_bf16_bits(x)
+        return Tensor(bf16_bits_to_f32(bits), bits)
+    return Tensor(x)
+
+
+def make_weights(cfg, seed=None):
+    """All draft weights of a workload, as a dict of Tensor (layers: list)."""
+    seed = 1000 + cfg["index"] if seed is None else seed
+    dt = cfg["dtype"]
+    H, V, T = cfg["hidden"], cfg["vocab"], cfg["n_taps"]
+    nq, nkv, d, I = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"], cfg["intermediate"]
+    G = H // cfg["conv_group_size"]
+    kc, r = cfg["conv_kernel_size"], cfg["selector_rank"]
+    w = {
+        "embed": _draw(seed, "embed", (V, H), 0.02, dt),
+        "lm_head": _draw(seed, "lm_head", (V, H), 0.02, dt),
+        "fc": _draw(seed, "fc", (H, T * H), 0.02, dt),
+        "hidden_norm": _draw(seed, "hidden_norm", (H,), 0.1, dt, 1.0),
+        "final_norm": _draw(seed, "final_norm", (H,), 0.1, dt, 1.0),
+        "sel": _draw(seed, "sel", (2 * r, H), 0.02, dt),
+        "layers": [],
+    }
+    for l in range(cfg["n_layers"]):
+        p = f"layer{l}."
+        w["layers"].append({
+            "attn_norm": _draw(seed, p + "attn_norm", (H,), 0.1, dt, 1.0),
+            "tapgen_attn": _draw(seed, p + "tapgen_attn", (kc * G, H), 0.02, dt),
+            "qkv": _draw(seed, p + "qkv", ((nq + 2 * nkv) * d, H), 0.02, dt),
+            "q_norm": _draw(seed, p + "q_norm", (d,), 0.1, dt, 1.0),
+            "k_norm": _draw(seed, p + "k_norm", (d,), 0.1, dt, 1.0),
+            "o": _draw(seed, p + "o", (H, nq * d), 0.02, dt),
+            "mlp_norm": _draw(seed, p + "mlp_norm", (H,), 0.1, dt, 1.0),
+            "tapgen_mlp": _draw(seed, p + "tapgen_mlp", (kc * G, H), 0.02, dt),
+            "gate_up": _draw(seed, p + "gate_up", (2 * I, H), 0.02, dt),
+            "down": _draw(seed, p + "down", (H, I), 0.02, dt),
+        })
+    return w
+
+
+def values_of(w):
+    """Weight dict of Tensor -> weight dict of float32 value arrays."""
+    out = {k: v.values for k, v in w.items() if k != "layers"}
+    out["layers"] = [{k: v.values for k, v in L.items()} for L in w["layers"]]
+    return out
+
+
+def make_taps(cfg, n_rows, seed=None, stream="taps"):
+    """[n_rows, T*H] target-layer taps (row-RMS-normalised for bf16)."""
+    seed = 1000 + cfg["index"] if seed is None else seed
+    x = _rng(seed, stream).standard_normal(size=(n_rows, cfg["n_taps"] * cfg["hidden"]),
+                                           dtype=np.float32)
+    if cfg["dtype"] == "bf16":
+        x /= np.sqrt(np.mean(x.astype(np.float64) ** 2, axis=1, keepdims=True)).astype(np.float32)
+        bits = to_bf16_bits(x)
+        return Tensor(bf16_bits_to_f32(bits), bits)
+    return Tensor(x)
+
+
+def make_context_lengths(cfg, seed=None):
+    """Per-sequence context lengths (fixed, or uniform in [lo, hi])."""
+    seed = 1000 + cfg["index"] if seed is None else seed
+    c = cfg["context"]
+    if isinstance(c, tuple):
+        return _rng(seed, "ctx_len").integers(c[0], c[1] + 1, size=cfg["batch"]).astype(np.int32)
+    return np.full(cfg["batch"], c, dtype=np.int32)
+
+
+def make_tokens(cfg, shape, seed=None, stream="tokens"):
+    """Uniform random token ids in [0, vocab - 1) (never the mask id)."""
+    seed = 1000 + cfg["index"] if seed is None else seed
+    return _rng(seed, stream).integers(0, cfg["vocab"] - 1, size=shape).astype(np.int32)
+
+
+def make_target_logits(cfg, seed=None, stream="target_logits"):
+    """[b, B, V] float32 N(0,1) logits whose argmax is the toy target's token."""
+    seed = 1000 + cfg["index"] if seed is None else seed
+    return _rng(seed, stream).standard_normal(
+        size=(cfg["batch"], cfg["block_size"], cfg["vocab"]), dtype=np.float32)
+
+
+def make_agreeing_target(path, cfg, p, seed=None, stream="agree"):
+    """Target tokens that agree with the proposed path at each position with
+    probability p (else a different random token); the bonus slot is random.
+    path [b, D] -> target [b, D+1]."""
+    seed = 1000 + cfg["index"] if seed is None else seed
+    g = _rng(seed, stream)
+    b, D = path.shape
+    V = cfg["vocab"]
+    t = g.integers(0, V - 1, size=(b, D + 1)).astype(np.int32)
+    agree = g.random(size=(b, D)) < p
+    other = t[:, :D]
+    other = np.where(other == path, (other + 1) % (V - 1), other)
+    t[:, :D] = np.where(agree, path, other)
+    return t
+
+
+def paged_layout(ctx_cap, page_size, batch, seed, spare_pages=0):
+    """Block table [batch, max_pages] as a seeded random permutation of
+    physical pages; returns (block_table int32, n_pages)."""
+    max_pages = -(-int(ctx_cap) // page_size)
+    n_pages = batch * max_pages + spare_pages
+    perm = _rng(seed, "pages").permutation(n_pages).astype(np.int32)
+    return perm[: batch * max_pages].reshape(batch, max_pages), n_pages

@@ -1,0 +1,487 @@
+"""Pins of the CPU oracle to facts outside itself (closed forms, special cases
+that reduce to a library routine, brute force, hand-worked golden cases).
+
+Each test names the oracle function it pins and the fact it uses.  A plausible
+mistake (dropped term, wrong sign or index, transposed operand) in the pinned
+function should fail at least one of them.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from tests.conftest import read_golden
+
+
+def tiny_cfg(**over):
+    c = dict(hidden=64, n_q_heads=4, n_kv_heads=2, head_dim=16, intermediate=96,
+             vocab=50, n_layers=1, n_taps=3, block_size=4, conv_kernel_size=2,
+             conv_group_size=8, top_k=3, selector_rank=4, page_size=16,
+             mask_token_id=49, rms_eps=1e-6, rope_theta=1.0e4,
+             input_embedding_scale=1.0, output_multiplier=1.0,
+             final_logit_softcap=0.0)
+    c.update(over)
+    return c
+
+
+def tiny_weights(cfg, seed=0, scale=0.3):
+    g = np.random.default_rng(seed)
+    H, V, T = cfg["hidden"], cfg["vocab"], cfg["n_taps"]
+    nq, nkv, d, I = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"], cfg["intermediate"]
+    G = H // cfg["conv_group_size"]
+    kc, r = cfg["conv_kernel_size"], cfg["selector_rank"]
+    n = lambda *s: g.standard_normal(s) * scale
+    one = lambda k: 1.0 + 0.1 * g.standard_normal(k)
+    W = dict(embed=n(V, H), lm_head=n(V, H), fc=n(H, T * H) / math.sqrt(T),
+             hidden_norm=one(H), final_norm=one(H), sel=n(2 * r, H), layers=[])
+    for _ in range(cfg["n_layers"]):
+        W["layers"].append(dict(
+            attn_norm=one(H), tapgen_attn=n(kc * G, H), qkv=n((nq + 2 * nkv) * d, H) / 4,
+            q_norm=one(d), k_norm=one(d), o=n(H, nq * d) / 4, mlp_norm=one(H),
+            tapgen_mlp=n(kc * G, H), gate_up=n(2 * I, H) / 4, down=n(H, I) / 4))
+    return W
+
+
+def empty_ctx(cfg):
+    z = np.zeros((0, cfg["n_kv_heads"], cfg["head_dim"]))
+    return [(z, z) for _ in range(cfg["n_layers"])]
+
+
+# ----------------------------------------------------------------- bf16_round
+
+def test_bf16_round_ties_to_even_exact_values():
+    # 1 + 2^-8 is the midpoint of 1 and 1 + 2^-7: ties go to the even mantissa (1.0)
+    assert O.bf16_round(1.0 + 2.0 ** -8) == 1.0
+    # 1 + 3*2^-8 is the midpoint of 1+2^-7 (odd) and 1+2^-6 (even)
+    assert O.bf16_round(1.0 + 3 * 2.0 ** -8) == 1.0 + 2.0 ** -6
+    assert O.bf16_round(-(1.0 + 3 * 2.0 ** -8)) == -(1.0 + 2.0 ** -6)
+    assert O.bf16_round(0.0) == 0.0
+    assert O.bf16_round(3.0) == 3.0
+    # just above a midpoint rounds up
+    assert O.bf16_round(1.0 + 2.0 ** -8 + 2.0 ** -30) == 1.0 + 2.0 ** -7
+
+
+def test_bf16_round_matches_torch_conversion():
+    g = np.random.default_rng(1)
+    x = np.concatenate([g.standard_normal(20000) * 10.0 ** g.integers(-30, 30, 20000),
+                        g.standard_normal(1000) * 1e-39])       # bf16 subnormals
+    x32 = x.astype(np.float32)
+    ref = torch.from_numpy(x32).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.bf16_round(x32.astype(np.float64)), ref)
+
+
+# ------------------------------------------------------------------- rms_norm
+
+def test_rms_norm_matches_torch_and_closed_form():
+    g = np.random.default_rng(2)
+    x = g.standard_normal((5, 33))
+    gam = g.standard_normal(33)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (33,), torch.from_numpy(gam),
+                                       eps=1e-6).numpy()
+    np.testing.assert_allclose(O.rms_norm(x, gam, 1e-6), ref, rtol=1e-12, atol=1e-12)
+    # constant vector c*1: each entry becomes c / sqrt(c^2 + eps) * gamma
+    c, eps = -0.37, 1e-3
+    y = O.rms_norm(np.full(8, c), np.arange(1, 9, dtype=float), eps)
+    np.testing.assert_allclose(y, c / math.sqrt(c * c + eps) * np.arange(1, 9), rtol=1e-14)
+
+
+# ----------------------------------------------------------------------- rope
+
+def test_rope_d2_is_a_plane_rotation_by_pos_radians():
+    # d = 2: one frequency theta^0 = 1, so the angle is the position itself
+    x = np.array([[[0.3, -1.2]]])
+    for pos in (0, 1, 5, 1000):
+        y = O.rope(x, np.array([pos]), 1.0e6)[0, 0]
+        c, s = math.cos(pos), math.sin(pos)
+        np.testing.assert_allclose(y, [0.3 * c + 1.2 * s, -1.2 * c + 0.3 * s], rtol=1e-12, atol=1e-15)
+
+
+def test_rope_relative_position_and_norm():
+    g = np.random.default_rng(3)
+    q = g.standard_normal((1, 1, 64))
+    k = g.standard_normal((1, 1, 64))
+    dot = lambda m, n: float(np.sum(O.rope(q, np.array([m]), 1e6) * O.rope(k, np.array([n]), 1e6)))
+    assert abs(dot(10, 3) - dot(1010, 1003)) < 1e-9
+    assert abs(dot(7, 7) - float(np.sum(q * k))) < 1e-9
+    assert abs(dot(5, 9) - dot(9, 5)) > 1e-6            # the rotation has a direction
+    y = O.rope(q, np.array([12345]), 1e6)
+    assert abs(np.linalg.norm(y) - np.linalg.norm(q)) < 1e-12
+    # pair i mixes with i + d/2 (rotate-half), not with i+1
+    e0 = np.zeros((1, 1, 8)); e0[0, 0, 0] = 1.0
+    y = O.rope(e0, np.array([1]), 1e4)[0, 0]
+    assert np.count_nonzero(np.abs(y) > 1e-15) == 2 and abs(y[4]) > 0.5
+
+
+def test_silu_matches_torch():
+    x = np.linspace(-20, 20, 1001)
+    np.testing.assert_allclose(O.silu(x), torch.nn.functional.silu(torch.from_numpy(x)).numpy(),
+                               rtol=1e-12, atol=1e-300)
+
+
+# --------------------------------------------------------------- dynamic conv
+
+def test_dynamic_conv_zero_generator_is_two_tap_average():
+    g = np.random.default_rng(4)
+    u = g.standard_normal((6, 32))
+    c = O.dynamic_conv(u, np.zeros((2 * 4, 32)), group_size=8)
+    prev = np.vstack([np.zeros((1, 32)), u[:-1]])
+    np.testing.assert_allclose(c, 0.5 * (u + prev), rtol=0, atol=1e-15)
+
+
+def test_dynamic_conv_is_left_looking_and_grouped():
+    g = np.random.default_rng(5)
+    u = g.standard_normal((8, 32))
+    w = g.standard_normal((8, 32))
+    c = O.dynamic_conv(u, w, group_size=8)
+    u2 = u.copy(); u2[5:] += 3.0
+    c2 = O.dynamic_conv(u2, w, group_size=8)
+    np.testing.assert_array_equal(c[:5], c2[:5])                 # t < 5 unchanged
+    # a generator that sends group 1 hard to tap 0 and group 2 hard to tap 1
+    H, gs = 32, 8
+    w = np.zeros((8, H))
+    u = np.abs(u) + 0.5                                          # positive so sum(u) > 0
+    w[2 * 1 + 0] = 100.0                                         # group 1, tap 0 (current)
+    w[2 * 2 + 1] = 100.0                                         # group 2, tap 1 (previous)
+    c = O.dynamic_conv(u, w, group_size=gs)
+    np.testing.assert_allclose(c[:, 8:16], u[:, 8:16], atol=1e-12)
+    prev = np.vstack([np.zeros((1, H)), u[:-1]])
+    np.testing.assert_allclose(c[:, 16:24], prev[:, 16:24], atol=1e-12)
+    np.testing.assert_allclose(c[:, 0:8], 0.5 * (u + prev)[:, 0:8], atol=1e-12)
+
+
+# ------------------------------------------------------------------ attention
+
+def test_block_attention_special_cases():
+    g = np.random.default_rng(6)
+    d = 8
+    # one key (no context, block of one): output is that value
+    q = g.standard_normal((1, 2, d)); kb = g.standard_normal((1, 1, d)); vb = g.standard_normal((1, 1, d))
+    z = np.zeros((0, 1, d))
+    out = O.block_attention(q, z, z, kb, vb)
+    np.testing.assert_allclose(out[0, 0], vb[0, 0], rtol=1e-14)
+    np.testing.assert_allclose(out[0, 1], vb[0, 0], rtol=1e-14)
+    # identical keys: uniform weights, output = mean of all values (context and block)
+    kc = np.tile(kb, (5, 1, 1)); vc = g.standard_normal((5, 1, d))
+    kb3 = np.tile(kb, (3, 1, 1)); vb3 = g.standard_normal((3, 1, d))
+    q3 = g.standard_normal((3, 2, d))
+    out = O.block_attention(q3, kc, vc, kb3, vb3)
+    mean = np.concatenate([vc, vb3])[:, 0].mean(0)
+    np.testing.assert_allclose(out, np.broadcast_to(mean, out.shape), rtol=1e-12)
+
+
+def test_block_attention_matches_sdpa_non_causal_gqa():
+    g = np.random.default_rng(7)
+    B, nq, nkv, d, P = 5, 6, 2, 16, 9
+    q = g.standard_normal((B, nq, d)); Kc = g.standard_normal((P, nkv, d)); Vc = g.standard_normal((P, nkv, d))
+    Kb = g.standard_normal((B, nkv, d)); Vb = g.standard_normal((B, nkv, d))
+    out = O.block_attention(q, Kc, Vc, Kb, Vb)
+    K = torch.from_numpy(np.concatenate([Kc, Kb])).permute(1, 0, 2).repeat_interleave(nq // nkv, 0)
+    V = torch.from_numpy(np.concatenate([Vc, Vb])).permute(1, 0, 2).repeat_interleave(nq // nkv, 0)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q).permute(1, 0, 2), K, V, is_causal=False).permute(1, 0, 2).numpy()
+    np.testing.assert_allclose(out, ref, rtol=1e-10, atol=1e-12)
+    # the first block query sees the last block key (non-causal)
+    Kb2 = Kb.copy(); Kb2[B - 1] += 1.0
+    assert not np.allclose(O.block_attention(q, Kc, Vc, Kb2, Vb)[0], out[0])
+
+
+# --------------------------------------------------------- feature projection
+
+def test_feature_projection_identity_blocks_select_taps():
+    cfg = tiny_cfg()
+    W = tiny_weights(cfg)
+    H, T = cfg["hidden"], cfg["n_taps"]
+    g = np.random.default_rng(8)
+    taps = g.standard_normal((3, T * H))
+    st = O.Store(False)
+    for t in range(T):
+        W["fc"] = np.zeros((H, T * H)); W["fc"][:, t * H:(t + 1) * H] = np.eye(H)
+        f = O.project_features(cfg, W, taps, st)
+        np.testing.assert_allclose(f, O.rms_norm(taps[:, t * H:(t + 1) * H], W["hidden_norm"], 1e-6),
+                                   rtol=1e-12)
+
+
+def test_context_kv_identity_projection():
+    cfg = tiny_cfg(hidden=32, n_q_heads=2, n_kv_heads=1, head_dim=16)
+    H, d = 32, 16
+    Wl = {"qkv": np.zeros((4 * d, H)), "k_norm": np.full(d, 2.0)}
+    Wl["qkv"][2 * d:3 * d, :d] = np.eye(d)        # W_k reads f[:, :16]
+    Wl["qkv"][3 * d:4 * d, d:] = np.eye(d)        # W_v reads f[:, 16:]
+    f = np.random.default_rng(9).standard_normal((4, H))
+    pos = np.array([0, 3, 4, 100])
+    k, v = O.context_kv(cfg, Wl, f, pos, O.Store(False))
+    np.testing.assert_allclose(v[:, 0], f[:, d:], rtol=1e-15)
+    np.testing.assert_allclose(k[0, 0], O.rms_norm(f[0, :d], np.full(d, 2.0), 1e-6), rtol=1e-12)
+    np.testing.assert_allclose(k[:, 0], O.rope(O.rms_norm(f[:, None, :d], np.full(d, 2.0), 1e-6), pos,
+                                               cfg["rope_theta"])[:, 0], rtol=1e-12)
+
+
+# ---------------------------------------------------------------- draft block
+
+def test_draft_layer_residual_identity_when_outputs_zero():
+    cfg = tiny_cfg()
+    W = tiny_weights(cfg)
+    Wl = dict(W["layers"][0]); Wl["o"] = np.zeros_like(Wl["o"]); Wl["down"] = np.zeros_like(Wl["down"])
+    h = np.random.default_rng(10).standard_normal((4, cfg["hidden"]))
+    out = O.draft_layer(cfg, Wl, h, *empty_ctx(cfg)[0], np.arange(4), O.Store(False))
+    np.testing.assert_array_equal(out, h)
+
+
+def test_draft_block_invariant_to_common_position_shift():
+    # scores depend on relative positions only: shifting the context's and the
+    # block's positions together leaves the logits unchanged (anchor at P).
+    cfg = tiny_cfg()
+    W = tiny_weights(cfg)
+    taps = np.random.default_rng(11).standard_normal((6, cfg["n_taps"] * cfg["hidden"]))
+    st = O.Store(False)
+    ctx0 = O.append_context(cfg, W, empty_ctx(cfg), taps, 0, st)
+    z0 = O.draft_block(cfg, W, 7, ctx0, st)
+    # context keys at positions 40..45 but the block still placed right after 6
+    # context rows (draft_block puts the anchor at the context length): a
+    # mismatched offset, which must change the logits
+    ctx40 = O.append_context(cfg, W, empty_ctx(cfg), taps, 40, st)
+    z40 = O.draft_block(cfg, W, 7, ctx40, st)
+    # both context and block moved by 40, built by hand from the same pieces
+    f = O.project_features(cfg, W, taps, st)
+    k, v = O.context_kv(cfg, W["layers"][0], f, 40 + np.arange(6), st)
+    B = cfg["block_size"]
+    toks = np.array([7] + [cfg["mask_token_id"]] * (B - 1))
+    h = W["embed"][toks].astype(np.float64)
+    h = O.draft_layer(cfg, W["layers"][0], h, k, v, 46 + np.arange(B), st)
+    z_shift = (O.rms_norm(h[1:], W["final_norm"], 1e-6) @ W["lm_head"].T)
+    np.testing.assert_allclose(z_shift, z0, rtol=1e-9, atol=1e-10)
+    assert not np.allclose(z40, z0, atol=1e-6)      # a mismatched offset does change it
+
+
+def test_draft_block_softcap_and_multiplier():
+    cfg = tiny_cfg()
+    W = tiny_weights(cfg)
+    st = O.Store(False)
+    ctx = O.append_context(cfg, W, empty_ctx(cfg), np.ones((2, cfg["n_taps"] * cfg["hidden"])), 0, st)
+    z = O.draft_block(cfg, W, 3, ctx, st)
+    z2 = O.draft_block(dict(cfg, output_multiplier=2.5), W, 3, ctx, st)
+    np.testing.assert_allclose(z2, 2.5 * z, rtol=1e-13)
+    z3 = O.draft_block(dict(cfg, final_logit_softcap=0.5), W, 3, ctx, st)
+    np.testing.assert_allclose(z3, 0.5 * np.tanh(z / 0.5), rtol=1e-13)
+    assert np.all(np.abs(z3) < 0.5)
+
+
+def test_draft_block_anchor_is_the_only_non_mask_token():
+    cfg = tiny_cfg()
+    W = tiny_weights(cfg)
+    st = O.Store(False)
+    ctx = O.append_context(cfg, W, empty_ctx(cfg), np.ones((2, cfg["n_taps"] * cfg["hidden"])), 0, st)
+    za = O.draft_block(cfg, W, 3, ctx, st)
+    zb = O.draft_block(cfg, W, 4, ctx, st)
+    assert za.shape == (cfg["block_size"] - 1, cfg["vocab"])
+    assert not np.allclose(za, zb)
+    # anchor == mask id gives a block of identical tokens; only the left-looking
+    # conv and positions tell positions apart
+    zm = O.draft_block(cfg, W, cfg["mask_token_id"], ctx, st)
+    assert np.all(np.isfinite(zm))
+
+
+# ----------------------------------------------------------------------- top-k
+
+def _topk_by_selection(z, k):
+    z = list(z)
+    chosen = []
+    for _ in range(k):
+        best = None
+        for i, v in enumerate(z):
+            if i in chosen:
+                continue
+            if best is None or v > z[best]:
+                best = i
+        chosen.append(best)
+    return chosen
+
+
+def test_topk_golden_ties():
+    for k, vals, exp in read_golden("topk_ties.txt"):
+        z = np.array([float(x) for x in vals.split()])
+        ids, v = O.topk(z, int(k))
+        assert list(ids) == [int(x) for x in exp.split()]
+        np.testing.assert_array_equal(v, z[ids])
+
+
+def test_topk_matches_selection_with_many_ties():
+    g = np.random.default_rng(12)
+    for _ in range(50):
+        z = g.integers(-3, 4, size=40).astype(float)        # heavy ties
+        ids, _ = O.topk(z, 7)
+        assert list(ids) == _topk_by_selection(z, 7)
+
+
+# -------------------------------------------------------------------- selector
+
+def _sel_case(k, D, seed, scale=1.0):
+    cfg = tiny_cfg(vocab=200, hidden=32, selector_rank=4, top_k=k, block_size=D + 1)
+    g = np.random.default_rng(seed)
+    W = {"embed": g.standard_normal((200, 32)), "sel": g.standard_normal((8, 32)) * 0.3 * scale}
+    cand = np.stack([g.choice(199, size=k, replace=False) for _ in range(D)])
+    z = np.sort(g.standard_normal((D, k)), axis=1)[:, ::-1].copy()
+    return cfg, W, int(g.integers(0, 199)), cand, z
+
+
+@pytest.mark.parametrize("k,D,seed", [(4, 7, 0), (3, 5, 1), (3, 5, 2), (2, 6, 3), (4, 4, 4)])
+def test_viterbi_equals_brute_force(k, D, seed):
+    cfg, W, anchor, cand, z = _sel_case(k, D, seed)
+    p, idx, s = O.select_path(cfg, W, anchor, cand, z)
+    pb, idxb, sb = O.brute_force_path(cfg, W, anchor, cand, z)
+    assert list(idx) == list(idxb)
+    assert list(p) == list(pb)
+    assert abs(s - sb) < 1e-12
+
+
+def test_viterbi_pairwise_term_changes_path():
+    # with N(0,1)-scale factors some lattices pick a path other than the per-
+    # position argmax, so the pairwise term is really used
+    changed = 0
+    for seed in range(40):
+        cfg, W, anchor, cand, z = _sel_case(3, 5, 100 + seed, scale=3.0)
+        _, idx, _ = O.select_path(cfg, W, anchor, cand, z)
+        changed += int(np.any(idx != 0))
+    assert changed > 0
+
+
+def test_selector_without_pairwise_term_is_per_position_top1():
+    cfg, W, anchor, cand, z = _sel_case(4, 7, 5)
+    W["sel"] = np.zeros_like(W["sel"])
+    p, idx, s = O.select_path(cfg, W, anchor, cand, z)
+    assert list(idx) == [0] * 7                       # z sorted descending per position
+    lse = np.log(np.exp(z).sum(1))
+    assert abs(s - float(np.sum(z[:, 0] - lse))) < 1e-12
+
+
+def test_selector_two_position_hand_example():
+    # k = 2, D = 2, rank 1.  E rows: token t -> [t], W_a = [1], W_b = [1],
+    # so <A[p], Bf[c]> = p * c.  Anchor 1; candidates pos1 = (2, 0), pos2 = (0, 3),
+    # logits all zero.  Position 1 after anchor 1: scores (2, 0).
+    # Position 2 after 2: scores (0, 6); after 0: scores (0, 0).
+    cfg = dict(selector_rank=1)
+    W = {"embed": np.arange(5, dtype=float)[:, None], "sel": np.array([[1.0], [1.0]])}
+    cand = np.array([[2, 0], [0, 3]])
+    z = np.zeros((2, 2))
+    p, idx, s = O.select_path(cfg, W, 1, cand, z)
+    l1 = 2 - math.log(math.exp(2) + 1)
+    l2 = 6 - math.log(1 + math.exp(6))
+    assert list(p) == [2, 3]
+    assert abs(s - (l1 + l2)) < 1e-14
+
+
+def test_selector_ties_pick_smallest_indices():
+    cfg = dict(selector_rank=1)
+    W = {"embed": np.zeros((10, 1)), "sel": np.zeros((2, 1))}
+    cand = np.array([[4, 5, 6], [7, 8, 9]])
+    p, idx, s = O.select_path(cfg, W, 0, cand, np.zeros((2, 3)))
+    assert list(idx) == [0, 0]
+    assert abs(s - 2 * math.log(1 / 3)) < 1e-14
+
+
+# ---------------------------------------------------------------------- verify
+
+def test_verify_golden_cases():
+    for path, tgt, a, out, nxt in read_golden("verify_cases.txt"):
+        path = [int(x) for x in path.split()]
+        tgt = [int(x) for x in tgt.split()]
+        ga, gout, gn = O.verify_accept(path, tgt)
+        assert ga == int(a)
+        assert gout == [int(x) for x in out.split()]
+        assert gn == int(nxt)
+
+
+def test_counter_identities():
+    g = np.random.default_rng(13)
+    c = O.Counters(7)
+    for _ in range(500):
+        path = g.integers(0, 3, 7)
+        tgt = g.integers(0, 3, 8)
+        a, out, _ = O.verify_accept(path, tgt)
+        assert 0 <= a <= 7 and len(out) == a + 1
+        c.add(a)
+    assert c.hist.sum() == c.steps == 500
+    assert c.drafted == 7 * c.steps
+    assert c.accepted + c.rollback == c.drafted
+    assert 0.0 <= c.acceptance_rate <= 1.0
+    assert abs(c.mean_acceptance_length - (1 + c.accepted / c.steps)) < 1e-15
+    assert c.acc_pos[0] == c.steps - c.hist[0]
+    assert np.all(np.diff(c.acc_pos) <= 0)
+    assert c.accepted == c.acc_pos.sum()
+
+
+def test_geometric_acceptance_closed_form():
+    # target agrees with the proposal independently with p at each position:
+    # E[a] = sum_{m=1}^{D} p^m (2.1412 for p = 0.7, D = 7)
+    g = np.random.default_rng(14)
+    p, D, n = 0.7, 7, 40000
+    c = O.Counters(D)
+    for _ in range(n):
+        path = g.integers(0, 1000, D)
+        agree = g.random(D) < p
+        tgt = np.append(np.where(agree, path, path + 1000), 5)
+        c.add(O.verify_accept(path, tgt)[0])
+    expect = sum(p ** m for m in range(1, D + 1))
+    sd = np.sqrt(np.sum((np.arange(D + 1) - expect) ** 2 * c.hist) / n)
+    assert abs(c.accepted / n - expect) < 4 * sd / math.sqrt(n)
+    assert abs(expect - 2.1412) < 1e-4
+
+
+# --------------------------------------------------------------- loss decay
+
+def test_loss_decay_golden():
+    for B, gamma, k, expr in read_golden("loss_decay.txt"):
+        w = O.loss_decay_weights(int(B), float(gamma))
+        assert len(w) == int(B) - 1
+        exact = 1.0 if expr == "1" else math.exp(eval(expr[4:-1], {}))
+        assert abs(w[int(k) - 1] - exact) < 1e-15
+    w = O.loss_decay_weights(16, 7.0)
+    np.testing.assert_allclose(w[1:] / w[:-1], math.exp(-1 / 7), rtol=1e-14)
+
+
+# ------------------------------------------------------------- lossless loop
+
+@pytest.mark.parametrize("D,kind", [(7, "random"), (7, "perfect"), (3, "wrong"), (5, "mixed")])
+def test_speculative_generation_is_lossless(D, kind):
+    g = np.random.default_rng(15)
+    V = 64
+    table = g.integers(0, V, V)
+    greedy = O.greedy_generate(table, 3, 200)
+
+    def propose(anchor):
+        if kind == "random":
+            return list(g.integers(0, V, D))
+        out, t = [], anchor
+        for i in range(D):
+            t = int(table[t])
+            if kind == "wrong" or (kind == "mixed" and g.random() < 0.3):
+                out.append((t + 1) % V)
+                t = out[-1]
+            else:
+                out.append(t)
+        return out
+
+    spec, cnt = O.speculative_generate(table, 3, 200, propose)
+    assert spec == greedy
+    if kind == "perfect":
+        assert cnt.hist[D] == cnt.steps
+    if kind == "wrong":
+        assert cnt.accepted == 0
+
+
+def test_bf16_storage_mode_rounds_block_outputs():
+    cfg = tiny_cfg()
+    W = tiny_weights(cfg)
+    st = O.Store(True)
+    taps = O.bf16_round(np.random.default_rng(16).standard_normal((4, cfg["n_taps"] * cfg["hidden"])))
+    ctx = O.append_context(cfg, W, empty_ctx(cfg), taps, 0, st)
+    for K, V in ctx:
+        np.testing.assert_array_equal(K, O.bf16_round(K))
+        np.testing.assert_array_equal(V, O.bf16_round(V))
+    z16 = O.draft_block(cfg, W, 5, ctx, st)
+    z64 = O.draft_block(cfg, W, 5, O.append_context(cfg, W, empty_ctx(cfg), taps, 0, O.Store(False)),
+                        O.Store(False))
+    assert 0 < np.max(np.abs(z16 - z64)) < 0.2

@@ -1,0 +1,224 @@
+"""ctypes binding of libdflash2.so: argument marshalling only.
+
+Every function here has the name of the C entry point it calls and does no
+arithmetic of its own: it turns torch tensors into device pointers, Python
+numbers into C ints/floats, and raises ``DFlash2Error`` on a non-OK status.
+There is no fallback: without the built library, loading raises.
+"""
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdflash2.so")
+
+F32 = 0
+BF16 = 1
+
+STATUS = {0: "ok", -1: "invalid argument", -2: "shape", -3: "block size", -4: "dtype",
+          -5: "workspace", -6: "cuda", -7: "unsupported"}
+DEV_BAD_PAGE, DEV_BAD_TOKEN, DEV_WAIT_TIMEOUT, DEV_BAD_LENGTH = 0x1, 0x2, 0x4, 0x8
+
+
+class DFlash2Error(RuntimeError):
+    def __init__(self, fn, status, text):
+        super().__init__(f"{fn} failed: status {status} ({text})")
+        self.status = status
+
+
+class Config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "hidden", "n_q_heads", "n_kv_heads", "head_dim", "intermediate", "vocab",
+        "n_layers", "n_taps", "block_size", "conv_kernel_size", "conv_group_size",
+        "top_k", "selector_rank", "page_size", "mask_token_id", "dtype")] + \
+        [(n, ctypes.c_float) for n in (
+            "rms_eps", "rope_theta", "input_embedding_scale", "output_multiplier",
+            "final_logit_softcap")]
+
+
+_LAYER_FIELDS = ("attn_norm", "tapgen_attn", "qkv", "q_norm", "k_norm", "o", "mlp_norm",
+                 "tapgen_mlp", "gate_up", "down")
+
+
+class LayerWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in _LAYER_FIELDS]
+
+
+_TOP_FIELDS = ("embed", "lm_head", "fc", "hidden_norm", "final_norm", "sel")
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in _TOP_FIELDS] + [("layers", ctypes.POINTER(LayerWeights))]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library (raises if it was never built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                              "(the product path has no fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, S, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.POINTER
+        L.dflash2_status_string.restype = ctypes.c_char_p
+        L.dflash2_status_string.argtypes = [I]
+        L.dflash2_version.restype = I
+        L.dflash2_validate_config.restype = I
+        L.dflash2_validate_config.argtypes = [F(Config)]
+        L.dflash2_workspace_size.restype = S
+        L.dflash2_workspace_size.argtypes = [F(Config), I, I, I]
+        L.dflash2_append_context.restype = I
+        L.dflash2_append_context.argtypes = [F(Config), F(Weights), P, P, I, P, I, I, P, I, P, P, P, S, P]
+        L.dflash2_draft_step.restype = I
+        L.dflash2_draft_step.argtypes = [F(Config), F(Weights), P, P, I, P, I, I, P, I, P, P, P,
+                                         P, P, P, P, S, P]
+        L.dflash2_select_path.restype = I
+        L.dflash2_select_path.argtypes = [F(Config), F(Weights), I, P, P, P, P, P, P, S, P]
+        L.dflash2_verify_accept.restype = I
+        L.dflash2_verify_accept.argtypes = [I, I, P, P, P, P, P, P, P, P, P]
+        L.dflash2_read_device_status.restype = I
+        L.dflash2_read_device_status.argtypes = [P, S, P]
+        L.dflash2_test_gemm.restype = I
+        L.dflash2_test_gemm.argtypes = [I, P, I, I, P, I, I, P, S, P]
+        L.dflash2_test_topk_workspace.restype = S
+        L.dflash2_test_topk_workspace.argtypes = [I, I, I]
+        L.dflash2_test_gemm_topk.restype = I
+        L.dflash2_test_gemm_topk.argtypes = [I, P, I, I, P, I, I, ctypes.c_float, ctypes.c_float, P, P, P,
+                                             P, S, P]
+        _lib = L
+    return _lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn, rc):
+    if rc != 0:
+        raise DFlash2Error(fn, rc, lib().dflash2_status_string(rc).decode())
+    return rc
+
+
+def make_config(d):
+    """Config struct from a dict with the header's field names (extra keys ignored)."""
+    c = Config()
+    for name, _ in Config._fields_:
+        v = d[name]
+        if name == "dtype" and isinstance(v, str):
+            v = {"f32": F32, "bf16": BF16}[v]
+        setattr(c, name, v)
+    return c
+
+
+class WeightSet:
+    """Holds a Weights struct over torch device tensors (kept alive here)."""
+
+    def __init__(self, tensors):
+        self.tensors = tensors
+        n = len(tensors["layers"])
+        self._layers = (LayerWeights * n)()
+        for i, L in enumerate(tensors["layers"]):
+            for f in _LAYER_FIELDS:
+                setattr(self._layers[i], f, _ptr(L[f]))
+        self.struct = Weights(*[_ptr(tensors[f]) for f in _TOP_FIELDS],
+                              ctypes.cast(self._layers, ctypes.POINTER(LayerWeights)))
+
+
+def dflash2_status_string(status):
+    return lib().dflash2_status_string(status).decode()
+
+
+def dflash2_version():
+    return lib().dflash2_version()
+
+
+def dflash2_validate_config(cfg):
+    return lib().dflash2_validate_config(ctypes.byref(cfg))
+
+
+def dflash2_workspace_size(cfg, max_batch, max_new_rows, max_ctx):
+    return lib().dflash2_workspace_size(ctypes.byref(cfg), max_batch, max_new_rows, max_ctx)
+
+
+def dflash2_append_context(cfg, w, k_cache, v_cache, n_pages, block_table, max_pages, batch, ctx_len,
+                           n_new, new_taps, new_off, workspace, stream=None):
+    return _check("dflash2_append_context", lib().dflash2_append_context(
+        ctypes.byref(cfg), ctypes.byref(w.struct), _ptr(k_cache), _ptr(v_cache), n_pages,
+        _ptr(block_table), max_pages, batch, _ptr(ctx_len), n_new, _ptr(new_taps), _ptr(new_off),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def dflash2_draft_step(cfg, w, k_cache, v_cache, n_pages, block_table, max_pages, batch, ctx_len,
+                       n_new, new_taps, new_off, anchor, cand_id, cand_logit, debug_logits,
+                       workspace, stream=None):
+    return _check("dflash2_draft_step", lib().dflash2_draft_step(
+        ctypes.byref(cfg), ctypes.byref(w.struct), _ptr(k_cache), _ptr(v_cache), n_pages,
+        _ptr(block_table), max_pages, batch, _ptr(ctx_len), n_new, _ptr(new_taps), _ptr(new_off),
+        _ptr(anchor), _ptr(cand_id), _ptr(cand_logit), _ptr(debug_logits),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def dflash2_select_path(cfg, w, batch, anchor, cand_id, cand_logit, path, path_score, workspace,
+                        stream=None):
+    return _check("dflash2_select_path", lib().dflash2_select_path(
+        ctypes.byref(cfg), ctypes.byref(w.struct), batch, _ptr(anchor), _ptr(cand_id),
+        _ptr(cand_logit), _ptr(path), _ptr(path_score), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def dflash2_verify_accept(batch, block_size, path, target, accept_len, out_tok, n_out, next_anchor,
+                          seq_len=None, counters=None, stream=None):
+    return _check("dflash2_verify_accept", lib().dflash2_verify_accept(
+        batch, block_size, _ptr(path), _ptr(target), _ptr(accept_len), _ptr(out_tok), _ptr(n_out),
+        _ptr(next_anchor), _ptr(seq_len), _ptr(counters), _stream(stream)))
+
+
+def dflash2_read_device_status(workspace, stream=None):
+    rc = lib().dflash2_read_device_status(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                          _stream(stream))
+    if rc < 0:
+        _check("dflash2_read_device_status", rc)
+    return rc
+
+
+# --------------------------------------------------------------- test hooks
+# (include/dflash2_testing.h: the internal contraction and the lm_head top-k
+# path on their own, for parity tests)
+
+def dflash2_test_gemm(dtype, W, X, splits, partial, stream=None):
+    M, K = W.shape
+    N = X.shape[0]
+    rc = lib().dflash2_test_gemm(dtype, _ptr(W), M, K, _ptr(X), N, splits, _ptr(partial),
+                                 partial.numel() * partial.element_size(), _stream(stream))
+    if rc < 0:
+        _check("dflash2_test_gemm", rc)
+    return rc
+
+
+def dflash2_test_topk_workspace(dtype, M, N):
+    return lib().dflash2_test_topk_workspace(dtype, M, N)
+
+
+def dflash2_test_gemm_topk(dtype, W, X, k, mult, cap, cand_id, cand_logit, debug, workspace, stream=None):
+    M, K = W.shape
+    N = X.shape[0]
+    return _check("dflash2_test_gemm_topk", lib().dflash2_test_gemm_topk(
+        dtype, _ptr(W), M, K, _ptr(X), N, k, mult, cap, _ptr(cand_id), _ptr(cand_logit), _ptr(debug),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))

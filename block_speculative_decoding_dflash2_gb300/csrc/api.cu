@@ -1,0 +1,457 @@
+// C ABI of the DFlash2 draft step: argument checks, workspace plan and the
+// launch sequence of each entry point (declared in include/dflash2.h).
+//
+// Step order on the caller's stream ("Train a DFlash Drafter for
+// Speculative Decoding", "What is DFlash?" and "Variants"):
+//   (a) fc GEMM -> RMSNorm -> per layer [W_k;W_v] GEMM -> k-norm/RoPE -> paged K/V
+//   (b) embed [anchor, MASK...] -> per layer:
+//         norm -> tap GEMM -> dyn conv -> QKV GEMM -> q/k norm + RoPE
+//         -> attention(context + block) -> O GEMM -> +residual, norm
+//         -> tap GEMM -> dyn conv -> gate/up GEMM -> SiLU*up -> down GEMM
+//         -> +residual, next norm (final norm packs positions 1..B-1)
+//   (c) lm_head GEMM with streaming top-k -> merge
+//   (d) selector gather -> factor GEMM -> Viterbi;  verify/accept
+#include <algorithm>
+#include <atomic>
+#include <cstring>
+#include <map>
+#include <tuple>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace df2 {
+namespace {
+
+constexpr int kVersion = 10000;
+
+std::atomic<long long> g_launches{0};
+void* volatile g_stage_events[DFLASH2_N_STAGE_EVENTS] = {nullptr};
+std::atomic<int> g_stage_on{0};
+
+// Records stage event i on the call's stream (an external record, so it is
+// kept as an event node when the stream is being captured into a graph).
+void stage_event(int i, cudaStream_t st) {
+  if (!g_stage_on.load(std::memory_order_relaxed)) return;
+  cudaEvent_t ev = static_cast<cudaEvent_t>(g_stage_events[i]);
+  if (ev) cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+}
+
+int esize(int dtype) { return dtype == DFLASH2_BF16 ? 2 : 4; }
+
+size_t al(size_t x) { return (x + 255) & ~size_t(255); }
+
+int check_config(const dflash2_config* c) {
+  if (!c) return DFLASH2_ERR_INVALID_ARG;
+  if (c->dtype != DFLASH2_F32 && c->dtype != DFLASH2_BF16) return DFLASH2_ERR_DTYPE;
+  if (c->block_size < 2 || c->block_size > 32) return DFLASH2_ERR_BLOCK_SIZE;
+  if (c->hidden <= 0 || c->n_q_heads <= 0 || c->n_kv_heads <= 0 || c->intermediate <= 0 || c->vocab <= 0 ||
+      c->n_layers <= 0 || c->n_taps <= 0 || c->page_size <= 0)
+    return DFLASH2_ERR_SHAPE;
+  if (c->head_dim != 64 && c->head_dim != 128) return DFLASH2_ERR_SHAPE;
+  if (c->n_q_heads % c->n_kv_heads) return DFLASH2_ERR_SHAPE;
+  if (c->conv_kernel_size != 2) return DFLASH2_ERR_SHAPE;
+  if (c->conv_group_size <= 0 || c->hidden % c->conv_group_size) return DFLASH2_ERR_SHAPE;
+  if (c->top_k < 1 || c->top_k > KMAX || c->top_k > c->vocab) return DFLASH2_ERR_SHAPE;
+  if (c->selector_rank < 1 || c->selector_rank > 128) return DFLASH2_ERR_SHAPE;
+  if (c->mask_token_id < 0 || c->mask_token_id >= c->vocab) return DFLASH2_ERR_SHAPE;
+  if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return DFLASH2_ERR_SHAPE;
+  if (c->dtype == DFLASH2_BF16 && (c->hidden % 8 || c->intermediate % 8)) return DFLASH2_ERR_SHAPE;
+  const int R = (c->n_q_heads / c->n_kv_heads) * c->block_size;
+  if (R * c->head_dim > 128 * 128) return DFLASH2_ERR_SHAPE;  // attention rows held in shared memory
+  if (viterbi_smem_bytes(c->block_size - 1, c->top_k, c->selector_rank) > 200 * 1024) return DFLASH2_ERR_SHAPE;
+  // element counts used as 32-bit ints by the launchers
+  if ((long long)c->vocab * c->hidden > (1LL << 40)) return DFLASH2_ERR_SHAPE;
+  return DFLASH2_OK;
+}
+
+// Largest split-K partial buffer any contraction of a call can need, over
+// every SM count the library accepts.
+size_t partial_bound(int M, int N, int K) {
+  if (N <= 0) return 0;
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int>, size_t> memo;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    auto it = memo.find(std::make_tuple(M, N, K));
+    if (it != memo.end()) return it->second;
+  }
+  size_t best = 0;
+  const int probes[2] = {std::min(N, 256), N};
+  for (int n : probes)
+    for (int nsm = 1; nsm <= kMaxSM; ++nsm) {
+      const int s = gemm_splits(M, n, K, nsm, false);
+      best = std::max(best, (size_t)s * n * M * sizeof(float));
+    }
+  std::lock_guard<std::mutex> g(mu);
+  memo[std::make_tuple(M, N, K)] = best;
+  return best;
+}
+
+struct Layout {
+  size_t status, f, P, h, u, u2, q, kb, vb, attn, O, act, hn, logits, lv, li, selx, total;
+};
+
+Layout plan(const dflash2_config& c, int batch, int n_new, int max_ctx) {
+  const int H = c.hidden, B = c.block_size, D = B - 1, es = esize(c.dtype);
+  const int nq = c.n_q_heads, nkv = c.n_kv_heads, d = c.head_dim, I = c.intermediate;
+  const int G = H / c.conv_group_size, r = c.selector_rank, k = c.top_k;
+  const int rows = batch * B;
+  const int nsel = batch * (D * k + 1);
+  size_t P = 0;
+  if (n_new > 0) {
+    P = std::max(P, partial_bound(H, n_new, c.n_taps * H));
+    P = std::max(P, partial_bound(2 * nkv * d, n_new, H));
+  }
+  if (batch > 0) {
+    P = std::max(P, partial_bound(2 * G, rows, H));
+    P = std::max(P, partial_bound((nq + 2 * nkv) * d, rows, H));
+    P = std::max(P, partial_bound(H, rows, nq * d));
+    P = std::max(P, partial_bound(2 * I, rows, H));
+    P = std::max(P, partial_bound(H, rows, I));
+    P = std::max(P, partial_bound(2 * r, nsel, H));
+  }
+  const int n_lists = std::max(kMaxSM, topk_scan_lists(c.vocab));
+  Layout L;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += al(bytes);
+    return at;
+  };
+  L.status = take(256);
+  L.f = take((size_t)n_new * H * es);
+  L.P = take(P);
+  L.h = take((size_t)rows * H * 4);
+  L.u = take((size_t)rows * H * es);
+  L.u2 = take((size_t)rows * H * es);
+  L.q = take((size_t)rows * nq * d * es);
+  L.kb = take((size_t)rows * nkv * d * es);
+  L.vb = take((size_t)rows * nkv * d * es);
+  L.attn = take(batch > 0 ? attn_part_bytes(batch, B, nq, nkv, d, max_ctx) : 0);
+  L.O = take((size_t)rows * nq * d * es);
+  L.act = take((size_t)rows * I * es);
+  L.hn = take((size_t)batch * D * H * es);
+  L.logits = take(c.dtype == DFLASH2_F32 ? (size_t)batch * D * c.vocab * 4 : 0);
+  L.lv = take((size_t)n_lists * batch * D * KMAX * 4);
+  L.li = take((size_t)n_lists * batch * D * KMAX * 4);
+  L.selx = take((size_t)nsel * H * es);
+  L.total = o;
+  return L;
+}
+
+// Per-device facts: SM count and whether it is the sm_103 part this build targets.
+int device_ctx(Ctx* ctx, void* stream, void* ws) {
+  static int nsm_cache[64] = {0};
+  static int ok_cache[64] = {0};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DFLASH2_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    if (!nsm_cache[dev]) {
+      int n = 0, maj = 0, mi = 0;
+      if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&mi, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return DFLASH2_ERR_CUDA;
+      nsm_cache[dev] = std::min(n, kMaxSM);
+      ok_cache[dev] = (maj == 10 && mi == 3) ? 1 : 0;
+    }
+    if (!ok_cache[dev]) return DFLASH2_ERR_UNSUPPORTED;
+    ctx->nsm = nsm_cache[dev];
+  }
+  ctx->stream = static_cast<cudaStream_t>(stream);
+  ctx->status = static_cast<unsigned*>(ws);
+  return DFLASH2_OK;
+}
+
+#define TRY(x)                    \
+  do {                            \
+    const int rc_ = (x);          \
+    if (rc_ != DFLASH2_OK) return rc_; \
+  } while (0)
+
+template <typename P>
+P* at(void* ws, size_t off) {
+  return reinterpret_cast<P*>(static_cast<char*>(ws) + off);
+}
+
+int gemm(const dflash2_config& c, const Ctx& ctx, const void* W, int M, int K, const void* X, int N, float* P,
+         int* S) {
+  GemmOp g;
+  std::memset(&g, 0, sizeof(g));
+  g.W = W;
+  g.M = M;
+  g.K = K;
+  g.ldw = K;
+  g.X = X;
+  g.N = N;
+  g.ldx = K;
+  g.out = P;
+  g.mult = 1.f;
+  if (c.dtype == DFLASH2_BF16) {
+    g.splits = gemm_splits(M, N, K, ctx.nsm, false);
+    *S = g.splits;
+    return gemm_bf16(g, ctx);
+  }
+  g.splits = 1;
+  *S = 1;
+  return gemm_f32(g, ctx);
+}
+
+const char* elem_ptr(const void* base, size_t elems, int dtype) {
+  return static_cast<const char*>(base) + elems * esize(dtype);
+}
+
+int check_weights(const dflash2_config& c, const dflash2_weights* w) {
+  if (!w || !w->embed || !w->lm_head || !w->fc || !w->hidden_norm || !w->final_norm || !w->sel || !w->layers)
+    return DFLASH2_ERR_INVALID_ARG;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const dflash2_layer_weights& L = w->layers[l];
+    if (!L.attn_norm || !L.tapgen_attn || !L.qkv || !L.q_norm || !L.k_norm || !L.o || !L.mlp_norm ||
+        !L.tapgen_mlp || !L.gate_up || !L.down)
+      return DFLASH2_ERR_INVALID_ARG;
+  }
+  return DFLASH2_OK;
+}
+
+// stage (a): projection + paged K/V append of n_new rows
+int run_append(const dflash2_config& c, const dflash2_weights& w, void* kc, void* vc, int n_pages,
+               const int32_t* block_table, int max_pages, int batch, const int32_t* ctx_len, int n_new,
+               const void* taps, const int32_t* new_off, void* ws, const Layout& L, const Ctx& ctx) {
+  if (n_new == 0) return DFLASH2_OK;
+  const int H = c.hidden, nq = c.n_q_heads, nkv = c.n_kv_heads, d = c.head_dim;
+  float* P = at<float>(ws, L.P);
+  void* f = at<char>(ws, L.f);
+  int S = 1;
+  TRY(gemm(c, ctx, w.fc, H, c.n_taps * H, taps, n_new, P, &S));
+  TRY(launch_rows_feature_norm(c.dtype, P, S, n_new, H, w.hidden_norm, c.rms_eps, f, ctx));
+  const size_t layer_elems = (size_t)n_pages * c.page_size * nkv * d;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const dflash2_layer_weights& Lw = w.layers[l];
+    const void* wkv = elem_ptr(Lw.qkv, (size_t)nq * d * H, c.dtype);
+    TRY(gemm(c, ctx, wkv, 2 * nkv * d, H, f, n_new, P, &S));
+    TRY(launch_kv_append(c.dtype, P, S, n_new, nkv, d, Lw.k_norm, c.rms_eps, c.rope_theta, ctx_len, new_off, batch,
+                         block_table, max_pages, c.page_size, n_pages,
+                         const_cast<char*>(elem_ptr(kc, l * layer_elems, c.dtype)),
+                         const_cast<char*>(elem_ptr(vc, l * layer_elems, c.dtype)), ctx));
+  }
+  return DFLASH2_OK;
+}
+
+int check_cache_args(void* kc, void* vc, int n_pages, const int32_t* block_table, int max_pages, int batch,
+                     const int32_t* ctx_len, int n_new, const void* taps, const int32_t* new_off) {
+  if (batch <= 0 || n_new < 0 || n_pages <= 0 || max_pages <= 0) return DFLASH2_ERR_SHAPE;
+  if (!kc || !vc || !block_table || !ctx_len || !new_off) return DFLASH2_ERR_INVALID_ARG;
+  if (n_new > 0 && !taps) return DFLASH2_ERR_INVALID_ARG;
+  return DFLASH2_OK;
+}
+
+}  // namespace
+
+void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+}  // namespace df2
+
+using namespace df2;
+
+extern "C" {
+
+const char* dflash2_status_string(int s) {
+  switch (s) {
+    case DFLASH2_OK: return "ok";
+    case DFLASH2_ERR_INVALID_ARG: return "invalid argument (null pointer, negative size or bad enum)";
+    case DFLASH2_ERR_SHAPE: return "inconsistent or unsupported dimensions";
+    case DFLASH2_ERR_BLOCK_SIZE: return "block size out of range or not drafts + 1";
+    case DFLASH2_ERR_DTYPE: return "unsupported dtype";
+    case DFLASH2_ERR_WORKSPACE: return "workspace missing or too small";
+    case DFLASH2_ERR_CUDA: return "a CUDA call failed";
+    case DFLASH2_ERR_UNSUPPORTED: return "unsupported device or request (this build targets sm_103a)";
+    default: return "unknown status";
+  }
+}
+
+int dflash2_version(void) { return kVersion; }
+
+int64_t dflash2_launch_count(void) { return g_launches.load(); }
+
+void dflash2_set_stage_events(void* const* events) {
+  if (!events) {
+    g_stage_on.store(0);
+    return;
+  }
+  for (int i = 0; i < DFLASH2_N_STAGE_EVENTS; ++i) g_stage_events[i] = events[i];
+  g_stage_on.store(1);
+}
+
+int dflash2_validate_config(const dflash2_config* cfg) { return check_config(cfg); }
+
+size_t dflash2_workspace_size(const dflash2_config* cfg, int max_batch, int max_new_rows, int max_ctx) {
+  if (check_config(cfg) != DFLASH2_OK || max_batch < 0 || max_new_rows < 0 || max_ctx < 0) return 0;
+  return plan(*cfg, max_batch, max_new_rows, max_ctx).total;
+}
+
+int dflash2_append_context(const dflash2_config* cfg, const dflash2_weights* w, void* k_cache, void* v_cache,
+                           int n_pages, const int32_t* block_table, int max_pages, int batch,
+                           const int32_t* ctx_len, int n_new, const void* new_taps, const int32_t* new_off,
+                           void* workspace, size_t ws_bytes, void* stream) {
+  TRY(check_config(cfg));
+  TRY(check_weights(*cfg, w));
+  TRY(check_cache_args(k_cache, v_cache, n_pages, block_table, max_pages, batch, ctx_len, n_new, new_taps, new_off));
+  if (!workspace) return DFLASH2_ERR_WORKSPACE;
+  const Layout L = plan(*cfg, 0, n_new, 0);
+  if (ws_bytes < L.total) return DFLASH2_ERR_WORKSPACE;
+  Ctx ctx;
+  TRY(device_ctx(&ctx, stream, workspace));
+  return run_append(*cfg, *w, k_cache, v_cache, n_pages, block_table, max_pages, batch, ctx_len, n_new, new_taps,
+                    new_off, workspace, L, ctx);
+}
+
+int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void* k_cache, void* v_cache,
+                       int n_pages, const int32_t* block_table, int max_pages, int batch, const int32_t* ctx_len,
+                       int n_new, const void* new_taps, const int32_t* new_off, const int32_t* anchor,
+                       int32_t* cand_id, float* cand_logit, float* debug_logits, void* workspace, size_t ws_bytes,
+                       void* stream) {
+  TRY(check_config(cfg));
+  TRY(check_weights(*cfg, w));
+  TRY(check_cache_args(k_cache, v_cache, n_pages, block_table, max_pages, batch, ctx_len, n_new, new_taps, new_off));
+  if (!anchor || !cand_id || !cand_logit) return DFLASH2_ERR_INVALID_ARG;
+  if (!workspace) return DFLASH2_ERR_WORKSPACE;
+  const dflash2_config& c = *cfg;
+  const int max_ctx = max_pages * c.page_size;
+  const Layout L = plan(c, batch, n_new, max_ctx);
+  if (ws_bytes < L.total) return DFLASH2_ERR_WORKSPACE;
+  if ((long long)batch * (c.block_size - 1) > 32 * 256) return DFLASH2_ERR_SHAPE;
+  Ctx ctx;
+  TRY(device_ctx(&ctx, stream, workspace));
+
+  stage_event(0, ctx.stream);
+  TRY(run_append(c, *w, k_cache, v_cache, n_pages, block_table, max_pages, batch, ctx_len, n_new, new_taps, new_off,
+                 workspace, L, ctx));
+  stage_event(1, ctx.stream);
+
+  const int H = c.hidden, B = c.block_size, D = B - 1, nq = c.n_q_heads, nkv = c.n_kv_heads, d = c.head_dim;
+  const int I = c.intermediate, G = H / c.conv_group_size, rows = batch * B;
+  float* P = at<float>(workspace, L.P);
+  float* h = at<float>(workspace, L.h);
+  void* u = at<char>(workspace, L.u);
+  void* u2 = at<char>(workspace, L.u2);
+  void* q = at<char>(workspace, L.q);
+  void* kb = at<char>(workspace, L.kb);
+  void* vb = at<char>(workspace, L.vb);
+  void* O = at<char>(workspace, L.O);
+  void* act = at<char>(workspace, L.act);
+  void* hn = at<char>(workspace, L.hn);
+  const size_t layer_elems = (size_t)n_pages * c.page_size * nkv * d;
+  int S = 1;
+
+  TRY(launch_embed_block(c.dtype, anchor, c.mask_token_id, batch, B, w->embed, c.vocab, H, c.input_embedding_scale,
+                         h, ctx));
+  TRY(launch_residual_norm(c.dtype, h, nullptr, 1, rows, H, w->layers[0].attn_norm, c.rms_eps, u, B, 0, ctx));
+  for (int l = 0; l < c.n_layers; ++l) {
+    const dflash2_layer_weights& Lw = w->layers[l];
+    // attention sublayer
+    TRY(gemm(c, ctx, Lw.tapgen_attn, 2 * G, H, u, rows, P, &S));
+    TRY(launch_dyn_conv(c.dtype, u, P, S, rows, H, c.conv_group_size, B, u2, ctx));
+    TRY(gemm(c, ctx, Lw.qkv, (nq + 2 * nkv) * d, H, u2, rows, P, &S));
+    TRY(launch_qkv_epilogue(c.dtype, P, S, rows, B, nq, nkv, d, Lw.q_norm, Lw.k_norm, c.rms_eps, c.rope_theta,
+                            ctx_len, new_off, q, kb, vb, ctx));
+    TRY(launch_attention(c.dtype, q, kb, vb, elem_ptr(k_cache, l * layer_elems, c.dtype),
+                         elem_ptr(v_cache, l * layer_elems, c.dtype), block_table, max_pages, c.page_size, n_pages,
+                         ctx_len, new_off, batch, B, nq, nkv, d, max_ctx, at<float>(workspace, L.attn), O, ctx));
+    TRY(gemm(c, ctx, Lw.o, H, nq * d, O, rows, P, &S));
+    TRY(launch_residual_norm(c.dtype, h, P, S, rows, H, Lw.mlp_norm, c.rms_eps, u, B, 0, ctx));
+    // MLP sublayer
+    TRY(gemm(c, ctx, Lw.tapgen_mlp, 2 * G, H, u, rows, P, &S));
+    TRY(launch_dyn_conv(c.dtype, u, P, S, rows, H, c.conv_group_size, B, u2, ctx));
+    TRY(gemm(c, ctx, Lw.gate_up, 2 * I, H, u2, rows, P, &S));
+    TRY(launch_act(c.dtype, P, S, rows, I, act, ctx));
+    TRY(gemm(c, ctx, Lw.down, H, I, act, rows, P, &S));
+    if (l + 1 < c.n_layers)
+      TRY(launch_residual_norm(c.dtype, h, P, S, rows, H, w->layers[l + 1].attn_norm, c.rms_eps, u, B, 0, ctx));
+    else
+      TRY(launch_residual_norm(c.dtype, h, P, S, rows, H, w->final_norm, c.rms_eps, hn, B, 1, ctx));
+  }
+
+  stage_event(2, ctx.stream);
+  // (c) lm_head over block positions 1..B-1 with the streaming top-k
+  float* lv = at<float>(workspace, L.lv);
+  int* li = at<int>(workspace, L.li);
+  int n_lists = 0;
+  const int nrow = batch * D;
+  if (c.dtype == DFLASH2_BF16) {
+    GemmOp g;
+    std::memset(&g, 0, sizeof(g));
+    g.W = w->lm_head;
+    g.M = c.vocab;
+    g.K = H;
+    g.ldw = H;
+    g.X = hn;
+    g.N = nrow;
+    g.ldx = H;
+    g.splits = 1;
+    g.topk = true;
+    g.lists_v = lv;
+    g.lists_i = li;
+    g.debug = debug_logits;
+    g.mult = c.output_multiplier;
+    g.cap = c.final_logit_softcap;
+    TRY(gemm_bf16(g, ctx));
+    n_lists = gemm_topk_lists(c.vocab, nrow, H, ctx.nsm, c.dtype);
+  } else {
+    float* logits = at<float>(workspace, L.logits);
+    TRY(gemm(c, ctx, w->lm_head, c.vocab, H, hn, nrow, logits, &S));
+    TRY(launch_topk_scan(logits, nrow, c.vocab, c.output_multiplier, c.final_logit_softcap, debug_logits, lv, li,
+                         &n_lists, ctx));
+  }
+  stage_event(3, ctx.stream);
+  TRY(launch_topk_merge(lv, li, n_lists, nrow, c.top_k, cand_id, cand_logit, ctx));
+  stage_event(4, ctx.stream);
+  return DFLASH2_OK;
+}
+
+int dflash2_select_path(const dflash2_config* cfg, const dflash2_weights* w, int batch, const int32_t* anchor,
+                        const int32_t* cand_id, const float* cand_logit, int32_t* path, float* path_score,
+                        void* workspace, size_t ws_bytes, void* stream) {
+  TRY(check_config(cfg));
+  if (!w || !w->embed || !w->sel) return DFLASH2_ERR_INVALID_ARG;
+  if (batch <= 0) return DFLASH2_ERR_SHAPE;
+  if (!anchor || !cand_id || !cand_logit || !path) return DFLASH2_ERR_INVALID_ARG;
+  if (!workspace) return DFLASH2_ERR_WORKSPACE;
+  const dflash2_config& c = *cfg;
+  const Layout L = plan(c, batch, 0, 0);
+  if (ws_bytes < L.total) return DFLASH2_ERR_WORKSPACE;
+  Ctx ctx;
+  TRY(device_ctx(&ctx, stream, workspace));
+  const int D = c.block_size - 1, k = c.top_k, r = c.selector_rank, H = c.hidden;
+  void* x = at<char>(workspace, L.selx);
+  float* P = at<float>(workspace, L.P);
+  int S = 1;
+  TRY(launch_sel_gather(c.dtype, anchor, cand_id, batch, D, k, w->embed, c.vocab, H, x, ctx));
+  TRY(gemm(c, ctx, w->sel, 2 * r, H, x, batch * (D * k + 1), P, &S));
+  return launch_viterbi(P, S, anchor, cand_id, cand_logit, batch, D, k, r, path, path_score, ctx);
+}
+
+int dflash2_verify_accept(int batch, int block_size, const int32_t* path, const int32_t* target,
+                          int32_t* accept_len, int32_t* out_tok, int32_t* n_out, int32_t* next_anchor,
+                          int32_t* seq_len, int64_t* counters, void* stream) {
+  if (block_size < 2 || block_size > 32) return DFLASH2_ERR_BLOCK_SIZE;
+  if (batch <= 0) return DFLASH2_ERR_SHAPE;
+  if (!path || !target || !accept_len || !out_tok || !n_out || !next_anchor) return DFLASH2_ERR_INVALID_ARG;
+  return launch_verify(batch, block_size, path, target, accept_len, out_tok, n_out, next_anchor, seq_len, counters,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int dflash2_read_device_status(void* workspace, size_t ws_bytes, void* stream) {
+  if (!workspace || ws_bytes < 256) return DFLASH2_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess) return DFLASH2_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, sizeof(v), st) != cudaSuccess) return DFLASH2_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return DFLASH2_ERR_CUDA;
+  return (int)(v & 0x7fffffffu);
+}
+
+}  // extern "C"

@@ -1,0 +1,509 @@
+// Weight-streaming GEMM on the 5th-generation tensor cores (tcgen05) fed by
+// TMA, for the dense contractions of the draft step: feature projection,
+// context K/V, conv tap generators, QKV, O, gate/up, down, the selector
+// factors and the lm_head ("Train a DFlash Drafter for Speculative
+// Decoding", "What is DFlash?": a draft stack plus the target's shared
+// lm_head).
+//
+// Shape of the problem: M (weight rows) is large, N (activation rows = the
+// block positions of the batch) is small, K is the hidden width.  The MMA
+// therefore runs swap-AB: a 128-row weight tile is operand A (MMA M = 128),
+// the activation tile is operand B (MMA N = BN in 16..256), the fp32
+// accumulator lives in TMEM.  At batch 1 the kernel is HBM-bound: every
+// weight byte is read once per step, so the design goal is to keep enough
+// TMA bytes in flight per SM (a 4..12-stage ring) on a persistent grid of
+// one CTA per SM.
+//
+// Warp roles (192 threads):
+//   warp 0      TMA producer (one lane): weight + activation tiles -> ring
+//   warp 1      MMA issuer (one lane) and TMEM owner
+//   warps 2..5  epilogue: TMEM -> registers -> either fp32 split-K partials
+//               (out[s][n][m], coalesced over m) or the streaming top-k.
+// The accumulator is double-buffered in TMEM so the epilogue of one tile
+// overlaps the MMAs of the next.
+//
+// Every wait is bounded (1 s); on timeout the kernel records
+// DFLASH2_DEV_WAIT_TIMEOUT, lets the other roles bail out, waits (bounded)
+// for its own TMA copies and MMAs in flight, frees TMEM and returns.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <climits>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace df2 {
+
+namespace {
+
+constexpr int BM = 128;     // MMA M: weight rows per tile
+constexpr int BK = 64;      // K elements per ring stage (128 bytes of bf16)
+constexpr int SMEM_BUDGET = 227 * 1024;
+constexpr uint64_t WAIT_NS = 1000000000ull;
+constexpr int THREADS = 192;
+
+struct TcArgs {
+  int M, N, K;
+  int n_chunks, splits, m_tiles, n_tiles, units;
+  float* out;
+  float* lists_v;
+  int* lists_i;
+  float* debug;
+  float mult, cap;
+  unsigned* status;
+};
+
+template <int BN>
+struct TcCfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int TOPK_EXTRA = 16 * BM * 4 + BN * KMAX * 8;
+  static constexpr int FIXED = 1024 /* alignment slack */ + 1024 /* barriers */;
+  __host__ __device__ static constexpr int stages(bool topk) {
+    return ((SMEM_BUDGET - FIXED - (topk ? TOPK_EXTRA : 0)) / STAGE) > 12
+               ? 12
+               : ((SMEM_BUDGET - FIXED - (topk ? TOPK_EXTRA : 0)) / STAGE);
+  }
+  __host__ __device__ static constexpr int smem_bytes(bool topk) { return FIXED + stages(topk) * STAGE + (topk ? TOPK_EXTRA : 0); }
+  static constexpr uint32_t TMEM_COLS = (2 * BN <= 32)    ? 32
+                                        : (2 * BN <= 64)  ? 64
+                                        : (2 * BN <= 128) ? 128
+                                        : (2 * BN <= 256) ? 256
+                                                          : 512;
+};
+
+__device__ __forceinline__ void named_sync_epi() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Named barrier over the 4 epilogue warps that also ORs a predicate, so the
+// warps take the same branch after it (no warp left waiting on a barrier
+// the others skipped).
+__device__ __forceinline__ bool named_sync_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 1, 128, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred)
+      : "memory");
+  return r != 0;
+}
+
+template <int BN, bool TOPK>
+__global__ void __launch_bounds__(THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcArgs a) {
+  using C = TcCfg<BN>;
+  constexpr int STAGES = C::stages(TOPK);
+  constexpr int A_BYTES = C::A_BYTES, B_BYTES = C::B_BYTES;
+  static_assert(STAGES >= 2, "ring too small");
+  static_assert(B_BYTES % 1024 == 0, "B tile must keep 1024-byte swizzle atoms aligned");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stA = smem;
+  uint8_t* stB = smem + STAGES * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stB + STAGES * B_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* stg = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 1024);  // [16][BM]
+  float* lv_s = stg + 16 * BM;                                                       // [BN][KMAX]
+  int* li_s = reinterpret_cast<int*>(lv_s + BN * KMAX);                              // [BN][KMAX]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(tfull + i, 1);
+      mbar_init(tempty + i, 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto fail = [&]() {
+    *abort_flag = 1;
+    flag(a.status, DFLASH2_DEV_WAIT_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      long issued = 0;
+      for (int u = blockIdx.x; u < a.units && !*abort_flag; u += gridDim.x) {
+        const int sp = u % a.splits, t = u / a.splits;
+        const int mt = t % a.m_tiles, nt = t / a.m_tiles;
+        const int k0 = (int)((long)sp * a.n_chunks / a.splits);
+        const int k1 = (int)((long)(sp + 1) * a.n_chunks / a.splits);
+        bool ok = true;
+        for (int kc = k0; kc < k1; ++kc) {
+          if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, WAIT_NS)) {
+            fail();
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full + stage, A_BYTES + B_BYTES);
+          tma_load_2d(stA + stage * A_BYTES, &tmA, full + stage, kc * BK, mt * BM, pol_w);
+          tma_load_2d(stB + stage * B_BYTES, &tmB, full + stage, kc * BK, nt * BN, pol_x);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+      if (*abort_flag) {
+        // wait (bounded) for every copy this thread issued to land
+        for (int s = 0; s < STAGES; ++s) {
+          const long cnt = issued / STAGES + (s < issued % STAGES ? 1 : 0);
+          if (cnt > 0) {
+            volatile int never = 0;
+            mbar_wait(full + s, (uint32_t)((cnt - 1) & 1), &never, WAIT_NS);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(BM, BN);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+        const int sp = u % a.splits;
+        const int k0 = (int)((long)sp * a.n_chunks / a.splits);
+        const int k1 = (int)((long)(sp + 1) * a.n_chunks / a.splits);
+        if (!mbar_wait(tempty + acc, acc_phase ^ 1u, abort_flag, WAIT_NS)) {
+          fail();
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(acc * BN);
+        for (int kc = k0; kc < k1; ++kc) {
+          if (!mbar_wait(full + stage, phase, abort_flag, WAIT_NS)) {
+            fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sdesc_sw128(smem_u32(stA + stage * A_BYTES));
+          const uint64_t bd = sdesc_sw128(smem_u32(stB + stage * B_BYTES));
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_bf16(d, ad + 2u * kk, bd + 2u * kk, idesc, (kc > k0 || kk > 0) ? 1u : 0u);
+          umma_commit(empty + stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(tfull + acc);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // every MMA issued by this thread completes before TMEM can be freed
+      umma_commit(drain);
+      volatile int never = 0;
+      mbar_wait(drain, 0, &never, WAIT_NS);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    const int ew = warp - 2;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int cur_nt = -1;
+    uint32_t touched = 0;
+
+    auto reset_lists = [&]() {
+      for (int i = threadIdx.x - 64; i < BN * KMAX; i += 128) {
+        lv_s[i] = -INFINITY;
+        li_s[i] = INT_MAX;
+      }
+    };
+    auto flush_lists = [&](int nt, bool sentinel) {
+      for (int i = threadIdx.x - 64; i < BN * KMAX; i += 128) {
+        const int c = i / KMAX, e = i % KMAX;
+        const int n = nt * BN + c;
+        if (n < a.N) {
+          const size_t o = ((size_t)blockIdx.x * a.N + n) * KMAX + e;
+          a.lists_v[o] = sentinel ? -INFINITY : lv_s[i];
+          a.lists_i[o] = sentinel ? INT_MAX : li_s[i];
+        }
+      }
+    };
+
+    for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
+      const int sp = u % a.splits, t = u / a.splits;
+      const int mt = t % a.m_tiles, nt = t / a.m_tiles;
+      const bool got = mbar_wait(tfull + acc, acc_phase, abort_flag, WAIT_NS);
+      if (!got) fail();
+      if constexpr (TOPK) {
+        if (named_sync_or(!got || *abort_flag)) break;
+      } else {
+        if (!got) break;
+      }
+      tc_fence_after();
+      const int m = mt * BM + row;
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      if constexpr (!TOPK) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          float v[16];
+          tmem_ld16(tbase + c0, v);
+          if (m < a.M) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int n = nt * BN + c0 + j;
+              if (n < a.N) a.out[((size_t)sp * a.N + n) * a.M + m] = v[j];
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(tempty + acc);
+      } else {
+        if (nt != cur_nt) {
+          named_sync_epi();
+          if (cur_nt >= 0) flush_lists(cur_nt, false);
+          named_sync_epi();
+          reset_lists();
+          cur_nt = nt;
+          touched |= 1u << nt;
+          named_sync_epi();
+        }
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          float v[16];
+          tmem_ld16(tbase + c0, v);
+          if (c0 + 16 >= BN) {
+            tc_fence_before();
+            mbar_arrive(tempty + acc);
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            float z = a.mult * v[j];
+            if (a.cap > 0.f) z = a.cap * tanhf(z / a.cap);
+            v[j] = z;
+          }
+          if (a.debug != nullptr && m < a.M) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int n = nt * BN + c0 + j;
+              if (n < a.N) a.debug[(size_t)n * a.M + m] = v[j];
+            }
+          }
+          named_sync_epi();  // previous chunk's scans are done with the staging tile
+#pragma unroll
+          for (int j = 0; j < 16; ++j) stg[j * BM + row] = v[j];
+          named_sync_epi();
+          for (int jj = ew; jj < 16; jj += 4) {
+            const int c = c0 + jj;
+            if (nt * BN + c >= a.N) continue;
+            float* Lv = lv_s + c * KMAX;
+            int* Li = li_s + c * KMAX;
+            float lv = lane < KMAX ? Lv[lane] : -INFINITY;
+            int li = lane < KMAX ? Li[lane] : INT_MAX;
+            float tv = __shfl_sync(0xffffffffu, lv, KMAX - 1);
+            int ti = __shfl_sync(0xffffffffu, li, KMAX - 1);
+#pragma unroll 1
+            for (int r = 0; r < 4; ++r) {
+              const int rr = r * 32 + lane;
+              const int mm = mt * BM + rr;
+              const float x = stg[jj * BM + rr];
+              const bool pass = (mm < a.M) && beats(x, mm, tv, ti);
+              unsigned mask = __ballot_sync(0xffffffffu, pass);
+              while (mask) {
+                const int src = __ffs(mask) - 1;
+                mask &= mask - 1;
+                const float cv = __shfl_sync(0xffffffffu, x, src);
+                warp_list_offer(lv, li, tv, ti, cv, mt * BM + r * 32 + src);
+              }
+            }
+            if (lane < KMAX) {
+              Lv[lane] = lv;
+              Li[lane] = li;
+            }
+            __syncwarp();
+          }
+        }
+      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if constexpr (TOPK) {
+      if (!named_sync_or(*abort_flag != 0)) {
+        if (cur_nt >= 0) flush_lists(cur_nt, false);
+        for (int nt = 0; nt < a.n_tiles; ++nt)
+          if (!(touched & (1u << nt))) flush_lists(nt, true);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map over rows x cols (row stride ld elements), box of
+// 64 columns x box_rows rows, 128-byte swizzle, zero fill out of bounds.
+int make_map(CUtensorMap* map, const void* base, int rows, int cols, int ld, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return DFLASH2_ERR_CUDA;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || ((size_t)ld * 2) % 16) return DFLASH2_ERR_SHAPE;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+}
+
+int pick_bn(int N) {
+  if (N <= 16) return 16;
+  if (N <= 32) return 32;
+  if (N <= 64) return 64;
+  if (N <= 128) return 128;
+  return 256;
+}
+
+template <int BN, bool TOPK>
+int launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs& args, int grid, cudaStream_t st) {
+  constexpr int smem = TcCfg<BN>::smem_bytes(TOPK);
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(tc_gemm_kernel<BN, TOPK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return DFLASH2_ERR_CUDA;
+    attr_set = true;
+  }
+  tc_gemm_kernel<BN, TOPK><<<grid, THREADS, smem, st>>>(ma, mb, args);
+  count_launch();
+  return cudaPeekAtLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+}
+
+}  // namespace
+
+int gemm_splits(int M, int N, int K, int nsm, bool topk) {
+  if (topk || N > 256) return 1;  // many activation rows: enough tiles without splitting K
+  const int bn = pick_bn(N);
+  const long base = (long)((M + BM - 1) / BM) * ((N + bn - 1) / bn);
+  const int chunks = (K + BK - 1) / BK;
+  if (base >= nsm) return 1;
+  const int smax = std::min(64, chunks);
+  long best = LONG_MAX;
+  int bs = 1;
+  for (int s = 1; s <= smax; ++s) {
+    const long waves = (base * s + nsm - 1) / nsm;
+    const long cost = waves * ((chunks + s - 1) / s);
+    if (cost < best) {
+      best = cost;
+      bs = s;
+    }
+  }
+  return bs;
+}
+
+int gemm_topk_lists(int M, int N, int K, int nsm, int dtype) {
+  (void)K;
+  if (dtype == DFLASH2_BF16) {
+    const int bn = pick_bn(N);
+    const long units = (long)((M + BM - 1) / BM) * ((N + bn - 1) / bn);
+    return (int)std::min<long>(units, nsm);
+  }
+  return topk_scan_lists(M);
+}
+
+int gemm_max_lists() { return std::max(kMaxSM, 0); }
+
+int gemm_bf16(const GemmOp& g, const Ctx& c) {
+  if (g.M <= 0 || g.N <= 0 || g.K <= 0) return DFLASH2_ERR_SHAPE;
+  const int bn = pick_bn(g.N);
+  TcArgs a;
+  a.M = g.M;
+  a.N = g.N;
+  a.K = g.K;
+  a.n_chunks = (g.K + BK - 1) / BK;
+  a.m_tiles = (g.M + BM - 1) / BM;
+  a.n_tiles = (g.N + bn - 1) / bn;
+  a.splits = g.topk ? 1 : std::max(1, std::min(g.splits, a.n_chunks));
+  a.units = a.m_tiles * a.n_tiles * a.splits;
+  a.out = g.out;
+  a.lists_v = g.lists_v;
+  a.lists_i = g.lists_i;
+  a.debug = g.debug;
+  a.mult = g.mult;
+  a.cap = g.cap;
+  a.status = c.status;
+  if (g.topk && a.n_tiles > 32) return DFLASH2_ERR_SHAPE;
+  const int grid = std::min(a.units, c.nsm);
+
+  CUtensorMap ma, mb;
+  int rc = make_map(&ma, g.W, g.M, g.K, g.ldw, BM);
+  if (rc) return rc;
+  rc = make_map(&mb, g.X, g.N, g.K, g.ldx, bn);
+  if (rc) return rc;
+
+  switch (bn) {
+    case 16: return g.topk ? launch_bn<16, true>(ma, mb, a, grid, c.stream) : launch_bn<16, false>(ma, mb, a, grid, c.stream);
+    case 32: return g.topk ? launch_bn<32, true>(ma, mb, a, grid, c.stream) : launch_bn<32, false>(ma, mb, a, grid, c.stream);
+    case 64: return g.topk ? launch_bn<64, true>(ma, mb, a, grid, c.stream) : launch_bn<64, false>(ma, mb, a, grid, c.stream);
+    case 128: return g.topk ? launch_bn<128, true>(ma, mb, a, grid, c.stream) : launch_bn<128, false>(ma, mb, a, grid, c.stream);
+    default: return g.topk ? launch_bn<256, true>(ma, mb, a, grid, c.stream) : launch_bn<256, false>(ma, mb, a, grid, c.stream);
+  }
+}
+
+}  // namespace df2

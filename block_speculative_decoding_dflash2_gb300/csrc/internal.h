@@ -1,0 +1,92 @@
+// Host-side interfaces between the C ABI layer and the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/dflash2.h"
+
+namespace df2 {
+
+struct Ctx {
+  cudaStream_t stream;
+  unsigned* status;  // device status word (workspace offset 0)
+  int nsm;           // SMs of the current device
+};
+
+// One dense contraction out[n][m] = sum_k W[m][k] * X[n][k]  (swap-AB: the
+// weight rows stream along the MMA M axis, the few activation rows form N).
+struct GemmOp {
+  const void* W;  // [M, K] row stride ldw elements
+  int M, K, ldw;
+  const void* X;  // [N, K] row stride ldx elements
+  int N, ldx;
+  // partial epilogue: out[s][n][m] fp32, s < splits
+  float* out;
+  int splits;
+  // top-k epilogue (lm_head): per-CTA sorted lists of KMAX entries
+  bool topk;
+  float* lists_v;  // [n_lists][N][KMAX]
+  int* lists_i;
+  float* debug;  // nullable [N][M] logits after the transform
+  float mult, cap;
+};
+
+// K-split count the launchers use for an M x N x K contraction on `nsm` SMs.
+int gemm_splits(int M, int N, int K, int nsm, bool topk);
+// Number of partial top-k lists a top-k GEMM of this shape writes.
+int gemm_topk_lists(int M, int N, int K, int nsm, int dtype);
+// Upper bound of the above over every SM count this library accepts.
+int gemm_max_lists();
+constexpr int kMaxSM = 256;
+
+// Host-side count of kernel launches (instrumentation).
+void count_launch(int n = 1);
+
+int gemm_bf16(const GemmOp& g, const Ctx& c);  // tcgen05 + TMA (sm_103a)
+int gemm_f32(const GemmOp& g, const Ctx& c);   // exact fp32 FMA, SIMT
+
+// element-wise / row kernels (elementwise.cu); T = float or bf16 by dtype
+int launch_rows_feature_norm(int dtype, const float* P, int S, int rows, int H, const void* gamma, float eps,
+                             void* f_out, const Ctx& c);
+int launch_kv_append(int dtype, const float* P, int S, int rows, int nkv, int d, const void* k_norm, float eps,
+                     float theta, const int32_t* ctx_len, const int32_t* new_off, int batch,
+                     const int32_t* block_table, int max_pages, int page_size, int n_pages, void* kc, void* vc,
+                     const Ctx& c);
+int launch_embed_block(int dtype, const int32_t* anchor, int mask_id, int batch, int B, const void* embed, int V,
+                       int H, float scale, float* h_out, const Ctx& c);
+int launch_residual_norm(int dtype, float* h, const float* P, int S, int rows, int H, const void* gamma, float eps,
+                         void* u_out, int B, int skip_anchor, const Ctx& c);
+int launch_dyn_conv(int dtype, const void* u, const float* P, int S, int rows, int H, int group_size, int B,
+                    void* u2_out, const Ctx& c);
+int launch_qkv_epilogue(int dtype, const float* P, int S, int rows, int B, int nq, int nkv, int d,
+                        const void* q_norm, const void* k_norm, float eps, float theta, const int32_t* ctx_len,
+                        const int32_t* new_off, void* q, void* kb, void* vb, const Ctx& c);
+int launch_act(int dtype, const float* P, int S, int rows, int I, void* act, const Ctx& c);
+
+// attention (attention.cu)
+int launch_attention(int dtype, const void* q, const void* kb, const void* vb, const void* kc, const void* vc,
+                     const int32_t* block_table, int max_pages, int page_size, int n_pages,
+                     const int32_t* ctx_len, const int32_t* new_off, int batch, int B, int nq, int nkv, int d,
+                     int max_ctx, float* part, void* o_out, const Ctx& c);
+size_t attn_part_bytes(int batch, int B, int nq, int nkv, int d, int max_ctx);
+
+// top-k (topk.cu)
+int launch_topk_scan(const float* logits, int rows, int V, float mult, float cap, float* debug, float* lists_v,
+                     int* lists_i, int* n_lists, const Ctx& c);
+int topk_scan_lists(int V);
+int launch_topk_merge(const float* lists_v, const int* lists_i, int n_lists, int rows, int k, int32_t* cand_id,
+                      float* cand_logit, const Ctx& c);
+
+// selector and verify (selector.cu, verify.cu)
+int launch_sel_gather(int dtype, const int32_t* anchor, const int32_t* cand_id, int batch, int D, int k,
+                      const void* embed, int V, int H, void* x_out, const Ctx& c);
+int launch_viterbi(const float* P, int S, const int32_t* anchor, const int32_t* cand_id, const float* cand_logit,
+                   int batch, int D, int k, int r, int32_t* path, float* path_score, const Ctx& c);
+size_t viterbi_smem_bytes(int D, int k, int r);
+int launch_verify(int batch, int B, const int32_t* path, const int32_t* target, int32_t* accept_len,
+                  int32_t* out_tok, int32_t* n_out, int32_t* next_anchor, int32_t* seq_len, int64_t* counters,
+                  cudaStream_t st);
+
+}  // namespace df2

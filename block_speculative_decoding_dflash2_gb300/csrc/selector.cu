@@ -1,0 +1,160 @@
+// DFlash 2 pairwise path selector ("Train a DFlash Drafter for Speculative
+// Decoding", "Variants": a pairwise path selector that walks one coherent
+// path through each position's top-k candidates; "Objective": its term is a
+// cross-entropy over the position's top-k candidates given the true
+// predecessor; "Key Config Fields": selector_rank is its width).
+//
+// Reading implemented here: factors A = W_a E[tok] and Bf = W_b E[tok] of the
+// shared embedding; transition score of candidate j at draft position i
+// after predecessor p
+//     S_i(p, j) = z_i[j] + <A[prev], Bf[c_ij]>,
+//     T_i(p, j) = S_i(p, j) - logsumexp_j' S_i(p, j'),
+// and the path maximising sum_i T_i (Viterbi, ties to the smaller
+// predecessor index, then to the smaller final index).
+//
+// sel_gather_kernel lays out E rows of [anchor, all candidates] so the factor
+// contraction runs on the same GEMM as the rest of the step; viterbi_kernel
+// (one CTA per sequence) reduces the factor partials into shared memory and
+// runs the k x k dynamic programme over the B-1 positions.
+#include <climits>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace df2 {
+
+namespace {
+
+template <typename T>
+__global__ void __launch_bounds__(256) sel_gather_kernel(const int32_t* __restrict__ anchor,
+                                                         const int32_t* __restrict__ cand_id, int D, int k,
+                                                         const T* __restrict__ E, int V, int H, T* __restrict__ x,
+                                                         unsigned* status) {
+  const int r = blockIdx.x;
+  const int nt = D * k + 1;
+  const int s = r / nt, t = r % nt;
+  int tok = t == 0 ? anchor[s] : cand_id[(size_t)s * D * k + (t - 1)];
+  if (tok < 0 || tok >= V) {
+    if (threadIdx.x == 0) flag(status, DFLASH2_DEV_BAD_TOKEN);
+    tok = -1;
+  }
+  for (int m = threadIdx.x; m < H; m += blockDim.x) x[(size_t)r * H + m] = tok < 0 ? T(0.f) : E[(size_t)tok * H + m];
+}
+
+__global__ void __launch_bounds__(256) viterbi_kernel(const float* __restrict__ P, int S, int batch,
+                                                      const int32_t* __restrict__ cand_id,
+                                                      const float* __restrict__ cand_logit, int D, int k, int r,
+                                                      int32_t* __restrict__ path, float* __restrict__ path_score) {
+  extern __shared__ float sm[];
+  const int s = blockIdx.x;
+  const int nt = D * k + 1, w = 2 * r;
+  float* F = sm;                     // [nt][2r] factors: A = F[t][0:r], Bf = F[t][r:2r]
+  float* Sm = F + (size_t)nt * w;    // [k][k] scores / totals
+  float* delta = Sm + k * k;         // [k]
+  float* nd = delta + k;             // [k]
+  int* bp = reinterpret_cast<int*>(nd + k);  // [D][k]
+
+  const size_t stride = (size_t)batch * nt * w;
+  for (int idx = threadIdx.x; idx < nt * w; idx += blockDim.x) {
+    float a = 0.f;
+    for (int sp = 0; sp < S; ++sp) a += P[sp * stride + (size_t)s * nt * w + idx];
+    F[idx] = a;
+  }
+  __syncthreads();
+  const float* z = cand_logit + (size_t)s * D * k;
+  auto dot = [&](int ta, int tb) {  // <A[ta], Bf[tb]>
+    const float* a = F + (size_t)ta * w;
+    const float* b = F + (size_t)tb * w + r;
+    float acc = 0.f;
+    for (int c = 0; c < r; ++c) acc = fmaf(a[c], b[c], acc);
+    return acc;
+  };
+  // position 1: the predecessor is the anchor (factor row 0)
+  for (int j = threadIdx.x; j < k; j += blockDim.x) Sm[j] = z[j] + dot(0, 1 + j);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = -INFINITY;
+    for (int j = 0; j < k; ++j) m = fmaxf(m, Sm[j]);
+    float sum = 0.f;
+    for (int j = 0; j < k; ++j) sum += expf(Sm[j] - m);
+    const float lse = m + logf(sum);
+    for (int j = 0; j < k; ++j) delta[j] = Sm[j] - lse;
+  }
+  __syncthreads();
+  for (int i = 1; i < D; ++i) {
+    for (int pr = threadIdx.x; pr < k * k; pr += blockDim.x) {
+      const int p = pr / k, j = pr % k;
+      Sm[pr] = z[i * k + j] + dot(1 + (i - 1) * k + p, 1 + i * k + j);
+    }
+    __syncthreads();
+    for (int p = threadIdx.x; p < k; p += blockDim.x) {
+      float m = -INFINITY;
+      for (int j = 0; j < k; ++j) m = fmaxf(m, Sm[p * k + j]);
+      float sum = 0.f;
+      for (int j = 0; j < k; ++j) sum += expf(Sm[p * k + j] - m);
+      const float lse = m + logf(sum);
+      for (int j = 0; j < k; ++j) Sm[p * k + j] = delta[p] + (Sm[p * k + j] - lse);
+    }
+    __syncthreads();
+    for (int j = threadIdx.x; j < k; j += blockDim.x) {
+      float best = Sm[j];
+      int arg = 0;
+      for (int p = 1; p < k; ++p)
+        if (Sm[p * k + j] > best) {
+          best = Sm[p * k + j];
+          arg = p;
+        }
+      nd[j] = best;
+      bp[i * k + j] = arg;
+    }
+    __syncthreads();
+    for (int j = threadIdx.x; j < k; j += blockDim.x) delta[j] = nd[j];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    int j = 0;
+    for (int jj = 1; jj < k; ++jj)
+      if (delta[jj] > delta[j]) j = jj;
+    if (path_score) path_score[s] = delta[j];
+    for (int i = D - 1; i >= 0; --i) {
+      path[(size_t)s * D + i] = cand_id[((size_t)s * D + i) * k + j];
+      if (i > 0) j = bp[i * k + j];
+    }
+  }
+}
+
+}  // namespace
+
+size_t viterbi_smem_bytes(int D, int k, int r) {
+  return sizeof(float) * ((size_t)(D * k + 1) * 2 * r + (size_t)k * k + 2 * (size_t)k) + sizeof(int) * (size_t)D * k;
+}
+
+int launch_sel_gather(int dtype, const int32_t* anchor, const int32_t* cand_id, int batch, int D, int k,
+                      const void* embed, int V, int H, void* x_out, const Ctx& c) {
+  const int rows = batch * (D * k + 1);
+  if (dtype == DFLASH2_BF16)
+    sel_gather_kernel<bf16><<<rows, 256, 0, c.stream>>>(anchor, cand_id, D, k, static_cast<const bf16*>(embed), V, H,
+                                                         static_cast<bf16*>(x_out), c.status);
+  else
+    sel_gather_kernel<float><<<rows, 256, 0, c.stream>>>(anchor, cand_id, D, k, static_cast<const float*>(embed), V,
+                                                          H, static_cast<float*>(x_out), c.status);
+  count_launch();
+  return cudaPeekAtLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+}
+
+int launch_viterbi(const float* P, int S, const int32_t* anchor, const int32_t* cand_id, const float* cand_logit,
+                   int batch, int D, int k, int r, int32_t* path, float* path_score, const Ctx& c) {
+  (void)anchor;  // the anchor's factors are row 0 of P
+  const size_t smem = viterbi_smem_bytes(D, k, r);
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(viterbi_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) != cudaSuccess)
+      return DFLASH2_ERR_CUDA;
+    attr = true;
+  }
+  viterbi_kernel<<<batch, 256, smem, c.stream>>>(P, S, batch, cand_id, cand_logit, D, k, r, path, path_score);
+  count_launch();
+  return cudaPeekAtLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+}
+
+}  // namespace df2

@@ -1,0 +1,120 @@
+// Test hooks declared in include/dflash2_testing.h: the internal contraction
+// and the lm_head top-k path, callable on their own for parity tests.
+#include <algorithm>
+#include <cstring>
+
+#include "../../include/dflash2_testing.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace df2 {
+namespace {
+
+int test_ctx(Ctx* c, void* stream, unsigned* status) {
+  int dev = 0, n = 0, maj = 0, mi = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DFLASH2_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&mi, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return DFLASH2_ERR_CUDA;
+  if (maj != 10 || mi != 3) return DFLASH2_ERR_UNSUPPORTED;
+  c->nsm = std::min(n, kMaxSM);
+  c->stream = static_cast<cudaStream_t>(stream);
+  c->status = status;
+  return DFLASH2_OK;
+}
+
+size_t al(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+}  // namespace df2
+
+using namespace df2;
+
+extern "C" {
+
+int dflash2_test_gemm(int dtype, const void* W, int M, int K, const void* X, int N, int splits, float* partial,
+                      size_t out_bytes, void* stream) {
+  if (dtype != DFLASH2_BF16 && dtype != DFLASH2_F32) return DFLASH2_ERR_DTYPE;
+  if (!W || !X || !partial) return DFLASH2_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0) return DFLASH2_ERR_SHAPE;
+  Ctx c;
+  const int rc = test_ctx(&c, stream, nullptr);
+  if (rc) return rc;
+  GemmOp g;
+  std::memset(&g, 0, sizeof(g));
+  g.W = W;
+  g.M = M;
+  g.K = K;
+  g.ldw = K;
+  g.X = X;
+  g.N = N;
+  g.ldx = K;
+  g.out = partial;
+  g.mult = 1.f;
+  if (dtype == DFLASH2_F32) {
+    g.splits = 1;
+  } else {
+    const int chunks = (K + 63) / 64;
+    g.splits = splits > 0 ? std::min(std::min(splits, 64), chunks) : gemm_splits(M, N, K, c.nsm, false);
+  }
+  if ((size_t)g.splits * N * M * sizeof(float) > out_bytes) return DFLASH2_ERR_WORKSPACE;
+  const int r = dtype == DFLASH2_BF16 ? gemm_bf16(g, c) : gemm_f32(g, c);
+  return r ? r : g.splits;
+}
+
+size_t dflash2_test_topk_workspace(int dtype, int M, int N) {
+  const int n_lists = std::max(kMaxSM, topk_scan_lists(M));
+  size_t t = al(256) + 2 * al((size_t)n_lists * N * KMAX * 4);
+  if (dtype == DFLASH2_F32) t += al((size_t)N * M * 4);
+  return t;
+}
+
+int dflash2_test_gemm_topk(int dtype, const void* W, int M, int K, const void* X, int N, int k, float mult,
+                           float cap, int32_t* cand_id, float* cand_logit, float* debug, void* workspace,
+                           size_t ws_bytes, void* stream) {
+  if (dtype != DFLASH2_BF16 && dtype != DFLASH2_F32) return DFLASH2_ERR_DTYPE;
+  if (!W || !X || !cand_id || !cand_logit || !workspace) return DFLASH2_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0 || k < 1 || k > KMAX || k > M || N > 32 * 256) return DFLASH2_ERR_SHAPE;
+  if (ws_bytes < dflash2_test_topk_workspace(dtype, M, N)) return DFLASH2_ERR_WORKSPACE;
+  Ctx c;
+  int rc = test_ctx(&c, stream, static_cast<unsigned*>(workspace));
+  if (rc) return rc;
+  const int n_lists_cap = std::max(kMaxSM, topk_scan_lists(M));
+  char* base = static_cast<char*>(workspace);
+  float* lv = reinterpret_cast<float*>(base + al(256));
+  int* li = reinterpret_cast<int*>(base + al(256) + al((size_t)n_lists_cap * N * KMAX * 4));
+  int n_lists = 0;
+  GemmOp g;
+  std::memset(&g, 0, sizeof(g));
+  g.W = W;
+  g.M = M;
+  g.K = K;
+  g.ldw = K;
+  g.X = X;
+  g.N = N;
+  g.ldx = K;
+  g.mult = mult;
+  g.cap = cap;
+  if (dtype == DFLASH2_BF16) {
+    g.splits = 1;
+    g.topk = true;
+    g.lists_v = lv;
+    g.lists_i = li;
+    g.debug = debug;
+    rc = gemm_bf16(g, c);
+    if (rc) return rc;
+    n_lists = gemm_topk_lists(M, N, K, c.nsm, dtype);
+  } else {
+    float* logits = reinterpret_cast<float*>(base + al(256) + 2 * al((size_t)n_lists_cap * N * KMAX * 4));
+    g.splits = 1;
+    g.out = logits;
+    rc = gemm_f32(g, c);
+    if (rc) return rc;
+    rc = launch_topk_scan(logits, N, M, mult, cap, debug, lv, li, &n_lists, c);
+    if (rc) return rc;
+  }
+  return launch_topk_merge(lv, li, n_lists, N, k, cand_id, cand_logit, c);
+}
+
+}  // extern "C"

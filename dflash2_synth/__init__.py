@@ -52,7 +52,7 @@ def config_of(name, **over):
     """Model/config dict of a workload (mask token = vocab - 1)."""
     c = dict(WORKLOADS[name])
     c.update(over)
-    c["mask_token_id"] = c["vocab"] - 1
+    c.setdefault("mask_token_id", c["vocab"] - 1)
     return c
 
 
@@ -91,16 +91,39 @@ def _rng(seed, name):
     return np.random.Generator(np.random.PCG64([seed, h]))
 
 
-def _draw(seed, name, shape, std, dtype, mean=0.0):
-    x = _rng(seed, name).standard_normal(size=shape, dtype=np.float32)
+_CHUNK = 1 << 22  # elements per independent stream of a large tensor
+
+
+def _fill(out, bits, seed, name, lo, hi, std, mean, dtype):
+    x = _rng(seed, f"{name}#{lo // _CHUNK}").standard_normal(size=hi - lo, dtype=np.float32)
     if std != 1.0:
         x *= np.float32(std)
     if mean != 0.0:
         x += np.float32(mean)
     if dtype == "bf16":
-        bits = to_bf16_bits(x)
-        return Tensor(bf16_bits_to_f32(bits), bits)
-    return Tensor(x)
+        b = to_bf16_bits(x)
+        bits[lo:hi] = b
+        out[lo:hi] = bf16_bits_to_f32(b)
+    else:
+        out[lo:hi] = x
+
+
+def _draw(seed, name, shape, std, dtype, mean=0.0):
+    """N(mean, std) draws; large tensors are cut into chunks of _CHUNK
+    elements, each from its own stream (seed, name#chunk), filled in parallel."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.float32)
+    bits = np.empty(n, dtype=np.uint16) if dtype == "bf16" else None
+    bounds = [(lo, min(n, lo + _CHUNK)) for lo in range(0, n, _CHUNK)]
+    if len(bounds) > 1:
+        import concurrent.futures
+        import os
+        with concurrent.futures.ThreadPoolExecutor(min(32, os.cpu_count() or 4)) as ex:
+            list(ex.map(lambda b: _fill(out, bits, seed, name, b[0], b[1], std, mean, dtype), bounds))
+    else:
+        for lo, hi in bounds:
+            _fill(out, bits, seed, name, lo, hi, std, mean, dtype)
+    return Tensor(out.reshape(shape), None if bits is None else bits.reshape(shape))
 
 
 def make_weights(cfg, seed=None):
@@ -201,3 +224,33 @@ def paged_layout(ctx_cap, page_size, batch, seed, spare_pages=0):
     n_pages = batch * max_pages + spare_pages
     perm = _rng(seed, "pages").permutation(n_pages).astype(np.int32)
     return perm[: batch * max_pages].reshape(batch, max_pages), n_pages
+
+
+# ---------------------------------------------------------------------------
+# torch placement (format conversion only)
+# ---------------------------------------------------------------------------
+
+def to_torch(t, device="cuda"):
+    """Tensor -> torch tensor on `device` (bf16 from its bit patterns)."""
+    import torch
+    if t.bits is not None:
+        return torch.from_numpy(t.bits.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(t.values)).to(device)
+
+
+def device_weights(w, device="cuda"):
+    """Weight dict of Tensor -> weight dict of torch device tensors."""
+    out = {k: to_torch(v, device) for k, v in w.items() if k != "layers"}
+    out["layers"] = [{k: to_torch(v, device) for k, v in L.items()} for L in w["layers"]]
+    return out
+
+
+def small_bf16_config(**over):
+    """A small bf16 shape that still spans several tiles with ragged edges:
+    V = 1000 (7 full 128-row tiles + 104), 2 layers, GQA 4:2."""
+    c = dict(_COMMON, index=10, dtype="bf16", hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=64,
+             intermediate=704, vocab=1000, n_layers=2, block_size=8, top_k=8, selector_rank=16,
+             batch=3, context=(40, 200))
+    c.update(over)
+    c.setdefault("mask_token_id", c["vocab"] - 1)
+    return c

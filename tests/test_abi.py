@@ -1,0 +1,104 @@
+"""The C ABI loads, exports every declared symbol, and its host-side checks
+behave (no GPU needed: only calls that return before touching CUDA)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.conftest import ROOT
+
+pytestmark = pytest.mark.skipif(
+    not (os.path.exists("/usr/local/cuda/bin/nvcc") or __import__("shutil").which("nvcc")),
+    reason="nvcc is needed to build the library")
+
+
+@pytest.fixture(scope="module")
+def B():
+    from block_speculative_decoding_dflash2_gb300 import build as bld
+    bld.build()
+    from block_speculative_decoding_dflash2_gb300 import binding
+    binding.lib()
+    return binding
+
+
+def declared(header):
+    text = open(os.path.join(ROOT, "include", header)).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dflash2_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(B):
+    names = declared("dflash2.h") + declared("dflash2_testing.h")
+    assert "dflash2_draft_step" in names and "dflash2_select_path" in names
+    assert "dflash2_verify_accept" in names
+    lib = ctypes.CDLL(B.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_struct_sizes_match_header(B):
+    # 16 ints + 5 floats; 10 and 6+1 pointers
+    assert ctypes.sizeof(B.Config) == 21 * 4
+    assert ctypes.sizeof(B.LayerWeights) == 10 * 8
+    assert ctypes.sizeof(B.Weights) == 7 * 8
+
+
+def _cfg(B, name, **over):
+    import dflash2_synth as S
+    return B.make_config(S.config_of(name, **over))
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "qwen3_8b_b1", "qwen3_8b_b32_paged", "qwen3_27b_b8"])
+def test_workload_configs_validate(B, name):
+    assert B.dflash2_validate_config(_cfg(B, name)) == 0
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(block_size=1), -3), (dict(block_size=33), -3), (dict(dtype=7), -4),
+    (dict(head_dim=96), -2), (dict(conv_kernel_size=3), -2), (dict(top_k=17), -2),
+    (dict(conv_group_size=33), -2), (dict(n_q_heads=6, n_kv_heads=4), -2),
+    (dict(mask_token_id=4096), -2), (dict(selector_rank=0), -2), (dict(page_size=0), -2),
+])
+def test_bad_configs_are_rejected(B, over, code):
+    assert B.dflash2_validate_config(_cfg(B, "tiny_fp32", **over)) == code
+    assert B.dflash2_workspace_size(_cfg(B, "tiny_fp32", **over), 1, 8, 128) == 0
+
+
+def test_null_config_and_status_strings(B):
+    assert B.lib().dflash2_validate_config(None) == -1
+    for s in (0, -1, -2, -3, -4, -5, -6, -7):
+        assert B.dflash2_status_string(s)
+    assert B.dflash2_version() >= 10000
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "qwen3_8b_b1", "qwen3_27b_b8"])
+def test_workspace_size_is_monotone(B, name):
+    c = _cfg(B, name)
+    prev = 0
+    for b, n, ctx in [(1, 0, 16), (1, 8, 128), (2, 8, 128), (2, 64, 512), (4, 64, 2048), (8, 300, 4096)]:
+        s = B.dflash2_workspace_size(c, b, n, ctx)
+        assert s >= prev > -1
+        prev = s
+    for b in range(1, 9):
+        for n in (0, 1, 8, 17, 64):
+            assert B.dflash2_workspace_size(c, b, n, 512) <= B.dflash2_workspace_size(c, 8, 64, 512)
+
+
+def test_host_side_error_paths_return_before_cuda(B):
+    L = B.lib()
+    # verify: bad block size / batch / null pointers
+    assert L.dflash2_verify_accept(1, 1, 1, 1, 1, 1, 1, 1, None, None, None) == -3
+    assert L.dflash2_verify_accept(0, 8, 1, 1, 1, 1, 1, 1, None, None, None) == -2
+    assert L.dflash2_verify_accept(1, 8, None, 1, 1, 1, 1, 1, None, None, None) == -1
+    c = _cfg(B, "tiny_fp32")
+    w = B.Weights()  # all null
+    assert L.dflash2_draft_step(ctypes.byref(c), ctypes.byref(w), 1, 1, 1, 1, 1, 1, 1, 0, None, 1, 1, 1, 1,
+                                None, 1, 1 << 30, None) == -1
+    bad = _cfg(B, "tiny_fp32", block_size=40)
+    assert L.dflash2_draft_step(ctypes.byref(bad), ctypes.byref(w), 1, 1, 1, 1, 1, 1, 1, 0, None, 1, 1, 1, 1,
+                                None, 1, 1 << 30, None) == -3
+    assert L.dflash2_select_path(ctypes.byref(c), ctypes.byref(w), 1, 1, 1, 1, 1, None, 1, 1 << 30,
+                                 None) == -1
+    assert L.dflash2_read_device_status(None, 0, None) == -5

@@ -1,0 +1,137 @@
+"""Full draft-step parity (stages a-c) with the oracle, the paged cache, the
+device-side guards, and the lossless speculative loop through all three
+entry points."""
+
+import numpy as np
+import pytest
+
+import dflash2_synth as S
+import oracle as O
+from tests.helpers import TOL, Case, lib, topk_compare
+
+pytestmark = pytest.mark.gpu
+
+
+def check_case(case, expect_near_max=1):
+    cfg = case.cfg
+    tol = TOL[cfg["dtype"]]
+    k = cfg["top_k"]
+    dbg = case.debug.double().cpu().numpy()
+    assert case.status == 0
+    assert np.all(np.isfinite(dbg))
+    z = case.oracle_logits()
+    err = np.max(np.abs(dbg - z))
+    assert err <= tol, f"max |logit - oracle| = {err}"
+    cid = case.runner.cand_id.cpu().numpy()
+    cz = case.runner.cand_logit.cpu().numpy()
+    # component parity: oracle top-k of the GPU's own logits, bit-exact
+    ids, vals = O.topk(dbg, k)
+    np.testing.assert_array_equal(cid, ids)
+    np.testing.assert_array_equal(cz, vals.astype(np.float32))
+    # end-to-end: against the oracle's logits, near-ties counted
+    near = topk_compare(cid, z, k, tol)
+    assert near <= expect_near_max
+    return err, near
+
+
+def test_tiny_fp32_draft_step():
+    cfg = S.config_of("tiny_fp32")
+    case = Case(cfg, ctx_lens=[128], n_new=[8]).run_gpu()
+    check_case(case)
+
+
+def test_tiny_fp32_no_new_rows_and_zero_context():
+    cfg = S.config_of("tiny_fp32")
+    check_case(Case(cfg, ctx_lens=[0], n_new=[0], seed=3).run_gpu())
+    check_case(Case(cfg, ctx_lens=[0], n_new=[5], seed=4).run_gpu())
+
+
+def test_small_bf16_paged_ragged_batch():
+    cfg = S.small_bf16_config()
+    case = Case(cfg, ctx_lens=[40, 0, 200], n_new=[1, 8, 3], seed=11).run_gpu()
+    check_case(case)
+
+
+def test_small_bf16_block16_and_groups():
+    cfg = S.small_bf16_config(block_size=16, n_q_heads=8, n_kv_heads=2, head_dim=128, top_k=16,
+                              conv_group_size=64, index=12)
+    case = Case(cfg, ctx_lens=[77, 130], n_new=[16, 2], seed=12).run_gpu()
+    check_case(case)
+
+
+@pytest.mark.slow
+def test_qwen3_8b_shape_batch1():
+    cfg = S.config_of("qwen3_8b_b1")
+    case = Case(cfg, ctx_lens=[2048], n_new=[8], seed=21).run_gpu()
+    err, near = check_case(case, expect_near_max=2)
+
+
+def test_device_guards_flag_bad_page_and_token():
+    import torch
+    cfg = S.small_bf16_config(index=13)
+    case = Case(cfg, ctx_lens=[40, 40], n_new=[2, 2], seed=13)
+    case.run_gpu()
+    assert case.status == 0
+    # corrupt one block-table entry and one anchor: flagged, no fault
+    r = case.runner
+    r.block_table[1, 0] = r.n_pages + 5
+    case.anchor = case.anchor.copy()
+    case.anchor[0] = cfg["vocab"] + 3
+    case.run_gpu()
+    assert case.status & lib().DEV_BAD_PAGE
+    assert case.status & lib().DEV_BAD_TOKEN
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "small_bf16"])
+def test_lossless_speculative_loop(name):
+    """Draft -> select -> verify on the GPU against a toy greedy target: the
+    emitted tokens equal plain greedy decoding, and every step's path equals
+    the oracle's on the same candidates."""
+    import torch
+    B = lib()
+    from block_speculative_decoding_dflash2_gb300.runner import DraftRunner
+    cfg = S.config_of("tiny_fp32") if name == "tiny_fp32" else S.small_bf16_config(batch=1, index=14)
+    V, Bsz = cfg["vocab"], cfg["block_size"]
+    D = Bsz - 1
+    g = np.random.default_rng(5)
+    table = g.integers(0, V - 1, V)
+    n_tok, prompt = 96, 24
+    W = S.make_weights(cfg)
+    Wv = S.values_of(W)
+    taps = S.make_taps(cfg, prompt + n_tok + Bsz + 2, stream="loop")   # row = position
+    r = DraftRunner(cfg, S.device_weights(W), 1, prompt + n_tok + 2 * Bsz, max_new=prompt)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(np.asarray(a, dtype=np.int32))).cuda()
+    tt = S.to_torch(taps)
+    r.append(dev([0]), tt[:prompt].contiguous(), dev([0, prompt]))
+    st = O.Store(cfg["dtype"] == "bf16")
+    last = int(g.integers(0, V - 1))
+    greedy = O.greedy_generate(table, last, n_tok)
+    out = [int(table[last])]
+    anchor = out[0]
+    L, n_new = prompt, 0
+    seq = torch.zeros(1, dtype=torch.int32, device="cuda")
+    while len(out) < n_tok:
+        new = tt[L:L + n_new].contiguous() if n_new else None
+        r.draft(dev([L]), new, dev([0, n_new]), dev([anchor]))
+        r.select(dev([anchor]))
+        path = r.path.cpu().numpy()[0]
+        # oracle selector on the GPU's lattice
+        p_ref, _, _ = O.select_path(cfg, Wv, anchor, r.cand_id.cpu().numpy()[0],
+                                    r.cand_logit.cpu().numpy()[0].astype(np.float64))
+        assert list(p_ref) == list(path)
+        tgt = [int(table[anchor])] + [int(table[p]) for p in path]
+        r.verify(dev([tgt]), seq)
+        a = int(r.accept_len.cpu()[0])
+        a_ref, toks, nxt = O.verify_accept(path, tgt)
+        assert a == a_ref
+        assert list(r.out_tok.cpu().numpy()[0, :a + 1]) == toks
+        out.extend(toks)
+        L += n_new
+        n_new = a + 1
+        anchor = int(r.next_anchor.cpu()[0])
+        assert anchor == nxt
+    assert out[:n_tok] == greedy
+    c = r.counters.cpu().numpy()
+    assert c[0] > 0 and c[1] == D * c[0] and c[2] + c[3] == c[1] and c[4:4 + Bsz].sum() == c[0]
+    assert r.device_status() == 0

@@ -1,0 +1,127 @@
+"""Parity of the dense contraction (tcgen05 + TMA path for bf16, SIMT path for
+fp32) and of the lm_head's streaming top-k against a float64 matrix product
+and the oracle's top-k."""
+
+import numpy as np
+import pytest
+
+import dflash2_synth as S
+import oracle as O
+from tests.helpers import lib
+
+pytestmark = pytest.mark.gpu
+
+
+def _mat(rows, cols, seed, std, dtype):
+    return S._draw(seed, f"m{rows}x{cols}", (rows, cols), std, dtype)
+
+
+@pytest.mark.parametrize("M,N,K,splits", [
+    (128, 16, 64, 1),        # one tile, one K chunk
+    (256, 8, 4096, 0),       # library split-K choice
+    (1000, 7, 256, 1),       # ragged M tile, N below the MMA width
+    (1000, 17, 520, 3),      # ragged M and ragged K tail, N -> 32-wide tile
+    (384, 100, 1024, 2),     # 128-wide activation tile
+    (512, 256, 512, 1),      # 256-wide activation tile
+    (300, 300, 128, 1),      # two activation tiles, ragged everywhere
+    (4096, 8, 12288, 0),     # feature projection shape (8B)
+    (6144, 8, 4096, 0),      # QKV shape (8B)
+])
+def test_bf16_gemm_matches_float64_product(M, N, K, splits):
+    import torch
+    B = lib()
+    W = _mat(M, K, 1, 0.05, "bf16")
+    X = _mat(N, K, 2, 1.0, "bf16")
+    cap = 64
+    part = torch.full((cap, N, M), float("nan"), device="cuda")
+    used = B.dflash2_test_gemm(B.BF16, S.to_torch(W), S.to_torch(X), splits, part)
+    torch.cuda.synchronize()
+    assert 1 <= used <= 64
+    got = part[:used].double().sum(0).cpu().numpy()
+    w64, x64 = W.values.astype(np.float64), X.values.astype(np.float64)
+    ref = x64 @ w64.T
+    bound = np.abs(x64) @ np.abs(w64).T
+    err = np.abs(got - ref)
+    assert np.all(np.isfinite(got))
+    assert np.all(err <= 1e-4 * bound + 1e-6), float(np.max(err / (bound + 1e-30)))
+
+
+@pytest.mark.parametrize("M,N,K", [(1000, 7, 256), (4096, 8, 768), (130, 40, 64)])
+def test_f32_gemm_matches_float64_product(M, N, K):
+    import torch
+    B = lib()
+    W = _mat(M, K, 3, 0.05, "f32")
+    X = _mat(N, K, 4, 1.0, "f32")
+    part = torch.full((1, N, M), float("nan"), device="cuda")
+    assert B.dflash2_test_gemm(B.F32, S.to_torch(W), S.to_torch(X), 0, part) == 1
+    torch.cuda.synchronize()
+    got = part[0].double().cpu().numpy()
+    ref = X.values.astype(np.float64) @ W.values.astype(np.float64).T
+    bound = np.abs(X.values.astype(np.float64)) @ np.abs(W.values.astype(np.float64)).T
+    assert np.all(np.abs(got - ref) <= 1e-5 * bound + 1e-7)
+
+
+def _topk_run(dtype, W, X, k, mult=1.0, cap=0.0):
+    import torch
+    B = lib()
+    M, N = W.shape[0], X.shape[0]
+    ws = torch.zeros(B.dflash2_test_topk_workspace(dtype, M, N), dtype=torch.uint8, device="cuda")
+    cid = torch.full((N, k), -7, dtype=torch.int32, device="cuda")
+    cz = torch.zeros((N, k), dtype=torch.float32, device="cuda")
+    dbg = torch.full((N, M), float("nan"), device="cuda")
+    B.dflash2_test_gemm_topk(dtype, S.to_torch(W), S.to_torch(X), k, mult, cap, cid, cz, dbg, ws)
+    torch.cuda.synchronize()
+    return cid.cpu().numpy(), cz.cpu().numpy(), dbg.cpu().numpy()
+
+
+@pytest.mark.parametrize("dtype,M,N,k", [
+    ("bf16", 1000, 7, 4), ("bf16", 1000, 16, 16), ("bf16", 4096 + 50, 40, 16), ("bf16", 2000, 300, 8),
+    ("bf16", 151936, 7, 16), ("f32", 4096, 7, 4), ("f32", 3000, 9, 16),
+])
+def test_lm_head_topk_component_parity(dtype, M, N, k):
+    K = 256
+    W = _mat(M, K, 5, 0.05, dtype)
+    X = _mat(N, K, 6, 1.0, dtype)
+    cid, cz, dbg = _topk_run(1 if dtype == "bf16" else 0, W, X, k)
+    assert np.all(np.isfinite(dbg))
+    # the logits the kernel scored agree with the float64 product
+    ref = X.values.astype(np.float64) @ W.values.astype(np.float64).T
+    bound = np.abs(X.values.astype(np.float64)) @ np.abs(W.values.astype(np.float64)).T
+    assert np.all(np.abs(dbg - ref) <= 1e-4 * bound + 1e-6)
+    # component parity: the oracle's top-k of the GPU's own logits, bit-exact
+    ids, vals = O.topk(dbg.astype(np.float64), k)
+    np.testing.assert_array_equal(cid, ids)
+    np.testing.assert_array_equal(cz, vals.astype(np.float32))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_lm_head_topk_exact_ties_take_smaller_ids(dtype):
+    # rows repeat with period 5, so every logit value appears many times
+    base = _mat(5, 128, 7, 0.05, dtype)
+    reps = 700
+    vals = np.tile(base.values, (reps, 1))
+    if dtype == "bf16":
+        W = S.Tensor(vals, np.tile(base.bits, (reps, 1)))
+    else:
+        W = S.Tensor(np.ascontiguousarray(vals))
+    X = _mat(6, 128, 8, 1.0, dtype)
+    cid, _, dbg = _topk_run(1 if dtype == "bf16" else 0, W, X, 16)
+    ids, _ = O.topk(dbg.astype(np.float64), 16)
+    np.testing.assert_array_equal(cid, ids)
+    # all ties: the best value's 16 smallest ids come first
+    for r in range(6):
+        best = int(np.argmax(dbg[r, :5]))
+        assert list(cid[r]) == [best + 5 * j for j in range(16)]
+
+
+def test_lm_head_multiplier_and_softcap():
+    K, M, N = 128, 1000, 7
+    W = _mat(M, K, 9, 0.5, "bf16")
+    X = _mat(N, K, 10, 1.0, "bf16")
+    cid, cz, dbg = _topk_run(1, W, X, 8, mult=2.0, cap=3.0)
+    ref = X.values.astype(np.float64) @ W.values.astype(np.float64).T
+    z = 3.0 * np.tanh(2.0 * ref / 3.0)
+    assert np.max(np.abs(dbg - z)) < 1e-4
+    assert np.all(np.abs(dbg) <= 3.0)
+    ids, _ = O.topk(dbg.astype(np.float64), 8)
+    np.testing.assert_array_equal(cid, ids)

@@ -1,0 +1,136 @@
+"""Parity of the selector (factor gather + GEMM + Viterbi) and of greedy
+verify/accept/rollback with the oracle, on identical inputs."""
+
+import numpy as np
+import pytest
+
+import dflash2_synth as S
+import oracle as O
+from tests.conftest import read_golden
+from tests.helpers import lib
+
+pytestmark = pytest.mark.gpu
+
+
+def sel_cfg(dtype, V, H, k, D, r):
+    return dict(hidden=H, n_q_heads=2, n_kv_heads=2, head_dim=64, intermediate=64, vocab=V, n_layers=1,
+                n_taps=1, block_size=D + 1, conv_kernel_size=2, conv_group_size=H, top_k=k,
+                selector_rank=r, page_size=16, mask_token_id=V - 1, dtype=dtype, rms_eps=1e-6,
+                rope_theta=1e6, input_embedding_scale=1.0, output_multiplier=1.0,
+                final_logit_softcap=0.0)
+
+
+def run_select(dtype, V, H, k, D, r, b, seed, emb_std=1.0, sel_std=0.3, logit_std=1.0):
+    import torch
+    B = lib()
+    cfg = sel_cfg(dtype, V, H, k, D, r)
+    E = S._draw(seed, "E", (V, H), emb_std / np.sqrt(H), dtype)
+    Wsel = S._draw(seed, "sel", (2 * r, H), sel_std, dtype)
+    g = np.random.default_rng(seed)
+    cand = np.stack([np.stack([g.choice(V - 1, size=k, replace=False) for _ in range(D)]) for _ in range(b)])
+    z = -np.sort(-g.standard_normal((b, D, k)).astype(np.float32) * logit_std, axis=2)
+    anchor = g.integers(0, V - 1, size=b).astype(np.int32)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    w = B.WeightSet({"embed": S.to_torch(E), "sel": S.to_torch(Wsel), "lm_head": None, "fc": None,
+                     "hidden_norm": None, "final_norm": None, "layers": []})
+    c = B.make_config(cfg)
+    ws = torch.zeros(B.dflash2_workspace_size(c, b, 0, 16), dtype=torch.uint8, device="cuda")
+    path = torch.full((b, D), -5, dtype=torch.int32, device="cuda")
+    score = torch.zeros(b, dtype=torch.float32, device="cuda")
+    B.dflash2_select_path(c, w, b, dev(anchor), dev(cand.astype(np.int32)), dev(z), path, score, ws)
+    torch.cuda.synchronize()
+    Wo = {"embed": E.values, "sel": Wsel.values}
+    return cfg, Wo, anchor, cand, z, path.cpu().numpy(), score.cpu().numpy()
+
+
+@pytest.mark.parametrize("dtype,V,H,k,D,r,b", [
+    ("bf16", 4096, 256, 16, 7, 64, 4),
+    ("bf16", 2000, 128, 4, 7, 16, 3),
+    ("bf16", 151936, 4096, 16, 7, 64, 2),
+    ("bf16", 5000, 512, 16, 15, 64, 2),
+    ("f32", 4096, 256, 4, 7, 16, 3),
+])
+def test_selector_matches_oracle_viterbi(dtype, V, H, k, D, r, b):
+    cfg, W, anchor, cand, z, path, score = run_select(dtype, V, H, k, D, r, b, seed=V + k)
+    near = 0
+    for s in range(b):
+        p, idx, sc = O.select_path(cfg, W, int(anchor[s]), cand[s], z[s].astype(np.float64))
+        assert abs(score[s] - sc) < 1e-3 * max(1.0, abs(sc))
+        if list(path[s]) != list(p):
+            # a different path is allowed only if the oracle scores it within 1e-4
+            gi = [list(cand[s, i]).index(path[s, i]) for i in range(D)]
+            alt = O.path_score(cfg, W, int(anchor[s]), cand[s], z[s].astype(np.float64), gi)
+            assert sc - alt < 1e-4, (s, list(path[s]), list(p))
+            near += 1
+    assert near <= max(1, b // 4)
+
+
+def test_selector_pairwise_term_matters_and_brute_force():
+    # strong factors so paths leave the per-position argmax; k=4, D=7 brute force
+    cfg, W, anchor, cand, z, path, score = run_select("bf16", 1000, 128, 4, 7, 16, 6, seed=3,
+                                                      emb_std=3.0, sel_std=1.0, logit_std=0.5)
+    moved = 0
+    for s in range(6):
+        pb, idxb, sb = O.brute_force_path(cfg, W, int(anchor[s]), cand[s], z[s].astype(np.float64))
+        assert list(path[s]) == list(pb)
+        assert abs(score[s] - sb) < 1e-3 * max(1.0, abs(sb))
+        moved += int(np.any(idxb != 0))
+    assert moved > 0
+
+
+def test_selector_without_pairwise_term_is_top1():
+    import torch
+    cfg, W, anchor, cand, z, path, score = run_select("bf16", 1000, 128, 8, 7, 16, 3, seed=4, sel_std=0.0)
+    np.testing.assert_array_equal(path, cand[:, :, 0])
+
+
+def _verify(paths, targets, B_, seq_len=None, counters=None):
+    import torch
+    B = lib()
+    b = paths.shape[0]
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+    acc = torch.full((b,), -9, dtype=torch.int32, device="cuda")
+    out = torch.full((b, B_), -9, dtype=torch.int32, device="cuda")
+    n_out = torch.zeros(b, dtype=torch.int32, device="cuda")
+    nxt = torch.zeros(b, dtype=torch.int32, device="cuda")
+    sl = dev(seq_len) if seq_len is not None else None
+    B.dflash2_verify_accept(b, B_, dev(paths), dev(targets), acc, out, n_out, nxt, sl, counters)
+    torch.cuda.synchronize()
+    return acc.cpu().numpy(), out.cpu().numpy(), n_out.cpu().numpy(), nxt.cpu().numpy(), \
+        (sl.cpu().numpy() if sl is not None else None)
+
+
+def test_verify_golden_cases_on_gpu():
+    for path, tgt, a, out, nxt in read_golden("verify_cases.txt"):
+        p = np.array([[int(x) for x in path.split()]])
+        t = np.array([[int(x) for x in tgt.split()]])
+        Bsz = t.shape[1]
+        acc, o, n, nx, _ = _verify(p, t, Bsz)
+        assert acc[0] == int(a) and nx[0] == int(nxt) and n[0] == int(a) + 1
+        exp = [int(x) for x in out.split()]
+        assert list(o[0, :len(exp)]) == exp and np.all(o[0, len(exp):] == -1)
+
+
+@pytest.mark.parametrize("B_", [2, 8, 16, 32])
+def test_verify_and_counters_match_oracle(B_):
+    import torch
+    g = np.random.default_rng(B_)
+    b, D = 300, B_ - 1
+    paths = g.integers(0, 3, (b, D))
+    targets = g.integers(0, 3, (b, B_))
+    seq = g.integers(0, 1000, b)
+    counters = torch.zeros(4 + 2 * B_ - 1, dtype=torch.int64, device="cuda")
+    acc, out, n, nx, sl = _verify(paths, targets, B_, seq_len=seq, counters=counters)
+    acc2, *_ = _verify(paths, targets, B_, counters=counters)      # accumulate a second time
+    cnt = O.Counters(D)
+    for s in range(b):
+        a, toks, na = O.verify_accept(paths[s], targets[s])
+        cnt.add(a)
+        cnt.add(a)
+        assert acc[s] == a and nx[s] == na and n[s] == a + 1
+        assert list(out[s, :a + 1]) == toks and np.all(out[s, a + 1:] == -1)
+        assert sl[s] == seq[s] + a + 1
+    c = counters.cpu().numpy()
+    assert c[0] == cnt.steps and c[1] == cnt.drafted and c[2] == cnt.accepted and c[3] == cnt.rollback
+    np.testing.assert_array_equal(c[4:4 + B_], cnt.hist)
+    np.testing.assert_array_equal(c[4 + B_:], cnt.acc_pos)

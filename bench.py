@@ -191,10 +191,7 @@ def run_ours(a, rank, world):
     for e in evs:
         e.record()
     torch.cuda.synchronize()
-    import ctypes
-    arr = (ctypes.c_void_p * 5)(*[e.cuda_event for e in evs])
-    Bd.lib().dflash2_set_stage_events.argtypes = [ctypes.c_void_p]
-    Bd.lib().dflash2_set_stage_events(ctypes.cast(arr, ctypes.c_void_p))
+    keep = Bd.dflash2_set_stage_events(evs)  # noqa: F841  (the handle array must outlive the capture)
     s = torch.cuda.Stream()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(s):

@@ -83,8 +83,15 @@ def lib():
         L.dflash2_verify_accept.argtypes = [I, I, P, P, P, P, P, P, P, P, P]
         L.dflash2_read_device_status.restype = I
         L.dflash2_read_device_status.argtypes = [P, S, P]
+        L.dflash2_test_gemm_workspace.restype = S
+        L.dflash2_test_gemm_workspace.argtypes = [I, I, I]
         L.dflash2_test_gemm.restype = I
-        L.dflash2_test_gemm.argtypes = [I, P, I, I, P, I, I, P, S, P]
+        L.dflash2_test_gemm.argtypes = [I, P, I, I, P, I, I, I, P, P, S, P]
+        L.dflash2_test_layout.restype = I
+        L.dflash2_test_layout.argtypes = [F(Config), I, I, I, F(ctypes.c_size_t), I]
+        L.dflash2_launch_count.restype = ctypes.c_int64
+        L.dflash2_set_stage_events.restype = None
+        L.dflash2_set_stage_events.argtypes = [P]
         L.dflash2_test_topk_workspace.restype = S
         L.dflash2_test_topk_workspace.argtypes = [I, I, I]
         L.dflash2_test_gemm_topk.restype = I
@@ -202,11 +209,15 @@ def dflash2_read_device_status(workspace, stream=None):
 # (include/dflash2_testing.h: the internal contraction and the lm_head top-k
 # path on their own, for parity tests)
 
-def dflash2_test_gemm(dtype, W, X, splits, partial, stream=None):
+def dflash2_test_gemm_workspace(M, N, splits):
+    return lib().dflash2_test_gemm_workspace(M, N, splits)
+
+
+def dflash2_test_gemm(dtype, W, X, splits, out, workspace, accumulate=False, stream=None):
     M, K = W.shape
     N = X.shape[0]
-    rc = lib().dflash2_test_gemm(dtype, _ptr(W), M, K, _ptr(X), N, splits, _ptr(partial),
-                                 partial.numel() * partial.element_size(), _stream(stream))
+    rc = lib().dflash2_test_gemm(dtype, _ptr(W), M, K, _ptr(X), N, splits, int(accumulate), _ptr(out),
+                                 _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     if rc < 0:
         _check("dflash2_test_gemm", rc)
     return rc
@@ -222,3 +233,24 @@ def dflash2_test_gemm_topk(dtype, W, X, k, mult, cap, cand_id, cand_logit, debug
     return _check("dflash2_test_gemm_topk", lib().dflash2_test_gemm_topk(
         dtype, _ptr(W), M, K, _ptr(X), N, k, mult, cap, _ptr(cand_id), _ptr(cand_logit), _ptr(debug),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def dflash2_test_layout(cfg, batch, n_new, max_ctx):
+    """Workspace byte offsets of {f, h, u, u2, q, kb, vb, O, act, hn}."""
+    out = (ctypes.c_size_t * 10)()
+    _check("dflash2_test_layout", lib().dflash2_test_layout(ctypes.byref(cfg), batch, n_new, max_ctx, out, 10))
+    return dict(zip(("f", "h", "u", "u2", "q", "kb", "vb", "O", "act", "hn"), list(out)))
+
+
+def dflash2_launch_count():
+    return lib().dflash2_launch_count()
+
+
+def dflash2_set_stage_events(events):
+    """events: None, or 5 torch.cuda.Event(enable_timing=True) already recorded once."""
+    if events is None:
+        lib().dflash2_set_stage_events(None)
+        return None
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    lib().dflash2_set_stage_events(ctypes.cast(arr, ctypes.c_void_p))
+    return arr

@@ -30,12 +30,23 @@ std::atomic<long long> g_launches{0};
 void* volatile g_stage_events[DFLASH2_N_STAGE_EVENTS] = {nullptr};
 std::atomic<int> g_stage_on{0};
 
-// Records stage event i on the call's stream (an external record, so it is
-// kept as an event node when the stream is being captured into a graph).
-void stage_event(int i, cudaStream_t st) {
-  if (!g_stage_on.load(std::memory_order_relaxed)) return;
+// Records stage event i on the call's stream.  While the stream is being
+// captured the record is made external, so it stays in the graph as an event
+// node that later replays fire; otherwise it is a plain record.
+int stage_event(int i, cudaStream_t st) {
+  if (!g_stage_on.load(std::memory_order_relaxed)) return DFLASH2_OK;
   cudaEvent_t ev = static_cast<cudaEvent_t>(g_stage_events[i]);
-  if (ev) cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+  if (!ev) return DFLASH2_OK;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(st, &cs);
+  if (e == cudaSuccess)
+    e = cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal)
+                                            : cudaEventRecord(ev, st);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return DFLASH2_ERR_CUDA;
+  }
+  return DFLASH2_OK;
 }
 
 int esize(int dtype) { return dtype == DFLASH2_BF16 ? 2 : 4; }
@@ -57,7 +68,8 @@ int check_config(const dflash2_config* c) {
   if (c->selector_rank < 1 || c->selector_rank > 128) return DFLASH2_ERR_SHAPE;
   if (c->mask_token_id < 0 || c->mask_token_id >= c->vocab) return DFLASH2_ERR_SHAPE;
   if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return DFLASH2_ERR_SHAPE;
-  if (c->dtype == DFLASH2_BF16 && (c->hidden % 8 || c->intermediate % 8)) return DFLASH2_ERR_SHAPE;
+  // 16-byte vector access of rows and channel groups
+  if (c->hidden % 8 || c->intermediate % 8 || c->conv_group_size % 4) return DFLASH2_ERR_SHAPE;
   const int R = (c->n_q_heads / c->n_kv_heads) * c->block_size;
   if (R * c->head_dim > 128 * 128) return DFLASH2_ERR_SHAPE;  // attention rows held in shared memory
   if (viterbi_smem_bytes(c->block_size - 1, c->top_k, c->selector_rank) > 200 * 1024) return DFLASH2_ERR_SHAPE;
@@ -82,7 +94,7 @@ size_t partial_bound(int M, int N, int K) {
   for (int n : probes)
     for (int nsm = 1; nsm <= kMaxSM; ++nsm) {
       const int s = gemm_splits(M, n, K, nsm, false);
-      best = std::max(best, (size_t)s * n * M * sizeof(float));
+      if (s > 1) best = std::max(best, (size_t)s * n * M * sizeof(float));
     }
   std::lock_guard<std::mutex> g(mu);
   memo[std::make_tuple(M, N, K)] = best;
@@ -90,7 +102,7 @@ size_t partial_bound(int M, int N, int K) {
 }
 
 struct Layout {
-  size_t status, f, P, h, u, u2, q, kb, vb, attn, O, act, hn, logits, lv, li, selx, total;
+  size_t status, cnt, f, Y, P, h, u, u2, q, kb, vb, attn, O, act, hn, logits, lv, li, selx, total;
 };
 
 Layout plan(const dflash2_config& c, int batch, int n_new, int max_ctx) {
@@ -99,18 +111,21 @@ Layout plan(const dflash2_config& c, int batch, int n_new, int max_ctx) {
   const int G = H / c.conv_group_size, r = c.selector_rank, k = c.top_k;
   const int rows = batch * B;
   const int nsel = batch * (D * k + 1);
-  size_t P = 0;
-  if (n_new > 0) {
-    P = std::max(P, partial_bound(H, n_new, c.n_taps * H));
-    P = std::max(P, partial_bound(2 * nkv * d, n_new, H));
-  }
-  if (batch > 0) {
-    P = std::max(P, partial_bound(2 * G, rows, H));
-    P = std::max(P, partial_bound((nq + 2 * nkv) * d, rows, H));
-    P = std::max(P, partial_bound(H, rows, nq * d));
-    P = std::max(P, partial_bound(2 * I, rows, H));
-    P = std::max(P, partial_bound(H, rows, I));
-    P = std::max(P, partial_bound(2 * r, nsel, H));
+  // every contraction of a call: {M, N, K, writes Y}
+  struct Shape {
+    int M, N, K;
+    bool y;
+  };
+  const Shape shapes[8] = {{H, n_new, c.n_taps * H, true},      {2 * nkv * d, n_new, H, true},
+                           {2 * G, rows, H, true},              {(nq + 2 * nkv) * d, rows, H, true},
+                           {H, rows, nq * d, false},            {2 * I, rows, H, true},
+                           {H, rows, I, false},                 {2 * r, nsel, H, true}};
+  size_t P = 0, Yb = 0, tiles = 0;
+  for (const Shape& sh : shapes) {
+    if (sh.N <= 0) continue;
+    P = std::max(P, partial_bound(sh.M, sh.N, sh.K));
+    if (sh.y) Yb = std::max(Yb, (size_t)sh.N * sh.M * sizeof(float));
+    tiles = std::max(tiles, (size_t)gemm_tiles(sh.M, sh.N));
   }
   const int n_lists = std::max(kMaxSM, topk_scan_lists(c.vocab));
   Layout L;
@@ -121,7 +136,9 @@ Layout plan(const dflash2_config& c, int batch, int n_new, int max_ctx) {
     return at;
   };
   L.status = take(256);
+  L.cnt = take(tiles * sizeof(int));
   L.f = take((size_t)n_new * H * es);
+  L.Y = take(Yb);
   L.P = take(P);
   L.h = take((size_t)rows * H * 4);
   L.u = take((size_t)rows * H * es);
@@ -178,8 +195,10 @@ P* at(void* ws, size_t off) {
   return reinterpret_cast<P*>(static_cast<char*>(ws) + off);
 }
 
-int gemm(const dflash2_config& c, const Ctx& ctx, const void* W, int M, int K, const void* X, int N, float* P,
-         int* S) {
+// out[n][m] (= or +=) sum_k W[m][k] X[n][k]; split-K partials and tile
+// counters live in the workspace regions of L.
+int gemm(const dflash2_config& c, const Ctx& ctx, void* ws, const Layout& L, const void* W, int M, int K,
+         const void* X, int N, float* out, bool accumulate) {
   GemmOp g;
   std::memset(&g, 0, sizeof(g));
   g.W = W;
@@ -189,15 +208,16 @@ int gemm(const dflash2_config& c, const Ctx& ctx, const void* W, int M, int K, c
   g.X = X;
   g.N = N;
   g.ldx = K;
-  g.out = P;
+  g.out = out;
+  g.accumulate = accumulate;
+  g.partial = reinterpret_cast<float*>(static_cast<char*>(ws) + L.P);
+  g.counters = reinterpret_cast<int*>(static_cast<char*>(ws) + L.cnt);
   g.mult = 1.f;
   if (c.dtype == DFLASH2_BF16) {
     g.splits = gemm_splits(M, N, K, ctx.nsm, false);
-    *S = g.splits;
     return gemm_bf16(g, ctx);
   }
   g.splits = 1;
-  *S = 1;
   return gemm_f32(g, ctx);
 }
 
@@ -223,17 +243,16 @@ int run_append(const dflash2_config& c, const dflash2_weights& w, void* kc, void
                const void* taps, const int32_t* new_off, void* ws, const Layout& L, const Ctx& ctx) {
   if (n_new == 0) return DFLASH2_OK;
   const int H = c.hidden, nq = c.n_q_heads, nkv = c.n_kv_heads, d = c.head_dim;
-  float* P = at<float>(ws, L.P);
+  float* Y = at<float>(ws, L.Y);
   void* f = at<char>(ws, L.f);
-  int S = 1;
-  TRY(gemm(c, ctx, w.fc, H, c.n_taps * H, taps, n_new, P, &S));
-  TRY(launch_rows_feature_norm(c.dtype, P, S, n_new, H, w.hidden_norm, c.rms_eps, f, ctx));
+  TRY(gemm(c, ctx, ws, L, w.fc, H, c.n_taps * H, taps, n_new, Y, false));
+  TRY(launch_rows_feature_norm(c.dtype, Y, n_new, H, w.hidden_norm, c.rms_eps, f, ctx));
   const size_t layer_elems = (size_t)n_pages * c.page_size * nkv * d;
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash2_layer_weights& Lw = w.layers[l];
     const void* wkv = elem_ptr(Lw.qkv, (size_t)nq * d * H, c.dtype);
-    TRY(gemm(c, ctx, wkv, 2 * nkv * d, H, f, n_new, P, &S));
-    TRY(launch_kv_append(c.dtype, P, S, n_new, nkv, d, Lw.k_norm, c.rms_eps, c.rope_theta, ctx_len, new_off, batch,
+    TRY(gemm(c, ctx, ws, L, wkv, 2 * nkv * d, H, f, n_new, Y, false));
+    TRY(launch_kv_append(c.dtype, Y, n_new, nkv, d, Lw.k_norm, c.rms_eps, c.rope_theta, ctx_len, new_off, batch,
                          block_table, max_pages, c.page_size, n_pages,
                          const_cast<char*>(elem_ptr(kc, l * layer_elems, c.dtype)),
                          const_cast<char*>(elem_ptr(vc, l * layer_elems, c.dtype)), ctx));
@@ -252,6 +271,15 @@ int check_cache_args(void* kc, void* vc, int n_pages, const int32_t* block_table
 }  // namespace
 
 void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+int workspace_offsets(const dflash2_config* c, int batch, int n_new, int max_ctx, size_t* out, int n) {
+  if (check_config(c) != DFLASH2_OK) return DFLASH2_ERR_SHAPE;
+  if (!out || n < 10) return DFLASH2_ERR_INVALID_ARG;
+  const Layout L = plan(*c, batch, n_new, max_ctx);
+  const size_t v[10] = {L.f, L.h, L.u, L.u2, L.q, L.kb, L.vb, L.O, L.act, L.hn};
+  for (int i = 0; i < 10; ++i) out[i] = v[i];
+  return DFLASH2_OK;
+}
 
 }  // namespace df2
 
@@ -327,14 +355,14 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
   Ctx ctx;
   TRY(device_ctx(&ctx, stream, workspace));
 
-  stage_event(0, ctx.stream);
+  TRY(stage_event(0, ctx.stream));
   TRY(run_append(c, *w, k_cache, v_cache, n_pages, block_table, max_pages, batch, ctx_len, n_new, new_taps, new_off,
                  workspace, L, ctx));
-  stage_event(1, ctx.stream);
+  TRY(stage_event(1, ctx.stream));
 
   const int H = c.hidden, B = c.block_size, D = B - 1, nq = c.n_q_heads, nkv = c.n_kv_heads, d = c.head_dim;
   const int I = c.intermediate, G = H / c.conv_group_size, rows = batch * B;
-  float* P = at<float>(workspace, L.P);
+  float* Y = at<float>(workspace, L.Y);
   float* h = at<float>(workspace, L.h);
   void* u = at<char>(workspace, L.u);
   void* u2 = at<char>(workspace, L.u2);
@@ -345,37 +373,36 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
   void* act = at<char>(workspace, L.act);
   void* hn = at<char>(workspace, L.hn);
   const size_t layer_elems = (size_t)n_pages * c.page_size * nkv * d;
-  int S = 1;
+  void* ws = workspace;
 
-  TRY(launch_embed_block(c.dtype, anchor, c.mask_token_id, batch, B, w->embed, c.vocab, H, c.input_embedding_scale,
-                         h, ctx));
-  TRY(launch_residual_norm(c.dtype, h, nullptr, 1, rows, H, w->layers[0].attn_norm, c.rms_eps, u, B, 0, ctx));
+  TRY(launch_embed_norm(c.dtype, anchor, c.mask_token_id, batch, B, w->embed, c.vocab, H, c.input_embedding_scale,
+                        w->layers[0].attn_norm, c.rms_eps, h, u, ctx));
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash2_layer_weights& Lw = w->layers[l];
-    // attention sublayer
-    TRY(gemm(c, ctx, Lw.tapgen_attn, 2 * G, H, u, rows, P, &S));
-    TRY(launch_dyn_conv(c.dtype, u, P, S, rows, H, c.conv_group_size, B, u2, ctx));
-    TRY(gemm(c, ctx, Lw.qkv, (nq + 2 * nkv) * d, H, u2, rows, P, &S));
-    TRY(launch_qkv_epilogue(c.dtype, P, S, rows, B, nq, nkv, d, Lw.q_norm, Lw.k_norm, c.rms_eps, c.rope_theta,
-                            ctx_len, new_off, q, kb, vb, ctx));
+    // attention sublayer: conv around the normed input, QKV, attention, O (+= residual)
+    TRY(gemm(c, ctx, ws, L, Lw.tapgen_attn, 2 * G, H, u, rows, Y, false));
+    TRY(launch_dyn_conv(c.dtype, u, Y, rows, H, c.conv_group_size, B, u2, ctx));
+    TRY(gemm(c, ctx, ws, L, Lw.qkv, (nq + 2 * nkv) * d, H, u2, rows, Y, false));
+    TRY(launch_qkv_epilogue(c.dtype, Y, rows, B, nq, nkv, d, Lw.q_norm, Lw.k_norm, c.rms_eps, c.rope_theta, ctx_len,
+                            new_off, q, kb, vb, ctx));
     TRY(launch_attention(c.dtype, q, kb, vb, elem_ptr(k_cache, l * layer_elems, c.dtype),
                          elem_ptr(v_cache, l * layer_elems, c.dtype), block_table, max_pages, c.page_size, n_pages,
                          ctx_len, new_off, batch, B, nq, nkv, d, max_ctx, at<float>(workspace, L.attn), O, ctx));
-    TRY(gemm(c, ctx, Lw.o, H, nq * d, O, rows, P, &S));
-    TRY(launch_residual_norm(c.dtype, h, P, S, rows, H, Lw.mlp_norm, c.rms_eps, u, B, 0, ctx));
-    // MLP sublayer
-    TRY(gemm(c, ctx, Lw.tapgen_mlp, 2 * G, H, u, rows, P, &S));
-    TRY(launch_dyn_conv(c.dtype, u, P, S, rows, H, c.conv_group_size, B, u2, ctx));
-    TRY(gemm(c, ctx, Lw.gate_up, 2 * I, H, u2, rows, P, &S));
-    TRY(launch_act(c.dtype, P, S, rows, I, act, ctx));
-    TRY(gemm(c, ctx, Lw.down, H, I, act, rows, P, &S));
+    TRY(gemm(c, ctx, ws, L, Lw.o, H, nq * d, O, rows, h, true));
+    TRY(launch_rownorm(c.dtype, h, rows, H, Lw.mlp_norm, c.rms_eps, u, B, 0, ctx));
+    // MLP sublayer: conv around the normed input, gate/up, SiLU*up, down (+= residual)
+    TRY(gemm(c, ctx, ws, L, Lw.tapgen_mlp, 2 * G, H, u, rows, Y, false));
+    TRY(launch_dyn_conv(c.dtype, u, Y, rows, H, c.conv_group_size, B, u2, ctx));
+    TRY(gemm(c, ctx, ws, L, Lw.gate_up, 2 * I, H, u2, rows, Y, false));
+    TRY(launch_act(c.dtype, Y, rows, I, act, ctx));
+    TRY(gemm(c, ctx, ws, L, Lw.down, H, I, act, rows, h, true));
     if (l + 1 < c.n_layers)
-      TRY(launch_residual_norm(c.dtype, h, P, S, rows, H, w->layers[l + 1].attn_norm, c.rms_eps, u, B, 0, ctx));
+      TRY(launch_rownorm(c.dtype, h, rows, H, w->layers[l + 1].attn_norm, c.rms_eps, u, B, 0, ctx));
     else
-      TRY(launch_residual_norm(c.dtype, h, P, S, rows, H, w->final_norm, c.rms_eps, hn, B, 1, ctx));
+      TRY(launch_rownorm(c.dtype, h, rows, H, w->final_norm, c.rms_eps, hn, B, 1, ctx));
   }
 
-  stage_event(2, ctx.stream);
+  TRY(stage_event(2, ctx.stream));
   // (c) lm_head over block positions 1..B-1 with the streaming top-k
   float* lv = at<float>(workspace, L.lv);
   int* li = at<int>(workspace, L.li);
@@ -402,13 +429,13 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
     n_lists = gemm_topk_lists(c.vocab, nrow, H, ctx.nsm, c.dtype);
   } else {
     float* logits = at<float>(workspace, L.logits);
-    TRY(gemm(c, ctx, w->lm_head, c.vocab, H, hn, nrow, logits, &S));
+    TRY(gemm(c, ctx, workspace, L, w->lm_head, c.vocab, H, hn, nrow, logits, false));
     TRY(launch_topk_scan(logits, nrow, c.vocab, c.output_multiplier, c.final_logit_softcap, debug_logits, lv, li,
                          &n_lists, ctx));
   }
-  stage_event(3, ctx.stream);
+  TRY(stage_event(3, ctx.stream));
   TRY(launch_topk_merge(lv, li, n_lists, nrow, c.top_k, cand_id, cand_logit, ctx));
-  stage_event(4, ctx.stream);
+  TRY(stage_event(4, ctx.stream));
   return DFLASH2_OK;
 }
 
@@ -427,11 +454,10 @@ int dflash2_select_path(const dflash2_config* cfg, const dflash2_weights* w, int
   TRY(device_ctx(&ctx, stream, workspace));
   const int D = c.block_size - 1, k = c.top_k, r = c.selector_rank, H = c.hidden;
   void* x = at<char>(workspace, L.selx);
-  float* P = at<float>(workspace, L.P);
-  int S = 1;
+  float* Y = at<float>(workspace, L.Y);
   TRY(launch_sel_gather(c.dtype, anchor, cand_id, batch, D, k, w->embed, c.vocab, H, x, ctx));
-  TRY(gemm(c, ctx, w->sel, 2 * r, H, x, batch * (D * k + 1), P, &S));
-  return launch_viterbi(P, S, anchor, cand_id, cand_logit, batch, D, k, r, path, path_score, ctx);
+  TRY(gemm(c, ctx, workspace, L, w->sel, 2 * r, H, x, batch * (D * k + 1), Y, false));
+  return launch_viterbi(Y, cand_id, cand_logit, batch, D, k, r, path, path_score, ctx);
 }
 
 int dflash2_verify_accept(int batch, int block_size, const int32_t* path, const int32_t* target,

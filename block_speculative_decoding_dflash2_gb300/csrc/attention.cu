@@ -11,7 +11,8 @@
 // query rows that share that kv head (GQA packing), streams its key chunk
 // through shared memory with an online softmax and writes an unnormalised
 // partial (acc, running max, running sum).  A second kernel combines the
-// chunks.  No CTA waits on another.
+// chunks.  No CTA waits on another.  Keys are gathered row by row (one page
+// lookup per key, then 16-byte loads of its d contiguous elements).
 #include <algorithm>
 
 #include "common.cuh"
@@ -25,12 +26,30 @@ constexpr int AT = 256;  // threads
 constexpr int KT = 32;   // keys per shared-memory tile
 
 size_t attn_smem(int R, int d) {
-  return sizeof(float) * ((size_t)R * d        /* Qs */
+  return sizeof(float) * ((size_t)R * d          /* Qs */
                           + (size_t)KT * (d + 1) /* Ks */
                           + (size_t)KT * d       /* Vs */
                           + (size_t)R * KT       /* Ss */
                           + (size_t)R * d        /* acc */
-                          + 3 * (size_t)R);      /* m, l, fac */
+                          + 3 * (size_t)R + 1)   /* m, l, fac (+ alignment) */
+         + sizeof(long long) * KT;               /* per-key row offsets */
+}
+
+// 8 consecutive elements as floats (16 bytes of bf16, or two float4).
+__device__ __forceinline__ void load8(const bf16* p, float* o) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    o[2 * i] = f.x;
+    o[2 * i + 1] = f.y;
+  }
+}
+__device__ __forceinline__ void load8(const float* p, float* o) {
+  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+  o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+  o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
 }
 
 template <typename T>
@@ -50,6 +69,8 @@ __global__ void __launch_bounds__(AT) attn_partial_kernel(
   float* mrow = acc + R * d;
   float* lrow = mrow + R;
   float* fac = lrow + R;
+  // every region above has an even float count except m, l, fac (3R): pad to 8 bytes
+  long long* koff = reinterpret_cast<long long*>(fac + R + (R & 1));
 
   const int P = ctx_len[s] + (new_off[s + 1] - new_off[s]);
   const int L = P + B;
@@ -64,41 +85,64 @@ __global__ void __launch_bounds__(AT) attn_partial_kernel(
   }
   if (P > max_pages * page_size && sp == 0 && threadIdx.x == 0) flag(status, DFLASH2_DEV_BAD_LENGTH);
   const float scale = rsqrtf((float)d);
-  for (int idx = threadIdx.x; idx < R * d; idx += blockDim.x) {
-    const int r = idx / d, c = idx % d;
+  const int c8 = d / 8;  // 8-element chunks per row
+  for (int idx = threadIdx.x; idx < R * c8; idx += blockDim.x) {
+    const int r = idx / c8, c = (idx % c8) * 8;
     const int i = r / grp, h = g * grp + r % grp;
-    Qs[idx] = ld(&q[(((size_t)s * B + i) * nq + h) * d + c]) * scale;
-    acc[idx] = 0.f;
+    float v[8];
+    load8(q + (((size_t)s * B + i) * nq + h) * d + c, v);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      Qs[r * d + c + e] = v[e] * scale;
+      acc[r * d + c + e] = 0.f;
+    }
   }
   for (int r = threadIdx.x; r < R; r += blockDim.x) {
     mrow[r] = -INFINITY;
     lrow[r] = 0.f;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  // a key's row offset: into the paged cache, or (bit 62 set) into kb/vb
+  constexpr long long BLOCK_BIT = 1LL << 62;
   for (int t0 = k0; t0 < k1; t0 += KT) {
     const int nk = min(KT, k1 - t0);
     __syncthreads();
-    for (int idx = threadIdx.x; idx < nk * d; idx += blockDim.x) {
-      const int kk = idx / d, c = idx % d;
-      const int j = t0 + kk;
-      float kv = 0.f, vv = 0.f;
+    if (threadIdx.x < nk) {
+      const int j = t0 + threadIdx.x;
+      long long o = -1;
       if (j < P) {
         const int pi = j / page_size;
         const int page = pi < max_pages ? block_table[(size_t)s * max_pages + pi] : -1;
-        if (page >= 0 && page < n_pages) {
-          const size_t o = (((size_t)page * page_size + j % page_size) * nkv + g) * d + c;
-          kv = ld(&kc[o]);
-          vv = ld(&vc[o]);
-        } else if (c == 0) {
+        if (page >= 0 && page < n_pages)
+          o = (((long long)page * page_size + j % page_size) * nkv + g) * d;
+        else
           flag(status, DFLASH2_DEV_BAD_PAGE);
-        }
       } else {
-        const size_t o = (((size_t)s * B + (j - P)) * nkv + g) * d + c;
-        kv = ld(&kb[o]);
-        vv = ld(&vb[o]);
+        o = BLOCK_BIT | ((((long long)s * B + (j - P)) * nkv + g) * d);
       }
-      Ks[kk * (d + 1) + c] = kv;
-      Vs[kk * d + c] = vv;
+      koff[threadIdx.x] = o;
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < nk * c8; idx += blockDim.x) {
+      const int kk = idx / c8, c = (idx % c8) * 8;
+      const long long o = koff[kk];
+      float kv[8], vv[8];
+      if (o < 0) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) kv[e] = vv[e] = 0.f;
+      } else if (o & BLOCK_BIT) {
+        const long long oo = o & ~BLOCK_BIT;
+        load8(kb + oo + c, kv);
+        load8(vb + oo + c, vv);
+      } else {
+        load8(kc + o + c, kv);
+        load8(vc + o + c, vv);
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        Ks[kk * (d + 1) + c + e] = kv[e];
+        Vs[kk * d + c + e] = vv[e];
+      }
     }
     __syncthreads();
     for (int idx = threadIdx.x; idx < R * nk; idx += blockDim.x) {
@@ -232,7 +276,7 @@ int launch_attention(int dtype, const void* q, const void* kb, const void* vb, c
                                                                        static_cast<float*>(o_out));
   }
   count_launch(2);
-  return cudaPeekAtLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
 }
 
 }  // namespace df2

@@ -15,7 +15,7 @@ constexpr int TM = 64, TN = 32, TK = 16;
 
 __global__ void __launch_bounds__(256) simt_gemm_kernel(const float* __restrict__ W, int M, int K, int ldw,
                                                         const float* __restrict__ X, int N, int ldx,
-                                                        float* __restrict__ out) {
+                                                        float* __restrict__ out, int accumulate) {
   __shared__ float Ws[TK][TM + 1];
   __shared__ float Xs[TK][TN + 1];
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -47,7 +47,10 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const float* __restrict_
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int m = m0 + tx + 16 * i, n = n0 + ty + 16 * j;
-      if (m < M && n < N) out[(size_t)n * M + m] = acc[i][j];
+      if (m < M && n < N) {
+        float* p = out + (size_t)n * M + m;
+        *p = accumulate ? *p + acc[i][j] : acc[i][j];
+      }
     }
 }
 
@@ -57,9 +60,10 @@ int gemm_f32(const GemmOp& g, const Ctx& c) {
   if (g.M <= 0 || g.N <= 0 || g.K <= 0) return DFLASH2_ERR_SHAPE;
   dim3 grid((g.M + TM - 1) / TM, (g.N + TN - 1) / TN);
   simt_gemm_kernel<<<grid, 256, 0, c.stream>>>(static_cast<const float*>(g.W), g.M, g.K, g.ldw,
-                                                static_cast<const float*>(g.X), g.N, g.ldx, g.out);
+                                                static_cast<const float*>(g.X), g.N, g.ldx, g.out,
+                                                g.accumulate ? 1 : 0);
   count_launch();
-  return cudaPeekAtLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
 }
 
 }  // namespace df2

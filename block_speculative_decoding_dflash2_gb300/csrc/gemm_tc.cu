@@ -47,7 +47,10 @@ constexpr int THREADS = 192;
 struct TcArgs {
   int M, N, K;
   int n_chunks, splits, m_tiles, n_tiles, units;
-  float* out;
+  float* out;       // final [N][M] fp32 (stored, or added to when accumulate)
+  float* partial;   // [splits][N][M] fp32 when splits > 1
+  int* counters;    // [n_tiles * m_tiles] arrival counters, zero between launches
+  int accumulate;
   float* lists_v;
   int* lists_i;
   float* debug;
@@ -114,6 +117,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = abort_flag + 1;
   float* stg = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 1024);  // [16][BM]
   float* lv_s = stg + 16 * BM;                                                       // [BN][KMAX]
   int* li_s = reinterpret_cast<int*>(lv_s + BN * KMAX);                              // [BN][KMAX]
@@ -271,15 +275,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int mt = t % a.m_tiles, nt = t / a.m_tiles;
       const bool got = mbar_wait(tfull + acc, acc_phase, abort_flag, WAIT_NS);
       if (!got) fail();
-      if constexpr (TOPK) {
-        if (named_sync_or(!got || *abort_flag)) break;
-      } else {
-        if (!got) break;
-      }
+      if (named_sync_or(!got || *abort_flag)) break;
       tc_fence_after();
       const int m = mt * BM + row;
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       if constexpr (!TOPK) {
+        // one K split: the tile is final.  Several: write this split's
+        // partial; the last split to arrive at the tile (arrival counter)
+        // sums all partials in split order and writes the final tile, so
+        // the result is deterministic and no CTA ever waits for another.
+        const bool direct = a.splits == 1;
+        float* dst = direct ? a.out : a.partial + (size_t)sp * a.N * a.M;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 16) {
           float v[16];
@@ -288,12 +294,37 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int n = nt * BN + c0 + j;
-              if (n < a.N) a.out[((size_t)sp * a.N + n) * a.M + m] = v[j];
+              if (n < a.N) {
+                float* p = dst + (size_t)n * a.M + m;
+                if (direct && a.accumulate) *p += v[j];
+                else *p = v[j];
+              }
             }
           }
         }
         tc_fence_before();
         mbar_arrive(tempty + acc);
+        if (!direct) {
+          const int tidx = nt * a.m_tiles + mt;
+          __threadfence();
+          named_sync_epi();
+          if (threadIdx.x == 64) *last_flag = (atomicAdd(a.counters + tidx, 1) == a.splits - 1) ? 1 : 0;
+          named_sync_epi();
+          if (*last_flag) {
+            __threadfence();
+            if (m < a.M) {
+              const int n1 = min(a.N, (nt + 1) * BN);
+              for (int n = nt * BN; n < n1; ++n) {
+                float s = 0.f;
+                for (int s2 = 0; s2 < a.splits; ++s2) s += __ldcg(a.partial + ((size_t)s2 * a.N + n) * a.M + m);
+                float* p = a.out + (size_t)n * a.M + m;
+                if (a.accumulate) *p += s;
+                else *p = s;
+              }
+            }
+            if (threadIdx.x == 64) a.counters[tidx] = 0;
+          }
+        }
       } else {
         if (nt != cur_nt) {
           named_sync_epi();
@@ -412,8 +443,12 @@ int make_map(CUtensorMap* map, const void* base, int rows, int cols, int ld, int
   return r == CUDA_SUCCESS ? DFLASH2_OK : DFLASH2_ERR_CUDA;
 }
 
-int pick_bn(int N) {
+// Activation rows per tile.  With very few weight tiles (M <= 512) the rows
+// are spread over 16-row tiles so the grid still fills the SMs; otherwise the
+// smallest MMA width that holds all rows (at most 256).
+int pick_bn(int M, int N) {
   if (N <= 16) return 16;
+  if ((M + BM - 1) / BM <= 4 && N <= 256) return 16;
   if (N <= 32) return 32;
   if (N <= 64) return 64;
   if (N <= 128) return 128;
@@ -432,35 +467,35 @@ int launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs& args, 
   }
   tc_gemm_kernel<BN, TOPK><<<grid, THREADS, smem, st>>>(ma, mb, args);
   count_launch();
-  return cudaPeekAtLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
 }
 
 }  // namespace
 
+// K splits: about one wave of units over the SMs, but at least 8 K chunks per
+// unit (so a unit's epilogue -- partial store, fence, arrival count -- hides
+// behind the next unit's stream) and fp32 partials (s*N*M*4 bytes) below half
+// the weight bytes (M*K*2).
 int gemm_splits(int M, int N, int K, int nsm, bool topk) {
   if (topk || N > 256) return 1;  // many activation rows: enough tiles without splitting K
-  const int bn = pick_bn(N);
-  const long base = (long)((M + BM - 1) / BM) * ((N + bn - 1) / bn);
+  const long base = gemm_tiles(M, N);
   const int chunks = (K + BK - 1) / BK;
-  if (base >= nsm) return 1;
-  const int smax = std::min(64, chunks);
-  long best = LONG_MAX;
-  int bs = 1;
-  for (int s = 1; s <= smax; ++s) {
-    const long waves = (base * s + nsm - 1) / nsm;
-    const long cost = waves * ((chunks + s - 1) / s);
-    if (cost < best) {
-      best = cost;
-      bs = s;
-    }
-  }
-  return bs;
+  if (2 * base >= nsm) return 1;
+  long s = nsm / base;
+  s = std::min<long>(s, chunks / 8);
+  s = std::min<long>(s, K / (4 * N));
+  return (int)std::max<long>(1, std::min<long>(s, 64));
+}
+
+int gemm_tiles(int M, int N) {
+  const int bn = pick_bn(M, N);
+  return ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
 }
 
 int gemm_topk_lists(int M, int N, int K, int nsm, int dtype) {
   (void)K;
   if (dtype == DFLASH2_BF16) {
-    const int bn = pick_bn(N);
+    const int bn = pick_bn(M, N);
     const long units = (long)((M + BM - 1) / BM) * ((N + bn - 1) / bn);
     return (int)std::min<long>(units, nsm);
   }
@@ -471,7 +506,7 @@ int gemm_max_lists() { return std::max(kMaxSM, 0); }
 
 int gemm_bf16(const GemmOp& g, const Ctx& c) {
   if (g.M <= 0 || g.N <= 0 || g.K <= 0) return DFLASH2_ERR_SHAPE;
-  const int bn = pick_bn(g.N);
+  const int bn = pick_bn(g.M, g.N);
   TcArgs a;
   a.M = g.M;
   a.N = g.N;
@@ -482,6 +517,10 @@ int gemm_bf16(const GemmOp& g, const Ctx& c) {
   a.splits = g.topk ? 1 : std::max(1, std::min(g.splits, a.n_chunks));
   a.units = a.m_tiles * a.n_tiles * a.splits;
   a.out = g.out;
+  a.partial = g.partial;
+  a.counters = g.counters;
+  a.accumulate = g.accumulate ? 1 : 0;
+  if (!g.topk && a.splits > 1 && (!g.partial || !g.counters)) return DFLASH2_ERR_INVALID_ARG;
   a.lists_v = g.lists_v;
   a.lists_i = g.lists_i;
   a.debug = g.debug;

@@ -22,9 +22,15 @@ struct GemmOp {
   int M, K, ldw;
   const void* X;  // [N, K] row stride ldx elements
   int N, ldx;
-  // partial epilogue: out[s][n][m] fp32, s < splits
+  // plain epilogue: out[n][m] fp32 (ld = M), stored or, with accumulate,
+  // added to.  With splits > 1 each split writes partial[s][n][m] and the
+  // last split to finish a tile (counters[tile], zero on entry and on exit)
+  // reduces the tile in split order.
   float* out;
   int splits;
+  float* partial;
+  int* counters;
+  bool accumulate;
   // top-k epilogue (lm_head): per-CTA sorted lists of KMAX entries
   bool topk;
   float* lists_v;  // [n_lists][N][KMAX]
@@ -44,26 +50,33 @@ constexpr int kMaxSM = 256;
 // Host-side count of kernel launches (instrumentation).
 void count_launch(int n = 1);
 
+// Byte offsets in the workspace of the draft step's intermediates
+// {f, h, u, u2, q, kb, vb, O, act, hn} for a call of these sizes (test hook).
+int workspace_offsets(const dflash2_config* c, int batch, int n_new, int max_ctx, size_t* out, int n);
+
 int gemm_bf16(const GemmOp& g, const Ctx& c);  // tcgen05 + TMA (sm_103a)
 int gemm_f32(const GemmOp& g, const Ctx& c);   // exact fp32 FMA, SIMT
 
-// element-wise / row kernels (elementwise.cu); T = float or bf16 by dtype
-int launch_rows_feature_norm(int dtype, const float* P, int S, int rows, int H, const void* gamma, float eps,
-                             void* f_out, const Ctx& c);
-int launch_kv_append(int dtype, const float* P, int S, int rows, int nkv, int d, const void* k_norm, float eps,
-                     float theta, const int32_t* ctx_len, const int32_t* new_off, int batch,
-                     const int32_t* block_table, int max_pages, int page_size, int n_pages, void* kc, void* vc,
-                     const Ctx& c);
-int launch_embed_block(int dtype, const int32_t* anchor, int mask_id, int batch, int B, const void* embed, int V,
-                       int H, float scale, float* h_out, const Ctx& c);
-int launch_residual_norm(int dtype, float* h, const float* P, int S, int rows, int H, const void* gamma, float eps,
-                         void* u_out, int B, int skip_anchor, const Ctx& c);
-int launch_dyn_conv(int dtype, const void* u, const float* P, int S, int rows, int H, int group_size, int B,
-                    void* u2_out, const Ctx& c);
-int launch_qkv_epilogue(int dtype, const float* P, int S, int rows, int B, int nq, int nkv, int d,
-                        const void* q_norm, const void* k_norm, float eps, float theta, const int32_t* ctx_len,
-                        const int32_t* new_off, void* q, void* kb, void* vb, const Ctx& c);
-int launch_act(int dtype, const float* P, int S, int rows, int I, void* act, const Ctx& c);
+// Tiles (m_tiles * n_tiles) of a contraction, the size of its counter array.
+int gemm_tiles(int M, int N);
+
+// element-wise / row kernels (elementwise.cu); T = float or bf16 by dtype.
+// Y is the producing contraction's final fp32 output, row-major [rows][width].
+int launch_rows_feature_norm(int dtype, const float* Y, int rows, int H, const void* gamma, float eps, void* f_out,
+                             const Ctx& c);
+int launch_kv_append(int dtype, const float* Y, int rows, int nkv, int d, const void* k_norm, float eps, float theta,
+                     const int32_t* ctx_len, const int32_t* new_off, int batch, const int32_t* block_table,
+                     int max_pages, int page_size, int n_pages, void* kc, void* vc, const Ctx& c);
+int launch_embed_norm(int dtype, const int32_t* anchor, int mask_id, int batch, int B, const void* embed, int V, int H,
+                      float scale, const void* gamma, float eps, float* h_out, void* u_out, const Ctx& c);
+int launch_rownorm(int dtype, const float* h, int rows, int H, const void* gamma, float eps, void* u_out, int B,
+                   int skip_anchor, const Ctx& c);
+int launch_dyn_conv(int dtype, const void* u, const float* Y, int rows, int H, int group_size, int B, void* u2_out,
+                    const Ctx& c);
+int launch_qkv_epilogue(int dtype, const float* Y, int rows, int B, int nq, int nkv, int d, const void* q_norm,
+                        const void* k_norm, float eps, float theta, const int32_t* ctx_len, const int32_t* new_off,
+                        void* q, void* kb, void* vb, const Ctx& c);
+int launch_act(int dtype, const float* Y, int rows, int I, void* act, const Ctx& c);
 
 // attention (attention.cu)
 int launch_attention(int dtype, const void* q, const void* kb, const void* vb, const void* kc, const void* vc,
@@ -82,8 +95,8 @@ int launch_topk_merge(const float* lists_v, const int* lists_i, int n_lists, int
 // selector and verify (selector.cu, verify.cu)
 int launch_sel_gather(int dtype, const int32_t* anchor, const int32_t* cand_id, int batch, int D, int k,
                       const void* embed, int V, int H, void* x_out, const Ctx& c);
-int launch_viterbi(const float* P, int S, const int32_t* anchor, const int32_t* cand_id, const float* cand_logit,
-                   int batch, int D, int k, int r, int32_t* path, float* path_score, const Ctx& c);
+int launch_viterbi(const float* Y, const int32_t* cand_id, const float* cand_logit, int batch, int D, int k, int r,
+                   int32_t* path, float* path_score, const Ctx& c);
 size_t viterbi_smem_bytes(int D, int k, int r);
 int launch_verify(int batch, int B, const int32_t* path, const int32_t* target, int32_t* accept_len,
                   int32_t* out_tok, int32_t* n_out, int32_t* next_anchor, int32_t* seq_len, int64_t* counters,

@@ -14,7 +14,7 @@
 //
 // sel_gather_kernel lays out E rows of [anchor, all candidates] so the factor
 // contraction runs on the same GEMM as the rest of the step; viterbi_kernel
-// (one CTA per sequence) reduces the factor partials into shared memory and
+// (one CTA per sequence) stages that sequence's factors in shared memory and
 // runs the k x k dynamic programme over the B-1 positions.
 #include <climits>
 
@@ -41,45 +41,55 @@ __global__ void __launch_bounds__(256) sel_gather_kernel(const int32_t* __restri
   for (int m = threadIdx.x; m < H; m += blockDim.x) x[(size_t)r * H + m] = tok < 0 ? T(0.f) : E[(size_t)tok * H + m];
 }
 
-__global__ void __launch_bounds__(256) viterbi_kernel(const float* __restrict__ P, int S, int batch,
+__global__ void __launch_bounds__(256) viterbi_kernel(const float* __restrict__ Y, int batch,
                                                       const int32_t* __restrict__ cand_id,
                                                       const float* __restrict__ cand_logit, int D, int k, int r,
                                                       int32_t* __restrict__ path, float* __restrict__ path_score) {
   extern __shared__ float sm[];
   const int s = blockIdx.x;
-  const int nt = D * k + 1, w = 2 * r;
-  float* F = sm;                     // [nt][2r] factors: A = F[t][0:r], Bf = F[t][r:2r]
-  float* Sm = F + (size_t)nt * w;    // [k][k] scores / totals
+  const int nt = D * k + 1, w = 2 * r, ws = w + 1;  // padded row stride: no bank conflicts across candidates
+  float* F = sm;                     // [nt][ws] factors: A = F[t][0:r], Bf = F[t][r:2r]
+  float* Sm = F + (size_t)nt * ws;   // [k][k] scores / totals
   float* delta = Sm + k * k;         // [k]
   float* nd = delta + k;             // [k]
   int* bp = reinterpret_cast<int*>(nd + k);  // [D][k]
+  (void)batch;
 
-  const size_t stride = (size_t)batch * nt * w;
-  for (int idx = threadIdx.x; idx < nt * w; idx += blockDim.x) {
-    float a = 0.f;
-    for (int sp = 0; sp < S; ++sp) a += P[sp * stride + (size_t)s * nt * w + idx];
-    F[idx] = a;
-  }
+  const float* y = Y + (size_t)s * nt * w;
+  for (int idx = threadIdx.x; idx < nt * w; idx += blockDim.x) F[(idx / w) * ws + idx % w] = y[idx];
   __syncthreads();
   const float* z = cand_logit + (size_t)s * D * k;
   auto dot = [&](int ta, int tb) {  // <A[ta], Bf[tb]>
-    const float* a = F + (size_t)ta * w;
-    const float* b = F + (size_t)tb * w + r;
+    const float* a = F + (size_t)ta * ws;
+    const float* b = F + (size_t)tb * ws + r;
     float acc = 0.f;
     for (int c = 0; c < r; ++c) acc = fmaf(a[c], b[c], acc);
     return acc;
   };
+  // normalise each row p of Sm[p][0..k) into log-probabilities and add delta[p]
+  // (add_delta = false for the first position): one half-warp per row, lane
+  // j of the half holds column j (k <= 16), shuffle reductions stay in the half
+  auto row_logsoftmax = [&](int rows_, bool add_delta) {
+    const int hw = threadIdx.x >> 4, j = threadIdx.x & 15, nhw = blockDim.x >> 4;
+    const unsigned hmask = (threadIdx.x & 16) ? 0xffff0000u : 0x0000ffffu;
+    for (int p = hw; p < rows_; p += nhw) {
+      const float x = j < k ? Sm[p * k + j] : -INFINITY;
+      float m = x;
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(hmask, m, o));
+      float sum = j < k ? expf(x - m) : 0.f;
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(hmask, sum, o);
+      const float lse = m + logf(sum);
+      if (j < k) Sm[p * k + j] = (add_delta ? delta[p] : 0.f) + (x - lse);
+    }
+  };
   // position 1: the predecessor is the anchor (factor row 0)
   for (int j = threadIdx.x; j < k; j += blockDim.x) Sm[j] = z[j] + dot(0, 1 + j);
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float m = -INFINITY;
-    for (int j = 0; j < k; ++j) m = fmaxf(m, Sm[j]);
-    float sum = 0.f;
-    for (int j = 0; j < k; ++j) sum += expf(Sm[j] - m);
-    const float lse = m + logf(sum);
-    for (int j = 0; j < k; ++j) delta[j] = Sm[j] - lse;
-  }
+  row_logsoftmax(1, false);
+  __syncthreads();
+  for (int j = threadIdx.x; j < k; j += blockDim.x) delta[j] = Sm[j];
   __syncthreads();
   for (int i = 1; i < D; ++i) {
     for (int pr = threadIdx.x; pr < k * k; pr += blockDim.x) {
@@ -87,14 +97,7 @@ __global__ void __launch_bounds__(256) viterbi_kernel(const float* __restrict__ 
       Sm[pr] = z[i * k + j] + dot(1 + (i - 1) * k + p, 1 + i * k + j);
     }
     __syncthreads();
-    for (int p = threadIdx.x; p < k; p += blockDim.x) {
-      float m = -INFINITY;
-      for (int j = 0; j < k; ++j) m = fmaxf(m, Sm[p * k + j]);
-      float sum = 0.f;
-      for (int j = 0; j < k; ++j) sum += expf(Sm[p * k + j] - m);
-      const float lse = m + logf(sum);
-      for (int j = 0; j < k; ++j) Sm[p * k + j] = delta[p] + (Sm[p * k + j] - lse);
-    }
+    row_logsoftmax(k, true);
     __syncthreads();
     for (int j = threadIdx.x; j < k; j += blockDim.x) {
       float best = Sm[j];
@@ -126,7 +129,8 @@ __global__ void __launch_bounds__(256) viterbi_kernel(const float* __restrict__ 
 }  // namespace
 
 size_t viterbi_smem_bytes(int D, int k, int r) {
-  return sizeof(float) * ((size_t)(D * k + 1) * 2 * r + (size_t)k * k + 2 * (size_t)k) + sizeof(int) * (size_t)D * k;
+  return sizeof(float) * ((size_t)(D * k + 1) * (2 * r + 1) + (size_t)k * k + 2 * (size_t)k) +
+         sizeof(int) * (size_t)D * k;
 }
 
 int launch_sel_gather(int dtype, const int32_t* anchor, const int32_t* cand_id, int batch, int D, int k,
@@ -139,12 +143,11 @@ int launch_sel_gather(int dtype, const int32_t* anchor, const int32_t* cand_id, 
     sel_gather_kernel<float><<<rows, 256, 0, c.stream>>>(anchor, cand_id, D, k, static_cast<const float*>(embed), V,
                                                           H, static_cast<float*>(x_out), c.status);
   count_launch();
-  return cudaPeekAtLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
 }
 
-int launch_viterbi(const float* P, int S, const int32_t* anchor, const int32_t* cand_id, const float* cand_logit,
-                   int batch, int D, int k, int r, int32_t* path, float* path_score, const Ctx& c) {
-  (void)anchor;  // the anchor's factors are row 0 of P
+int launch_viterbi(const float* Y, const int32_t* cand_id, const float* cand_logit, int batch, int D, int k, int r,
+                   int32_t* path, float* path_score, const Ctx& c) {
   const size_t smem = viterbi_smem_bytes(D, k, r);
   static bool attr = false;
   if (!attr) {
@@ -152,9 +155,9 @@ int launch_viterbi(const float* P, int S, const int32_t* anchor, const int32_t* 
       return DFLASH2_ERR_CUDA;
     attr = true;
   }
-  viterbi_kernel<<<batch, 256, smem, c.stream>>>(P, S, batch, cand_id, cand_logit, D, k, r, path, path_score);
+  viterbi_kernel<<<batch, 256, smem, c.stream>>>(Y, batch, cand_id, cand_logit, D, k, r, path, path_score);
   count_launch();
-  return cudaPeekAtLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
 }
 
 }  // namespace df2

@@ -33,10 +33,16 @@ using namespace df2;
 
 extern "C" {
 
-int dflash2_test_gemm(int dtype, const void* W, int M, int K, const void* X, int N, int splits, float* partial,
-                      size_t out_bytes, void* stream) {
+size_t dflash2_test_gemm_workspace(int M, int N, int splits) {
+  if (M <= 0 || N <= 0) return 0;
+  const int s = std::max(1, std::min(64, splits > 0 ? splits : 64));
+  return al((size_t)gemm_tiles(M, N) * sizeof(int)) + al((size_t)s * N * M * sizeof(float));
+}
+
+int dflash2_test_gemm(int dtype, const void* W, int M, int K, const void* X, int N, int splits, int accumulate,
+                      float* out, void* workspace, size_t ws_bytes, void* stream) {
   if (dtype != DFLASH2_BF16 && dtype != DFLASH2_F32) return DFLASH2_ERR_DTYPE;
-  if (!W || !X || !partial) return DFLASH2_ERR_INVALID_ARG;
+  if (!W || !X || !out || !workspace) return DFLASH2_ERR_INVALID_ARG;
   if (M <= 0 || N <= 0 || K <= 0) return DFLASH2_ERR_SHAPE;
   Ctx c;
   const int rc = test_ctx(&c, stream, nullptr);
@@ -50,7 +56,8 @@ int dflash2_test_gemm(int dtype, const void* W, int M, int K, const void* X, int
   g.X = X;
   g.N = N;
   g.ldx = K;
-  g.out = partial;
+  g.out = out;
+  g.accumulate = accumulate != 0;
   g.mult = 1.f;
   if (dtype == DFLASH2_F32) {
     g.splits = 1;
@@ -58,9 +65,17 @@ int dflash2_test_gemm(int dtype, const void* W, int M, int K, const void* X, int
     const int chunks = (K + 63) / 64;
     g.splits = splits > 0 ? std::min(std::min(splits, 64), chunks) : gemm_splits(M, N, K, c.nsm, false);
   }
-  if ((size_t)g.splits * N * M * sizeof(float) > out_bytes) return DFLASH2_ERR_WORKSPACE;
+  char* base = static_cast<char*>(workspace);
+  g.counters = reinterpret_cast<int*>(base);
+  g.partial = reinterpret_cast<float*>(base + al((size_t)gemm_tiles(M, N) * sizeof(int)));
+  if (al((size_t)gemm_tiles(M, N) * sizeof(int)) + (size_t)g.splits * N * M * sizeof(float) > ws_bytes)
+    return DFLASH2_ERR_WORKSPACE;
   const int r = dtype == DFLASH2_BF16 ? gemm_bf16(g, c) : gemm_f32(g, c);
   return r ? r : g.splits;
+}
+
+int dflash2_test_layout(const dflash2_config* cfg, int batch, int n_new, int max_ctx, size_t* offsets, int n) {
+  return workspace_offsets(cfg, batch, n_new, max_ctx, offsets, n);
 }
 
 size_t dflash2_test_topk_workspace(int dtype, int M, int N) {

@@ -5,10 +5,10 @@
 //
 // The lm_head GEMM (tcgen05 path) already leaves one sorted list of KMAX
 // entries per CTA and row.  topk_scan_kernel produces the same lists from
-// stored logits (fp32 path).  topk_merge_kernel reduces the lists of a row:
-// only entries at least as good as the best of the lists' last entries can
-// be in the global top-KMAX, so it gathers those (typically a few dozen)
-// and ranks them exactly.
+// stored logits (fp32 path).  topk_merge_kernel reduces the lists of a row
+// with a tree of two-list merges in shared memory; each merge ranks every
+// entry of both lists against the other in one warp, so the result does not
+// depend on how the vocabulary was split.
 #include <algorithm>
 #include <climits>
 
@@ -18,8 +18,6 @@
 namespace df2 {
 
 namespace {
-
-constexpr int MAXC = 256 * KMAX;  // candidate slots of the merge (n_lists <= 256)
 
 int scan_chunks(int V) { return std::max(1, std::min(64, (V + 1023) / 1024)); }
 
@@ -56,78 +54,62 @@ __global__ void __launch_bounds__(128) topk_scan_kernel(const float* __restrict_
   }
 }
 
+// Merges sorted lists a (lanes 0..15 hold a[lane]) and b (lanes 16..31 hold
+// b[lane-16]) into the best KMAX, written to out_v/out_i[0..KMAX).  An entry's
+// rank in the union is its index in its own list plus the number of entries
+// of the other list that beat it (the order is strict: ids are distinct).
+__device__ __forceinline__ void warp_merge2(float v, int id, float* out_v, int* out_i) {
+  const int lane = threadIdx.x & 31;
+  const int other = lane < KMAX ? KMAX : 0;
+  int rank = lane & (KMAX - 1);
+#pragma unroll
+  for (int t = 0; t < KMAX; ++t) {
+    const float ov = __shfl_sync(0xffffffffu, v, other + t);
+    const int oi = __shfl_sync(0xffffffffu, id, other + t);
+    rank += beats(ov, oi, v, id) ? 1 : 0;
+  }
+  __syncwarp();
+  if (rank < KMAX) {
+    out_v[rank] = v;
+    out_i[rank] = id;
+  }
+  __syncwarp();
+}
+
+// One CTA per row.  The row's n_lists lists are staged in shared memory and
+// merged pairwise, level by level (list 2j absorbs list 2j+1), one warp per
+// pair.  dynamic shared memory: n_lists * KMAX * 8 bytes.
 __global__ void __launch_bounds__(256) topk_merge_kernel(const float* __restrict__ lists_v,
                                                          const int* __restrict__ lists_i, int n_lists, int rows,
                                                          int k, int32_t* __restrict__ cand_id,
                                                          float* __restrict__ cand_logit) {
-  __shared__ float cv[MAXC];
-  __shared__ int ci[MAXC];
-  __shared__ float rv[32];
-  __shared__ int ri[32];
-  __shared__ int cnt;
+  extern __shared__ float mv[];
+  int* mi = reinterpret_cast<int*>(mv + n_lists * KMAX);
   const int row = blockIdx.x;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  // threshold = best of the lists' last entries
-  float bv = -INFINITY;
-  int bi = INT_MAX;
-  for (int l = threadIdx.x; l < n_lists; l += blockDim.x) {
-    const size_t o = ((size_t)l * rows + row) * KMAX + (KMAX - 1);
-    const float v = lists_v[o];
-    const int i = lists_i[o];
-    if (beats(v, i, bv, bi)) {
-      bv = v;
-      bi = i;
-    }
-  }
-  for (int o = 16; o > 0; o >>= 1) {
-    const float v = __shfl_xor_sync(0xffffffffu, bv, o);
-    const int i = __shfl_xor_sync(0xffffffffu, bi, o);
-    if (beats(v, i, bv, bi)) {
-      bv = v;
-      bi = i;
-    }
-  }
-  if (lane == 0) {
-    rv[warp] = bv;
-    ri[warp] = bi;
-  }
-  if (threadIdx.x == 0) cnt = 0;
-  __syncthreads();
-  float tv = rv[0];
-  int ti = ri[0];
-  for (int w = 1; w < (int)(blockDim.x >> 5); ++w)
-    if (beats(rv[w], ri[w], tv, ti)) {
-      tv = rv[w];
-      ti = ri[w];
-    }
-  // gather every real entry that is not beaten by the threshold
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   for (int idx = threadIdx.x; idx < n_lists * KMAX; idx += blockDim.x) {
     const int l = idx / KMAX, e = idx % KMAX;
     const size_t o = ((size_t)l * rows + row) * KMAX + e;
-    const float v = lists_v[o];
-    const int i = lists_i[o];
-    if (i != INT_MAX && !beats(tv, ti, v, i)) {
-      const int p = atomicAdd(&cnt, 1);
-      if (p < MAXC) {
-        cv[p] = v;
-        ci[p] = i;
-      }
-    }
+    mv[idx] = lists_v[o];
+    mi[idx] = lists_i[o];
   }
   __syncthreads();
-  const int C = min(cnt, MAXC);
-  for (int e = threadIdx.x; e < k; e += blockDim.x) {  // slots no candidate reaches stay empty
-    cand_id[(size_t)row * k + e] = -1;
-    cand_logit[(size_t)row * k + e] = -INFINITY;
-  }
-  __syncthreads();
-  for (int a = threadIdx.x; a < C; a += blockDim.x) {
-    int rank = 0;
-    for (int b = 0; b < C; ++b) rank += beats(cv[b], ci[b], cv[a], ci[a]) ? 1 : 0;
-    if (rank < k) {
-      cand_id[(size_t)row * k + rank] = ci[a];
-      cand_logit[(size_t)row * k + rank] = cv[a];
+  for (int stride = 1; stride < n_lists; stride *= 2) {
+    for (int a = warp * 2 * stride; a < n_lists; a += nw * 2 * stride) {
+      const int b = a + stride;
+      if (b >= n_lists) continue;  // odd list out: carried to the next level as is
+      const int src = lane < KMAX ? a : b;
+      const float v = mv[src * KMAX + (lane & (KMAX - 1))];
+      const int id = mi[src * KMAX + (lane & (KMAX - 1))];
+      __syncwarp();
+      warp_merge2(v, id, mv + a * KMAX, mi + a * KMAX);
     }
+    __syncthreads();
+  }
+  for (int e = threadIdx.x; e < k; e += blockDim.x) {
+    const int id = mi[e];
+    cand_id[(size_t)row * k + e] = id == INT_MAX ? -1 : id;
+    cand_logit[(size_t)row * k + e] = mv[e];
   }
 }
 
@@ -143,15 +125,16 @@ int launch_topk_scan(const float* logits, int rows, int V, float mult, float cap
   topk_scan_kernel<<<grid, 128, 0, c.stream>>>(logits, rows, V, len, mult, cap, debug, lists_v, lists_i);
   *n_lists = chunks * 4;
   count_launch();
-  return cudaPeekAtLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
 }
 
 int launch_topk_merge(const float* lists_v, const int* lists_i, int n_lists, int rows, int k, int32_t* cand_id,
                       float* cand_logit, const Ctx& c) {
-  if (n_lists > 256 || k > KMAX) return DFLASH2_ERR_SHAPE;
-  topk_merge_kernel<<<rows, 256, 0, c.stream>>>(lists_v, lists_i, n_lists, rows, k, cand_id, cand_logit);
+  if (n_lists < 1 || n_lists > 256 || k > KMAX) return DFLASH2_ERR_SHAPE;
+  const size_t smem = (size_t)n_lists * KMAX * 8;  // <= 32 KB
+  topk_merge_kernel<<<rows, 256, smem, c.stream>>>(lists_v, lists_i, n_lists, rows, k, cand_id, cand_logit);
   count_launch();
-  return cudaPeekAtLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
 }
 
 }  // namespace df2

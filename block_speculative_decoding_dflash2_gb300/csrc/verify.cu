@@ -52,7 +52,7 @@ int launch_verify(int batch, int B, const int32_t* path, const int32_t* target, 
   verify_kernel<<<(batch + threads - 1) / threads, threads, 0, st>>>(batch, B, path, target, accept_len, out_tok,
                                                                      n_out, next_anchor, seq_len, counters);
   count_launch();
-  return cudaPeekAtLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
 }
 
 }  // namespace df2

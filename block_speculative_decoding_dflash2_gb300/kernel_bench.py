@@ -1,0 +1,61 @@
+"""Runs one hot kernel of the library a few times on a fixed shape, for
+profiler captures (ncu) and quick timing.
+
+  python -m block_speculative_decoding_dflash2_gb300.kernel_bench --kernel lm_head [--launches 3]
+
+Kernels:
+  lm_head   the lm_head contraction with its fused streaming top-k
+            (vocab 151936 x hidden 4096 bf16, 7 block rows, top-16) through
+            the dflash2_test_gemm_topk hook, then the top-k merge;
+  gate_up   the MLP gate/up contraction (24576 x 4096, 8 rows);
+  fc        the feature projection (4096 x 12288, 8 rows, split-K).
+Weights are seeded N(0, 0.02) bf16 drawn on the device (timing only; no
+parity is checked here).  Prints the mean CUDA-event time per launch.
+"""
+
+import argparse
+
+import torch
+
+from . import binding as B
+from .build import build
+
+SHAPES = {"lm_head": (151936, 4096, 7), "gate_up": (24576, 4096, 8), "fc": (4096, 12288, 8),
+          "qkv": (6144, 4096, 8), "down": (4096, 12288, 8), "o": (4096, 4096, 8)}
+
+
+def main():
+    p = argparse.ArgumentParser()
+    p.add_argument("--kernel", default="lm_head", choices=sorted(SHAPES))
+    p.add_argument("--launches", type=int, default=3)
+    a = p.parse_args()
+    build()
+    M, K, N = SHAPES[a.kernel]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1234)
+    W = (torch.randn((M, K), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    X = torch.randn((N, K), generator=g, device="cuda").to(torch.bfloat16)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if a.kernel == "lm_head":
+        ws = torch.zeros(B.dflash2_test_topk_workspace(B.BF16, M, N), dtype=torch.uint8, device="cuda")
+        cid = torch.empty((N, 16), dtype=torch.int32, device="cuda")
+        cz = torch.empty((N, 16), dtype=torch.float32, device="cuda")
+        run = lambda: B.dflash2_test_gemm_topk(B.BF16, W, X, 16, 1.0, 0.0, cid, cz, None, ws)
+    else:
+        out = torch.empty((N, M), dtype=torch.float32, device="cuda")
+        ws = torch.zeros(B.dflash2_test_gemm_workspace(M, N, 0), dtype=torch.uint8, device="cuda")
+        run = lambda: B.dflash2_test_gemm(B.BF16, W, X, 0, out, ws)
+    run()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(a.launches):
+        run()
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / a.launches
+    gb = M * K * 2 / 1e9
+    print(f"{a.kernel}: M={M} K={K} N={N}: {ms * 1e3:.1f} us per call, {gb / (ms / 1e3):.0f} GB/s of weights")
+
+
+if __name__ == "__main__":
+    main()

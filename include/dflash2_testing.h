@@ -12,22 +12,45 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "dflash2.h"
+
 #ifdef __cplusplus
 extern "C" {
 #endif
 
 /*
- * partial[s][n][m] = sum over the s-th K range of W[m][k] * X[n][k]
- * (the split-K partials whose sum over s is W X^T, stored transposed).
+ * out[n][m] = sum_k W[m][k] * X[n][k]   (or out[n][m] += ... with accumulate),
+ * through the library's contraction: W X^T stored transposed, fp32.
  *   dtype      DFLASH2_BF16 (tcgen05 path) or DFLASH2_F32 (SIMT path, 1 split)
  *   W          [M, K], X [N, K], row-major, element type = dtype
- *   splits     K splits to use (bf16: 1..64, clamped to ceil(K/64); <= 0 picks
- *              the library's own choice); f32 always uses 1
- *   partial    float [splits_used][N][M]; out_bytes its capacity in bytes
+ *   splits     K splits (bf16: 1..64, clamped to ceil(K/64); <= 0 picks the
+ *              library's own choice); with several splits the last split to
+ *              finish each tile reduces the partials in split order
+ *   out        float [N][M]
+ *   workspace  zeroed on first use, at least dflash2_test_gemm_workspace bytes
  * Returns the number of splits used (>= 1) or a negative status.
  */
-int dflash2_test_gemm(int dtype, const void *W, int M, int K, const void *X, int N, int splits,
-                      float *partial, size_t out_bytes, void *stream);
+size_t dflash2_test_gemm_workspace(int M, int N, int splits);
+int dflash2_test_gemm(int dtype, const void *W, int M, int K, const void *X, int N, int splits, int accumulate,
+                      float *out, void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Byte offsets, inside the workspace of a dflash2_draft_step call with these
+ * sizes (max_ctx = max_pages * page_size), of the intermediates that call
+ * leaves behind, in this order:
+ *   [0] f    [n_new, H]        projected features of the appended rows
+ *   [1] h    [batch*B, H] fp32 residual stream after the last layer
+ *   [2] u    [batch*B, H]      normed input of the last MLP sublayer
+ *   [3] u2   [batch*B, H]      that input after the dynamic convolution
+ *   [4] q    [batch*B, nq, d]  block queries of the last layer (normed, rotated)
+ *   [5] kb   [batch*B, nkv, d] block keys of the last layer (normed, rotated)
+ *   [6] vb   [batch*B, nkv, d] block values of the last layer
+ *   [7] O    [batch*B, nq*d]   attention output of the last layer
+ *   [8] act  [batch*B, I]      SiLU(gate)*up of the last layer
+ *   [9] hn   [batch*(B-1), H]  final-normed hidden states of positions 1..B-1
+ * Element type is cfg.dtype except h.  `n` must be >= 10.  Host only.
+ */
+int dflash2_test_layout(const dflash2_config *cfg, int batch, int n_new, int max_ctx, size_t *offsets, int n);
 
 /*
  * Top-k of the rows of z = mult * (X W^T), softcapped when cap > 0, through

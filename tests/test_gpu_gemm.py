@@ -26,24 +26,31 @@ def _mat(rows, cols, seed, std, dtype):
     (300, 300, 128, 1),      # two activation tiles, ragged everywhere
     (4096, 8, 12288, 0),     # feature projection shape (8B)
     (6144, 8, 4096, 0),      # QKV shape (8B)
+    (4096, 8, 4096, 64),     # one K chunk per split: 64-way in-kernel reduction
 ])
-def test_bf16_gemm_matches_float64_product(M, N, K, splits):
+@pytest.mark.parametrize("accumulate", [False, True])
+def test_bf16_gemm_matches_float64_product(M, N, K, splits, accumulate):
     import torch
     B = lib()
     W = _mat(M, K, 1, 0.05, "bf16")
     X = _mat(N, K, 2, 1.0, "bf16")
-    cap = 64
-    part = torch.full((cap, N, M), float("nan"), device="cuda")
-    used = B.dflash2_test_gemm(B.BF16, S.to_torch(W), S.to_torch(X), splits, part)
-    torch.cuda.synchronize()
-    assert 1 <= used <= 64
-    got = part[:used].double().sum(0).cpu().numpy()
-    w64, x64 = W.values.astype(np.float64), X.values.astype(np.float64)
-    ref = x64 @ w64.T
-    bound = np.abs(x64) @ np.abs(w64).T
-    err = np.abs(got - ref)
-    assert np.all(np.isfinite(got))
-    assert np.all(err <= 1e-4 * bound + 1e-6), float(np.max(err / (bound + 1e-30)))
+    base = np.random.default_rng(3).standard_normal((N, M)).astype(np.float32)
+    out = torch.from_numpy(base).cuda() if accumulate else torch.full((N, M), float("nan"), device="cuda")
+    ws = torch.zeros(B.dflash2_test_gemm_workspace(M, N, splits), dtype=torch.uint8, device="cuda")
+    for rep in range(2):  # twice: the tile counters must come back to zero
+        if accumulate and rep == 1:
+            out.copy_(torch.from_numpy(base))
+        used = B.dflash2_test_gemm(B.BF16, S.to_torch(W), S.to_torch(X), splits, out, ws, accumulate)
+        torch.cuda.synchronize()
+        assert 1 <= used <= 64
+        got = out.double().cpu().numpy() - (base if accumulate else 0.0)
+        w64, x64 = W.values.astype(np.float64), X.values.astype(np.float64)
+        ref = x64 @ w64.T
+        bound = np.abs(x64) @ np.abs(w64).T + (np.abs(base) if accumulate else 0.0)
+        err = np.abs(got - ref)
+        assert np.all(np.isfinite(got))
+        assert np.all(err <= 1e-4 * bound + 1e-6), float(np.max(err / (bound + 1e-30)))
+    assert int(ws[:4 * ((M + 127) // 128)].view(torch.int32).abs().sum()) == 0
 
 
 @pytest.mark.parametrize("M,N,K", [(1000, 7, 256), (4096, 8, 768), (130, 40, 64)])
@@ -52,10 +59,11 @@ def test_f32_gemm_matches_float64_product(M, N, K):
     B = lib()
     W = _mat(M, K, 3, 0.05, "f32")
     X = _mat(N, K, 4, 1.0, "f32")
-    part = torch.full((1, N, M), float("nan"), device="cuda")
-    assert B.dflash2_test_gemm(B.F32, S.to_torch(W), S.to_torch(X), 0, part) == 1
+    out = torch.full((N, M), float("nan"), device="cuda")
+    ws = torch.zeros(B.dflash2_test_gemm_workspace(M, N, 1), dtype=torch.uint8, device="cuda")
+    assert B.dflash2_test_gemm(B.F32, S.to_torch(W), S.to_torch(X), 0, out, ws) == 1
     torch.cuda.synchronize()
-    got = part[0].double().cpu().numpy()
+    got = out.double().cpu().numpy()
     ref = X.values.astype(np.float64) @ W.values.astype(np.float64).T
     bound = np.abs(X.values.astype(np.float64)) @ np.abs(W.values.astype(np.float64)).T
     assert np.all(np.abs(got - ref) <= 1e-5 * bound + 1e-7)

@@ -236,10 +236,10 @@ def dflash2_test_gemm_topk(dtype, W, X, k, mult, cap, cand_id, cand_logit, debug
 
 
 def dflash2_test_layout(cfg, batch, n_new, max_ctx):
-    """Workspace byte offsets of {f, h, u, u2, q, kb, vb, O, act, hn}."""
-    out = (ctypes.c_size_t * 10)()
-    _check("dflash2_test_layout", lib().dflash2_test_layout(ctypes.byref(cfg), batch, n_new, max_ctx, out, 10))
-    return dict(zip(("f", "h", "u", "u2", "q", "kb", "vb", "O", "act", "hn"), list(out)))
+    """Workspace byte offsets of {f, h, u, u2, q, kb, vb, O, act, hn, ua, u2a}."""
+    out = (ctypes.c_size_t * 12)()
+    _check("dflash2_test_layout", lib().dflash2_test_layout(ctypes.byref(cfg), batch, n_new, max_ctx, out, 12))
+    return dict(zip(("f", "h", "u", "u2", "q", "kb", "vb", "O", "act", "hn", "ua", "u2a"), list(out)))
 
 
 def dflash2_launch_count():

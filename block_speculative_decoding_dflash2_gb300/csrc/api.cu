@@ -102,7 +102,7 @@ size_t partial_bound(int M, int N, int K) {
 }
 
 struct Layout {
-  size_t status, cnt, f, Y, P, h, u, u2, q, kb, vb, attn, O, act, hn, logits, lv, li, selx, total;
+  size_t status, cnt, f, Y, P, h, u, u2, ua, u2a, q, kb, vb, attn, O, act, hn, logits, lv, li, selx, total;
 };
 
 Layout plan(const dflash2_config& c, int batch, int n_new, int max_ctx) {
@@ -143,6 +143,8 @@ Layout plan(const dflash2_config& c, int batch, int n_new, int max_ctx) {
   L.h = take((size_t)rows * H * 4);
   L.u = take((size_t)rows * H * es);
   L.u2 = take((size_t)rows * H * es);
+  L.ua = take((size_t)rows * H * es);
+  L.u2a = take((size_t)rows * H * es);
   L.q = take((size_t)rows * nq * d * es);
   L.kb = take((size_t)rows * nkv * d * es);
   L.vb = take((size_t)rows * nkv * d * es);
@@ -274,10 +276,10 @@ void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
 int workspace_offsets(const dflash2_config* c, int batch, int n_new, int max_ctx, size_t* out, int n) {
   if (check_config(c) != DFLASH2_OK) return DFLASH2_ERR_SHAPE;
-  if (!out || n < 10) return DFLASH2_ERR_INVALID_ARG;
+  if (!out || n < 12) return DFLASH2_ERR_INVALID_ARG;
   const Layout L = plan(*c, batch, n_new, max_ctx);
-  const size_t v[10] = {L.f, L.h, L.u, L.u2, L.q, L.kb, L.vb, L.O, L.act, L.hn};
-  for (int i = 0; i < 10; ++i) out[i] = v[i];
+  const size_t v[12] = {L.f, L.h, L.u, L.u2, L.q, L.kb, L.vb, L.O, L.act, L.hn, L.ua, L.u2a};
+  for (int i = 0; i < 12; ++i) out[i] = v[i];
   return DFLASH2_OK;
 }
 
@@ -364,8 +366,10 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
   const int I = c.intermediate, G = H / c.conv_group_size, rows = batch * B;
   float* Y = at<float>(workspace, L.Y);
   float* h = at<float>(workspace, L.h);
-  void* u = at<char>(workspace, L.u);
-  void* u2 = at<char>(workspace, L.u2);
+  void* u = at<char>(workspace, L.u);    // MLP sublayer: normed input
+  void* u2 = at<char>(workspace, L.u2);  // MLP sublayer: after the conv
+  void* ua = at<char>(workspace, L.ua);   // attention sublayer: normed input
+  void* u2a = at<char>(workspace, L.u2a); // attention sublayer: after the conv
   void* q = at<char>(workspace, L.q);
   void* kb = at<char>(workspace, L.kb);
   void* vb = at<char>(workspace, L.vb);
@@ -376,13 +380,13 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
   void* ws = workspace;
 
   TRY(launch_embed_norm(c.dtype, anchor, c.mask_token_id, batch, B, w->embed, c.vocab, H, c.input_embedding_scale,
-                        w->layers[0].attn_norm, c.rms_eps, h, u, ctx));
+                        w->layers[0].attn_norm, c.rms_eps, h, ua, ctx));
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash2_layer_weights& Lw = w->layers[l];
     // attention sublayer: conv around the normed input, QKV, attention, O (+= residual)
-    TRY(gemm(c, ctx, ws, L, Lw.tapgen_attn, 2 * G, H, u, rows, Y, false));
-    TRY(launch_dyn_conv(c.dtype, u, Y, rows, H, c.conv_group_size, B, u2, ctx));
-    TRY(gemm(c, ctx, ws, L, Lw.qkv, (nq + 2 * nkv) * d, H, u2, rows, Y, false));
+    TRY(gemm(c, ctx, ws, L, Lw.tapgen_attn, 2 * G, H, ua, rows, Y, false));
+    TRY(launch_dyn_conv(c.dtype, ua, Y, rows, H, c.conv_group_size, B, u2a, ctx));
+    TRY(gemm(c, ctx, ws, L, Lw.qkv, (nq + 2 * nkv) * d, H, u2a, rows, Y, false));
     TRY(launch_qkv_epilogue(c.dtype, Y, rows, B, nq, nkv, d, Lw.q_norm, Lw.k_norm, c.rms_eps, c.rope_theta, ctx_len,
                             new_off, q, kb, vb, ctx));
     TRY(launch_attention(c.dtype, q, kb, vb, elem_ptr(k_cache, l * layer_elems, c.dtype),
@@ -397,7 +401,7 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
     TRY(launch_act(c.dtype, Y, rows, I, act, ctx));
     TRY(gemm(c, ctx, ws, L, Lw.down, H, I, act, rows, h, true));
     if (l + 1 < c.n_layers)
-      TRY(launch_rownorm(c.dtype, h, rows, H, w->layers[l + 1].attn_norm, c.rms_eps, u, B, 0, ctx));
+      TRY(launch_rownorm(c.dtype, h, rows, H, w->layers[l + 1].attn_norm, c.rms_eps, ua, B, 0, ctx));
     else
       TRY(launch_rownorm(c.dtype, h, rows, H, w->final_norm, c.rms_eps, hn, B, 1, ctx));
   }

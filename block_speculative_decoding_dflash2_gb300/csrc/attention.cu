@@ -189,6 +189,261 @@ __global__ void __launch_bounds__(AT) attn_partial_kernel(
   }
 }
 
+// ------------------------------------------------------------------------
+// bf16 path on the tensor cores (mma.sync m16n8k16, fp32 accumulation).
+// Same work split and partial format as attn_partial_kernel.  The CTA's
+// query rows form 16-row blocks; each warp owns one or two (row block, key
+// share) combinations with its own online-softmax state in registers.  For
+// every 16-key step: S = Q K^T (K rows read with ldmatrix as the col-major B
+// operand), scale, mask, online softmax, then O += P V with P split into
+// bf16 hi + lo parts (two MMAs), so the probabilities keep ~16 bits.
+
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+
+__device__ __forceinline__ void ldsm4_t(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+constexpr int MKT = 64;  // keys per shared-memory tile (mma path)
+
+template <int DH>
+size_t attn_mma_smem(int R) {
+  const int nrb = (R + 15) / 16;
+  const int ks = nrb >= 4 ? 1 : 4 / nrb;
+  return (size_t)(nrb * 16 + 2 * MKT) * (DH + 8) * 2 + (size_t)nrb * ks * 16 * (DH + 2) * 4 + MKT * 8;
+}
+
+// CPW: (row block, key share) combinations per warp (1 or 2), so the
+// register-resident accumulators are sized to what the launch needs.
+template <int DH, int MCPW>
+__global__ void __launch_bounds__(128) attn_mma_kernel(
+    const bf16* __restrict__ q, const bf16* __restrict__ kb, const bf16* __restrict__ vb, const bf16* __restrict__ kc,
+    const bf16* __restrict__ vc, const int32_t* __restrict__ block_table, int max_pages, int page_size, int n_pages,
+    const int32_t* __restrict__ ctx_len, const int32_t* __restrict__ new_off, int B, int nq, int nkv, int CH,
+    int nsplit, float* __restrict__ part, unsigned* status) {
+  constexpr int LD = DH + 8;  // padded smem row (elements): ldmatrix rows hit distinct banks
+  constexpr int NT = DH / 8;  // n8 tiles across the head dimension
+  extern __shared__ __align__(16) uint8_t smraw[];
+  const int sp = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+  const int grp = nq / nkv, R = grp * B;
+  const int nrb = (R + 15) / 16;
+  const int ksplit = nrb >= 4 ? 1 : 4 / nrb;
+  const int ncombo = nrb * ksplit;
+  bf16* Qs = reinterpret_cast<bf16*>(smraw);
+  bf16* Ks = Qs + nrb * 16 * LD;
+  bf16* Vs = Ks + MKT * LD;
+  float* comb = reinterpret_cast<float*>(Vs + MKT * LD);  // [ncombo][16][DH + 2]
+  long long* koff = reinterpret_cast<long long*>(comb + (size_t)ncombo * 16 * (DH + 2));
+
+  const int P = ctx_len[s] + (new_off[s + 1] - new_off[s]);
+  const int L = P + B;
+  const int k0 = sp * CH, k1 = min(k0 + CH, L);
+  float* out = part + ((((size_t)s * nkv + g) * nsplit + sp) * R) * (DH + 2);
+  if (k0 >= L) {
+    for (int r = threadIdx.x; r < R; r += blockDim.x) {
+      out[(size_t)r * (DH + 2) + DH] = -INFINITY;
+      out[(size_t)r * (DH + 2) + DH + 1] = 0.f;
+    }
+    return;
+  }
+  if (P > max_pages * page_size && sp == 0 && threadIdx.x == 0) flag(status, DFLASH2_DEV_BAD_LENGTH);
+  const float scale = rsqrtf((float)DH);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int C8 = DH / 8;
+  // query rows (zero padding to whole 16-row blocks)
+  for (int idx = threadIdx.x; idx < nrb * 16 * C8; idx += blockDim.x) {
+    const int r = idx / C8, c = (idx % C8) * 8;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < R) {
+      const int i = r / grp, h = g * grp + r % grp;
+      v = *reinterpret_cast<const uint4*>(q + (((size_t)s * B + i) * nq + h) * DH + c);
+    }
+    *reinterpret_cast<uint4*>(Qs + r * LD + c) = v;
+  }
+  // per-combination online-softmax state: rows lane/4 and lane/4 + 8 of the block
+  float m_st[MCPW][2], l_st[MCPW][2], acc[MCPW][NT][4];
+#pragma unroll
+  for (int c = 0; c < MCPW; ++c) {
+    m_st[c][0] = m_st[c][1] = -INFINITY;
+    l_st[c][0] = l_st[c][1] = 0.f;
+#pragma unroll
+    for (int n = 0; n < NT; ++n) acc[c][n][0] = acc[c][n][1] = acc[c][n][2] = acc[c][n][3] = 0.f;
+  }
+  constexpr long long BLOCK_BIT = 1LL << 62;
+  for (int t0 = k0; t0 < k1; t0 += MKT) {
+    const int nk = min(MKT, k1 - t0);
+    __syncthreads();
+    if (threadIdx.x < MKT) {
+      const int j = t0 + threadIdx.x;
+      long long o = -1;
+      if (threadIdx.x < nk) {
+        if (j < P) {
+          const int pi = j / page_size;
+          const int page = pi < max_pages ? block_table[(size_t)s * max_pages + pi] : -1;
+          if (page >= 0 && page < n_pages)
+            o = (((long long)page * page_size + j % page_size) * nkv + g) * DH;
+          else
+            flag(status, DFLASH2_DEV_BAD_PAGE);
+        } else {
+          o = BLOCK_BIT | ((((long long)s * B + (j - P)) * nkv + g) * DH);
+        }
+      }
+      koff[threadIdx.x] = o;
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < MKT * C8; idx += blockDim.x) {
+      const int kk = idx / C8, c = (idx % C8) * 8;
+      const long long o = koff[kk];
+      uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);  // missing keys read as zeros
+      if (o >= 0) {
+        const bf16* ks_ = (o & BLOCK_BIT) ? kb + (o & ~BLOCK_BIT) : kc + o;
+        const bf16* vs_ = (o & BLOCK_BIT) ? vb + (o & ~BLOCK_BIT) : vc + o;
+        kv = *reinterpret_cast<const uint4*>(ks_ + c);
+        vv = *reinterpret_cast<const uint4*>(vs_ + c);
+      }
+      *reinterpret_cast<uint4*>(Ks + kk * LD + c) = kv;
+      *reinterpret_cast<uint4*>(Vs + kk * LD + c) = vv;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int slot = 0; slot < MCPW; ++slot) {
+      const int combo = warp + slot * 4;
+      if (combo >= ncombo) break;
+      const int rb = combo / ksplit, ks = combo % ksplit;
+      const int kbeg = ks * (MKT / ksplit), kend = min(nk, (ks + 1) * (MKT / ksplit));
+      for (int j0 = kbeg; j0 < kend; j0 += 16) {
+        // S = Q K^T for 16 rows x 16 keys (two n8 tiles)
+        float S0[4] = {0.f, 0.f, 0.f, 0.f}, S1[4] = {0.f, 0.f, 0.f, 0.f};
+        const int mi = lane >> 3;
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          uint32_t a[4], bk[4];
+          ldsm4(a, Qs + (rb * 16 + (mi & 1) * 8 + (lane & 7)) * LD + kk * 16 + (mi >> 1) * 8);
+          ldsm4(bk, Ks + (j0 + (mi >> 1) * 8 + (lane & 7)) * LD + kk * 16 + (mi & 1) * 8);
+          mma16816(S0, a, bk[0], bk[1]);
+          mma16816(S1, a, bk[2], bk[3]);
+        }
+        // scale and mask keys past the chunk
+        const int cbase = j0 + (lane & 3) * 2;
+        float sv[8] = {S0[0], S0[1], S0[2], S0[3], S1[0], S1[1], S1[2], S1[3]};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int key = cbase + (e >= 4 ? 8 : 0) + (e & 1);
+          sv[e] = key < kend ? sv[e] * scale : -INFINITY;
+        }
+        // online softmax for the two rows this lane holds (row A: e = 0,1,4,5; row B: 2,3,6,7)
+        float mx0 = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[4], sv[5]));
+        float mx1 = fmaxf(fmaxf(sv[2], sv[3]), fmaxf(sv[6], sv[7]));
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+        }
+        const float mn0 = fmaxf(m_st[slot][0], mx0), mn1 = fmaxf(m_st[slot][1], mx1);
+        const float f0 = expf(m_st[slot][0] - mn0), f1 = expf(m_st[slot][1] - mn1);
+        m_st[slot][0] = mn0;
+        m_st[slot][1] = mn1;
+        float p[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) p[e] = expf(sv[e] - ((e & 2) ? mn1 : mn0));
+        float s0 = p[0] + p[1] + p[4] + p[5], s1 = p[2] + p[3] + p[6] + p[7];
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+          s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+          s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+        }
+        l_st[slot][0] = l_st[slot][0] * f0 + s0;
+        l_st[slot][1] = l_st[slot][1] * f1 + s1;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          acc[slot][n][0] *= f0;
+          acc[slot][n][1] *= f0;
+          acc[slot][n][2] *= f1;
+          acc[slot][n][3] *= f1;
+        }
+        // P as the A operand, split hi + lo
+        float lo[8];
+        uint32_t ph[4], pl[4];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) lo[e] = p[e] - __bfloat162float(__float2bfloat16_rn(p[e]));
+        ph[0] = pack_bf16(p[0], p[1]);
+        ph[1] = pack_bf16(p[2], p[3]);
+        ph[2] = pack_bf16(p[4], p[5]);
+        ph[3] = pack_bf16(p[6], p[7]);
+        pl[0] = pack_bf16(lo[0], lo[1]);
+        pl[1] = pack_bf16(lo[2], lo[3]);
+        pl[2] = pack_bf16(lo[4], lo[5]);
+        pl[3] = pack_bf16(lo[6], lo[7]);
+#pragma unroll
+        for (int n2 = 0; n2 < DH / 16; ++n2) {
+          uint32_t bv[4];
+          ldsm4_t(bv, Vs + (j0 + (mi & 1) * 8 + (lane & 7)) * LD + n2 * 16 + (mi >> 1) * 8);
+          mma16816(acc[slot][2 * n2], ph, bv[0], bv[1]);
+          mma16816(acc[slot][2 * n2], pl, bv[0], bv[1]);
+          mma16816(acc[slot][2 * n2 + 1], ph, bv[2], bv[3]);
+          mma16816(acc[slot][2 * n2 + 1], pl, bv[2], bv[3]);
+        }
+      }
+    }
+  }
+  // each combination's state -> shared memory, then rows combine their key shares
+#pragma unroll
+  for (int slot = 0; slot < MCPW; ++slot) {
+    const int combo = warp + slot * 4;
+    if (combo >= ncombo) break;
+    float* cb = comb + (size_t)combo * 16 * (DH + 2);
+    const int r0 = lane >> 2, c0 = (lane & 3) * 2;
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      cb[r0 * (DH + 2) + n * 8 + c0] = acc[slot][n][0];
+      cb[r0 * (DH + 2) + n * 8 + c0 + 1] = acc[slot][n][1];
+      cb[(r0 + 8) * (DH + 2) + n * 8 + c0] = acc[slot][n][2];
+      cb[(r0 + 8) * (DH + 2) + n * 8 + c0 + 1] = acc[slot][n][3];
+    }
+    if ((lane & 3) == 0) {
+      cb[r0 * (DH + 2) + DH] = m_st[slot][0];
+      cb[r0 * (DH + 2) + DH + 1] = l_st[slot][0];
+      cb[(r0 + 8) * (DH + 2) + DH] = m_st[slot][1];
+      cb[(r0 + 8) * (DH + 2) + DH + 1] = l_st[slot][1];
+    }
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < R * (DH + 2); idx += blockDim.x) {
+    const int r = idx / (DH + 2), c = idx % (DH + 2);
+    const int rb = r / 16, rr = r % 16;
+    float M = -INFINITY;
+    for (int ks = 0; ks < ksplit; ++ks) {
+      const float* cb = comb + (size_t)(rb * ksplit + ks) * 16 * (DH + 2) + rr * (DH + 2);
+      if (cb[DH + 1] > 0.f) M = fmaxf(M, cb[DH]);
+    }
+    float v = 0.f;
+    for (int ks = 0; ks < ksplit; ++ks) {
+      const float* cb = comb + (size_t)(rb * ksplit + ks) * 16 * (DH + 2) + rr * (DH + 2);
+      if (cb[DH + 1] > 0.f) v += (c == DH ? 0.f : (c == DH + 1 ? cb[DH + 1] : cb[c])) * expf(cb[DH] - M);
+    }
+    out[(size_t)r * (DH + 2) + c] = c == DH ? M : v;
+  }
+}
+
 // O[s, i, h, :] = sum_chunks acc e^(m - M) / sum_chunks l e^(m - M)
 template <typename T>
 __global__ void attn_combine_kernel(const float* __restrict__ part, int B, int nq, int nkv, int d, int nsplit,
@@ -260,7 +515,34 @@ int launch_attention(int dtype, const void* q, const void* kb, const void* vb, c
     attr = true;
   }
   if (smem > 200 * 1024) return DFLASH2_ERR_SHAPE;
-  if (dtype == DFLASH2_BF16) {
+  const int nrb = (R + 15) / 16;
+  const int ncombo = nrb * (nrb >= 4 ? 1 : 4 / nrb);
+  if (dtype == DFLASH2_BF16 && (d == 64 || d == 128) && ncombo <= 8) {
+    static bool mattr = false;
+    if (!mattr) {
+      const int mx = 200 * 1024;
+      if (cudaFuncSetAttribute(attn_mma_kernel<64, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx) ||
+          cudaFuncSetAttribute(attn_mma_kernel<64, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx) ||
+          cudaFuncSetAttribute(attn_mma_kernel<128, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx) ||
+          cudaFuncSetAttribute(attn_mma_kernel<128, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx))
+        return DFLASH2_ERR_CUDA;
+      mattr = true;
+    }
+    const size_t ms = d == 64 ? attn_mma_smem<64>(R) : attn_mma_smem<128>(R);
+    if (ms > 200 * 1024) return DFLASH2_ERR_SHAPE;
+    auto args = [&](auto kern) {
+      kern<<<grid, 128, ms, c.stream>>>(static_cast<const bf16*>(q), static_cast<const bf16*>(kb),
+                                        static_cast<const bf16*>(vb), static_cast<const bf16*>(kc),
+                                        static_cast<const bf16*>(vc), block_table, max_pages, page_size, n_pages,
+                                        ctx_len, new_off, B, nq, nkv, ch, nsplit, part, c.status);
+    };
+    if (d == 64)
+      ncombo <= 4 ? args(attn_mma_kernel<64, 1>) : args(attn_mma_kernel<64, 2>);
+    else
+      ncombo <= 4 ? args(attn_mma_kernel<128, 1>) : args(attn_mma_kernel<128, 2>);
+    attn_combine_kernel<bf16><<<batch * B * nq, 128, 0, c.stream>>>(part, B, nq, nkv, d, nsplit,
+                                                                      static_cast<bf16*>(o_out));
+  } else if (dtype == DFLASH2_BF16) {
     attn_partial_kernel<bf16><<<grid, AT, smem, c.stream>>>(
         static_cast<const bf16*>(q), static_cast<const bf16*>(kb), static_cast<const bf16*>(vb),
         static_cast<const bf16*>(kc), static_cast<const bf16*>(vc), block_table, max_pages, page_size, n_pages,

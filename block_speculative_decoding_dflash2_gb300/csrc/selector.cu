@@ -14,8 +14,9 @@
 //
 // sel_gather_kernel lays out E rows of [anchor, all candidates] so the factor
 // contraction runs on the same GEMM as the rest of the step; viterbi_kernel
-// (one CTA per sequence) stages that sequence's factors in shared memory and
-// runs the k x k dynamic programme over the B-1 positions.
+// (one CTA per sequence) stages that sequence's factors, logits and
+// candidate ids in shared memory and runs the k x k dynamic programme over
+// the B-1 positions without touching global memory again.
 #include <climits>
 
 #include "common.cuh"
@@ -25,6 +26,8 @@ namespace df2 {
 
 namespace {
 
+// x[r] = E[token of row r], rows = [anchor, cand(0,0..k-1), cand(1,..), ...]
+// per sequence; 16-byte copies (H is a multiple of 8).
 template <typename T>
 __global__ void __launch_bounds__(256) sel_gather_kernel(const int32_t* __restrict__ anchor,
                                                          const int32_t* __restrict__ cand_id, int D, int k,
@@ -38,27 +41,40 @@ __global__ void __launch_bounds__(256) sel_gather_kernel(const int32_t* __restri
     if (threadIdx.x == 0) flag(status, DFLASH2_DEV_BAD_TOKEN);
     tok = -1;
   }
-  for (int m = threadIdx.x; m < H; m += blockDim.x) x[(size_t)r * H + m] = tok < 0 ? T(0.f) : E[(size_t)tok * H + m];
+  constexpr int PER = 16 / sizeof(T);
+  uint4* dst = reinterpret_cast<uint4*>(x + (size_t)r * H);
+  const uint4* src = reinterpret_cast<const uint4*>(E + (size_t)(tok < 0 ? 0 : tok) * H);
+  for (int m = threadIdx.x; m < H / PER; m += blockDim.x) dst[m] = tok < 0 ? make_uint4(0, 0, 0, 0) : src[m];
 }
 
-__global__ void __launch_bounds__(256) viterbi_kernel(const float* __restrict__ Y, int batch,
+__global__ void __launch_bounds__(256) viterbi_kernel(const float* __restrict__ Y,
                                                       const int32_t* __restrict__ cand_id,
                                                       const float* __restrict__ cand_logit, int D, int k, int r,
                                                       int32_t* __restrict__ path, float* __restrict__ path_score) {
   extern __shared__ float sm[];
   const int s = blockIdx.x;
   const int nt = D * k + 1, w = 2 * r, ws = w + 1;  // padded row stride: no bank conflicts across candidates
-  float* F = sm;                     // [nt][ws] factors: A = F[t][0:r], Bf = F[t][r:2r]
-  float* Sm = F + (size_t)nt * ws;   // [k][k] scores / totals
-  float* delta = Sm + k * k;         // [k]
-  float* nd = delta + k;             // [k]
-  int* bp = reinterpret_cast<int*>(nd + k);  // [D][k]
-  (void)batch;
+  float* F = sm;                               // [nt][ws] factors: A = F[t][0:r], Bf = F[t][r:2r]
+  float* zs = F + (size_t)nt * ws;             // [D][k] candidate logits
+  float* Sm = zs + D * k;                      // [k][k] scores / totals
+  float* delta = Sm + k * k;                   // [k]
+  float* nd = delta + k;                       // [k]
+  int* cid = reinterpret_cast<int*>(nd + k);   // [D][k] candidate ids
+  int* bp = cid + D * k;                       // [D][k] back pointers
 
-  const float* y = Y + (size_t)s * nt * w;
-  for (int idx = threadIdx.x; idx < nt * w; idx += blockDim.x) F[(idx / w) * ws + idx % w] = y[idx];
+  const float2* y = reinterpret_cast<const float2*>(Y + (size_t)s * nt * w);
+  const int w2 = w / 2;
+  for (int idx = threadIdx.x; idx < nt * w2; idx += blockDim.x) {
+    const int t = idx / w2, c = (idx - t * w2) * 2;
+    const float2 v = y[idx];
+    F[t * ws + c] = v.x;
+    F[t * ws + c + 1] = v.y;
+  }
+  for (int idx = threadIdx.x; idx < D * k; idx += blockDim.x) {
+    zs[idx] = cand_logit[(size_t)s * D * k + idx];
+    cid[idx] = cand_id[(size_t)s * D * k + idx];
+  }
   __syncthreads();
-  const float* z = cand_logit + (size_t)s * D * k;
   auto dot = [&](int ta, int tb) {  // <A[ta], Bf[tb]>
     const float* a = F + (size_t)ta * ws;
     const float* b = F + (size_t)tb * ws + r;
@@ -85,7 +101,7 @@ __global__ void __launch_bounds__(256) viterbi_kernel(const float* __restrict__ 
     }
   };
   // position 1: the predecessor is the anchor (factor row 0)
-  for (int j = threadIdx.x; j < k; j += blockDim.x) Sm[j] = z[j] + dot(0, 1 + j);
+  for (int j = threadIdx.x; j < k; j += blockDim.x) Sm[j] = zs[j] + dot(0, 1 + j);
   __syncthreads();
   row_logsoftmax(1, false);
   __syncthreads();
@@ -93,8 +109,8 @@ __global__ void __launch_bounds__(256) viterbi_kernel(const float* __restrict__ 
   __syncthreads();
   for (int i = 1; i < D; ++i) {
     for (int pr = threadIdx.x; pr < k * k; pr += blockDim.x) {
-      const int p = pr / k, j = pr % k;
-      Sm[pr] = z[i * k + j] + dot(1 + (i - 1) * k + p, 1 + i * k + j);
+      const int p = pr / k, j = pr - p * k;
+      Sm[pr] = zs[i * k + j] + dot(1 + (i - 1) * k + p, 1 + i * k + j);
     }
     __syncthreads();
     row_logsoftmax(k, true);
@@ -120,7 +136,7 @@ __global__ void __launch_bounds__(256) viterbi_kernel(const float* __restrict__ 
       if (delta[jj] > delta[j]) j = jj;
     if (path_score) path_score[s] = delta[j];
     for (int i = D - 1; i >= 0; --i) {
-      path[(size_t)s * D + i] = cand_id[((size_t)s * D + i) * k + j];
+      path[(size_t)s * D + i] = cid[i * k + j];
       if (i > 0) j = bp[i * k + j];
     }
   }
@@ -129,18 +145,18 @@ __global__ void __launch_bounds__(256) viterbi_kernel(const float* __restrict__ 
 }  // namespace
 
 size_t viterbi_smem_bytes(int D, int k, int r) {
-  return sizeof(float) * ((size_t)(D * k + 1) * (2 * r + 1) + (size_t)k * k + 2 * (size_t)k) +
-         sizeof(int) * (size_t)D * k;
+  return sizeof(float) * ((size_t)(D * k + 1) * (2 * r + 1) + (size_t)D * k + (size_t)k * k + 2 * (size_t)k) +
+         sizeof(int) * 2 * (size_t)D * k;
 }
 
 int launch_sel_gather(int dtype, const int32_t* anchor, const int32_t* cand_id, int batch, int D, int k,
                       const void* embed, int V, int H, void* x_out, const Ctx& c) {
   const int rows = batch * (D * k + 1);
   if (dtype == DFLASH2_BF16)
-    sel_gather_kernel<bf16><<<rows, 256, 0, c.stream>>>(anchor, cand_id, D, k, static_cast<const bf16*>(embed), V, H,
+    sel_gather_kernel<bf16><<<rows, 128, 0, c.stream>>>(anchor, cand_id, D, k, static_cast<const bf16*>(embed), V, H,
                                                          static_cast<bf16*>(x_out), c.status);
   else
-    sel_gather_kernel<float><<<rows, 256, 0, c.stream>>>(anchor, cand_id, D, k, static_cast<const float*>(embed), V,
+    sel_gather_kernel<float><<<rows, 128, 0, c.stream>>>(anchor, cand_id, D, k, static_cast<const float*>(embed), V,
                                                           H, static_cast<float*>(x_out), c.status);
   count_launch();
   return cudaGetLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
@@ -155,7 +171,7 @@ int launch_viterbi(const float* Y, const int32_t* cand_id, const float* cand_log
       return DFLASH2_ERR_CUDA;
     attr = true;
   }
-  viterbi_kernel<<<batch, 256, smem, c.stream>>>(Y, batch, cand_id, cand_logit, D, k, r, path, path_score);
+  viterbi_kernel<<<batch, 256, smem, c.stream>>>(Y, cand_id, cand_logit, D, k, r, path, path_score);
   count_launch();
   return cudaGetLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
 }

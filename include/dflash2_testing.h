@@ -48,7 +48,9 @@ int dflash2_test_gemm(int dtype, const void *W, int M, int K, const void *X, int
  *   [7] O    [batch*B, nq*d]   attention output of the last layer
  *   [8] act  [batch*B, I]      SiLU(gate)*up of the last layer
  *   [9] hn   [batch*(B-1), H]  final-normed hidden states of positions 1..B-1
- * Element type is cfg.dtype except h.  `n` must be >= 10.  Host only.
+ *  [10] ua   [batch*B, H]      normed input of the last attention sublayer
+ *  [11] u2a  [batch*B, H]      that input after the dynamic convolution
+ * Element type is cfg.dtype except h.  `n` must be >= 12.  Host only.
  */
 int dflash2_test_layout(const dflash2_config *cfg, int batch, int n_new, int max_ctx, size_t *offsets, int n);
 

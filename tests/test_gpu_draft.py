@@ -59,6 +59,15 @@ def test_small_bf16_block16_and_groups():
     check_case(case)
 
 
+def test_small_bf16_gqa5_block16():
+    # 5 query heads per kv head x 16 block rows = 80 rows per kv head: the
+    # attention kernel's two-combination-per-warp variant (27B-class layout)
+    cfg = S.small_bf16_config(block_size=16, n_q_heads=10, n_kv_heads=2, head_dim=128, top_k=16,
+                              hidden=512, index=16)
+    case = Case(cfg, ctx_lens=[300, 33], n_new=[16, 4], seed=18).run_gpu()
+    check_case(case)
+
+
 @pytest.mark.slow
 def test_qwen3_8b_shape_batch1():
     # End to end at this shape the bf16 pipeline is rounding-chaotic: the

@@ -106,15 +106,17 @@ def run_stagewise(case):
     act = R.get("act", (rows, I))
     h = R.get("h", (rows, H), fp32=True)
     hn = R.get("hn", (b * D, H))
-    q_ref, k_ref, v_ref, O_ref, h_mid = [], [], [], [], []
+    ua = R.get("ua", (rows, H))
+    u2a = R.get("u2a", (rows, H))
+    q_ref, k_ref, v_ref, O_ref, h_mid, ua_ref, u2a_ref = [], [], [], [], [], [], []
     for s in range(b):
         P = int(case.ctx_lens[s] + case.n_new[s])
         sl = slice(s * B_, (s + 1) * B_)
         toks = np.array([int(case.anchor[s])] + [cfg["mask_token_id"]] * D)
         h0 = cfg["input_embedding_scale"] * Wv["embed"][toks].astype(np.float64)
-        u = st(O.rms_norm(h0, Wl["attn_norm"], eps))
-        u2 = st(u + O.dynamic_conv(u, Wl["tapgen_attn"], cfg["conv_group_size"]))
-        qkv = u2 @ Wl["qkv"].astype(np.float64).T
+        ua_ref.append(st(O.rms_norm(h0, Wl["attn_norm"], eps)))
+        u2a_ref.append(st(ua[sl] + O.dynamic_conv(ua[sl], Wl["tapgen_attn"], cfg["conv_group_size"])))
+        qkv = u2a[sl] @ Wl["qkv"].astype(np.float64).T
         pos = P + np.arange(B_)
         q_ref.append(st(O.rope(O.rms_norm(qkv[:, :nq * d].reshape(B_, nq, d), Wl["q_norm"], eps), pos,
                                cfg["rope_theta"])))
@@ -124,9 +126,11 @@ def run_stagewise(case):
         Kc, Vc = cache_rows(case, 0, s, np.arange(P))
         O_ref.append(st(O.block_attention(q[sl], Kc, Vc, kb[sl], vb[sl])).reshape(B_, nq * d))
         h_mid.append(h0 + Og[sl] @ Wl["o"].astype(np.float64).T)
-    check_ulps("q", q, np.concatenate(q_ref), 3)
-    check_ulps("k_blk", kb, np.concatenate(k_ref), 3)
-    check_ulps("v_blk", vb, np.concatenate(v_ref), 3)
+    check_ulps("u_attn", ua, np.concatenate(ua_ref), 2)
+    check_ulps("u2_attn", u2a, np.concatenate(u2a_ref), 2)
+    check_ulps("q", q, np.concatenate(q_ref), 2)
+    check_ulps("k_blk", kb, np.concatenate(k_ref), 2)
+    check_ulps("v_blk", vb, np.concatenate(v_ref), 2)
     check_ulps("attn_O", Og, np.concatenate(O_ref), 2)
     h_mid = np.concatenate(h_mid)
     check_ulps("u_mlp", u_m, st(O.rms_norm(h_mid, Wl["mlp_norm"], eps)), 2)

@@ -59,6 +59,8 @@ __global__ void __launch_bounds__(AT) attn_partial_kernel(
     const int32_t* __restrict__ ctx_len, const int32_t* __restrict__ new_off, int B, int nq, int nkv, int d, int CH,
     int nsplit, float* __restrict__ part, unsigned* status) {
   extern __shared__ float sm[];
+  pdl_launch_next();
+  pdl_wait();
   const int sp = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
   const int grp = nq / nkv, R = grp * B;
   float* Qs = sm;
@@ -243,6 +245,8 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(
   constexpr int LD = DH + 8;  // padded smem row (elements): ldmatrix rows hit distinct banks
   constexpr int NT = DH / 8;  // n8 tiles across the head dimension
   extern __shared__ __align__(16) uint8_t smraw[];
+  pdl_launch_next();
+  pdl_wait();
   const int sp = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
   const int grp = nq / nkv, R = grp * B;
   const int nrb = (R + 15) / 16;
@@ -444,34 +448,75 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(
   }
 }
 
-// O[s, i, h, :] = sum_chunks acc e^(m - M) / sum_chunks l e^(m - M)
+// O[s, i, h, :] = sum_chunks acc e^(m - M) / sum_chunks l e^(m - M).
+// One CTA per (sequence, kv head, group of CR query rows): the chunk weights
+// e^(m - M) / den of its rows are formed once in shared memory, then every
+// output element sums its chunks with coalesced, batched loads.
+constexpr int CR = 8;
+
 template <typename T>
-__global__ void attn_combine_kernel(const float* __restrict__ part, int B, int nq, int nkv, int d, int nsplit,
-                                    T* __restrict__ o) {
-  const int h = blockIdx.x % nq;
-  const int si = blockIdx.x / nq;  // s*B + i
-  const int s = si / B, i = si % B;
-  const int grp = nq / nkv, g = h / grp, R = grp * B;
-  const int r = i * grp + h % grp;
-  const float* base = part + (((size_t)s * nkv + g) * nsplit) * R * (d + 2) + (size_t)r * (d + 2);
+__global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restrict__ part, int B, int nq, int nkv,
+                                                           int d, int nsplit, T* __restrict__ o) {
+  extern __shared__ float cw[];  // [nsplit][CR] weights
+  pdl_launch_next();
+  pdl_wait();
+  const int nrg = (nq / nkv * B + CR - 1) / CR;
+  const int rg = blockIdx.x % nrg, g = (blockIdx.x / nrg) % nkv, s = blockIdx.x / (nrg * nkv);
+  const int grp = nq / nkv, R = grp * B;
+  const int r0 = rg * CR, nr = min(CR, R - r0);
+  const float* base = part + (((size_t)s * nkv + g) * nsplit) * R * (d + 2);
   const size_t sstride = (size_t)R * (d + 2);
-  float M = -INFINITY;
-  for (int sp = 0; sp < nsplit; ++sp) {
-    const float* p = base + sp * sstride;
-    if (p[d + 1] > 0.f) M = fmaxf(M, p[d]);
-  }
-  float den = 0.f;
-  for (int sp = 0; sp < nsplit; ++sp) {
-    const float* p = base + sp * sstride;
-    if (p[d + 1] > 0.f) den += p[d + 1] * expf(p[d] - M);
-  }
-  for (int c = threadIdx.x; c < d; c += blockDim.x) {
-    float num = 0.f;
-    for (int sp = 0; sp < nsplit; ++sp) {
-      const float* p = base + sp * sstride;
-      if (p[d + 1] > 0.f) num += p[c] * expf(p[d] - M);
+  // m and l of every (chunk, row) into shared memory (cw = m, cl = l)
+  float* cl = cw + nsplit * CR;
+  for (int idx = threadIdx.x; idx < nsplit * CR; idx += blockDim.x) {
+    const int sp = idx / CR, rr = idx % CR;
+    float m = -INFINITY, l = 0.f;
+    if (rr < nr) {
+      const float* p = base + sp * sstride + (size_t)(r0 + rr) * (d + 2);
+      l = p[d + 1];
+      m = l > 0.f ? p[d] : -INFINITY;
     }
-    st(&o[(size_t)si * nq * d + h * d + c], num / den);
+    cw[idx] = m;
+    cl[idx] = l;
+  }
+  __syncthreads();
+  if (threadIdx.x < CR) {
+    const int rr = threadIdx.x;
+    float M = -INFINITY;
+    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, cw[sp * CR + rr]);
+    float den = 0.f;
+    for (int sp = 0; sp < nsplit; ++sp) {
+      const float m = cw[sp * CR + rr];
+      if (m > -INFINITY && rr < nr) {
+        const float e = expf(m - M);
+        den += cl[sp * CR + rr] * e;
+        cw[sp * CR + rr] = e;
+      } else {
+        cw[sp * CR + rr] = 0.f;
+      }
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    for (int sp = 0; sp < nsplit; ++sp) cw[sp * CR + rr] *= inv;
+  }
+  __syncthreads();
+  constexpr int U = 8;
+  for (int idx = threadIdx.x; idx < nr * d; idx += blockDim.x) {
+    const int rr = idx / d, c = idx % d;
+    const float* p = base + (size_t)(r0 + rr) * (d + 2) + c;
+    float num = 0.f;
+    for (int sp0 = 0; sp0 < nsplit; sp0 += U) {
+      float v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) v[u] = sp0 + u < nsplit ? p[(sp0 + u) * sstride] : 0.f;
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (sp0 + u < nsplit) {
+          const float w = cw[(sp0 + u) * CR + rr];
+          if (w != 0.f) num += v[u] * w;  // empty chunks leave acc unwritten
+        }
+    }
+    const int r = r0 + rr, i = r / grp, h = g * grp + r % grp;
+    st(&o[((size_t)s * B + i) * nq * d + h * d + c], num);
   }
 }
 
@@ -530,35 +575,39 @@ int launch_attention(int dtype, const void* q, const void* kb, const void* vb, c
     }
     const size_t ms = d == 64 ? attn_mma_smem<64>(R) : attn_mma_smem<128>(R);
     if (ms > 200 * 1024) return DFLASH2_ERR_SHAPE;
-    auto args = [&](auto kern) {
-      kern<<<grid, 128, ms, c.stream>>>(static_cast<const bf16*>(q), static_cast<const bf16*>(kb),
-                                        static_cast<const bf16*>(vb), static_cast<const bf16*>(kc),
-                                        static_cast<const bf16*>(vc), block_table, max_pages, page_size, n_pages,
-                                        ctx_len, new_off, B, nq, nkv, ch, nsplit, part, c.status);
-    };
+    const bf16 *q_ = static_cast<const bf16*>(q), *kb_ = static_cast<const bf16*>(kb),
+               *vb_ = static_cast<const bf16*>(vb), *kc_ = static_cast<const bf16*>(kc),
+               *vc_ = static_cast<const bf16*>(vc);
+    int rc;
     if (d == 64)
-      ncombo <= 4 ? args(attn_mma_kernel<64, 1>) : args(attn_mma_kernel<64, 2>);
+      rc = launch_k(ncombo <= 4 ? attn_mma_kernel<64, 1> : attn_mma_kernel<64, 2>, grid, dim3(128), ms, c.stream,
+                    q_, kb_, vb_, kc_, vc_, block_table, max_pages, page_size, n_pages, ctx_len, new_off, B, nq, nkv,
+                    ch, nsplit, part, c.status);
     else
-      ncombo <= 4 ? args(attn_mma_kernel<128, 1>) : args(attn_mma_kernel<128, 2>);
-    attn_combine_kernel<bf16><<<batch * B * nq, 128, 0, c.stream>>>(part, B, nq, nkv, d, nsplit,
-                                                                      static_cast<bf16*>(o_out));
+      rc = launch_k(ncombo <= 4 ? attn_mma_kernel<128, 1> : attn_mma_kernel<128, 2>, grid, dim3(128), ms,
+                    c.stream, q_, kb_, vb_, kc_, vc_, block_table, max_pages, page_size, n_pages, ctx_len, new_off,
+                    B, nq, nkv, ch, nsplit, part, c.status);
+    if (rc) return rc;
   } else if (dtype == DFLASH2_BF16) {
-    attn_partial_kernel<bf16><<<grid, AT, smem, c.stream>>>(
-        static_cast<const bf16*>(q), static_cast<const bf16*>(kb), static_cast<const bf16*>(vb),
-        static_cast<const bf16*>(kc), static_cast<const bf16*>(vc), block_table, max_pages, page_size, n_pages,
-        ctx_len, new_off, B, nq, nkv, d, ch, nsplit, part, c.status);
-    attn_combine_kernel<bf16><<<batch * B * nq, 128, 0, c.stream>>>(part, B, nq, nkv, d, nsplit,
-                                                                      static_cast<bf16*>(o_out));
+    const int rc = launch_k(attn_partial_kernel<bf16>, grid, dim3(AT), smem, c.stream, static_cast<const bf16*>(q),
+                            static_cast<const bf16*>(kb), static_cast<const bf16*>(vb), static_cast<const bf16*>(kc),
+                            static_cast<const bf16*>(vc), block_table, max_pages, page_size, n_pages, ctx_len,
+                            new_off, B, nq, nkv, d, ch, nsplit, part, c.status);
+    if (rc) return rc;
   } else {
-    attn_partial_kernel<float><<<grid, AT, smem, c.stream>>>(
-        static_cast<const float*>(q), static_cast<const float*>(kb), static_cast<const float*>(vb),
-        static_cast<const float*>(kc), static_cast<const float*>(vc), block_table, max_pages, page_size, n_pages,
-        ctx_len, new_off, B, nq, nkv, d, ch, nsplit, part, c.status);
-    attn_combine_kernel<float><<<batch * B * nq, 128, 0, c.stream>>>(part, B, nq, nkv, d, nsplit,
-                                                                       static_cast<float*>(o_out));
+    const int rc = launch_k(attn_partial_kernel<float>, grid, dim3(AT), smem, c.stream,
+                            static_cast<const float*>(q), static_cast<const float*>(kb), static_cast<const float*>(vb),
+                            static_cast<const float*>(kc), static_cast<const float*>(vc), block_table, max_pages,
+                            page_size, n_pages, ctx_len, new_off, B, nq, nkv, d, ch, nsplit, part, c.status);
+    if (rc) return rc;
   }
-  count_launch(2);
-  return cudaGetLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+  const dim3 cgrid(batch * nkv * ((R + CR - 1) / CR));
+  const size_t csm = 2 * (size_t)nsplit * CR * sizeof(float);
+  if (dtype == DFLASH2_BF16)
+    return launch_k(attn_combine_kernel<bf16>, cgrid, dim3(256), csm, c.stream, (const float*)part, B, nq, nkv, d,
+                    nsplit, static_cast<bf16*>(o_out));
+  return launch_k(attn_combine_kernel<float>, cgrid, dim3(256), csm, c.stream, (const float*)part, B, nq, nkv, d,
+                  nsplit, static_cast<float*>(o_out));
 }
 
 }  // namespace df2

@@ -51,6 +51,12 @@ __device__ __forceinline__ float block_sum(float v, float* sh) {
   return t;
 }
 
+// ----------------------------------------------------------------- PDL
+// Programmatic dependent launch: let the next kernel of the stream start its
+// launch now, and wait for the previous kernel's completion (and memory) here.
+__device__ __forceinline__ void pdl_launch_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ----------------------------------------------------------------- status
 
 __device__ __forceinline__ void flag(unsigned* status, unsigned code) {

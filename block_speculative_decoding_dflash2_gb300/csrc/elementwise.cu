@@ -108,6 +108,8 @@ __global__ void __launch_bounds__(RT) feature_norm_kernel(const float* __restric
                                                           const T* __restrict__ gamma, float eps, T* __restrict__ f) {
   extern __shared__ float xs[];
   __shared__ float red[32];
+  pdl_launch_next();
+  pdl_wait();
   const size_t n = blockIdx.x;
   for (int m = threadIdx.x * 4; m < H; m += blockDim.x * 4)
     *reinterpret_cast<float4*>(xs + m) = *reinterpret_cast<const float4*>(Y + n * H + m);
@@ -135,6 +137,8 @@ __global__ void __launch_bounds__(RT) kv_append_kernel(const float* __restrict__
                                                        const int32_t* __restrict__ block_table, int max_pages,
                                                        int page_size, int n_pages, T* __restrict__ kc,
                                                        T* __restrict__ vc, unsigned* status) {
+  pdl_launch_next();
+  pdl_wait();
   const int n = blockIdx.x;
   const int s = owner_of(new_off, batch, n);
   const int pos = ctx_len[s] + (n - new_off[s]);
@@ -176,6 +180,8 @@ __global__ void __launch_bounds__(RT) embed_norm_kernel(const int32_t* __restric
                                                         T* __restrict__ u, unsigned* status) {
   extern __shared__ float xs[];
   __shared__ float red[32];
+  pdl_launch_next();
+  pdl_wait();
   const int row = blockIdx.x;
   const int s = row / B, i = row % B;
   int tok = i == 0 ? anchor[s] : mask_id;
@@ -202,6 +208,8 @@ __global__ void __launch_bounds__(RT) rownorm_kernel(const float* __restrict__ h
                                                      float eps, T* __restrict__ u, int B, int skip_anchor) {
   extern __shared__ float xs[];
   __shared__ float red[32];
+  pdl_launch_next();
+  pdl_wait();
   const int row = blockIdx.x;
   int orow = row;
   if (skip_anchor) {
@@ -222,6 +230,8 @@ template <typename T>
 __global__ void __launch_bounds__(RT) dyn_conv_kernel(const T* __restrict__ u, const float* __restrict__ Y, int H,
                                                       int gs, int B, T* __restrict__ u2) {
   extern __shared__ float alpha[];  // [G][2]
+  pdl_launch_next();
+  pdl_wait();
   const int row = blockIdx.x;
   const int i = row % B;
   const int G = H / gs;
@@ -253,6 +263,8 @@ __global__ void __launch_bounds__(RT) qkv_epi_kernel(const float* __restrict__ Y
                                                      double log2_theta, const int32_t* __restrict__ ctx_len,
                                                      const int32_t* __restrict__ new_off, T* __restrict__ q,
                                                      T* __restrict__ kb, T* __restrict__ vb) {
+  pdl_launch_next();
+  pdl_wait();
   const int row = blockIdx.x;
   const int s = row / B, i = row % B;
   const int pos = ctx_len[s] + (new_off[s + 1] - new_off[s]) + i;
@@ -280,6 +292,8 @@ __global__ void __launch_bounds__(RT) qkv_epi_kernel(const float* __restrict__ Y
 // act = SiLU(gate) * up from the stacked gate/up output Y [rows][2I].
 template <typename T>
 __global__ void __launch_bounds__(RT) act_kernel(const float* __restrict__ Y, int rows, int I, T* __restrict__ act) {
+  pdl_launch_next();
+  pdl_wait();
   const size_t total4 = (size_t)rows * I / 4;
   for (size_t q4 = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q4 < total4; q4 += (size_t)gridDim.x * blockDim.x) {
     const size_t idx = q4 * 4;
@@ -289,11 +303,6 @@ __global__ void __launch_bounds__(RT) act_kernel(const float* __restrict__ Y, in
     st4(act + idx, make_float4(g.x / (1.f + expf(-g.x)) * up.x, g.y / (1.f + expf(-g.y)) * up.y,
                                g.z / (1.f + expf(-g.z)) * up.z, g.w / (1.f + expf(-g.w)) * up.w));
   }
-}
-
-inline int check() {
-  count_launch();
-  return cudaGetLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
 }
 
 }  // namespace
@@ -312,9 +321,10 @@ inline int check() {
 int launch_rows_feature_norm(int dtype, const float* Y, int rows, int H, const void* gamma, float eps, void* f_out,
                              const Ctx& c) {
   if (rows <= 0) return DFLASH2_OK;
-  DF2_DISPATCH(dtype, feature_norm_kernel<T><<<rows, RT, H * sizeof(float), c.stream>>>(
-                          Y, H, static_cast<const T*>(gamma), eps, static_cast<T*>(f_out)));
-  return check();
+  int rc;
+  DF2_DISPATCH(dtype, rc = launch_k(feature_norm_kernel<T>, dim3(rows), dim3(RT), H * sizeof(float), c.stream, Y, H,
+                                    static_cast<const T*>(gamma), eps, static_cast<T*>(f_out)));
+  return rc;
 }
 
 int launch_kv_append(int dtype, const float* Y, int rows, int nkv, int d, const void* k_norm, float eps, float theta,
@@ -322,50 +332,58 @@ int launch_kv_append(int dtype, const float* Y, int rows, int nkv, int d, const 
                      int max_pages, int page_size, int n_pages, void* kc, void* vc, const Ctx& c) {
   if (rows <= 0) return DFLASH2_OK;
   const double l2t = std::log2((double)theta);
-  DF2_DISPATCH(dtype, kv_append_kernel<T><<<rows, RT, 0, c.stream>>>(
-                          Y, nkv, d, static_cast<const T*>(k_norm), eps, l2t, ctx_len, new_off, batch, block_table,
-                          max_pages, page_size, n_pages, static_cast<T*>(kc), static_cast<T*>(vc), c.status));
-  return check();
+  int rc;
+  DF2_DISPATCH(dtype, rc = launch_k(kv_append_kernel<T>, dim3(rows), dim3(RT), 0, c.stream, Y, nkv, d,
+                                    static_cast<const T*>(k_norm), eps, l2t, ctx_len, new_off, batch, block_table,
+                                    max_pages, page_size, n_pages, static_cast<T*>(kc), static_cast<T*>(vc),
+                                    c.status));
+  return rc;
 }
 
 int launch_embed_norm(int dtype, const int32_t* anchor, int mask_id, int batch, int B, const void* embed, int V, int H,
                       float scale, const void* gamma, float eps, float* h_out, void* u_out, const Ctx& c) {
-  DF2_DISPATCH(dtype, embed_norm_kernel<T><<<batch * B, RT, H * sizeof(float), c.stream>>>(
-                          anchor, mask_id, B, static_cast<const T*>(embed), V, H, scale,
-                          static_cast<const T*>(gamma), eps, h_out, static_cast<T*>(u_out), c.status));
-  return check();
+  int rc;
+  DF2_DISPATCH(dtype, rc = launch_k(embed_norm_kernel<T>, dim3(batch * B), dim3(RT), H * sizeof(float), c.stream,
+                                    anchor, mask_id, B, static_cast<const T*>(embed), V, H, scale,
+                                    static_cast<const T*>(gamma), eps, h_out, static_cast<T*>(u_out), c.status));
+  return rc;
 }
 
 int launch_rownorm(int dtype, const float* h, int rows, int H, const void* gamma, float eps, void* u_out, int B,
                    int skip_anchor, const Ctx& c) {
-  DF2_DISPATCH(dtype, rownorm_kernel<T><<<rows, RT, H * sizeof(float), c.stream>>>(
-                          h, H, static_cast<const T*>(gamma), eps, static_cast<T*>(u_out), B, skip_anchor));
-  return check();
+  int rc;
+  DF2_DISPATCH(dtype, rc = launch_k(rownorm_kernel<T>, dim3(rows), dim3(RT), H * sizeof(float), c.stream, h, H,
+                                    static_cast<const T*>(gamma), eps, static_cast<T*>(u_out), B, skip_anchor));
+  return rc;
 }
 
 int launch_dyn_conv(int dtype, const void* u, const float* Y, int rows, int H, int group_size, int B, void* u2_out,
                     const Ctx& c) {
   const int G = H / group_size;
-  DF2_DISPATCH(dtype, dyn_conv_kernel<T><<<rows, RT, 2 * G * sizeof(float), c.stream>>>(
-                          static_cast<const T*>(u), Y, H, group_size, B, static_cast<T*>(u2_out)));
-  return check();
+  int rc;
+  DF2_DISPATCH(dtype, rc = launch_k(dyn_conv_kernel<T>, dim3(rows), dim3(RT), 2 * G * sizeof(float), c.stream,
+                                    static_cast<const T*>(u), Y, H, group_size, B, static_cast<T*>(u2_out)));
+  return rc;
 }
 
 int launch_qkv_epilogue(int dtype, const float* Y, int rows, int B, int nq, int nkv, int d, const void* q_norm,
                         const void* k_norm, float eps, float theta, const int32_t* ctx_len, const int32_t* new_off,
                         void* q, void* kb, void* vb, const Ctx& c) {
   const double l2t = std::log2((double)theta);
-  DF2_DISPATCH(dtype, qkv_epi_kernel<T><<<rows, RT, 0, c.stream>>>(
-                          Y, B, nq, nkv, d, static_cast<const T*>(q_norm), static_cast<const T*>(k_norm), eps, l2t,
-                          ctx_len, new_off, static_cast<T*>(q), static_cast<T*>(kb), static_cast<T*>(vb)));
-  return check();
+  int rc;
+  DF2_DISPATCH(dtype, rc = launch_k(qkv_epi_kernel<T>, dim3(rows), dim3(RT), 0, c.stream, Y, B, nq, nkv, d,
+                                    static_cast<const T*>(q_norm), static_cast<const T*>(k_norm), eps, l2t, ctx_len,
+                                    new_off, static_cast<T*>(q), static_cast<T*>(kb), static_cast<T*>(vb)));
+  return rc;
 }
 
 int launch_act(int dtype, const float* Y, int rows, int I, void* act, const Ctx& c) {
   const size_t total4 = (size_t)rows * I / 4;
   const int blocks = (int)std::min<size_t>((total4 + RT - 1) / RT, (size_t)c.nsm * 4);
-  DF2_DISPATCH(dtype, act_kernel<T><<<blocks, RT, 0, c.stream>>>(Y, rows, I, static_cast<T*>(act)));
-  return check();
+  int rc;
+  DF2_DISPATCH(dtype, rc = launch_k(act_kernel<T>, dim3(blocks), dim3(RT), 0, c.stream, Y, rows, I,
+                                    static_cast<T*>(act)));
+  return rc;
 }
 
 }  // namespace df2

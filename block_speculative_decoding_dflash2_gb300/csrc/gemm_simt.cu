@@ -18,6 +18,8 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const float* __restrict_
                                                         float* __restrict__ out, int accumulate) {
   __shared__ float Ws[TK][TM + 1];
   __shared__ float Xs[TK][TN + 1];
+  pdl_launch_next();
+  pdl_wait();
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const int m0 = blockIdx.x * TM, n0 = blockIdx.y * TN;
   float acc[4][2] = {};
@@ -59,11 +61,8 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const float* __restrict_
 int gemm_f32(const GemmOp& g, const Ctx& c) {
   if (g.M <= 0 || g.N <= 0 || g.K <= 0) return DFLASH2_ERR_SHAPE;
   dim3 grid((g.M + TM - 1) / TM, (g.N + TN - 1) / TN);
-  simt_gemm_kernel<<<grid, 256, 0, c.stream>>>(static_cast<const float*>(g.W), g.M, g.K, g.ldw,
-                                                static_cast<const float*>(g.X), g.N, g.ldx, g.out,
-                                                g.accumulate ? 1 : 0);
-  count_launch();
-  return cudaGetLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+  return launch_k(simt_gemm_kernel, grid, dim3(256), 0, c.stream, static_cast<const float*>(g.W), g.M, g.K, g.ldw,
+                  static_cast<const float*>(g.X), g.N, g.ldx, g.out, g.accumulate ? 1 : 0);
 }
 
 }  // namespace df2

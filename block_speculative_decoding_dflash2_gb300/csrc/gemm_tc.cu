@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   int* li_s = reinterpret_cast<int*>(lv_s + BN * KMAX);                              // [BN][KMAX]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_launch_next();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -160,16 +161,48 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
-      int stage = 0;
-      uint32_t phase = 0;
-      long issued = 0;
-      for (int u = blockIdx.x; u < a.units && !*abort_flag; u += gridDim.x) {
+      // this CTA's chunks, in order: units blockIdx.x, +gridDim.x, ...; each a K range
+      auto unit_range = [&](int u, int& k0, int& k1, int& mt, int& nt) {
         const int sp = u % a.splits, t = u / a.splits;
-        const int mt = t % a.m_tiles, nt = t / a.m_tiles;
-        const int k0 = (int)((long)sp * a.n_chunks / a.splits);
-        const int k1 = (int)((long)(sp + 1) * a.n_chunks / a.splits);
+        mt = t % a.m_tiles;
+        nt = t / a.m_tiles;
+        k0 = (int)((long)sp * a.n_chunks / a.splits);
+        k1 = (int)((long)(sp + 1) * a.n_chunks / a.splits);
+      };
+      int u = blockIdx.x, kc = 0, k1 = 0, mt = 0, nt = 0;
+      if (u < a.units) unit_range(u, kc, k1, mt, nt);
+      // 1. weight tiles of the first ring's worth of chunks, before waiting for
+      //    the previous kernel (no kernel on the stream writes the weights)
+      int pre = 0;
+      {
+        int uu = u, kk = kc, kk1 = k1, mm = mt, nn = nt;
+        while (pre < STAGES && uu < a.units) {
+          mbar_arrive_expect_tx(full + pre, A_BYTES + B_BYTES);
+          tma_load_2d(stA + pre * A_BYTES, &tmA, full + pre, kk * BK, mm * BM, pol_w);
+          ++pre;
+          if (++kk == kk1) {
+            uu += gridDim.x;
+            if (uu < a.units) unit_range(uu, kk, kk1, mm, nn);
+          }
+        }
+      }
+      pdl_wait();
+      // 2. the activation tiles of those chunks
+      long issued = 0;
+      for (int i = 0; i < pre; ++i) {
+        tma_load_2d(stB + i * B_BYTES, &tmB, full + i, kc * BK, nt * BN, pol_x);
+        ++issued;
+        if (++kc == k1) {
+          u += gridDim.x;
+          if (u < a.units) unit_range(u, kc, k1, mt, nt);
+        }
+      }
+      int stage = pre % STAGES;
+      uint32_t phase = pre == STAGES ? 1u : 0u;
+      // 3. steady state
+      while (u < a.units && !*abort_flag) {
         bool ok = true;
-        for (int kc = k0; kc < k1; ++kc) {
+        for (; kc < k1; ++kc) {
           if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, WAIT_NS)) {
             fail();
             ok = false;
@@ -185,6 +218,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
         if (!ok) break;
+        u += gridDim.x;
+        if (u < a.units) unit_range(u, kc, k1, mt, nt);
       }
       if (*abort_flag) {
         // wait (bounded) for every copy this thread issued to land
@@ -244,6 +279,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    pdl_wait();  // outputs, partials and counters may still be in use by the previous kernel
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
     const int ew = warp - 2;
@@ -465,25 +501,25 @@ int launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs& args, 
       return DFLASH2_ERR_CUDA;
     attr_set = true;
   }
-  tc_gemm_kernel<BN, TOPK><<<grid, THREADS, smem, st>>>(ma, mb, args);
-  count_launch();
-  return cudaGetLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+  return launch_k(tc_gemm_kernel<BN, TOPK>, dim3(grid), dim3(THREADS), smem, st, ma, mb, args);
 }
 
 }  // namespace
 
 // K splits: about one wave of units over the SMs, but at least 8 K chunks per
 // unit (so a unit's epilogue -- partial store, fence, arrival count -- hides
-// behind the next unit's stream) and fp32 partials (s*N*M*4 bytes) below half
-// the weight bytes (M*K*2).
+// behind the next unit's stream) and fp32 partials (s*N*M*4 bytes) at most a
+// quarter of the weight bytes (M*K*2).
 int gemm_splits(int M, int N, int K, int nsm, bool topk) {
   if (topk || N > 256) return 1;  // many activation rows: enough tiles without splitting K
   const long base = gemm_tiles(M, N);
   const int chunks = (K + BK - 1) / BK;
+  // enough tiles to keep most SMs streaming: no split (measured: splitting a
+  // 192-tile contraction 3 or 4 ways is slower than its uneven last wave)
   if (2 * base >= nsm) return 1;
   long s = nsm / base;
   s = std::min<long>(s, chunks / 8);
-  s = std::min<long>(s, K / (4 * N));
+  s = std::min<long>(s, K / (8 * N));
   return (int)std::max<long>(1, std::min<long>(s, 64));
 }
 

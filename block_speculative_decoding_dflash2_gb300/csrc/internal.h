@@ -50,6 +50,28 @@ constexpr int kMaxSM = 256;
 // Host-side count of kernel launches (instrumentation).
 void count_launch(int n = 1);
 
+// Launches `kern` with programmatic stream serialization: it may start while
+// the previous kernel of the stream drains.  Every kernel of this library
+// calls pdl_wait() (griddepcontrol.wait) before it touches memory that an
+// earlier kernel writes, so only prologues (and, in the GEMM, the weight
+// stream, which nothing on the stream writes) overlap.  Counts the launch.
+template <typename... KArgs, typename... Args>
+inline int launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                    Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  count_launch();
+  return cudaLaunchKernelEx(&cfg, kern, args...) == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+}
+
 // Byte offsets in the workspace of the draft step's intermediates
 // {f, h, u, u2, q, kb, vb, O, act, hn} for a call of these sizes (test hook).
 int workspace_offsets(const dflash2_config* c, int batch, int n_new, int max_ctx, size_t* out, int n);

@@ -33,6 +33,8 @@ __global__ void __launch_bounds__(256) sel_gather_kernel(const int32_t* __restri
                                                          const int32_t* __restrict__ cand_id, int D, int k,
                                                          const T* __restrict__ E, int V, int H, T* __restrict__ x,
                                                          unsigned* status) {
+  pdl_launch_next();
+  pdl_wait();
   const int r = blockIdx.x;
   const int nt = D * k + 1;
   const int s = r / nt, t = r % nt;
@@ -52,6 +54,8 @@ __global__ void __launch_bounds__(256) viterbi_kernel(const float* __restrict__ 
                                                       const float* __restrict__ cand_logit, int D, int k, int r,
                                                       int32_t* __restrict__ path, float* __restrict__ path_score) {
   extern __shared__ float sm[];
+  pdl_launch_next();
+  pdl_wait();
   const int s = blockIdx.x;
   const int nt = D * k + 1, w = 2 * r, ws = w + 1;  // padded row stride: no bank conflicts across candidates
   float* F = sm;                               // [nt][ws] factors: A = F[t][0:r], Bf = F[t][r:2r]
@@ -64,11 +68,23 @@ __global__ void __launch_bounds__(256) viterbi_kernel(const float* __restrict__ 
 
   const float2* y = reinterpret_cast<const float2*>(Y + (size_t)s * nt * w);
   const int w2 = w / 2;
-  for (int idx = threadIdx.x; idx < nt * w2; idx += blockDim.x) {
-    const int t = idx / w2, c = (idx - t * w2) * 2;
-    const float2 v = y[idx];
-    F[t * ws + c] = v.x;
-    F[t * ws + c + 1] = v.y;
+  constexpr int U = 8;  // loads in flight per thread
+  for (int base = threadIdx.x; base < nt * w2; base += blockDim.x * U) {
+    float2 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int idx = base + u * blockDim.x;
+      if (idx < nt * w2) v[u] = y[idx];
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int idx = base + u * blockDim.x;
+      if (idx < nt * w2) {
+        const int t = idx / w2, c = (idx - t * w2) * 2;
+        F[t * ws + c] = v[u].x;
+        F[t * ws + c + 1] = v[u].y;
+      }
+    }
   }
   for (int idx = threadIdx.x; idx < D * k; idx += blockDim.x) {
     zs[idx] = cand_logit[(size_t)s * D * k + idx];
@@ -153,13 +169,10 @@ int launch_sel_gather(int dtype, const int32_t* anchor, const int32_t* cand_id, 
                       const void* embed, int V, int H, void* x_out, const Ctx& c) {
   const int rows = batch * (D * k + 1);
   if (dtype == DFLASH2_BF16)
-    sel_gather_kernel<bf16><<<rows, 128, 0, c.stream>>>(anchor, cand_id, D, k, static_cast<const bf16*>(embed), V, H,
-                                                         static_cast<bf16*>(x_out), c.status);
-  else
-    sel_gather_kernel<float><<<rows, 128, 0, c.stream>>>(anchor, cand_id, D, k, static_cast<const float*>(embed), V,
-                                                          H, static_cast<float*>(x_out), c.status);
-  count_launch();
-  return cudaGetLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+    return launch_k(sel_gather_kernel<bf16>, dim3(rows), dim3(128), 0, c.stream, anchor, cand_id, D, k,
+                    static_cast<const bf16*>(embed), V, H, static_cast<bf16*>(x_out), c.status);
+  return launch_k(sel_gather_kernel<float>, dim3(rows), dim3(128), 0, c.stream, anchor, cand_id, D, k,
+                  static_cast<const float*>(embed), V, H, static_cast<float*>(x_out), c.status);
 }
 
 int launch_viterbi(const float* Y, const int32_t* cand_id, const float* cand_logit, int batch, int D, int k, int r,
@@ -171,9 +184,8 @@ int launch_viterbi(const float* Y, const int32_t* cand_id, const float* cand_log
       return DFLASH2_ERR_CUDA;
     attr = true;
   }
-  viterbi_kernel<<<batch, 256, smem, c.stream>>>(Y, cand_id, cand_logit, D, k, r, path, path_score);
-  count_launch();
-  return cudaGetLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+  return launch_k(viterbi_kernel, dim3(batch), dim3(256), smem, c.stream, Y, cand_id, cand_logit, D, k, r, path,
+                  path_score);
 }
 
 }  // namespace df2

@@ -26,6 +26,8 @@ int scan_chunks(int V) { return std::max(1, std::min(64, (V + 1023) / 1024)); }
 __global__ void __launch_bounds__(128) topk_scan_kernel(const float* __restrict__ logits, int rows, int V, int len,
                                                         float mult, float cap, float* __restrict__ debug,
                                                         float* __restrict__ lists_v, int* __restrict__ lists_i) {
+  pdl_launch_next();
+  pdl_wait();
   const int c = blockIdx.x, row = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int v0 = c * len, v1 = min(V, v0 + len);
@@ -84,14 +86,32 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(const float* __restrict
                                                          int k, int32_t* __restrict__ cand_id,
                                                          float* __restrict__ cand_logit) {
   extern __shared__ float mv[];
+  pdl_launch_next();
+  pdl_wait();
   int* mi = reinterpret_cast<int*>(mv + n_lists * KMAX);
   const int row = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  for (int idx = threadIdx.x; idx < n_lists * KMAX; idx += blockDim.x) {
-    const int l = idx / KMAX, e = idx % KMAX;
-    const size_t o = ((size_t)l * rows + row) * KMAX + e;
-    mv[idx] = lists_v[o];
-    mi[idx] = lists_i[o];
+  constexpr int U = 8;  // loads in flight per thread
+  for (int base = threadIdx.x; base < n_lists * KMAX; base += blockDim.x * U) {
+    float v[U];
+    int id[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int idx = base + u * blockDim.x;
+      if (idx < n_lists * KMAX) {
+        const size_t o = ((size_t)(idx / KMAX) * rows + row) * KMAX + idx % KMAX;
+        v[u] = lists_v[o];
+        id[u] = lists_i[o];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int idx = base + u * blockDim.x;
+      if (idx < n_lists * KMAX) {
+        mv[idx] = v[u];
+        mi[idx] = id[u];
+      }
+    }
   }
   __syncthreads();
   for (int stride = 1; stride < n_lists; stride *= 2) {
@@ -121,20 +141,17 @@ int launch_topk_scan(const float* logits, int rows, int V, float mult, float cap
                      int* lists_i, int* n_lists, const Ctx& c) {
   const int chunks = scan_chunks(V);
   const int len = (V + chunks - 1) / chunks;
-  dim3 grid(chunks, rows);
-  topk_scan_kernel<<<grid, 128, 0, c.stream>>>(logits, rows, V, len, mult, cap, debug, lists_v, lists_i);
   *n_lists = chunks * 4;
-  count_launch();
-  return cudaGetLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+  return launch_k(topk_scan_kernel, dim3(chunks, rows), dim3(128), 0, c.stream, logits, rows, V, len, mult, cap,
+                  debug, lists_v, lists_i);
 }
 
 int launch_topk_merge(const float* lists_v, const int* lists_i, int n_lists, int rows, int k, int32_t* cand_id,
                       float* cand_logit, const Ctx& c) {
   if (n_lists < 1 || n_lists > 256 || k > KMAX) return DFLASH2_ERR_SHAPE;
   const size_t smem = (size_t)n_lists * KMAX * 8;  // <= 32 KB
-  topk_merge_kernel<<<rows, 256, smem, c.stream>>>(lists_v, lists_i, n_lists, rows, k, cand_id, cand_logit);
-  count_launch();
-  return cudaGetLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+  return launch_k(topk_merge_kernel, dim3(rows), dim3(256), smem, c.stream, lists_v, lists_i, n_lists, rows, k,
+                  cand_id, cand_logit);
 }
 
 }  // namespace df2

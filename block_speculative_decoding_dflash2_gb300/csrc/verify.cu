@@ -20,6 +20,8 @@ __global__ void verify_kernel(int batch, int B, const int32_t* __restrict__ path
                               int32_t* __restrict__ accept_len, int32_t* __restrict__ out_tok,
                               int32_t* __restrict__ n_out, int32_t* __restrict__ next_anchor,
                               int32_t* __restrict__ seq_len, int64_t* __restrict__ counters) {
+  pdl_launch_next();
+  pdl_wait();
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= batch) return;
   const int D = B - 1;
@@ -49,10 +51,8 @@ int launch_verify(int batch, int B, const int32_t* path, const int32_t* target, 
                   int32_t* out_tok, int32_t* n_out, int32_t* next_anchor, int32_t* seq_len, int64_t* counters,
                   cudaStream_t st) {
   const int threads = 128;
-  verify_kernel<<<(batch + threads - 1) / threads, threads, 0, st>>>(batch, B, path, target, accept_len, out_tok,
-                                                                     n_out, next_anchor, seq_len, counters);
-  count_launch();
-  return cudaGetLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+  return launch_k(verify_kernel, dim3((batch + threads - 1) / threads), dim3(threads), 0, st, batch, B, path, target,
+                  accept_len, out_tok, n_out, next_anchor, seq_len, counters);
 }
 
 }  // namespace df2

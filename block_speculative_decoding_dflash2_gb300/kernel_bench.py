@@ -28,6 +28,7 @@ def main():
     p = argparse.ArgumentParser()
     p.add_argument("--kernel", default="lm_head", choices=sorted(SHAPES))
     p.add_argument("--launches", type=int, default=3)
+    p.add_argument("--splits", type=int, default=0, help="K splits (0: the library's choice)")
     a = p.parse_args()
     build()
     M, K, N = SHAPES[a.kernel]
@@ -43,8 +44,8 @@ def main():
         run = lambda: B.dflash2_test_gemm_topk(B.BF16, W, X, 16, 1.0, 0.0, cid, cz, None, ws)
     else:
         out = torch.empty((N, M), dtype=torch.float32, device="cuda")
-        ws = torch.zeros(B.dflash2_test_gemm_workspace(M, N, 0), dtype=torch.uint8, device="cuda")
-        run = lambda: B.dflash2_test_gemm(B.BF16, W, X, 0, out, ws)
+        ws = torch.zeros(B.dflash2_test_gemm_workspace(M, N, a.splits), dtype=torch.uint8, device="cuda")
+        run = lambda: B.dflash2_test_gemm(B.BF16, W, X, a.splits, out, ws)
     run()
     torch.cuda.synchronize()
     e0.record()
@@ -54,7 +55,8 @@ def main():
     e1.synchronize()
     ms = e0.elapsed_time(e1) / a.launches
     gb = M * K * 2 / 1e9
-    print(f"{a.kernel}: M={M} K={K} N={N}: {ms * 1e3:.1f} us per call, {gb / (ms / 1e3):.0f} GB/s of weights")
+    print(f"{a.kernel}: M={M} K={K} N={N} splits={a.splits}: {ms * 1e3:.1f} us per call, "
+          f"{gb / (ms / 1e3):.0f} GB/s of weights")
 
 
 if __name__ == "__main__":

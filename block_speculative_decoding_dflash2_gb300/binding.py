@@ -87,6 +87,9 @@ def lib():
         L.dflash2_test_gemm_workspace.argtypes = [I, I, I]
         L.dflash2_test_gemm.restype = I
         L.dflash2_test_gemm.argtypes = [I, P, I, I, P, I, I, I, P, P, S, P]
+        L.dflash2_select_path_static.restype = I
+        L.dflash2_select_path_static.argtypes = [F(Config), F(Weights), I, P, P, P, P, P, P]
+        L.dflash2_select_path_static_capacity.restype = S
         L.dflash2_test_layout.restype = I
         L.dflash2_test_layout.argtypes = [F(Config), I, I, I, F(ctypes.c_size_t), I]
         L.dflash2_launch_count.restype = ctypes.c_int64
@@ -254,3 +257,15 @@ def dflash2_set_stage_events(events):
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     lib().dflash2_set_stage_events(ctypes.cast(arr, ctypes.c_void_p))
     return arr
+
+
+def dflash2_select_path_static(cfg, w, batch, anchor, cand_id, cand_logit, path, path_score, stream=None):
+    """dflash2_select_path for callers that cannot allocate device memory: the
+    library's own fixed scratch array replaces the workspace (see the header)."""
+    return _check("dflash2_select_path_static", lib().dflash2_select_path_static(
+        ctypes.byref(cfg), ctypes.byref(w.struct), batch, _ptr(anchor), _ptr(cand_id), _ptr(cand_logit),
+        _ptr(path), _ptr(path_score), _stream(stream)))
+
+
+def dflash2_select_path_static_capacity():
+    return lib().dflash2_select_path_static_capacity()

@@ -17,7 +17,7 @@ OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdflash2.so")
 
 SOURCES = ["api.cu", "gemm_tc.cu", "gemm_simt.cu", "elementwise.cu", "attention.cu",
-           "topk.cu", "selector.cu", "verify.cu", "testing.cu"]
+           "topk.cu", "selector.cu", "verify.cu", "testing.cu", "select_static.cu"]
 HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "internal.h"),
            os.path.join(ROOT, "include", "dflash2.h"), os.path.join(ROOT, "include", "dflash2_testing.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -240,6 +240,36 @@ int dflash2_select_path(const dflash2_config *cfg, const dflash2_weights *w,
                         void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * dflash2_select_path without a workspace, for callers that cannot allocate
+ * device memory: code running inside a custom device allocator's callbacks,
+ * or inside a host runtime or plugin interface that owns all device memory
+ * and hands the library only its inputs and outputs.  The pages have no
+ * counterpart of this entry point; it exists only for such callers.
+ *
+ * Same arguments, results and status codes as dflash2_select_path, minus the
+ * workspace.  Its scratch is one fixed device array inside the library
+ * (dflash2_select_path_static_capacity() bytes, 8 MiB), which every GPU that
+ * loads the library keeps until the process exits.  A call whose batch needs
+ * more scratch than that returns DFLASH2_ERR_WORKSPACE without launching
+ * anything (at the Qwen3-8B selector shape, hidden 4096, 7 drafts, top-16,
+ * rank 64, the limit is 8 sequences per call).  The call allocates nothing
+ * and calls no allocating library routine.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before capturing a stream into a CUDA graph.  All calls share the one
+ * array: calls that overlap on the GPU (different streams or threads) race
+ * and must not be issued; calls ordered on one stream are safe.  Each call
+ * clears the part of the array that must start at zero.
+ */
+int dflash2_select_path_static(const dflash2_config *cfg, const dflash2_weights *w, int batch,
+                               const int32_t *anchor, const int32_t *cand_id, const float *cand_logit,
+                               int32_t *path, float *path_score, void *stream);
+
+/* Bytes of the fixed scratch array dflash2_select_path_static uses. */
+size_t dflash2_select_path_static_capacity(void);
+
+/*
  * Stage (d2): greedy verification ("Prerequisites": the target verifies
  * [id_last, draft...] in one batch; "Validation": output token ids equal
  * plain greedy decoding).

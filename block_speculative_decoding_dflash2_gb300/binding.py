@@ -84,7 +84,7 @@ def lib():
         L.dflash2_read_device_status.restype = I
         L.dflash2_read_device_status.argtypes = [P, S, P]
         L.dflash2_test_gemm_workspace.restype = S
-        L.dflash2_test_gemm_workspace.argtypes = [I, I, I]
+        L.dflash2_test_gemm_workspace.argtypes = [I, I]
         L.dflash2_test_gemm.restype = I
         L.dflash2_test_gemm.argtypes = [I, P, I, I, P, I, I, I, P, P, S, P]
         L.dflash2_select_path_static.restype = I
@@ -212,14 +212,16 @@ def dflash2_read_device_status(workspace, stream=None):
 # (include/dflash2_testing.h: the internal contraction and the lm_head top-k
 # path on their own, for parity tests)
 
-def dflash2_test_gemm_workspace(M, N, splits):
-    return lib().dflash2_test_gemm_workspace(M, N, splits)
+def dflash2_test_gemm_workspace(M, N):
+    return lib().dflash2_test_gemm_workspace(M, N)
 
 
-def dflash2_test_gemm(dtype, W, X, splits, out, workspace, accumulate=False, stream=None):
+def dflash2_test_gemm(dtype, W, X, ctas, out, workspace, accumulate=False, stream=None):
+    """ctas: 0 = the library's schedule, > 0 = stream-K over that many CTAs,
+    < 0 = whole tiles.  Returns the CTA count launched."""
     M, K = W.shape
     N = X.shape[0]
-    rc = lib().dflash2_test_gemm(dtype, _ptr(W), M, K, _ptr(X), N, splits, int(accumulate), _ptr(out),
+    rc = lib().dflash2_test_gemm(dtype, _ptr(W), M, K, _ptr(X), N, ctas, int(accumulate), _ptr(out),
                                  _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     if rc < 0:
         _check("dflash2_test_gemm", rc)
@@ -239,10 +241,11 @@ def dflash2_test_gemm_topk(dtype, W, X, k, mult, cap, cand_id, cand_logit, debug
 
 
 def dflash2_test_layout(cfg, batch, n_new, max_ctx):
-    """Workspace byte offsets of {f, h, u, u2, q, kb, vb, O, act, hn, ua, u2a}."""
-    out = (ctypes.c_size_t * 12)()
-    _check("dflash2_test_layout", lib().dflash2_test_layout(ctypes.byref(cfg), batch, n_new, max_ctx, out, 12))
-    return dict(zip(("f", "h", "u", "u2", "q", "kb", "vb", "O", "act", "hn", "ua", "u2a"), list(out)))
+    """Workspace byte offsets of {f, h, u, u2, q, kb, vb, O, act, hn, ua, u2a, cnt, cnta}."""
+    out = (ctypes.c_size_t * 14)()
+    _check("dflash2_test_layout", lib().dflash2_test_layout(ctypes.byref(cfg), batch, n_new, max_ctx, out, 14))
+    return dict(zip(("f", "h", "u", "u2", "q", "kb", "vb", "O", "act", "hn", "ua", "u2a", "cnt", "cnta"),
+                    list(out)))
 
 
 def dflash2_launch_count():

@@ -14,8 +14,6 @@
 #include <algorithm>
 #include <atomic>
 #include <cstring>
-#include <map>
-#include <tuple>
 #include <mutex>
 
 #include "common.cuh"
@@ -78,31 +76,9 @@ int check_config(const dflash2_config* c) {
   return DFLASH2_OK;
 }
 
-// Largest split-K partial buffer any contraction of a call can need, over
-// every SM count the library accepts.
-size_t partial_bound(int M, int N, int K) {
-  if (N <= 0) return 0;
-  static std::mutex mu;
-  static std::map<std::tuple<int, int, int>, size_t> memo;
-  {
-    std::lock_guard<std::mutex> g(mu);
-    auto it = memo.find(std::make_tuple(M, N, K));
-    if (it != memo.end()) return it->second;
-  }
-  size_t best = 0;
-  const int probes[2] = {std::min(N, 256), N};
-  for (int n : probes)
-    for (int nsm = 1; nsm <= kMaxSM; ++nsm) {
-      const int s = gemm_splits(M, n, K, nsm, false);
-      if (s > 1) best = std::max(best, (size_t)s * n * M * sizeof(float));
-    }
-  std::lock_guard<std::mutex> g(mu);
-  memo[std::make_tuple(M, N, K)] = best;
-  return best;
-}
-
 struct Layout {
-  size_t status, cnt, f, Y, P, h, u, u2, ua, u2a, q, kb, vb, attn, O, act, hn, logits, lv, li, selx, total;
+  size_t status, cnt, cnta, f, Y, P, Ya, Pa, h, u, u2, ua, u2a, q, kb, vb, attn, O, act, hn, logits, lv, li, selx,
+      total;
 };
 
 Layout plan(const dflash2_config& c, int batch, int n_new, int max_ctx) {
@@ -120,12 +96,16 @@ Layout plan(const dflash2_config& c, int batch, int n_new, int max_ctx) {
                            {2 * G, rows, H, true},              {(nq + 2 * nkv) * d, rows, H, true},
                            {H, rows, nq * d, false},            {2 * I, rows, H, true},
                            {H, rows, I, false},                 {2 * r, nsel, H, true}};
-  size_t P = 0, Yb = 0, tiles = 0;
-  for (const Shape& sh : shapes) {
+  // the append branch (shapes 0-1) runs concurrently with the block branch
+  // (shapes 2-7), so each has its own output, partial and counter regions
+  size_t P = 0, Yb = 0, Pa = 0, Yba = 0;
+  for (int i = 0; i < 8; ++i) {
+    const Shape& sh = shapes[i];
     if (sh.N <= 0) continue;
-    P = std::max(P, partial_bound(sh.M, sh.N, sh.K));
-    if (sh.y) Yb = std::max(Yb, (size_t)sh.N * sh.M * sizeof(float));
-    tiles = std::max(tiles, (size_t)gemm_tiles(sh.M, sh.N));
+    size_t& p = i < 2 ? Pa : P;
+    size_t& y = i < 2 ? Yba : Yb;
+    p = std::max(p, c.dtype == DFLASH2_BF16 ? gemm_partial_bytes(sh.M, sh.N) : 0);
+    if (sh.y) y = std::max(y, (size_t)sh.N * sh.M * sizeof(float));
   }
   const int n_lists = std::max(kMaxSM, topk_scan_lists(c.vocab));
   Layout L;
@@ -135,11 +115,16 @@ Layout plan(const dflash2_config& c, int batch, int n_new, int max_ctx) {
     o += al(bytes);
     return at;
   };
+  // the status word and both counter arrays sit at the same offsets for every
+  // call and size, so counters left at zero by one call are zero for the next
   L.status = take(256);
-  L.cnt = take(tiles * sizeof(int));
+  L.cnt = take(kMaxSM * sizeof(int));
+  L.cnta = take(kMaxSM * sizeof(int));
   L.f = take((size_t)n_new * H * es);
   L.Y = take(Yb);
   L.P = take(P);
+  L.Ya = take(Yba);
+  L.Pa = take(Pa);
   L.h = take((size_t)rows * H * 4);
   L.u = take((size_t)rows * H * es);
   L.u2 = take((size_t)rows * H * es);
@@ -186,6 +171,32 @@ int device_ctx(Ctx* ctx, void* stream, void* ws) {
   return DFLASH2_OK;
 }
 
+// Per-device side stream and fork/join events of the draft step (created on
+// first use; the enqueue of one draft step holds g_side_mu).
+struct SideStream {
+  cudaStream_t s;
+  cudaEvent_t fork, join;
+};
+std::mutex g_side_mu;
+
+int side_stream(SideStream* out) {
+  static SideStream per_dev[64];
+  static bool made[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DFLASH2_ERR_CUDA;
+  if (!made[dev]) {
+    SideStream sd;
+    if (cudaStreamCreateWithFlags(&sd.s, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming) != cudaSuccess)
+      return DFLASH2_ERR_CUDA;
+    per_dev[dev] = sd;
+    made[dev] = true;
+  }
+  *out = per_dev[dev];
+  return DFLASH2_OK;
+}
+
 #define TRY(x)                    \
   do {                            \
     const int rc_ = (x);          \
@@ -198,9 +209,10 @@ P* at(void* ws, size_t off) {
 }
 
 // out[n][m] (= or +=) sum_k W[m][k] X[n][k]; split-K partials and tile
-// counters live in the workspace regions of L.
+// counters live in the workspace regions of L (the append branch's own
+// regions when `append_branch`, since it runs concurrently with the block).
 int gemm(const dflash2_config& c, const Ctx& ctx, void* ws, const Layout& L, const void* W, int M, int K,
-         const void* X, int N, float* out, bool accumulate) {
+         const void* X, int N, float* out, bool accumulate, bool append_branch = false) {
   GemmOp g;
   std::memset(&g, 0, sizeof(g));
   g.W = W;
@@ -212,14 +224,10 @@ int gemm(const dflash2_config& c, const Ctx& ctx, void* ws, const Layout& L, con
   g.ldx = K;
   g.out = out;
   g.accumulate = accumulate;
-  g.partial = reinterpret_cast<float*>(static_cast<char*>(ws) + L.P);
-  g.counters = reinterpret_cast<int*>(static_cast<char*>(ws) + L.cnt);
+  g.partial = reinterpret_cast<float*>(static_cast<char*>(ws) + (append_branch ? L.Pa : L.P));
+  g.counters = reinterpret_cast<int*>(static_cast<char*>(ws) + (append_branch ? L.cnta : L.cnt));
   g.mult = 1.f;
-  if (c.dtype == DFLASH2_BF16) {
-    g.splits = gemm_splits(M, N, K, ctx.nsm, false);
-    return gemm_bf16(g, ctx);
-  }
-  g.splits = 1;
+  if (c.dtype == DFLASH2_BF16) return gemm_bf16(g, ctx);
   return gemm_f32(g, ctx);
 }
 
@@ -245,19 +253,22 @@ int run_append(const dflash2_config& c, const dflash2_weights& w, void* kc, void
                const void* taps, const int32_t* new_off, void* ws, const Layout& L, const Ctx& ctx) {
   if (n_new == 0) return DFLASH2_OK;
   const int H = c.hidden, nq = c.n_q_heads, nkv = c.n_kv_heads, d = c.head_dim;
-  float* Y = at<float>(ws, L.Y);
+  float* Y = at<float>(ws, L.Ya);
   void* f = at<char>(ws, L.f);
-  TRY(gemm(c, ctx, ws, L, w.fc, H, c.n_taps * H, taps, n_new, Y, false));
-  TRY(launch_rows_feature_norm(c.dtype, Y, n_new, H, w.hidden_norm, c.rms_eps, f, ctx));
+  // the first launch keeps the caller's ctx.pdl (false right after a fork)
+  TRY(gemm(c, ctx, ws, L, w.fc, H, c.n_taps * H, taps, n_new, Y, false, true));
+  Ctx rest = ctx;
+  rest.pdl = true;
+  TRY(launch_rows_feature_norm(c.dtype, Y, n_new, H, w.hidden_norm, c.rms_eps, f, rest));
   const size_t layer_elems = (size_t)n_pages * c.page_size * nkv * d;
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash2_layer_weights& Lw = w.layers[l];
     const void* wkv = elem_ptr(Lw.qkv, (size_t)nq * d * H, c.dtype);
-    TRY(gemm(c, ctx, ws, L, wkv, 2 * nkv * d, H, f, n_new, Y, false));
+    TRY(gemm(c, rest, ws, L, wkv, 2 * nkv * d, H, f, n_new, Y, false, true));
     TRY(launch_kv_append(c.dtype, Y, n_new, nkv, d, Lw.k_norm, c.rms_eps, c.rope_theta, ctx_len, new_off, batch,
                          block_table, max_pages, c.page_size, n_pages,
                          const_cast<char*>(elem_ptr(kc, l * layer_elems, c.dtype)),
-                         const_cast<char*>(elem_ptr(vc, l * layer_elems, c.dtype)), ctx));
+                         const_cast<char*>(elem_ptr(vc, l * layer_elems, c.dtype)), rest));
   }
   return DFLASH2_OK;
 }
@@ -276,10 +287,10 @@ void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
 int workspace_offsets(const dflash2_config* c, int batch, int n_new, int max_ctx, size_t* out, int n) {
   if (check_config(c) != DFLASH2_OK) return DFLASH2_ERR_SHAPE;
-  if (!out || n < 12) return DFLASH2_ERR_INVALID_ARG;
+  if (!out || n < 14) return DFLASH2_ERR_INVALID_ARG;
   const Layout L = plan(*c, batch, n_new, max_ctx);
-  const size_t v[12] = {L.f, L.h, L.u, L.u2, L.q, L.kb, L.vb, L.O, L.act, L.hn, L.ua, L.u2a};
-  for (int i = 0; i < 12; ++i) out[i] = v[i];
+  const size_t v[14] = {L.f, L.h, L.u, L.u2, L.q, L.kb, L.vb, L.O, L.act, L.hn, L.ua, L.u2a, L.cnt, L.cnta};
+  for (int i = 0; i < 14; ++i) out[i] = v[i];
   return DFLASH2_OK;
 }
 
@@ -357,10 +368,27 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
   Ctx ctx;
   TRY(device_ctx(&ctx, stream, workspace));
 
+  // Stage (a) does not feed the block until its attention: run it on the
+  // device's side stream, forked from and joined back into the caller's
+  // stream (event edges, so graph capture records two parallel branches).
+  std::lock_guard<std::mutex> side_lock(g_side_mu);
+  SideStream side;
+  TRY(side_stream(&side));
+  const bool forked = n_new > 0;
   TRY(stage_event(0, ctx.stream));
-  TRY(run_append(c, *w, k_cache, v_cache, n_pages, block_table, max_pages, batch, ctx_len, n_new, new_taps, new_off,
-                 workspace, L, ctx));
-  TRY(stage_event(1, ctx.stream));
+  if (forked) {
+    if (cudaEventRecord(side.fork, ctx.stream) != cudaSuccess || cudaStreamWaitEvent(side.s, side.fork, 0) != cudaSuccess)
+      return DFLASH2_ERR_CUDA;
+    Ctx actx = ctx;
+    actx.stream = side.s;
+    actx.pdl = false;  // full dependency on the fork event
+    TRY(run_append(c, *w, k_cache, v_cache, n_pages, block_table, max_pages, batch, ctx_len, n_new, new_taps,
+                   new_off, workspace, L, actx));
+    TRY(stage_event(1, side.s));
+    if (cudaEventRecord(side.join, side.s) != cudaSuccess) return DFLASH2_ERR_CUDA;
+  } else {
+    TRY(stage_event(1, ctx.stream));
+  }
 
   const int H = c.hidden, B = c.block_size, D = B - 1, nq = c.n_q_heads, nkv = c.n_kv_heads, d = c.head_dim;
   const int I = c.intermediate, G = H / c.conv_group_size, rows = batch * B;
@@ -379,32 +407,55 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
   const size_t layer_elems = (size_t)n_pages * c.page_size * nkv * d;
   void* ws = workspace;
 
-  TRY(launch_embed_norm(c.dtype, anchor, c.mask_token_id, batch, B, w->embed, c.vocab, H, c.input_embedding_scale,
-                        w->layers[0].attn_norm, c.rms_eps, h, ua, ctx));
+  // sublayer prologues: one fused kernel (norm, tap logits, conv) when the
+  // sequence's B rows fit its shared memory, else norm + tap GEMM + conv
+  const bool fused = conv_prologue_fits(c.dtype, batch, B, H, G, ctx.nsm);
+  if (fused)
+    TRY(launch_conv_prologue(c.dtype, nullptr, anchor, c.mask_token_id, w->embed, c.vocab, c.input_embedding_scale,
+                             w->layers[0].attn_norm, c.rms_eps, w->layers[0].tapgen_attn, batch, B, H,
+                             c.conv_group_size, h, ua, u2a, ctx));
+  else
+    TRY(launch_embed_norm(c.dtype, anchor, c.mask_token_id, batch, B, w->embed, c.vocab, H, c.input_embedding_scale,
+                          w->layers[0].attn_norm, c.rms_eps, h, ua, ctx));
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash2_layer_weights& Lw = w->layers[l];
     // attention sublayer: conv around the normed input, QKV, attention, O (+= residual)
-    TRY(gemm(c, ctx, ws, L, Lw.tapgen_attn, 2 * G, H, ua, rows, Y, false));
-    TRY(launch_dyn_conv(c.dtype, ua, Y, rows, H, c.conv_group_size, B, u2a, ctx));
+    if (fused) {
+      if (l > 0)
+        TRY(launch_conv_prologue(c.dtype, h, nullptr, 0, w->embed, c.vocab, 1.f, Lw.attn_norm, c.rms_eps,
+                                 Lw.tapgen_attn, batch, B, H, c.conv_group_size, nullptr, ua, u2a, ctx));
+    } else {
+      if (l > 0) TRY(launch_rownorm(c.dtype, h, rows, H, Lw.attn_norm, c.rms_eps, ua, B, 0, ctx));
+      TRY(gemm(c, ctx, ws, L, Lw.tapgen_attn, 2 * G, H, ua, rows, Y, false));
+      TRY(launch_dyn_conv(c.dtype, ua, Y, rows, H, c.conv_group_size, B, u2a, ctx));
+    }
     TRY(gemm(c, ctx, ws, L, Lw.qkv, (nq + 2 * nkv) * d, H, u2a, rows, Y, false));
     TRY(launch_qkv_epilogue(c.dtype, Y, rows, B, nq, nkv, d, Lw.q_norm, Lw.k_norm, c.rms_eps, c.rope_theta, ctx_len,
                             new_off, q, kb, vb, ctx));
+    // the attention reads the appended K/V: a full dependency on the join
+    Ctx jctx = ctx;
+    if (forked && l == 0) {
+      if (cudaStreamWaitEvent(ctx.stream, side.join, 0) != cudaSuccess) return DFLASH2_ERR_CUDA;
+      jctx.pdl = false;
+    }
     TRY(launch_attention(c.dtype, q, kb, vb, elem_ptr(k_cache, l * layer_elems, c.dtype),
                          elem_ptr(v_cache, l * layer_elems, c.dtype), block_table, max_pages, c.page_size, n_pages,
-                         ctx_len, new_off, batch, B, nq, nkv, d, max_ctx, at<float>(workspace, L.attn), O, ctx));
+                         ctx_len, new_off, batch, B, nq, nkv, d, max_ctx, at<float>(workspace, L.attn), O, jctx));
     TRY(gemm(c, ctx, ws, L, Lw.o, H, nq * d, O, rows, h, true));
-    TRY(launch_rownorm(c.dtype, h, rows, H, Lw.mlp_norm, c.rms_eps, u, B, 0, ctx));
     // MLP sublayer: conv around the normed input, gate/up, SiLU*up, down (+= residual)
-    TRY(gemm(c, ctx, ws, L, Lw.tapgen_mlp, 2 * G, H, u, rows, Y, false));
-    TRY(launch_dyn_conv(c.dtype, u, Y, rows, H, c.conv_group_size, B, u2, ctx));
+    if (fused) {
+      TRY(launch_conv_prologue(c.dtype, h, nullptr, 0, w->embed, c.vocab, 1.f, Lw.mlp_norm, c.rms_eps, Lw.tapgen_mlp,
+                               batch, B, H, c.conv_group_size, nullptr, u, u2, ctx));
+    } else {
+      TRY(launch_rownorm(c.dtype, h, rows, H, Lw.mlp_norm, c.rms_eps, u, B, 0, ctx));
+      TRY(gemm(c, ctx, ws, L, Lw.tapgen_mlp, 2 * G, H, u, rows, Y, false));
+      TRY(launch_dyn_conv(c.dtype, u, Y, rows, H, c.conv_group_size, B, u2, ctx));
+    }
     TRY(gemm(c, ctx, ws, L, Lw.gate_up, 2 * I, H, u2, rows, Y, false));
     TRY(launch_act(c.dtype, Y, rows, I, act, ctx));
     TRY(gemm(c, ctx, ws, L, Lw.down, H, I, act, rows, h, true));
-    if (l + 1 < c.n_layers)
-      TRY(launch_rownorm(c.dtype, h, rows, H, w->layers[l + 1].attn_norm, c.rms_eps, ua, B, 0, ctx));
-    else
-      TRY(launch_rownorm(c.dtype, h, rows, H, w->final_norm, c.rms_eps, hn, B, 1, ctx));
   }
+  TRY(launch_rownorm(c.dtype, h, rows, H, w->final_norm, c.rms_eps, hn, B, 1, ctx));
 
   TRY(stage_event(2, ctx.stream));
   // (c) lm_head over block positions 1..B-1 with the streaming top-k
@@ -422,7 +473,6 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
     g.X = hn;
     g.N = nrow;
     g.ldx = H;
-    g.splits = 1;
     g.topk = true;
     g.lists_v = lv;
     g.lists_i = li;

@@ -192,11 +192,22 @@ __global__ void __launch_bounds__(AT) attn_partial_kernel(
 }
 
 // ------------------------------------------------------------------------
-// bf16 path on the tensor cores (mma.sync m16n8k16, fp32 accumulation).
-// Same work split and partial format as attn_partial_kernel.  The CTA's
-// query rows form 16-row blocks; each warp owns one or two (row block, key
-// share) combinations with its own online-softmax state in registers.  For
-// every 16-key step: S = Q K^T (K rows read with ldmatrix as the col-major B
+// bf16 path: one thread-block cluster per (kv head, sequence).  The NS CTAs
+// of the cluster split the keys [0, P + B) into NS contiguous chunks.  Each
+// CTA runs a flash-attention pass over its chunk on the tensor cores
+// (mma.sync m16n8k16, fp32 accumulation), with its 64-key K/V tiles
+// double-buffered in shared memory by cp.async (one page lookup per key),
+// and leaves unnormalised partials (acc, running max, running sum) for the
+// grp*B query rows in shared memory.  After a cluster barrier every CTA
+// merges all partials of its share of the rows through distributed shared
+// memory and writes O: no partial goes to global memory and no second kernel
+// runs.
+//
+// Within a CTA the query rows form 16-row blocks and each tile's keys are cut
+// into ksplit shares; each of the 8 warps owns one or two (row block, key
+// share) combinations with its own online-softmax state in registers, and
+// each combination is one partial of the cluster-wide merge.  For every
+// 16-key step: S = Q K^T (K rows read with ldmatrix as the col-major B
 // operand), scale, mask, online softmax, then O += P V with P split into
 // bf16 hi + lo parts (two MMAs), so the probabilities keep ~16 bits.
 
@@ -225,64 +236,114 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-constexpr int MKT = 64;  // keys per shared-memory tile (mma path)
+constexpr int MKT = 64;         // keys per tile
+constexpr int KST = 2;          // K/V tile stages
+constexpr int kMaxCluster = 8;  // CTAs per cluster (portable limit)
+constexpr int CLW = 8;          // warps per CTA
+constexpr int CLT = 32 * CLW;   // threads: four per key of a tile
+constexpr int kMaxShares = 4;   // key shares per 16-row block (16 keys each per tile)
 
-template <int DH>
-size_t attn_mma_smem(int R) {
-  const int nrb = (R + 15) / 16;
-  const int ks = nrb >= 4 ? 1 : 4 / nrb;
-  return (size_t)(nrb * 16 + 2 * MKT) * (DH + 8) * 2 + (size_t)nrb * ks * 16 * (DH + 2) * 4 + MKT * 8;
+// Key shares per 16-row block: enough (row block, share) combinations to
+// give every warp one, each share at least 16 keys of a tile.
+__host__ __device__ inline int attn_ksplit(int nrb) {
+  const int k = nrb >= CLW ? 1 : CLW / nrb;
+  return k < kMaxShares ? k : kMaxShares;
 }
 
-// CPW: (row block, key share) combinations per warp (1 or 2), so the
+// Shared memory: Q rows, the K/V stages, the per-combination partial states
+// (read by the whole cluster), the merge weights of this CTA's rows.
+template <int DH>
+size_t attn_cl_smem(int R) {
+  const int nrb = (R + 15) / 16;
+  const size_t qb = (size_t)nrb * 16 * (DH + 8) * 2;
+  const size_t kvb = (size_t)KST * 2 * MKT * (DH + 8) * 2;
+  const size_t comb = (size_t)nrb * attn_ksplit(nrb) * 16 * (DH + 2) * 4;
+  return qb + kvb + comb + (size_t)(R + kMaxCluster) * kMaxShares * 4;
+}
+
+// MCPW: (row block, key share) combinations per warp (1 or 2), so the
 // register-resident accumulators are sized to what the launch needs.
 template <int DH, int MCPW>
-__global__ void __launch_bounds__(128) attn_mma_kernel(
+__global__ void __launch_bounds__(CLT) attn_cluster_kernel(
     const bf16* __restrict__ q, const bf16* __restrict__ kb, const bf16* __restrict__ vb, const bf16* __restrict__ kc,
     const bf16* __restrict__ vc, const int32_t* __restrict__ block_table, int max_pages, int page_size, int n_pages,
-    const int32_t* __restrict__ ctx_len, const int32_t* __restrict__ new_off, int B, int nq, int nkv, int CH,
-    int nsplit, float* __restrict__ part, unsigned* status) {
+    const int32_t* __restrict__ ctx_len, const int32_t* __restrict__ new_off, int B, int nq, int nkv,
+    bf16* __restrict__ o, unsigned* status) {
   constexpr int LD = DH + 8;  // padded smem row (elements): ldmatrix rows hit distinct banks
   constexpr int NT = DH / 8;  // n8 tiles across the head dimension
+  constexpr int C8 = DH / 8;  // 16-byte chunks per row
+  constexpr int FS = DH + 2;  // partial row: acc[DH], m, l
+  constexpr int TPK = CLT / MKT;  // threads per key in a tile load
+  constexpr int NPMAX = kMaxCluster * kMaxShares;
   extern __shared__ __align__(16) uint8_t smraw[];
   pdl_launch_next();
-  pdl_wait();
+  const int NS = gridDim.x;  // the cluster spans x
   const int sp = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
   const int grp = nq / nkv, R = grp * B;
   const int nrb = (R + 15) / 16;
-  const int ksplit = nrb >= 4 ? 1 : 4 / nrb;
+  const int ksplit = attn_ksplit(nrb);
   const int ncombo = nrb * ksplit;
+  const int np = NS * ksplit;  // partials per row across the cluster
   bf16* Qs = reinterpret_cast<bf16*>(smraw);
-  bf16* Ks = Qs + nrb * 16 * LD;
-  bf16* Vs = Ks + MKT * LD;
-  float* comb = reinterpret_cast<float*>(Vs + MKT * LD);  // [ncombo][16][DH + 2]
-  long long* koff = reinterpret_cast<long long*>(comb + (size_t)ncombo * 16 * (DH + 2));
+  bf16* KV = Qs + nrb * 16 * LD;                                      // [KST][K, V][MKT][LD]
+  float* comb = reinterpret_cast<float*>(KV + (size_t)KST * 2 * MKT * LD);  // [ncombo][16][FS]
+  float* wts = comb + (size_t)ncombo * 16 * FS;                       // [rows of this CTA][np]
 
+  pdl_wait();
   const int P = ctx_len[s] + (new_off[s + 1] - new_off[s]);
   const int L = P + B;
-  const int k0 = sp * CH, k1 = min(k0 + CH, L);
-  float* out = part + ((((size_t)s * nkv + g) * nsplit + sp) * R) * (DH + 2);
-  if (k0 >= L) {
-    for (int r = threadIdx.x; r < R; r += blockDim.x) {
-      out[(size_t)r * (DH + 2) + DH] = -INFINITY;
-      out[(size_t)r * (DH + 2) + DH + 1] = 0.f;
-    }
-    return;
-  }
+  const int CH = (((L + NS - 1) / NS) + 15) & ~15;
+  const int k0 = min(sp * CH, L), k1 = min(k0 + CH, L);
   if (P > max_pages * page_size && sp == 0 && threadIdx.x == 0) flag(status, DFLASH2_DEV_BAD_LENGTH);
   const float scale = rsqrtf((float)DH);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int C8 = DH / 8;
+
   // query rows (zero padding to whole 16-row blocks)
   for (int idx = threadIdx.x; idx < nrb * 16 * C8; idx += blockDim.x) {
     const int r = idx / C8, c = (idx % C8) * 8;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < R) {
-      const int i = r / grp, h = g * grp + r % grp;
-      v = *reinterpret_cast<const uint4*>(q + (((size_t)s * B + i) * nq + h) * DH + c);
-    }
-    *reinterpret_cast<uint4*>(Qs + r * LD + c) = v;
+    const bf16* src = q;
+    if (r < R) src = q + (((size_t)s * B + r / grp) * nq + g * grp + r % grp) * DH + c;
+    cp_async16(Qs + r * LD + c, src, r < R);
   }
+  // K/V rows of keys t0 .. t0 + MKT - 1 into stage stg; keys past k1, and
+  // keys whose page is invalid (flagged), read as zeros
+  auto issue = [&](int t0, int stg) {
+    bf16* Ks = KV + (size_t)stg * 2 * MKT * LD;
+    bf16* Vs = Ks + MKT * LD;
+    const int kk = threadIdx.x / TPK, part = threadIdx.x % TPK;
+    const int j = t0 + kk;
+    const bf16* ksrc = kc;
+    const bf16* vsrc = vc;
+    bool ok = false;
+    if (j < k1) {
+      if (j < P) {
+        const int pi = j / page_size;
+        const int page = pi < max_pages ? block_table[(size_t)s * max_pages + pi] : -1;
+        if (page >= 0 && page < n_pages) {
+          const size_t off = (((size_t)page * page_size + j % page_size) * nkv + g) * DH;
+          ksrc = kc + off;
+          vsrc = vc + off;
+          ok = true;
+        } else {
+          flag(status, DFLASH2_DEV_BAD_PAGE);
+        }
+      } else {
+        const size_t off = (((size_t)s * B + (j - P)) * nkv + g) * DH;
+        ksrc = kb + off;
+        vsrc = vb + off;
+        ok = true;
+      }
+    }
+#pragma unroll
+    for (int c = part * (C8 / TPK); c < (part + 1) * (C8 / TPK); ++c) {
+      cp_async16(Ks + kk * LD + c * 8, ok ? ksrc + c * 8 : kc, ok);
+      cp_async16(Vs + kk * LD + c * 8, ok ? vsrc + c * 8 : vc, ok);
+    }
+  };
+  const int ntiles = (k1 - k0 + MKT - 1) / MKT;  // 0 for an empty chunk
+  if (ntiles > 0) issue(k0, 0);
+  cp_async_commit();  // group 0: Q and tile 0
+
   // per-combination online-softmax state: rows lane/4 and lane/4 + 8 of the block
   float m_st[MCPW][2], l_st[MCPW][2], acc[MCPW][NT][4];
 #pragma unroll
@@ -292,45 +353,17 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(
 #pragma unroll
     for (int n = 0; n < NT; ++n) acc[c][n][0] = acc[c][n][1] = acc[c][n][2] = acc[c][n][3] = 0.f;
   }
-  constexpr long long BLOCK_BIT = 1LL << 62;
-  for (int t0 = k0; t0 < k1; t0 += MKT) {
-    const int nk = min(MKT, k1 - t0);
+  for (int t = 0; t < ntiles; ++t) {
+    if (t + 1 < ntiles) issue(k0 + (t + 1) * MKT, (t + 1) % KST);
+    cp_async_commit();
+    cp_async_wait<1>();  // all but the newest group have landed
     __syncthreads();
-    if (threadIdx.x < MKT) {
-      const int j = t0 + threadIdx.x;
-      long long o = -1;
-      if (threadIdx.x < nk) {
-        if (j < P) {
-          const int pi = j / page_size;
-          const int page = pi < max_pages ? block_table[(size_t)s * max_pages + pi] : -1;
-          if (page >= 0 && page < n_pages)
-            o = (((long long)page * page_size + j % page_size) * nkv + g) * DH;
-          else
-            flag(status, DFLASH2_DEV_BAD_PAGE);
-        } else {
-          o = BLOCK_BIT | ((((long long)s * B + (j - P)) * nkv + g) * DH);
-        }
-      }
-      koff[threadIdx.x] = o;
-    }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < MKT * C8; idx += blockDim.x) {
-      const int kk = idx / C8, c = (idx % C8) * 8;
-      const long long o = koff[kk];
-      uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);  // missing keys read as zeros
-      if (o >= 0) {
-        const bf16* ks_ = (o & BLOCK_BIT) ? kb + (o & ~BLOCK_BIT) : kc + o;
-        const bf16* vs_ = (o & BLOCK_BIT) ? vb + (o & ~BLOCK_BIT) : vc + o;
-        kv = *reinterpret_cast<const uint4*>(ks_ + c);
-        vv = *reinterpret_cast<const uint4*>(vs_ + c);
-      }
-      *reinterpret_cast<uint4*>(Ks + kk * LD + c) = kv;
-      *reinterpret_cast<uint4*>(Vs + kk * LD + c) = vv;
-    }
-    __syncthreads();
+    const bf16* Ks = KV + (size_t)(t % KST) * 2 * MKT * LD;
+    const bf16* Vs = Ks + MKT * LD;
+    const int nk = min(MKT, k1 - (k0 + t * MKT));
 #pragma unroll
     for (int slot = 0; slot < MCPW; ++slot) {
-      const int combo = warp + slot * 4;
+      const int combo = warp + slot * CLW;
       if (combo >= ncombo) break;
       const int rb = combo / ksplit, ks = combo % ksplit;
       const int kbeg = ks * (MKT / ksplit), kend = min(nk, (ks + 1) * (MKT / ksplit));
@@ -346,7 +379,7 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(
           mma16816(S0, a, bk[0], bk[1]);
           mma16816(S1, a, bk[2], bk[3]);
         }
-        // scale and mask keys past the chunk
+        // scale and mask keys past the share
         const int cbase = j0 + (lane & 3) * 2;
         float sv[8] = {S0[0], S0[1], S0[2], S0[3], S1[0], S1[1], S1[2], S1[3]};
 #pragma unroll
@@ -358,9 +391,9 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(
         float mx0 = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[4], sv[5]));
         float mx1 = fmaxf(fmaxf(sv[2], sv[3]), fmaxf(sv[6], sv[7]));
 #pragma unroll
-        for (int o = 1; o <= 2; o <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+        for (int o2 = 1; o2 <= 2; o2 <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
         }
         const float mn0 = fmaxf(m_st[slot][0], mx0), mn1 = fmaxf(m_st[slot][1], mx1);
         const float f0 = expf(m_st[slot][0] - mn0), f1 = expf(m_st[slot][1] - mn1);
@@ -371,9 +404,9 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(
         for (int e = 0; e < 8; ++e) p[e] = expf(sv[e] - ((e & 2) ? mn1 : mn0));
         float s0 = p[0] + p[1] + p[4] + p[5], s1 = p[2] + p[3] + p[6] + p[7];
 #pragma unroll
-        for (int o = 1; o <= 2; o <<= 1) {
-          s0 += __shfl_xor_sync(0xffffffffu, s0, o);
-          s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+        for (int o2 = 1; o2 <= 2; o2 <<= 1) {
+          s0 += __shfl_xor_sync(0xffffffffu, s0, o2);
+          s1 += __shfl_xor_sync(0xffffffffu, s1, o2);
         }
         l_st[slot][0] = l_st[slot][0] * f0 + s0;
         l_st[slot][1] = l_st[slot][1] * f1 + s1;
@@ -408,44 +441,83 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(
         }
       }
     }
+    __syncthreads();  // this stage is refilled two tiles later
   }
-  // each combination's state -> shared memory, then rows combine their key shares
+  cp_async_wait<0>();
+  // each combination's partial state -> shared memory (empty ones: m = -inf, l = 0)
 #pragma unroll
   for (int slot = 0; slot < MCPW; ++slot) {
-    const int combo = warp + slot * 4;
+    const int combo = warp + slot * CLW;
     if (combo >= ncombo) break;
-    float* cb = comb + (size_t)combo * 16 * (DH + 2);
+    float* cb = comb + (size_t)combo * 16 * FS;
     const int r0 = lane >> 2, c0 = (lane & 3) * 2;
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
-      cb[r0 * (DH + 2) + n * 8 + c0] = acc[slot][n][0];
-      cb[r0 * (DH + 2) + n * 8 + c0 + 1] = acc[slot][n][1];
-      cb[(r0 + 8) * (DH + 2) + n * 8 + c0] = acc[slot][n][2];
-      cb[(r0 + 8) * (DH + 2) + n * 8 + c0 + 1] = acc[slot][n][3];
+      cb[r0 * FS + n * 8 + c0] = acc[slot][n][0];
+      cb[r0 * FS + n * 8 + c0 + 1] = acc[slot][n][1];
+      cb[(r0 + 8) * FS + n * 8 + c0] = acc[slot][n][2];
+      cb[(r0 + 8) * FS + n * 8 + c0 + 1] = acc[slot][n][3];
     }
     if ((lane & 3) == 0) {
-      cb[r0 * (DH + 2) + DH] = m_st[slot][0];
-      cb[r0 * (DH + 2) + DH + 1] = l_st[slot][0];
-      cb[(r0 + 8) * (DH + 2) + DH] = m_st[slot][1];
-      cb[(r0 + 8) * (DH + 2) + DH + 1] = l_st[slot][1];
+      cb[r0 * FS + DH] = m_st[slot][0];
+      cb[r0 * FS + DH + 1] = l_st[slot][0];
+      cb[(r0 + 8) * FS + DH] = m_st[slot][1];
+      cb[(r0 + 8) * FS + DH + 1] = l_st[slot][1];
     }
+  }
+  cluster_sync();  // every CTA's partials are complete and visible to the cluster
+
+  // Row r's partials: CTA p (key chunk), share ks, in that order; the row's
+  // state in CTA p sits at comb[((r / 16) * ksplit + ks) * 16 + r % 16].
+  // This CTA merges rows r = sp, sp + NS, ...: weights e^(m - M) / den.
+  const int nmine = sp < R ? (R - sp + NS - 1) / NS : 0;
+  for (int mi = threadIdx.x; mi < nmine; mi += blockDim.x) {
+    const int r = sp + mi * NS;
+    const float* base = comb + ((size_t)(r / 16) * ksplit * 16 + r % 16) * FS + DH;
+    float2 ml[NPMAX];
+#pragma unroll
+    for (int i = 0; i < NPMAX; ++i)
+      if (i < np) ml[i] = ld_dsmem2(dsmem_addr(base + (size_t)(i % ksplit) * 16 * FS, i / ksplit));
+    float M = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < NPMAX; ++i)
+      if (i < np && ml[i].y > 0.f) M = fmaxf(M, ml[i].x);
+    float den = 0.f;
+#pragma unroll
+    for (int i = 0; i < NPMAX; ++i)
+      if (i < np) {
+        ml[i].x = ml[i].y > 0.f ? expf(ml[i].x - M) : 0.f;
+        den += ml[i].y * ml[i].x;
+      }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+    for (int i = 0; i < NPMAX; ++i)
+      if (i < np) wts[mi * np + i] = ml[i].x * inv;
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < R * (DH + 2); idx += blockDim.x) {
-    const int r = idx / (DH + 2), c = idx % (DH + 2);
-    const int rb = r / 16, rr = r % 16;
-    float M = -INFINITY;
-    for (int ks = 0; ks < ksplit; ++ks) {
-      const float* cb = comb + (size_t)(rb * ksplit + ks) * 16 * (DH + 2) + rr * (DH + 2);
-      if (cb[DH + 1] > 0.f) M = fmaxf(M, cb[DH]);
-    }
-    float v = 0.f;
-    for (int ks = 0; ks < ksplit; ++ks) {
-      const float* cb = comb + (size_t)(rb * ksplit + ks) * 16 * (DH + 2) + rr * (DH + 2);
-      if (cb[DH + 1] > 0.f) v += (c == DH ? 0.f : (c == DH + 1 ? cb[DH + 1] : cb[c])) * expf(cb[DH] - M);
-    }
-    out[(size_t)r * (DH + 2) + c] = c == DH ? M : v;
+  // O = sum over partials of acc * weight, two elements per thread
+  for (int idx = threadIdx.x; idx < nmine * (DH / 2); idx += blockDim.x) {
+    const int mi = idx / (DH / 2), c = (idx % (DH / 2)) * 2;
+    const int r = sp + mi * NS;
+    const float* base = comb + ((size_t)(r / 16) * ksplit * 16 + r % 16) * FS + c;
+    float2 v[NPMAX];
+#pragma unroll
+    for (int i = 0; i < NPMAX; ++i)
+      if (i < np) v[i] = ld_dsmem2(dsmem_addr(base + (size_t)(i % ksplit) * 16 * FS, i / ksplit));
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < NPMAX; ++i)
+      if (i < np) {
+        const float w = wts[mi * np + i];
+        if (w != 0.f) {
+          a0 += v[i].x * w;
+          a1 += v[i].y * w;
+        }
+      }
+    const int i = r / grp, h = g * grp + r % grp;
+    *reinterpret_cast<__nv_bfloat162*>(o + ((size_t)s * B + i) * nq * DH + h * DH + c) = __floats2bfloat162_rn(a0, a1);
   }
+  cluster_sync();  // the other CTAs may still be reading this CTA's partials
 }
 
 // O[s, i, h, :] = sum_chunks acc e^(m - M) / sum_chunks l e^(m - M).
@@ -541,15 +613,49 @@ size_t attn_part_bytes(int max_batch, int B, int nq, int nkv, int d, int max_ctx
   return best;
 }
 
+// CTAs per cluster: one per 64 keys of the longest sequence, at most 8.
+int attn_cluster_ctas(int max_ctx, int B) {
+  const long L = (long)max_ctx + B;
+  return (int)std::max(1L, std::min<long>(kMaxCluster, (L + MKT - 1) / MKT));
+}
+
 int launch_attention(int dtype, const void* q, const void* kb, const void* vb, const void* kc, const void* vc,
                      const int32_t* block_table, int max_pages, int page_size, int n_pages,
                      const int32_t* ctx_len, const int32_t* new_off, int batch, int B, int nq, int nkv, int d,
                      int max_ctx, float* part, void* o_out, const Ctx& c) {
+  const int R = (nq / nkv) * B;
+  const int nrb = (R + 15) / 16;
+  const int ncombo = nrb * attn_ksplit(nrb);
+  if (dtype == DFLASH2_BF16 && (d == 64 || d == 128) && ncombo <= 2 * CLW) {
+    static bool mattr = false;  // set once, before any capture
+    if (!mattr) {
+      const int mx = 200 * 1024;
+      if (cudaFuncSetAttribute(attn_cluster_kernel<64, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx) ||
+          cudaFuncSetAttribute(attn_cluster_kernel<64, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx) ||
+          cudaFuncSetAttribute(attn_cluster_kernel<128, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx) ||
+          cudaFuncSetAttribute(attn_cluster_kernel<128, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx))
+        return DFLASH2_ERR_CUDA;
+      mattr = true;
+    }
+    const size_t ms = d == 64 ? attn_cl_smem<64>(R) : attn_cl_smem<128>(R);
+    if (ms > 200 * 1024) return DFLASH2_ERR_SHAPE;
+    const int ns = attn_cluster_ctas(max_ctx, B);
+    const dim3 grid(ns, nkv, batch);
+    const bf16 *q_ = static_cast<const bf16*>(q), *kb_ = static_cast<const bf16*>(kb),
+               *vb_ = static_cast<const bf16*>(vb), *kc_ = static_cast<const bf16*>(kc),
+               *vc_ = static_cast<const bf16*>(vc);
+    bf16* o_ = static_cast<bf16*>(o_out);
+    auto kern = d == 64 ? (ncombo <= CLW ? attn_cluster_kernel<64, 1> : attn_cluster_kernel<64, 2>)
+                        : (ncombo <= CLW ? attn_cluster_kernel<128, 1> : attn_cluster_kernel<128, 2>);
+    return launch_kx(kern, grid, dim3(CLT), ms, c, ns, q_, kb_, vb_, kc_, vc_, block_table, max_pages, page_size,
+                     n_pages, ctx_len, new_off, B, nq, nkv, o_, c.status);
+  }
+  // SIMT path (fp32 storage, or row counts beyond the tensor-core kernel):
+  // key-chunk partials in global memory, then the combine kernel
   const int ch = chunk_of(max_ctx, B, batch, nkv, c.nsm);
   const int nsplit = (max_ctx + B + ch - 1) / ch;
-  const int R = (nq / nkv) * B;
   const size_t smem = attn_smem(R, d);
-  dim3 grid(nsplit, nkv, batch);
+  const dim3 grid(nsplit, nkv, batch);
   static bool attr = false;  // set once, before any capture, to the largest size the config check allows
   if (!attr) {
     if (cudaFuncSetAttribute(attn_partial_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
@@ -560,54 +666,27 @@ int launch_attention(int dtype, const void* q, const void* kb, const void* vb, c
     attr = true;
   }
   if (smem > 200 * 1024) return DFLASH2_ERR_SHAPE;
-  const int nrb = (R + 15) / 16;
-  const int ncombo = nrb * (nrb >= 4 ? 1 : 4 / nrb);
-  if (dtype == DFLASH2_BF16 && (d == 64 || d == 128) && ncombo <= 8) {
-    static bool mattr = false;
-    if (!mattr) {
-      const int mx = 200 * 1024;
-      if (cudaFuncSetAttribute(attn_mma_kernel<64, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx) ||
-          cudaFuncSetAttribute(attn_mma_kernel<64, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx) ||
-          cudaFuncSetAttribute(attn_mma_kernel<128, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx) ||
-          cudaFuncSetAttribute(attn_mma_kernel<128, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx))
-        return DFLASH2_ERR_CUDA;
-      mattr = true;
-    }
-    const size_t ms = d == 64 ? attn_mma_smem<64>(R) : attn_mma_smem<128>(R);
-    if (ms > 200 * 1024) return DFLASH2_ERR_SHAPE;
-    const bf16 *q_ = static_cast<const bf16*>(q), *kb_ = static_cast<const bf16*>(kb),
-               *vb_ = static_cast<const bf16*>(vb), *kc_ = static_cast<const bf16*>(kc),
-               *vc_ = static_cast<const bf16*>(vc);
-    int rc;
-    if (d == 64)
-      rc = launch_k(ncombo <= 4 ? attn_mma_kernel<64, 1> : attn_mma_kernel<64, 2>, grid, dim3(128), ms, c.stream,
-                    q_, kb_, vb_, kc_, vc_, block_table, max_pages, page_size, n_pages, ctx_len, new_off, B, nq, nkv,
-                    ch, nsplit, part, c.status);
-    else
-      rc = launch_k(ncombo <= 4 ? attn_mma_kernel<128, 1> : attn_mma_kernel<128, 2>, grid, dim3(128), ms,
-                    c.stream, q_, kb_, vb_, kc_, vc_, block_table, max_pages, page_size, n_pages, ctx_len, new_off,
-                    B, nq, nkv, ch, nsplit, part, c.status);
-    if (rc) return rc;
-  } else if (dtype == DFLASH2_BF16) {
-    const int rc = launch_k(attn_partial_kernel<bf16>, grid, dim3(AT), smem, c.stream, static_cast<const bf16*>(q),
-                            static_cast<const bf16*>(kb), static_cast<const bf16*>(vb), static_cast<const bf16*>(kc),
-                            static_cast<const bf16*>(vc), block_table, max_pages, page_size, n_pages, ctx_len,
-                            new_off, B, nq, nkv, d, ch, nsplit, part, c.status);
-    if (rc) return rc;
-  } else {
-    const int rc = launch_k(attn_partial_kernel<float>, grid, dim3(AT), smem, c.stream,
-                            static_cast<const float*>(q), static_cast<const float*>(kb), static_cast<const float*>(vb),
-                            static_cast<const float*>(kc), static_cast<const float*>(vc), block_table, max_pages,
-                            page_size, n_pages, ctx_len, new_off, B, nq, nkv, d, ch, nsplit, part, c.status);
-    if (rc) return rc;
-  }
+  int rc;
+  if (dtype == DFLASH2_BF16)
+    rc = launch_k(attn_partial_kernel<bf16>, grid, dim3(AT), smem, c, static_cast<const bf16*>(q),
+                  static_cast<const bf16*>(kb), static_cast<const bf16*>(vb), static_cast<const bf16*>(kc),
+                  static_cast<const bf16*>(vc), block_table, max_pages, page_size, n_pages, ctx_len, new_off, B, nq,
+                  nkv, d, ch, nsplit, part, c.status);
+  else
+    rc = launch_k(attn_partial_kernel<float>, grid, dim3(AT), smem, c, static_cast<const float*>(q),
+                  static_cast<const float*>(kb), static_cast<const float*>(vb), static_cast<const float*>(kc),
+                  static_cast<const float*>(vc), block_table, max_pages, page_size, n_pages, ctx_len, new_off, B, nq,
+                  nkv, d, ch, nsplit, part, c.status);
+  if (rc) return rc;
+  Ctx cc = c;
+  cc.pdl = true;  // same-stream successor of the partial kernel
   const dim3 cgrid(batch * nkv * ((R + CR - 1) / CR));
   const size_t csm = 2 * (size_t)nsplit * CR * sizeof(float);
   if (dtype == DFLASH2_BF16)
-    return launch_k(attn_combine_kernel<bf16>, cgrid, dim3(256), csm, c.stream, (const float*)part, B, nq, nkv, d,
-                    nsplit, static_cast<bf16*>(o_out));
-  return launch_k(attn_combine_kernel<float>, cgrid, dim3(256), csm, c.stream, (const float*)part, B, nq, nkv, d,
-                  nsplit, static_cast<float*>(o_out));
+    return launch_k(attn_combine_kernel<bf16>, cgrid, dim3(256), csm, cc, (const float*)part, B, nq, nkv, d, nsplit,
+                    static_cast<bf16*>(o_out));
+  return launch_k(attn_combine_kernel<float>, cgrid, dim3(256), csm, cc, (const float*)part, B, nq, nkv, d, nsplit,
+                  static_cast<float*>(o_out));
 }
 
 }  // namespace df2

@@ -127,8 +127,9 @@ __device__ __forceinline__ int owner_of(const int32_t* new_off, int batch, int n
   return lo;
 }
 
-// Context K/V of appended rows -> paged cache (one CTA per row, one warp per
-// kv head): K = RoPE(RMSNorm_k(W_k f)), V = W_v f at the row's absolute position.
+// Context K/V of appended rows -> paged cache, one warp per (row, head):
+// K = RoPE(RMSNorm_k(W_k f)) and V = W_v f at the row's absolute position.
+// grid = (rows, ceil(2 nkv / warps per CTA)); warps past 2 nkv idle.
 template <typename T>
 __global__ void __launch_bounds__(RT) kv_append_kernel(const float* __restrict__ Y, int nkv, int d,
                                                        const T* __restrict__ k_norm, float eps, double log2_theta,
@@ -140,35 +141,36 @@ __global__ void __launch_bounds__(RT) kv_append_kernel(const float* __restrict__
   pdl_launch_next();
   pdl_wait();
   const int n = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hh = blockIdx.y * (RT / 32) + warp;  // 0..nkv-1: K heads, nkv..2nkv-1: V heads
+  if (hh >= 2 * nkv) return;
   const int s = owner_of(new_off, batch, n);
   const int pos = ctx_len[s] + (n - new_off[s]);
   if (pos < 0 || pos >= max_pages * page_size) {
-    if (threadIdx.x == 0) flag(status, DFLASH2_DEV_BAD_LENGTH);
+    if (lane == 0) flag(status, DFLASH2_DEV_BAD_LENGTH);
     return;
   }
   const int page = block_table[(size_t)s * max_pages + pos / page_size];
   if (page < 0 || page >= n_pages) {
-    if (threadIdx.x == 0) flag(status, DFLASH2_DEV_BAD_PAGE);
+    if (lane == 0) flag(status, DFLASH2_DEV_BAD_PAGE);
     return;
   }
   const size_t dst = ((size_t)page * page_size + pos % page_size) * nkv * d;
-  const float* y = Y + (size_t)n * 2 * nkv * d;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const float* y = Y + (size_t)n * 2 * nkv * d + (size_t)hh * d;
   const int nj = d / 32;
-  float cs[2], sn[2];
-  for (int j = 0; j < d / 64; ++j) rope_cs(pos, lane + 32 * j, d, log2_theta, &cs[j], &sn[j]);
-  for (int h = warp; h < nkv; h += nw) {
-    float x[4];
+  float x[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (j < nj) x[j] = y[h * d + lane + 32 * j];
+  for (int j = 0; j < 4; ++j)
+    if (j < nj) x[j] = y[lane + 32 * j];
+  if (hh < nkv) {
+    float cs[2], sn[2];
+    for (int j = 0; j < d / 64; ++j) rope_cs(pos, lane + 32 * j, d, log2_theta, &cs[j], &sn[j]);
     head_norm_rope(x, d, k_norm, eps, cs, sn);
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (j < nj) st(&kc[dst + h * d + lane + 32 * j], x[j]);
   }
-  for (int e = threadIdx.x * 4; e < nkv * d; e += blockDim.x * 4)
-    st4(vc + dst + e, *reinterpret_cast<const float4*>(y + nkv * d + e));
+  T* out = (hh < nkv ? kc : vc) + dst + (size_t)(hh < nkv ? hh : hh - nkv) * d;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (j < nj) st(&out[lane + 32 * j], x[j]);
 }
 
 // h[row] = scale * E[token], token = anchor (slot 0) or the mask id; then
@@ -255,8 +257,169 @@ __global__ void __launch_bounds__(RT) dyn_conv_kernel(const T* __restrict__ u, c
   }
 }
 
-// Block Q/K/V: per-head RMSNorm + RoPE of q and k at the block positions
-// (anchor at the context length after the append), v copied.
+// DFlash2 sublayer prologue, fused into one kernel: u = RMSNorm_gamma(x) with
+// x the residual row h (or, for the first sublayer, the scaled block
+// embedding), the dynamic tap logits lambda = W_tap u, their two-way softmax
+// alpha, and the two-tap grouped convolution u2 = u + alpha0 u_t + alpha1 u_{t-1}
+// (u_{-1} = 0 at the anchor).  One CTA per (run of gpc channel groups,
+// sequence): it normalises the B rows of its sequence into shared memory (as
+// stored, so the tap logits see the stored u), forms the tap logits of its
+// groups, and writes u and u2 of its groups' channels (and h, for the
+// embedding).  Tap row 2g + j of W_tap is tap j of group g.
+//
+// The kernel is latency-bound (a few hundred KB per CTA), so every phase is
+// one round of loads in flight: the CTA's tap rows are copied to shared
+// memory (cp.async) before the dependency wait, since no kernel writes the
+// weights; each row is split over nw / B warps with all of a lane's loads
+// issued at once.
+constexpr int PT = 512;  // threads of the prologue kernel
+constexpr int PU = 16;   // vector loads in flight per lane
+
+template <typename T, bool EMBED>
+__global__ void __launch_bounds__(PT) conv_prologue_kernel(
+    const float* __restrict__ h_in, const int32_t* __restrict__ anchor, int mask_id, const T* __restrict__ E, int V,
+    float scale, const T* __restrict__ gamma, float eps, const T* __restrict__ Wt, int H, int gs, int gpc, int B,
+    int stage_w, float* __restrict__ h_out, T* __restrict__ u_out, T* __restrict__ u2_out, unsigned* status) {
+  extern __shared__ __align__(16) uint8_t smraw[];
+  constexpr int NW = PT / 32;
+  const int s = blockIdx.y, G = H / gs;
+  const int g0 = blockIdx.x * gpc, ng = min(gpc, G - g0);
+  T* us = reinterpret_cast<T*>(smraw);                 // [B][H] normed rows as stored
+  T* wsm = us + (size_t)B * H;                         // [2 gpc][H] tap rows (stage_w)
+  float* rinv = reinterpret_cast<float*>(wsm + (stage_w ? (size_t)2 * gpc * H : 0));  // [B]
+  float* lam = rinv + B;                               // [B][2 gpc] tap logits, then alpha
+  float* red = lam + B * 2 * gpc;                      // [B][NW] partial sums of squares
+  __shared__ int toks[32];
+  pdl_launch_next();
+  if (stage_w) {  // the weights are not written by any kernel of the stream
+    constexpr int E16 = 16 / sizeof(T);
+    const T* src = Wt + (size_t)2 * g0 * H;
+    for (int i = threadIdx.x; i < 2 * ng * H / E16; i += PT) cp_async16(wsm + (size_t)i * E16, src + (size_t)i * E16, true);
+    cp_async_commit();
+  }
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (EMBED) {
+    for (int t = threadIdx.x; t < B; t += PT) {
+      int tok = t == 0 ? anchor[s] : mask_id;
+      if (tok < 0 || tok >= V) {
+        flag(status, DFLASH2_DEV_BAD_TOKEN);
+        tok = -1;
+      }
+      toks[t] = tok;
+    }
+    __syncthreads();
+  }
+  // 4 consecutive elements of source row t at column m
+  auto xrow = [&](int t, int m) -> float4 {
+    if (EMBED) {
+      const int tok = toks[t];
+      if (tok < 0) return make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 e = ld4(E + (size_t)tok * H + m);
+      return make_float4(scale * e.x, scale * e.y, scale * e.z, scale * e.w);
+    }
+    return *reinterpret_cast<const float4*>(h_in + ((size_t)s * B + t) * H + m);
+  };
+  // row t is split into wpr contiguous segments of sl columns, one warp each
+  const int wpr = max(1, NW / B), rows_at_once = NW / wpr;
+  const int sl = (H / 4 + wpr - 1) / wpr * 4;
+  // 1. sums of squares per (row, segment), then 1/rms per row
+  for (int t0 = 0; t0 < B; t0 += rows_at_once) {
+    const int t = t0 + warp / wpr, seg = warp % wpr;
+    if (warp / wpr < rows_at_once && t < B) {
+      const int m1 = min(H, (seg + 1) * sl);
+      float ss = 0.f;
+      for (int m0 = seg * sl + lane * 4; m0 < m1; m0 += 128 * PU) {
+        float4 v[PU];
+#pragma unroll
+        for (int k = 0; k < PU; ++k) v[k] = m0 + 128 * k < m1 ? xrow(t, m0 + 128 * k) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < PU; ++k) ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) red[t * NW + seg] = ss;
+    }
+  }
+  __syncthreads();
+  for (int t = threadIdx.x; t < B; t += PT) {
+    float ss = 0.f;
+    for (int k = 0; k < wpr; ++k) ss += red[t * NW + k];
+    rinv[t] = rsqrtf(ss / (float)H + eps);
+  }
+  __syncthreads();
+  // 2. the stored u rows into shared memory (the x reloads hit L1)
+  for (int t0 = 0; t0 < B; t0 += rows_at_once) {
+    const int t = t0 + warp / wpr, seg = warp % wpr;
+    if (warp / wpr < rows_at_once && t < B) {
+      const int m1 = min(H, (seg + 1) * sl);
+      const float r = rinv[t];
+      constexpr int PU2 = PU / 2;  // two vectors per element: x and gamma
+      for (int m0 = seg * sl + lane * 4; m0 < m1; m0 += 128 * PU2) {
+        float4 v[PU2], gm[PU2];
+#pragma unroll
+        for (int k = 0; k < PU2; ++k)
+          if (m0 + 128 * k < m1) {
+            v[k] = xrow(t, m0 + 128 * k);
+            gm[k] = ld4(gamma + m0 + 128 * k);
+          }
+#pragma unroll
+        for (int k = 0; k < PU2; ++k)
+          if (m0 + 128 * k < m1) st4(us + (size_t)t * H + m0 + 128 * k, scale4(v[k], r, gm[k]));
+      }
+    }
+  }
+  if (stage_w) cp_async_wait<0>();
+  __syncthreads();
+  // 3. tap logits of this CTA's groups: one warp per (row, tap row)
+  for (int p = warp; p < B * 2 * ng; p += NW) {
+    const int t = p / (2 * ng), jj = p % (2 * ng);
+    const T* w = stage_w ? wsm + (size_t)jj * H : Wt + (size_t)(2 * g0 + jj) * H;
+    float acc = 0.f;
+    for (int m0 = lane * 4; m0 < H; m0 += 128 * PU) {
+      float4 wv[PU];
+#pragma unroll
+      for (int k = 0; k < PU; ++k) wv[k] = m0 + 128 * k < H ? ld4(w + m0 + 128 * k) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < PU; ++k)
+        if (m0 + 128 * k < H) {
+          const float4 uv = ld4(us + (size_t)t * H + m0 + 128 * k);
+          acc += wv[k].x * uv.x + wv[k].y * uv.y + wv[k].z * uv.z + wv[k].w * uv.w;
+        }
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) lam[t * 2 * gpc + jj] = acc;
+  }
+  __syncthreads();
+  // 4. alpha = softmax over the two taps of each (row, group)
+  for (int idx = threadIdx.x; idx < B * ng; idx += PT) {
+    const int t = idx / ng, gl = idx % ng;
+    float* l = lam + t * 2 * gpc + 2 * gl;
+    const float mx = fmaxf(l[0], l[1]);
+    const float e0 = expf(l[0] - mx), e1 = expf(l[1] - mx);
+    const float inv = 1.f / (e0 + e1);
+    l[0] = e0 * inv;
+    l[1] = e1 * inv;
+  }
+  __syncthreads();
+  // 5. the convolution over this CTA's channels; u (and h) stored alongside
+  const int c0 = g0 * gs, nc = ng * gs;
+  for (int idx = threadIdx.x * 4; idx < B * nc; idx += PT * 4) {
+    const int t = idx / nc, cc = idx % nc, m = c0 + cc;
+    const float* a = lam + t * 2 * gpc + 2 * (cc / gs);  // gs % 4 == 0: the 4 channels share a group
+    const float a0 = a[0], a1 = a[1];
+    const float4 ut = ld4(us + (size_t)t * H + m);
+    const float4 up = t > 0 ? ld4(us + (size_t)(t - 1) * H + m) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const size_t o = ((size_t)s * B + t) * H + m;
+    st4(u_out + o, ut);
+    st4(u2_out + o, make_float4(ut.x + a0 * ut.x + a1 * up.x, ut.y + a0 * ut.y + a1 * up.y,
+                                ut.z + a0 * ut.z + a1 * up.z, ut.w + a0 * ut.w + a1 * up.w));
+    if (EMBED) *reinterpret_cast<float4*>(h_out + o) = xrow(t, m);
+  }
+}
+
+// Block Q/K/V, one warp per (row, head): per-head RMSNorm + RoPE of q and k
+// at the block positions (anchor at the context length after the append), v
+// copied.  grid = (rows, ceil((nq + 2 nkv) / warps per CTA)).
 template <typename T>
 __global__ void __launch_bounds__(RT) qkv_epi_kernel(const float* __restrict__ Y, int B, int nq, int nkv, int d,
                                                      const T* __restrict__ qn, const T* __restrict__ kn, float eps,
@@ -266,27 +429,28 @@ __global__ void __launch_bounds__(RT) qkv_epi_kernel(const float* __restrict__ Y
   pdl_launch_next();
   pdl_wait();
   const int row = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hh = blockIdx.y * (RT / 32) + warp;  // q heads, then k heads, then v heads
+  if (hh >= nq + 2 * nkv) return;
   const int s = row / B, i = row % B;
-  const int pos = ctx_len[s] + (new_off[s + 1] - new_off[s]) + i;
-  const int w3 = (nq + 2 * nkv) * d;
-  const float* y = Y + (size_t)row * w3;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const float* y = Y + (size_t)row * (nq + 2 * nkv) * d + (size_t)hh * d;
   const int nj = d / 32;
-  float cs[2], sn[2];
-  for (int j = 0; j < d / 64; ++j) rope_cs(pos, lane + 32 * j, d, log2_theta, &cs[j], &sn[j]);
-  for (int hh = warp; hh < nq + nkv; hh += nw) {
-    float x[4];
+  float x[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (j < nj) x[j] = y[hh * d + lane + 32 * j];
+  for (int j = 0; j < 4; ++j)
+    if (j < nj) x[j] = y[lane + 32 * j];
+  if (hh < nq + nkv) {
+    const int pos = ctx_len[s] + (new_off[s + 1] - new_off[s]) + i;
+    float cs[2], sn[2];
+    for (int j = 0; j < d / 64; ++j) rope_cs(pos, lane + 32 * j, d, log2_theta, &cs[j], &sn[j]);
     head_norm_rope(x, d, hh < nq ? qn : kn, eps, cs, sn);
-    T* dst = hh < nq ? q + (size_t)row * nq * d + hh * d : kb + (size_t)row * nkv * d + (hh - nq) * d;
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (j < nj) st(&dst[lane + 32 * j], x[j]);
   }
-  for (int e = threadIdx.x * 4; e < nkv * d; e += blockDim.x * 4)
-    st4(vb + (size_t)row * nkv * d + e, *reinterpret_cast<const float4*>(y + (nq + nkv) * d + e));
+  T* dst = hh < nq         ? q + ((size_t)row * nq + hh) * d
+           : hh < nq + nkv ? kb + ((size_t)row * nkv + hh - nq) * d
+                           : vb + ((size_t)row * nkv + hh - nq - nkv) * d;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (j < nj) st(&dst[lane + 32 * j], x[j]);
 }
 
 // act = SiLU(gate) * up from the stacked gate/up output Y [rows][2I].
@@ -322,7 +486,7 @@ int launch_rows_feature_norm(int dtype, const float* Y, int rows, int H, const v
                              const Ctx& c) {
   if (rows <= 0) return DFLASH2_OK;
   int rc;
-  DF2_DISPATCH(dtype, rc = launch_k(feature_norm_kernel<T>, dim3(rows), dim3(RT), H * sizeof(float), c.stream, Y, H,
+  DF2_DISPATCH(dtype, rc = launch_k(feature_norm_kernel<T>, dim3(rows), dim3(RT), H * sizeof(float), c, Y, H,
                                     static_cast<const T*>(gamma), eps, static_cast<T*>(f_out)));
   return rc;
 }
@@ -333,7 +497,8 @@ int launch_kv_append(int dtype, const float* Y, int rows, int nkv, int d, const 
   if (rows <= 0) return DFLASH2_OK;
   const double l2t = std::log2((double)theta);
   int rc;
-  DF2_DISPATCH(dtype, rc = launch_k(kv_append_kernel<T>, dim3(rows), dim3(RT), 0, c.stream, Y, nkv, d,
+  const dim3 grid(rows, (2 * nkv + RT / 32 - 1) / (RT / 32));
+  DF2_DISPATCH(dtype, rc = launch_k(kv_append_kernel<T>, grid, dim3(RT), 0, c, Y, nkv, d,
                                     static_cast<const T*>(k_norm), eps, l2t, ctx_len, new_off, batch, block_table,
                                     max_pages, page_size, n_pages, static_cast<T*>(kc), static_cast<T*>(vc),
                                     c.status));
@@ -343,7 +508,7 @@ int launch_kv_append(int dtype, const float* Y, int rows, int nkv, int d, const 
 int launch_embed_norm(int dtype, const int32_t* anchor, int mask_id, int batch, int B, const void* embed, int V, int H,
                       float scale, const void* gamma, float eps, float* h_out, void* u_out, const Ctx& c) {
   int rc;
-  DF2_DISPATCH(dtype, rc = launch_k(embed_norm_kernel<T>, dim3(batch * B), dim3(RT), H * sizeof(float), c.stream,
+  DF2_DISPATCH(dtype, rc = launch_k(embed_norm_kernel<T>, dim3(batch * B), dim3(RT), H * sizeof(float), c,
                                     anchor, mask_id, B, static_cast<const T*>(embed), V, H, scale,
                                     static_cast<const T*>(gamma), eps, h_out, static_cast<T*>(u_out), c.status));
   return rc;
@@ -352,7 +517,7 @@ int launch_embed_norm(int dtype, const int32_t* anchor, int mask_id, int batch, 
 int launch_rownorm(int dtype, const float* h, int rows, int H, const void* gamma, float eps, void* u_out, int B,
                    int skip_anchor, const Ctx& c) {
   int rc;
-  DF2_DISPATCH(dtype, rc = launch_k(rownorm_kernel<T>, dim3(rows), dim3(RT), H * sizeof(float), c.stream, h, H,
+  DF2_DISPATCH(dtype, rc = launch_k(rownorm_kernel<T>, dim3(rows), dim3(RT), H * sizeof(float), c, h, H,
                                     static_cast<const T*>(gamma), eps, static_cast<T*>(u_out), B, skip_anchor));
   return rc;
 }
@@ -361,8 +526,64 @@ int launch_dyn_conv(int dtype, const void* u, const float* Y, int rows, int H, i
                     const Ctx& c) {
   const int G = H / group_size;
   int rc;
-  DF2_DISPATCH(dtype, rc = launch_k(dyn_conv_kernel<T>, dim3(rows), dim3(RT), 2 * G * sizeof(float), c.stream,
+  DF2_DISPATCH(dtype, rc = launch_k(dyn_conv_kernel<T>, dim3(rows), dim3(RT), 2 * G * sizeof(float), c,
                                     static_cast<const T*>(u), Y, H, group_size, B, static_cast<T*>(u2_out)));
+  return rc;
+}
+
+// Shared memory of the prologue: the B normed rows, the CTA's tap rows when
+// staged, 1/rms, tap logits and the per-warp partial sums.
+size_t conv_prologue_smem(int dtype, int B, int H, int gpc, bool stage_w) {
+  const size_t es = dtype == DFLASH2_BF16 ? 2 : 4;
+  return (size_t)B * H * es + (stage_w ? (size_t)2 * gpc * H * es : 0) +
+         (size_t)B * (1 + 2 * gpc + PT / 32) * sizeof(float);
+}
+
+int conv_prologue_groups(int G, int batch, int nsm) {
+  // about two CTAs per SM: groups per CTA grows with the batch
+  const long want = std::max(1L, (long)2 * nsm / std::max(1, batch));
+  return (int)std::max(1L, std::min<long>(G, ((long)G + want - 1) / want));
+}
+
+constexpr size_t kPrologueSmem = 200 * 1024;
+
+bool conv_prologue_fits(int dtype, int batch, int B, int H, int G, int nsm) {
+  return B <= 32 && conv_prologue_smem(dtype, B, H, conv_prologue_groups(G, batch, nsm), false) <= kPrologueSmem;
+}
+
+int launch_conv_prologue(int dtype, const float* h_in, const int32_t* anchor, int mask_id, const void* embed, int V,
+                         float scale, const void* gamma, float eps, const void* w_tap, int batch, int B, int H,
+                         int group_size, float* h_out, void* u_out, void* u2_out, const Ctx& c) {
+  const int G = H / group_size;
+  const int gpc = conv_prologue_groups(G, batch, c.nsm);
+  const bool stage_w = conv_prologue_smem(dtype, B, H, gpc, true) <= kPrologueSmem;
+  const size_t smem = conv_prologue_smem(dtype, B, H, gpc, stage_w);
+  if (smem > kPrologueSmem || B > 32) return DFLASH2_ERR_SHAPE;
+  static bool attr = false;  // set once, before any capture
+  if (!attr) {
+    if (cudaFuncSetAttribute(conv_prologue_kernel<bf16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kPrologueSmem) ||
+        cudaFuncSetAttribute(conv_prologue_kernel<bf16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kPrologueSmem) ||
+        cudaFuncSetAttribute(conv_prologue_kernel<float, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kPrologueSmem) ||
+        cudaFuncSetAttribute(conv_prologue_kernel<float, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kPrologueSmem))
+      return DFLASH2_ERR_CUDA;
+    attr = true;
+  }
+  const dim3 grid((G + gpc - 1) / gpc, batch);
+  int rc;
+  if (h_in)
+    DF2_DISPATCH(dtype, rc = launch_k(conv_prologue_kernel<T, false>, grid, dim3(PT), smem, c, h_in, anchor, mask_id,
+                                      static_cast<const T*>(embed), V, scale, static_cast<const T*>(gamma), eps,
+                                      static_cast<const T*>(w_tap), H, group_size, gpc, B, stage_w ? 1 : 0, h_out,
+                                      static_cast<T*>(u_out), static_cast<T*>(u2_out), c.status));
+  else
+    DF2_DISPATCH(dtype, rc = launch_k(conv_prologue_kernel<T, true>, grid, dim3(PT), smem, c, h_in, anchor, mask_id,
+                                      static_cast<const T*>(embed), V, scale, static_cast<const T*>(gamma), eps,
+                                      static_cast<const T*>(w_tap), H, group_size, gpc, B, stage_w ? 1 : 0, h_out,
+                                      static_cast<T*>(u_out), static_cast<T*>(u2_out), c.status));
   return rc;
 }
 
@@ -371,7 +592,8 @@ int launch_qkv_epilogue(int dtype, const float* Y, int rows, int B, int nq, int 
                         void* q, void* kb, void* vb, const Ctx& c) {
   const double l2t = std::log2((double)theta);
   int rc;
-  DF2_DISPATCH(dtype, rc = launch_k(qkv_epi_kernel<T>, dim3(rows), dim3(RT), 0, c.stream, Y, B, nq, nkv, d,
+  const dim3 grid(rows, (nq + 2 * nkv + RT / 32 - 1) / (RT / 32));
+  DF2_DISPATCH(dtype, rc = launch_k(qkv_epi_kernel<T>, grid, dim3(RT), 0, c, Y, B, nq, nkv, d,
                                     static_cast<const T*>(q_norm), static_cast<const T*>(k_norm), eps, l2t, ctx_len,
                                     new_off, static_cast<T*>(q), static_cast<T*>(kb), static_cast<T*>(vb)));
   return rc;
@@ -381,7 +603,7 @@ int launch_act(int dtype, const float* Y, int rows, int I, void* act, const Ctx&
   const size_t total4 = (size_t)rows * I / 4;
   const int blocks = (int)std::min<size_t>((total4 + RT - 1) / RT, (size_t)c.nsm * 4);
   int rc;
-  DF2_DISPATCH(dtype, rc = launch_k(act_kernel<T>, dim3(blocks), dim3(RT), 0, c.stream, Y, rows, I,
+  DF2_DISPATCH(dtype, rc = launch_k(act_kernel<T>, dim3(blocks), dim3(RT), 0, c, Y, rows, I,
                                     static_cast<T*>(act)));
   return rc;
 }

@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const float* __restrict_
 int gemm_f32(const GemmOp& g, const Ctx& c) {
   if (g.M <= 0 || g.N <= 0 || g.K <= 0) return DFLASH2_ERR_SHAPE;
   dim3 grid((g.M + TM - 1) / TM, (g.N + TN - 1) / TN);
-  return launch_k(simt_gemm_kernel, grid, dim3(256), 0, c.stream, static_cast<const float*>(g.W), g.M, g.K, g.ldw,
+  return launch_k(simt_gemm_kernel, grid, dim3(256), 0, c, static_cast<const float*>(g.W), g.M, g.K, g.ldw,
                   static_cast<const float*>(g.X), g.N, g.ldx, g.out, g.accumulate ? 1 : 0);
 }
 

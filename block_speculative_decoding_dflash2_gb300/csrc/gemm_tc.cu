@@ -14,12 +14,23 @@
 // TMA bytes in flight per SM (a 4..12-stage ring) on a persistent grid of
 // one CTA per SM.
 //
+// Work schedule.  A contraction is (tiles) x (K chunks of 64).  With few
+// tiles per SM, whole tiles leave SMs idle in the last wave, so every
+// non-top-k contraction is split "stream-K" style: the tiles' chunks are laid
+// end to end and CTA g streams the contiguous share [g W / G, (g+1) W / G) of
+// all W = tiles x chunks, crossing tile boundaries.  A tile covered by one
+// CTA is written directly; a tile shared by several CTAs is written by its
+// pieces as fp32 partials, and the last piece to arrive (arrival counter,
+// indexed by the tile's first CTA) sums them in CTA order, so the result is
+// deterministic and no CTA waits for another.  The top-k contraction (the
+// lm_head) needs whole tiles: its CTAs take whole tiles round-robin.
+//
 // Warp roles (192 threads):
 //   warp 0      TMA producer (one lane): weight + activation tiles -> ring
 //   warp 1      MMA issuer (one lane) and TMEM owner
-//   warps 2..5  epilogue: TMEM -> registers -> either fp32 split-K partials
-//               (out[s][n][m], coalesced over m) or the streaming top-k.
-// The accumulator is double-buffered in TMEM so the epilogue of one tile
+//   warps 2..5  epilogue: TMEM -> registers -> the output tile, a partial
+//               piece (coalesced over m), or the streaming top-k.
+// The accumulator is double-buffered in TMEM so the epilogue of one unit
 // overlaps the MMAs of the next.
 //
 // Every wait is bounded (1 s); on timeout the kernel records
@@ -46,10 +57,12 @@ constexpr int THREADS = 192;
 
 struct TcArgs {
   int M, N, K;
-  int n_chunks, splits, m_tiles, n_tiles, units;
+  int n_chunks, m_tiles, n_tiles, tiles;
+  long work;        // tiles * n_chunks
+  int stream;       // 1: stream-K shares of the work; 0: whole tiles round-robin
   float* out;       // final [N][M] fp32 (stored, or added to when accumulate)
-  float* partial;   // [splits][N][M] fp32 when splits > 1
-  int* counters;    // [n_tiles * m_tiles] arrival counters, zero between launches
+  float* partial;   // stream: [gridDim.x][2][BN][BM] pieces of shared tiles
+  int* counters;    // stream: [gridDim.x] arrival counters, zero between launches
   int accumulate;
   float* lists_v;
   int* lists_i;
@@ -77,6 +90,48 @@ struct TcCfg {
                                         : (2 * BN <= 256) ? 256
                                                           : 512;
 };
+
+// The units of this CTA in order: (tile, first chunk, end chunk).
+struct UnitIter {
+  long c, cend;  // stream: chunk cursor and end; tiles: tile cursor and count
+  int nc, step, stream;
+  __device__ __forceinline__ bool next(int& t, int& k0, int& k1) {
+    if (c >= cend) return false;
+    if (stream) {
+      t = (int)(c / nc);
+      k0 = (int)(c - (long)t * nc);
+      k1 = (int)min((long)nc, (long)k0 + (cend - c));
+      c += k1 - k0;
+    } else {
+      t = (int)c;
+      k0 = 0;
+      k1 = nc;
+      c += step;
+    }
+    return true;
+  }
+};
+
+__device__ __forceinline__ long share_start(long work, int G, int g) { return (long)g * work / G; }
+
+__device__ __forceinline__ UnitIter unit_iter(const TcArgs& a) {
+  UnitIter it;
+  it.nc = a.n_chunks;
+  it.stream = a.stream;
+  if (a.stream) {
+    it.c = share_start(a.work, gridDim.x, blockIdx.x);
+    it.cend = share_start(a.work, gridDim.x, blockIdx.x + 1);
+    it.step = 0;
+  } else {
+    it.c = blockIdx.x;
+    it.cend = a.tiles;
+    it.step = gridDim.x;
+  }
+  return it;
+}
+
+// CTA whose share holds chunk c: the largest g with share_start(g) <= c.
+__device__ __forceinline__ int share_of(long c, long work, int G) { return (int)(((c + 1) * G - 1) / work); }
 
 __device__ __forceinline__ void named_sync_epi() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -161,47 +216,37 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
-      // this CTA's chunks, in order: units blockIdx.x, +gridDim.x, ...; each a K range
-      auto unit_range = [&](int u, int& k0, int& k1, int& mt, int& nt) {
-        const int sp = u % a.splits, t = u / a.splits;
-        mt = t % a.m_tiles;
-        nt = t / a.m_tiles;
-        k0 = (int)((long)sp * a.n_chunks / a.splits);
-        k1 = (int)((long)(sp + 1) * a.n_chunks / a.splits);
-      };
-      int u = blockIdx.x, kc = 0, k1 = 0, mt = 0, nt = 0;
-      if (u < a.units) unit_range(u, kc, k1, mt, nt);
+      UnitIter it = unit_iter(a);
+      int t = 0, kc = 0, k1 = 0;
+      bool have = it.next(t, kc, k1);
       // 1. weight tiles of the first ring's worth of chunks, before waiting for
       //    the previous kernel (no kernel on the stream writes the weights)
       int pre = 0;
       {
-        int uu = u, kk = kc, kk1 = k1, mm = mt, nn = nt;
-        while (pre < STAGES && uu < a.units) {
+        UnitIter pit = it;
+        int tt = t, kk = kc, kk1 = k1;
+        bool h = have;
+        while (pre < STAGES && h) {
           mbar_arrive_expect_tx(full + pre, A_BYTES + B_BYTES);
-          tma_load_2d(stA + pre * A_BYTES, &tmA, full + pre, kk * BK, mm * BM, pol_w);
+          tma_load_2d(stA + pre * A_BYTES, &tmA, full + pre, kk * BK, (tt % a.m_tiles) * BM, pol_w);
           ++pre;
-          if (++kk == kk1) {
-            uu += gridDim.x;
-            if (uu < a.units) unit_range(uu, kk, kk1, mm, nn);
-          }
+          if (++kk == kk1) h = pit.next(tt, kk, kk1);
         }
       }
       pdl_wait();
       // 2. the activation tiles of those chunks
       long issued = 0;
       for (int i = 0; i < pre; ++i) {
-        tma_load_2d(stB + i * B_BYTES, &tmB, full + i, kc * BK, nt * BN, pol_x);
+        tma_load_2d(stB + i * B_BYTES, &tmB, full + i, kc * BK, (t / a.m_tiles) * BN, pol_x);
         ++issued;
-        if (++kc == k1) {
-          u += gridDim.x;
-          if (u < a.units) unit_range(u, kc, k1, mt, nt);
-        }
+        if (++kc == k1) have = it.next(t, kc, k1);
       }
       int stage = pre % STAGES;
       uint32_t phase = pre == STAGES ? 1u : 0u;
       // 3. steady state
-      while (u < a.units && !*abort_flag) {
+      while (have && !*abort_flag) {
         bool ok = true;
+        const int mt = t % a.m_tiles, nt = t / a.m_tiles;
         for (; kc < k1; ++kc) {
           if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, WAIT_NS)) {
             fail();
@@ -218,8 +263,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
         if (!ok) break;
-        u += gridDim.x;
-        if (u < a.units) unit_range(u, kc, k1, mt, nt);
+        have = it.next(t, kc, k1);
       }
       if (*abort_flag) {
         // wait (bounded) for every copy this thread issued to land
@@ -239,10 +283,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
-        const int sp = u % a.splits;
-        const int k0 = (int)((long)sp * a.n_chunks / a.splits);
-        const int k1 = (int)((long)(sp + 1) * a.n_chunks / a.splits);
+      UnitIter it = unit_iter(a);
+      int t, k0, k1;
+      while (ok && it.next(t, k0, k1)) {
         if (!mbar_wait(tempty + acc, acc_phase ^ 1u, abort_flag, WAIT_NS)) {
           fail();
           break;
@@ -306,8 +349,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     };
 
-    for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
-      const int sp = u % a.splits, t = u / a.splits;
+    UnitIter it = unit_iter(a);
+    int t, k0, k1;
+    while (it.next(t, k0, k1)) {
       const int mt = t % a.m_tiles, nt = t / a.m_tiles;
       const bool got = mbar_wait(tfull + acc, acc_phase, abort_flag, WAIT_NS);
       if (!got) fail();
@@ -316,49 +360,85 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int m = mt * BM + row;
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       if constexpr (!TOPK) {
-        // one K split: the tile is final.  Several: write this split's
-        // partial; the last split to arrive at the tile (arrival counter)
-        // sums all partials in split order and writes the final tile, so
-        // the result is deterministic and no CTA ever waits for another.
-        const bool direct = a.splits == 1;
-        float* dst = direct ? a.out : a.partial + (size_t)sp * a.N * a.M;
+        // pieces of tile t: CTAs g_first .. g_last share its chunks
+        int g_first = blockIdx.x, g_last = blockIdx.x;
+        if (a.stream) {
+          const long c0t = (long)t * a.n_chunks;
+          g_first = share_of(c0t, a.work, gridDim.x);
+          g_last = share_of(c0t + a.n_chunks - 1, a.work, gridDim.x);
+        }
+        const bool direct = g_first == g_last;
+        // a CTA's piece of a shared tile is its first unit (slot 0) when its
+        // share starts inside the tile, else its last unit (slot 1)
+        auto piece = [&](int g) {
+          const int slot = share_start(a.work, gridDim.x, g) / a.n_chunks == t ? 0 : 1;
+          return a.partial + ((size_t)g * 2 + slot) * BN * BM;
+        };
+        float* pc = direct ? nullptr : piece(blockIdx.x);
+        // (each block of 16 columns: all loads first, then the stores, so
+        //  the loads of old values and of pieces overlap instead of queueing)
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 16) {
           float v[16];
           tmem_ld16(tbase + c0, v);
-          if (m < a.M) {
+          if (!direct) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int n = nt * BN + c0 + j;
-              if (n < a.N) {
-                float* p = dst + (size_t)n * a.M + m;
-                if (direct && a.accumulate) *p += v[j];
-                else *p = v[j];
-              }
+            for (int j = 0; j < 16; ++j) pc[(c0 + j) * BM + row] = v[j];
+          } else if (m < a.M) {
+            float* p0 = a.out + (size_t)(nt * BN + c0) * a.M + m;
+            const int nj = min(16, a.N - (nt * BN + c0));
+            if (a.accumulate) {
+              float old[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) old[j] = j < nj ? p0[(size_t)j * a.M] : 0.f;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] += old[j];
             }
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (j < nj) p0[(size_t)j * a.M] = v[j];
           }
         }
         tc_fence_before();
         mbar_arrive(tempty + acc);
         if (!direct) {
-          const int tidx = nt * a.m_tiles + mt;
           __threadfence();
           named_sync_epi();
-          if (threadIdx.x == 64) *last_flag = (atomicAdd(a.counters + tidx, 1) == a.splits - 1) ? 1 : 0;
+          if (threadIdx.x == 64)
+            *last_flag = (atomicAdd(a.counters + g_first, 1) == g_last - g_first) ? 1 : 0;
           named_sync_epi();
           if (*last_flag) {
             __threadfence();
-            if (m < a.M) {
-              const int n1 = min(a.N, (nt + 1) * BN);
-              for (int n = nt * BN; n < n1; ++n) {
-                float s = 0.f;
-                for (int s2 = 0; s2 < a.splits; ++s2) s += __ldcg(a.partial + ((size_t)s2 * a.N + n) * a.M + m);
-                float* p = a.out + (size_t)n * a.M + m;
-                if (a.accumulate) *p += s;
-                else *p = s;
+            // sum the pieces in CTA order, 16 columns at a time
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN && nt * BN + c0 < a.N; c0 += 16) {
+              float sum[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) sum[j] = 0.f;
+              for (int g = g_first; g <= g_last; ++g) {
+                const float* pg = piece(g) + (size_t)c0 * BM + row;
+                float v[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = __ldcg(pg + j * BM);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) sum[j] += v[j];
+              }
+              if (m < a.M) {
+                float* p0 = a.out + (size_t)(nt * BN + c0) * a.M + m;
+                const int nj = min(16, a.N - (nt * BN + c0));
+                if (a.accumulate) {
+                  float old[16];
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) old[j] = j < nj ? p0[(size_t)j * a.M] : 0.f;
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) sum[j] = old[j] + sum[j];
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  if (j < nj) p0[(size_t)j * a.M] = sum[j];
               }
             }
-            if (threadIdx.x == 64) a.counters[tidx] = 0;
+            if (threadIdx.x == 64) a.counters[g_first] = 0;
           }
         }
       } else {
@@ -492,7 +572,7 @@ int pick_bn(int M, int N) {
 }
 
 template <int BN, bool TOPK>
-int launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs& args, int grid, cudaStream_t st) {
+int launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs& args, int grid, const Ctx& c) {
   constexpr int smem = TcCfg<BN>::smem_bytes(TOPK);
   static bool attr_set = false;
   if (!attr_set) {
@@ -501,27 +581,12 @@ int launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs& args, 
       return DFLASH2_ERR_CUDA;
     attr_set = true;
   }
-  return launch_k(tc_gemm_kernel<BN, TOPK>, dim3(grid), dim3(THREADS), smem, st, ma, mb, args);
+  return launch_k(tc_gemm_kernel<BN, TOPK>, dim3(grid), dim3(THREADS), smem, c, ma, mb, args);
 }
 
 }  // namespace
 
-// K splits: about one wave of units over the SMs, but at least 8 K chunks per
-// unit (so a unit's epilogue -- partial store, fence, arrival count -- hides
-// behind the next unit's stream) and fp32 partials (s*N*M*4 bytes) at most a
-// quarter of the weight bytes (M*K*2).
-int gemm_splits(int M, int N, int K, int nsm, bool topk) {
-  if (topk || N > 256) return 1;  // many activation rows: enough tiles without splitting K
-  const long base = gemm_tiles(M, N);
-  const int chunks = (K + BK - 1) / BK;
-  // enough tiles to keep most SMs streaming: no split (measured: splitting a
-  // 192-tile contraction 3 or 4 ways is slower than its uneven last wave)
-  if (2 * base >= nsm) return 1;
-  long s = nsm / base;
-  s = std::min<long>(s, chunks / 8);
-  s = std::min<long>(s, K / (8 * N));
-  return (int)std::max<long>(1, std::min<long>(s, 64));
-}
+size_t gemm_partial_bytes(int M, int N) { return (size_t)kMaxSM * 2 * BM * pick_bn(M, N) * sizeof(float); }
 
 int gemm_tiles(int M, int N) {
   const int bn = pick_bn(M, N);
@@ -550,13 +615,16 @@ int gemm_bf16(const GemmOp& g, const Ctx& c) {
   a.n_chunks = (g.K + BK - 1) / BK;
   a.m_tiles = (g.M + BM - 1) / BM;
   a.n_tiles = (g.N + bn - 1) / bn;
-  a.splits = g.topk ? 1 : std::max(1, std::min(g.splits, a.n_chunks));
-  a.units = a.m_tiles * a.n_tiles * a.splits;
+  a.tiles = a.m_tiles * a.n_tiles;
+  a.work = (long)a.tiles * a.n_chunks;
+  a.stream = (!g.topk && g.ctas >= 0) ? 1 : 0;
   a.out = g.out;
   a.partial = g.partial;
   a.counters = g.counters;
   a.accumulate = g.accumulate ? 1 : 0;
-  if (!g.topk && a.splits > 1 && (!g.partial || !g.counters)) return DFLASH2_ERR_INVALID_ARG;
+  if (a.stream && (!g.partial || !g.counters)) return DFLASH2_ERR_INVALID_ARG;
+  const long want = a.stream ? (g.ctas > 0 ? std::min(g.ctas, kMaxSM) : c.nsm) : c.nsm;
+  const int grid = (int)std::min<long>(want, a.stream ? a.work : a.tiles);
   a.lists_v = g.lists_v;
   a.lists_i = g.lists_i;
   a.debug = g.debug;
@@ -564,7 +632,6 @@ int gemm_bf16(const GemmOp& g, const Ctx& c) {
   a.cap = g.cap;
   a.status = c.status;
   if (g.topk && a.n_tiles > 32) return DFLASH2_ERR_SHAPE;
-  const int grid = std::min(a.units, c.nsm);
 
   CUtensorMap ma, mb;
   int rc = make_map(&ma, g.W, g.M, g.K, g.ldw, BM);
@@ -573,11 +640,11 @@ int gemm_bf16(const GemmOp& g, const Ctx& c) {
   if (rc) return rc;
 
   switch (bn) {
-    case 16: return g.topk ? launch_bn<16, true>(ma, mb, a, grid, c.stream) : launch_bn<16, false>(ma, mb, a, grid, c.stream);
-    case 32: return g.topk ? launch_bn<32, true>(ma, mb, a, grid, c.stream) : launch_bn<32, false>(ma, mb, a, grid, c.stream);
-    case 64: return g.topk ? launch_bn<64, true>(ma, mb, a, grid, c.stream) : launch_bn<64, false>(ma, mb, a, grid, c.stream);
-    case 128: return g.topk ? launch_bn<128, true>(ma, mb, a, grid, c.stream) : launch_bn<128, false>(ma, mb, a, grid, c.stream);
-    default: return g.topk ? launch_bn<256, true>(ma, mb, a, grid, c.stream) : launch_bn<256, false>(ma, mb, a, grid, c.stream);
+    case 16: return g.topk ? launch_bn<16, true>(ma, mb, a, grid, c) : launch_bn<16, false>(ma, mb, a, grid, c);
+    case 32: return g.topk ? launch_bn<32, true>(ma, mb, a, grid, c) : launch_bn<32, false>(ma, mb, a, grid, c);
+    case 64: return g.topk ? launch_bn<64, true>(ma, mb, a, grid, c) : launch_bn<64, false>(ma, mb, a, grid, c);
+    case 128: return g.topk ? launch_bn<128, true>(ma, mb, a, grid, c) : launch_bn<128, false>(ma, mb, a, grid, c);
+    default: return g.topk ? launch_bn<256, true>(ma, mb, a, grid, c) : launch_bn<256, false>(ma, mb, a, grid, c);
   }
 }
 

@@ -13,6 +13,7 @@ struct Ctx {
   cudaStream_t stream;
   unsigned* status;  // device status word (workspace offset 0)
   int nsm;           // SMs of the current device
+  bool pdl = true;   // launch with programmatic stream serialization
 };
 
 // One dense contraction out[n][m] = sum_k W[m][k] * X[n][k]  (swap-AB: the
@@ -23,11 +24,12 @@ struct GemmOp {
   const void* X;  // [N, K] row stride ldx elements
   int N, ldx;
   // plain epilogue: out[n][m] fp32 (ld = M), stored or, with accumulate,
-  // added to.  With splits > 1 each split writes partial[s][n][m] and the
-  // last split to finish a tile (counters[tile], zero on entry and on exit)
-  // reduces the tile in split order.
+  // added to.  The bf16 path splits the work stream-K style over `ctas`
+  // CTAs (0: one per SM; -1: whole tiles, no pieces); tiles shared between
+  // CTAs go through `partial` (gemm_partial_bytes) and `counters`
+  // (kMaxSM ints, zero on entry and on exit).
   float* out;
-  int splits;
+  int ctas;
   float* partial;
   int* counters;
   bool accumulate;
@@ -39,37 +41,57 @@ struct GemmOp {
   float mult, cap;
 };
 
-// K-split count the launchers use for an M x N x K contraction on `nsm` SMs.
-int gemm_splits(int M, int N, int K, int nsm, bool topk);
+// Bytes of stream-K partial pieces an M x N contraction can need (any SM count).
+size_t gemm_partial_bytes(int M, int N);
 // Number of partial top-k lists a top-k GEMM of this shape writes.
 int gemm_topk_lists(int M, int N, int K, int nsm, int dtype);
 // Upper bound of the above over every SM count this library accepts.
 int gemm_max_lists();
-constexpr int kMaxSM = 256;
+constexpr int kMaxSM = 256;  // CTAs of a stream-K launch, and its counter array length
 
 // Host-side count of kernel launches (instrumentation).
 void count_launch(int n = 1);
 
-// Launches `kern` with programmatic stream serialization: it may start while
-// the previous kernel of the stream drains.  Every kernel of this library
-// calls pdl_wait() (griddepcontrol.wait) before it touches memory that an
-// earlier kernel writes, so only prologues (and, in the GEMM, the weight
-// stream, which nothing on the stream writes) overlap.  Counts the launch.
+// Launches `kern` on c.stream, counting the launch.  With c.pdl the launch
+// uses programmatic stream serialization: it may start while the previous
+// kernel of the stream drains.  Every kernel of this library calls pdl_wait()
+// (griddepcontrol.wait) before it touches memory that an earlier kernel
+// writes, so only prologues (and, in the GEMM, the weight stream, which
+// nothing on the stream writes) overlap.  The first kernel after a
+// cross-stream event wait is launched with c.pdl = false: its dependency on
+// the other stream must be a full one.  cluster_x > 1 groups the CTAs into
+// thread-block clusters of that many CTAs along x.
 template <typename... KArgs, typename... Args>
-inline int launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                    Args... args) {
+inline int launch_kx(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, const Ctx& c, int cluster_x,
+                     Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute at[2];
+  int n = 0;
+  if (c.pdl) {
+    at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 1) {
+    at[n].id = cudaLaunchAttributeClusterDimension;
+    at[n].val.clusterDim.x = cluster_x;
+    at[n].val.clusterDim.y = 1;
+    at[n].val.clusterDim.z = 1;
+    ++n;
+  }
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = n;
   count_launch();
   return cudaLaunchKernelEx(&cfg, kern, args...) == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+}
+
+template <typename... KArgs, typename... Args>
+inline int launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, const Ctx& c, Args... args) {
+  return launch_kx(kern, grid, block, smem, c, 1, args...);
 }
 
 // Byte offsets in the workspace of the draft step's intermediates
@@ -99,6 +121,16 @@ int launch_qkv_epilogue(int dtype, const float* Y, int rows, int B, int nq, int 
                         const void* k_norm, float eps, float theta, const int32_t* ctx_len, const int32_t* new_off,
                         void* q, void* kb, void* vb, const Ctx& c);
 int launch_act(int dtype, const float* Y, int rows, int I, void* act, const Ctx& c);
+// Fused sublayer prologue (RMSNorm, tap logits, two-tap conv) for each
+// sequence's B rows: from the residual h_in, or, with h_in == nullptr, from
+// the block embedding [anchor, mask...] (then h_out receives it).  Writes u
+// (normed, as stored) and u2 (after the conv).  conv_prologue_fits says
+// whether the B rows fit its shared memory; otherwise the caller runs
+// rownorm + tap GEMM + dyn_conv.
+bool conv_prologue_fits(int dtype, int batch, int B, int H, int G, int nsm);
+int launch_conv_prologue(int dtype, const float* h_in, const int32_t* anchor, int mask_id, const void* embed, int V,
+                         float scale, const void* gamma, float eps, const void* w_tap, int batch, int B, int H,
+                         int group_size, float* h_out, void* u_out, void* u2_out, const Ctx& c);
 
 // attention (attention.cu)
 int launch_attention(int dtype, const void* q, const void* kb, const void* vb, const void* kc, const void* vc,

@@ -84,12 +84,11 @@ int dflash2_select_path_static(const dflash2_config* cfg, const dflash2_weights*
     return DFLASH2_ERR_CUDA;
   if (maj != 10 || mi != 3) return DFLASH2_ERR_UNSUPPORTED;
   nsm = std::min(nsm, kMaxSM);
-  const int splits = c.dtype == DFLASH2_BF16 ? gemm_splits(2 * r, nsel, H, nsm, false) : 1;
-  const size_t o_cnt = 256;
-  const size_t o_x = o_cnt + al((size_t)gemm_tiles(2 * r, nsel) * sizeof(int));
+  // the factor contraction runs on whole tiles (no stream-K pieces), so the
+  // scratch holds only the gathered rows and the factors
+  const size_t o_x = 256;
   const size_t o_y = o_x + al((size_t)nsel * H * es);
-  const size_t o_p = o_y + al((size_t)nsel * 2 * r * sizeof(float));
-  const size_t need = o_p + (splits > 1 ? al((size_t)splits * nsel * 2 * r * sizeof(float)) : 0);
+  const size_t need = o_y + al((size_t)nsel * 2 * r * sizeof(float));
   if (need > kStaticScratchBytes) return DFLASH2_ERR_WORKSPACE;  // batch too large for the fixed scratch
   int err = DFLASH2_OK;
   char* base = static_cast<char*>(scratch_address(&err));
@@ -98,7 +97,7 @@ int dflash2_select_path_static(const dflash2_config* cfg, const dflash2_weights*
   ctx.stream = static_cast<cudaStream_t>(stream);
   ctx.status = reinterpret_cast<unsigned*>(base);
   ctx.nsm = nsm;
-  // the status word and the split-K tile counters must start at zero
+  // the status word must start at zero
   if (cudaMemsetAsync(base, 0, o_x, ctx.stream) != cudaSuccess) return DFLASH2_ERR_CUDA;
   int rc = launch_sel_gather(c.dtype, anchor, cand_id, batch, D, k, w->embed, c.vocab, H, base + o_x, ctx);
   if (rc) return rc;
@@ -112,9 +111,7 @@ int dflash2_select_path_static(const dflash2_config* cfg, const dflash2_weights*
   g.N = nsel;
   g.ldx = H;
   g.out = reinterpret_cast<float*>(base + o_y);
-  g.splits = splits;
-  g.partial = reinterpret_cast<float*>(base + o_p);
-  g.counters = reinterpret_cast<int*>(base + o_cnt);
+  g.ctas = -1;
   g.mult = 1.f;
   rc = c.dtype == DFLASH2_BF16 ? gemm_bf16(g, ctx) : gemm_f32(g, ctx);
   if (rc) return rc;

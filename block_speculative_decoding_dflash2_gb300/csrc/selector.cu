@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(256) sel_gather_kernel(const int32_t* __restri
   for (int m = threadIdx.x; m < H / PER; m += blockDim.x) dst[m] = tok < 0 ? make_uint4(0, 0, 0, 0) : src[m];
 }
 
-__global__ void __launch_bounds__(256) viterbi_kernel(const float* __restrict__ Y,
+__global__ void __launch_bounds__(512) viterbi_kernel(const float* __restrict__ Y,
                                                       const int32_t* __restrict__ cand_id,
                                                       const float* __restrict__ cand_logit, int D, int k, int r,
                                                       int32_t* __restrict__ path, float* __restrict__ path_score) {
@@ -60,29 +60,51 @@ __global__ void __launch_bounds__(256) viterbi_kernel(const float* __restrict__ 
   const int nt = D * k + 1, w = 2 * r, ws = w + 1;  // padded row stride: no bank conflicts across candidates
   float* F = sm;                               // [nt][ws] factors: A = F[t][0:r], Bf = F[t][r:2r]
   float* zs = F + (size_t)nt * ws;             // [D][k] candidate logits
-  float* Sm = zs + D * k;                      // [k][k] scores / totals
-  float* delta = Sm + k * k;                   // [k]
+  float* Sm = zs + D * k;                      // [1 + (D-1)k][k] transition log-probabilities
+  float* delta = Sm + (1 + (D - 1) * k) * k;   // [k]
   float* nd = delta + k;                       // [k]
   int* cid = reinterpret_cast<int*>(nd + k);   // [D][k] candidate ids
   int* bp = cid + D * k;                       // [D][k] back pointers
 
-  const float2* y = reinterpret_cast<const float2*>(Y + (size_t)s * nt * w);
-  const int w2 = w / 2;
-  constexpr int U = 8;  // loads in flight per thread
-  for (int base = threadIdx.x; base < nt * w2; base += blockDim.x * U) {
-    float2 v[U];
+  // stage the factors: U vector loads in flight per thread
+  constexpr int U = 8;
+  if ((w & 3) == 0) {
+    const float4* y = reinterpret_cast<const float4*>(Y + (size_t)s * nt * w);
+    const int w4 = w / 4, n4 = nt * w4;
+    for (int base = threadIdx.x; base < n4; base += blockDim.x * U) {
+      float4 v[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int idx = base + u * blockDim.x;
-      if (idx < nt * w2) v[u] = y[idx];
+      for (int u = 0; u < U; ++u)
+        if (base + u * blockDim.x < n4) v[u] = y[base + u * blockDim.x];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int idx = base + u * blockDim.x;
+        if (idx < n4) {
+          const int t = idx / w4, c = (idx - t * w4) * 4;
+          float* f = F + t * ws + c;
+          f[0] = v[u].x;
+          f[1] = v[u].y;
+          f[2] = v[u].z;
+          f[3] = v[u].w;
+        }
+      }
     }
+  } else {
+    const float2* y = reinterpret_cast<const float2*>(Y + (size_t)s * nt * w);
+    const int w2 = w / 2, n2 = nt * w2;
+    for (int base = threadIdx.x; base < n2; base += blockDim.x * U) {
+      float2 v[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int idx = base + u * blockDim.x;
-      if (idx < nt * w2) {
-        const int t = idx / w2, c = (idx - t * w2) * 2;
-        F[t * ws + c] = v[u].x;
-        F[t * ws + c + 1] = v[u].y;
+      for (int u = 0; u < U; ++u)
+        if (base + u * blockDim.x < n2) v[u] = y[base + u * blockDim.x];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int idx = base + u * blockDim.x;
+        if (idx < n2) {
+          const int t = idx / w2, c = (idx - t * w2) * 2;
+          F[t * ws + c] = v[u].x;
+          F[t * ws + c + 1] = v[u].y;
+        }
       }
     }
   }
@@ -98,14 +120,27 @@ __global__ void __launch_bounds__(256) viterbi_kernel(const float* __restrict__ 
     for (int c = 0; c < r; ++c) acc = fmaf(a[c], b[c], acc);
     return acc;
   };
-  // normalise each row p of Sm[p][0..k) into log-probabilities and add delta[p]
-  // (add_delta = false for the first position): one half-warp per row, lane
-  // j of the half holds column j (k <= 16), shuffle reductions stay in the half
-  auto row_logsoftmax = [&](int rows_, bool add_delta) {
+  // 1. every transition score at once (they do not depend on the DP): row 0 is
+  //    position 1 after the anchor; row 1 + (i-1)k + p is position i+1 after
+  //    candidate p of position i
+  const int nrow = 1 + (D - 1) * k;
+  for (int idx = threadIdx.x; idx < nrow * k; idx += blockDim.x) {
+    const int row = idx / k, j = idx - row * k;
+    if (row == 0) {
+      Sm[idx] = zs[j] + dot(0, 1 + j);
+    } else {
+      const int i = 1 + (row - 1) / k, p = (row - 1) % k;
+      Sm[idx] = zs[i * k + j] + dot(1 + (i - 1) * k + p, 1 + i * k + j);
+    }
+  }
+  __syncthreads();
+  // 2. each row -> log-probabilities (one half-warp per row, lane j of the
+  //    half holds column j, k <= 16; shuffles stay in the half)
+  {
     const int hw = threadIdx.x >> 4, j = threadIdx.x & 15, nhw = blockDim.x >> 4;
     const unsigned hmask = (threadIdx.x & 16) ? 0xffff0000u : 0x0000ffffu;
-    for (int p = hw; p < rows_; p += nhw) {
-      const float x = j < k ? Sm[p * k + j] : -INFINITY;
+    for (int row = hw; row < nrow; row += nhw) {
+      const float x = j < k ? Sm[row * k + j] : -INFINITY;
       float m = x;
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(hmask, m, o));
@@ -113,32 +148,25 @@ __global__ void __launch_bounds__(256) viterbi_kernel(const float* __restrict__ 
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(hmask, sum, o);
       const float lse = m + logf(sum);
-      if (j < k) Sm[p * k + j] = (add_delta ? delta[p] : 0.f) + (x - lse);
+      if (j < k) Sm[row * k + j] = x - lse;
     }
-  };
-  // position 1: the predecessor is the anchor (factor row 0)
-  for (int j = threadIdx.x; j < k; j += blockDim.x) Sm[j] = zs[j] + dot(0, 1 + j);
+  }
   __syncthreads();
-  row_logsoftmax(1, false);
-  __syncthreads();
+  // 3. the max-plus recurrence over positions
   for (int j = threadIdx.x; j < k; j += blockDim.x) delta[j] = Sm[j];
   __syncthreads();
   for (int i = 1; i < D; ++i) {
-    for (int pr = threadIdx.x; pr < k * k; pr += blockDim.x) {
-      const int p = pr / k, j = pr - p * k;
-      Sm[pr] = zs[i * k + j] + dot(1 + (i - 1) * k + p, 1 + i * k + j);
-    }
-    __syncthreads();
-    row_logsoftmax(k, true);
-    __syncthreads();
+    const float* T = Sm + (1 + (i - 1) * k) * k;  // [p][j]
     for (int j = threadIdx.x; j < k; j += blockDim.x) {
-      float best = Sm[j];
+      float best = delta[0] + T[j];
       int arg = 0;
-      for (int p = 1; p < k; ++p)
-        if (Sm[p * k + j] > best) {
-          best = Sm[p * k + j];
+      for (int p = 1; p < k; ++p) {
+        const float v = delta[p] + T[p * k + j];
+        if (v > best) {
+          best = v;
           arg = p;
         }
+      }
       nd[j] = best;
       bp[i * k + j] = arg;
     }
@@ -161,7 +189,8 @@ __global__ void __launch_bounds__(256) viterbi_kernel(const float* __restrict__ 
 }  // namespace
 
 size_t viterbi_smem_bytes(int D, int k, int r) {
-  return sizeof(float) * ((size_t)(D * k + 1) * (2 * r + 1) + (size_t)D * k + (size_t)k * k + 2 * (size_t)k) +
+  return sizeof(float) * ((size_t)(D * k + 1) * (2 * r + 1) + (size_t)D * k + (size_t)(1 + (D - 1) * k) * k +
+                          2 * (size_t)k) +
          sizeof(int) * 2 * (size_t)D * k;
 }
 
@@ -169,9 +198,9 @@ int launch_sel_gather(int dtype, const int32_t* anchor, const int32_t* cand_id, 
                       const void* embed, int V, int H, void* x_out, const Ctx& c) {
   const int rows = batch * (D * k + 1);
   if (dtype == DFLASH2_BF16)
-    return launch_k(sel_gather_kernel<bf16>, dim3(rows), dim3(128), 0, c.stream, anchor, cand_id, D, k,
+    return launch_k(sel_gather_kernel<bf16>, dim3(rows), dim3(128), 0, c, anchor, cand_id, D, k,
                     static_cast<const bf16*>(embed), V, H, static_cast<bf16*>(x_out), c.status);
-  return launch_k(sel_gather_kernel<float>, dim3(rows), dim3(128), 0, c.stream, anchor, cand_id, D, k,
+  return launch_k(sel_gather_kernel<float>, dim3(rows), dim3(128), 0, c, anchor, cand_id, D, k,
                   static_cast<const float*>(embed), V, H, static_cast<float*>(x_out), c.status);
 }
 
@@ -184,7 +213,7 @@ int launch_viterbi(const float* Y, const int32_t* cand_id, const float* cand_log
       return DFLASH2_ERR_CUDA;
     attr = true;
   }
-  return launch_k(viterbi_kernel, dim3(batch), dim3(256), smem, c.stream, Y, cand_id, cand_logit, D, k, r, path,
+  return launch_k(viterbi_kernel, dim3(batch), dim3(512), smem, c, Y, cand_id, cand_logit, D, k, r, path,
                   path_score);
 }
 

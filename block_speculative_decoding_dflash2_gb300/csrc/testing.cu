@@ -33,17 +33,17 @@ using namespace df2;
 
 extern "C" {
 
-size_t dflash2_test_gemm_workspace(int M, int N, int splits) {
+size_t dflash2_test_gemm_workspace(int M, int N) {
   if (M <= 0 || N <= 0) return 0;
-  const int s = std::max(1, std::min(64, splits > 0 ? splits : 64));
-  return al((size_t)gemm_tiles(M, N) * sizeof(int)) + al((size_t)s * N * M * sizeof(float));
+  return al((size_t)kMaxSM * sizeof(int)) + al(gemm_partial_bytes(M, N));
 }
 
-int dflash2_test_gemm(int dtype, const void* W, int M, int K, const void* X, int N, int splits, int accumulate,
+int dflash2_test_gemm(int dtype, const void* W, int M, int K, const void* X, int N, int ctas, int accumulate,
                       float* out, void* workspace, size_t ws_bytes, void* stream) {
   if (dtype != DFLASH2_BF16 && dtype != DFLASH2_F32) return DFLASH2_ERR_DTYPE;
   if (!W || !X || !out || !workspace) return DFLASH2_ERR_INVALID_ARG;
   if (M <= 0 || N <= 0 || K <= 0) return DFLASH2_ERR_SHAPE;
+  if (ws_bytes < dflash2_test_gemm_workspace(M, N)) return DFLASH2_ERR_WORKSPACE;
   Ctx c;
   const int rc = test_ctx(&c, stream, nullptr);
   if (rc) return rc;
@@ -59,19 +59,20 @@ int dflash2_test_gemm(int dtype, const void* W, int M, int K, const void* X, int
   g.out = out;
   g.accumulate = accumulate != 0;
   g.mult = 1.f;
-  if (dtype == DFLASH2_F32) {
-    g.splits = 1;
-  } else {
-    const int chunks = (K + 63) / 64;
-    g.splits = splits > 0 ? std::min(std::min(splits, 64), chunks) : gemm_splits(M, N, K, c.nsm, false);
-  }
+  g.ctas = ctas < 0 ? -1 : std::min(ctas, kMaxSM);
   char* base = static_cast<char*>(workspace);
   g.counters = reinterpret_cast<int*>(base);
-  g.partial = reinterpret_cast<float*>(base + al((size_t)gemm_tiles(M, N) * sizeof(int)));
-  if (al((size_t)gemm_tiles(M, N) * sizeof(int)) + (size_t)g.splits * N * M * sizeof(float) > ws_bytes)
-    return DFLASH2_ERR_WORKSPACE;
-  const int r = dtype == DFLASH2_BF16 ? gemm_bf16(g, c) : gemm_f32(g, c);
-  return r ? r : g.splits;
+  g.partial = reinterpret_cast<float*>(base + al((size_t)kMaxSM * sizeof(int)));
+  if (dtype == DFLASH2_F32) {
+    const int r = gemm_f32(g, c);
+    return r ? r : 1;
+  }
+  const int r = gemm_bf16(g, c);
+  if (r) return r;
+  // the CTA count gemm_bf16 launched
+  const long tiles = (long)gemm_tiles(M, N), work = tiles * ((K + 63) / 64);
+  if (g.ctas < 0) return (int)std::min<long>(tiles, c.nsm);
+  return (int)std::min<long>(g.ctas > 0 ? g.ctas : c.nsm, work);
 }
 
 int dflash2_test_layout(const dflash2_config* cfg, int batch, int n_new, int max_ctx, size_t* offsets, int n) {
@@ -112,7 +113,6 @@ int dflash2_test_gemm_topk(int dtype, const void* W, int M, int K, const void* X
   g.mult = mult;
   g.cap = cap;
   if (dtype == DFLASH2_BF16) {
-    g.splits = 1;
     g.topk = true;
     g.lists_v = lv;
     g.lists_i = li;
@@ -122,7 +122,6 @@ int dflash2_test_gemm_topk(int dtype, const void* W, int M, int K, const void* X
     n_lists = gemm_topk_lists(M, N, K, c.nsm, dtype);
   } else {
     float* logits = reinterpret_cast<float*>(base + al(256) + 2 * al((size_t)n_lists_cap * N * KMAX * 4));
-    g.splits = 1;
     g.out = logits;
     rc = gemm_f32(g, c);
     if (rc) return rc;

@@ -142,7 +142,7 @@ int launch_topk_scan(const float* logits, int rows, int V, float mult, float cap
   const int chunks = scan_chunks(V);
   const int len = (V + chunks - 1) / chunks;
   *n_lists = chunks * 4;
-  return launch_k(topk_scan_kernel, dim3(chunks, rows), dim3(128), 0, c.stream, logits, rows, V, len, mult, cap,
+  return launch_k(topk_scan_kernel, dim3(chunks, rows), dim3(128), 0, c, logits, rows, V, len, mult, cap,
                   debug, lists_v, lists_i);
 }
 
@@ -150,7 +150,7 @@ int launch_topk_merge(const float* lists_v, const int* lists_i, int n_lists, int
                       float* cand_logit, const Ctx& c) {
   if (n_lists < 1 || n_lists > 256 || k > KMAX) return DFLASH2_ERR_SHAPE;
   const size_t smem = (size_t)n_lists * KMAX * 8;  // <= 32 KB
-  return launch_k(topk_merge_kernel, dim3(rows), dim3(256), smem, c.stream, lists_v, lists_i, n_lists, rows, k,
+  return launch_k(topk_merge_kernel, dim3(rows), dim3(256), smem, c, lists_v, lists_i, n_lists, rows, k,
                   cand_id, cand_logit);
 }
 

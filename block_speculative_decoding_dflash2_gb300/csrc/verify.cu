@@ -51,7 +51,8 @@ int launch_verify(int batch, int B, const int32_t* path, const int32_t* target, 
                   int32_t* out_tok, int32_t* n_out, int32_t* next_anchor, int32_t* seq_len, int64_t* counters,
                   cudaStream_t st) {
   const int threads = 128;
-  return launch_k(verify_kernel, dim3((batch + threads - 1) / threads), dim3(threads), 0, st, batch, B, path, target,
+  const Ctx c{st, nullptr, 0, true};
+  return launch_k(verify_kernel, dim3((batch + threads - 1) / threads), dim3(threads), 0, c, batch, B, path, target,
                   accept_len, out_tok, n_out, next_anchor, seq_len, counters);
 }
 

@@ -8,9 +8,10 @@ Kernels:
             (vocab 151936 x hidden 4096 bf16, 7 block rows, top-16) through
             the dflash2_test_gemm_topk hook, then the top-k merge;
   gate_up   the MLP gate/up contraction (24576 x 4096, 8 rows);
-  fc        the feature projection (4096 x 12288, 8 rows, split-K).
+  fc, qkv, down, o   the other contractions of the 8B-shaped draft step.
 Weights are seeded N(0, 0.02) bf16 drawn on the device (timing only; no
-parity is checked here).  Prints the mean CUDA-event time per launch.
+parity is checked here).  L2 is flushed (a 256 MiB write) before every
+launch; prints the mean CUDA-event time per launch.
 """
 
 import argparse
@@ -28,7 +29,8 @@ def main():
     p = argparse.ArgumentParser()
     p.add_argument("--kernel", default="lm_head", choices=sorted(SHAPES))
     p.add_argument("--launches", type=int, default=3)
-    p.add_argument("--splits", type=int, default=0, help="K splits (0: the library's choice)")
+    p.add_argument("--ctas", type=int, default=0,
+                   help="contraction schedule: 0 = the library's, >0 = stream-K over that many CTAs, <0 = whole tiles")
     a = p.parse_args()
     build()
     M, K, N = SHAPES[a.kernel]
@@ -44,18 +46,22 @@ def main():
         run = lambda: B.dflash2_test_gemm_topk(B.BF16, W, X, 16, 1.0, 0.0, cid, cz, None, ws)
     else:
         out = torch.empty((N, M), dtype=torch.float32, device="cuda")
-        ws = torch.zeros(B.dflash2_test_gemm_workspace(M, N, a.splits), dtype=torch.uint8, device="cuda")
-        run = lambda: B.dflash2_test_gemm(B.BF16, W, X, a.splits, out, ws)
+        ws = torch.zeros(B.dflash2_test_gemm_workspace(M, N), dtype=torch.uint8, device="cuda")
+        run = lambda: B.dflash2_test_gemm(B.BF16, W, X, a.ctas, out, ws)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     run()
     torch.cuda.synchronize()
-    e0.record()
+    total = 0.0
     for _ in range(a.launches):
+        flush.zero_()
+        e0.record()
         run()
-    e1.record()
-    e1.synchronize()
-    ms = e0.elapsed_time(e1) / a.launches
+        e1.record()
+        e1.synchronize()
+        total += e0.elapsed_time(e1)
+    ms = total / a.launches
     gb = M * K * 2 / 1e9
-    print(f"{a.kernel}: M={M} K={K} N={N} splits={a.splits}: {ms * 1e3:.1f} us per call, "
+    print(f"{a.kernel}: M={M} K={K} N={N} ctas={a.ctas}: {ms * 1e3:.1f} us per call, "
           f"{gb / (ms / 1e3):.0f} GB/s of weights")
 
 

@@ -21,17 +21,19 @@ extern "C" {
 /*
  * out[n][m] = sum_k W[m][k] * X[n][k]   (or out[n][m] += ... with accumulate),
  * through the library's contraction: W X^T stored transposed, fp32.
- *   dtype      DFLASH2_BF16 (tcgen05 path) or DFLASH2_F32 (SIMT path, 1 split)
+ *   dtype      DFLASH2_BF16 (tcgen05 path) or DFLASH2_F32 (SIMT path)
  *   W          [M, K], X [N, K], row-major, element type = dtype
- *   splits     K splits (bf16: 1..64, clamped to ceil(K/64); <= 0 picks the
- *              library's own choice); with several splits the last split to
- *              finish each tile reduces the partials in split order
+ *   ctas       bf16 work schedule: 0 = the library's own (stream-K shares of
+ *              all tile x K-chunk work, one CTA per SM); > 0 = stream-K over
+ *              that many CTAs (at most 256; tiles shared by several CTAs are
+ *              summed by the last piece to arrive, in CTA order); < 0 =
+ *              whole tiles, one CTA each, round-robin.  Ignored for f32.
  *   out        float [N][M]
  *   workspace  zeroed on first use, at least dflash2_test_gemm_workspace bytes
- * Returns the number of splits used (>= 1) or a negative status.
+ * Returns the number of CTAs launched (>= 1) or a negative status.
  */
-size_t dflash2_test_gemm_workspace(int M, int N, int splits);
-int dflash2_test_gemm(int dtype, const void *W, int M, int K, const void *X, int N, int splits, int accumulate,
+size_t dflash2_test_gemm_workspace(int M, int N);
+int dflash2_test_gemm(int dtype, const void *W, int M, int K, const void *X, int N, int ctas, int accumulate,
                       float *out, void *workspace, size_t ws_bytes, void *stream);
 
 /*
@@ -50,7 +52,11 @@ int dflash2_test_gemm(int dtype, const void *W, int M, int K, const void *X, int
  *   [9] hn   [batch*(B-1), H]  final-normed hidden states of positions 1..B-1
  *  [10] ua   [batch*B, H]      normed input of the last attention sublayer
  *  [11] u2a  [batch*B, H]      that input after the dynamic convolution
- * Element type is cfg.dtype except h.  `n` must be >= 12.  Host only.
+ *  [12] cnt  int[]             split-K tile counters of the block branch
+ *  [13] cnta int[]             split-K tile counters of the append branch
+ * Element type is cfg.dtype except h.  `n` must be >= 14.  Host only.
+ * The counters (zero between calls) must sit at the same offsets for every
+ * call shape, dflash2_append_context (batch 0) included.
  */
 int dflash2_test_layout(const dflash2_config *cfg, int batch, int n_new, int max_ctx, size_t *offsets, int n);
 

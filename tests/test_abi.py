@@ -86,6 +86,20 @@ def test_workspace_size_is_monotone(B, name):
             assert B.dflash2_workspace_size(c, b, n, 512) <= B.dflash2_workspace_size(c, 8, 64, 512)
 
 
+@pytest.mark.parametrize("name", ["tiny_fp32", "qwen3_8b_b1", "qwen3_27b_b8"])
+def test_counter_regions_do_not_move_between_calls(B, name):
+    # split-K tile counters are left at zero by one call and must be zero at
+    # the next: their offsets may not depend on the call's shape (the
+    # context append plans its workspace with batch 0)
+    c = _cfg(B, name)
+    seen = {(o["cnt"], o["cnta"]) for o in (B.dflash2_test_layout(c, b, n, ctx)
+                                           for b, n, ctx in [(0, 333, 0), (0, 1, 0), (1, 8, 2048),
+                                                             (2, 20, 512), (8, 300, 4096)])}
+    assert len(seen) == 1
+    cnt, cnta = seen.pop()
+    assert cnt < cnta and cnta - cnt >= 128 * 4
+
+
 def test_host_side_error_paths_return_before_cuda(B):
     L = B.lib()
     # verify: bad block size / batch / null pointers

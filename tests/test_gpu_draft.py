@@ -52,6 +52,15 @@ def test_small_bf16_paged_ragged_batch():
     check_case(case)
 
 
+def test_fp32_rows_beyond_fused_prologue():
+    # 32 block rows x 2048 fp32 channels (256 KiB) exceed the fused sublayer
+    # prologue's shared memory: norm, tap GEMM and conv run as three kernels
+    cfg = S.config_of("tiny_fp32", hidden=2048, n_taps=1, intermediate=512, vocab=1000, n_layers=2,
+                      block_size=32, top_k=4, index=17)
+    case = Case(cfg, ctx_lens=[50], n_new=[32], seed=17).run_gpu()
+    check_case(case)
+
+
 def test_small_bf16_block16_and_groups():
     cfg = S.small_bf16_config(block_size=16, n_q_heads=8, n_kv_heads=2, head_dim=128, top_k=16,
                               conv_group_size=64, index=12)

@@ -16,33 +16,36 @@ def _mat(rows, cols, seed, std, dtype):
     return S._draw(seed, f"m{rows}x{cols}", (rows, cols), std, dtype)
 
 
-@pytest.mark.parametrize("M,N,K,splits", [
-    (128, 16, 64, 1),        # one tile, one K chunk
-    (256, 8, 4096, 0),       # library split-K choice
-    (1000, 7, 256, 1),       # ragged M tile, N below the MMA width
+@pytest.mark.parametrize("M,N,K,ctas", [
+    (128, 16, 64, 0),        # one tile, one K chunk
+    (256, 8, 4096, 0),       # the library's stream-K schedule
+    (1000, 7, 256, 5),       # ragged M tile, N below the MMA width, pieces across tiles
     (1000, 17, 520, 3),      # ragged M and ragged K tail, N -> 32-wide tile
-    (384, 100, 1024, 2),     # 128-wide activation tile
-    (512, 256, 512, 1),      # 256-wide activation tile
-    (300, 300, 128, 1),      # two activation tiles, ragged everywhere
+    (384, 100, 1024, 7),     # 128-wide activation tile
+    (512, 256, 512, -1),     # 256-wide activation tile, whole tiles
+    (300, 300, 128, 11),     # two activation tiles, ragged everywhere
     (4096, 8, 12288, 0),     # feature projection shape (8B)
     (6144, 8, 4096, 0),      # QKV shape (8B)
-    (4096, 8, 4096, 64),     # one K chunk per split: 64-way in-kernel reduction
+    (24576, 8, 4096, 0),     # gate/up shape (8B): 1.26 tiles per CTA
+    (4096, 8, 4096, 256),    # 8 K chunks per CTA: 8 pieces per tile
+    (4096, 8, 4096, 1),      # one CTA streams every tile whole
+    (1000, 7, 256, -1),      # whole tiles round-robin
 ])
 @pytest.mark.parametrize("accumulate", [False, True])
-def test_bf16_gemm_matches_float64_product(M, N, K, splits, accumulate):
+def test_bf16_gemm_matches_float64_product(M, N, K, ctas, accumulate):
     import torch
     B = lib()
     W = _mat(M, K, 1, 0.05, "bf16")
     X = _mat(N, K, 2, 1.0, "bf16")
     base = np.random.default_rng(3).standard_normal((N, M)).astype(np.float32)
     out = torch.from_numpy(base).cuda() if accumulate else torch.full((N, M), float("nan"), device="cuda")
-    ws = torch.zeros(B.dflash2_test_gemm_workspace(M, N, splits), dtype=torch.uint8, device="cuda")
-    for rep in range(2):  # twice: the tile counters must come back to zero
+    ws = torch.zeros(B.dflash2_test_gemm_workspace(M, N), dtype=torch.uint8, device="cuda")
+    for rep in range(2):  # twice: the arrival counters must come back to zero
         if accumulate and rep == 1:
             out.copy_(torch.from_numpy(base))
-        used = B.dflash2_test_gemm(B.BF16, S.to_torch(W), S.to_torch(X), splits, out, ws, accumulate)
+        used = B.dflash2_test_gemm(B.BF16, S.to_torch(W), S.to_torch(X), ctas, out, ws, accumulate)
         torch.cuda.synchronize()
-        assert 1 <= used <= 64
+        assert 1 <= used <= 256 and (ctas <= 0 or used <= ctas)
         got = out.double().cpu().numpy() - (base if accumulate else 0.0)
         w64, x64 = W.values.astype(np.float64), X.values.astype(np.float64)
         ref = x64 @ w64.T
@@ -50,7 +53,24 @@ def test_bf16_gemm_matches_float64_product(M, N, K, splits, accumulate):
         err = np.abs(got - ref)
         assert np.all(np.isfinite(got))
         assert np.all(err <= 1e-4 * bound + 1e-6), float(np.max(err / (bound + 1e-30)))
-    assert int(ws[:4 * ((M + 127) // 128)].view(torch.int32).abs().sum()) == 0
+        assert int(ws[:4 * 256].view(torch.int32).abs().sum()) == 0
+
+
+def test_bf16_gemm_is_deterministic():
+    # pieces of shared tiles are summed in CTA order: bit-identical reruns
+    import torch
+    B = lib()
+    M, N, K = 4096, 8, 12288
+    W = S.to_torch(_mat(M, K, 5, 0.05, "bf16"))
+    X = S.to_torch(_mat(N, K, 6, 1.0, "bf16"))
+    ws = torch.zeros(B.dflash2_test_gemm_workspace(M, N), dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(3):
+        out = torch.empty((N, M), device="cuda")
+        B.dflash2_test_gemm(B.BF16, W, X, 0, out, ws)
+        outs.append(out.cpu())
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
 
 
 @pytest.mark.parametrize("M,N,K", [(1000, 7, 256), (4096, 8, 768), (130, 40, 64)])
@@ -60,7 +80,7 @@ def test_f32_gemm_matches_float64_product(M, N, K):
     W = _mat(M, K, 3, 0.05, "f32")
     X = _mat(N, K, 4, 1.0, "f32")
     out = torch.full((N, M), float("nan"), device="cuda")
-    ws = torch.zeros(B.dflash2_test_gemm_workspace(M, N, 1), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(B.dflash2_test_gemm_workspace(M, N), dtype=torch.uint8, device="cuda")
     assert B.dflash2_test_gemm(B.F32, S.to_torch(W), S.to_torch(X), 0, out, ws) == 1
     torch.cuda.synchronize()
     got = out.double().cpu().numpy()

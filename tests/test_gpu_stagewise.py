@@ -171,3 +171,12 @@ def test_stagewise_qwen3_8b_shape():
     cfg = S.config_of("qwen3_8b_b1")
     case = Case(cfg, ctx_lens=[2040], n_new=[8], seed=17).run_gpu()
     run_stagewise(case)
+
+
+def test_stagewise_gqa5_block16():
+    # 80 query rows per kv head (5 q heads x 16 block rows), two contexts
+    # that end mid-page, 16 + 4 appended rows split along K in the projection
+    cfg = S.small_bf16_config(block_size=16, n_q_heads=10, n_kv_heads=2, head_dim=128, top_k=16, hidden=512,
+                              n_layers=1, index=16)
+    case = Case(cfg, ctx_lens=[300, 33], n_new=[16, 4], seed=18).run_gpu()
+    run_stagewise(case)

@@ -39,8 +39,8 @@ L2_FLUSH_BYTES = 256 << 20
 def args_():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=50)
-    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=WORKLOAD)
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -96,7 +96,7 @@ class Clocks:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
@@ -132,6 +132,27 @@ class Clocks:
             out.update(sm_mhz=statistics.median(sm), sm_max_mhz=max(mx), samples=len(sm))
         out["reasons"] = sorted(reasons)
         return out
+
+
+# ---------------------------------------------------------------- ranks
+
+def max_over_ranks(x, device):
+    """The largest x over the ranks of the default process group (x alone
+    without one): the slowest replica sets the whole job's time."""
+    import torch
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return x
+    if torch.distributed.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(steps, world, max_total_ms):
+    """Steps/s of the whole job: every replica ran `steps` steps of its own
+    sequences (weak scaling), in at most max_total_ms."""
+    return world * steps / (max_total_ms / 1e3)
 
 
 # ---------------------------------------------------------------- our arm
@@ -213,7 +234,7 @@ def run_ours(a, rank, world):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clk.start()
-    time.sleep(0.3)
+    time.sleep(0.2)  # let the sampler start; the timed steps below run for about a second
     step_ms, lm_ms, stage_ms = [], [], [[] for _ in range(4)]
     for _ in range(a.steps):
         flush.zero_()
@@ -229,11 +250,7 @@ def run_ours(a, rank, world):
     if world > 1:
         torch.distributed.barrier()
     clocks = clk.stop()
-    total_ms = sum(step_ms)
-    if world > 1:
-        tt = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(sum(step_ms), "cuda")
     assert r.device_status() == 0
 
     # end to end through the public API with host buffers (pinned), per step:
@@ -277,18 +294,14 @@ def run_ours(a, rank, world):
         t1.record()
         t1.synchronize()
         e2e_ms.append(t0.elapsed_time(t1))
-    e2e_total = sum(e2e_ms)
-    if world > 1:
-        tt = torch.tensor([e2e_total], device="cuda")
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_total = float(tt.item())
+    e2e_total = max_over_ranks(sum(e2e_ms), "cuda")
 
     pk, src = peaks()
     bytes_, flops, lm_bytes = work_model(cfg, [int(x) for x in ctx], [int(x) for x in n_new])
     lm_avg_s = statistics.mean(lm_ms) / 1e3
     step_s = total_ms / a.steps / 1e3
     lm_ach = lm_bytes / lm_avg_s / 1e9
-    steps_per_s = world * a.steps / (total_ms / 1e3)
+    steps_per_s = whole_job_rate(a.steps, world, total_ms)
     res = {
         "metric": METRIC,
         "value": steps_per_s,
@@ -324,7 +337,7 @@ def run_ours(a, rank, world):
                      "algorithmic_bytes": lm_bytes, "avg_launch_us": lm_avg_s * 1e6,
                      "peak_source": f"{src} (burst copy GB/s)"},
         "clocks": clocks,
-        "e2e": {"value": world * a.steps / (e2e_total / 1e3), "unit": "draft steps/s",
+        "e2e": {"value": whole_job_rate(a.steps, world, e2e_total), "unit": "draft steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "api": "dflash2_draft_step + dflash2_select_path + dflash2_verify_accept, eager"},
         "gpu_launches": launches_per_step * a.steps,

@@ -12,6 +12,7 @@
 //   (c) lm_head GEMM with streaming top-k -> merge
 //   (d) selector gather -> factor GEMM -> Viterbi;  verify/accept
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <cstring>
 #include <mutex>
@@ -78,7 +79,7 @@ int check_config(const dflash2_config* c) {
 
 struct Layout {
   size_t status, cnt, cnta, f, Y, P, Ya, Pa, h, u, u2, ua, u2a, q, kb, vb, attn, O, act, hn, logits, lv, li, selx,
-      total;
+      rope, ropea, dsta, total;
 };
 
 Layout plan(const dflash2_config& c, int batch, int n_new, int max_ctx) {
@@ -141,6 +142,9 @@ Layout plan(const dflash2_config& c, int batch, int n_new, int max_ctx) {
   L.lv = take((size_t)n_lists * batch * D * KMAX * 4);
   L.li = take((size_t)n_lists * batch * D * KMAX * 4);
   L.selx = take((size_t)nsel * H * es);
+  L.rope = take((size_t)rows * (d / 2) * sizeof(float2));     // block rows' RoPE table
+  L.ropea = take((size_t)n_new * (d / 2) * sizeof(float2));   // appended rows' RoPE table
+  L.dsta = take((size_t)n_new * sizeof(long long));           // appended rows' cache offsets
   L.total = o;
   return L;
 }
@@ -211,6 +215,27 @@ P* at(void* ws, size_t off) {
 // out[n][m] (= or +=) sum_k W[m][k] X[n][k]; split-K partials and tile
 // counters live in the workspace regions of L (the append branch's own
 // regions when `append_branch`, since it runs concurrently with the block).
+GemmOp gemm_op(const void* W, int M, int K, const void* X, int N) {
+  GemmOp g;
+  std::memset(&g, 0, sizeof(g));
+  g.W = W;
+  g.M = M;
+  g.K = K;
+  g.ldw = K;
+  g.X = X;
+  g.N = N;
+  g.ldx = K;
+  g.mult = 1.f;
+  return g;
+}
+
+// A bf16 contraction with a fused epilogue (partials/counters of its branch).
+int gemm_fused(GemmOp g, const Ctx& ctx, void* ws, const Layout& L, bool append_branch) {
+  g.partial = reinterpret_cast<float*>(static_cast<char*>(ws) + (append_branch ? L.Pa : L.P));
+  g.counters = reinterpret_cast<int*>(static_cast<char*>(ws) + (append_branch ? L.cnta : L.cnt));
+  return gemm_bf16(g, ctx);
+}
+
 int gemm(const dflash2_config& c, const Ctx& ctx, void* ws, const Layout& L, const void* W, int M, int K,
          const void* X, int N, float* out, bool accumulate, bool append_branch = false) {
   GemmOp g;
@@ -259,16 +284,49 @@ int run_append(const dflash2_config& c, const dflash2_weights& w, void* kc, void
   TRY(gemm(c, ctx, ws, L, w.fc, H, c.n_taps * H, taps, n_new, Y, false, true));
   Ctx rest = ctx;
   rest.pdl = true;
-  TRY(launch_rows_feature_norm(c.dtype, Y, n_new, H, w.hidden_norm, c.rms_eps, f, rest));
+  const bool fused_kv = c.dtype == DFLASH2_BF16 && gemm_fusable(2 * nkv * d, n_new, kEpiHeads);
+  RopeTab rt;
+  std::memset(&rt, 0, sizeof(rt));
+  if (fused_kv) {  // the feature norm also leaves the appended rows' RoPE angles and cache offsets
+    rt.cs = at<float2>(ws, L.ropea);
+    rt.dst = at<long long>(ws, L.dsta);
+    rt.d = d;
+    rt.freq = rope_freq(d, c.rope_theta);
+    rt.ctx_len = ctx_len;
+    rt.new_off = new_off;
+    rt.batch = batch;
+    rt.block_table = block_table;
+    rt.max_pages = max_pages;
+    rt.page_size = c.page_size;
+    rt.n_pages = n_pages;
+    rt.nkv = nkv;
+  }
+  TRY(launch_rows_feature_norm(c.dtype, Y, n_new, H, w.hidden_norm, c.rms_eps, f, rt, rest));
   const size_t layer_elems = (size_t)n_pages * c.page_size * nkv * d;
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash2_layer_weights& Lw = w.layers[l];
     const void* wkv = elem_ptr(Lw.qkv, (size_t)nq * d * H, c.dtype);
-    TRY(gemm(c, rest, ws, L, wkv, 2 * nkv * d, H, f, n_new, Y, false, true));
-    TRY(launch_kv_append(c.dtype, Y, n_new, nkv, d, Lw.k_norm, c.rms_eps, c.rope_theta, ctx_len, new_off, batch,
-                         block_table, max_pages, c.page_size, n_pages,
-                         const_cast<char*>(elem_ptr(kc, l * layer_elems, c.dtype)),
-                         const_cast<char*>(elem_ptr(vc, l * layer_elems, c.dtype)), rest));
+    char* kcl = const_cast<char*>(elem_ptr(kc, l * layer_elems, c.dtype));
+    char* vcl = const_cast<char*>(elem_ptr(vc, l * layer_elems, c.dtype));
+    if (fused_kv) {
+      // K/V epilogue fused: k-norm + RoPE + paged store of the appended rows
+      GemmOp g = gemm_op(wkv, 2 * nkv * d, H, f, n_new);
+      g.epi = kEpiHeads;
+      g.hd = d;
+      g.n_kh = nkv;
+      g.kn = Lw.k_norm;
+      g.eps = c.rms_eps;
+      g.rope = at<float2>(ws, L.ropea);
+      g.dst = at<long long>(ws, L.dsta);
+      g.append = 1;
+      g.kc = kcl;
+      g.vc = vcl;
+      TRY(gemm_fused(g, rest, ws, L, true));
+    } else {
+      TRY(gemm(c, rest, ws, L, wkv, 2 * nkv * d, H, f, n_new, Y, false, true));
+      TRY(launch_kv_append(c.dtype, Y, n_new, nkv, d, Lw.k_norm, c.rms_eps, c.rope_theta, ctx_len, new_off, batch,
+                           block_table, max_pages, c.page_size, n_pages, kcl, vcl, rest));
+    }
   }
   return DFLASH2_OK;
 }
@@ -282,6 +340,13 @@ int check_cache_args(void* kc, void* vc, int n_pages, const int32_t* block_table
 }
 
 }  // namespace
+
+RopeFreq rope_freq(int d, float theta) {
+  RopeFreq f;
+  const double l2t = std::log2((double)theta);
+  for (int i = 0; i < 64; ++i) f.inv[i] = 2 * i < d ? std::exp2(-(2.0 * i / d) * l2t) : 0.0;
+  return f;
+}
 
 void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
@@ -410,28 +475,56 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
   // sublayer prologues: one fused kernel (norm, tap logits, conv) when the
   // sequence's B rows fit its shared memory, else norm + tap GEMM + conv
   const bool fused = conv_prologue_fits(c.dtype, batch, B, H, G, ctx.nsm);
+  const bool fused_qkv = c.dtype == DFLASH2_BF16 && gemm_fusable((nq + 2 * nkv) * d, rows, kEpiHeads);
+  RopeTab rt;  // the block rows' RoPE angles, left by the first kernel for the fused QKV epilogues
+  std::memset(&rt, 0, sizeof(rt));
+  if (fused_qkv) {
+    rt.cs = at<float2>(workspace, L.rope);
+    rt.d = d;
+    rt.freq = rope_freq(d, c.rope_theta);
+    rt.ctx_len = ctx_len;
+    rt.new_off = new_off;
+    rt.batch = batch;
+  }
   if (fused)
     TRY(launch_conv_prologue(c.dtype, nullptr, anchor, c.mask_token_id, w->embed, c.vocab, c.input_embedding_scale,
                              w->layers[0].attn_norm, c.rms_eps, w->layers[0].tapgen_attn, batch, B, H,
-                             c.conv_group_size, h, ua, u2a, ctx));
+                             c.conv_group_size, h, ua, u2a, rt, ctx));
   else
     TRY(launch_embed_norm(c.dtype, anchor, c.mask_token_id, batch, B, w->embed, c.vocab, H, c.input_embedding_scale,
-                          w->layers[0].attn_norm, c.rms_eps, h, ua, ctx));
+                          w->layers[0].attn_norm, c.rms_eps, h, ua, rt, ctx));
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash2_layer_weights& Lw = w->layers[l];
     // attention sublayer: conv around the normed input, QKV, attention, O (+= residual)
     if (fused) {
       if (l > 0)
         TRY(launch_conv_prologue(c.dtype, h, nullptr, 0, w->embed, c.vocab, 1.f, Lw.attn_norm, c.rms_eps,
-                                 Lw.tapgen_attn, batch, B, H, c.conv_group_size, nullptr, ua, u2a, ctx));
+                                 Lw.tapgen_attn, batch, B, H, c.conv_group_size, nullptr, ua, u2a, RopeTab{}, ctx));
     } else {
       if (l > 0) TRY(launch_rownorm(c.dtype, h, rows, H, Lw.attn_norm, c.rms_eps, ua, B, 0, ctx));
       TRY(gemm(c, ctx, ws, L, Lw.tapgen_attn, 2 * G, H, ua, rows, Y, false));
       TRY(launch_dyn_conv(c.dtype, ua, Y, rows, H, c.conv_group_size, B, u2a, ctx));
     }
-    TRY(gemm(c, ctx, ws, L, Lw.qkv, (nq + 2 * nkv) * d, H, u2a, rows, Y, false));
-    TRY(launch_qkv_epilogue(c.dtype, Y, rows, B, nq, nkv, d, Lw.q_norm, Lw.k_norm, c.rms_eps, c.rope_theta, ctx_len,
-                            new_off, q, kb, vb, ctx));
+    if (fused_qkv) {
+      // q/k-norm + RoPE fused into the QKV epilogue
+      GemmOp g = gemm_op(Lw.qkv, (nq + 2 * nkv) * d, H, u2a, rows);
+      g.epi = kEpiHeads;
+      g.hd = d;
+      g.n_qh = nq;
+      g.n_kh = nkv;
+      g.qn = Lw.q_norm;
+      g.kn = Lw.k_norm;
+      g.eps = c.rms_eps;
+      g.rope = at<float2>(ws, L.rope);
+      g.q = q;
+      g.kb = kb;
+      g.vb = vb;
+      TRY(gemm_fused(g, ctx, ws, L, false));
+    } else {
+      TRY(gemm(c, ctx, ws, L, Lw.qkv, (nq + 2 * nkv) * d, H, u2a, rows, Y, false));
+      TRY(launch_qkv_epilogue(c.dtype, Y, rows, B, nq, nkv, d, Lw.q_norm, Lw.k_norm, c.rms_eps, c.rope_theta,
+                              ctx_len, new_off, q, kb, vb, ctx));
+    }
     // the attention reads the appended K/V: a full dependency on the join
     Ctx jctx = ctx;
     if (forked && l == 0) {
@@ -445,14 +538,21 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
     // MLP sublayer: conv around the normed input, gate/up, SiLU*up, down (+= residual)
     if (fused) {
       TRY(launch_conv_prologue(c.dtype, h, nullptr, 0, w->embed, c.vocab, 1.f, Lw.mlp_norm, c.rms_eps, Lw.tapgen_mlp,
-                               batch, B, H, c.conv_group_size, nullptr, u, u2, ctx));
+                               batch, B, H, c.conv_group_size, nullptr, u, u2, RopeTab{}, ctx));
     } else {
       TRY(launch_rownorm(c.dtype, h, rows, H, Lw.mlp_norm, c.rms_eps, u, B, 0, ctx));
       TRY(gemm(c, ctx, ws, L, Lw.tapgen_mlp, 2 * G, H, u, rows, Y, false));
       TRY(launch_dyn_conv(c.dtype, u, Y, rows, H, c.conv_group_size, B, u2, ctx));
     }
-    TRY(gemm(c, ctx, ws, L, Lw.gate_up, 2 * I, H, u2, rows, Y, false));
-    TRY(launch_act(c.dtype, Y, rows, I, act, ctx));
+    if (c.dtype == DFLASH2_BF16 && gemm_fusable(2 * I, rows, kEpiSwiglu)) {
+      GemmOp g = gemm_op(Lw.gate_up, 2 * I, H, u2, rows);  // SiLU(gate) * up fused into the epilogue
+      g.epi = kEpiSwiglu;
+      g.act = act;
+      TRY(gemm_fused(g, ctx, ws, L, false));
+    } else {
+      TRY(gemm(c, ctx, ws, L, Lw.gate_up, 2 * I, H, u2, rows, Y, false));
+      TRY(launch_act(c.dtype, Y, rows, I, act, ctx));
+    }
     TRY(gemm(c, ctx, ws, L, Lw.down, H, I, act, rows, h, true));
   }
   TRY(launch_rownorm(c.dtype, h, rows, H, w->final_norm, c.rms_eps, hn, B, 1, ctx));

@@ -195,18 +195,19 @@ __global__ void __launch_bounds__(AT) attn_partial_kernel(
 // bf16 path: one thread-block cluster per (kv head, sequence).  The NS CTAs
 // of the cluster split the keys [0, P + B) into NS contiguous chunks.  Each
 // CTA runs a flash-attention pass over its chunk on the tensor cores
-// (mma.sync m16n8k16, fp32 accumulation), with its 64-key K/V tiles
-// double-buffered in shared memory by cp.async (one page lookup per key),
-// and leaves unnormalised partials (acc, running max, running sum) for the
-// grp*B query rows in shared memory.  After a cluster barrier every CTA
-// merges all partials of its share of the rows through distributed shared
-// memory and writes O: no partial goes to global memory and no second kernel
-// runs.
+// (mma.sync m16n8k16, fp32 accumulation), with its 128-key K/V tiles
+// double-buffered in shared memory by cp.async (page ids loaded once),
+// and leaves an unnormalised partial (acc, running max, running sum) for each
+// of the grp*B query rows in shared memory.  After a cluster barrier every
+// CTA merges the cluster's partials of its share of the rows through
+// distributed shared memory and writes O: no partial goes to global memory
+// and no second kernel runs.
 //
 // Within a CTA the query rows form 16-row blocks and each tile's keys are cut
-// into ksplit shares; each of the 8 warps owns one or two (row block, key
-// share) combinations with its own online-softmax state in registers, and
-// each combination is one partial of the cluster-wide merge.  For every
+// into ksplit shares; each of the 16 warps owns one (row block, key share)
+// combination with its own online-softmax state in registers.  The CTA
+// first merges a row's shares in shared memory, so the cluster-wide merge
+// reads one partial per CTA.  For every
 // 16-key step: S = Q K^T (K rows read with ldmatrix as the col-major B
 // operand), scale, mask, online softmax, then O += P V with P split into
 // bf16 hi + lo parts (two MMAs), so the probabilities keep ~16 bits.
@@ -236,45 +237,51 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-constexpr int MKT = 64;         // keys per tile
-constexpr int KST = 2;          // K/V tile stages
-constexpr int kMaxCluster = 8;  // CTAs per cluster (portable limit)
-constexpr int CLW = 8;          // warps per CTA
-constexpr int CLT = 32 * CLW;   // threads: four per key of a tile
-constexpr int kMaxShares = 4;   // key shares per 16-row block (16 keys each per tile)
+constexpr int MKT = 128;         // keys per tile
+constexpr int KST = 2;           // K/V tile stages
+constexpr int kMaxCluster = 8;   // CTAs per cluster (portable)
+constexpr int CLW = 16;          // warps per CTA
+constexpr int CLT = 32 * CLW;    // threads
+constexpr int kMaxShares = 8;    // key shares per 16-row block (16 keys each per tile)
 
-// Key shares per 16-row block: enough (row block, share) combinations to
-// give every warp one, each share at least 16 keys of a tile.
+// Key shares per 16-row block: a power of two, so each share is a whole
+// number of 16-key steps, and enough (row block, share) combinations to give
+// most warps one (at most CLW combinations for 16 row blocks or fewer).
 __host__ __device__ inline int attn_ksplit(int nrb) {
-  const int k = nrb >= CLW ? 1 : CLW / nrb;
-  return k < kMaxShares ? k : kMaxShares;
+  int k = 1;
+  while (k < kMaxShares && nrb * 2 * k <= CLW) k *= 2;
+  return k;
 }
 
-// Shared memory: Q rows, the K/V stages, the per-combination partial states
-// (read by the whole cluster), the merge weights of this CTA's rows.
+// Shared memory: Q rows; the K/V stages, which after the key loop hold the
+// per-combination partial states (read by the whole cluster); the merge
+// weights of this CTA's rows; the page ids of its key chunk (npg of them).
 template <int DH>
-size_t attn_cl_smem(int R) {
+__host__ __device__ inline size_t attn_kv_bytes(int R) {
   const int nrb = (R + 15) / 16;
-  const size_t qb = (size_t)nrb * 16 * (DH + 8) * 2;
   const size_t kvb = (size_t)KST * 2 * MKT * (DH + 8) * 2;
   const size_t comb = (size_t)nrb * attn_ksplit(nrb) * 16 * (DH + 2) * 4;
-  return qb + kvb + comb + (size_t)(R + kMaxCluster) * kMaxShares * 4;
+  return kvb > comb ? kvb : comb;
+}
+template <int DH>
+size_t attn_cl_smem(int R, int npg) {
+  const int nrb = (R + 15) / 16;
+  const size_t qb = (size_t)nrb * 16 * (DH + 8) * 2;
+  return qb + attn_kv_bytes<DH>(R) + (size_t)(R + kMaxCluster) * kMaxShares * 2 * 4 + (size_t)npg * 4 + 8 +
+         KST * sizeof(uint64_t);
 }
 
-// MCPW: (row block, key share) combinations per warp (1 or 2), so the
-// register-resident accumulators are sized to what the launch needs.
-template <int DH, int MCPW>
-__global__ void __launch_bounds__(CLT) attn_cluster_kernel(
+template <int DH>
+__global__ void __launch_bounds__(CLT, 1) attn_cluster_kernel(
     const bf16* __restrict__ q, const bf16* __restrict__ kb, const bf16* __restrict__ vb, const bf16* __restrict__ kc,
     const bf16* __restrict__ vc, const int32_t* __restrict__ block_table, int max_pages, int page_size, int n_pages,
-    const int32_t* __restrict__ ctx_len, const int32_t* __restrict__ new_off, int B, int nq, int nkv,
+    const int32_t* __restrict__ ctx_len, const int32_t* __restrict__ new_off, int B, int nq, int nkv, int npg,
     bf16* __restrict__ o, unsigned* status) {
+  constexpr int MCPW = 1;  // (row block, key share) combinations per warp
   constexpr int LD = DH + 8;  // padded smem row (elements): ldmatrix rows hit distinct banks
   constexpr int NT = DH / 8;  // n8 tiles across the head dimension
   constexpr int C8 = DH / 8;  // 16-byte chunks per row
   constexpr int FS = DH + 2;  // partial row: acc[DH], m, l
-  constexpr int TPK = CLT / MKT;  // threads per key in a tile load
-  constexpr int NPMAX = kMaxCluster * kMaxShares;
   extern __shared__ __align__(16) uint8_t smraw[];
   pdl_launch_next();
   const int NS = gridDim.x;  // the cluster spans x
@@ -285,9 +292,15 @@ __global__ void __launch_bounds__(CLT) attn_cluster_kernel(
   const int ncombo = nrb * ksplit;
   const int np = NS * ksplit;  // partials per row across the cluster
   bf16* Qs = reinterpret_cast<bf16*>(smraw);
-  bf16* KV = Qs + nrb * 16 * LD;                                      // [KST][K, V][MKT][LD]
-  float* comb = reinterpret_cast<float*>(KV + (size_t)KST * 2 * MKT * LD);  // [ncombo][16][FS]
-  float* wts = comb + (size_t)ncombo * 16 * FS;                       // [rows of this CTA][np]
+  bf16* KV = Qs + nrb * 16 * LD;                        // [KST][K, V][MKT][LD]
+  float* comb = reinterpret_cast<float*>(KV);            // [ncombo][16][FS], after the key loop
+  float* wts = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(KV) + attn_kv_bytes<DH>(R));  // merge weights
+  int* pg = reinterpret_cast<int*>(wts + (size_t)(R + kMaxCluster) * kMaxShares * 2);  // page ids of the chunk
+  uint64_t* kvbar = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(pg + npg) + 7) & ~uintptr_t(7));
+  if (threadIdx.x == 0) {  // one K/V stage completes when its 2*MKT row copies have landed
+    for (int i = 0; i < KST; ++i) mbar_init(kvbar + i, 2 * MKT);
+    fence_barrier_init();
+  }
 
   pdl_wait();
   const int P = ctx_len[s] + (new_off[s + 1] - new_off[s]);
@@ -298,6 +311,15 @@ __global__ void __launch_bounds__(CLT) attn_cluster_kernel(
   const float scale = rsqrtf((float)DH);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // page ids of the chunk's context keys, once (-1: past the table)
+  const int pbase = k0 / page_size;
+  const int pend = k0 < min(k1, P) ? (min(k1, P) - 1) / page_size + 1 : pbase;
+  for (int i = threadIdx.x; i < pend - pbase && i < npg; i += blockDim.x) {
+    const int pi = pbase + i;
+    pg[i] = pi < max_pages ? block_table[(size_t)s * max_pages + pi] : -1;
+  }
+  if (pend - pbase > npg && threadIdx.x == 0) flag(status, DFLASH2_DEV_BAD_LENGTH);
+  __syncthreads();
   // query rows (zero padding to whole 16-row blocks)
   for (int idx = threadIdx.x; idx < nrb * 16 * C8; idx += blockDim.x) {
     const int r = idx / C8, c = (idx % C8) * 8;
@@ -305,44 +327,42 @@ __global__ void __launch_bounds__(CLT) attn_cluster_kernel(
     if (r < R) src = q + (((size_t)s * B + r / grp) * nq + g * grp + r % grp) * DH + c;
     cp_async16(Qs + r * LD + c, src, r < R);
   }
-  // K/V rows of keys t0 .. t0 + MKT - 1 into stage stg; keys past k1, and
-  // keys whose page is invalid (flagged), read as zeros
+  // K/V rows of keys t0 .. t0 + MKT - 1 into stage stg: thread kk copies the
+  // K row of key kk, thread MKT + kk its V row, each one 16-byte-aligned bulk
+  // copy of DH elements, and arrives on the stage barrier with its byte
+  // count.  Keys past k1, and keys whose page is invalid (flagged), are
+  // written as zeros instead.
   auto issue = [&](int t0, int stg) {
-    bf16* Ks = KV + (size_t)stg * 2 * MKT * LD;
-    bf16* Vs = Ks + MKT * LD;
-    const int kk = threadIdx.x / TPK, part = threadIdx.x % TPK;
+    if (threadIdx.x >= 2 * MKT) return;
+    const bool is_v = threadIdx.x >= MKT;
+    const int kk = threadIdx.x - (is_v ? MKT : 0);
+    bf16* dst = KV + (size_t)stg * 2 * MKT * LD + (is_v ? MKT * LD : 0) + (size_t)kk * LD;
     const int j = t0 + kk;
-    const bf16* ksrc = kc;
-    const bf16* vsrc = vc;
-    bool ok = false;
+    const bf16* src = nullptr;
     if (j < k1) {
       if (j < P) {
-        const int pi = j / page_size;
-        const int page = pi < max_pages ? block_table[(size_t)s * max_pages + pi] : -1;
-        if (page >= 0 && page < n_pages) {
-          const size_t off = (((size_t)page * page_size + j % page_size) * nkv + g) * DH;
-          ksrc = kc + off;
-          vsrc = vc + off;
-          ok = true;
-        } else {
+        const int li = j / page_size - pbase;
+        const int page = li < npg ? pg[li] : -1;
+        if (page >= 0 && page < n_pages)
+          src = (is_v ? vc : kc) + (((size_t)page * page_size + j % page_size) * nkv + g) * DH;
+        else if (!is_v)
           flag(status, DFLASH2_DEV_BAD_PAGE);
-        }
       } else {
-        const size_t off = (((size_t)s * B + (j - P)) * nkv + g) * DH;
-        ksrc = kb + off;
-        vsrc = vb + off;
-        ok = true;
+        src = (is_v ? vb : kb) + (((size_t)s * B + (j - P)) * nkv + g) * DH;
       }
     }
+    mbar_arrive_expect_tx(kvbar + stg, src ? DH * 2 : 0);
+    if (src) {
+      bulk_g2s(dst, src, DH * 2, kvbar + stg);
+    } else {
 #pragma unroll
-    for (int c = part * (C8 / TPK); c < (part + 1) * (C8 / TPK); ++c) {
-      cp_async16(Ks + kk * LD + c * 8, ok ? ksrc + c * 8 : kc, ok);
-      cp_async16(Vs + kk * LD + c * 8, ok ? vsrc + c * 8 : vc, ok);
+      for (int c = 0; c < C8; ++c) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0, 0, 0, 0);
     }
   };
   const int ntiles = (k1 - k0 + MKT - 1) / MKT;  // 0 for an empty chunk
+  cp_async_commit();  // the Q rows
   if (ntiles > 0) issue(k0, 0);
-  cp_async_commit();  // group 0: Q and tile 0
+  volatile int never = 0;
 
   // per-combination online-softmax state: rows lane/4 and lane/4 + 8 of the block
   float m_st[MCPW][2], l_st[MCPW][2], acc[MCPW][NT][4];
@@ -353,10 +373,12 @@ __global__ void __launch_bounds__(CLT) attn_cluster_kernel(
 #pragma unroll
     for (int n = 0; n < NT; ++n) acc[c][n][0] = acc[c][n][1] = acc[c][n][2] = acc[c][n][3] = 0.f;
   }
+  cp_async_wait<0>();
   for (int t = 0; t < ntiles; ++t) {
     if (t + 1 < ntiles) issue(k0 + (t + 1) * MKT, (t + 1) % KST);
-    cp_async_commit();
-    cp_async_wait<1>();  // all but the newest group have landed
+    // tile t has landed (bounded wait: on a timeout the status says so)
+    if (!mbar_wait(kvbar + t % KST, (uint32_t)((t / KST) & 1), &never, 1000000000ull) && threadIdx.x == 0)
+      flag(status, DFLASH2_DEV_WAIT_TIMEOUT);
     __syncthreads();
     const bf16* Ks = KV + (size_t)(t % KST) * 2 * MKT * LD;
     const bf16* Vs = Ks + MKT * LD;
@@ -443,7 +465,7 @@ __global__ void __launch_bounds__(CLT) attn_cluster_kernel(
     }
     __syncthreads();  // this stage is refilled two tiles later
   }
-  cp_async_wait<0>();
+  __syncthreads();  // the K/V stages now hold the partial states
   // each combination's partial state -> shared memory (empty ones: m = -inf, l = 0)
 #pragma unroll
   for (int slot = 0; slot < MCPW; ++slot) {
@@ -465,53 +487,91 @@ __global__ void __launch_bounds__(CLT) attn_cluster_kernel(
       cb[(r0 + 8) * FS + DH + 1] = l_st[slot][1];
     }
   }
-  cluster_sync();  // every CTA's partials are complete and visible to the cluster
+  __syncthreads();
+  // 1. merge each row's key shares in place, into its share-0 slot: weights
+  //    e^(m_ks - M) per share (wk), merged (m, l) written by the row's thread
+  float* wk = wts;  // [R][ksplit] in-CTA share weights
+  for (int r = threadIdx.x; r < R; r += blockDim.x) {
+    float* base = comb + ((size_t)(r / 16) * ksplit * 16 + r % 16) * FS + DH;
+    float M = -INFINITY;
+    for (int ks = 0; ks < ksplit; ++ks) {
+      const float* b = base + (size_t)ks * 16 * FS;
+      if (b[1] > 0.f) M = fmaxf(M, b[0]);
+    }
+    float l = 0.f;
+    for (int ks = 0; ks < ksplit; ++ks) {
+      const float* b = base + (size_t)ks * 16 * FS;
+      const float w = b[1] > 0.f ? expf(b[0] - M) : 0.f;
+      wk[r * ksplit + ks] = w;
+      l += b[1] * w;
+    }
+    base[0] = M;
+    base[1] = l;
+  }
+  __syncthreads();
+  if (ksplit > 1) {
+    for (int idx = threadIdx.x; idx < R * (DH / 2); idx += blockDim.x) {
+      const int r = idx / (DH / 2), c = (idx % (DH / 2)) * 2;
+      float2* base = reinterpret_cast<float2*>(comb + ((size_t)(r / 16) * ksplit * 16 + r % 16) * FS + c);
+      float2 acc2 = make_float2(0.f, 0.f);
+      for (int ks = 0; ks < ksplit; ++ks) {
+        const float w = wk[r * ksplit + ks];
+        if (w != 0.f) {
+          const float2 v = base[(size_t)ks * 16 * FS / 2];
+          acc2.x += v.x * w;
+          acc2.y += v.y * w;
+        }
+      }
+      *base = acc2;
+    }
+  }
+  cluster_sync();  // every CTA's merged partials are complete and visible to the cluster
 
-  // Row r's partials: CTA p (key chunk), share ks, in that order; the row's
-  // state in CTA p sits at comb[((r / 16) * ksplit + ks) * 16 + r % 16].
-  // This CTA merges rows r = sp, sp + NS, ...: weights e^(m - M) / den.
+  // 2. row r's partials: one per CTA p of the cluster, in its share-0 slot.
+  //    This CTA merges rows r = sp, sp + NS, ...: weights e^(m_p - M) / den.
   const int nmine = sp < R ? (R - sp + NS - 1) / NS : 0;
+  float* cw = wts + (size_t)R * ksplit;  // [rows of this CTA][NS]
   for (int mi = threadIdx.x; mi < nmine; mi += blockDim.x) {
     const int r = sp + mi * NS;
     const float* base = comb + ((size_t)(r / 16) * ksplit * 16 + r % 16) * FS + DH;
-    float2 ml[NPMAX];
+    float2 ml[kMaxCluster];
 #pragma unroll
-    for (int i = 0; i < NPMAX; ++i)
-      if (i < np) ml[i] = ld_dsmem2(dsmem_addr(base + (size_t)(i % ksplit) * 16 * FS, i / ksplit));
+    for (int p = 0; p < kMaxCluster; ++p)
+      if (p < NS) ml[p] = ld_dsmem2(dsmem_addr(base, p));
     float M = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < NPMAX; ++i)
-      if (i < np && ml[i].y > 0.f) M = fmaxf(M, ml[i].x);
+    for (int p = 0; p < kMaxCluster; ++p)
+      if (p < NS && ml[p].y > 0.f) M = fmaxf(M, ml[p].x);
     float den = 0.f;
 #pragma unroll
-    for (int i = 0; i < NPMAX; ++i)
-      if (i < np) {
-        ml[i].x = ml[i].y > 0.f ? expf(ml[i].x - M) : 0.f;
-        den += ml[i].y * ml[i].x;
+    for (int p = 0; p < kMaxCluster; ++p)
+      if (p < NS) {
+        ml[p].x = ml[p].y > 0.f ? expf(ml[p].x - M) : 0.f;
+        den += ml[p].y * ml[p].x;
       }
     const float inv = den > 0.f ? 1.f / den : 0.f;
 #pragma unroll
-    for (int i = 0; i < NPMAX; ++i)
-      if (i < np) wts[mi * np + i] = ml[i].x * inv;
+    for (int p = 0; p < kMaxCluster; ++p)
+      if (p < NS) cw[mi * NS + p] = ml[p].x * inv;
   }
   __syncthreads();
-  // O = sum over partials of acc * weight, two elements per thread
+  // O = sum over the cluster's partials of acc * weight, two elements per thread
   for (int idx = threadIdx.x; idx < nmine * (DH / 2); idx += blockDim.x) {
     const int mi = idx / (DH / 2), c = (idx % (DH / 2)) * 2;
     const int r = sp + mi * NS;
     const float* base = comb + ((size_t)(r / 16) * ksplit * 16 + r % 16) * FS + c;
-    float2 v[NPMAX];
+    float2 v[kMaxCluster];
 #pragma unroll
-    for (int i = 0; i < NPMAX; ++i)
-      if (i < np) v[i] = ld_dsmem2(dsmem_addr(base + (size_t)(i % ksplit) * 16 * FS, i / ksplit));
+    for (int p = 0; p < kMaxCluster; ++p)
+      if (p < NS) v[p] = ld_dsmem2(dsmem_addr(base, p));
     float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-    for (int i = 0; i < NPMAX; ++i)
-      if (i < np) {
-        const float w = wts[mi * np + i];
+    for (int p = 0; p < kMaxCluster; ++p)
+      if (p < NS) {
+        const float w = cw[mi * NS + p];
         if (w != 0.f) {
-          a0 += v[i].x * w;
-          a1 += v[i].y * w;
+          a0 += v[p].x * w;
+          a1 += v[p].y * w;
         }
       }
     const int i = r / grp, h = g * grp + r % grp;
@@ -599,6 +659,35 @@ int chunk_of(int max_ctx, int B, int batch, int nkv, int nsm) {
   return (int)std::max(64L, std::min(1024L, ch));
 }
 
+// CTAs per cluster: one per 64 keys of the longest sequence, at most 16, and
+// no more than it takes to give the SMs about two CTAs each.
+int attn_cluster_ctas(int max_ctx, int B, int batch, int nkv, int nsm) {
+  const long L = (long)max_ctx + B;
+  const long fill = std::max(1L, (2L * nsm + (long)nkv * batch - 1) / ((long)nkv * batch));
+  return (int)std::max(1L, std::min<long>({(long)kMaxCluster, (L + MKT - 1) / MKT, fill}));
+}
+
+template <int DH>
+int launch_cluster(int R, int max_ctx, int page_size, int batch, int nkv, const Ctx& c, const bf16* q,
+                   const bf16* kb, const bf16* vb, const bf16* kc, const bf16* vc, const int32_t* block_table,
+                   int max_pages, int n_pages, const int32_t* ctx_len, const int32_t* new_off, int B, int nq,
+                   bf16* o) {
+  static bool attr = false;  // set once, before any capture
+  if (!attr) {
+    if (cudaFuncSetAttribute(attn_cluster_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024))
+      return DFLASH2_ERR_CUDA;
+    attr = true;
+  }
+  const int ns = attn_cluster_ctas(max_ctx, B, batch, nkv, c.nsm);
+  // chunk length bound (keys), then its pages
+  const long ch = ((((long)max_ctx + B + ns - 1) / ns) + 15) & ~15L;
+  const int npg = (int)((ch + page_size - 1) / page_size + 1);
+  const size_t smem = attn_cl_smem<DH>(R, npg);
+  if (smem > 200 * 1024) return DFLASH2_ERR_SHAPE;
+  return launch_kx(attn_cluster_kernel<DH>, dim3(ns, nkv, batch), dim3(CLT), smem, c, ns, q, kb, vb, kc, vc,
+                   block_table, max_pages, page_size, n_pages, ctx_len, new_off, B, nq, nkv, npg, o, c.status);
+}
+
 }  // namespace
 
 // Upper bound over every batch <= max_batch and SM count <= kMaxSM (the
@@ -613,12 +702,6 @@ size_t attn_part_bytes(int max_batch, int B, int nq, int nkv, int d, int max_ctx
   return best;
 }
 
-// CTAs per cluster: one per 64 keys of the longest sequence, at most 8.
-int attn_cluster_ctas(int max_ctx, int B) {
-  const long L = (long)max_ctx + B;
-  return (int)std::max(1L, std::min<long>(kMaxCluster, (L + MKT - 1) / MKT));
-}
-
 int launch_attention(int dtype, const void* q, const void* kb, const void* vb, const void* kc, const void* vc,
                      const int32_t* block_table, int max_pages, int page_size, int n_pages,
                      const int32_t* ctx_len, const int32_t* new_off, int batch, int B, int nq, int nkv, int d,
@@ -626,29 +709,16 @@ int launch_attention(int dtype, const void* q, const void* kb, const void* vb, c
   const int R = (nq / nkv) * B;
   const int nrb = (R + 15) / 16;
   const int ncombo = nrb * attn_ksplit(nrb);
-  if (dtype == DFLASH2_BF16 && (d == 64 || d == 128) && ncombo <= 2 * CLW) {
-    static bool mattr = false;  // set once, before any capture
-    if (!mattr) {
-      const int mx = 200 * 1024;
-      if (cudaFuncSetAttribute(attn_cluster_kernel<64, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx) ||
-          cudaFuncSetAttribute(attn_cluster_kernel<64, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx) ||
-          cudaFuncSetAttribute(attn_cluster_kernel<128, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx) ||
-          cudaFuncSetAttribute(attn_cluster_kernel<128, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx))
-        return DFLASH2_ERR_CUDA;
-      mattr = true;
-    }
-    const size_t ms = d == 64 ? attn_cl_smem<64>(R) : attn_cl_smem<128>(R);
-    if (ms > 200 * 1024) return DFLASH2_ERR_SHAPE;
-    const int ns = attn_cluster_ctas(max_ctx, B);
-    const dim3 grid(ns, nkv, batch);
+  if (dtype == DFLASH2_BF16 && (d == 64 || d == 128) && ncombo <= CLW) {
     const bf16 *q_ = static_cast<const bf16*>(q), *kb_ = static_cast<const bf16*>(kb),
                *vb_ = static_cast<const bf16*>(vb), *kc_ = static_cast<const bf16*>(kc),
                *vc_ = static_cast<const bf16*>(vc);
     bf16* o_ = static_cast<bf16*>(o_out);
-    auto kern = d == 64 ? (ncombo <= CLW ? attn_cluster_kernel<64, 1> : attn_cluster_kernel<64, 2>)
-                        : (ncombo <= CLW ? attn_cluster_kernel<128, 1> : attn_cluster_kernel<128, 2>);
-    return launch_kx(kern, grid, dim3(CLT), ms, c, ns, q_, kb_, vb_, kc_, vc_, block_table, max_pages, page_size,
-                     n_pages, ctx_len, new_off, B, nq, nkv, o_, c.status);
+    if (d == 64)
+      return launch_cluster<64>(R, max_ctx, page_size, batch, nkv, c, q_, kb_, vb_, kc_, vc_, block_table, max_pages,
+                                n_pages, ctx_len, new_off, B, nq, o_);
+    return launch_cluster<128>(R, max_ctx, page_size, batch, nkv, c, q_, kb_, vb_, kc_, vc_, block_table, max_pages,
+                               n_pages, ctx_len, new_off, B, nq, o_);
   }
   // SIMT path (fp32 storage, or row counts beyond the tensor-core kernel):
   // key-chunk partials in global memory, then the combine kernel

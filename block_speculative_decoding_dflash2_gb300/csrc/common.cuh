@@ -88,17 +88,6 @@ __device__ __forceinline__ void warp_list_offer(float& lv, int& li, float& tv, i
   ti = __shfl_sync(0xffffffffu, li, KMAX - 1);
 }
 
-// ----------------------------------------------------------------- rope
-// Rotation angle of pair i at position pos, evaluated in double so long
-// contexts keep full float accuracy (a handful of evaluations per head).
-__device__ __forceinline__ void rope_cs(int pos, int i, int d, float theta, float* c, float* s) {
-  const double inv = exp(-(2.0 * (double)i / (double)d) * log((double)theta));
-  double sn, cs;
-  sincos((double)pos * inv, &sn, &cs);
-  *c = (float)cs;
-  *s = (float)sn;
-}
-
 // ----------------------------------------------------------------- PTX: smem
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -123,6 +112,18 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Contiguous global -> shared copy of `bytes` (a multiple of 16; both
+// addresses 16-byte aligned) by the bulk-copy engine, completing on mbarrier
+// `bar` (complete_tx).  Preceded by a proxy fence so that earlier generic
+// accesses to the destination are ordered before the async write.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "fence.proxy.async.shared::cta;\n\t"
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // ----------------------------------------------------------------- PTX: clusters

@@ -10,11 +10,13 @@
 //   "What is DFlash?"  block = [anchor, MASK...]; features from the target's
 //                      tapped hidden states condition every draft layer
 //                      (as extra keys/values: the context K/V written here);
-//   "Variants"         the DFlash 2 two-tap in-block convolution around every
-//                      sublayer (dyn_conv_kernel);
+//   "Variants"         DFlash 2's short (two-tap) convolution along the block
+//                      around each sublayer (conv_prologue_kernel, or
+//                      dyn_conv_kernel after a separate norm and tap GEMM);
 //   "Key Config Fields" input_embedding_scale, conv_group_size.
 #include <algorithm>
 #include <cmath>
+#include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -64,15 +66,26 @@ __device__ __forceinline__ void norm_row(const float* xs, int H, const T* gamma,
 }
 
 // ---------------------------------------------------------------- rope
-// cos/sin of position pos for rotary pair i of a d-wide head:
-// angle = pos * theta^(-2i/d).  The angle is formed and reduced modulo 2*pi
-// in double (a few operations), then sincosf of the reduced fp32 angle, so
+// cos/sin of position pos for a rotary pair with inverse frequency inv
+// (= theta^(-2i/d)): the angle pos * inv is formed and reduced modulo 2*pi
+// in double (three operations), then sincosf of the reduced fp32 angle, so
 // long contexts keep full fp32 accuracy.
-__device__ __forceinline__ void rope_cs(int pos, int i, int d, double log2_theta, float* c, float* s) {
-  const double inv = exp2(-(2.0 * (double)i / (double)d) * log2_theta);
+__device__ __forceinline__ void rope_cs(int pos, double inv, float* c, float* s) {
   double a = (double)pos * inv;
   a -= 6.283185307179586 * rint(a * 0.15915494309189535);
   sincosf((float)a, s, c);
+}
+
+// RoPE table entries of block row t of sequence sq (position: the context
+// length after the append, plus t), pairs i = tid, tid + nt, ... < d/2.
+__device__ __forceinline__ void rope_table_block(const RopeTab& rt, int sq, int B, int t, int tid, int nt) {
+  const int pos = rt.ctx_len[sq] + (rt.new_off[sq + 1] - rt.new_off[sq]) + t;
+  float2* row = rt.cs + ((size_t)sq * B + t) * (rt.d / 2);
+  for (int i = tid; i < rt.d / 2; i += nt) {
+    float c, sn;
+    rope_cs(pos, rt.freq.inv[i], &c, &sn);
+    row[i] = make_float2(c, sn);
+  }
 }
 
 // Per-head RMSNorm + RoPE of one d-wide head held by a warp: lane holds
@@ -102,20 +115,6 @@ __device__ __forceinline__ void head_norm_rope(float (&x)[4], int d, const T* ga
 
 // ---------------------------------------------------------------- kernels
 
-// f[n] = RMSNorm_hidden(Y[n])  -- feature projection epilogue.
-template <typename T>
-__global__ void __launch_bounds__(RT) feature_norm_kernel(const float* __restrict__ Y, int H,
-                                                          const T* __restrict__ gamma, float eps, T* __restrict__ f) {
-  extern __shared__ float xs[];
-  __shared__ float red[32];
-  pdl_launch_next();
-  pdl_wait();
-  const size_t n = blockIdx.x;
-  for (int m = threadIdx.x * 4; m < H; m += blockDim.x * 4)
-    *reinterpret_cast<float4*>(xs + m) = *reinterpret_cast<const float4*>(Y + n * H + m);
-  norm_row(xs, H, gamma, eps, f + n * H, red);
-}
-
 // Sequence that owns appended row n: the largest s with new_off[s] <= n.
 __device__ __forceinline__ int owner_of(const int32_t* new_off, int batch, int n) {
   int lo = 0, hi = batch - 1;
@@ -127,12 +126,54 @@ __device__ __forceinline__ int owner_of(const int32_t* new_off, int batch, int n
   return lo;
 }
 
+// f[n] = RMSNorm_hidden(Y[n])  -- feature projection epilogue.  With
+// rt.cs, also the RoPE table entries of appended row n and its paged-cache
+// destination (for the fused K/V epilogue of the context projection).
+template <typename T>
+__global__ void __launch_bounds__(RT) feature_norm_kernel(const float* __restrict__ Y, int H,
+                                                          const T* __restrict__ gamma, float eps, T* __restrict__ f,
+                                                          const __grid_constant__ RopeTab rt, unsigned* status) {
+  extern __shared__ float xs[];
+  __shared__ float red[32];
+  __shared__ int pos_s;
+  pdl_launch_next();
+  pdl_wait();
+  const size_t n = blockIdx.x;
+  if (rt.cs) {
+    if (threadIdx.x == 0) {
+      const int sq = owner_of(rt.new_off, rt.batch, (int)n);
+      int pos = rt.ctx_len[sq] + ((int)n - rt.new_off[sq]);
+      long long dst = -1;
+      if (pos < 0 || pos >= rt.max_pages * rt.page_size) {
+        flag(status, DFLASH2_DEV_BAD_LENGTH);
+        pos = 0;
+      } else {
+        const int page = rt.block_table[(size_t)sq * rt.max_pages + pos / rt.page_size];
+        if (page < 0 || page >= rt.n_pages) flag(status, DFLASH2_DEV_BAD_PAGE);
+        else dst = ((long long)page * rt.page_size + pos % rt.page_size) * rt.nkv * rt.d;
+      }
+      rt.dst[n] = dst;
+      pos_s = pos;
+    }
+    __syncthreads();
+    float2* row = rt.cs + n * (rt.d / 2);
+    for (int i = threadIdx.x; i < rt.d / 2; i += blockDim.x) {
+      float c, sn;
+      rope_cs(pos_s, rt.freq.inv[i], &c, &sn);
+      row[i] = make_float2(c, sn);
+    }
+  }
+  for (int m = threadIdx.x * 4; m < H; m += blockDim.x * 4)
+    *reinterpret_cast<float4*>(xs + m) = *reinterpret_cast<const float4*>(Y + n * H + m);
+  norm_row(xs, H, gamma, eps, f + n * H, red);
+}
+
 // Context K/V of appended rows -> paged cache, one warp per (row, head):
 // K = RoPE(RMSNorm_k(W_k f)) and V = W_v f at the row's absolute position.
 // grid = (rows, ceil(2 nkv / warps per CTA)); warps past 2 nkv idle.
 template <typename T>
 __global__ void __launch_bounds__(RT) kv_append_kernel(const float* __restrict__ Y, int nkv, int d,
-                                                       const T* __restrict__ k_norm, float eps, double log2_theta,
+                                                       const T* __restrict__ k_norm, float eps, const __grid_constant__ RopeFreq freq,
                                                        const int32_t* __restrict__ ctx_len,
                                                        const int32_t* __restrict__ new_off, int batch,
                                                        const int32_t* __restrict__ block_table, int max_pages,
@@ -164,7 +205,7 @@ __global__ void __launch_bounds__(RT) kv_append_kernel(const float* __restrict__
     if (j < nj) x[j] = y[lane + 32 * j];
   if (hh < nkv) {
     float cs[2], sn[2];
-    for (int j = 0; j < d / 64; ++j) rope_cs(pos, lane + 32 * j, d, log2_theta, &cs[j], &sn[j]);
+    for (int j = 0; j < d / 64; ++j) rope_cs(pos, freq.inv[lane + 32 * j], &cs[j], &sn[j]);
     head_norm_rope(x, d, k_norm, eps, cs, sn);
   }
   T* out = (hh < nkv ? kc : vc) + dst + (size_t)(hh < nkv ? hh : hh - nkv) * d;
@@ -179,13 +220,15 @@ template <typename T>
 __global__ void __launch_bounds__(RT) embed_norm_kernel(const int32_t* __restrict__ anchor, int mask_id, int B,
                                                         const T* __restrict__ E, int V, int H, float scale,
                                                         const T* __restrict__ gamma, float eps, float* __restrict__ h,
-                                                        T* __restrict__ u, unsigned* status) {
+                                                        T* __restrict__ u, const __grid_constant__ RopeTab rt,
+                                                        unsigned* status) {
   extern __shared__ float xs[];
   __shared__ float red[32];
   pdl_launch_next();
   pdl_wait();
   const int row = blockIdx.x;
   const int s = row / B, i = row % B;
+  if (rt.cs) rope_table_block(rt, s, B, i, threadIdx.x, blockDim.x);
   int tok = i == 0 ? anchor[s] : mask_id;
   if (tok < 0 || tok >= V) {
     if (threadIdx.x == 0) flag(status, DFLASH2_DEV_BAD_TOKEN);
@@ -267,21 +310,43 @@ __global__ void __launch_bounds__(RT) dyn_conv_kernel(const T* __restrict__ u, c
 // groups, and writes u and u2 of its groups' channels (and h, for the
 // embedding).  Tap row 2g + j of W_tap is tap j of group g.
 //
-// The kernel is latency-bound (a few hundred KB per CTA), so every phase is
-// one round of loads in flight: the CTA's tap rows are copied to shared
-// memory (cp.async) before the dependency wait, since no kernel writes the
-// weights; each row is split over nw / B warps with all of a lane's loads
-// issued at once.
+// The kernel is latency-bound (a few hundred KB per CTA), so it is built
+// around one round of loads: the CTA's tap rows are copied to shared memory
+// (cp.async) before the dependency wait, since no kernel writes the weights;
+// each row is split over NW / B warps, and a lane issues all its loads of x
+// and gamma at once and keeps x in registers across the 1/rms reduction.
 constexpr int PT = 512;  // threads of the prologue kernel
-constexpr int PU = 16;   // vector loads in flight per lane
+constexpr int PUB = 16;  // 4-element vectors per lane and round (bf16)
+
+template <typename T>
+struct Vec4Raw;  // 4 elements as loaded, converted to float4 at use
+template <>
+struct Vec4Raw<float> {
+  float4 v;
+  __device__ __forceinline__ void load(const float* p) { v = *reinterpret_cast<const float4*>(p); }
+  __device__ __forceinline__ float4 f() const { return v; }
+};
+template <>
+struct Vec4Raw<bf16> {
+  uint2 v;
+  __device__ __forceinline__ void load(const bf16* p) { v = *reinterpret_cast<const uint2*>(p); }
+  __device__ __forceinline__ float4 f() const {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+  }
+};
 
 template <typename T, bool EMBED>
 __global__ void __launch_bounds__(PT) conv_prologue_kernel(
     const float* __restrict__ h_in, const int32_t* __restrict__ anchor, int mask_id, const T* __restrict__ E, int V,
     float scale, const T* __restrict__ gamma, float eps, const T* __restrict__ Wt, int H, int gs, int gpc, int B,
-    int stage_w, float* __restrict__ h_out, T* __restrict__ u_out, T* __restrict__ u2_out, unsigned* status) {
+    int stage_w, float* __restrict__ h_out, T* __restrict__ u_out, T* __restrict__ u2_out, const __grid_constant__ RopeTab rt,
+    unsigned* status) {
   extern __shared__ __align__(16) uint8_t smraw[];
   constexpr int NW = PT / 32;
+  constexpr int PU = sizeof(T) == 2 ? PUB : PUB / 2;  // fp32 rows: half, to stay in registers
+  using XT = typename std::conditional<EMBED, T, float>::type;  // element type of the source rows
   const int s = blockIdx.y, G = H / gs;
   const int g0 = blockIdx.x * gpc, ng = min(gpc, G - g0);
   T* us = reinterpret_cast<T*>(smraw);                 // [B][H] normed rows as stored
@@ -294,11 +359,22 @@ __global__ void __launch_bounds__(PT) conv_prologue_kernel(
   if (stage_w) {  // the weights are not written by any kernel of the stream
     constexpr int E16 = 16 / sizeof(T);
     const T* src = Wt + (size_t)2 * g0 * H;
-    for (int i = threadIdx.x; i < 2 * ng * H / E16; i += PT) cp_async16(wsm + (size_t)i * E16, src + (size_t)i * E16, true);
+    for (int i = threadIdx.x; i < 2 * ng * H / E16; i += PT)
+      cp_async16(wsm + (size_t)i * E16, src + (size_t)i * E16, true);
     cp_async_commit();
   }
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (EMBED && rt.cs && blockIdx.x == 0) {  // the block rows' RoPE table, by one CTA per sequence
+    const int hp = rt.d / 2;
+    const int pos0 = rt.ctx_len[s] + (rt.new_off[s + 1] - rt.new_off[s]);
+    for (int idx = threadIdx.x; idx < B * hp; idx += PT) {
+      const int t = idx / hp, i = idx - t * hp;
+      float c, sn;
+      rope_cs(pos0 + t, rt.freq.inv[i], &c, &sn);
+      rt.cs[((size_t)s * B + t) * hp + i] = make_float2(c, sn);
+    }
+  }
   if (EMBED) {
     for (int t = threadIdx.x; t < B; t += PT) {
       int tok = t == 0 ? anchor[s] : mask_id;
@@ -310,61 +386,69 @@ __global__ void __launch_bounds__(PT) conv_prologue_kernel(
     }
     __syncthreads();
   }
-  // 4 consecutive elements of source row t at column m
-  auto xrow = [&](int t, int m) -> float4 {
-    if (EMBED) {
-      const int tok = toks[t];
-      if (tok < 0) return make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 e = ld4(E + (size_t)tok * H + m);
-      return make_float4(scale * e.x, scale * e.y, scale * e.z, scale * e.w);
-    }
-    return *reinterpret_cast<const float4*>(h_in + ((size_t)s * B + t) * H + m);
+  // source row t (nullptr: a zero row, for an invalid token) and its scale
+  auto src_row = [&](int t) -> const XT* {
+    if constexpr (EMBED) return toks[t] < 0 ? nullptr : E + (size_t)toks[t] * H;
+    else return h_in + ((size_t)s * B + t) * H;
   };
+  const float xs = EMBED ? scale : 1.f;
   // row t is split into wpr contiguous segments of sl columns, one warp each
   const int wpr = max(1, NW / B), rows_at_once = NW / wpr;
   const int sl = (H / 4 + wpr - 1) / wpr * 4;
-  // 1. sums of squares per (row, segment), then 1/rms per row
+  const bool one_round = sl <= 128 * PU;  // uniform: each lane's x fits its registers
   for (int t0 = 0; t0 < B; t0 += rows_at_once) {
     const int t = t0 + warp / wpr, seg = warp % wpr;
-    if (warp / wpr < rows_at_once && t < B) {
-      const int m1 = min(H, (seg + 1) * sl);
-      float ss = 0.f;
-      for (int m0 = seg * sl + lane * 4; m0 < m1; m0 += 128 * PU) {
-        float4 v[PU];
-#pragma unroll
-        for (int k = 0; k < PU; ++k) v[k] = m0 + 128 * k < m1 ? xrow(t, m0 + 128 * k) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int k = 0; k < PU; ++k) ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
-      }
-      ss = warp_sum(ss);
-      if (lane == 0) red[t * NW + seg] = ss;
-    }
-  }
-  __syncthreads();
-  for (int t = threadIdx.x; t < B; t += PT) {
+    const bool active = warp / wpr < rows_at_once && t < B;
+    const XT* x = active ? src_row(t) : nullptr;
+    const int m1 = min(H, (seg + 1) * sl);
+    Vec4Raw<XT> xv[PU];
+    Vec4Raw<T> gv[PU];
     float ss = 0.f;
-    for (int k = 0; k < wpr; ++k) ss += red[t * NW + k];
-    rinv[t] = rsqrtf(ss / (float)H + eps);
-  }
-  __syncthreads();
-  // 2. the stored u rows into shared memory (the x reloads hit L1)
-  for (int t0 = 0; t0 < B; t0 += rows_at_once) {
-    const int t = t0 + warp / wpr, seg = warp % wpr;
-    if (warp / wpr < rows_at_once && t < B) {
-      const int m1 = min(H, (seg + 1) * sl);
-      const float r = rinv[t];
-      constexpr int PU2 = PU / 2;  // two vectors per element: x and gamma
-      for (int m0 = seg * sl + lane * 4; m0 < m1; m0 += 128 * PU2) {
-        float4 v[PU2], gm[PU2];
+    // 1. sums of squares (one round of loads when the segment fits)
+    if (active) {
+      for (int m0 = seg * sl + lane * 4; m0 < m1; m0 += 128 * PU) {
 #pragma unroll
-        for (int k = 0; k < PU2; ++k)
+        for (int k = 0; k < PU; ++k)
           if (m0 + 128 * k < m1) {
-            v[k] = xrow(t, m0 + 128 * k);
-            gm[k] = ld4(gamma + m0 + 128 * k);
+            if (x) xv[k].load(x + m0 + 128 * k);
+            if (one_round) gv[k].load(gamma + m0 + 128 * k);
           }
 #pragma unroll
-        for (int k = 0; k < PU2; ++k)
-          if (m0 + 128 * k < m1) st4(us + (size_t)t * H + m0 + 128 * k, scale4(v[k], r, gm[k]));
+        for (int k = 0; k < PU; ++k)
+          if (m0 + 128 * k < m1 && x) {
+            const float4 v = xv[k].f();
+            ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+          }
+      }
+      ss = warp_sum(ss) * xs * xs;
+      if (lane == 0) red[t * NW + seg] = ss;
+    }
+    __syncthreads();
+    if (threadIdx.x < B && threadIdx.x >= t0 && threadIdx.x < t0 + rows_at_once) {
+      float sum = 0.f;
+      for (int k = 0; k < wpr; ++k) sum += red[threadIdx.x * NW + k];
+      rinv[threadIdx.x] = rsqrtf(sum / (float)H + eps);
+    }
+    __syncthreads();
+    // 2. the stored u rows into shared memory
+    if (active) {
+      const float r = rinv[t];
+      for (int m0 = seg * sl + lane * 4; m0 < m1; m0 += 128 * PU) {
+        if (!one_round) {
+#pragma unroll
+          for (int k = 0; k < PU; ++k)
+            if (m0 + 128 * k < m1) {
+              if (x) xv[k].load(x + m0 + 128 * k);
+              gv[k].load(gamma + m0 + 128 * k);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < PU; ++k)
+          if (m0 + 128 * k < m1) {
+            float4 v = x ? xv[k].f() : make_float4(0.f, 0.f, 0.f, 0.f);
+            v = make_float4(xs * v.x, xs * v.y, xs * v.z, xs * v.w);
+            st4(us + (size_t)t * H + m0 + 128 * k, scale4(v, r, gv[k].f()));
+          }
       }
     }
   }
@@ -376,14 +460,15 @@ __global__ void __launch_bounds__(PT) conv_prologue_kernel(
     const T* w = stage_w ? wsm + (size_t)jj * H : Wt + (size_t)(2 * g0 + jj) * H;
     float acc = 0.f;
     for (int m0 = lane * 4; m0 < H; m0 += 128 * PU) {
-      float4 wv[PU];
+      Vec4Raw<T> wv[PU];
 #pragma unroll
-      for (int k = 0; k < PU; ++k) wv[k] = m0 + 128 * k < H ? ld4(w + m0 + 128 * k) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int k = 0; k < PU; ++k)
+        if (m0 + 128 * k < H) wv[k].load(w + m0 + 128 * k);
 #pragma unroll
       for (int k = 0; k < PU; ++k)
         if (m0 + 128 * k < H) {
-          const float4 uv = ld4(us + (size_t)t * H + m0 + 128 * k);
-          acc += wv[k].x * uv.x + wv[k].y * uv.y + wv[k].z * uv.z + wv[k].w * uv.w;
+          const float4 wf = wv[k].f(), uv = ld4(us + (size_t)t * H + m0 + 128 * k);
+          acc += wf.x * uv.x + wf.y * uv.y + wf.z * uv.z + wf.w * uv.w;
         }
     }
     acc = warp_sum(acc);
@@ -413,7 +498,17 @@ __global__ void __launch_bounds__(PT) conv_prologue_kernel(
     st4(u_out + o, ut);
     st4(u2_out + o, make_float4(ut.x + a0 * ut.x + a1 * up.x, ut.y + a0 * ut.y + a1 * up.y,
                                 ut.z + a0 * ut.z + a1 * up.z, ut.w + a0 * ut.w + a1 * up.w));
-    if (EMBED) *reinterpret_cast<float4*>(h_out + o) = xrow(t, m);
+    if (EMBED) {
+      const XT* x = src_row(t);
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (x) {
+        Vec4Raw<XT> xr;
+        xr.load(x + m);
+        v = xr.f();
+        v = make_float4(xs * v.x, xs * v.y, xs * v.z, xs * v.w);
+      }
+      *reinterpret_cast<float4*>(h_out + o) = v;
+    }
   }
 }
 
@@ -423,7 +518,8 @@ __global__ void __launch_bounds__(PT) conv_prologue_kernel(
 template <typename T>
 __global__ void __launch_bounds__(RT) qkv_epi_kernel(const float* __restrict__ Y, int B, int nq, int nkv, int d,
                                                      const T* __restrict__ qn, const T* __restrict__ kn, float eps,
-                                                     double log2_theta, const int32_t* __restrict__ ctx_len,
+                                                     const __grid_constant__ RopeFreq freq,
+                                                     const int32_t* __restrict__ ctx_len,
                                                      const int32_t* __restrict__ new_off, T* __restrict__ q,
                                                      T* __restrict__ kb, T* __restrict__ vb) {
   pdl_launch_next();
@@ -442,7 +538,7 @@ __global__ void __launch_bounds__(RT) qkv_epi_kernel(const float* __restrict__ Y
   if (hh < nq + nkv) {
     const int pos = ctx_len[s] + (new_off[s + 1] - new_off[s]) + i;
     float cs[2], sn[2];
-    for (int j = 0; j < d / 64; ++j) rope_cs(pos, lane + 32 * j, d, log2_theta, &cs[j], &sn[j]);
+    for (int j = 0; j < d / 64; ++j) rope_cs(pos, freq.inv[lane + 32 * j], &cs[j], &sn[j]);
     head_norm_rope(x, d, hh < nq ? qn : kn, eps, cs, sn);
   }
   T* dst = hh < nq         ? q + ((size_t)row * nq + hh) * d
@@ -483,11 +579,11 @@ __global__ void __launch_bounds__(RT) act_kernel(const float* __restrict__ Y, in
   } while (0)
 
 int launch_rows_feature_norm(int dtype, const float* Y, int rows, int H, const void* gamma, float eps, void* f_out,
-                             const Ctx& c) {
+                             const RopeTab& rt, const Ctx& c) {
   if (rows <= 0) return DFLASH2_OK;
   int rc;
   DF2_DISPATCH(dtype, rc = launch_k(feature_norm_kernel<T>, dim3(rows), dim3(RT), H * sizeof(float), c, Y, H,
-                                    static_cast<const T*>(gamma), eps, static_cast<T*>(f_out)));
+                                    static_cast<const T*>(gamma), eps, static_cast<T*>(f_out), rt, c.status));
   return rc;
 }
 
@@ -495,22 +591,24 @@ int launch_kv_append(int dtype, const float* Y, int rows, int nkv, int d, const 
                      const int32_t* ctx_len, const int32_t* new_off, int batch, const int32_t* block_table,
                      int max_pages, int page_size, int n_pages, void* kc, void* vc, const Ctx& c) {
   if (rows <= 0) return DFLASH2_OK;
-  const double l2t = std::log2((double)theta);
+  const RopeFreq freq = rope_freq(d, theta);
   int rc;
   const dim3 grid(rows, (2 * nkv + RT / 32 - 1) / (RT / 32));
   DF2_DISPATCH(dtype, rc = launch_k(kv_append_kernel<T>, grid, dim3(RT), 0, c, Y, nkv, d,
-                                    static_cast<const T*>(k_norm), eps, l2t, ctx_len, new_off, batch, block_table,
+                                    static_cast<const T*>(k_norm), eps, freq, ctx_len, new_off, batch, block_table,
                                     max_pages, page_size, n_pages, static_cast<T*>(kc), static_cast<T*>(vc),
                                     c.status));
   return rc;
 }
 
 int launch_embed_norm(int dtype, const int32_t* anchor, int mask_id, int batch, int B, const void* embed, int V, int H,
-                      float scale, const void* gamma, float eps, float* h_out, void* u_out, const Ctx& c) {
+                      float scale, const void* gamma, float eps, float* h_out, void* u_out, const RopeTab& rt,
+                      const Ctx& c) {
   int rc;
   DF2_DISPATCH(dtype, rc = launch_k(embed_norm_kernel<T>, dim3(batch * B), dim3(RT), H * sizeof(float), c,
                                     anchor, mask_id, B, static_cast<const T*>(embed), V, H, scale,
-                                    static_cast<const T*>(gamma), eps, h_out, static_cast<T*>(u_out), c.status));
+                                    static_cast<const T*>(gamma), eps, h_out, static_cast<T*>(u_out), rt,
+                                    c.status));
   return rc;
 }
 
@@ -553,7 +651,8 @@ bool conv_prologue_fits(int dtype, int batch, int B, int H, int G, int nsm) {
 
 int launch_conv_prologue(int dtype, const float* h_in, const int32_t* anchor, int mask_id, const void* embed, int V,
                          float scale, const void* gamma, float eps, const void* w_tap, int batch, int B, int H,
-                         int group_size, float* h_out, void* u_out, void* u2_out, const Ctx& c) {
+                         int group_size, float* h_out, void* u_out, void* u2_out, const RopeTab& rt,
+                         const Ctx& c) {
   const int G = H / group_size;
   const int gpc = conv_prologue_groups(G, batch, c.nsm);
   const bool stage_w = conv_prologue_smem(dtype, B, H, gpc, true) <= kPrologueSmem;
@@ -578,23 +677,23 @@ int launch_conv_prologue(int dtype, const float* h_in, const int32_t* anchor, in
     DF2_DISPATCH(dtype, rc = launch_k(conv_prologue_kernel<T, false>, grid, dim3(PT), smem, c, h_in, anchor, mask_id,
                                       static_cast<const T*>(embed), V, scale, static_cast<const T*>(gamma), eps,
                                       static_cast<const T*>(w_tap), H, group_size, gpc, B, stage_w ? 1 : 0, h_out,
-                                      static_cast<T*>(u_out), static_cast<T*>(u2_out), c.status));
+                                      static_cast<T*>(u_out), static_cast<T*>(u2_out), rt, c.status));
   else
     DF2_DISPATCH(dtype, rc = launch_k(conv_prologue_kernel<T, true>, grid, dim3(PT), smem, c, h_in, anchor, mask_id,
                                       static_cast<const T*>(embed), V, scale, static_cast<const T*>(gamma), eps,
                                       static_cast<const T*>(w_tap), H, group_size, gpc, B, stage_w ? 1 : 0, h_out,
-                                      static_cast<T*>(u_out), static_cast<T*>(u2_out), c.status));
+                                      static_cast<T*>(u_out), static_cast<T*>(u2_out), rt, c.status));
   return rc;
 }
 
 int launch_qkv_epilogue(int dtype, const float* Y, int rows, int B, int nq, int nkv, int d, const void* q_norm,
                         const void* k_norm, float eps, float theta, const int32_t* ctx_len, const int32_t* new_off,
                         void* q, void* kb, void* vb, const Ctx& c) {
-  const double l2t = std::log2((double)theta);
+  const RopeFreq freq = rope_freq(d, theta);
   int rc;
   const dim3 grid(rows, (nq + 2 * nkv + RT / 32 - 1) / (RT / 32));
   DF2_DISPATCH(dtype, rc = launch_k(qkv_epi_kernel<T>, grid, dim3(RT), 0, c, Y, B, nq, nkv, d,
-                                    static_cast<const T*>(q_norm), static_cast<const T*>(k_norm), eps, l2t, ctx_len,
+                                    static_cast<const T*>(q_norm), static_cast<const T*>(k_norm), eps, freq, ctx_len,
                                     new_off, static_cast<T*>(q), static_cast<T*>(kb), static_cast<T*>(vb)));
   return rc;
 }

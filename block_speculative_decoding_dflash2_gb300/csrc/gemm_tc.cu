@@ -25,6 +25,16 @@
 // deterministic and no CTA waits for another.  The top-k contraction (the
 // lm_head) needs whole tiles: its CTAs take whole tiles round-robin.
 //
+// Epilogues: the plain fp32 output (stored or added to), the streaming top-k
+// of the lm_head, and two fused ones that remove a kernel each:
+//   SWIGLU  the gate/up contraction: a 128-row tile holds 64 gate rows and
+//           the 64 matching up rows (two 64-row TMA boxes), and the epilogue
+//           writes SiLU(gate) * up in bf16;
+//   HEADS   the q/k/v contractions: a tile holds one 128-wide head (or two
+//           64-wide), and the epilogue applies the per-head RMSNorm and
+//           RoPE of q and k and stores bf16 q, k, v: to the block's q/k/v
+//           buffers, or, for appended context rows, into the paged cache.
+//
 // Warp roles (192 threads):
 //   warp 0      TMA producer (one lane): weight + activation tiles -> ring
 //   warp 1      MMA issuer (one lane) and TMEM owner
@@ -39,6 +49,8 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
+#include <cstring>
 #include <climits>
 #include <mutex>
 
@@ -69,7 +81,22 @@ struct TcArgs {
   float* debug;
   float mult, cap;
   unsigned* status;
+  // SWIGLU
+  bf16* act;  // [N][I], I = M / 2
+  int I;
+  // HEADS: M rows = n_qh q heads, n_kh k heads, n_kh v heads of width hd
+  int hd, n_qh, n_kh;
+  const bf16* qn;  // [hd] q-norm gain (n_qh > 0)
+  const bf16* kn;  // [hd] k-norm gain
+  float eps;
+  const float2* rope;    // [N][hd/2] (cos, sin) at each column's position
+  const long long* dst;  // appended rows: [N] element offset of the row in the paged cache, -1: skip
+  int append;
+  bf16 *q, *kb, *vb;  // block rows: [N][heads][hd]
+  bf16 *kc, *vc;      // appended rows: paged cache [pages][page_size][n_kh][hd]
 };
+
+enum { EPI_PLAIN = 0, EPI_TOPK = 1, EPI_SWIGLU = 2, EPI_HEADS = 3 };
 
 template <int BN>
 struct TcCfg {
@@ -77,13 +104,15 @@ struct TcCfg {
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int TOPK_EXTRA = 16 * BM * 4 + BN * KMAX * 8;
+  static constexpr int FUSE_EXTRA = 16 * BM * 4 + 4 * 16 * 4;  // exchange tile, column sums
   static constexpr int FIXED = 1024 /* alignment slack */ + 1024 /* barriers */;
-  __host__ __device__ static constexpr int stages(bool topk) {
-    return ((SMEM_BUDGET - FIXED - (topk ? TOPK_EXTRA : 0)) / STAGE) > 12
-               ? 12
-               : ((SMEM_BUDGET - FIXED - (topk ? TOPK_EXTRA : 0)) / STAGE);
+  __host__ __device__ static constexpr int extra(int epi) {
+    return epi == EPI_TOPK ? TOPK_EXTRA : (epi >= EPI_SWIGLU ? FUSE_EXTRA : 0);
   }
-  __host__ __device__ static constexpr int smem_bytes(bool topk) { return FIXED + stages(topk) * STAGE + (topk ? TOPK_EXTRA : 0); }
+  __host__ __device__ static constexpr int stages(int epi) {
+    return ((SMEM_BUDGET - FIXED - extra(epi)) / STAGE) > 12 ? 12 : ((SMEM_BUDGET - FIXED - extra(epi)) / STAGE);
+  }
+  __host__ __device__ static constexpr int smem_bytes(int epi) { return FIXED + stages(epi) * STAGE + extra(epi); }
   static constexpr uint32_t TMEM_COLS = (2 * BN <= 32)    ? 32
                                         : (2 * BN <= 64)  ? 64
                                         : (2 * BN <= 128) ? 128
@@ -151,11 +180,12 @@ __device__ __forceinline__ bool named_sync_or(bool pred) {
   return r != 0;
 }
 
-template <int BN, bool TOPK>
+template <int BN, int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcArgs a) {
   using C = TcCfg<BN>;
-  constexpr int STAGES = C::stages(TOPK);
+  constexpr bool TOPK = EPI == EPI_TOPK;
+  constexpr int STAGES = C::stages(EPI);
   constexpr int A_BYTES = C::A_BYTES, B_BYTES = C::B_BYTES;
   static_assert(STAGES >= 2, "ring too small");
   static_assert(B_BYTES % 1024 == 0, "B tile must keep 1024-byte swizzle atoms aligned");
@@ -176,6 +206,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   float* stg = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 1024);  // [16][BM]
   float* lv_s = stg + 16 * BM;                                                       // [BN][KMAX]
   int* li_s = reinterpret_cast<int*>(lv_s + BN * KMAX);                              // [BN][KMAX]
+  float* ssb = stg + 16 * BM;  // fused: [4 warps][16 columns] sums
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_launch_next();
@@ -216,6 +247,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
+      // weight tile of chunk kc for m-tile mt (SWIGLU: 64 gate rows + the 64 matching up rows)
+      auto load_a = [&](int st, int kc_, int mt_) {
+        if constexpr (EPI == EPI_SWIGLU) {
+          tma_load_2d(stA + st * A_BYTES, &tmA, full + st, kc_ * BK, mt_ * (BM / 2), pol_w);
+          tma_load_2d(stA + st * A_BYTES + A_BYTES / 2, &tmA, full + st, kc_ * BK, a.I + mt_ * (BM / 2), pol_w);
+        } else {
+          tma_load_2d(stA + st * A_BYTES, &tmA, full + st, kc_ * BK, mt_ * BM, pol_w);
+        }
+      };
       UnitIter it = unit_iter(a);
       int t = 0, kc = 0, k1 = 0;
       bool have = it.next(t, kc, k1);
@@ -228,7 +268,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         bool h = have;
         while (pre < STAGES && h) {
           mbar_arrive_expect_tx(full + pre, A_BYTES + B_BYTES);
-          tma_load_2d(stA + pre * A_BYTES, &tmA, full + pre, kk * BK, (tt % a.m_tiles) * BM, pol_w);
+          load_a(pre, kk, tt % a.m_tiles);
           ++pre;
           if (++kk == kk1) h = pit.next(tt, kk, kk1);
         }
@@ -254,7 +294,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           mbar_arrive_expect_tx(full + stage, A_BYTES + B_BYTES);
-          tma_load_2d(stA + stage * A_BYTES, &tmA, full + stage, kc * BK, mt * BM, pol_w);
+          load_a(stage, kc, mt);
           tma_load_2d(stB + stage * B_BYTES, &tmB, full + stage, kc * BK, nt * BN, pol_x);
           ++issued;
           if (++stage == STAGES) {
@@ -375,8 +415,105 @@ __global__ void __launch_bounds__(THREADS, 1)
           return a.partial + ((size_t)g * 2 + slot) * BN * BM;
         };
         float* pc = direct ? nullptr : piece(blockIdx.x);
-        // (each block of 16 columns: all loads first, then the stores, so
-        //  the loads of old values and of pieces overlap instead of queueing)
+        // final values of columns nt*BN + c0 .. +15 of this thread's row m.
+        // All loads of a step are issued before its stores, so they overlap
+        // instead of queueing.  The fused epilogues synchronise the four
+        // epilogue warps; every call site is uniform across them.
+        auto finish = [&](float(&v)[16], int c0) {
+          const int nb = nt * BN + c0;       // first column
+          const int nj = min(16, a.N - nb);  // valid columns (may be <= 0)
+          if constexpr (EPI == EPI_PLAIN) {
+            if (m < a.M && nj > 0) {
+              float* p0 = a.out + (size_t)nb * a.M + m;
+              if (a.accumulate) {
+                float old[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) old[j] = j < nj ? p0[(size_t)j * a.M] : 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = old[j] + v[j];
+              }
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (j < nj) p0[(size_t)j * a.M] = v[j];
+            }
+          } else if constexpr (EPI == EPI_SWIGLU) {
+            // rows 0..63: gate of index i = mt*64 + row; rows 64..127: up of the same i
+            constexpr int HB = BM / 2;
+            const int hr = row & (HB - 1);
+            if (row >= HB) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) stg[j * HB + hr] = v[j];
+            }
+            named_sync_epi();
+            if (row < HB) {
+              const int i = mt * HB + hr;
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (j < nj) {
+                  const float gt = v[j], up = stg[j * HB + hr];
+                  a.act[(size_t)(nb + j) * a.I + i] = __float2bfloat16_rn(gt / (1.f + expf(-gt)) * up);
+                }
+            }
+            named_sync_epi();
+          } else if constexpr (EPI == EPI_HEADS) {
+            const int tid = threadIdx.x - 64, wq = tid >> 5;
+            const int d = a.hd;
+            const int hg = m / d, di = m - hg * d;
+            const bool valid = m < a.M;
+            const int kind = hg < a.n_qh ? 0 : (hg < a.n_qh + a.n_kh ? 1 : 2);  // q, k, v
+            // per-column sums of squares over this warp's 32 rows
+            float x[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) x[j] = warp_sum(valid ? v[j] * v[j] : 0.f);
+            if (lane == 0) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) ssb[wq * 16 + j] = x[j];
+            }
+            named_sync_epi();
+            // RMSNorm of q/k heads (a head spans all 128 rows, or a 64-row half)
+            const float gdi = (kind < 2 && valid) ? ld((kind == 0 ? a.qn : a.kn) + di) : 1.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float ss = d == BM ? (ssb[j] + ssb[16 + j]) + (ssb[32 + j] + ssb[48 + j])
+                                       : (wq < 2 ? ssb[j] + ssb[16 + j] : ssb[32 + j] + ssb[48 + j]);
+              x[j] = kind < 2 ? v[j] * (rsqrtf(ss / (float)d + a.eps) * gdi) : v[j];
+              stg[j * BM + row] = x[j];
+            }
+            named_sync_epi();
+            // RoPE: rotate-half pairs (di, di + d/2), angles from the table
+            if (kind < 2 && valid) {
+              const int half = d / 2, ip = di % half;
+              const float sgn = di < half ? -1.f : 1.f;
+              float2 cs[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (j < nj) cs[j] = a.rope[(size_t)(nb + j) * half + ip];
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (j < nj) x[j] = x[j] * cs[j].x + sgn * (stg[j * BM + (row ^ half)] * cs[j].y);
+            }
+            if (valid) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                if (j >= nj) continue;
+                const bf16 val = __float2bfloat16_rn(x[j]);
+                const size_t n = (size_t)(nb + j);
+                if (!a.append) {
+                  if (kind == 0) a.q[(n * a.n_qh + hg) * d + di] = val;
+                  else if (kind == 1) a.kb[(n * a.n_kh + (hg - a.n_qh)) * d + di] = val;
+                  else a.vb[(n * a.n_kh + (hg - a.n_qh - a.n_kh)) * d + di] = val;
+                } else {
+                  const long long dj = a.dst[nb + j];
+                  if (dj >= 0) {
+                    if (kind == 1) a.kc[dj + (size_t)(hg - a.n_qh) * d + di] = val;
+                    else if (kind == 2) a.vc[dj + (size_t)(hg - a.n_qh - a.n_kh) * d + di] = val;
+                  }
+                }
+              }
+            }
+            named_sync_epi();  // the exchange tile and column info are reused next
+          }
+        };
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 16) {
           float v[16];
@@ -384,19 +521,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (!direct) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) pc[(c0 + j) * BM + row] = v[j];
-          } else if (m < a.M) {
-            float* p0 = a.out + (size_t)(nt * BN + c0) * a.M + m;
-            const int nj = min(16, a.N - (nt * BN + c0));
-            if (a.accumulate) {
-              float old[16];
-#pragma unroll
-              for (int j = 0; j < 16; ++j) old[j] = j < nj ? p0[(size_t)j * a.M] : 0.f;
-#pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] += old[j];
-            }
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (j < nj) p0[(size_t)j * a.M] = v[j];
+          } else {
+            finish(v, c0);
           }
         }
         tc_fence_before();
@@ -415,28 +541,24 @@ __global__ void __launch_bounds__(THREADS, 1)
               float sum[16];
 #pragma unroll
               for (int j = 0; j < 16; ++j) sum[j] = 0.f;
-              for (int g = g_first; g <= g_last; ++g) {
-                const float* pg = piece(g) + (size_t)c0 * BM + row;
-                float v[16];
+              constexpr int PB = 4;  // pieces per round of loads
+              for (int g0 = g_first; g0 <= g_last; g0 += PB) {
+                float v[PB][16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) v[j] = __ldcg(pg + j * BM);
+                for (int q2 = 0; q2 < PB; ++q2)
+                  if (g0 + q2 <= g_last) {
+                    const float* pg = piece(g0 + q2) + (size_t)c0 * BM + row;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) sum[j] += v[j];
+                    for (int j = 0; j < 16; ++j) v[q2][j] = __ldcg(pg + j * BM);
+                  }
+#pragma unroll
+                for (int q2 = 0; q2 < PB; ++q2)
+                  if (g0 + q2 <= g_last) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) sum[j] += v[q2][j];
+                  }
               }
-              if (m < a.M) {
-                float* p0 = a.out + (size_t)(nt * BN + c0) * a.M + m;
-                const int nj = min(16, a.N - (nt * BN + c0));
-                if (a.accumulate) {
-                  float old[16];
-#pragma unroll
-                  for (int j = 0; j < 16; ++j) old[j] = j < nj ? p0[(size_t)j * a.M] : 0.f;
-#pragma unroll
-                  for (int j = 0; j < 16; ++j) sum[j] = old[j] + sum[j];
-                }
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                  if (j < nj) p0[(size_t)j * a.M] = sum[j];
-              }
+              finish(sum, c0);
             }
             if (threadIdx.x == 64) a.counters[g_first] = 0;
           }
@@ -571,20 +693,39 @@ int pick_bn(int M, int N) {
   return 256;
 }
 
-template <int BN, bool TOPK>
+template <int BN, int EPI>
 int launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs& args, int grid, const Ctx& c) {
-  constexpr int smem = TcCfg<BN>::smem_bytes(TOPK);
+  constexpr int smem = TcCfg<BN>::smem_bytes(EPI);
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(tc_gemm_kernel<BN, TOPK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+    if (cudaFuncSetAttribute(tc_gemm_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
       return DFLASH2_ERR_CUDA;
     attr_set = true;
   }
-  return launch_k(tc_gemm_kernel<BN, TOPK>, dim3(grid), dim3(THREADS), smem, c, ma, mb, args);
+  return launch_k(tc_gemm_kernel<BN, EPI>, dim3(grid), dim3(THREADS), smem, c, ma, mb, args);
+}
+
+template <int BN>
+int launch_epi(int epi, const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs& args, int grid, const Ctx& c) {
+  switch (epi) {
+    case EPI_TOPK: return launch_bn<BN, EPI_TOPK>(ma, mb, args, grid, c);
+    case EPI_SWIGLU:
+      if constexpr (BN <= 64) return launch_bn<BN, EPI_SWIGLU>(ma, mb, args, grid, c);
+      return DFLASH2_ERR_SHAPE;
+    case EPI_HEADS:
+      if constexpr (BN <= 64) return launch_bn<BN, EPI_HEADS>(ma, mb, args, grid, c);
+      return DFLASH2_ERR_SHAPE;
+    default: return launch_bn<BN, EPI_PLAIN>(ma, mb, args, grid, c);
+  }
 }
 
 }  // namespace
+
+bool gemm_fusable(int M, int N, int epi) {
+  if (pick_bn(M, N) > 64) return false;
+  return epi != kEpiSwiglu || M % BM == 0;
+}
 
 size_t gemm_partial_bytes(int M, int N) { return (size_t)kMaxSM * 2 * BM * pick_bn(M, N) * sizeof(float); }
 
@@ -608,7 +749,10 @@ int gemm_max_lists() { return std::max(kMaxSM, 0); }
 int gemm_bf16(const GemmOp& g, const Ctx& c) {
   if (g.M <= 0 || g.N <= 0 || g.K <= 0) return DFLASH2_ERR_SHAPE;
   const int bn = pick_bn(g.M, g.N);
+  const int epi = g.topk ? EPI_TOPK : g.epi;
+  if (epi >= EPI_SWIGLU && !gemm_fusable(g.M, g.N, epi)) return DFLASH2_ERR_SHAPE;
   TcArgs a;
+  std::memset(&a, 0, sizeof(a));
   a.M = g.M;
   a.N = g.N;
   a.K = g.K;
@@ -623,7 +767,12 @@ int gemm_bf16(const GemmOp& g, const Ctx& c) {
   a.counters = g.counters;
   a.accumulate = g.accumulate ? 1 : 0;
   if (a.stream && (!g.partial || !g.counters)) return DFLASH2_ERR_INVALID_ARG;
-  const long want = a.stream ? (g.ctas > 0 ? std::min(g.ctas, kMaxSM) : c.nsm) : c.nsm;
+  // stream-K: one CTA per SM, but at least kMinChunks chunks per CTA, so a
+  // shared tile has few pieces to sum (each piece costs its last CTA a load)
+  constexpr long kMinChunks = 8;
+  const long want = a.stream ? (g.ctas > 0 ? std::min(g.ctas, kMaxSM)
+                                           : std::max(1L, std::min<long>(c.nsm, a.work / kMinChunks)))
+                             : c.nsm;
   const int grid = (int)std::min<long>(want, a.stream ? a.work : a.tiles);
   a.lists_v = g.lists_v;
   a.lists_i = g.lists_i;
@@ -632,19 +781,44 @@ int gemm_bf16(const GemmOp& g, const Ctx& c) {
   a.cap = g.cap;
   a.status = c.status;
   if (g.topk && a.n_tiles > 32) return DFLASH2_ERR_SHAPE;
+  if (epi == EPI_SWIGLU) {
+    if (!g.act) return DFLASH2_ERR_INVALID_ARG;
+    a.act = static_cast<bf16*>(g.act);
+    a.I = g.M / 2;
+  } else if (epi == EPI_HEADS) {
+    if (g.hd * (g.n_qh + 2 * g.n_kh) != g.M || (g.hd != 64 && g.hd != BM) || !g.kn || (g.n_qh > 0 && !g.qn) ||
+        !g.rope)
+      return DFLASH2_ERR_INVALID_ARG;
+    if (g.append ? (!g.kc || !g.vc || !g.dst || g.n_qh != 0) : (!g.q || !g.kb || !g.vb))
+      return DFLASH2_ERR_INVALID_ARG;
+    a.hd = g.hd;
+    a.n_qh = g.n_qh;
+    a.n_kh = g.n_kh;
+    a.qn = static_cast<const bf16*>(g.qn);
+    a.kn = static_cast<const bf16*>(g.kn);
+    a.eps = g.eps;
+    a.rope = g.rope;
+    a.dst = g.dst;
+    a.append = g.append;
+    a.q = static_cast<bf16*>(g.q);
+    a.kb = static_cast<bf16*>(g.kb);
+    a.vb = static_cast<bf16*>(g.vb);
+    a.kc = static_cast<bf16*>(g.kc);
+    a.vc = static_cast<bf16*>(g.vc);
+  }
 
   CUtensorMap ma, mb;
-  int rc = make_map(&ma, g.W, g.M, g.K, g.ldw, BM);
+  int rc = make_map(&ma, g.W, g.M, g.K, g.ldw, epi == EPI_SWIGLU ? BM / 2 : BM);
   if (rc) return rc;
   rc = make_map(&mb, g.X, g.N, g.K, g.ldx, bn);
   if (rc) return rc;
 
   switch (bn) {
-    case 16: return g.topk ? launch_bn<16, true>(ma, mb, a, grid, c) : launch_bn<16, false>(ma, mb, a, grid, c);
-    case 32: return g.topk ? launch_bn<32, true>(ma, mb, a, grid, c) : launch_bn<32, false>(ma, mb, a, grid, c);
-    case 64: return g.topk ? launch_bn<64, true>(ma, mb, a, grid, c) : launch_bn<64, false>(ma, mb, a, grid, c);
-    case 128: return g.topk ? launch_bn<128, true>(ma, mb, a, grid, c) : launch_bn<128, false>(ma, mb, a, grid, c);
-    default: return g.topk ? launch_bn<256, true>(ma, mb, a, grid, c) : launch_bn<256, false>(ma, mb, a, grid, c);
+    case 16: return launch_epi<16>(epi, ma, mb, a, grid, c);
+    case 32: return launch_epi<32>(epi, ma, mb, a, grid, c);
+    case 64: return launch_epi<64>(epi, ma, mb, a, grid, c);
+    case 128: return launch_epi<128>(epi, ma, mb, a, grid, c);
+    default: return launch_epi<256>(epi, ma, mb, a, grid, c);
   }
 }
 

@@ -39,7 +39,27 @@ struct GemmOp {
   int* lists_i;
   float* debug;  // nullable [N][M] logits after the transform
   float mult, cap;
+  // fused epilogues (bf16 path, activation tiles of at most 64 rows; see
+  // gemm_fusable): 0 = plain fp32 out; kEpiSwiglu = gate/up rows [0, M/2) and
+  // [M/2, M) -> act [N][M/2] bf16 = SiLU(gate) * up; kEpiHeads = per-head
+  // RMSNorm + RoPE of q/k heads and copy of v heads, to q/kb/vb (block rows)
+  // or to the paged cache (appended rows).
+  int epi;
+  void* act;
+  int hd, n_qh, n_kh;
+  const void* qn;
+  const void* kn;
+  float eps;
+  const float2* rope;    // [N][hd/2] (cos, sin) per column (RopeTab::cs)
+  const long long* dst;  // appended rows: [N] paged-cache offsets (RopeTab::dst)
+  int append;
+  void *q, *kb, *vb, *kc, *vc;
 };
+constexpr int kEpiSwiglu = 2, kEpiHeads = 3;
+
+// Whether an M x N contraction can take a fused epilogue (activation tiles of
+// at most 64 rows; the gate/up pairing also needs M % 128 == 0).
+bool gemm_fusable(int M, int N, int epi);
 
 // Bytes of stream-K partial pieces an M x N contraction can need (any SM count).
 size_t gemm_partial_bytes(int M, int N);
@@ -104,15 +124,39 @@ int gemm_f32(const GemmOp& g, const Ctx& c);   // exact fp32 FMA, SIMT
 // Tiles (m_tiles * n_tiles) of a contraction, the size of its counter array.
 int gemm_tiles(int M, int N);
 
+// Inverse frequencies theta^(-2i/d) of the rotary pairs i < d/2, in double,
+// computed once on the host and passed to the kernels that form angles.
+struct RopeFreq {
+  double inv[64];
+};
+RopeFreq rope_freq(int d, float theta);
+
+// RoPE angles (and, for appended rows, paged-cache destinations) that the
+// row kernels running ahead of a fused heads epilogue store for it: the
+// block rows' table comes from the first sublayer prologue (or the embedding
+// kernel), the appended rows' from the feature norm.
+struct RopeTab {
+  float2* cs;       // [rows][d/2] (cos, sin) of pair i at the row's position; nullptr: not wanted
+  long long* dst;   // appended rows: element offset of the row in the paged cache (-1: invalid)
+  int d;
+  RopeFreq freq;
+  const int32_t* ctx_len;
+  const int32_t* new_off;
+  int batch;
+  const int32_t* block_table;  // appended rows only
+  int max_pages, page_size, n_pages, nkv;
+};
+
 // element-wise / row kernels (elementwise.cu); T = float or bf16 by dtype.
 // Y is the producing contraction's final fp32 output, row-major [rows][width].
 int launch_rows_feature_norm(int dtype, const float* Y, int rows, int H, const void* gamma, float eps, void* f_out,
-                             const Ctx& c);
+                             const RopeTab& rt, const Ctx& c);
 int launch_kv_append(int dtype, const float* Y, int rows, int nkv, int d, const void* k_norm, float eps, float theta,
                      const int32_t* ctx_len, const int32_t* new_off, int batch, const int32_t* block_table,
                      int max_pages, int page_size, int n_pages, void* kc, void* vc, const Ctx& c);
 int launch_embed_norm(int dtype, const int32_t* anchor, int mask_id, int batch, int B, const void* embed, int V, int H,
-                      float scale, const void* gamma, float eps, float* h_out, void* u_out, const Ctx& c);
+                      float scale, const void* gamma, float eps, float* h_out, void* u_out, const RopeTab& rt,
+                      const Ctx& c);
 int launch_rownorm(int dtype, const float* h, int rows, int H, const void* gamma, float eps, void* u_out, int B,
                    int skip_anchor, const Ctx& c);
 int launch_dyn_conv(int dtype, const void* u, const float* Y, int rows, int H, int group_size, int B, void* u2_out,
@@ -130,7 +174,7 @@ int launch_act(int dtype, const float* Y, int rows, int I, void* act, const Ctx&
 bool conv_prologue_fits(int dtype, int batch, int B, int H, int G, int nsm);
 int launch_conv_prologue(int dtype, const float* h_in, const int32_t* anchor, int mask_id, const void* embed, int V,
                          float scale, const void* gamma, float eps, const void* w_tap, int batch, int B, int H,
-                         int group_size, float* h_out, void* u_out, void* u2_out, const Ctx& c);
+                         int group_size, float* h_out, void* u_out, void* u2_out, const RopeTab& rt, const Ctx& c);
 
 // attention (attention.cu)
 int launch_attention(int dtype, const void* q, const void* kb, const void* vb, const void* kc, const void* vc,

@@ -1,8 +1,8 @@
 // DFlash 2 pairwise path selector ("Train a DFlash Drafter for Speculative
-// Decoding", "Variants": a pairwise path selector that walks one coherent
-// path through each position's top-k candidates; "Objective": its term is a
-// cross-entropy over the position's top-k candidates given the true
-// predecessor; "Key Config Fields": selector_rank is its width).
+// Decoding", "Variants": pairwise scores between consecutive choices pick one
+// of each position's top-k candidates so the picks form one consistent
+// sequence; "Objective": trained by a cross-entropy over a position's top-k
+// given the true predecessor; "Key Config Fields": selector_rank is its width).
 //
 // Reading implemented here: factors A = W_a E[tok] and Bf = W_b E[tok] of the
 // shared embedding; transition score of candidate j at draft position i
@@ -53,11 +53,13 @@ __global__ void __launch_bounds__(512) viterbi_kernel(const float* __restrict__ 
                                                       const int32_t* __restrict__ cand_id,
                                                       const float* __restrict__ cand_logit, int D, int k, int r,
                                                       int32_t* __restrict__ path, float* __restrict__ path_score) {
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   pdl_launch_next();
   pdl_wait();
   const int s = blockIdx.x;
-  const int nt = D * k + 1, w = 2 * r, ws = w + 1;  // padded row stride: no bank conflicts across candidates
+  // padded row stride: rows start on different banks; a multiple of 4 when
+  // r is, so the dot products read float4s
+  const int nt = D * k + 1, w = 2 * r, ws = (r & 3) == 0 ? w + 4 : w + 1;
   float* F = sm;                               // [nt][ws] factors: A = F[t][0:r], Bf = F[t][r:2r]
   float* zs = F + (size_t)nt * ws;             // [D][k] candidate logits
   float* Sm = zs + D * k;                      // [1 + (D-1)k][k] transition log-probabilities
@@ -113,12 +115,23 @@ __global__ void __launch_bounds__(512) viterbi_kernel(const float* __restrict__ 
     cid[idx] = cand_id[(size_t)s * D * k + idx];
   }
   __syncthreads();
-  auto dot = [&](int ta, int tb) {  // <A[ta], Bf[tb]>
+  auto dot = [&](int ta, int tb) {  // <A[ta], Bf[tb]>: four partial sums, combined pairwise
     const float* a = F + (size_t)ta * ws;
     const float* b = F + (size_t)tb * ws + r;
-    float acc = 0.f;
-    for (int c = 0; c < r; ++c) acc = fmaf(a[c], b[c], acc);
-    return acc;
+    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+    if ((r & 3) == 0) {
+#pragma unroll 4
+      for (int c = 0; c < r; c += 4) {
+        const float4 x = *reinterpret_cast<const float4*>(a + c), y = *reinterpret_cast<const float4*>(b + c);
+        acc0 = fmaf(x.x, y.x, acc0);
+        acc1 = fmaf(x.y, y.y, acc1);
+        acc2 = fmaf(x.z, y.z, acc2);
+        acc3 = fmaf(x.w, y.w, acc3);
+      }
+    } else {
+      for (int c = 0; c < r; ++c) acc0 = fmaf(a[c], b[c], acc0);
+    }
+    return (acc0 + acc1) + (acc2 + acc3);
   };
   // 1. every transition score at once (they do not depend on the DP): row 0 is
   //    position 1 after the anchor; row 1 + (i-1)k + p is position i+1 after
@@ -189,7 +202,8 @@ __global__ void __launch_bounds__(512) viterbi_kernel(const float* __restrict__ 
 }  // namespace
 
 size_t viterbi_smem_bytes(int D, int k, int r) {
-  return sizeof(float) * ((size_t)(D * k + 1) * (2 * r + 1) + (size_t)D * k + (size_t)(1 + (D - 1) * k) * k +
+  const size_t ws = (r & 3) == 0 ? 2 * r + 4 : 2 * r + 1;
+  return sizeof(float) * ((size_t)(D * k + 1) * ws + (size_t)D * k + (size_t)(1 + (D - 1) * k) * k +
                           2 * (size_t)k) +
          sizeof(int) * 2 * (size_t)D * k;
 }

@@ -72,7 +72,8 @@ int dflash2_test_gemm(int dtype, const void* W, int M, int K, const void* X, int
   // the CTA count gemm_bf16 launched
   const long tiles = (long)gemm_tiles(M, N), work = tiles * ((K + 63) / 64);
   if (g.ctas < 0) return (int)std::min<long>(tiles, c.nsm);
-  return (int)std::min<long>(g.ctas > 0 ? g.ctas : c.nsm, work);
+  if (g.ctas > 0) return (int)std::min<long>(g.ctas, work);
+  return (int)std::min<long>(std::max(1L, std::min<long>(c.nsm, work / 8)), work);
 }
 
 int dflash2_test_layout(const dflash2_config* cfg, int batch, int n_new, int max_ctx, size_t* offsets, int n) {

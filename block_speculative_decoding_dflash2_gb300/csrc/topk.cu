@@ -5,10 +5,10 @@
 //
 // The lm_head GEMM (tcgen05 path) already leaves one sorted list of KMAX
 // entries per CTA and row.  topk_scan_kernel produces the same lists from
-// stored logits (fp32 path).  topk_merge_kernel reduces the lists of a row
-// with a tree of two-list merges in shared memory; each merge ranks every
-// entry of both lists against the other in one warp, so the result does not
-// depend on how the vocabulary was split.
+// stored logits (fp32 path).  topk_merge_kernel reduces the lists of a row:
+// the 16th best list head bounds the answer from below, and one warp picks
+// the top k of the entries it does not beat, so the result does not depend
+// on how the vocabulary was split.
 #include <algorithm>
 #include <climits>
 
@@ -56,49 +56,61 @@ __global__ void __launch_bounds__(128) topk_scan_kernel(const float* __restrict_
   }
 }
 
-// Merges sorted lists a (lanes 0..15 hold a[lane]) and b (lanes 16..31 hold
-// b[lane-16]) into the best KMAX, written to out_v/out_i[0..KMAX).  An entry's
-// rank in the union is its index in its own list plus the number of entries
-// of the other list that beat it (the order is strict: ids are distinct).
-__device__ __forceinline__ void warp_merge2(float v, int id, float* out_v, int* out_i) {
+// Top KMAX of `n` candidates (v[i], id[i]) in shared memory by one warp: a
+// sorted list in lanes 0..15, offered only the candidates that beat its last
+// entry (one ballot per 32 candidates).  Returns the list in (lv, li).
+__device__ __forceinline__ void warp_topk(const float* v, const int* id, int n, float& lv, int& li, float& tv,
+                                          int& ti) {
   const int lane = threadIdx.x & 31;
-  const int other = lane < KMAX ? KMAX : 0;
-  int rank = lane & (KMAX - 1);
-#pragma unroll
-  for (int t = 0; t < KMAX; ++t) {
-    const float ov = __shfl_sync(0xffffffffu, v, other + t);
-    const int oi = __shfl_sync(0xffffffffu, id, other + t);
-    rank += beats(ov, oi, v, id) ? 1 : 0;
+  lv = -INFINITY;
+  li = INT_MAX;
+  tv = -INFINITY;
+  ti = INT_MAX;
+  for (int base = 0; base < n; base += 32) {
+    const int i = base + lane;
+    const float x = i < n ? v[i] : -INFINITY;
+    const int xi = i < n ? id[i] : INT_MAX;
+    unsigned mask = __ballot_sync(0xffffffffu, i < n && beats(x, xi, tv, ti));
+    while (mask) {
+      const int src = __ffs(mask) - 1;
+      mask &= mask - 1;
+      warp_list_offer(lv, li, tv, ti, __shfl_sync(0xffffffffu, x, src), __shfl_sync(0xffffffffu, xi, src));
+    }
   }
-  __syncwarp();
-  if (rank < KMAX) {
-    out_v[rank] = v;
-    out_i[rank] = id;
-  }
-  __syncwarp();
 }
 
-// One CTA per row.  The row's n_lists lists are staged in shared memory and
-// merged pairwise, level by level (list 2j absorbs list 2j+1), one warp per
-// pair.  dynamic shared memory: n_lists * KMAX * 8 bytes.
-__global__ void __launch_bounds__(256) topk_merge_kernel(const float* __restrict__ lists_v,
-                                                         const int* __restrict__ lists_i, int n_lists, int rows,
-                                                         int k, int32_t* __restrict__ cand_id,
-                                                         float* __restrict__ cand_logit) {
+// One CTA per row.  The row's n_lists sorted lists are staged in shared
+// memory in one round of loads.  The 16th best list head tau bounds the
+// answer from below (16 distinct entries are at least tau), so only entries
+// that tau does not beat can be in the top KMAX; those survivors are
+// collected and one warp picks the top k of them.  The result is the exact
+// top k under the strict (value, id) order, whatever the vocabulary split.
+// dynamic shared memory: 2 * n_lists * KMAX * 8 bytes.
+constexpr int MT = 512;  // threads of the merge kernel
+
+__global__ void __launch_bounds__(MT) topk_merge_kernel(const float* __restrict__ lists_v,
+                                                        const int* __restrict__ lists_i, int n_lists, int rows,
+                                                        int k, int32_t* __restrict__ cand_id,
+                                                        float* __restrict__ cand_logit) {
   extern __shared__ float mv[];
+  __shared__ float tau_v;
+  __shared__ int tau_i, n_surv;
   pdl_launch_next();
   pdl_wait();
-  int* mi = reinterpret_cast<int*>(mv + n_lists * KMAX);
+  const int total = n_lists * KMAX;
+  int* mi = reinterpret_cast<int*>(mv + total);
+  float* sv = reinterpret_cast<float*>(mi + total);
+  int* si = reinterpret_cast<int*>(sv + total);
   const int row = blockIdx.x;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  constexpr int U = 8;  // loads in flight per thread
-  for (int base = threadIdx.x; base < n_lists * KMAX; base += blockDim.x * U) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int U = 8;  // loads in flight per thread (n_lists <= 256: one round)
+  for (int base = threadIdx.x; base < total; base += MT * U) {
     float v[U];
     int id[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int idx = base + u * blockDim.x;
-      if (idx < n_lists * KMAX) {
+      const int idx = base + u * MT;
+      if (idx < total) {
         const size_t o = ((size_t)(idx / KMAX) * rows + row) * KMAX + idx % KMAX;
         v[u] = lists_v[o];
         id[u] = lists_i[o];
@@ -106,30 +118,53 @@ __global__ void __launch_bounds__(256) topk_merge_kernel(const float* __restrict
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int idx = base + u * blockDim.x;
-      if (idx < n_lists * KMAX) {
+      const int idx = base + u * MT;
+      if (idx < total) {
         mv[idx] = v[u];
         mi[idx] = id[u];
       }
     }
   }
+  if (threadIdx.x == 0) n_surv = 0;
   __syncthreads();
-  for (int stride = 1; stride < n_lists; stride *= 2) {
-    for (int a = warp * 2 * stride; a < n_lists; a += nw * 2 * stride) {
-      const int b = a + stride;
-      if (b >= n_lists) continue;  // odd list out: carried to the next level as is
-      const int src = lane < KMAX ? a : b;
-      const float v = mv[src * KMAX + (lane & (KMAX - 1))];
-      const int id = mi[src * KMAX + (lane & (KMAX - 1))];
-      __syncwarp();
-      warp_merge2(v, id, mv + a * KMAX, mi + a * KMAX);
+  // tau: the KMAX-th best list head (heads are list entries 0, stride KMAX)
+  if (warp == 0) {
+    float lv, tv;
+    int li, ti;
+    // stage the heads contiguously in the survivor buffer, then select
+    for (int l = lane; l < n_lists; l += 32) {
+      sv[l] = mv[l * KMAX];
+      si[l] = mi[l * KMAX];
     }
-    __syncthreads();
+    __syncwarp();
+    warp_topk(sv, si, n_lists, lv, li, tv, ti);
+    if (lane == 0) {
+      tau_v = n_lists >= KMAX ? tv : -INFINITY;
+      tau_i = n_lists >= KMAX ? ti : INT_MAX;
+    }
   }
-  for (int e = threadIdx.x; e < k; e += blockDim.x) {
-    const int id = mi[e];
-    cand_id[(size_t)row * k + e] = id == INT_MAX ? -1 : id;
-    cand_logit[(size_t)row * k + e] = mv[e];
+  __syncthreads();
+  // survivors: entries that tau does not beat
+  const float tv0 = tau_v;
+  const int ti0 = tau_i;
+  for (int idx = threadIdx.x; idx < total; idx += MT) {
+    const float v = mv[idx];
+    const int id = mi[idx];
+    if (!beats(tv0, ti0, v, id)) {
+      const int p = atomicAdd(&n_surv, 1);
+      sv[p] = v;
+      si[p] = id;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    float lv, tv;
+    int li, ti;
+    warp_topk(sv, si, n_surv, lv, li, tv, ti);
+    if (lane < k) {
+      cand_id[(size_t)row * k + lane] = li == INT_MAX ? -1 : li;
+      cand_logit[(size_t)row * k + lane] = lv;
+    }
   }
 }
 
@@ -149,9 +184,16 @@ int launch_topk_scan(const float* logits, int rows, int V, float mult, float cap
 int launch_topk_merge(const float* lists_v, const int* lists_i, int n_lists, int rows, int k, int32_t* cand_id,
                       float* cand_logit, const Ctx& c) {
   if (n_lists < 1 || n_lists > 256 || k > KMAX) return DFLASH2_ERR_SHAPE;
-  const size_t smem = (size_t)n_lists * KMAX * 8;  // <= 32 KB
-  return launch_k(topk_merge_kernel, dim3(rows), dim3(256), smem, c, lists_v, lists_i, n_lists, rows, k,
-                  cand_id, cand_logit);
+  const size_t smem = 2 * (size_t)n_lists * KMAX * 8;  // lists and survivors, <= 64 KB
+  static bool attr = false;  // set once, before any capture
+  if (!attr) {
+    if (cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024) !=
+        cudaSuccess)
+      return DFLASH2_ERR_CUDA;
+    attr = true;
+  }
+  return launch_k(topk_merge_kernel, dim3(rows), dim3(MT), smem, c, lists_v, lists_i, n_lists, rows, k, cand_id,
+                  cand_logit);
 }
 
 }  // namespace df2

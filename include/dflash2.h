@@ -84,7 +84,7 @@ extern "C" {
  *   n_taps                 T, number of target layers tapped (target_layer_ids)
  *   block_size             B = 1 anchor + (B-1) drafts, 2..32
  *   conv_kernel_size       taps of the in-block convolution; must be 2
- *   conv_group_size        channels per dynamic correction; H % it == 0
+ *   conv_group_size        channels sharing one set of dynamic taps; H % it == 0
  *   top_k                  selector_top_k, 1..16
  *   selector_rank          r, 1..128
  *   page_size              context KV page length (tokens per page)
@@ -177,8 +177,8 @@ size_t dflash2_workspace_size(const dflash2_config *cfg, int max_batch,
 
 /*
  * Stage (a): feature projection and context K/V append.
- * "What is DFlash?": the draft is conditioned on hidden states captured from
- * the frozen target at target_layer_ids through a trained feature projection.
+ * "What is DFlash?": the draft reads hidden states tapped from the frozen
+ * target at target_layer_ids, mapped by a trained projection.
  *   n_new      host int, total appended rows (sum over the batch), >= 0
  *   new_taps   [n_new, T*H] target taps of the newly committed positions,
  *              concatenated in target_layer_ids order, rows grouped by

@@ -20,8 +20,8 @@ the source pages it follows, by page title and section:
               "What is DFlash?", "Variants", "Objective", "Data",
               "Key Config Fields").
 
-Where the pages leave a step open, the reading taken is marked READING and
-listed with the same number in the design notes.  Functions whose result
+Where the pages leave a step open, the docstring says which reading was
+taken ("Reading taken: ...").  Functions whose result
 cannot be pinned to anything but their own definition say "parity unpinned".
 """
 

@@ -12,7 +12,7 @@ Pages cited (title, then section):
 
 Numbers are float64 throughout.  With ``bf16=True`` the oracle rounds to
 bfloat16 (round to nearest, ties to even) at exactly the points where the GPU
-path stores a bf16 tensor between kernels (READING R15); everything else stays
+path stores a bf16 tensor between kernels (a reading: the pages fix no precision); everything else stays
 float64.  Pin status of each function is stated in its docstring; the pins
 themselves live in ``tests/test_oracle_pins.py``.
 
@@ -81,7 +81,7 @@ def _f64(a):
 def rms_norm(x, gamma, eps):
     """RMSNorm over the last axis: x / sqrt(mean(x^2) + eps) * gamma.
 
-    [Train] "What is DFlash?": the draft trains "its norms".  READING R3: the
+    [Train] "What is DFlash?": the draft trains "its norms".  Reading taken: the
     norm is RMSNorm (the Qwen3 targets the pages name in "Key Config Fields"
     use it) with learned gain gamma and no bias.
     """
@@ -91,7 +91,7 @@ def rms_norm(x, gamma, eps):
 
 
 def rope(x, pos, theta):
-    """Rotary position embedding, rotate-half layout.  READING R6.
+    """Rotary position embedding, rotate-half layout.  (A reading where the pages are silent.)
 
     x has shape [..., n_heads, d]; pos has shape x.shape[:-2].  For
     i < d/2 the pair (x[i], x[i+d/2]) is rotated by pos * theta**(-2i/d).
@@ -112,12 +112,15 @@ def silu(x):
 
 
 def dynamic_conv(u, w_tap, group_size, kernel_size=2):
-    """DFlash2 in-block dynamic grouped convolution of one block.  READING R7.
+    """DFlash2 in-block dynamic grouped convolution of one block.
 
-    [Train] "Variants": DFlash 2 adds "a two-tap in-block convolution around
-    every sublayer"; "Key Config Fields": conv_kernel_size is the number of
-    taps and conv_group_size the "channels per dynamic correction";
-    [vLLM] "DFlash2 inference": the convolutions are "dynamic".
+    [Train] "Variants": DFlash 2 wraps each sublayer of the draft in a short
+    convolution along the block (two taps); "Key Config Fields":
+    conv_kernel_size counts its taps and conv_group_size is how many channels
+    share one set of dynamic tap weights; [vLLM] "DFlash2 inference" calls
+    these convolutions dynamic.  Reading taken where the pages stop: taps are
+    predicted per position and group from the normed input and normalised by
+    a softmax over the taps; the window looks left and stays in the block.
 
     u       [B, H]  normed sublayer input of one block (position 0 = anchor)
     w_tap   [Kc*G, H]  tap generator; row Kc*g + j is tap j of group g
@@ -147,12 +150,11 @@ def dynamic_conv(u, w_tap, group_size, kernel_size=2):
 # --------------------------------------------------------------------------
 
 def project_features(cfg, W, taps, st):
-    """f = RMSNorm_hidden(taps @ W_fc^T).  READING R2.
+    """f = RMSNorm_hidden(taps @ W_fc^T).  (A reading where the pages are silent.)
 
-    [Train] "What is DFlash?": the block is "conditioned on hidden states
-    captured from the frozen target at target_layer_ids" through a trained
-    "feature projection"; [vLLM] "DFlash2 inference": dflash_config carries
-    target_layer_ids.  taps [n, T*H] is the concatenation of the T tapped
+    [Train] "What is DFlash?": the draft reads hidden states tapped from the
+    frozen target at target_layer_ids, mapped by a trained projection;
+    [vLLM] "DFlash2 inference": dflash_config carries target_layer_ids.  taps [n, T*H] is the concatenation of the T tapped
     hidden states in target_layer_ids order.  Parity unpinned beyond the
     special cases in the pin tests (identity blocks select one tap).
     """
@@ -163,7 +165,7 @@ def project_features(cfg, W, taps, st):
 def context_kv(cfg, Wl, f, pos, st):
     """Context keys/values of one draft layer from projected features.
 
-    READING R4: the features enter every draft layer as extra keys/values,
+    Reading taken: the features enter every draft layer as extra keys/values,
     K = RoPE(RMSNorm_k(W_k f)), V = W_v f, at their absolute positions.
     f [n, H], pos [n] -> K, V [n, nkv, d].
     """
@@ -201,7 +203,7 @@ def block_attention(q, Kc, Vc, Kb, Vb):
 
     [Train] "What is DFlash?": one "non-causal forward pass" over the block;
     [vLLM] "Requirements": the backend must support "the draft model's
-    non-causal attention".  READING R8: every block query sees every context
+    non-causal attention".  Reading taken: every block query sees every context
     key and every block key, no mask, scale 1/sqrt(d), grouped-query sharing
     (q head h reads kv head h // (nq/nkv)).
     q [B, nq, d]; Kc, Vc [P, nkv, d]; Kb, Vb [B, nkv, d] -> O [B, nq, d].
@@ -225,8 +227,8 @@ def block_attention(q, Kc, Vc, Kb, Vb):
 
 
 def draft_layer(cfg, Wl, h, ctxK, ctxV, pos, st):
-    """One draft decoder layer (READING R8: a Qwen3-style pre-norm layer
-    without biases, with the DFlash2 conv around both sublayers, R7).
+    """One draft decoder layer (Reading taken: a Qwen3-style pre-norm layer
+    without biases, with the DFlash2 conv around both sublayers).
 
     h [B, H] residual stream of one block (float64, never rounded);
     pos [B] absolute positions of the block.
@@ -261,13 +263,13 @@ def draft_layer(cfg, Wl, h, ctxK, ctxV, pos, st):
 def draft_block(cfg, W, anchor, ctx, st):
     """Logits of block positions 1..B-1 for one sequence.
 
-    [Train] "What is DFlash?": position 0 holds the real anchor token, the
-    rest are MASK (READING R1: mask_token_id from the config), the block is
+    [Train] "What is DFlash?": position 0 holds the anchor (a real token),
+    the rest are MASK (mask_token_id from the config), the block is
     embedded with the target's shared, frozen embed_tokens and read out with
     its lm_head.  "Key Config Fields": input_embedding_scale scales the
     embedded block; output_multiplier / final_logit_softcapping are the
-    target's logit transform (READING R9: z = m*logit, then cap*tanh(z/cap)
-    when cap > 0).  READING R5: with P committed context positions the anchor
+    target's logit transform (Reading taken: z = m*logit, then cap*tanh(z/cap)
+    when cap > 0).  Reading taken: with P committed context positions the anchor
     sits at position P and block position i at P+i.
     Returns z [B-1, V] (float64).
     """
@@ -292,7 +294,7 @@ def draft_block(cfg, W, anchor, ctx, st):
 
 def topk(z, k):
     """The k largest entries of z (last axis), sorted by value descending,
-    equal values by smaller token id first.  READING R11.
+    equal values by smaller token id first.  (A reading where the pages are silent.)
 
     [llama] "Configuration Notes" / [Train] "Key Config Fields":
     selector_top_k candidates are scored per position.
@@ -338,10 +340,10 @@ def draft_step(cfg, W, ctxs, anchors, new_taps, st):
 def selector_factors(cfg, W, tokens):
     """Low-rank factors of tokens: A = W_a E[tok], Bf = W_b E[tok].
 
-    READING R12: [Train] "Key Config Fields": selector_rank is the selector
-    "width"; "Objective": the selector term is scored "against the
-    ground-truth predecessor", so a transition pairs a predecessor token with
-    a candidate token.  The factors read the shared embedding.
+    [Train] "Key Config Fields": selector_rank sets the selector's width;
+    "Objective": the selector's loss conditions each position on its true
+    predecessor, so a transition pairs a predecessor token with a candidate
+    token.  Reading: the factors read the shared embedding.
     tokens [...] -> A, Bf [..., r].
     """
     r = cfg["selector_rank"]
@@ -356,11 +358,12 @@ def _logsumexp(x, axis):
 
 
 def select_path(cfg, W, anchor, cand_id, cand_z):
-    """Max-score path through the candidate lattice (Viterbi).  READING R12.
+    """Max-score path through the candidate lattice (Viterbi).
 
-    [Train] "Variants": a "pairwise path selector that walks one coherent
-    path through each position's top-k candidates"; [llama] "Configuration
-    Notes": the selector has transitions with a confidence (draft_p_min).
+    [Train] "Variants": the DFlash 2 selector scores pairs of consecutive
+    choices and picks one candidate per position so the picks form a single
+    consistent sequence; [llama] "Configuration Notes": the selector's
+    transitions carry a confidence (draft_p_min).
 
     Score of choosing candidate j at position i after predecessor token p:
         S_i(p, j) = z_i[j] + <A[p], Bf[c_{i,j}]>
@@ -439,7 +442,7 @@ def brute_force_path(cfg, W, anchor, cand_id, cand_z):
 # --------------------------------------------------------------------------
 
 def verify_accept(path, target):
-    """Greedy verification of one proposal.  READING R13.
+    """Greedy verification of one proposal.  (A reading where the pages are silent.)
 
     [llama] "Prerequisites": the target verifies [id_last, draft...] in one
     batch; t_i is the target's greedy token after [anchor, path_1..path_{i-1}],

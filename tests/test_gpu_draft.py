@@ -61,6 +61,16 @@ def test_fp32_rows_beyond_fused_prologue():
     check_case(case)
 
 
+def test_small_bf16_wide_batch():
+    # 10 sequences x 8 block rows: activation tiles wider than the fused
+    # epilogues take, so the block's q/k/v and SiLU*up run as separate kernels
+    # (the appended rows still take the fused K/V epilogue)
+    cfg = S.small_bf16_config(index=19)
+    ctx = [5, 17, 40, 0, 64, 3, 31, 90, 12, 8]
+    case = Case(cfg, ctx_lens=ctx, n_new=[1, 2, 8, 3, 0, 5, 1, 4, 2, 6], seed=19).run_gpu()
+    check_case(case)
+
+
 def test_small_bf16_block16_and_groups():
     cfg = S.small_bf16_config(block_size=16, n_q_heads=8, n_kv_heads=2, head_dim=128, top_k=16,
                               conv_group_size=64, index=12)

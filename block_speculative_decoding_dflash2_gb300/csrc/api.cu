@@ -94,7 +94,7 @@ Layout plan(const dflash2_config& c, int batch, int n_new, int max_ctx) {
     bool y;
   };
   const Shape shapes[8] = {{H, n_new, c.n_taps * H, true},      {2 * nkv * d, n_new, H, true},
-                           {2 * G, rows, H, true},              {(nq + 2 * nkv) * d, rows, H, true},
+                           {2 * G, rows, H, true},              {(nq + 2 * nkv) * d, rows + n_new, H, true},
                            {H, rows, nq * d, false},            {2 * I, rows, H, true},
                            {H, rows, I, false},                 {2 * r, nsel, H, true}};
   // the append branch (shapes 0-1) runs concurrently with the block branch
@@ -121,7 +121,6 @@ Layout plan(const dflash2_config& c, int batch, int n_new, int max_ctx) {
   L.status = take(256);
   L.cnt = take(kMaxSM * sizeof(int));
   L.cnta = take(kMaxSM * sizeof(int));
-  L.f = take((size_t)n_new * H * es);
   L.Y = take(Yb);
   L.P = take(P);
   L.Ya = take(Yba);
@@ -130,7 +129,10 @@ Layout plan(const dflash2_config& c, int batch, int n_new, int max_ctx) {
   L.u = take((size_t)rows * H * es);
   L.u2 = take((size_t)rows * H * es);
   L.ua = take((size_t)rows * H * es);
-  L.u2a = take((size_t)rows * H * es);
+  // u2a and f are one region: the merged QKV contraction reads the block's
+  // conv output and the appended rows' features as one activation matrix
+  L.u2a = take((size_t)(rows + n_new) * H * es);
+  L.f = L.u2a + (size_t)rows * H * es;
   L.q = take((size_t)rows * nq * d * es);
   L.kb = take((size_t)rows * nkv * d * es);
   L.vb = take((size_t)rows * nkv * d * es);
@@ -272,22 +274,23 @@ int check_weights(const dflash2_config& c, const dflash2_weights* w) {
   return DFLASH2_OK;
 }
 
-// stage (a): projection + paged K/V append of n_new rows
-int run_append(const dflash2_config& c, const dflash2_weights& w, void* kc, void* vc, int n_pages,
-               const int32_t* block_table, int max_pages, int batch, const int32_t* ctx_len, int n_new,
-               const void* taps, const int32_t* new_off, void* ws, const Layout& L, const Ctx& ctx) {
-  if (n_new == 0) return DFLASH2_OK;
-  const int H = c.hidden, nq = c.n_q_heads, nkv = c.n_kv_heads, d = c.head_dim;
+// Stage (a), first half: the feature projection of the n_new appended rows
+// into f (fc contraction, then the hidden norm).  With want_tables, the norm
+// kernel also leaves the rows' RoPE angles and paged-cache offsets for a fused
+// K/V epilogue.
+int project_features(const dflash2_config& c, const dflash2_weights& w, int n_pages, const int32_t* block_table,
+                     int max_pages, int batch, const int32_t* ctx_len, int n_new, const void* taps,
+                     const int32_t* new_off, void* ws, const Layout& L, bool want_tables, const Ctx& ctx,
+                     Ctx* rest_out) {
+  const int H = c.hidden, nkv = c.n_kv_heads, d = c.head_dim;
   float* Y = at<float>(ws, L.Ya);
-  void* f = at<char>(ws, L.f);
   // the first launch keeps the caller's ctx.pdl (false right after a fork)
   TRY(gemm(c, ctx, ws, L, w.fc, H, c.n_taps * H, taps, n_new, Y, false, true));
   Ctx rest = ctx;
   rest.pdl = true;
-  const bool fused_kv = c.dtype == DFLASH2_BF16 && gemm_fusable(2 * nkv * d, n_new, kEpiHeads);
   RopeTab rt;
   std::memset(&rt, 0, sizeof(rt));
-  if (fused_kv) {  // the feature norm also leaves the appended rows' RoPE angles and cache offsets
+  if (want_tables) {
     rt.cs = at<float2>(ws, L.ropea);
     rt.dst = at<long long>(ws, L.dsta);
     rt.d = d;
@@ -301,7 +304,25 @@ int run_append(const dflash2_config& c, const dflash2_weights& w, void* kc, void
     rt.n_pages = n_pages;
     rt.nkv = nkv;
   }
-  TRY(launch_rows_feature_norm(c.dtype, Y, n_new, H, w.hidden_norm, c.rms_eps, f, rt, rest));
+  TRY(launch_rows_feature_norm(c.dtype, Y, n_new, H, w.hidden_norm, c.rms_eps, at<char>(ws, L.f), rt, rest));
+  if (rest_out) *rest_out = rest;
+  return DFLASH2_OK;
+}
+
+// Stage (a), whole: features, then every layer's context K/V of the appended
+// rows into the paged cache (a contraction per layer, K/V epilogue fused when
+// its shape allows).
+int run_append(const dflash2_config& c, const dflash2_weights& w, void* kc, void* vc, int n_pages,
+               const int32_t* block_table, int max_pages, int batch, const int32_t* ctx_len, int n_new,
+               const void* taps, const int32_t* new_off, void* ws, const Layout& L, const Ctx& ctx) {
+  if (n_new == 0) return DFLASH2_OK;
+  const int H = c.hidden, nq = c.n_q_heads, nkv = c.n_kv_heads, d = c.head_dim;
+  float* Y = at<float>(ws, L.Ya);
+  void* f = at<char>(ws, L.f);
+  const bool fused_kv = c.dtype == DFLASH2_BF16 && gemm_fusable(2 * nkv * d, n_new, kEpiHeads);
+  Ctx rest;
+  TRY(project_features(c, w, n_pages, block_table, max_pages, batch, ctx_len, n_new, taps, new_off, ws, L, fused_kv,
+                       ctx, &rest));
   const size_t layer_elems = (size_t)n_pages * c.page_size * nkv * d;
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash2_layer_weights& Lw = w.layers[l];
@@ -316,9 +337,9 @@ int run_append(const dflash2_config& c, const dflash2_weights& w, void* kc, void
       g.n_kh = nkv;
       g.kn = Lw.k_norm;
       g.eps = c.rms_eps;
-      g.rope = at<float2>(ws, L.ropea);
+      g.nblk = 0;
+      g.rope_app = at<float2>(ws, L.ropea);
       g.dst = at<long long>(ws, L.dsta);
-      g.append = 1;
       g.kc = kcl;
       g.vc = vcl;
       TRY(gemm_fused(g, rest, ws, L, true));
@@ -433,30 +454,48 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
   Ctx ctx;
   TRY(device_ctx(&ctx, stream, workspace));
 
-  // Stage (a) does not feed the block until its attention: run it on the
-  // device's side stream, forked from and joined back into the caller's
-  // stream (event edges, so graph capture records two parallel branches).
-  std::lock_guard<std::mutex> side_lock(g_side_mu);
+  const int H = c.hidden, B = c.block_size, D = B - 1, nq = c.n_q_heads, nkv = c.n_kv_heads, d = c.head_dim;
+  const int I = c.intermediate, G = H / c.conv_group_size, rows = batch * B;
+  // Stage (a) runs on the device's side stream, forked from and joined back
+  // into the caller's stream (event edges, so graph capture records two
+  // parallel branches), in one of two arrangements:
+  //  separate: the side stream runs the feature projection and every
+  //    layer's K/V contraction and joins before the first attention, so with
+  //    one layer the K/V work overlaps the block's own QKV contraction
+  //    (measured faster at one layer: the join stays late);
+  //  merged: with several layers, when the QKV contraction can take the
+  //    appended rows as extra activation columns (u2a and f are adjacent),
+  //    the side stream runs the feature projection only and joins before
+  //    layer 0's QKV contraction, and each layer's QKV contraction also
+  //    projects the appended rows' k/v into the cache (W_k and W_v read once
+  //    per layer instead of twice).
+  const int qkvM = (nq + 2 * nkv) * d;
+  const bool merged =
+      c.n_layers > 1 && c.dtype == DFLASH2_BF16 && gemm_fusable(qkvM, rows + n_new, kEpiHeads);
+  std::unique_lock<std::mutex> side_lock(g_side_mu, std::defer_lock);
   SideStream side;
-  TRY(side_stream(&side));
   const bool forked = n_new > 0;
   TRY(stage_event(0, ctx.stream));
   if (forked) {
+    side_lock.lock();
+    TRY(side_stream(&side));
     if (cudaEventRecord(side.fork, ctx.stream) != cudaSuccess || cudaStreamWaitEvent(side.s, side.fork, 0) != cudaSuccess)
       return DFLASH2_ERR_CUDA;
     Ctx actx = ctx;
     actx.stream = side.s;
     actx.pdl = false;  // full dependency on the fork event
-    TRY(run_append(c, *w, k_cache, v_cache, n_pages, block_table, max_pages, batch, ctx_len, n_new, new_taps,
-                   new_off, workspace, L, actx));
+    if (merged)
+      TRY(project_features(c, *w, n_pages, block_table, max_pages, batch, ctx_len, n_new, new_taps, new_off,
+                           workspace, L, true, actx, nullptr));
+    else
+      TRY(run_append(c, *w, k_cache, v_cache, n_pages, block_table, max_pages, batch, ctx_len, n_new, new_taps,
+                     new_off, workspace, L, actx));
     TRY(stage_event(1, side.s));
     if (cudaEventRecord(side.join, side.s) != cudaSuccess) return DFLASH2_ERR_CUDA;
   } else {
     TRY(stage_event(1, ctx.stream));
   }
 
-  const int H = c.hidden, B = c.block_size, D = B - 1, nq = c.n_q_heads, nkv = c.n_kv_heads, d = c.head_dim;
-  const int I = c.intermediate, G = H / c.conv_group_size, rows = batch * B;
   float* Y = at<float>(workspace, L.Y);
   float* h = at<float>(workspace, L.h);
   void* u = at<char>(workspace, L.u);    // MLP sublayer: normed input
@@ -475,7 +514,7 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
   // sublayer prologues: one fused kernel (norm, tap logits, conv) when the
   // sequence's B rows fit its shared memory, else norm + tap GEMM + conv
   const bool fused = conv_prologue_fits(c.dtype, batch, B, H, G, ctx.nsm);
-  const bool fused_qkv = c.dtype == DFLASH2_BF16 && gemm_fusable((nq + 2 * nkv) * d, rows, kEpiHeads);
+  const bool fused_qkv = merged || (c.dtype == DFLASH2_BF16 && gemm_fusable(qkvM, rows, kEpiHeads));
   RopeTab rt;  // the block rows' RoPE angles, left by the first kernel for the fused QKV epilogues
   std::memset(&rt, 0, sizeof(rt));
   if (fused_qkv) {
@@ -493,6 +532,7 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
   else
     TRY(launch_embed_norm(c.dtype, anchor, c.mask_token_id, batch, B, w->embed, c.vocab, H, c.input_embedding_scale,
                           w->layers[0].attn_norm, c.rms_eps, h, ua, rt, ctx));
+  const int n_app = merged ? n_new : 0;  // appended rows the QKV contractions carry
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash2_layer_weights& Lw = w->layers[l];
     // attention sublayer: conv around the normed input, QKV, attention, O (+= residual)
@@ -505,9 +545,17 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
       TRY(gemm(c, ctx, ws, L, Lw.tapgen_attn, 2 * G, H, ua, rows, Y, false));
       TRY(launch_dyn_conv(c.dtype, ua, Y, rows, H, c.conv_group_size, B, u2a, ctx));
     }
+    // merged: the QKV contraction reads the appended rows' features, a full
+    // dependency on the join
+    Ctx qctx = ctx;
+    if (forked && merged && l == 0) {
+      if (cudaStreamWaitEvent(ctx.stream, side.join, 0) != cudaSuccess) return DFLASH2_ERR_CUDA;
+      qctx.pdl = false;
+    }
     if (fused_qkv) {
-      // q/k-norm + RoPE fused into the QKV epilogue
-      GemmOp g = gemm_op(Lw.qkv, (nq + 2 * nkv) * d, H, u2a, rows);
+      // q/k-norm + RoPE fused into the QKV epilogue; merged: the appended rows'
+      // features ride along as extra columns and their k/v go to the cache
+      GemmOp g = gemm_op(Lw.qkv, qkvM, H, u2a, rows + n_app);
       g.epi = kEpiHeads;
       g.hd = d;
       g.n_qh = nq;
@@ -515,19 +563,26 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
       g.qn = Lw.q_norm;
       g.kn = Lw.k_norm;
       g.eps = c.rms_eps;
+      g.nblk = rows;
       g.rope = at<float2>(ws, L.rope);
       g.q = q;
       g.kb = kb;
       g.vb = vb;
-      TRY(gemm_fused(g, ctx, ws, L, false));
+      if (n_app > 0) {
+        g.rope_app = at<float2>(ws, L.ropea);
+        g.dst = at<long long>(ws, L.dsta);
+        g.kc = const_cast<char*>(elem_ptr(k_cache, l * layer_elems, c.dtype));
+        g.vc = const_cast<char*>(elem_ptr(v_cache, l * layer_elems, c.dtype));
+      }
+      TRY(gemm_fused(g, qctx, ws, L, false));
     } else {
       TRY(gemm(c, ctx, ws, L, Lw.qkv, (nq + 2 * nkv) * d, H, u2a, rows, Y, false));
       TRY(launch_qkv_epilogue(c.dtype, Y, rows, B, nq, nkv, d, Lw.q_norm, Lw.k_norm, c.rms_eps, c.rope_theta,
                               ctx_len, new_off, q, kb, vb, ctx));
     }
-    // the attention reads the appended K/V: a full dependency on the join
+    // separate: the attention reads the appended K/V, a full dependency on the join
     Ctx jctx = ctx;
-    if (forked && l == 0) {
+    if (forked && !merged && l == 0) {
       if (cudaStreamWaitEvent(ctx.stream, side.join, 0) != cudaSuccess) return DFLASH2_ERR_CUDA;
       jctx.pdl = false;
     }

@@ -89,10 +89,14 @@ struct TcArgs {
   const bf16* qn;  // [hd] q-norm gain (n_qh > 0)
   const bf16* kn;  // [hd] k-norm gain
   float eps;
-  const float2* rope;    // [N][hd/2] (cos, sin) at each column's position
-  const long long* dst;  // appended rows: [N] element offset of the row in the paged cache, -1: skip
-  int append;
-  bf16 *q, *kb, *vb;  // block rows: [N][heads][hd]
+  // Columns n < nblk are block rows (outputs q/kb/vb [n][heads][hd]); columns
+  // n >= nblk are appended context rows (k and v to the paged cache; their q
+  // heads are not needed and not stored).
+  int nblk;
+  const float2* rope;      // [nblk][hd/2] (cos, sin) at each block column's position
+  const float2* rope_app;  // [N - nblk][hd/2] the same for appended columns
+  const long long* dst;    // [N - nblk] element offset of an appended row in the paged cache, -1: skip
+  bf16 *q, *kb, *vb;  // block rows: [nblk][heads][hd]
   bf16 *kc, *vc;      // appended rows: paged cache [pages][page_size][n_kh][hd]
 };
 
@@ -316,6 +320,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     }
+    __syncwarp();  // lanes 1..31 wait here for the producer lane: the warp reaches the final barrier whole
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -360,6 +365,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       volatile int never = 0;
       mbar_wait(drain, 0, &never, WAIT_NS);
     }
+    __syncwarp();  // as for the producer warp
   } else {
     // ------------------------------------------------------------ epilogue
     pdl_wait();  // outputs, partials and counters may still be in use by the previous kernel
@@ -419,7 +425,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         // All loads of a step are issued before its stores, so they overlap
         // instead of queueing.  The fused epilogues synchronise the four
         // epilogue warps; every call site is uniform across them.
-        auto finish = [&](float(&v)[16], int c0) {
+        // (pre_old: the old output values when the caller already loaded them)
+        auto finish = [&](float(&v)[16], int c0, const float* pre_old) {
           const int nb = nt * BN + c0;       // first column
           const int nj = min(16, a.N - nb);  // valid columns (may be <= 0)
           if constexpr (EPI == EPI_PLAIN) {
@@ -428,7 +435,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               if (a.accumulate) {
                 float old[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) old[j] = j < nj ? p0[(size_t)j * a.M] : 0.f;
+                for (int j = 0; j < 16; ++j) old[j] = pre_old ? pre_old[j] : (j < nj ? p0[(size_t)j * a.M] : 0.f);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) v[j] = old[j] + v[j];
               }
@@ -480,14 +487,17 @@ __global__ void __launch_bounds__(THREADS, 1)
               stg[j * BM + row] = x[j];
             }
             named_sync_epi();
-            // RoPE: rotate-half pairs (di, di + d/2), angles from the table
+            // RoPE: rotate-half pairs (di, di + d/2), angles from the tables
             if (kind < 2 && valid) {
               const int half = d / 2, ip = di % half;
               const float sgn = di < half ? -1.f : 1.f;
               float2 cs[16];
 #pragma unroll
               for (int j = 0; j < 16; ++j)
-                if (j < nj) cs[j] = a.rope[(size_t)(nb + j) * half + ip];
+                if (j < nj) {
+                  const int n = nb + j;
+                  cs[j] = n < a.nblk ? a.rope[(size_t)n * half + ip] : a.rope_app[(size_t)(n - a.nblk) * half + ip];
+                }
 #pragma unroll
               for (int j = 0; j < 16; ++j)
                 if (j < nj) x[j] = x[j] * cs[j].x + sgn * (stg[j * BM + (row ^ half)] * cs[j].y);
@@ -498,12 +508,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (j >= nj) continue;
                 const bf16 val = __float2bfloat16_rn(x[j]);
                 const size_t n = (size_t)(nb + j);
-                if (!a.append) {
+                if ((int)n < a.nblk) {
                   if (kind == 0) a.q[(n * a.n_qh + hg) * d + di] = val;
                   else if (kind == 1) a.kb[(n * a.n_kh + (hg - a.n_qh)) * d + di] = val;
                   else a.vb[(n * a.n_kh + (hg - a.n_qh - a.n_kh)) * d + di] = val;
-                } else {
-                  const long long dj = a.dst[nb + j];
+                } else if (kind > 0) {
+                  const long long dj = a.dst[n - a.nblk];
                   if (dj >= 0) {
                     if (kind == 1) a.kc[dj + (size_t)(hg - a.n_qh) * d + di] = val;
                     else if (kind == 2) a.vc[dj + (size_t)(hg - a.n_qh - a.n_kh) * d + di] = val;
@@ -522,26 +532,38 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) pc[(c0 + j) * BM + row] = v[j];
           } else {
-            finish(v, c0);
+            finish(v, c0, nullptr);
           }
         }
         tc_fence_before();
         mbar_arrive(tempty + acc);
         if (!direct) {
-          __threadfence();
+          // the piece is written; one thread publishes it (the barrier orders the
+          // other threads' stores before its cumulative fence) and counts it
           named_sync_epi();
-          if (threadIdx.x == 64)
-            *last_flag = (atomicAdd(a.counters + g_first, 1) == g_last - g_first) ? 1 : 0;
+          if (threadIdx.x == 64) {
+            __threadfence();
+            const bool last = atomicAdd(a.counters + g_first, 1) == g_last - g_first;
+            if (last) __threadfence();  // acquire: the other pieces are visible to the CTA after the barrier
+            *last_flag = last ? 1 : 0;
+          }
           named_sync_epi();
           if (*last_flag) {
-            __threadfence();
             // sum the pieces in CTA order, 16 columns at a time
 #pragma unroll 1
             for (int c0 = 0; c0 < BN && nt * BN + c0 < a.N; c0 += 16) {
-              float sum[16];
+              float sum[16], old[16];
 #pragma unroll
               for (int j = 0; j < 16; ++j) sum[j] = 0.f;
-              constexpr int PB = 4;  // pieces per round of loads
+              // the old output values load in the same round as the pieces
+              const bool pre = EPI == EPI_PLAIN && a.accumulate && m < a.M;
+              if (pre) {
+                const int nj = min(16, a.N - (nt * BN + c0));
+                const float* p0 = a.out + (size_t)(nt * BN + c0) * a.M + m;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) old[j] = j < nj ? p0[(size_t)j * a.M] : 0.f;
+              }
+              constexpr int PB = EPI == EPI_HEADS ? 4 : 8;  // pieces per round of loads (registers)
               for (int g0 = g_first; g0 <= g_last; g0 += PB) {
                 float v[PB][16];
 #pragma unroll
@@ -558,7 +580,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int j = 0; j < 16; ++j) sum[j] += v[q2][j];
                   }
               }
-              finish(sum, c0);
+              finish(sum, c0, pre ? old : nullptr);
             }
             if (threadIdx.x == 64) a.counters[g_first] = 0;
           }
@@ -787,19 +809,20 @@ int gemm_bf16(const GemmOp& g, const Ctx& c) {
     a.I = g.M / 2;
   } else if (epi == EPI_HEADS) {
     if (g.hd * (g.n_qh + 2 * g.n_kh) != g.M || (g.hd != 64 && g.hd != BM) || !g.kn || (g.n_qh > 0 && !g.qn) ||
-        !g.rope)
+        g.nblk < 0 || g.nblk > g.N)
       return DFLASH2_ERR_INVALID_ARG;
-    if (g.append ? (!g.kc || !g.vc || !g.dst || g.n_qh != 0) : (!g.q || !g.kb || !g.vb))
-      return DFLASH2_ERR_INVALID_ARG;
+    if (g.nblk > 0 && (!g.rope || !g.q || !g.kb || !g.vb || g.n_qh == 0)) return DFLASH2_ERR_INVALID_ARG;
+    if (g.nblk < g.N && (!g.rope_app || !g.dst || !g.kc || !g.vc)) return DFLASH2_ERR_INVALID_ARG;
     a.hd = g.hd;
     a.n_qh = g.n_qh;
     a.n_kh = g.n_kh;
     a.qn = static_cast<const bf16*>(g.qn);
     a.kn = static_cast<const bf16*>(g.kn);
     a.eps = g.eps;
+    a.nblk = g.nblk;
     a.rope = g.rope;
+    a.rope_app = g.rope_app;
     a.dst = g.dst;
-    a.append = g.append;
     a.q = static_cast<bf16*>(g.q);
     a.kb = static_cast<bf16*>(g.kb);
     a.vb = static_cast<bf16*>(g.vb);

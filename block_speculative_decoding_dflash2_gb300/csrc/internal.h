@@ -50,9 +50,10 @@ struct GemmOp {
   const void* qn;
   const void* kn;
   float eps;
-  const float2* rope;    // [N][hd/2] (cos, sin) per column (RopeTab::cs)
-  const long long* dst;  // appended rows: [N] paged-cache offsets (RopeTab::dst)
-  int append;
+  int nblk;                // columns [0, nblk): block rows -> q/kb/vb; [nblk, N): appended rows -> cache
+  const float2* rope;      // [nblk][hd/2] (cos, sin) per block column (RopeTab::cs)
+  const float2* rope_app;  // [N - nblk][hd/2] per appended column
+  const long long* dst;    // [N - nblk] paged-cache offsets of the appended rows (RopeTab::dst)
   void *q, *kb, *vb, *kc, *vc;
 };
 constexpr int kEpiSwiglu = 2, kEpiHeads = 3;

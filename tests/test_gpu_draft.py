@@ -63,9 +63,10 @@ def test_fp32_rows_beyond_fused_prologue():
 
 def test_small_bf16_wide_batch():
     # 10 sequences x 8 block rows: activation tiles wider than the fused
-    # epilogues take, so the block's q/k/v and SiLU*up run as separate kernels
-    # (the appended rows still take the fused K/V epilogue)
-    cfg = S.small_bf16_config(index=19)
+    # epilogues take, so the block's q/k/v and SiLU*up run as separate
+    # kernels and stage (a) runs forked on the side stream (its K/V
+    # contraction still takes the fused paged-store epilogue)
+    cfg = S.small_bf16_config(n_q_heads=8, index=19)
     ctx = [5, 17, 40, 0, 64, 3, 31, 90, 12, 8]
     case = Case(cfg, ctx_lens=ctx, n_new=[1, 2, 8, 3, 0, 5, 1, 4, 2, 6], seed=19).run_gpu()
     check_case(case)

@@ -90,6 +90,12 @@ def lib():
         L.dflash2_select_path_static.restype = I
         L.dflash2_select_path_static.argtypes = [F(Config), F(Weights), I, P, P, P, P, P, P]
         L.dflash2_select_path_static_capacity.restype = S
+        L.dflash2_selector_table_bytes.restype = S
+        L.dflash2_selector_table_bytes.argtypes = [F(Config)]
+        L.dflash2_build_selector_table.restype = I
+        L.dflash2_build_selector_table.argtypes = [F(Config), F(Weights), P, P]
+        L.dflash2_select_path_table.restype = I
+        L.dflash2_select_path_table.argtypes = [F(Config), I, P, P, P, P, P, P, P, P]
         L.dflash2_test_layout.restype = I
         L.dflash2_test_layout.argtypes = [F(Config), I, I, I, F(ctypes.c_size_t), I]
         L.dflash2_launch_count.restype = ctypes.c_int64
@@ -193,6 +199,22 @@ def dflash2_select_path(cfg, w, batch, anchor, cand_id, cand_logit, path, path_s
         workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
+def dflash2_selector_table_bytes(cfg):
+    return lib().dflash2_selector_table_bytes(ctypes.byref(cfg))
+
+
+def dflash2_build_selector_table(cfg, w, table, stream=None):
+    return _check("dflash2_build_selector_table", lib().dflash2_build_selector_table(
+        ctypes.byref(cfg), ctypes.byref(w.struct), _ptr(table), _stream(stream)))
+
+
+def dflash2_select_path_table(cfg, batch, anchor, cand_id, cand_logit, table, path, path_score,
+                              workspace=None, stream=None):
+    return _check("dflash2_select_path_table", lib().dflash2_select_path_table(
+        ctypes.byref(cfg), batch, _ptr(anchor), _ptr(cand_id), _ptr(cand_logit), _ptr(table), _ptr(path),
+        _ptr(path_score), _ptr(workspace), _stream(stream)))
+
+
 def dflash2_verify_accept(batch, block_size, path, target, accept_len, out_tok, n_out, next_anchor,
                           seq_len=None, counters=None, stream=None):
     return _check("dflash2_verify_accept", lib().dflash2_verify_accept(
@@ -253,13 +275,18 @@ def dflash2_launch_count():
 
 
 def dflash2_set_stage_events(events):
-    """events: None, or 5 torch.cuda.Event(enable_timing=True) already recorded once."""
+    """events: None, or 5 torch.cuda.Event(enable_timing=True) already recorded once.
+
+    Returns a holder that the caller keeps alive for as long as the library
+    (or a graph captured while the events were set) may record into them."""
     if events is None:
         lib().dflash2_set_stage_events(None)
         return None
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     lib().dflash2_set_stage_events(ctypes.cast(arr, ctypes.c_void_p))
-    return arr
+    # a graph captured with these events records into them at every replay:
+    # the holder keeps the event objects (not only their handles) alive
+    return (arr, tuple(events))
 
 
 def dflash2_select_path_static(cfg, w, batch, anchor, cand_id, cand_logit, path, path_score, stream=None):

@@ -475,6 +475,13 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
   std::unique_lock<std::mutex> side_lock(g_side_mu, std::defer_lock);
   SideStream side;
   const bool forked = n_new > 0;
+  // The fused embedding prologue is latency-bound and the feature
+  // contraction bandwidth-bound, and neither fits an SM beside the other: a
+  // forked step splits the SMs, kForkPrologueSMs for the prologue (on fewer,
+  // wider CTAs) and the rest for the contraction, so the two overlap.
+  const bool fused = conv_prologue_fits(c.dtype, batch, B, H, G, ctx.nsm);
+  const bool split_sms = forked && fused && ctx.nsm > 2 * kForkPrologueSMs &&
+                         conv_prologue_fits(c.dtype, batch, B, H, G, kForkPrologueSMs / 2);
   TRY(stage_event(0, ctx.stream));
   if (forked) {
     side_lock.lock();
@@ -484,6 +491,7 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
     Ctx actx = ctx;
     actx.stream = side.s;
     actx.pdl = false;  // full dependency on the fork event
+    if (split_sms) actx.nsm = ctx.nsm - kForkPrologueSMs;
     if (merged)
       TRY(project_features(c, *w, n_pages, block_table, max_pages, batch, ctx_len, n_new, new_taps, new_off,
                            workspace, L, true, actx, nullptr));
@@ -513,7 +521,6 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
 
   // sublayer prologues: one fused kernel (norm, tap logits, conv) when the
   // sequence's B rows fit its shared memory, else norm + tap GEMM + conv
-  const bool fused = conv_prologue_fits(c.dtype, batch, B, H, G, ctx.nsm);
   const bool fused_qkv = merged || (c.dtype == DFLASH2_BF16 && gemm_fusable(qkvM, rows, kEpiHeads));
   RopeTab rt;  // the block rows' RoPE angles, left by the first kernel for the fused QKV epilogues
   std::memset(&rt, 0, sizeof(rt));
@@ -525,10 +532,13 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
     rt.new_off = new_off;
     rt.batch = batch;
   }
-  if (fused)
+  if (fused) {
+    Ctx ectx = ctx;
+    if (split_sms) ectx.nsm = kForkPrologueSMs / 2;  // the prologue sizes its grid at two CTAs per SM
     TRY(launch_conv_prologue(c.dtype, nullptr, anchor, c.mask_token_id, w->embed, c.vocab, c.input_embedding_scale,
                              w->layers[0].attn_norm, c.rms_eps, w->layers[0].tapgen_attn, batch, B, H,
-                             c.conv_group_size, h, ua, u2a, rt, ctx));
+                             c.conv_group_size, h, ua, u2a, rt, ectx));
+  }
   else
     TRY(launch_embed_norm(c.dtype, anchor, c.mask_token_id, batch, B, w->embed, c.vocab, H, c.input_embedding_scale,
                           w->layers[0].attn_norm, c.rms_eps, h, ua, rt, ctx));
@@ -666,7 +676,40 @@ int dflash2_select_path(const dflash2_config* cfg, const dflash2_weights* w, int
   float* Y = at<float>(workspace, L.Y);
   TRY(launch_sel_gather(c.dtype, anchor, cand_id, batch, D, k, w->embed, c.vocab, H, x, ctx));
   TRY(gemm(c, ctx, workspace, L, w->sel, 2 * r, H, x, batch * (D * k + 1), Y, false));
-  return launch_viterbi(Y, cand_id, cand_logit, batch, D, k, r, path, path_score, ctx);
+  return launch_viterbi(Y, nullptr, anchor, c.vocab, cand_id, cand_logit, batch, D, k, r, path, path_score, ctx);
+}
+
+size_t dflash2_selector_table_bytes(const dflash2_config* cfg) {
+  if (check_config(cfg) != DFLASH2_OK) return 0;
+  return (size_t)cfg->vocab * 2 * cfg->selector_rank * sizeof(float);
+}
+
+int dflash2_build_selector_table(const dflash2_config* cfg, const dflash2_weights* w, float* table, void* stream) {
+  TRY(check_config(cfg));
+  if (!w || !w->embed || !w->sel || !table) return DFLASH2_ERR_INVALID_ARG;
+  Ctx ctx;
+  TRY(device_ctx(&ctx, stream, nullptr));
+  const dflash2_config& c = *cfg;
+  // table[v][m] = sum_h sel[m][h] E[v][h]: the selector contraction with the
+  // whole vocabulary as its activation rows (whole tiles: no workspace)
+  GemmOp g = gemm_op(w->sel, 2 * c.selector_rank, c.hidden, w->embed, c.vocab);
+  g.out = table;
+  g.ctas = -1;
+  if (c.dtype == DFLASH2_BF16) return gemm_bf16(g, ctx);
+  return gemm_f32(g, ctx);
+}
+
+int dflash2_select_path_table(const dflash2_config* cfg, int batch, const int32_t* anchor, const int32_t* cand_id,
+                              const float* cand_logit, const float* table, int32_t* path, float* path_score,
+                              void* workspace, void* stream) {
+  TRY(check_config(cfg));
+  if (batch <= 0) return DFLASH2_ERR_SHAPE;
+  if (!anchor || !cand_id || !cand_logit || !table || !path) return DFLASH2_ERR_INVALID_ARG;
+  Ctx ctx;
+  TRY(device_ctx(&ctx, stream, workspace));
+  const dflash2_config& c = *cfg;
+  return launch_viterbi(nullptr, table, anchor, c.vocab, cand_id, cand_logit, batch, c.block_size - 1, c.top_k,
+                        c.selector_rank, path, path_score, ctx);
 }
 
 int dflash2_verify_accept(int batch, int block_size, const int32_t* path, const int32_t* target,

@@ -69,6 +69,9 @@ int gemm_topk_lists(int M, int N, int K, int nsm, int dtype);
 // Upper bound of the above over every SM count this library accepts.
 int gemm_max_lists();
 constexpr int kMaxSM = 256;  // CTAs of a stream-K launch, and its counter array length
+// SMs left to the fused embedding prologue while the side stream's feature
+// contraction runs beside it (the contraction takes the rest).
+constexpr int kForkPrologueSMs = 32;
 
 // Host-side count of kernel launches (instrumentation).
 void count_launch(int n = 1);
@@ -194,8 +197,11 @@ int launch_topk_merge(const float* lists_v, const int* lists_i, int n_lists, int
 // selector and verify (selector.cu, verify.cu)
 int launch_sel_gather(int dtype, const int32_t* anchor, const int32_t* cand_id, int batch, int D, int k,
                       const void* embed, int V, int H, void* x_out, const Ctx& c);
-int launch_viterbi(const float* Y, const int32_t* cand_id, const float* cand_logit, int batch, int D, int k, int r,
-                   int32_t* path, float* path_score, const Ctx& c);
+// Y: per-step factors [batch][D*k+1][2r]; or Y null and table [V][2r]
+// (factors of every token, gathered by the kernel).
+int launch_viterbi(const float* Y, const float* table, const int32_t* anchor, int V, const int32_t* cand_id,
+                   const float* cand_logit, int batch, int D, int k, int r, int32_t* path, float* path_score,
+                   const Ctx& c);
 size_t viterbi_smem_bytes(int D, int k, int r);
 int launch_verify(int batch, int B, const int32_t* path, const int32_t* target, int32_t* accept_len,
                   int32_t* out_tok, int32_t* n_out, int32_t* next_anchor, int32_t* seq_len, int64_t* counters,

@@ -115,8 +115,8 @@ int dflash2_select_path_static(const dflash2_config* cfg, const dflash2_weights*
   g.mult = 1.f;
   rc = c.dtype == DFLASH2_BF16 ? gemm_bf16(g, ctx) : gemm_f32(g, ctx);
   if (rc) return rc;
-  return launch_viterbi(reinterpret_cast<const float*>(base + o_y), cand_id, cand_logit, batch, D, k, r, path,
-                        path_score, ctx);
+  return launch_viterbi(reinterpret_cast<const float*>(base + o_y), nullptr, anchor, c.vocab, cand_id, cand_logit,
+                        batch, D, k, r, path, path_score, ctx);
 }
 
 }  // extern "C"

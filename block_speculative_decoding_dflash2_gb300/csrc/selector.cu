@@ -16,7 +16,10 @@
 // contraction runs on the same GEMM as the rest of the step; viterbi_kernel
 // (one CTA per sequence) stages that sequence's factors, logits and
 // candidate ids in shared memory and runs the k x k dynamic programme over
-// the B-1 positions without touching global memory again.
+// the B-1 positions without touching global memory again.  With a factor
+// table (the factors of every vocabulary token, built once), the kernel
+// gathers the rows of its tokens itself and the gather and contraction
+// launches drop out.
 #include <climits>
 
 #include "common.cuh"
@@ -49,11 +52,16 @@ __global__ void __launch_bounds__(256) sel_gather_kernel(const int32_t* __restri
   for (int m = threadIdx.x; m < H / PER; m += blockDim.x) dst[m] = tok < 0 ? make_uint4(0, 0, 0, 0) : src[m];
 }
 
-__global__ void __launch_bounds__(512) viterbi_kernel(const float* __restrict__ Y,
+// Factors: Y [batch][nt][2r] rows in [anchor, candidates] order, or (Y
+// null) rows of `table` [V][2r] at those tokens.
+__global__ void __launch_bounds__(512) viterbi_kernel(const float* __restrict__ Y, const float* __restrict__ table,
+                                                      const int32_t* __restrict__ anchor, int V,
                                                       const int32_t* __restrict__ cand_id,
                                                       const float* __restrict__ cand_logit, int D, int k, int r,
-                                                      int32_t* __restrict__ path, float* __restrict__ path_score) {
+                                                      int32_t* __restrict__ path, float* __restrict__ path_score,
+                                                      unsigned* status) {
   extern __shared__ __align__(16) float sm[];
+  __shared__ int tok0;
   pdl_launch_next();
   pdl_wait();
   const int s = blockIdx.x;
@@ -68,9 +76,54 @@ __global__ void __launch_bounds__(512) viterbi_kernel(const float* __restrict__ 
   int* cid = reinterpret_cast<int*>(nd + k);   // [D][k] candidate ids
   int* bp = cid + D * k;                       // [D][k] back pointers
 
+  for (int idx = threadIdx.x; idx < D * k; idx += blockDim.x) {
+    zs[idx] = cand_logit[(size_t)s * D * k + idx];
+    cid[idx] = cand_id[(size_t)s * D * k + idx];
+  }
   // stage the factors: U vector loads in flight per thread
   constexpr int U = 8;
-  if ((w & 3) == 0) {
+  if (!Y) {
+    if (threadIdx.x == 0) tok0 = anchor[s];
+    __syncthreads();
+    // row t of the sequence's lattice: the anchor, then candidate t-1
+    auto row_of = [&](int t) -> const float* {
+      const int tok = t == 0 ? tok0 : cid[t - 1];
+      if (tok < 0 || tok >= V) {
+        flag(status, DFLASH2_DEV_BAD_TOKEN);
+        return nullptr;
+      }
+      return table + (size_t)tok * w;
+    };
+    if ((w & 3) == 0) {
+      const int w4 = w / 4, n4 = nt * w4;
+      for (int base = threadIdx.x; base < n4; base += blockDim.x * U) {
+        float4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int idx = base + u * blockDim.x;
+          if (idx < n4) {
+            const int t = idx / w4;
+            const float* src = row_of(t);
+            v[u] = src ? reinterpret_cast<const float4*>(src)[idx - t * w4] : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int idx = base + u * blockDim.x;
+          if (idx < n4) {
+            const int t = idx / w4;
+            *reinterpret_cast<float4*>(F + t * ws + (idx - t * w4) * 4) = v[u];
+          }
+        }
+      }
+    } else {
+      for (int idx = threadIdx.x; idx < nt * w; idx += blockDim.x) {
+        const int t = idx / w;
+        const float* src = row_of(t);
+        F[t * ws + idx - t * w] = src ? src[idx - t * w] : 0.f;
+      }
+    }
+  } else if ((w & 3) == 0) {
     const float4* y = reinterpret_cast<const float4*>(Y + (size_t)s * nt * w);
     const int w4 = w / 4, n4 = nt * w4;
     for (int base = threadIdx.x; base < n4; base += blockDim.x * U) {
@@ -109,10 +162,6 @@ __global__ void __launch_bounds__(512) viterbi_kernel(const float* __restrict__ 
         }
       }
     }
-  }
-  for (int idx = threadIdx.x; idx < D * k; idx += blockDim.x) {
-    zs[idx] = cand_logit[(size_t)s * D * k + idx];
-    cid[idx] = cand_id[(size_t)s * D * k + idx];
   }
   __syncthreads();
   auto dot = [&](int ta, int tb) {  // <A[ta], Bf[tb]>: four partial sums, combined pairwise
@@ -218,8 +267,10 @@ int launch_sel_gather(int dtype, const int32_t* anchor, const int32_t* cand_id, 
                   static_cast<const float*>(embed), V, H, static_cast<float*>(x_out), c.status);
 }
 
-int launch_viterbi(const float* Y, const int32_t* cand_id, const float* cand_logit, int batch, int D, int k, int r,
-                   int32_t* path, float* path_score, const Ctx& c) {
+int launch_viterbi(const float* Y, const float* table, const int32_t* anchor, int V, const int32_t* cand_id,
+                   const float* cand_logit, int batch, int D, int k, int r, int32_t* path, float* path_score,
+                   const Ctx& c) {
+  if ((Y == nullptr) == (table == nullptr)) return DFLASH2_ERR_INVALID_ARG;
   const size_t smem = viterbi_smem_bytes(D, k, r);
   static bool attr = false;
   if (!attr) {
@@ -227,8 +278,8 @@ int launch_viterbi(const float* Y, const int32_t* cand_id, const float* cand_log
       return DFLASH2_ERR_CUDA;
     attr = true;
   }
-  return launch_k(viterbi_kernel, dim3(batch), dim3(512), smem, c, Y, cand_id, cand_logit, D, k, r, path,
-                  path_score);
+  return launch_k(viterbi_kernel, dim3(batch), dim3(512), smem, c, Y, table, anchor, V, cand_id, cand_logit, D, k, r,
+                  path, path_score, c.status);
 }
 
 }  // namespace df2

@@ -6,9 +6,9 @@
 // The lm_head GEMM (tcgen05 path) already leaves one sorted list of KMAX
 // entries per CTA and row.  topk_scan_kernel produces the same lists from
 // stored logits (fp32 path).  topk_merge_kernel reduces the lists of a row:
-// the 16th best list head bounds the answer from below, and one warp picks
-// the top k of the entries it does not beat, so the result does not depend
-// on how the vocabulary was split.
+// the 16th best list head bounds the answer from below, and the top k of the
+// entries it does not beat are found by counting ranks, so the result does
+// not depend on how the vocabulary was split.
 #include <algorithm>
 #include <climits>
 
@@ -56,35 +56,42 @@ __global__ void __launch_bounds__(128) topk_scan_kernel(const float* __restrict_
   }
 }
 
-// Top KMAX of `n` candidates (v[i], id[i]) in shared memory by one warp: a
-// sorted list in lanes 0..15, offered only the candidates that beat its last
-// entry (one ballot per 32 candidates).  Returns the list in (lv, li).
-__device__ __forceinline__ void warp_topk(const float* v, const int* id, int n, float& lv, int& li, float& tv,
-                                          int& ti) {
-  const int lane = threadIdx.x & 31;
-  lv = -INFINITY;
-  li = INT_MAX;
-  tv = -INFINITY;
-  ti = INT_MAX;
-  for (int base = 0; base < n; base += 32) {
-    const int i = base + lane;
-    const float x = i < n ? v[i] : -INFINITY;
-    const int xi = i < n ? id[i] : INT_MAX;
-    unsigned mask = __ballot_sync(0xffffffffu, i < n && beats(x, xi, tv, ti));
-    while (mask) {
-      const int src = __ffs(mask) - 1;
-      mask &= mask - 1;
-      warp_list_offer(lv, li, tv, ti, __shfl_sync(0xffffffffu, x, src), __shfl_sync(0xffffffffu, xi, src));
-    }
+// 64-bit key of a candidate: a larger key is a better candidate under the
+// (value descending, id ascending) order, so one integer compare replaces
+// the two-field one.  Value bits are mapped to an unsigned order (negative
+// zero first folded onto zero, which compares equal to it).
+__device__ __forceinline__ unsigned long long order_key(float v, int id) {
+  unsigned u = __float_as_uint(v + 0.f);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)u << 32) | (unsigned)(0x7fffffff - id);
+}
+
+__device__ __forceinline__ float key_value(unsigned long long key) {
+  const unsigned u = (unsigned)(key >> 32);
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
+}
+__device__ __forceinline__ int key_id(unsigned long long key) { return 0x7fffffff - (int)(unsigned)key; }
+
+// Rank of key x at slot sx among keys[0..n): the keys above it, plus the
+// equal ones (padding entries) at smaller slots.
+__device__ __forceinline__ int rank_of(const unsigned long long* keys, int n, unsigned long long x, int sx) {
+  int rank = 0;
+#pragma unroll 8
+  for (int m = 0; m < n; ++m) {
+    const unsigned long long y = keys[m];
+    rank += (y > x) | ((y == x) & (m < sx));
   }
+  return rank;
 }
 
 // One CTA per row.  The row's n_lists sorted lists are staged in shared
-// memory in one round of loads.  The 16th best list head tau bounds the
-// answer from below (16 distinct entries are at least tau), so only entries
-// that tau does not beat can be in the top KMAX; those survivors are
-// collected and one warp picks the top k of them.  The result is the exact
-// top k under the strict (value, id) order, whatever the vocabulary split.
+// memory in one round of loads.  The KMAX-th best list head tau bounds the
+// answer from below (KMAX distinct entries are at least tau), so only
+// entries that tau does not beat can be in the top KMAX.  Both selections
+// are rank counts over 64-bit order keys (a thread per element counts the
+// elements above it): tau is the head of rank KMAX-1, and a survivor of rank
+// q < k is output q.  The result is the exact top k under the strict
+// (value, id) order, whatever the vocabulary split.
 // dynamic shared memory: 2 * n_lists * KMAX * 8 bytes.
 constexpr int MT = 512;  // threads of the merge kernel
 
@@ -92,17 +99,15 @@ __global__ void __launch_bounds__(MT) topk_merge_kernel(const float* __restrict_
                                                         const int* __restrict__ lists_i, int n_lists, int rows,
                                                         int k, int32_t* __restrict__ cand_id,
                                                         float* __restrict__ cand_logit) {
-  extern __shared__ float mv[];
-  __shared__ float tau_v;
-  __shared__ int tau_i, n_surv;
+  extern __shared__ __align__(16) unsigned long long mk[];  // [total] keys of the list entries
+  __shared__ unsigned long long hk[256];                     // keys of the list heads
+  __shared__ unsigned long long tau;
+  __shared__ int n_surv;
   pdl_launch_next();
   pdl_wait();
   const int total = n_lists * KMAX;
-  int* mi = reinterpret_cast<int*>(mv + total);
-  float* sv = reinterpret_cast<float*>(mi + total);
-  int* si = reinterpret_cast<int*>(sv + total);
+  unsigned long long* sk = mk + total;                     // [total] survivor keys
   const int row = blockIdx.x;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   constexpr int U = 8;  // loads in flight per thread (n_lists <= 256: one round)
   for (int base = threadIdx.x; base < total; base += MT * U) {
     float v[U];
@@ -120,50 +125,43 @@ __global__ void __launch_bounds__(MT) topk_merge_kernel(const float* __restrict_
     for (int u = 0; u < U; ++u) {
       const int idx = base + u * MT;
       if (idx < total) {
-        mv[idx] = v[u];
-        mi[idx] = id[u];
+        const unsigned long long key = order_key(v[u], id[u]);
+        mk[idx] = key;
+        if (idx % KMAX == 0) hk[idx / KMAX] = key;
       }
     }
   }
-  if (threadIdx.x == 0) n_surv = 0;
-  __syncthreads();
-  // tau: the KMAX-th best list head (heads are list entries 0, stride KMAX)
-  if (warp == 0) {
-    float lv, tv;
-    int li, ti;
-    // stage the heads contiguously in the survivor buffer, then select
-    for (int l = lane; l < n_lists; l += 32) {
-      sv[l] = mv[l * KMAX];
-      si[l] = mi[l * KMAX];
-    }
-    __syncwarp();
-    warp_topk(sv, si, n_lists, lv, li, tv, ti);
-    if (lane == 0) {
-      tau_v = n_lists >= KMAX ? tv : -INFINITY;
-      tau_i = n_lists >= KMAX ? ti : INT_MAX;
-    }
+  if (threadIdx.x == 0) {
+    n_surv = 0;
+    tau = 0;  // fewer than KMAX lists: every entry survives
   }
   __syncthreads();
-  // survivors: entries that tau does not beat
-  const float tv0 = tau_v;
-  const int ti0 = tau_i;
+  // tau: the list head of rank KMAX-1
+  if (n_lists >= KMAX)
+    for (int l = threadIdx.x; l < n_lists; l += MT)
+      if (rank_of(hk, n_lists, hk[l], l) == KMAX - 1) tau = hk[l];
+  __syncthreads();
+  // survivors: entries whose key is at least tau's
+  const unsigned long long t0 = tau;
   for (int idx = threadIdx.x; idx < total; idx += MT) {
-    const float v = mv[idx];
-    const int id = mi[idx];
-    if (!beats(tv0, ti0, v, id)) {
-      const int p = atomicAdd(&n_surv, 1);
-      sv[p] = v;
-      si[p] = id;
+    const unsigned long long key = mk[idx];
+    if (key >= t0) {
+      sk[atomicAdd(&n_surv, 1)] = key;
     }
   }
   __syncthreads();
-  if (warp == 0) {
-    float lv, tv;
-    int li, ti;
-    warp_topk(sv, si, n_surv, lv, li, tv, ti);
-    if (lane < k) {
-      cand_id[(size_t)row * k + lane] = li == INT_MAX ? -1 : li;
-      cand_logit[(size_t)row * k + lane] = lv;
+  const int ns = n_surv;
+  for (int q = ns + threadIdx.x; q < k; q += MT) {  // fewer survivors than k (tiny vocabularies)
+    cand_id[(size_t)row * k + q] = -1;
+    cand_logit[(size_t)row * k + q] = -INFINITY;
+  }
+  for (int i = threadIdx.x; i < ns; i += MT) {
+    const unsigned long long key = sk[i];
+    const int rank = rank_of(sk, ns, key, i);
+    if (rank < k) {
+      const int id = key_id(key);
+      cand_id[(size_t)row * k + rank] = id == INT_MAX ? -1 : id;
+      cand_logit[(size_t)row * k + rank] = key_value(key);
     }
   }
 }
@@ -184,7 +182,7 @@ int launch_topk_scan(const float* logits, int rows, int V, float mult, float cap
 int launch_topk_merge(const float* lists_v, const int* lists_i, int n_lists, int rows, int k, int32_t* cand_id,
                       float* cand_logit, const Ctx& c) {
   if (n_lists < 1 || n_lists > 256 || k > KMAX) return DFLASH2_ERR_SHAPE;
-  const size_t smem = 2 * (size_t)n_lists * KMAX * 8;  // lists and survivors, <= 64 KB
+  const size_t smem = 2 * (size_t)n_lists * KMAX * 8;  // entry and survivor keys, <= 64 KB
   static bool attr = false;  // set once, before any capture
   if (!attr) {
     if (cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024) !=

@@ -45,12 +45,16 @@ class DraftRunner:
         i32 = dict(dtype=torch.int32, device=device)
         self.cand_id = torch.zeros((batch, D, k), **i32)
         self.cand_logit = torch.zeros((batch, D, k), dtype=torch.float32, device=device)
-        self.path = torch.zeros((batch, D), **i32)
+        # the step's int32 results share one buffer (`results`), so a caller
+        # reads them back to the host in one copy
+        self.results = torch.zeros((batch * (2 * D + 4),), **i32)
+        parts = torch.split(self.results, [batch * D, batch, batch * (D + 1), batch, batch])
+        self.path = parts[0].view(batch, D)
+        self.accept_len = parts[1]
+        self.out_tok = parts[2].view(batch, D + 1)
+        self.n_out = parts[3]
+        self.next_anchor = parts[4]
         self.path_score = torch.zeros((batch,), dtype=torch.float32, device=device)
-        self.accept_len = torch.zeros((batch,), **i32)
-        self.out_tok = torch.zeros((batch, D + 1), **i32)
-        self.n_out = torch.zeros((batch,), **i32)
-        self.next_anchor = torch.zeros((batch,), **i32)
         self.counters = torch.zeros((4 + 2 * (D + 1) - 1,), dtype=torch.int64, device=device)
 
     def append(self, ctx_len, taps, new_off, stream=None):
@@ -65,9 +69,20 @@ class DraftRunner:
                              self.max_pages, self.batch, ctx_len, n_new, taps, new_off, anchor, self.cand_id,
                              self.cand_logit, debug_logits, self.workspace, stream)
 
+    def build_selector_table(self, stream=None):
+        """Factors of every vocabulary token (built once; select() then looks
+        its rows up instead of contracting per step)."""
+        n = B.dflash2_selector_table_bytes(self.cfg) // 4
+        self.sel_table = torch.empty((n,), dtype=torch.float32, device=self.device)
+        B.dflash2_build_selector_table(self.cfg, self.w, self.sel_table, stream)
+
     def select(self, anchor, stream=None):
-        B.dflash2_select_path(self.cfg, self.w, self.batch, anchor, self.cand_id, self.cand_logit, self.path,
-                              self.path_score, self.workspace, stream)
+        if getattr(self, "sel_table", None) is not None:
+            B.dflash2_select_path_table(self.cfg, self.batch, anchor, self.cand_id, self.cand_logit,
+                                        self.sel_table, self.path, self.path_score, self.workspace, stream)
+        else:
+            B.dflash2_select_path(self.cfg, self.w, self.batch, anchor, self.cand_id, self.cand_logit,
+                                  self.path, self.path_score, self.workspace, stream)
 
     def verify(self, target, seq_len=None, stream=None):
         B.dflash2_verify_accept(self.batch, self.cfgd["block_size"], self.path, target, self.accept_len,

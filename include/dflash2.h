@@ -270,6 +270,40 @@ int dflash2_select_path_static(const dflash2_config *cfg, const dflash2_weights 
 size_t dflash2_select_path_static_capacity(void);
 
 /*
+ * The selector's factors of a token depend on nothing but the frozen
+ * embedding and W_sel, so they can be computed once for the whole
+ * vocabulary and looked up at every step instead of gathered and
+ * contracted per step.  The table is
+ *   table[v][0:r]  = W_a E[v],   table[v][r:2r] = W_b E[v]     (fp32)
+ * for v = 0..vocab-1, row-major [vocab, 2r] (selector_rank = r), computed
+ * with the same contraction (cfg.dtype inputs, fp32 accumulation) the
+ * per-step selector uses.
+ *
+ * dflash2_selector_table_bytes: bytes of the table (vocab * 2r * 4), 0 for
+ *   an invalid config.  Host only.
+ * dflash2_build_selector_table: fills `table` (device, caller-owned,
+ *   16-byte aligned) on `stream`; rebuild it whenever embed or sel change.
+ *   Needs no workspace.  Returns DFLASH2_OK, DFLASH2_ERR_INVALID_ARG (null
+ *   config, weights or table), a config error, or DFLASH2_ERR_CUDA.
+ */
+size_t dflash2_selector_table_bytes(const dflash2_config *cfg);
+int dflash2_build_selector_table(const dflash2_config *cfg, const dflash2_weights *w, float *table,
+                                 void *stream);
+
+/*
+ * dflash2_select_path on a factor table from dflash2_build_selector_table:
+ * same definition, outputs, tie rules and status codes, in one kernel per
+ * call (one CTA per sequence).  The factors of each sequence's anchor and
+ * candidates are rows of `table`; a token outside [0, vocab) gets zero
+ * factors and, when `workspace` is given, sets DFLASH2_DEV_BAD_TOKEN in its
+ * device status word (dflash2_read_device_status).  `workspace` is nullable:
+ * the call needs no scratch.
+ */
+int dflash2_select_path_table(const dflash2_config *cfg, int batch, const int32_t *anchor,
+                              const int32_t *cand_id, const float *cand_logit, const float *table,
+                              int32_t *path, float *path_score, void *workspace, void *stream);
+
+/*
  * Stage (d2): greedy verification ("Prerequisites": the target verifies
  * [id_last, draft...] in one batch; "Validation": output token ids equal
  * plain greedy decoding).

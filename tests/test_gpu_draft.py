@@ -117,8 +117,9 @@ def test_device_guards_flag_bad_page_and_token():
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("name", ["tiny_fp32", "small_bf16"])
-def test_lossless_speculative_loop(name):
+@pytest.mark.parametrize("name,kind", [("tiny_fp32", "gemm"), ("small_bf16", "gemm"), ("small_bf16", "table"),
+                                       ("tiny_fp32", "table")])
+def test_lossless_speculative_loop(name, kind):
     """Draft -> select -> verify on the GPU against a toy greedy target: the
     emitted tokens equal plain greedy decoding, and every step's path equals
     the oracle's on the same candidates."""
@@ -135,6 +136,8 @@ def test_lossless_speculative_loop(name):
     Wv = S.values_of(W)
     taps = S.make_taps(cfg, prompt + n_tok + Bsz + 2, stream="loop")   # row = position
     r = DraftRunner(cfg, S.device_weights(W), 1, prompt + n_tok + 2 * Bsz, max_new=prompt)
+    if kind == "table":
+        r.build_selector_table()
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(np.asarray(a, dtype=np.int32))).cuda()
     tt = S.to_torch(taps)
     r.append(dev([0]), tt[:prompt].contiguous(), dev([0, prompt]))

@@ -1,5 +1,6 @@
-"""Parity of the selector (factor gather + GEMM + Viterbi) and of greedy
-verify/accept/rollback with the oracle, on identical inputs."""
+"""Parity of the selector (factor gather + GEMM + Viterbi, or the per-token
+factor table + Viterbi) and of greedy verify/accept/rollback with the oracle,
+on identical inputs."""
 
 import numpy as np
 import pytest
@@ -20,7 +21,7 @@ def sel_cfg(dtype, V, H, k, D, r):
                 final_logit_softcap=0.0)
 
 
-def run_select(dtype, V, H, k, D, r, b, seed, emb_std=1.0, sel_std=0.3, logit_std=1.0):
+def run_select(dtype, V, H, k, D, r, b, seed, emb_std=1.0, sel_std=0.3, logit_std=1.0, kind="gemm"):
     import torch
     B = lib()
     cfg = sel_cfg(dtype, V, H, k, D, r)
@@ -37,12 +38,19 @@ def run_select(dtype, V, H, k, D, r, b, seed, emb_std=1.0, sel_std=0.3, logit_st
     ws = torch.zeros(B.dflash2_workspace_size(c, b, 0, 16), dtype=torch.uint8, device="cuda")
     path = torch.full((b, D), -5, dtype=torch.int32, device="cuda")
     score = torch.zeros(b, dtype=torch.float32, device="cuda")
-    B.dflash2_select_path(c, w, b, dev(anchor), dev(cand.astype(np.int32)), dev(z), path, score, ws)
+    if kind == "table":
+        table = torch.empty(B.dflash2_selector_table_bytes(c) // 4, dtype=torch.float32, device="cuda")
+        B.dflash2_build_selector_table(c, w, table)
+        B.dflash2_select_path_table(c, b, dev(anchor), dev(cand.astype(np.int32)), dev(z), table, path, score, ws)
+    else:
+        B.dflash2_select_path(c, w, b, dev(anchor), dev(cand.astype(np.int32)), dev(z), path, score, ws)
     torch.cuda.synchronize()
+    assert B.dflash2_read_device_status(ws) == 0
     Wo = {"embed": E.values, "sel": Wsel.values}
     return cfg, Wo, anchor, cand, z, path.cpu().numpy(), score.cpu().numpy()
 
 
+@pytest.mark.parametrize("kind", ["gemm", "table"])
 @pytest.mark.parametrize("dtype,V,H,k,D,r,b", [
     ("bf16", 4096, 256, 16, 7, 64, 4),
     ("bf16", 2000, 128, 4, 7, 16, 3),
@@ -50,8 +58,8 @@ def run_select(dtype, V, H, k, D, r, b, seed, emb_std=1.0, sel_std=0.3, logit_st
     ("bf16", 5000, 512, 16, 15, 64, 2),
     ("f32", 4096, 256, 4, 7, 16, 3),
 ])
-def test_selector_matches_oracle_viterbi(dtype, V, H, k, D, r, b):
-    cfg, W, anchor, cand, z, path, score = run_select(dtype, V, H, k, D, r, b, seed=V + k)
+def test_selector_matches_oracle_viterbi(dtype, V, H, k, D, r, b, kind):
+    cfg, W, anchor, cand, z, path, score = run_select(dtype, V, H, k, D, r, b, seed=V + k, kind=kind)
     near = 0
     for s in range(b):
         p, idx, sc = O.select_path(cfg, W, int(anchor[s]), cand[s], z[s].astype(np.float64))
@@ -65,10 +73,11 @@ def test_selector_matches_oracle_viterbi(dtype, V, H, k, D, r, b):
     assert near <= max(1, b // 4)
 
 
-def test_selector_pairwise_term_matters_and_brute_force():
+@pytest.mark.parametrize("kind", ["gemm", "table"])
+def test_selector_pairwise_term_matters_and_brute_force(kind):
     # strong factors so paths leave the per-position argmax; k=4, D=7 brute force
     cfg, W, anchor, cand, z, path, score = run_select("bf16", 1000, 128, 4, 7, 16, 6, seed=3,
-                                                      emb_std=3.0, sel_std=1.0, logit_std=0.5)
+                                                      emb_std=3.0, sel_std=1.0, logit_std=0.5, kind=kind)
     moved = 0
     for s in range(6):
         pb, idxb, sb = O.brute_force_path(cfg, W, int(anchor[s]), cand[s], z[s].astype(np.float64))
@@ -78,10 +87,63 @@ def test_selector_pairwise_term_matters_and_brute_force():
     assert moved > 0
 
 
-def test_selector_without_pairwise_term_is_top1():
-    import torch
-    cfg, W, anchor, cand, z, path, score = run_select("bf16", 1000, 128, 8, 7, 16, 3, seed=4, sel_std=0.0)
+@pytest.mark.parametrize("kind", ["gemm", "table"])
+def test_selector_without_pairwise_term_is_top1(kind):
+    cfg, W, anchor, cand, z, path, score = run_select("bf16", 1000, 128, 8, 7, 16, 3, seed=4, sel_std=0.0,
+                                                      kind=kind)
     np.testing.assert_array_equal(path, cand[:, :, 0])
+
+
+@pytest.mark.parametrize("dtype,V,H,r", [("bf16", 151936, 4096, 64), ("bf16", 1000, 128, 16),
+                                         ("f32", 4096, 256, 16)])
+def test_selector_table_rows_are_the_factors(dtype, V, H, r):
+    """Sampled rows of the table against the oracle's factors of those tokens
+    (W_a E[v], W_b E[v] in float64), every row's finiteness, and the ragged
+    last tile of the vocabulary."""
+    import torch
+    B = lib()
+    cfg = sel_cfg(dtype, V, H, 4, 7, r)
+    E = S._draw(7, "E", (V, H), 1.0 / np.sqrt(H), dtype)
+    Wsel = S._draw(7, "sel", (2 * r, H), 0.3, dtype)
+    w = B.WeightSet({"embed": S.to_torch(E), "sel": S.to_torch(Wsel), "lm_head": None, "fc": None,
+                     "hidden_norm": None, "final_norm": None, "layers": []})
+    c = B.make_config(cfg)
+    n = B.dflash2_selector_table_bytes(c) // 4
+    assert n == V * 2 * r
+    table = torch.full((n,), float("nan"), dtype=torch.float32, device="cuda")
+    B.dflash2_build_selector_table(c, w, table)
+    t = table.view(V, 2 * r).cpu().numpy()
+    assert np.all(np.isfinite(t))
+    rows = np.unique(np.concatenate([np.random.default_rng(1).integers(0, V, 64), [0, V - 1, V - 2]]))
+    A, Bf = O.selector_factors(cfg, {"embed": E.values, "sel": Wsel.values}, rows)
+    ref = np.concatenate([A, Bf], axis=1)
+    tol = 1e-4 if dtype == "f32" else 2e-3
+    np.testing.assert_allclose(t[rows], ref, atol=tol, rtol=0)
+
+
+def test_selector_table_flags_bad_tokens():
+    import torch
+    B = lib()
+    V, H, k, D, r, b = 1000, 128, 4, 7, 16, 2
+    cfg = sel_cfg("bf16", V, H, k, D, r)
+    E = S._draw(9, "E", (V, H), 1.0 / np.sqrt(H), "bf16")
+    Wsel = S._draw(9, "sel", (2 * r, H), 0.3, "bf16")
+    w = B.WeightSet({"embed": S.to_torch(E), "sel": S.to_torch(Wsel), "lm_head": None, "fc": None,
+                     "hidden_norm": None, "final_norm": None, "layers": []})
+    c = B.make_config(cfg)
+    table = torch.empty(B.dflash2_selector_table_bytes(c) // 4, dtype=torch.float32, device="cuda")
+    B.dflash2_build_selector_table(c, w, table)
+    ws = torch.zeros(B.dflash2_workspace_size(c, b, 0, 16), dtype=torch.uint8, device="cuda")
+    cand = torch.arange(b * D * k, dtype=torch.int32, device="cuda").reshape(b, D, k)
+    z = torch.zeros((b, D, k), dtype=torch.float32, device="cuda")
+    anchor = torch.tensor([3, V + 7], dtype=torch.int32, device="cuda")
+    path = torch.zeros((b, D), dtype=torch.int32, device="cuda")
+    B.dflash2_select_path_table(c, b, anchor, cand, z, table, path, None, ws)
+    torch.cuda.synchronize()
+    assert B.dflash2_read_device_status(ws) & B.DEV_BAD_TOKEN
+    # without a workspace the call still runs (no status word to flag)
+    B.dflash2_select_path_table(c, b, anchor, cand, z, table, path, None, None)
+    torch.cuda.synchronize()
 
 
 def _verify(paths, targets, B_, seq_len=None, counters=None):

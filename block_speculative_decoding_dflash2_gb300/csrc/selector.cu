@@ -71,9 +71,7 @@ __global__ void __launch_bounds__(512) viterbi_kernel(const float* __restrict__ 
   float* F = sm;                               // [nt][ws] factors: A = F[t][0:r], Bf = F[t][r:2r]
   float* zs = F + (size_t)nt * ws;             // [D][k] candidate logits
   float* Sm = zs + D * k;                      // [1 + (D-1)k][k] transition log-probabilities
-  float* delta = Sm + (1 + (D - 1) * k) * k;   // [k]
-  float* nd = delta + k;                       // [k]
-  int* cid = reinterpret_cast<int*>(nd + k);   // [D][k] candidate ids
+  int* cid = reinterpret_cast<int*>(Sm + (1 + (D - 1) * k) * k);  // [D][k] candidate ids
   int* bp = cid + D * k;                       // [D][k] back pointers
 
   for (int idx = threadIdx.x; idx < D * k; idx += blockDim.x) {
@@ -164,36 +162,75 @@ __global__ void __launch_bounds__(512) viterbi_kernel(const float* __restrict__ 
     }
   }
   __syncthreads();
-  auto dot = [&](int ta, int tb) {  // <A[ta], Bf[tb]>: four partial sums, combined pairwise
-    const float* a = F + (size_t)ta * ws;
-    const float* b = F + (size_t)tb * ws + r;
-    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-    if ((r & 3) == 0) {
-#pragma unroll 4
-      for (int c = 0; c < r; c += 4) {
-        const float4 x = *reinterpret_cast<const float4*>(a + c), y = *reinterpret_cast<const float4*>(b + c);
-        acc0 = fmaf(x.x, y.x, acc0);
-        acc1 = fmaf(x.y, y.y, acc1);
-        acc2 = fmaf(x.z, y.z, acc2);
-        acc3 = fmaf(x.w, y.w, acc3);
-      }
-    } else {
-      for (int c = 0; c < r; ++c) acc0 = fmaf(a[c], b[c], acc0);
-    }
-    return (acc0 + acc1) + (acc2 + acc3);
-  };
   // 1. every transition score at once (they do not depend on the DP): row 0 is
   //    position 1 after the anchor; row 1 + (i-1)k + p is position i+1 after
-  //    candidate p of position i
+  //    candidate p of position i.  A thread computes a 4 x 4 tile (4
+  //    predecessors x 4 candidates of one position): each factor it loads
+  //    serves 4 products, which keeps the shared-memory traffic at a quarter
+  //    of one dot product per score.
   const int nrow = 1 + (D - 1) * k;
-  for (int idx = threadIdx.x; idx < nrow * k; idx += blockDim.x) {
-    const int row = idx / k, j = idx - row * k;
-    if (row == 0) {
-      Sm[idx] = zs[j] + dot(0, 1 + j);
+  const int k4 = (k + 3) / 4;
+  const int n_tiles = k4 + (D - 1) * k4 * k4;
+  for (int tile = threadIdx.x; tile < n_tiles; tile += blockDim.x) {
+    int i, p0, j0, np;
+    if (tile < k4) {  // position 1: the anchor is the only predecessor
+      i = 0;
+      p0 = 0;
+      np = 1;
+      j0 = 4 * tile;
     } else {
-      const int i = 1 + (row - 1) / k, p = (row - 1) % k;
-      Sm[idx] = zs[i * k + j] + dot(1 + (i - 1) * k + p, 1 + i * k + j);
+      const int t = tile - k4;
+      i = 1 + t / (k4 * k4);
+      const int rem = t % (k4 * k4);
+      p0 = 4 * (rem / k4);
+      j0 = 4 * (rem % k4);
+      np = min(4, k - p0);
     }
+    const int nj = min(4, k - j0);
+    const float* arow[4];
+    const float* brow[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const int p = p0 + min(a, np - 1), j = j0 + min(a, nj - 1);  // clamped: spare lanes recompute an edge
+      arow[a] = F + (size_t)(i == 0 ? 0 : 1 + (i - 1) * k + p) * ws;
+      brow[a] = F + (size_t)(1 + i * k + j) * ws + r;
+    }
+    float acc[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+    if ((r & 3) == 0) {
+      for (int c = 0; c < r; c += 4) {
+        float4 x[4], y[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          x[a] = *reinterpret_cast<const float4*>(arow[a] + c);
+          y[a] = *reinterpret_cast<const float4*>(brow[a] + c);
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            acc[a][b] = fmaf(x[a].x, y[b].x, acc[a][b]);
+            acc[a][b] = fmaf(x[a].y, y[b].y, acc[a][b]);
+            acc[a][b] = fmaf(x[a].z, y[b].z, acc[a][b]);
+            acc[a][b] = fmaf(x[a].w, y[b].w, acc[a][b]);
+          }
+      }
+    } else {
+      for (int c = 0; c < r; ++c)
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(arow[a][c], brow[b][c], acc[a][b]);
+    }
+    const int row0 = i == 0 ? 0 : 1 + (i - 1) * k + p0;
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        if (a < np && b < nj) Sm[(row0 + a) * k + j0 + b] = zs[i * k + j0 + b] + acc[a][b];
   }
   __syncthreads();
   // 2. each row -> log-probabilities (one half-warp per row, lane j of the
@@ -214,36 +251,45 @@ __global__ void __launch_bounds__(512) viterbi_kernel(const float* __restrict__ 
     }
   }
   __syncthreads();
-  // 3. the max-plus recurrence over positions
-  for (int j = threadIdx.x; j < k; j += blockDim.x) delta[j] = Sm[j];
-  __syncthreads();
-  for (int i = 1; i < D; ++i) {
-    const float* T = Sm + (1 + (i - 1) * k) * k;  // [p][j]
-    for (int j = threadIdx.x; j < k; j += blockDim.x) {
-      float best = delta[0] + T[j];
+  // 3. the max-plus recurrence over positions and the backtrack, in one warp:
+  //    lane j holds delta[j]; ties keep the smaller predecessor (strict >,
+  //    predecessors in ascending order) and, at the end, the smaller index
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    float dl = lane < k ? Sm[lane] : -INFINITY;
+    for (int i = 1; i < D; ++i) {
+      const float* T = Sm + (1 + (i - 1) * k) * k;  // [p][j]
+      float best = -INFINITY;
       int arg = 0;
-      for (int p = 1; p < k; ++p) {
-        const float v = delta[p] + T[p * k + j];
+      for (int p = 0; p < k; ++p) {
+        const float v = __shfl_sync(0xffffffffu, dl, p) + (lane < k ? T[p * k + lane] : 0.f);
         if (v > best) {
           best = v;
           arg = p;
         }
       }
-      nd[j] = best;
-      bp[i * k + j] = arg;
+      if (lane < k) {
+        dl = best;
+        bp[i * k + lane] = arg;
+      }
     }
-    __syncthreads();
-    for (int j = threadIdx.x; j < k; j += blockDim.x) delta[j] = nd[j];
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) {
-    int j = 0;
-    for (int jj = 1; jj < k; ++jj)
-      if (delta[jj] > delta[j]) j = jj;
-    if (path_score) path_score[s] = delta[j];
-    for (int i = D - 1; i >= 0; --i) {
-      path[(size_t)s * D + i] = cid[i * k + j];
-      if (i > 0) j = bp[i * k + j];
+    __syncwarp();
+    int jb = 0;
+    float vb = __shfl_sync(0xffffffffu, dl, 0);
+    for (int jj = 1; jj < k; ++jj) {
+      const float v = __shfl_sync(0xffffffffu, dl, jj);
+      if (v > vb) {
+        vb = v;
+        jb = jj;
+      }
+    }
+    if (lane == 0) {
+      if (path_score) path_score[s] = vb;
+      int j = jb;
+      for (int i = D - 1; i >= 0; --i) {
+        path[(size_t)s * D + i] = cid[i * k + j];
+        if (i > 0) j = bp[i * k + j];
+      }
     }
   }
 }
@@ -252,8 +298,7 @@ __global__ void __launch_bounds__(512) viterbi_kernel(const float* __restrict__ 
 
 size_t viterbi_smem_bytes(int D, int k, int r) {
   const size_t ws = (r & 3) == 0 ? 2 * r + 4 : 2 * r + 1;
-  return sizeof(float) * ((size_t)(D * k + 1) * ws + (size_t)D * k + (size_t)(1 + (D - 1) * k) * k +
-                          2 * (size_t)k) +
+  return sizeof(float) * ((size_t)(D * k + 1) * ws + (size_t)D * k + (size_t)(1 + (D - 1) * k) * k) +
          sizeof(int) * 2 * (size_t)D * k;
 }
 

@@ -73,22 +73,22 @@ __device__ __forceinline__ float key_value(unsigned long long key) {
 __device__ __forceinline__ int key_id(unsigned long long key) { return 0x7fffffff - (int)(unsigned)key; }
 
 // Rank of key x at slot sx among keys[0..n): the keys above it, plus the
-// equal ones (padding entries) at smaller slots.
-__device__ __forceinline__ int rank_of(const unsigned long long* keys, int n, unsigned long long x, int sx) {
+// equal ones (padding entries) at smaller slots.  One warp: lanes split the
+// keys and the counts are summed across the warp.
+__device__ __forceinline__ int warp_rank_of(const unsigned long long* keys, int n, unsigned long long x, int sx) {
   int rank = 0;
-#pragma unroll 8
-  for (int m = 0; m < n; ++m) {
+  for (int m = threadIdx.x & 31; m < n; m += 32) {
     const unsigned long long y = keys[m];
     rank += (y > x) | ((y == x) & (m < sx));
   }
-  return rank;
+  return __reduce_add_sync(0xffffffffu, rank);
 }
 
 // One CTA per row.  The row's n_lists sorted lists are staged in shared
 // memory in one round of loads.  The KMAX-th best list head tau bounds the
 // answer from below (KMAX distinct entries are at least tau), so only
 // entries that tau does not beat can be in the top KMAX.  Both selections
-// are rank counts over 64-bit order keys (a thread per element counts the
+// are rank counts over 64-bit order keys (a warp per element counts the
 // elements above it): tau is the head of rank KMAX-1, and a survivor of rank
 // q < k is output q.  The result is the exact top k under the strict
 // (value, id) order, whatever the vocabulary split.
@@ -136,10 +136,12 @@ __global__ void __launch_bounds__(MT) topk_merge_kernel(const float* __restrict_
     tau = 0;  // fewer than KMAX lists: every entry survives
   }
   __syncthreads();
-  // tau: the list head of rank KMAX-1
+  // tau: the list head of rank KMAX-1 (a warp per head)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int NW = MT / 32;
   if (n_lists >= KMAX)
-    for (int l = threadIdx.x; l < n_lists; l += MT)
-      if (rank_of(hk, n_lists, hk[l], l) == KMAX - 1) tau = hk[l];
+    for (int l = warp; l < n_lists; l += NW)
+      if (warp_rank_of(hk, n_lists, hk[l], l) == KMAX - 1 && lane == 0) tau = hk[l];
   __syncthreads();
   // survivors: entries whose key is at least tau's
   const unsigned long long t0 = tau;
@@ -155,10 +157,10 @@ __global__ void __launch_bounds__(MT) topk_merge_kernel(const float* __restrict_
     cand_id[(size_t)row * k + q] = -1;
     cand_logit[(size_t)row * k + q] = -INFINITY;
   }
-  for (int i = threadIdx.x; i < ns; i += MT) {
+  for (int i = warp; i < ns; i += NW) {
     const unsigned long long key = sk[i];
-    const int rank = rank_of(sk, ns, key, i);
-    if (rank < k) {
+    const int rank = warp_rank_of(sk, ns, key, i);
+    if (rank < k && lane == 0) {
       const int id = key_id(key);
       cand_id[(size_t)row * k + rank] = id == INT_MAX ? -1 : id;
       cand_logit[(size_t)row * k + rank] = key_value(key);

@@ -8,7 +8,10 @@ Kernels:
             (vocab 151936 x hidden 4096 bf16, 7 block rows, top-16) through
             the dflash2_test_gemm_topk hook, then the top-k merge;
   gate_up   the MLP gate/up contraction (24576 x 4096, 8 rows);
-  fc, qkv, down, o   the other contractions of the 8B-shaped draft step.
+  fc, qkv, down, o   the other contractions of the 8B-shaped draft step;
+  select    the selector on a factor table (vocab 151936, rank 64, 7
+            positions x top-16, one sequence) through
+            dflash2_select_path_table.
 Weights are seeded N(0, 0.02) bf16 drawn on the device (timing only; no
 parity is checked here).  L2 is flushed (a 256 MiB write) before every
 launch; prints the mean CUDA-event time per launch.
@@ -27,12 +30,14 @@ SHAPES = {"lm_head": (151936, 4096, 7), "gate_up": (24576, 4096, 8), "fc": (4096
 
 def main():
     p = argparse.ArgumentParser()
-    p.add_argument("--kernel", default="lm_head", choices=sorted(SHAPES))
+    p.add_argument("--kernel", default="lm_head", choices=sorted(SHAPES) + ["select"])
     p.add_argument("--launches", type=int, default=3)
     p.add_argument("--ctas", type=int, default=0,
                    help="contraction schedule: 0 = the library's, >0 = stream-K over that many CTAs, <0 = whole tiles")
     a = p.parse_args()
     build()
+    if a.kernel == "select":
+        return bench_select(a)
     M, K, N = SHAPES[a.kernel]
     g = torch.Generator(device="cuda")
     g.manual_seed(1234)
@@ -63,6 +68,33 @@ def main():
     gb = M * K * 2 / 1e9
     print(f"{a.kernel}: M={M} K={K} N={N} ctas={a.ctas}: {ms * 1e3:.1f} us per call, "
           f"{gb / (ms / 1e3):.0f} GB/s of weights")
+
+
+def bench_select(a):
+    V, r, D, k = 151936, 64, 7, 16
+    cfg = B.make_config(dict(hidden=4096, n_q_heads=32, n_kv_heads=8, head_dim=128, intermediate=12288, vocab=V,
+                             n_layers=1, n_taps=3, block_size=D + 1, conv_kernel_size=2, conv_group_size=32,
+                             top_k=k, selector_rank=r, page_size=16, mask_token_id=V - 1, dtype="bf16",
+                             rms_eps=1e-6, rope_theta=1e6, input_embedding_scale=1.0, output_multiplier=1.0,
+                             final_logit_softcap=0.0))
+    g = torch.Generator(device="cuda")
+    g.manual_seed(99)
+    table = torch.randn((V * 2 * r,), generator=g, device="cuda") * 0.1
+    cand = torch.randint(0, V - 1, (1, D, k), generator=g, device="cuda", dtype=torch.int32)
+    z = torch.sort(torch.randn((1, D, k), generator=g, device="cuda"), dim=2, descending=True).values
+    anchor = torch.randint(0, V - 1, (1,), generator=g, device="cuda", dtype=torch.int32)
+    path = torch.empty((1, D), dtype=torch.int32, device="cuda")
+    score = torch.empty((1,), dtype=torch.float32, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    run = lambda: B.dflash2_select_path_table(cfg, 1, anchor, cand, z, table, path, score)
+    run()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(a.launches):
+        run()
+    e1.record()
+    e1.synchronize()
+    print(f"select: {e0.elapsed_time(e1) * 1e3 / a.launches:.1f} us per call (back to back)")
 
 
 if __name__ == "__main__":

@@ -88,20 +88,21 @@ class Case:
         self.status = r.device_status()
         return self
 
-    def oracle_logits(self):
+    def oracle_logits(self, seqs=None):
+        """The oracle's logits of every sequence, or of the sampled `seqs`
+        (sequences are independent: each is computed from its own rows)."""
         cfg = self.cfg
         st = O.Store(cfg["dtype"] == "bf16")
+        pre = np.concatenate([[0], np.cumsum(self.ctx_lens)])
+        new = np.concatenate([[0], np.cumsum(self.n_new)])
         out = []
-        p0 = 0
-        n0 = 0
-        for s in range(self.b):
+        for s in (range(self.b) if seqs is None else seqs):
             L, n = int(self.ctx_lens[s]), int(self.n_new[s])
+            p0, n0 = int(pre[s]), int(new[s])
             ctx = empty_ctx(cfg)
             if L:
                 ctx = O.append_context(cfg, self.Wv, ctx, self.taps_pre.values[p0:p0 + L], 0, st)
             if n:
                 ctx = O.append_context(cfg, self.Wv, ctx, self.taps_new.values[n0:n0 + n], L, st)
             out.append(O.draft_block(cfg, self.Wv, int(self.anchor[s]), ctx, st))
-            p0 += L
-            n0 += n
         return np.stack(out)

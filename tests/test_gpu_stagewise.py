@@ -30,11 +30,18 @@ def ulps(gpu, ref):
     return np.abs(gpu - ref) / np.exp2(e - 7)
 
 
-def check_ulps(name, gpu, ref, max_ulp, frac_over_1=0.01):
+def check_ulps(name, gpu, ref, max_ulp, frac_over_1=0.01, slack=None):
+    """At most max_ulp everywhere (or, where `slack` is given, an absolute
+    error within slack plus one ulp), and at most frac_over_1 of the
+    elements beyond 1 ulp."""
     u = ulps(gpu, ref)
     over = float(np.mean(u > 1.0 + 1e-9))
-    print(f"[stage] {name:8s} max {u.max():.2f} ulp, >1ulp {over:.2e}, n={u.size}")
-    assert u.max() <= max_ulp, (name, float(u.max()))
+    bad = u > max_ulp
+    if slack is not None:
+        ulp_ref = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 7)
+        bad &= np.abs(gpu - ref) > slack + ulp_ref
+    print(f"[stage] {name:8s} max {u.max():.2f} ulp, >1ulp {over:.2e}, beyond bound {int(bad.sum())}, n={u.size}")
+    assert not bad.any(), (name, float(u.max()))
     assert over <= frac_over_1, (name, over)
 
 
@@ -137,8 +144,16 @@ def run_stagewise(case):
     u2_ref = np.concatenate([st(u_m[s * B_:(s + 1) * B_] + O.dynamic_conv(
         u_m[s * B_:(s + 1) * B_], Wl["tapgen_mlp"], cfg["conv_group_size"])) for s in range(b)])
     check_ulps("u2_mlp", u2_m, u2_ref, 2)
-    gu = u2_m @ Wl["gate_up"].astype(np.float64).T
-    check_ulps("act", act, st(O.silu(gu[:, :I]) * gu[:, I:]), 2)
+    Wgu = Wl["gate_up"].astype(np.float64)
+    gu = u2_m @ Wgu.T
+    # beyond 2 ulps only where fp32 accumulation of gate or up (K terms) can
+    # move SiLU(gate)*up that far: a value of up (or gate) that is a small
+    # remainder of large terms carries their absolute rounding error
+    acc_err = 1e-5 * (np.abs(u2_m) @ np.abs(Wgu).T)
+    g, u = gu[:, :I], gu[:, I:]
+    sig = 1.0 / (1.0 + np.exp(-g))
+    slack = np.abs(sig * (1 + g * (1 - sig))) * np.abs(u) * acc_err[:, :I] + np.abs(g * sig) * acc_err[:, I:]
+    check_ulps("act", act, st(O.silu(g) * u), 2, slack=slack)
     h_ref = h_mid + act @ Wl["down"].astype(np.float64).T
     scale = np.abs(h_mid) + np.abs(act) @ np.abs(Wl["down"].astype(np.float64)).T + np.abs(Og) @ np.abs(
         Wl["o"].astype(np.float64)).T

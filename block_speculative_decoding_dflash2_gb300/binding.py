@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(_PKG, "libdflash2.so")
 
 F32 = 0
 BF16 = 1
+FP8W = 2
 
 STATUS = {0: "ok", -1: "invalid argument", -2: "shape", -3: "block size", -4: "dtype",
           -5: "workspace", -6: "cuda", -7: "unsupported"}
@@ -49,8 +50,21 @@ class LayerWeights(ctypes.Structure):
 _TOP_FIELDS = ("embed", "lm_head", "fc", "hidden_norm", "final_norm", "sel")
 
 
+_LAYER_SCALE_FIELDS = ("tapgen_attn", "qkv", "o", "tapgen_mlp", "gate_up", "down")
+
+
+class LayerScales(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in _LAYER_SCALE_FIELDS]
+
+
+class Scales(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("lm_head", "fc", "sel")] + \
+        [("layers", ctypes.POINTER(LayerScales))]
+
+
 class Weights(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_void_p) for n in _TOP_FIELDS] + [("layers", ctypes.POINTER(LayerWeights))]
+    _fields_ = [(n, ctypes.c_void_p) for n in _TOP_FIELDS] + [("layers", ctypes.POINTER(LayerWeights)),
+                                                              ("scales", ctypes.POINTER(Scales))]
 
 
 _lib = None
@@ -87,6 +101,8 @@ def lib():
         L.dflash2_test_gemm_workspace.argtypes = [I, I]
         L.dflash2_test_gemm.restype = I
         L.dflash2_test_gemm.argtypes = [I, P, I, I, P, I, I, I, P, P, S, P]
+        L.dflash2_test_gemm_fp8.restype = I
+        L.dflash2_test_gemm_fp8.argtypes = [P, P, I, I, P, I, I, I, P, P, S, P]
         L.dflash2_select_path_static.restype = I
         L.dflash2_select_path_static.argtypes = [F(Config), F(Weights), I, P, P, P, P, P, P]
         L.dflash2_select_path_static_capacity.restype = S
@@ -138,13 +154,14 @@ def make_config(d):
     for name, _ in Config._fields_:
         v = d[name]
         if name == "dtype" and isinstance(v, str):
-            v = {"f32": F32, "bf16": BF16}[v]
+            v = {"f32": F32, "bf16": BF16, "fp8w": FP8W}[v]
         setattr(c, name, v)
     return c
 
 
 class WeightSet:
-    """Holds a Weights struct over torch device tensors (kept alive here)."""
+    """Holds a Weights struct over torch device tensors (kept alive here);
+    tensors["scales"] (fp8 weights) fills its Scales struct."""
 
     def __init__(self, tensors):
         self.tensors = tensors
@@ -153,8 +170,18 @@ class WeightSet:
         for i, L in enumerate(tensors["layers"]):
             for f in _LAYER_FIELDS:
                 setattr(self._layers[i], f, _ptr(L[f]))
+        scales = None
+        sc = tensors.get("scales")
+        if sc is not None:
+            self._layer_scales = (LayerScales * n)()
+            for i, L in enumerate(sc["layers"]):
+                for f in _LAYER_SCALE_FIELDS:
+                    setattr(self._layer_scales[i], f, _ptr(L[f]))
+            self._scales = Scales(*[_ptr(sc[f]) for f in ("lm_head", "fc", "sel")],
+                                  ctypes.cast(self._layer_scales, ctypes.POINTER(LayerScales)))
+            scales = ctypes.pointer(self._scales)
         self.struct = Weights(*[_ptr(tensors[f]) for f in _TOP_FIELDS],
-                              ctypes.cast(self._layers, ctypes.POINTER(LayerWeights)))
+                              ctypes.cast(self._layers, ctypes.POINTER(LayerWeights)), scales)
 
 
 def dflash2_status_string(status):
@@ -247,6 +274,17 @@ def dflash2_test_gemm(dtype, W, X, ctas, out, workspace, accumulate=False, strea
                                  _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     if rc < 0:
         _check("dflash2_test_gemm", rc)
+    return rc
+
+
+def dflash2_test_gemm_fp8(W8, scale, X, ctas, out, workspace, accumulate=False, stream=None):
+    """W8: uint8 e4m3 codes [M, K]; scale: float32 [M]; X: bf16 [N, K]."""
+    M, K = W8.shape
+    N = X.shape[0]
+    rc = lib().dflash2_test_gemm_fp8(_ptr(W8), _ptr(scale), M, K, _ptr(X), N, ctas, int(accumulate), _ptr(out),
+                                     _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    if rc < 0:
+        _check("dflash2_test_gemm_fp8", rc)
     return rc
 
 

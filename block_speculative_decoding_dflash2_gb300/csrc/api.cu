@@ -48,13 +48,39 @@ int stage_event(int i, cudaStream_t st) {
   return DFLASH2_OK;
 }
 
-int esize(int dtype) { return dtype == DFLASH2_BF16 ? 2 : 4; }
+// Bytes of an activation / cache element (fp8 weights run on bf16 activations).
+int esize(int dtype) { return dtype == DFLASH2_F32 ? 4 : 2; }
+
+// The config as the activation path sees it: fp8-weight configs compute with
+// bf16 activations, cache and norm gains.
+dflash2_config act_config(const dflash2_config& c) {
+  dflash2_config a = c;
+  if (a.dtype == DFLASH2_FP8W) a.dtype = DFLASH2_BF16;
+  return a;
+}
+
+// Row scales of the fp8 weights (all null for F32 / BF16 configs).
+struct Scales {
+  const float *lm_head = nullptr, *fc = nullptr, *sel = nullptr;
+  const dflash2_layer_scales* layers = nullptr;
+  const float* of(const float* dflash2_layer_scales::*f, int l) const { return layers ? layers[l].*f : nullptr; }
+};
+Scales scales_of(const dflash2_config& cfg, const dflash2_weights& w) {
+  Scales s;
+  if (cfg.dtype == DFLASH2_FP8W && w.scales) {
+    s.lm_head = w.scales->lm_head;
+    s.fc = w.scales->fc;
+    s.sel = w.scales->sel;
+    s.layers = w.scales->layers;
+  }
+  return s;
+}
 
 size_t al(size_t x) { return (x + 255) & ~size_t(255); }
 
 int check_config(const dflash2_config* c) {
   if (!c) return DFLASH2_ERR_INVALID_ARG;
-  if (c->dtype != DFLASH2_F32 && c->dtype != DFLASH2_BF16) return DFLASH2_ERR_DTYPE;
+  if (c->dtype != DFLASH2_F32 && c->dtype != DFLASH2_BF16 && c->dtype != DFLASH2_FP8W) return DFLASH2_ERR_DTYPE;
   if (c->block_size < 2 || c->block_size > 32) return DFLASH2_ERR_BLOCK_SIZE;
   if (c->hidden <= 0 || c->n_q_heads <= 0 || c->n_kv_heads <= 0 || c->intermediate <= 0 || c->vocab <= 0 ||
       c->n_layers <= 0 || c->n_taps <= 0 || c->page_size <= 0)
@@ -82,7 +108,8 @@ struct Layout {
       rope, ropea, dsta, total;
 };
 
-Layout plan(const dflash2_config& c, int batch, int n_new, int max_ctx) {
+Layout plan(const dflash2_config& c0, int batch, int n_new, int max_ctx) {
+  const dflash2_config c = act_config(c0);
   const int H = c.hidden, B = c.block_size, D = B - 1, es = esize(c.dtype);
   const int nq = c.n_q_heads, nkv = c.n_kv_heads, d = c.head_dim, I = c.intermediate;
   const int G = H / c.conv_group_size, r = c.selector_rank, k = c.top_k;
@@ -217,10 +244,11 @@ P* at(void* ws, size_t off) {
 // out[n][m] (= or +=) sum_k W[m][k] X[n][k]; split-K partials and tile
 // counters live in the workspace regions of L (the append branch's own
 // regions when `append_branch`, since it runs concurrently with the block).
-GemmOp gemm_op(const void* W, int M, int K, const void* X, int N) {
+GemmOp gemm_op(const void* W, int M, int K, const void* X, int N, const float* wscale = nullptr) {
   GemmOp g;
   std::memset(&g, 0, sizeof(g));
   g.W = W;
+  g.wscale = wscale;
   g.M = M;
   g.K = K;
   g.ldw = K;
@@ -238,11 +266,14 @@ int gemm_fused(GemmOp g, const Ctx& ctx, void* ws, const Layout& L, bool append_
   return gemm_bf16(g, ctx);
 }
 
+// c: the activation config (act_config); wscale: the fp8 row scales of W, or null.
 int gemm(const dflash2_config& c, const Ctx& ctx, void* ws, const Layout& L, const void* W, int M, int K,
-         const void* X, int N, float* out, bool accumulate, bool append_branch = false) {
+         const void* X, int N, float* out, bool accumulate, bool append_branch = false,
+         const float* wscale = nullptr) {
   GemmOp g;
   std::memset(&g, 0, sizeof(g));
   g.W = W;
+  g.wscale = wscale;
   g.M = M;
   g.K = K;
   g.ldw = K;
@@ -271,6 +302,14 @@ int check_weights(const dflash2_config& c, const dflash2_weights* w) {
         !L.tapgen_mlp || !L.gate_up || !L.down)
       return DFLASH2_ERR_INVALID_ARG;
   }
+  if (c.dtype == DFLASH2_FP8W) {
+    const dflash2_scales* s = w->scales;
+    if (!s || !s->lm_head || !s->fc || !s->sel || !s->layers) return DFLASH2_ERR_INVALID_ARG;
+    for (int l = 0; l < c.n_layers; ++l) {
+      const dflash2_layer_scales& L = s->layers[l];
+      if (!L.tapgen_attn || !L.qkv || !L.o || !L.tapgen_mlp || !L.gate_up || !L.down) return DFLASH2_ERR_INVALID_ARG;
+    }
+  }
   return DFLASH2_OK;
 }
 
@@ -278,14 +317,14 @@ int check_weights(const dflash2_config& c, const dflash2_weights* w) {
 // into f (fc contraction, then the hidden norm).  With want_tables, the norm
 // kernel also leaves the rows' RoPE angles and paged-cache offsets for a fused
 // K/V epilogue.
-int project_features(const dflash2_config& c, const dflash2_weights& w, int n_pages, const int32_t* block_table,
-                     int max_pages, int batch, const int32_t* ctx_len, int n_new, const void* taps,
-                     const int32_t* new_off, void* ws, const Layout& L, bool want_tables, const Ctx& ctx,
-                     Ctx* rest_out) {
+int project_features(const dflash2_config& c, const dflash2_weights& w, const Scales& sc, int n_pages,
+                     const int32_t* block_table, int max_pages, int batch, const int32_t* ctx_len, int n_new,
+                     const void* taps, const int32_t* new_off, void* ws, const Layout& L, bool want_tables,
+                     const Ctx& ctx, Ctx* rest_out) {
   const int H = c.hidden, nkv = c.n_kv_heads, d = c.head_dim;
   float* Y = at<float>(ws, L.Ya);
   // the first launch keeps the caller's ctx.pdl (false right after a fork)
-  TRY(gemm(c, ctx, ws, L, w.fc, H, c.n_taps * H, taps, n_new, Y, false, true));
+  TRY(gemm(c, ctx, ws, L, w.fc, H, c.n_taps * H, taps, n_new, Y, false, true, sc.fc));
   Ctx rest = ctx;
   rest.pdl = true;
   RopeTab rt;
@@ -312,7 +351,7 @@ int project_features(const dflash2_config& c, const dflash2_weights& w, int n_pa
 // Stage (a), whole: features, then every layer's context K/V of the appended
 // rows into the paged cache (a contraction per layer, K/V epilogue fused when
 // its shape allows).
-int run_append(const dflash2_config& c, const dflash2_weights& w, void* kc, void* vc, int n_pages,
+int run_append(const dflash2_config& c, const dflash2_weights& w, const Scales& sc, void* kc, void* vc, int n_pages,
                const int32_t* block_table, int max_pages, int batch, const int32_t* ctx_len, int n_new,
                const void* taps, const int32_t* new_off, void* ws, const Layout& L, const Ctx& ctx) {
   if (n_new == 0) return DFLASH2_OK;
@@ -321,17 +360,20 @@ int run_append(const dflash2_config& c, const dflash2_weights& w, void* kc, void
   void* f = at<char>(ws, L.f);
   const bool fused_kv = c.dtype == DFLASH2_BF16 && gemm_fusable(2 * nkv * d, n_new, kEpiHeads);
   Ctx rest;
-  TRY(project_features(c, w, n_pages, block_table, max_pages, batch, ctx_len, n_new, taps, new_off, ws, L, fused_kv,
-                       ctx, &rest));
+  TRY(project_features(c, w, sc, n_pages, block_table, max_pages, batch, ctx_len, n_new, taps, new_off, ws, L,
+                       fused_kv, ctx, &rest));
   const size_t layer_elems = (size_t)n_pages * c.page_size * nkv * d;
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash2_layer_weights& Lw = w.layers[l];
-    const void* wkv = elem_ptr(Lw.qkv, (size_t)nq * d * H, c.dtype);
+    // the k and v rows of the qkv matrix (fp8: bytes, and their scales)
+    const float* skv = sc.layers ? sc.layers[l].qkv + (size_t)nq * d : nullptr;
+    const void* wkv = skv ? static_cast<const void*>(static_cast<const uint8_t*>(Lw.qkv) + (size_t)nq * d * H)
+                          : static_cast<const void*>(elem_ptr(Lw.qkv, (size_t)nq * d * H, c.dtype));
     char* kcl = const_cast<char*>(elem_ptr(kc, l * layer_elems, c.dtype));
     char* vcl = const_cast<char*>(elem_ptr(vc, l * layer_elems, c.dtype));
     if (fused_kv) {
       // K/V epilogue fused: k-norm + RoPE + paged store of the appended rows
-      GemmOp g = gemm_op(wkv, 2 * nkv * d, H, f, n_new);
+      GemmOp g = gemm_op(wkv, 2 * nkv * d, H, f, n_new, skv);
       g.epi = kEpiHeads;
       g.hd = d;
       g.n_kh = nkv;
@@ -344,7 +386,7 @@ int run_append(const dflash2_config& c, const dflash2_weights& w, void* kc, void
       g.vc = vcl;
       TRY(gemm_fused(g, rest, ws, L, true));
     } else {
-      TRY(gemm(c, rest, ws, L, wkv, 2 * nkv * d, H, f, n_new, Y, false, true));
+      TRY(gemm(c, rest, ws, L, wkv, 2 * nkv * d, H, f, n_new, Y, false, true, skv));
       TRY(launch_kv_append(c.dtype, Y, n_new, nkv, d, Lw.k_norm, c.rms_eps, c.rope_theta, ctx_len, new_off, batch,
                            block_table, max_pages, c.page_size, n_pages, kcl, vcl, rest));
     }
@@ -432,8 +474,8 @@ int dflash2_append_context(const dflash2_config* cfg, const dflash2_weights* w, 
   if (ws_bytes < L.total) return DFLASH2_ERR_WORKSPACE;
   Ctx ctx;
   TRY(device_ctx(&ctx, stream, workspace));
-  return run_append(*cfg, *w, k_cache, v_cache, n_pages, block_table, max_pages, batch, ctx_len, n_new, new_taps,
-                    new_off, workspace, L, ctx);
+  return run_append(act_config(*cfg), *w, scales_of(*cfg, *w), k_cache, v_cache, n_pages, block_table, max_pages,
+                    batch, ctx_len, n_new, new_taps, new_off, workspace, L, ctx);
 }
 
 int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void* k_cache, void* v_cache,
@@ -446,7 +488,8 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
   TRY(check_cache_args(k_cache, v_cache, n_pages, block_table, max_pages, batch, ctx_len, n_new, new_taps, new_off));
   if (!anchor || !cand_id || !cand_logit) return DFLASH2_ERR_INVALID_ARG;
   if (!workspace) return DFLASH2_ERR_WORKSPACE;
-  const dflash2_config& c = *cfg;
+  const dflash2_config c = act_config(*cfg);
+  const Scales sc = scales_of(*cfg, *w);
   const int max_ctx = max_pages * c.page_size;
   const Layout L = plan(c, batch, n_new, max_ctx);
   if (ws_bytes < L.total) return DFLASH2_ERR_WORKSPACE;
@@ -493,10 +536,10 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
     actx.pdl = false;  // full dependency on the fork event
     if (split_sms) actx.nsm = ctx.nsm - kForkPrologueSMs;
     if (merged)
-      TRY(project_features(c, *w, n_pages, block_table, max_pages, batch, ctx_len, n_new, new_taps, new_off,
+      TRY(project_features(c, *w, sc, n_pages, block_table, max_pages, batch, ctx_len, n_new, new_taps, new_off,
                            workspace, L, true, actx, nullptr));
     else
-      TRY(run_append(c, *w, k_cache, v_cache, n_pages, block_table, max_pages, batch, ctx_len, n_new, new_taps,
+      TRY(run_append(c, *w, sc, k_cache, v_cache, n_pages, block_table, max_pages, batch, ctx_len, n_new, new_taps,
                      new_off, workspace, L, actx));
     TRY(stage_event(1, side.s));
     if (cudaEventRecord(side.join, side.s) != cudaSuccess) return DFLASH2_ERR_CUDA;
@@ -536,8 +579,9 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
     Ctx ectx = ctx;
     if (split_sms) ectx.nsm = kForkPrologueSMs / 2;  // the prologue sizes its grid at two CTAs per SM
     TRY(launch_conv_prologue(c.dtype, nullptr, anchor, c.mask_token_id, w->embed, c.vocab, c.input_embedding_scale,
-                             w->layers[0].attn_norm, c.rms_eps, w->layers[0].tapgen_attn, batch, B, H,
-                             c.conv_group_size, h, ua, u2a, rt, ectx));
+                             w->layers[0].attn_norm, c.rms_eps, w->layers[0].tapgen_attn,
+                             sc.of(&dflash2_layer_scales::tapgen_attn, 0), batch, B, H, c.conv_group_size, h, ua, u2a,
+                             rt, ectx));
   }
   else
     TRY(launch_embed_norm(c.dtype, anchor, c.mask_token_id, batch, B, w->embed, c.vocab, H, c.input_embedding_scale,
@@ -545,14 +589,21 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
   const int n_app = merged ? n_new : 0;  // appended rows the QKV contractions carry
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash2_layer_weights& Lw = w->layers[l];
+    const float* s_tap_a = sc.of(&dflash2_layer_scales::tapgen_attn, l);
+    const float* s_qkv = sc.of(&dflash2_layer_scales::qkv, l);
+    const float* s_o = sc.of(&dflash2_layer_scales::o, l);
+    const float* s_tap_m = sc.of(&dflash2_layer_scales::tapgen_mlp, l);
+    const float* s_gu = sc.of(&dflash2_layer_scales::gate_up, l);
+    const float* s_down = sc.of(&dflash2_layer_scales::down, l);
     // attention sublayer: conv around the normed input, QKV, attention, O (+= residual)
     if (fused) {
       if (l > 0)
         TRY(launch_conv_prologue(c.dtype, h, nullptr, 0, w->embed, c.vocab, 1.f, Lw.attn_norm, c.rms_eps,
-                                 Lw.tapgen_attn, batch, B, H, c.conv_group_size, nullptr, ua, u2a, RopeTab{}, ctx));
+                                 Lw.tapgen_attn, s_tap_a, batch, B, H, c.conv_group_size, nullptr, ua, u2a, RopeTab{},
+                                 ctx));
     } else {
       if (l > 0) TRY(launch_rownorm(c.dtype, h, rows, H, Lw.attn_norm, c.rms_eps, ua, B, 0, ctx));
-      TRY(gemm(c, ctx, ws, L, Lw.tapgen_attn, 2 * G, H, ua, rows, Y, false));
+      TRY(gemm(c, ctx, ws, L, Lw.tapgen_attn, 2 * G, H, ua, rows, Y, false, false, s_tap_a));
       TRY(launch_dyn_conv(c.dtype, ua, Y, rows, H, c.conv_group_size, B, u2a, ctx));
     }
     // merged: the QKV contraction reads the appended rows' features, a full
@@ -565,7 +616,7 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
     if (fused_qkv) {
       // q/k-norm + RoPE fused into the QKV epilogue; merged: the appended rows'
       // features ride along as extra columns and their k/v go to the cache
-      GemmOp g = gemm_op(Lw.qkv, qkvM, H, u2a, rows + n_app);
+      GemmOp g = gemm_op(Lw.qkv, qkvM, H, u2a, rows + n_app, s_qkv);
       g.epi = kEpiHeads;
       g.hd = d;
       g.n_qh = nq;
@@ -586,7 +637,7 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
       }
       TRY(gemm_fused(g, qctx, ws, L, false));
     } else {
-      TRY(gemm(c, ctx, ws, L, Lw.qkv, (nq + 2 * nkv) * d, H, u2a, rows, Y, false));
+      TRY(gemm(c, ctx, ws, L, Lw.qkv, (nq + 2 * nkv) * d, H, u2a, rows, Y, false, false, s_qkv));
       TRY(launch_qkv_epilogue(c.dtype, Y, rows, B, nq, nkv, d, Lw.q_norm, Lw.k_norm, c.rms_eps, c.rope_theta,
                               ctx_len, new_off, q, kb, vb, ctx));
     }
@@ -599,26 +650,26 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
     TRY(launch_attention(c.dtype, q, kb, vb, elem_ptr(k_cache, l * layer_elems, c.dtype),
                          elem_ptr(v_cache, l * layer_elems, c.dtype), block_table, max_pages, c.page_size, n_pages,
                          ctx_len, new_off, batch, B, nq, nkv, d, max_ctx, at<float>(workspace, L.attn), O, jctx));
-    TRY(gemm(c, ctx, ws, L, Lw.o, H, nq * d, O, rows, h, true));
+    TRY(gemm(c, ctx, ws, L, Lw.o, H, nq * d, O, rows, h, true, false, s_o));
     // MLP sublayer: conv around the normed input, gate/up, SiLU*up, down (+= residual)
     if (fused) {
-      TRY(launch_conv_prologue(c.dtype, h, nullptr, 0, w->embed, c.vocab, 1.f, Lw.mlp_norm, c.rms_eps, Lw.tapgen_mlp,
+      TRY(launch_conv_prologue(c.dtype, h, nullptr, 0, w->embed, c.vocab, 1.f, Lw.mlp_norm, c.rms_eps, Lw.tapgen_mlp, s_tap_m,
                                batch, B, H, c.conv_group_size, nullptr, u, u2, RopeTab{}, ctx));
     } else {
       TRY(launch_rownorm(c.dtype, h, rows, H, Lw.mlp_norm, c.rms_eps, u, B, 0, ctx));
-      TRY(gemm(c, ctx, ws, L, Lw.tapgen_mlp, 2 * G, H, u, rows, Y, false));
+      TRY(gemm(c, ctx, ws, L, Lw.tapgen_mlp, 2 * G, H, u, rows, Y, false, false, s_tap_m));
       TRY(launch_dyn_conv(c.dtype, u, Y, rows, H, c.conv_group_size, B, u2, ctx));
     }
     if (c.dtype == DFLASH2_BF16 && gemm_fusable(2 * I, rows, kEpiSwiglu)) {
-      GemmOp g = gemm_op(Lw.gate_up, 2 * I, H, u2, rows);  // SiLU(gate) * up fused into the epilogue
+      GemmOp g = gemm_op(Lw.gate_up, 2 * I, H, u2, rows, s_gu);  // SiLU(gate) * up fused into the epilogue
       g.epi = kEpiSwiglu;
       g.act = act;
       TRY(gemm_fused(g, ctx, ws, L, false));
     } else {
-      TRY(gemm(c, ctx, ws, L, Lw.gate_up, 2 * I, H, u2, rows, Y, false));
+      TRY(gemm(c, ctx, ws, L, Lw.gate_up, 2 * I, H, u2, rows, Y, false, false, s_gu));
       TRY(launch_act(c.dtype, Y, rows, I, act, ctx));
     }
-    TRY(gemm(c, ctx, ws, L, Lw.down, H, I, act, rows, h, true));
+    TRY(gemm(c, ctx, ws, L, Lw.down, H, I, act, rows, h, true, false, s_down));
   }
   TRY(launch_rownorm(c.dtype, h, rows, H, w->final_norm, c.rms_eps, hn, B, 1, ctx));
 
@@ -632,6 +683,7 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
     GemmOp g;
     std::memset(&g, 0, sizeof(g));
     g.W = w->lm_head;
+    g.wscale = sc.lm_head;
     g.M = c.vocab;
     g.K = H;
     g.ldw = H;
@@ -666,7 +718,9 @@ int dflash2_select_path(const dflash2_config* cfg, const dflash2_weights* w, int
   if (batch <= 0) return DFLASH2_ERR_SHAPE;
   if (!anchor || !cand_id || !cand_logit || !path) return DFLASH2_ERR_INVALID_ARG;
   if (!workspace) return DFLASH2_ERR_WORKSPACE;
-  const dflash2_config& c = *cfg;
+  if (cfg->dtype == DFLASH2_FP8W && (!w->scales || !w->scales->sel)) return DFLASH2_ERR_INVALID_ARG;
+  const dflash2_config c = act_config(*cfg);
+  const Scales sc = scales_of(*cfg, *w);
   const Layout L = plan(c, batch, 0, 0);
   if (ws_bytes < L.total) return DFLASH2_ERR_WORKSPACE;
   Ctx ctx;
@@ -675,7 +729,7 @@ int dflash2_select_path(const dflash2_config* cfg, const dflash2_weights* w, int
   void* x = at<char>(workspace, L.selx);
   float* Y = at<float>(workspace, L.Y);
   TRY(launch_sel_gather(c.dtype, anchor, cand_id, batch, D, k, w->embed, c.vocab, H, x, ctx));
-  TRY(gemm(c, ctx, workspace, L, w->sel, 2 * r, H, x, batch * (D * k + 1), Y, false));
+  TRY(gemm(c, ctx, workspace, L, w->sel, 2 * r, H, x, batch * (D * k + 1), Y, false, false, sc.sel));
   return launch_viterbi(Y, nullptr, anchor, c.vocab, cand_id, cand_logit, batch, D, k, r, path, path_score, ctx);
 }
 
@@ -687,12 +741,13 @@ size_t dflash2_selector_table_bytes(const dflash2_config* cfg) {
 int dflash2_build_selector_table(const dflash2_config* cfg, const dflash2_weights* w, float* table, void* stream) {
   TRY(check_config(cfg));
   if (!w || !w->embed || !w->sel || !table) return DFLASH2_ERR_INVALID_ARG;
+  if (cfg->dtype == DFLASH2_FP8W && (!w->scales || !w->scales->sel)) return DFLASH2_ERR_INVALID_ARG;
   Ctx ctx;
   TRY(device_ctx(&ctx, stream, nullptr));
-  const dflash2_config& c = *cfg;
+  const dflash2_config c = act_config(*cfg);
   // table[v][m] = sum_h sel[m][h] E[v][h]: the selector contraction with the
   // whole vocabulary as its activation rows (whole tiles: no workspace)
-  GemmOp g = gemm_op(w->sel, 2 * c.selector_rank, c.hidden, w->embed, c.vocab);
+  GemmOp g = gemm_op(w->sel, 2 * c.selector_rank, c.hidden, w->embed, c.vocab, scales_of(*cfg, *w).sel);
   g.out = table;
   g.ctas = -1;
   if (c.dtype == DFLASH2_BF16) return gemm_bf16(g, ctx);

@@ -5,6 +5,8 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -124,6 +126,24 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory writes before
+// later async-proxy accesses (TMA, tcgen05.mma operand reads).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ----------------------------------------------------------------- fp8 weights
+// Two fp8 e4m3 codes (byte 0 -> .x, byte 1 -> .y) as bf16x2, exactly: every
+// finite e4m3 value (3 mantissa bits, exponents 2^-9..2^8) is a bf16 value.
+__device__ __forceinline__ __nv_bfloat162 e4m3x2_to_bf16x2(uint16_t q) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(q), __NV_E4M3);
+  return __float22bfloat162_rn(__half22float2(__half2(h)));
+}
+__device__ __forceinline__ float e4m3_to_float(uint8_t q) {
+  const __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(q), __NV_E4M3);
+  return __half2float(__half(h));
 }
 
 // ----------------------------------------------------------------- PTX: clusters

@@ -337,12 +337,25 @@ struct Vec4Raw<bf16> {
   }
 };
 
-template <typename T, bool EMBED>
+template <>
+struct Vec4Raw<uint8_t> {  // fp8 e4m3 tap weights (scaled per row after the dot product)
+  uint32_t v;
+  __device__ __forceinline__ void load(const uint8_t* p) { v = *reinterpret_cast<const uint32_t*>(p); }
+  __device__ __forceinline__ float4 f() const {
+    const float2 a = __bfloat1622float2(e4m3x2_to_bf16x2((uint16_t)(v & 0xffffu)));
+    const float2 b = __bfloat1622float2(e4m3x2_to_bf16x2((uint16_t)(v >> 16)));
+    return make_float4(a.x, a.y, b.x, b.y);
+  }
+};
+
+// WT: element type of the tap weights (T, or uint8_t e4m3 codes with the
+// per-row scales wsc: lambda = wsc[row] * sum_h q[row][h] u[h]).
+template <typename T, bool EMBED, typename WT = T>
 __global__ void __launch_bounds__(PT) conv_prologue_kernel(
     const float* __restrict__ h_in, const int32_t* __restrict__ anchor, int mask_id, const T* __restrict__ E, int V,
-    float scale, const T* __restrict__ gamma, float eps, const T* __restrict__ Wt, int H, int gs, int gpc, int B,
-    int stage_w, float* __restrict__ h_out, T* __restrict__ u_out, T* __restrict__ u2_out, const __grid_constant__ RopeTab rt,
-    unsigned* status) {
+    float scale, const T* __restrict__ gamma, float eps, const WT* __restrict__ Wt, const float* __restrict__ wsc,
+    int H, int gs, int gpc, int B, int stage_w, float* __restrict__ h_out, T* __restrict__ u_out,
+    T* __restrict__ u2_out, const __grid_constant__ RopeTab rt, unsigned* status) {
   extern __shared__ __align__(16) uint8_t smraw[];
   constexpr int NW = PT / 32;
   constexpr int PU = sizeof(T) == 2 ? PUB : PUB / 2;  // fp32 rows: half, to stay in registers
@@ -350,15 +363,15 @@ __global__ void __launch_bounds__(PT) conv_prologue_kernel(
   const int s = blockIdx.y, G = H / gs;
   const int g0 = blockIdx.x * gpc, ng = min(gpc, G - g0);
   T* us = reinterpret_cast<T*>(smraw);                 // [B][H] normed rows as stored
-  T* wsm = us + (size_t)B * H;                         // [2 gpc][H] tap rows (stage_w)
+  WT* wsm = reinterpret_cast<WT*>(us + (size_t)B * H); // [2 gpc][H] tap rows (stage_w)
   float* rinv = reinterpret_cast<float*>(wsm + (stage_w ? (size_t)2 * gpc * H : 0));  // [B]
   float* lam = rinv + B;                               // [B][2 gpc] tap logits, then alpha
   float* red = lam + B * 2 * gpc;                      // [B][NW] partial sums of squares
   __shared__ int toks[32];
   pdl_launch_next();
   if (stage_w) {  // the weights are not written by any kernel of the stream
-    constexpr int E16 = 16 / sizeof(T);
-    const T* src = Wt + (size_t)2 * g0 * H;
+    constexpr int E16 = 16 / sizeof(WT);
+    const WT* src = Wt + (size_t)2 * g0 * H;
     for (int i = threadIdx.x; i < 2 * ng * H / E16; i += PT)
       cp_async16(wsm + (size_t)i * E16, src + (size_t)i * E16, true);
     cp_async_commit();
@@ -457,10 +470,10 @@ __global__ void __launch_bounds__(PT) conv_prologue_kernel(
   // 3. tap logits of this CTA's groups: one warp per (row, tap row)
   for (int p = warp; p < B * 2 * ng; p += NW) {
     const int t = p / (2 * ng), jj = p % (2 * ng);
-    const T* w = stage_w ? wsm + (size_t)jj * H : Wt + (size_t)(2 * g0 + jj) * H;
+    const WT* w = stage_w ? wsm + (size_t)jj * H : Wt + (size_t)(2 * g0 + jj) * H;
     float acc = 0.f;
     for (int m0 = lane * 4; m0 < H; m0 += 128 * PU) {
-      Vec4Raw<T> wv[PU];
+      Vec4Raw<WT> wv[PU];
 #pragma unroll
       for (int k = 0; k < PU; ++k)
         if (m0 + 128 * k < H) wv[k].load(w + m0 + 128 * k);
@@ -472,7 +485,7 @@ __global__ void __launch_bounds__(PT) conv_prologue_kernel(
         }
     }
     acc = warp_sum(acc);
-    if (lane == 0) lam[t * 2 * gpc + jj] = acc;
+    if (lane == 0) lam[t * 2 * gpc + jj] = wsc ? acc * wsc[2 * g0 + jj] : acc;
   }
   __syncthreads();
   // 4. alpha = softmax over the two taps of each (row, group)
@@ -631,9 +644,9 @@ int launch_dyn_conv(int dtype, const void* u, const float* Y, int rows, int H, i
 
 // Shared memory of the prologue: the B normed rows, the CTA's tap rows when
 // staged, 1/rms, tap logits and the per-warp partial sums.
-size_t conv_prologue_smem(int dtype, int B, int H, int gpc, bool stage_w) {
+size_t conv_prologue_smem(int dtype, int B, int H, int gpc, bool stage_w, bool w8) {
   const size_t es = dtype == DFLASH2_BF16 ? 2 : 4;
-  return (size_t)B * H * es + (stage_w ? (size_t)2 * gpc * H * es : 0) +
+  return (size_t)B * H * es + (stage_w ? (size_t)2 * gpc * H * (w8 ? 1 : es) : 0) +
          (size_t)B * (1 + 2 * gpc + PT / 32) * sizeof(float);
 }
 
@@ -646,17 +659,19 @@ int conv_prologue_groups(int G, int batch, int nsm) {
 constexpr size_t kPrologueSmem = 200 * 1024;
 
 bool conv_prologue_fits(int dtype, int batch, int B, int H, int G, int nsm) {
-  return B <= 32 && conv_prologue_smem(dtype, B, H, conv_prologue_groups(G, batch, nsm), false) <= kPrologueSmem;
+  return B <= 32 && conv_prologue_smem(dtype, B, H, conv_prologue_groups(G, batch, nsm), false, false) <= kPrologueSmem;
 }
 
 int launch_conv_prologue(int dtype, const float* h_in, const int32_t* anchor, int mask_id, const void* embed, int V,
-                         float scale, const void* gamma, float eps, const void* w_tap, int batch, int B, int H,
-                         int group_size, float* h_out, void* u_out, void* u2_out, const RopeTab& rt,
-                         const Ctx& c) {
+                         float scale, const void* gamma, float eps, const void* w_tap, const float* tap_scale,
+                         int batch, int B, int H, int group_size, float* h_out, void* u_out, void* u2_out,
+                         const RopeTab& rt, const Ctx& c) {
   const int G = H / group_size;
   const int gpc = conv_prologue_groups(G, batch, c.nsm);
-  const bool stage_w = conv_prologue_smem(dtype, B, H, gpc, true) <= kPrologueSmem;
-  const size_t smem = conv_prologue_smem(dtype, B, H, gpc, stage_w);
+  const bool w8 = tap_scale != nullptr;
+  if (w8 && dtype != DFLASH2_BF16) return DFLASH2_ERR_DTYPE;
+  const bool stage_w = conv_prologue_smem(dtype, B, H, gpc, true, w8) <= kPrologueSmem;
+  const size_t smem = conv_prologue_smem(dtype, B, H, gpc, stage_w, w8);
   if (smem > kPrologueSmem || B > 32) return DFLASH2_ERR_SHAPE;
   static bool attr = false;  // set once, before any capture
   if (!attr) {
@@ -667,21 +682,37 @@ int launch_conv_prologue(int dtype, const float* h_in, const int32_t* anchor, in
         cudaFuncSetAttribute(conv_prologue_kernel<float, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kPrologueSmem) ||
         cudaFuncSetAttribute(conv_prologue_kernel<float, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kPrologueSmem))
+                             kPrologueSmem) ||
+        cudaFuncSetAttribute(conv_prologue_kernel<bf16, true, uint8_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kPrologueSmem) ||
+        cudaFuncSetAttribute(conv_prologue_kernel<bf16, false, uint8_t>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kPrologueSmem))
       return DFLASH2_ERR_CUDA;
     attr = true;
   }
   const dim3 grid((G + gpc - 1) / gpc, batch);
   int rc;
+  if (w8) {
+    const uint8_t* wq = static_cast<const uint8_t*>(w_tap);
+    if (h_in)
+      return launch_k(conv_prologue_kernel<bf16, false, uint8_t>, grid, dim3(PT), smem, c, h_in, anchor, mask_id,
+                      static_cast<const bf16*>(embed), V, scale, static_cast<const bf16*>(gamma), eps, wq, tap_scale,
+                      H, group_size, gpc, B, stage_w ? 1 : 0, h_out, static_cast<bf16*>(u_out),
+                      static_cast<bf16*>(u2_out), rt, c.status);
+    return launch_k(conv_prologue_kernel<bf16, true, uint8_t>, grid, dim3(PT), smem, c, h_in, anchor, mask_id,
+                    static_cast<const bf16*>(embed), V, scale, static_cast<const bf16*>(gamma), eps, wq, tap_scale, H,
+                    group_size, gpc, B, stage_w ? 1 : 0, h_out, static_cast<bf16*>(u_out), static_cast<bf16*>(u2_out),
+                    rt, c.status);
+  }
   if (h_in)
     DF2_DISPATCH(dtype, rc = launch_k(conv_prologue_kernel<T, false>, grid, dim3(PT), smem, c, h_in, anchor, mask_id,
                                       static_cast<const T*>(embed), V, scale, static_cast<const T*>(gamma), eps,
-                                      static_cast<const T*>(w_tap), H, group_size, gpc, B, stage_w ? 1 : 0, h_out,
+                                      static_cast<const T*>(w_tap), nullptr, H, group_size, gpc, B, stage_w ? 1 : 0, h_out,
                                       static_cast<T*>(u_out), static_cast<T*>(u2_out), rt, c.status));
   else
     DF2_DISPATCH(dtype, rc = launch_k(conv_prologue_kernel<T, true>, grid, dim3(PT), smem, c, h_in, anchor, mask_id,
                                       static_cast<const T*>(embed), V, scale, static_cast<const T*>(gamma), eps,
-                                      static_cast<const T*>(w_tap), H, group_size, gpc, B, stage_w ? 1 : 0, h_out,
+                                      static_cast<const T*>(w_tap), nullptr, H, group_size, gpc, B, stage_w ? 1 : 0, h_out,
                                       static_cast<T*>(u_out), static_cast<T*>(u2_out), rt, c.status));
   return rc;
 }

@@ -35,11 +35,16 @@
 //           RoPE of q and k and stores bf16 q, k, v: to the block's q/k/v
 //           buffers, or, for appended context rows, into the paged cache.
 //
-// Warp roles (192 threads):
+// Warp roles (192 threads; 320 with fp8 weights):
 //   warp 0      TMA producer (one lane): weight + activation tiles -> ring
 //   warp 1      MMA issuer (one lane) and TMEM owner
 //   warps 2..5  epilogue: TMEM -> registers -> the output tile, a partial
 //               piece (coalesced over m), or the streaming top-k.
+//   warps 6..9  fp8 weights only: converters.  The weight tile arrives as
+//               e4m3 bytes in a staging slot (half the bytes of bf16); the
+//               converters rewrite it as bf16 in the MMA operand layout
+//               (exact: every e4m3 value is a bf16 value), and the epilogue
+//               multiplies each output row by its weight row's fp32 scale.
 // The accumulator is double-buffered in TMEM so the epilogue of one unit
 // overlaps the MMAs of the next.
 //
@@ -66,6 +71,8 @@ constexpr int BK = 64;      // K elements per ring stage (128 bytes of bf16)
 constexpr int SMEM_BUDGET = 227 * 1024;
 constexpr uint64_t WAIT_NS = 1000000000ull;
 constexpr int THREADS = 192;
+constexpr int THREADS_FP8 = THREADS + 128;  // + 4 converter warps
+__host__ __device__ constexpr int threads_of(bool fp8) { return fp8 ? THREADS_FP8 : THREADS; }
 
 struct TcArgs {
   int M, N, K;
@@ -81,6 +88,7 @@ struct TcArgs {
   float* debug;
   float mult, cap;
   unsigned* status;
+  const float* wscale;  // fp8 weights: [M] per-row dequantisation scales (null: bf16 weights)
   // SWIGLU
   bf16* act;  // [N][I], I = M / 2
   int I;
@@ -102,11 +110,12 @@ struct TcArgs {
 
 enum { EPI_PLAIN = 0, EPI_TOPK = 1, EPI_SWIGLU = 2, EPI_HEADS = 3 };
 
-template <int BN>
+template <int BN, bool FP8 = false>
 struct TcCfg {
   static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int A8_BYTES = FP8 ? BM * BK : 0;  // e4m3 staging of a weight tile
   static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int STAGE = A_BYTES + A8_BYTES + B_BYTES;
   static constexpr int TOPK_EXTRA = 16 * BM * 4 + BN * KMAX * 8;
   static constexpr int FUSE_EXTRA = 16 * BM * 4 + 4 * 16 * 4;  // exchange tile, column sums
   static constexpr int FIXED = 1024 /* alignment slack */ + 1024 /* barriers */;
@@ -184,13 +193,13 @@ __device__ __forceinline__ bool named_sync_or(bool pred) {
   return r != 0;
 }
 
-template <int BN, int EPI>
-__global__ void __launch_bounds__(THREADS, 1)
+template <int BN, int EPI, bool FP8>
+__global__ void __launch_bounds__(threads_of(FP8), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcArgs a) {
-  using C = TcCfg<BN>;
+  using C = TcCfg<BN, FP8>;
   constexpr bool TOPK = EPI == EPI_TOPK;
   constexpr int STAGES = C::stages(EPI);
-  constexpr int A_BYTES = C::A_BYTES, B_BYTES = C::B_BYTES;
+  constexpr int A_BYTES = C::A_BYTES, B_BYTES = C::B_BYTES, A8_BYTES = C::A8_BYTES;
   static_assert(STAGES >= 2, "ring too small");
   static_assert(B_BYTES % 1024 == 0, "B tile must keep 1024-byte swizzle atoms aligned");
 
@@ -198,7 +207,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stA = smem;
   uint8_t* stB = smem + STAGES * A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(stB + STAGES * B_BYTES);
+  uint8_t* stA8 = stB + STAGES * B_BYTES;  // fp8: [STAGES][BM][BK] e4m3 staging (rows of 64 bytes)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stA8 + STAGES * A8_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* tfull = bars + 2 * STAGES;
@@ -207,6 +217,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = abort_flag + 1;
+  // fp8: the TMA barriers of the staging slots (full then means "converted")
+  uint64_t* full8 = drain + 4;
+  uint64_t* tma_full = FP8 ? full8 : full;
   float* stg = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 1024);  // [16][BM]
   float* lv_s = stg + 16 * BM;                                                       // [BN][KMAX]
   int* li_s = reinterpret_cast<int*>(lv_s + BN * KMAX);                              // [BN][KMAX]
@@ -217,8 +230,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full + s, 1);
+      mbar_init(full + s, FP8 ? 128 : 1);  // fp8: every converter thread arrives
       mbar_init(empty + s, 1);
+      if (FP8) mbar_init(full8 + s, 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(tfull + i, 1);
@@ -252,12 +266,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
       // weight tile of chunk kc for m-tile mt (SWIGLU: 64 gate rows + the 64 matching up rows)
+      // (fp8: into the staging slot; a byte per element, so the x
+      // coordinate is the same element index)
+      uint8_t* dstA = FP8 ? stA8 : stA;
+      constexpr int AB = FP8 ? A8_BYTES : A_BYTES;
       auto load_a = [&](int st, int kc_, int mt_) {
         if constexpr (EPI == EPI_SWIGLU) {
-          tma_load_2d(stA + st * A_BYTES, &tmA, full + st, kc_ * BK, mt_ * (BM / 2), pol_w);
-          tma_load_2d(stA + st * A_BYTES + A_BYTES / 2, &tmA, full + st, kc_ * BK, a.I + mt_ * (BM / 2), pol_w);
+          tma_load_2d(dstA + st * AB, &tmA, tma_full + st, kc_ * BK, mt_ * (BM / 2), pol_w);
+          tma_load_2d(dstA + st * AB + AB / 2, &tmA, tma_full + st, kc_ * BK, a.I + mt_ * (BM / 2), pol_w);
         } else {
-          tma_load_2d(stA + st * A_BYTES, &tmA, full + st, kc_ * BK, mt_ * BM, pol_w);
+          tma_load_2d(dstA + st * AB, &tmA, tma_full + st, kc_ * BK, mt_ * BM, pol_w);
         }
       };
       UnitIter it = unit_iter(a);
@@ -271,7 +289,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         int tt = t, kk = kc, kk1 = k1;
         bool h = have;
         while (pre < STAGES && h) {
-          mbar_arrive_expect_tx(full + pre, A_BYTES + B_BYTES);
+          mbar_arrive_expect_tx(tma_full + pre, AB + B_BYTES);
           load_a(pre, kk, tt % a.m_tiles);
           ++pre;
           if (++kk == kk1) h = pit.next(tt, kk, kk1);
@@ -281,7 +299,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // 2. the activation tiles of those chunks
       long issued = 0;
       for (int i = 0; i < pre; ++i) {
-        tma_load_2d(stB + i * B_BYTES, &tmB, full + i, kc * BK, (t / a.m_tiles) * BN, pol_x);
+        tma_load_2d(stB + i * B_BYTES, &tmB, tma_full + i, kc * BK, (t / a.m_tiles) * BN, pol_x);
         ++issued;
         if (++kc == k1) have = it.next(t, kc, k1);
       }
@@ -297,9 +315,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full + stage, A_BYTES + B_BYTES);
+          mbar_arrive_expect_tx(tma_full + stage, AB + B_BYTES);
           load_a(stage, kc, mt);
-          tma_load_2d(stB + stage * B_BYTES, &tmB, full + stage, kc * BK, nt * BN, pol_x);
+          tma_load_2d(stB + stage * B_BYTES, &tmB, tma_full + stage, kc * BK, nt * BN, pol_x);
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -315,7 +333,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const long cnt = issued / STAGES + (s < issued % STAGES ? 1 : 0);
           if (cnt > 0) {
             volatile int never = 0;
-            mbar_wait(full + s, (uint32_t)((cnt - 1) & 1), &never, WAIT_NS);
+            mbar_wait(tma_full + s, (uint32_t)((cnt - 1) & 1), &never, WAIT_NS);
           }
         }
       }
@@ -338,7 +356,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(acc * BN);
         for (int kc = k0; kc < k1; ++kc) {
-          if (!mbar_wait(full + stage, phase, abort_flag, WAIT_NS)) {
+          if (!mbar_wait(full + stage, phase, abort_flag, WAIT_NS) ||
+              (FP8 && !mbar_wait(full8 + stage, phase, abort_flag, WAIT_NS))) {
             fail();
             ok = false;
             break;
@@ -366,6 +385,52 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_wait(drain, 0, &never, WAIT_NS);
     }
     __syncwarp();  // as for the producer warp
+  } else if (FP8 && warp >= 6) {
+    // ------------------------------------------------------------ fp8 converters
+    // Slot s holds rows of 64 e4m3 bytes; thread ct rewrites 16-byte pieces
+    // (16 elements of row r) as two 16-byte bf16 chunks of the 128-byte
+    // swizzled operand row (chunk c of row r lives at chunk c ^ (r & 7)).
+    const int ct = threadIdx.x - THREADS;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    UnitIter it = unit_iter(a);
+    int t, k0, k1;
+    while (ok && it.next(t, k0, k1)) {
+      for (int kc = k0; kc < k1; ++kc) {
+        if (!mbar_wait(full8 + stage, phase, abort_flag, WAIT_NS)) {
+          fail();
+          ok = false;
+          break;
+        }
+        const uint8_t* src = stA8 + stage * A8_BYTES;
+        uint8_t* dst = stA + stage * A_BYTES;
+#pragma unroll
+        for (int i = 0; i < A8_BYTES / 16 / 128; ++i) {
+          const int piece = ct + i * 128;
+          const int r = piece >> 2, c0 = (piece & 3) * 2;
+          const uint4 q = *reinterpret_cast<const uint4*>(src + piece * 16);
+          const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+          uint32_t o[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 lo = e4m3x2_to_bf16x2((uint16_t)(w[e] & 0xffffu));
+            const __nv_bfloat162 hi = e4m3x2_to_bf16x2((uint16_t)(w[e] >> 16));
+            o[2 * e] = *reinterpret_cast<const uint32_t*>(&lo);
+            o[2 * e + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+          }
+          uint8_t* row = dst + r * 128;
+          *reinterpret_cast<uint4*>(row + ((c0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        fence_proxy_async_smem();  // the operand is read by tcgen05.mma (async proxy)
+        mbar_arrive(full + stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     pdl_wait();  // outputs, partials and counters may still be in use by the previous kernel
@@ -405,6 +470,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const int m = mt * BM + row;
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      // fp8 weights: the dequantisation scale of this thread's weight row
+      // (SWIGLU: row < 64 is gate row mt*64 + row, else up row I + mt*64 + row - 64)
+      float wsc = 1.f;
+      if constexpr (FP8) {
+        const int wr = EPI == EPI_SWIGLU ? (row < BM / 2 ? mt * (BM / 2) + row : a.I + mt * (BM / 2) + row - BM / 2) : m;
+        wsc = (EPI == EPI_SWIGLU || m < a.M) ? a.wscale[wr] : 0.f;
+      }
       if constexpr (!TOPK) {
         // pieces of tile t: CTAs g_first .. g_last share its chunks
         int g_first = blockIdx.x, g_last = blockIdx.x;
@@ -429,6 +501,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         auto finish = [&](float(&v)[16], int c0, const float* pre_old) {
           const int nb = nt * BN + c0;       // first column
           const int nj = min(16, a.N - nb);  // valid columns (may be <= 0)
+          if constexpr (FP8) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] *= wsc;
+          }
           if constexpr (EPI == EPI_PLAIN) {
             if (m < a.M && nj > 0) {
               float* p0 = a.out + (size_t)nb * a.M + m;
@@ -563,7 +639,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int j = 0; j < 16; ++j) old[j] = j < nj ? p0[(size_t)j * a.M] : 0.f;
               }
-              constexpr int PB = EPI == EPI_HEADS ? 4 : 8;  // pieces per round of loads (registers)
+              constexpr int PB = (EPI == EPI_HEADS || FP8) ? 4 : 8;  // pieces per round of loads (registers)
               for (int g0 = g_first; g0 <= g_last; g0 += PB) {
                 float v[PB][16];
 #pragma unroll
@@ -605,7 +681,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            float z = a.mult * v[j];
+            float z = a.mult * (FP8 ? wsc * v[j] : v[j]);
             if (a.cap > 0.f) z = a.cap * tanhf(z / a.cap);
             v[j] = z;
           }
@@ -703,6 +779,22 @@ int make_map(CUtensorMap* map, const void* base, int rows, int cols, int ld, int
   return r == CUDA_SUCCESS ? DFLASH2_OK : DFLASH2_ERR_CUDA;
 }
 
+// 2-D e4m3 tensor map over rows x cols bytes (row stride ld bytes), box of
+// 64 columns x box_rows rows, no swizzle (the converters read it row by row).
+int make_map8(CUtensorMap* map, const void* base, int rows, int cols, int ld, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return DFLASH2_ERR_CUDA;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || ld % 16) return DFLASH2_ERR_SHAPE;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+}
+
 // Activation rows per tile.  With very few weight tiles (M <= 512) the rows
 // are spread over 16-row tiles so the grid still fills the SMs; otherwise the
 // smallest MMA width that holds all rows (at most 256).
@@ -715,31 +807,37 @@ int pick_bn(int M, int N) {
   return 256;
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool FP8>
 int launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs& args, int grid, const Ctx& c) {
-  constexpr int smem = TcCfg<BN>::smem_bytes(EPI);
+  constexpr int smem = TcCfg<BN, FP8>::smem_bytes(EPI);
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(tc_gemm_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+    if (cudaFuncSetAttribute(tc_gemm_kernel<BN, EPI, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
       return DFLASH2_ERR_CUDA;
     attr_set = true;
   }
-  return launch_k(tc_gemm_kernel<BN, EPI>, dim3(grid), dim3(THREADS), smem, c, ma, mb, args);
+  return launch_k(tc_gemm_kernel<BN, EPI, FP8>, dim3(grid), dim3(threads_of(FP8)), smem, c, ma, mb, args);
+}
+
+template <int BN, bool FP8>
+int launch_epi(int epi, const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs& args, int grid, const Ctx& c) {
+  switch (epi) {
+    case EPI_TOPK: return launch_bn<BN, EPI_TOPK, FP8>(ma, mb, args, grid, c);
+    case EPI_SWIGLU:
+      if constexpr (BN <= 64) return launch_bn<BN, EPI_SWIGLU, FP8>(ma, mb, args, grid, c);
+      return DFLASH2_ERR_SHAPE;
+    case EPI_HEADS:
+      if constexpr (BN <= 64) return launch_bn<BN, EPI_HEADS, FP8>(ma, mb, args, grid, c);
+      return DFLASH2_ERR_SHAPE;
+    default: return launch_bn<BN, EPI_PLAIN, FP8>(ma, mb, args, grid, c);
+  }
 }
 
 template <int BN>
-int launch_epi(int epi, const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs& args, int grid, const Ctx& c) {
-  switch (epi) {
-    case EPI_TOPK: return launch_bn<BN, EPI_TOPK>(ma, mb, args, grid, c);
-    case EPI_SWIGLU:
-      if constexpr (BN <= 64) return launch_bn<BN, EPI_SWIGLU>(ma, mb, args, grid, c);
-      return DFLASH2_ERR_SHAPE;
-    case EPI_HEADS:
-      if constexpr (BN <= 64) return launch_bn<BN, EPI_HEADS>(ma, mb, args, grid, c);
-      return DFLASH2_ERR_SHAPE;
-    default: return launch_bn<BN, EPI_PLAIN>(ma, mb, args, grid, c);
-  }
+int launch_epi(int epi, bool fp8, const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs& args, int grid,
+               const Ctx& c) {
+  return fp8 ? launch_epi<BN, true>(epi, ma, mb, args, grid, c) : launch_epi<BN, false>(epi, ma, mb, args, grid, c);
 }
 
 }  // namespace
@@ -802,6 +900,7 @@ int gemm_bf16(const GemmOp& g, const Ctx& c) {
   a.mult = g.mult;
   a.cap = g.cap;
   a.status = c.status;
+  a.wscale = g.wscale;
   if (g.topk && a.n_tiles > 32) return DFLASH2_ERR_SHAPE;
   if (epi == EPI_SWIGLU) {
     if (!g.act) return DFLASH2_ERR_INVALID_ARG;
@@ -831,17 +930,19 @@ int gemm_bf16(const GemmOp& g, const Ctx& c) {
   }
 
   CUtensorMap ma, mb;
-  int rc = make_map(&ma, g.W, g.M, g.K, g.ldw, epi == EPI_SWIGLU ? BM / 2 : BM);
+  const bool fp8 = g.wscale != nullptr;
+  int rc = fp8 ? make_map8(&ma, g.W, g.M, g.K, g.ldw, epi == EPI_SWIGLU ? BM / 2 : BM)
+               : make_map(&ma, g.W, g.M, g.K, g.ldw, epi == EPI_SWIGLU ? BM / 2 : BM);
   if (rc) return rc;
   rc = make_map(&mb, g.X, g.N, g.K, g.ldx, bn);
   if (rc) return rc;
 
   switch (bn) {
-    case 16: return launch_epi<16>(epi, ma, mb, a, grid, c);
-    case 32: return launch_epi<32>(epi, ma, mb, a, grid, c);
-    case 64: return launch_epi<64>(epi, ma, mb, a, grid, c);
-    case 128: return launch_epi<128>(epi, ma, mb, a, grid, c);
-    default: return launch_epi<256>(epi, ma, mb, a, grid, c);
+    case 16: return launch_epi<16>(epi, fp8, ma, mb, a, grid, c);
+    case 32: return launch_epi<32>(epi, fp8, ma, mb, a, grid, c);
+    case 64: return launch_epi<64>(epi, fp8, ma, mb, a, grid, c);
+    case 128: return launch_epi<128>(epi, fp8, ma, mb, a, grid, c);
+    default: return launch_epi<256>(epi, fp8, ma, mb, a, grid, c);
   }
 }
 

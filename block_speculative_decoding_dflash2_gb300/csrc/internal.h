@@ -19,8 +19,9 @@ struct Ctx {
 // One dense contraction out[n][m] = sum_k W[m][k] * X[n][k]  (swap-AB: the
 // weight rows stream along the MMA M axis, the few activation rows form N).
 struct GemmOp {
-  const void* W;  // [M, K] row stride ldw elements
+  const void* W;  // [M, K] row stride ldw elements (bf16, or e4m3 bytes with wscale)
   int M, K, ldw;
+  const float* wscale;  // nullable [M]: W is fp8 e4m3 and row m is scaled by wscale[m]
   const void* X;  // [N, K] row stride ldx elements
   int N, ldx;
   // plain epilogue: out[n][m] fp32 (ld = M), stored or, with accumulate,
@@ -176,9 +177,12 @@ int launch_act(int dtype, const float* Y, int rows, int I, void* act, const Ctx&
 // whether the B rows fit its shared memory; otherwise the caller runs
 // rownorm + tap GEMM + dyn_conv.
 bool conv_prologue_fits(int dtype, int batch, int B, int H, int G, int nsm);
+// w_tap: [2G, H] of dtype, or (tap_scale != nullptr, bf16 activations) e4m3
+// codes whose row r is scaled by tap_scale[r].
 int launch_conv_prologue(int dtype, const float* h_in, const int32_t* anchor, int mask_id, const void* embed, int V,
-                         float scale, const void* gamma, float eps, const void* w_tap, int batch, int B, int H,
-                         int group_size, float* h_out, void* u_out, void* u2_out, const RopeTab& rt, const Ctx& c);
+                         float scale, const void* gamma, float eps, const void* w_tap, const float* tap_scale,
+                         int batch, int B, int H, int group_size, float* h_out, void* u_out, void* u2_out,
+                         const RopeTab& rt, const Ctx& c);
 
 // attention (attention.cu)
 int launch_attention(int dtype, const void* q, const void* kb, const void* vb, const void* kc, const void* vc,

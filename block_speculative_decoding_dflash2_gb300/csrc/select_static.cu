@@ -71,7 +71,10 @@ int dflash2_select_path_static(const dflash2_config* cfg, const dflash2_weights*
   if (!w || !w->embed || !w->sel) return DFLASH2_ERR_INVALID_ARG;
   if (batch <= 0) return DFLASH2_ERR_SHAPE;
   if (!anchor || !cand_id || !cand_logit || !path) return DFLASH2_ERR_INVALID_ARG;
-  const dflash2_config& c = *cfg;
+  const bool fp8 = cfg->dtype == DFLASH2_FP8W;
+  if (fp8 && (!w->scales || !w->scales->sel)) return DFLASH2_ERR_INVALID_ARG;
+  dflash2_config c = *cfg;
+  if (fp8) c.dtype = DFLASH2_BF16;  // bf16 embedding rows; e4m3 selector weights with row scales
   const int D = c.block_size - 1, k = c.top_k, r = c.selector_rank, H = c.hidden;
   const int es = c.dtype == DFLASH2_BF16 ? 2 : 4;
   const int nsel = batch * (D * k + 1);
@@ -104,6 +107,7 @@ int dflash2_select_path_static(const dflash2_config* cfg, const dflash2_weights*
   GemmOp g;
   std::memset(&g, 0, sizeof(g));
   g.W = w->sel;
+  g.wscale = fp8 ? w->scales->sel : nullptr;
   g.M = 2 * r;
   g.K = H;
   g.ldw = H;

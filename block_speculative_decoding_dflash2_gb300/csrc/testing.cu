@@ -38,8 +38,12 @@ size_t dflash2_test_gemm_workspace(int M, int N) {
   return al((size_t)kMaxSM * sizeof(int)) + al(gemm_partial_bytes(M, N));
 }
 
-int dflash2_test_gemm(int dtype, const void* W, int M, int K, const void* X, int N, int ctas, int accumulate,
-                      float* out, void* workspace, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int test_gemm(int dtype, const void* W, const float* wscale, int M, int K, const void* X, int N, int ctas,
+              int accumulate, float* out, void* workspace, size_t ws_bytes, void* stream) {
   if (dtype != DFLASH2_BF16 && dtype != DFLASH2_F32) return DFLASH2_ERR_DTYPE;
   if (!W || !X || !out || !workspace) return DFLASH2_ERR_INVALID_ARG;
   if (M <= 0 || N <= 0 || K <= 0) return DFLASH2_ERR_SHAPE;
@@ -50,6 +54,7 @@ int dflash2_test_gemm(int dtype, const void* W, int M, int K, const void* X, int
   GemmOp g;
   std::memset(&g, 0, sizeof(g));
   g.W = W;
+  g.wscale = wscale;
   g.M = M;
   g.K = K;
   g.ldw = K;
@@ -74,6 +79,21 @@ int dflash2_test_gemm(int dtype, const void* W, int M, int K, const void* X, int
   if (g.ctas < 0) return (int)std::min<long>(tiles, c.nsm);
   if (g.ctas > 0) return (int)std::min<long>(g.ctas, work);
   return (int)std::min<long>(std::max(1L, std::min<long>(c.nsm, work / 8)), work);
+}
+
+}  // namespace
+
+extern "C" {
+
+int dflash2_test_gemm(int dtype, const void* W, int M, int K, const void* X, int N, int ctas, int accumulate,
+                      float* out, void* workspace, size_t ws_bytes, void* stream) {
+  return test_gemm(dtype, W, nullptr, M, K, X, N, ctas, accumulate, out, workspace, ws_bytes, stream);
+}
+
+int dflash2_test_gemm_fp8(const void* W8, const float* scale, int M, int K, const void* X, int N, int ctas,
+                          int accumulate, float* out, void* workspace, size_t ws_bytes, void* stream) {
+  if (!scale) return DFLASH2_ERR_INVALID_ARG;
+  return test_gemm(DFLASH2_BF16, W8, scale, M, K, X, N, ctas, accumulate, out, workspace, ws_bytes, stream);
 }
 
 int dflash2_test_layout(const dflash2_config* cfg, int batch, int n_new, int max_ctx, size_t* offsets, int n) {

@@ -25,7 +25,7 @@ class DraftRunner:
         self.batch = batch
         self.device = device
         c = self.cfgd
-        self.dtype = torch.bfloat16 if self.cfg.dtype == B.BF16 else torch.float32
+        self.dtype = torch.float32 if self.cfg.dtype == B.F32 else torch.bfloat16  # activations and cache
         ps = c["page_size"]
         self.max_pages = -(-max_ctx // ps)
         if block_table is None:

@@ -45,7 +45,15 @@ WORKLOADS = {
                          n_kv_heads=8, head_dim=128, intermediate=17408,
                          vocab=151936, n_layers=1, block_size=16, top_k=16,
                          selector_rank=64, batch=8, context=8192),
+    # 30B-A3B-shaped throughput sweep: batch {1, 8, 64, 256} x context {1k, 8k}
+    # (config_of(..., batch=b, context=c)); the draft attention is sized on
+    # its own (32 q / 4 kv heads x 128), MLP 3H, groups of 32 channels
+    "a3b_30b_fp8": dict(_COMMON, index=4, dtype="fp8w", hidden=2688, n_q_heads=32,
+                        n_kv_heads=4, head_dim=128, intermediate=8064,
+                        vocab=131072, n_layers=2, block_size=7, top_k=16,
+                        selector_rank=32, batch=1, context=1024),
 }
+A3B_SWEEP = [(b, c) for b in (1, 8, 64, 256) for c in (1024, 8192)]
 
 
 def config_of(name, **over):
@@ -73,17 +81,66 @@ def bf16_bits_to_f32(bits):
 
 
 class Tensor:
-    """A drawn tensor: exact float32 values plus, for bf16, its bit patterns."""
+    """A drawn tensor: exact values plus its stored form: bf16 bit patterns,
+    or, for an fp8 matrix, e4m3 codes `q` with per-row float32 scales (then
+    `values` = decoded code * scale, exactly, in float64)."""
 
-    __slots__ = ("values", "bits")
+    __slots__ = ("values", "bits", "q", "scale")
 
-    def __init__(self, values, bits=None):
+    def __init__(self, values, bits=None, q=None, scale=None):
         self.values = values
         self.bits = bits
+        self.q = q
+        self.scale = scale
 
     @property
     def shape(self):
         return self.values.shape
+
+
+# ---------------------------------------------------------------------------
+# fp8 e4m3 weights (the format: 1 sign bit, 4 exponent bits with bias 7, 3
+# mantissa bits; exponent field 0 holds the subnormals m/8 * 2^-6; the
+# largest finite magnitude is 448; code 0x7f / 0xff is NaN, never produced)
+# ---------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+def e4m3_encode(x):
+    """float array -> e4m3 codes (uint8), round to nearest, ties to even;
+    magnitudes above 448 saturate to 448."""
+    x = np.asarray(x, dtype=np.float64)
+    sign = np.signbit(x).astype(np.uint8) << np.uint8(7)
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    e = np.clip(np.floor(np.log2(np.where(a > 0, a, 1.0))), -6, 8)
+    m = np.rint(a / np.exp2(e - 3))          # spacing 2^(e-3); exact quotient, half-even rounding
+    carry = m >= 16                          # rounded up to the next power of two
+    e = np.where(carry, e + 1, e)
+    m = np.where(carry, m / 2, m)
+    code = np.where(m >= 8, ((e + 7).astype(np.int64) << 3) | (m - 8).astype(np.int64), m.astype(np.int64))
+    return code.astype(np.uint8) | sign
+
+
+def e4m3_decode(q):
+    """e4m3 codes -> float64 values (NaN codes -> nan)."""
+    q = np.asarray(q, dtype=np.uint8).astype(np.int64)
+    s, e, m = (q >> 7) & 1, (q >> 3) & 15, q & 7
+    v = np.where(e == 0, m * 2.0 ** -9, (8 + m) * np.exp2(e.astype(np.float64) - 10))
+    v = np.where((e == 15) & (m == 7), np.nan, v)
+    return np.where(s == 1, -v, v)
+
+
+def quantize_rows_e4m3(w):
+    """Per-output-channel quantisation of a [rows, cols] matrix: scale =
+    max|row| / 448 (float32), q = e4m3(w / scale).  Returns a Tensor whose
+    values are the dequantised q * scale (float64, exact)."""
+    w = np.asarray(w, dtype=np.float32)
+    amax = np.max(np.abs(w), axis=1)
+    scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    q = e4m3_encode(w.astype(np.float64) / scale.astype(np.float64)[:, None])
+    values = e4m3_decode(q) * scale.astype(np.float64)[:, None]
+    return Tensor(values, q=q, scale=scale)
 
 
 def _rng(seed, name):
@@ -100,7 +157,7 @@ def _fill(out, bits, seed, name, lo, hi, std, mean, dtype):
         x *= np.float32(std)
     if mean != 0.0:
         x += np.float32(mean)
-    if dtype == "bf16":
+    if dtype in ("bf16", "fp8w"):
         b = to_bf16_bits(x)
         bits[lo:hi] = b
         out[lo:hi] = bf16_bits_to_f32(b)
@@ -113,7 +170,7 @@ def _draw(seed, name, shape, std, dtype, mean=0.0):
     elements, each from its own stream (seed, name#chunk), filled in parallel."""
     n = int(np.prod(shape))
     out = np.empty(n, dtype=np.float32)
-    bits = np.empty(n, dtype=np.uint16) if dtype == "bf16" else None
+    bits = np.empty(n, dtype=np.uint16) if dtype in ("bf16", "fp8w") else None
     bounds = [(lo, min(n, lo + _CHUNK)) for lo in range(0, n, _CHUNK)]
     if len(bounds) > 1:
         import concurrent.futures
@@ -127,35 +184,45 @@ def _draw(seed, name, shape, std, dtype, mean=0.0):
 
 
 def make_weights(cfg, seed=None):
-    """All draft weights of a workload, as a dict of Tensor (layers: list)."""
+    """All draft weights of a workload, as a dict of Tensor (layers: list).
+    With dtype "fp8w" the matrices other than the embedding are drawn in
+    float32 and quantised per output channel to e4m3 (quantize_rows_e4m3);
+    the embedding and the norm gains are bf16."""
     seed = 1000 + cfg["index"] if seed is None else seed
     dt = cfg["dtype"]
+    if dt == "fp8w":
+        def mat(name, shape):
+            return quantize_rows_e4m3(_draw(seed, name, shape, 0.02, "f32").values)
+        dt = "bf16"
+    else:
+        def mat(name, shape):
+            return _draw(seed, name, shape, 0.02, dt)
     H, V, T = cfg["hidden"], cfg["vocab"], cfg["n_taps"]
     nq, nkv, d, I = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"], cfg["intermediate"]
     G = H // cfg["conv_group_size"]
     kc, r = cfg["conv_kernel_size"], cfg["selector_rank"]
     w = {
         "embed": _draw(seed, "embed", (V, H), 0.02, dt),
-        "lm_head": _draw(seed, "lm_head", (V, H), 0.02, dt),
-        "fc": _draw(seed, "fc", (H, T * H), 0.02, dt),
+        "lm_head": mat("lm_head", (V, H)),
+        "fc": mat("fc", (H, T * H)),
         "hidden_norm": _draw(seed, "hidden_norm", (H,), 0.1, dt, 1.0),
         "final_norm": _draw(seed, "final_norm", (H,), 0.1, dt, 1.0),
-        "sel": _draw(seed, "sel", (2 * r, H), 0.02, dt),
+        "sel": mat("sel", (2 * r, H)),
         "layers": [],
     }
     for l in range(cfg["n_layers"]):
         p = f"layer{l}."
         w["layers"].append({
             "attn_norm": _draw(seed, p + "attn_norm", (H,), 0.1, dt, 1.0),
-            "tapgen_attn": _draw(seed, p + "tapgen_attn", (kc * G, H), 0.02, dt),
-            "qkv": _draw(seed, p + "qkv", ((nq + 2 * nkv) * d, H), 0.02, dt),
+            "tapgen_attn": mat(p + "tapgen_attn", (kc * G, H)),
+            "qkv": mat(p + "qkv", ((nq + 2 * nkv) * d, H)),
             "q_norm": _draw(seed, p + "q_norm", (d,), 0.1, dt, 1.0),
             "k_norm": _draw(seed, p + "k_norm", (d,), 0.1, dt, 1.0),
-            "o": _draw(seed, p + "o", (H, nq * d), 0.02, dt),
+            "o": mat(p + "o", (H, nq * d)),
             "mlp_norm": _draw(seed, p + "mlp_norm", (H,), 0.1, dt, 1.0),
-            "tapgen_mlp": _draw(seed, p + "tapgen_mlp", (kc * G, H), 0.02, dt),
-            "gate_up": _draw(seed, p + "gate_up", (2 * I, H), 0.02, dt),
-            "down": _draw(seed, p + "down", (H, I), 0.02, dt),
+            "tapgen_mlp": mat(p + "tapgen_mlp", (kc * G, H)),
+            "gate_up": mat(p + "gate_up", (2 * I, H)),
+            "down": mat(p + "down", (H, I)),
         })
     return w
 
@@ -172,7 +239,7 @@ def make_taps(cfg, n_rows, seed=None, stream="taps"):
     seed = 1000 + cfg["index"] if seed is None else seed
     x = _rng(seed, stream).standard_normal(size=(n_rows, cfg["n_taps"] * cfg["hidden"]),
                                            dtype=np.float32)
-    if cfg["dtype"] == "bf16":
+    if cfg["dtype"] != "f32":  # bf16 activations (also with fp8 weights)
         x /= np.sqrt(np.mean(x.astype(np.float64) ** 2, axis=1, keepdims=True)).astype(np.float32)
         bits = to_bf16_bits(x)
         return Tensor(bf16_bits_to_f32(bits), bits)
@@ -231,17 +298,26 @@ def paged_layout(ctx_cap, page_size, batch, seed, spare_pages=0):
 # ---------------------------------------------------------------------------
 
 def to_torch(t, device="cuda"):
-    """Tensor -> torch tensor on `device` (bf16 from its bit patterns)."""
+    """Tensor -> torch tensor on `device` (bf16 from its bit patterns; an fp8
+    matrix as its uint8 e4m3 codes)."""
     import torch
+    if t.q is not None:
+        return torch.from_numpy(np.ascontiguousarray(t.q)).to(device)
     if t.bits is not None:
         return torch.from_numpy(t.bits.view(np.int16)).to(device).view(torch.bfloat16)
     return torch.from_numpy(np.ascontiguousarray(t.values)).to(device)
 
 
 def device_weights(w, device="cuda"):
-    """Weight dict of Tensor -> weight dict of torch device tensors."""
+    """Weight dict of Tensor -> weight dict of torch device tensors; with fp8
+    matrices, also "scales": their per-row float32 scales in the same nesting."""
+    import torch
     out = {k: to_torch(v, device) for k, v in w.items() if k != "layers"}
     out["layers"] = [{k: to_torch(v, device) for k, v in L.items()} for L in w["layers"]]
+    if w["lm_head"].q is not None:
+        sc = lambda t: torch.from_numpy(t.scale).to(device)
+        out["scales"] = {k: sc(w[k]) for k in ("lm_head", "fc", "sel")}
+        out["scales"]["layers"] = [{k: sc(v) for k, v in L.items() if v.q is not None} for L in w["layers"]]
     return out
 
 

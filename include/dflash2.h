@@ -71,6 +71,11 @@ extern "C" {
 /* ---------------------------------------------------------------- types */
 #define DFLASH2_F32   0  /* float32 weights, activations and cache */
 #define DFLASH2_BF16  1  /* bfloat16 weights, activations and cache; fp32 accumulation */
+#define DFLASH2_FP8W  2  /* fp8 e4m3 linear weights with fp32 per-output-channel scales
+                            (dflash2_scales); bfloat16 embed, norm gains, activations and
+                            cache; fp32 accumulation.  A weight element is q * scale[row]:
+                            the contractions run on the exact bf16 value of q and apply
+                            the row's scale to the fp32 result. */
 
 /*
  * Draft model configuration ("Key Config Fields"; dflash_config of
@@ -89,7 +94,7 @@ extern "C" {
  *   selector_rank          r, 1..128
  *   page_size              context KV page length (tokens per page)
  *   mask_token_id          token filling block slots 1..B-1 ("Data" note)
- *   dtype                  DFLASH2_F32 or DFLASH2_BF16
+ *   dtype                  DFLASH2_F32, DFLASH2_BF16 or DFLASH2_FP8W
  *   rms_eps                RMSNorm epsilon
  *   rope_theta             rotary base
  *   input_embedding_scale  multiplies the embedded block (1 = identity)
@@ -105,7 +110,8 @@ typedef struct dflash2_config {
 } dflash2_config;
 
 /*
- * Weights of one draft layer (device pointers, element type = cfg.dtype).
+ * Weights of one draft layer (device pointers, element type = cfg.dtype;
+ * with DFLASH2_FP8W the matrices are e4m3 bytes and the norm gains bf16).
  * G = hidden / conv_group_size.  Matrices are [out_features, in_features].
  *   attn_norm    [H]                      RMSNorm gain before attention
  *   tapgen_attn  [2G, H]                  conv tap generator, row 2g+j = tap j of group g
@@ -125,6 +131,21 @@ typedef struct dflash2_layer_weights {
 } dflash2_layer_weights;
 
 /*
+ * DFLASH2_FP8W only: the fp32 per-output-channel scales of the e4m3 matrices
+ * (device pointers; one float per matrix row, in the row order of the
+ * matrix: qkv scales are q rows, then k rows, then v rows).
+ */
+typedef struct dflash2_layer_scales {
+    const float *tapgen_attn, *qkv, *o, *tapgen_mlp, *gate_up, *down;
+} dflash2_layer_scales;
+
+/* `layers` is a HOST array of n_layers entries. */
+typedef struct dflash2_scales {
+    const float *lm_head, *fc, *sel;
+    const dflash2_layer_scales *layers;
+} dflash2_scales;
+
+/*
  * All draft weights.  Host struct of device pointers; `layers` is a HOST
  * array of n_layers entries.
  *   embed        [V, H]     the target's frozen embed_tokens (shared)
@@ -134,10 +155,13 @@ typedef struct dflash2_layer_weights {
  *   final_norm   [H]        RMSNorm gain before the lm_head
  *   sel          [2r, H]    selector factors: rows 0..r-1 = W_a (predecessor),
  *                           rows r..2r-1 = W_b (candidate)
+ * With DFLASH2_FP8W, lm_head, fc, sel and the layer matrices are e4m3 bytes
+ * with the row scales of `scales`; embed and the norm gains are bf16.
  */
 typedef struct dflash2_weights {
     const void *embed, *lm_head, *fc, *hidden_norm, *final_norm, *sel;
     const dflash2_layer_weights *layers;
+    const dflash2_scales *scales;  /* host pointer; DFLASH2_FP8W only (NULL otherwise) */
 } dflash2_weights;
 
 /*

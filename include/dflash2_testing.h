@@ -37,6 +37,15 @@ int dflash2_test_gemm(int dtype, const void *W, int M, int K, const void *X, int
                       float *out, void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * The same contraction with fp8 e4m3 weights (the DFLASH2_FP8W path):
+ * out[n][m] = scale[m] * sum_k e4m3(W8[m][k]) * X[n][k], X bf16 [N, K],
+ * W8 [M, K] bytes (K a multiple of 16), scale float [M].  Same schedule,
+ * workspace and return value as dflash2_test_gemm.
+ */
+int dflash2_test_gemm_fp8(const void *W8, const float *scale, int M, int K, const void *X, int N, int ctas,
+                          int accumulate, float *out, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Byte offsets, inside the workspace of a dflash2_draft_step call with these
  * sizes (max_ctx = max_pages * page_size), of the intermediates that call
  * leaves behind, in this order:

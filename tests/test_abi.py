@@ -39,10 +39,12 @@ def test_every_declared_symbol_is_exported(B):
 
 
 def test_struct_sizes_match_header(B):
-    # 16 ints + 5 floats; 10 and 6+1 pointers
+    # 16 ints + 5 floats; 10 and 6+1+1 pointers; fp8 scales: 6 and 3+1
     assert ctypes.sizeof(B.Config) == 21 * 4
     assert ctypes.sizeof(B.LayerWeights) == 10 * 8
-    assert ctypes.sizeof(B.Weights) == 7 * 8
+    assert ctypes.sizeof(B.Weights) == 8 * 8
+    assert ctypes.sizeof(B.LayerScales) == 6 * 8
+    assert ctypes.sizeof(B.Scales) == 4 * 8
 
 
 def _cfg(B, name, **over):
@@ -50,7 +52,7 @@ def _cfg(B, name, **over):
     return B.make_config(S.config_of(name, **over))
 
 
-@pytest.mark.parametrize("name", ["tiny_fp32", "qwen3_8b_b1", "qwen3_8b_b32_paged", "qwen3_27b_b8"])
+@pytest.mark.parametrize("name", ["tiny_fp32", "qwen3_8b_b1", "qwen3_8b_b32_paged", "qwen3_27b_b8", "a3b_30b_fp8"])
 def test_workload_configs_validate(B, name):
     assert B.dflash2_validate_config(_cfg(B, name)) == 0
 
@@ -98,6 +100,26 @@ def test_counter_regions_do_not_move_between_calls(B, name):
     assert len(seen) == 1
     cnt, cnta = seen.pop()
     assert cnt < cnta and cnta - cnt >= 128 * 4
+
+
+def test_fp8_weights_need_their_scales(B):
+    # fp8 configs: the bf16-activation workspace, and weights without row
+    # scales are refused before any CUDA call
+    L = B.lib()
+    c8 = _cfg(B, "a3b_30b_fp8")
+    cb = _cfg(B, "a3b_30b_fp8", dtype="bf16")
+    assert B.dflash2_workspace_size(c8, 8, 56, 1024) == B.dflash2_workspace_size(cb, 8, 56, 1024) > 0
+    w = B.Weights()
+    for f in ("embed", "lm_head", "fc", "hidden_norm", "final_norm", "sel"):
+        setattr(w, f, 16)
+    layers = (B.LayerWeights * 2)()
+    for l in range(2):
+        for f in B._LAYER_FIELDS:
+            setattr(layers[l], f, 16)
+    w.layers = ctypes.cast(layers, ctypes.POINTER(B.LayerWeights))
+    assert L.dflash2_draft_step(ctypes.byref(c8), ctypes.byref(w), 1, 1, 1, 1, 1, 1, 1, 0, None, 1, 1, 1, 1,
+                                None, 1, 1 << 30, None) == -1
+    assert L.dflash2_build_selector_table(ctypes.byref(c8), ctypes.byref(w), 16, None) == -1
 
 
 def test_host_side_error_paths_return_before_cuda(B):

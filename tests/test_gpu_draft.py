@@ -118,7 +118,7 @@ def test_device_guards_flag_bad_page_and_token():
 
 
 @pytest.mark.parametrize("name,kind", [("tiny_fp32", "gemm"), ("small_bf16", "gemm"), ("small_bf16", "table"),
-                                       ("tiny_fp32", "table")])
+                                       ("tiny_fp32", "table"), ("small_fp8", "table")])
 def test_lossless_speculative_loop(name, kind):
     """Draft -> select -> verify on the GPU against a toy greedy target: the
     emitted tokens equal plain greedy decoding, and every step's path equals
@@ -126,7 +126,8 @@ def test_lossless_speculative_loop(name, kind):
     import torch
     B = lib()
     from block_speculative_decoding_dflash2_gb300.runner import DraftRunner
-    cfg = S.config_of("tiny_fp32") if name == "tiny_fp32" else S.small_bf16_config(batch=1, index=14)
+    cfg = (S.config_of("tiny_fp32") if name == "tiny_fp32" else
+           S.small_bf16_config(batch=1, index=14, dtype="fp8w" if name == "small_fp8" else "bf16"))
     V, Bsz = cfg["vocab"], cfg["block_size"]
     D = Bsz - 1
     g = np.random.default_rng(5)
@@ -141,7 +142,7 @@ def test_lossless_speculative_loop(name, kind):
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(np.asarray(a, dtype=np.int32))).cuda()
     tt = S.to_torch(taps)
     r.append(dev([0]), tt[:prompt].contiguous(), dev([0, prompt]))
-    st = O.Store(cfg["dtype"] == "bf16")
+    st = O.Store(cfg["dtype"] != "f32")
     last = int(g.integers(0, V - 1))
     greedy = O.greedy_generate(table, last, n_tok)
     out = [int(table[last])]

@@ -56,6 +56,58 @@ def test_bf16_gemm_matches_float64_product(M, N, K, ctas, accumulate):
         assert int(ws[:4 * 256].view(torch.int32).abs().sum()) == 0
 
 
+@pytest.mark.parametrize("M,N,K,ctas", [
+    (128, 16, 64, 0),        # one tile, one K chunk
+    (1000, 7, 512, 5),       # ragged M tile, pieces across tiles
+    (384, 70, 1024, -1),     # 128-wide activation tile, whole tiles
+    (2688, 7, 8064, 0),      # the 30B-A3B down / feature projection shape
+    (5120, 14, 2688, 0),     # the 30B-A3B QKV shape with appended rows
+])
+@pytest.mark.parametrize("accumulate", [False, True])
+def test_fp8_gemm_matches_dequantised_product(M, N, K, ctas, accumulate):
+    """e4m3 weights with per-row scales against the float64 product of the
+    dequantised weights (the converters' e4m3 -> bf16 step is exact, so the
+    error is fp32 accumulation and the final scaling only)."""
+    import torch
+    B = lib()
+    W = S.quantize_rows_e4m3(_mat(M, K, 11, 0.05, "f32").values)
+    X = _mat(N, K, 12, 1.0, "bf16")
+    base = np.random.default_rng(13).standard_normal((N, M)).astype(np.float32)
+    out = torch.from_numpy(base).cuda() if accumulate else torch.full((N, M), float("nan"), device="cuda")
+    ws = torch.zeros(B.dflash2_test_gemm_workspace(M, N), dtype=torch.uint8, device="cuda")
+    used = B.dflash2_test_gemm_fp8(torch.from_numpy(W.q).cuda(), torch.from_numpy(W.scale).cuda(), S.to_torch(X),
+                                   ctas, out, ws, accumulate)
+    torch.cuda.synchronize()
+    assert 1 <= used <= 256
+    got = out.double().cpu().numpy() - (base if accumulate else 0.0)
+    x64 = X.values.astype(np.float64)
+    ref = x64 @ W.values.T
+    bound = np.abs(x64) @ np.abs(W.values).T + (np.abs(base) if accumulate else 0.0)
+    err = np.abs(got - ref)
+    assert np.all(np.isfinite(got))
+    assert np.all(err <= 1e-4 * bound + 1e-6), float(np.max(err / (bound + 1e-30)))
+    assert int(ws[:4 * 256].view(torch.int32).abs().sum()) == 0
+
+
+def test_fp8_gemm_reads_every_code_exactly():
+    """Every finite e4m3 code through the converters: W8 row m holds the 256
+    codes (NaN codes replaced by 0) shifted by m, X = one-hot rows, scale 1,
+    so out[n][m] is the decoded code itself, bit for bit."""
+    import torch
+    B = lib()
+    M, K = 128, 256
+    codes = (np.arange(K)[None, :] + np.arange(M)[:, None]) % 256
+    codes = np.where((codes & 0x7F) == 0x7F, 0, codes).astype(np.uint8)
+    X = np.zeros((K, K), dtype=np.float32)
+    X[np.arange(K), np.arange(K)] = 1.0
+    Xb = torch.from_numpy(S.to_bf16_bits(X).view(np.int16)).cuda().view(torch.bfloat16)
+    out = torch.full((K, M), float("nan"), device="cuda")
+    ws = torch.zeros(B.dflash2_test_gemm_workspace(M, K), dtype=torch.uint8, device="cuda")
+    B.dflash2_test_gemm_fp8(torch.from_numpy(codes).cuda(), torch.ones(M, device="cuda"), Xb, -1, out, ws)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out.cpu().numpy(), S.e4m3_decode(codes).T.astype(np.float32))
+
+
 def test_bf16_gemm_is_deterministic():
     # pieces of shared tiles are summed in CTA order: bit-identical reruns
     import torch

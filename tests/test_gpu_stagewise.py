@@ -34,6 +34,7 @@ def check_ulps(name, gpu, ref, max_ulp, frac_over_1=0.01, slack=None):
     """At most max_ulp everywhere (or, where `slack` is given, an absolute
     error within slack plus one ulp), and at most frac_over_1 of the
     elements beyond 1 ulp."""
+    assert np.all(np.isfinite(gpu)) and np.all(np.isfinite(ref)), (name, "non-finite values")
     u = ulps(gpu, ref)
     over = float(np.mean(u > 1.0 + 1e-9))
     bad = u > max_ulp
@@ -52,7 +53,7 @@ class Reader:
         r = case.runner
         self.torch = torch
         self.ws = r.workspace
-        self.bf16 = case.cfg["dtype"] == "bf16"
+        self.bf16 = case.cfg["dtype"] != "f32"
         self.off = B.dflash2_test_layout(r.cfg, case.b, int(case.n_new.sum()),
                                          r.max_pages * case.cfg["page_size"])
 
@@ -82,7 +83,7 @@ def run_stagewise(case):
     assert cfg["n_layers"] == 1
     Wv = case.Wv
     Wl = Wv["layers"][0]
-    st = O.Store(cfg["dtype"] == "bf16")
+    st = O.Store(cfg["dtype"] != "f32")
     H, B_, nq, nkv, d, I = (cfg["hidden"], cfg["block_size"], cfg["n_q_heads"], cfg["n_kv_heads"],
                             cfg["head_dim"], cfg["intermediate"])
     D, b, eps = B_ - 1, case.b, cfg["rms_eps"]

@@ -112,6 +112,12 @@ def lib():
         L.dflash2_build_selector_table.argtypes = [F(Config), F(Weights), P, P]
         L.dflash2_select_path_table.restype = I
         L.dflash2_select_path_table.argtypes = [F(Config), I, P, P, P, P, P, P, P, P]
+        L.dflash2_select_path_table_ex.restype = I
+        L.dflash2_select_path_table_ex.argtypes = [F(Config), I, P, P, P, P, F(DraftOpts), P, P, P, P, P]
+        L.dflash2_select_path_ex.restype = I
+        L.dflash2_select_path_ex.argtypes = [F(Config), F(Weights), I, P, P, P, F(DraftOpts), P, P, P, P, S, P]
+        L.dflash2_verify_accept_ex.restype = I
+        L.dflash2_verify_accept_ex.argtypes = [I, I, P, P, P, P, P, P, P, P, P, P]
         L.dflash2_test_layout.restype = I
         L.dflash2_test_layout.argtypes = [F(Config), I, I, I, F(ctypes.c_size_t), I]
         L.dflash2_launch_count.restype = ctypes.c_int64
@@ -157,6 +163,10 @@ def make_config(d):
             v = {"f32": F32, "bf16": BF16, "fp8w": FP8W}[v]
         setattr(c, name, v)
     return c
+
+
+class DraftOpts(ctypes.Structure):
+    _fields_ = [("n_max", ctypes.c_int), ("p_min", ctypes.c_float)]
 
 
 class WeightSet:
@@ -240,6 +250,32 @@ def dflash2_select_path_table(cfg, batch, anchor, cand_id, cand_logit, table, pa
     return _check("dflash2_select_path_table", lib().dflash2_select_path_table(
         ctypes.byref(cfg), batch, _ptr(anchor), _ptr(cand_id), _ptr(cand_logit), _ptr(table), _ptr(path),
         _ptr(path_score), _ptr(workspace), _stream(stream)))
+
+
+def _opts(n_max, p_min):
+    return ctypes.byref(DraftOpts(int(n_max), float(p_min)))
+
+
+def dflash2_select_path_ex(cfg, w, batch, anchor, cand_id, cand_logit, n_max, p_min, path, path_score, n_draft,
+                           workspace, stream=None):
+    return _check("dflash2_select_path_ex", lib().dflash2_select_path_ex(
+        ctypes.byref(cfg), ctypes.byref(w.struct), batch, _ptr(anchor), _ptr(cand_id), _ptr(cand_logit),
+        _opts(n_max, p_min), _ptr(path), _ptr(path_score), _ptr(n_draft), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def dflash2_select_path_table_ex(cfg, batch, anchor, cand_id, cand_logit, table, n_max, p_min, path, path_score,
+                                 n_draft, workspace=None, stream=None):
+    return _check("dflash2_select_path_table_ex", lib().dflash2_select_path_table_ex(
+        ctypes.byref(cfg), batch, _ptr(anchor), _ptr(cand_id), _ptr(cand_logit), _ptr(table), _opts(n_max, p_min),
+        _ptr(path), _ptr(path_score), _ptr(n_draft), _ptr(workspace), _stream(stream)))
+
+
+def dflash2_verify_accept_ex(batch, block_size, path, n_draft, target, accept_len, out_tok, n_out, next_anchor,
+                             seq_len=None, counters=None, stream=None):
+    return _check("dflash2_verify_accept_ex", lib().dflash2_verify_accept_ex(
+        batch, block_size, _ptr(path), _ptr(n_draft), _ptr(target), _ptr(accept_len), _ptr(out_tok), _ptr(n_out),
+        _ptr(next_anchor), _ptr(seq_len), _ptr(counters), _stream(stream)))
 
 
 def dflash2_verify_accept(batch, block_size, path, target, accept_len, out_tok, n_out, next_anchor,

@@ -710,9 +710,10 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
   return DFLASH2_OK;
 }
 
-int dflash2_select_path(const dflash2_config* cfg, const dflash2_weights* w, int batch, const int32_t* anchor,
-                        const int32_t* cand_id, const float* cand_logit, int32_t* path, float* path_score,
-                        void* workspace, size_t ws_bytes, void* stream) {
+int dflash2_select_path_ex(const dflash2_config* cfg, const dflash2_weights* w, int batch, const int32_t* anchor,
+                           const int32_t* cand_id, const float* cand_logit, const dflash2_draft_opts* opts,
+                           int32_t* path, float* path_score, int32_t* n_draft, void* workspace, size_t ws_bytes,
+                           void* stream) {
   TRY(check_config(cfg));
   if (!w || !w->embed || !w->sel) return DFLASH2_ERR_INVALID_ARG;
   if (batch <= 0) return DFLASH2_ERR_SHAPE;
@@ -730,7 +731,15 @@ int dflash2_select_path(const dflash2_config* cfg, const dflash2_weights* w, int
   float* Y = at<float>(workspace, L.Y);
   TRY(launch_sel_gather(c.dtype, anchor, cand_id, batch, D, k, w->embed, c.vocab, H, x, ctx));
   TRY(gemm(c, ctx, workspace, L, w->sel, 2 * r, H, x, batch * (D * k + 1), Y, false, false, sc.sel));
-  return launch_viterbi(Y, nullptr, anchor, c.vocab, cand_id, cand_logit, batch, D, k, r, path, path_score, ctx);
+  return launch_viterbi(Y, nullptr, anchor, c.vocab, cand_id, cand_logit, batch, D, k, r, path, path_score, ctx,
+                        opts ? opts->n_max : 0, opts ? opts->p_min : 0.f, n_draft);
+}
+
+int dflash2_select_path(const dflash2_config* cfg, const dflash2_weights* w, int batch, const int32_t* anchor,
+                        const int32_t* cand_id, const float* cand_logit, int32_t* path, float* path_score,
+                        void* workspace, size_t ws_bytes, void* stream) {
+  return dflash2_select_path_ex(cfg, w, batch, anchor, cand_id, cand_logit, nullptr, path, path_score, nullptr,
+                                workspace, ws_bytes, stream);
 }
 
 size_t dflash2_selector_table_bytes(const dflash2_config* cfg) {
@@ -754,9 +763,10 @@ int dflash2_build_selector_table(const dflash2_config* cfg, const dflash2_weight
   return gemm_f32(g, ctx);
 }
 
-int dflash2_select_path_table(const dflash2_config* cfg, int batch, const int32_t* anchor, const int32_t* cand_id,
-                              const float* cand_logit, const float* table, int32_t* path, float* path_score,
-                              void* workspace, void* stream) {
+int dflash2_select_path_table_ex(const dflash2_config* cfg, int batch, const int32_t* anchor,
+                                 const int32_t* cand_id, const float* cand_logit, const float* table,
+                                 const dflash2_draft_opts* opts, int32_t* path, float* path_score, int32_t* n_draft,
+                                 void* workspace, void* stream) {
   TRY(check_config(cfg));
   if (batch <= 0) return DFLASH2_ERR_SHAPE;
   if (!anchor || !cand_id || !cand_logit || !table || !path) return DFLASH2_ERR_INVALID_ARG;
@@ -764,7 +774,15 @@ int dflash2_select_path_table(const dflash2_config* cfg, int batch, const int32_
   TRY(device_ctx(&ctx, stream, workspace));
   const dflash2_config& c = *cfg;
   return launch_viterbi(nullptr, table, anchor, c.vocab, cand_id, cand_logit, batch, c.block_size - 1, c.top_k,
-                        c.selector_rank, path, path_score, ctx);
+                        c.selector_rank, path, path_score, ctx, opts ? opts->n_max : 0, opts ? opts->p_min : 0.f,
+                        n_draft);
+}
+
+int dflash2_select_path_table(const dflash2_config* cfg, int batch, const int32_t* anchor, const int32_t* cand_id,
+                              const float* cand_logit, const float* table, int32_t* path, float* path_score,
+                              void* workspace, void* stream) {
+  return dflash2_select_path_table_ex(cfg, batch, anchor, cand_id, cand_logit, table, nullptr, path, path_score,
+                                      nullptr, workspace, stream);
 }
 
 int dflash2_verify_accept(int batch, int block_size, const int32_t* path, const int32_t* target,
@@ -773,8 +791,18 @@ int dflash2_verify_accept(int batch, int block_size, const int32_t* path, const 
   if (block_size < 2 || block_size > 32) return DFLASH2_ERR_BLOCK_SIZE;
   if (batch <= 0) return DFLASH2_ERR_SHAPE;
   if (!path || !target || !accept_len || !out_tok || !n_out || !next_anchor) return DFLASH2_ERR_INVALID_ARG;
-  return launch_verify(batch, block_size, path, target, accept_len, out_tok, n_out, next_anchor, seq_len, counters,
-                       static_cast<cudaStream_t>(stream));
+  return launch_verify(batch, block_size, path, nullptr, target, accept_len, out_tok, n_out, next_anchor, seq_len,
+                       counters, static_cast<cudaStream_t>(stream));
+}
+
+int dflash2_verify_accept_ex(int batch, int block_size, const int32_t* path, const int32_t* n_draft,
+                             const int32_t* target, int32_t* accept_len, int32_t* out_tok, int32_t* n_out,
+                             int32_t* next_anchor, int32_t* seq_len, int64_t* counters, void* stream) {
+  if (block_size < 2 || block_size > 32) return DFLASH2_ERR_BLOCK_SIZE;
+  if (batch <= 0) return DFLASH2_ERR_SHAPE;
+  if (!path || !target || !accept_len || !out_tok || !n_out || !next_anchor) return DFLASH2_ERR_INVALID_ARG;
+  return launch_verify(batch, block_size, path, n_draft, target, accept_len, out_tok, n_out, next_anchor, seq_len,
+                       counters, static_cast<cudaStream_t>(stream));
 }
 
 int dflash2_read_device_status(void* workspace, size_t ws_bytes, void* stream) {

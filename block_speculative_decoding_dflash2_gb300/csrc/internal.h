@@ -203,12 +203,16 @@ int launch_sel_gather(int dtype, const int32_t* anchor, const int32_t* cand_id, 
                       const void* embed, int V, int H, void* x_out, const Ctx& c);
 // Y: per-step factors [batch][D*k+1][2r]; or Y null and table [V][2r]
 // (factors of every token, gathered by the kernel).
+// Drafting knobs: the walk covers positions 1..n_max (<= D) and the path is
+// cut before the first chosen transition with probability < p_min; n_draft
+// (nullable) receives the drafts kept.  launch_viterbi = n_max D, no cut.
 int launch_viterbi(const float* Y, const float* table, const int32_t* anchor, int V, const int32_t* cand_id,
                    const float* cand_logit, int batch, int D, int k, int r, int32_t* path, float* path_score,
-                   const Ctx& c);
+                   const Ctx& c, int n_max = 0, float p_min = 0.f, int32_t* n_draft = nullptr);
 size_t viterbi_smem_bytes(int D, int k, int r);
-int launch_verify(int batch, int B, const int32_t* path, const int32_t* target, int32_t* accept_len,
-                  int32_t* out_tok, int32_t* n_out, int32_t* next_anchor, int32_t* seq_len, int64_t* counters,
-                  cudaStream_t st);
+// n_draft: nullable [batch] drafts kept per sequence (B-1 when null).
+int launch_verify(int batch, int B, const int32_t* path, const int32_t* n_draft, const int32_t* target,
+                  int32_t* accept_len, int32_t* out_tok, int32_t* n_out, int32_t* next_anchor, int32_t* seq_len,
+                  int64_t* counters, cudaStream_t st);
 
 }  // namespace df2

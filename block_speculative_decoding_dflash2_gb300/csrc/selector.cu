@@ -59,7 +59,8 @@ __global__ void __launch_bounds__(512) viterbi_kernel(const float* __restrict__ 
                                                       const int32_t* __restrict__ cand_id,
                                                       const float* __restrict__ cand_logit, int D, int k, int r,
                                                       int32_t* __restrict__ path, float* __restrict__ path_score,
-                                                      unsigned* status) {
+                                                      unsigned* status, int Dp, float log_p_min,
+                                                      int32_t* __restrict__ n_draft) {
   extern __shared__ __align__(16) float sm[];
   __shared__ int tok0;
   pdl_launch_next();
@@ -254,10 +255,12 @@ __global__ void __launch_bounds__(512) viterbi_kernel(const float* __restrict__ 
   // 3. the max-plus recurrence over positions and the backtrack, in one warp:
   //    lane j holds delta[j]; ties keep the smaller predecessor (strict >,
   //    predecessors in ascending order) and, at the end, the smaller index
+  //    over the first Dp positions (draft_n_max), then the cut at the first
+  //    chosen transition whose log-probability is below log(p_min)
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     float dl = lane < k ? Sm[lane] : -INFINITY;
-    for (int i = 1; i < D; ++i) {
+    for (int i = 1; i < Dp; ++i) {
       const float* T = Sm + (1 + (i - 1) * k) * k;  // [p][j]
       float best = -INFINITY;
       int arg = 0;
@@ -284,12 +287,25 @@ __global__ void __launch_bounds__(512) viterbi_kernel(const float* __restrict__ 
       }
     }
     if (lane == 0) {
-      if (path_score) path_score[s] = vb;
+      int js[32];
       int j = jb;
-      for (int i = D - 1; i >= 0; --i) {
-        path[(size_t)s * D + i] = cid[i * k + j];
+      for (int i = Dp - 1; i >= 0; --i) {
+        js[i] = j;
         if (i > 0) j = bp[i * k + j];
       }
+      // kept drafts: the walk stops before the first transition below p_min
+      int n = 0;
+      float score = 0.f;
+      while (n < Dp) {
+        const float t = Sm[(n == 0 ? 0 : 1 + (n - 1) * k + js[n - 1]) * k + js[n]];
+        if (t < log_p_min) break;
+        score += t;
+        ++n;
+      }
+      if (log_p_min == -INFINITY) score = vb;  // no cut: the recurrence's own maximum
+      for (int i = 0; i < D; ++i) path[(size_t)s * D + i] = i < n ? cid[i * k + js[i]] : -1;
+      if (path_score) path_score[s] = score;
+      if (n_draft) n_draft[s] = n;
     }
   }
 }
@@ -314,8 +330,11 @@ int launch_sel_gather(int dtype, const int32_t* anchor, const int32_t* cand_id, 
 
 int launch_viterbi(const float* Y, const float* table, const int32_t* anchor, int V, const int32_t* cand_id,
                    const float* cand_logit, int batch, int D, int k, int r, int32_t* path, float* path_score,
-                   const Ctx& c) {
+                   const Ctx& c, int n_max, float p_min, int32_t* n_draft) {
   if ((Y == nullptr) == (table == nullptr)) return DFLASH2_ERR_INVALID_ARG;
+  if (n_max < 0 || n_max > D || !(p_min >= 0.f) || p_min > 1.f) return DFLASH2_ERR_SHAPE;
+  const int Dp = n_max == 0 ? D : n_max;
+  const float log_p_min = p_min > 0.f ? logf(p_min) : -INFINITY;
   const size_t smem = viterbi_smem_bytes(D, k, r);
   static bool attr = false;
   if (!attr) {
@@ -324,7 +343,7 @@ int launch_viterbi(const float* Y, const float* table, const int32_t* anchor, in
     attr = true;
   }
   return launch_k(viterbi_kernel, dim3(batch), dim3(512), smem, c, Y, table, anchor, V, cand_id, cand_logit, D, k, r,
-                  path, path_score, c.status);
+                  path, path_score, c.status, Dp, log_p_min, n_draft);
 }
 
 }  // namespace df2

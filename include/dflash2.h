@@ -328,6 +328,38 @@ int dflash2_select_path_table(const dflash2_config *cfg, int batch, const int32_
                               int32_t *path, float *path_score, void *workspace, void *stream);
 
 /*
+ * Drafting knobs ("DFlash2 Speculative Decoding" (llama-cpp-python wiki),
+ * "Configuration Notes": draft_n_max bounds the tokens drafted per step;
+ * drafting stops early at a low-confidence selector transition,
+ * draft_p_min).  Host struct.
+ *   n_max  drafts per step, 1..B-1 (0 = B-1): the selector walks positions
+ *          1..n_max only (the max-score path over that shorter lattice)
+ *   p_min  in [0, 1]: the path is cut before the first position whose chosen
+ *          transition has probability exp(T_i(prev, chosen)) < p_min
+ *          (0 = never cut)
+ */
+typedef struct dflash2_draft_opts {
+    int n_max;
+    float p_min;
+} dflash2_draft_opts;
+
+/*
+ * dflash2_select_path / dflash2_select_path_table with drafting knobs (opts
+ * nullable: no knobs).  n_draft: nullable [batch] int32 out, the drafts kept
+ * (0..n_max); path slots from n_draft on are -1; path_score is the kept
+ * positions' summed log-probability.  DFLASH2_ERR_SHAPE for n_max outside
+ * 0..B-1 or p_min outside [0, 1].
+ */
+int dflash2_select_path_ex(const dflash2_config *cfg, const dflash2_weights *w, int batch,
+                           const int32_t *anchor, const int32_t *cand_id, const float *cand_logit,
+                           const dflash2_draft_opts *opts, int32_t *path, float *path_score, int32_t *n_draft,
+                           void *workspace, size_t ws_bytes, void *stream);
+int dflash2_select_path_table_ex(const dflash2_config *cfg, int batch, const int32_t *anchor,
+                                 const int32_t *cand_id, const float *cand_logit, const float *table,
+                                 const dflash2_draft_opts *opts, int32_t *path, float *path_score,
+                                 int32_t *n_draft, void *workspace, void *stream);
+
+/*
  * Stage (d2): greedy verification ("Prerequisites": the target verifies
  * [id_last, draft...] in one batch; "Validation": output token ids equal
  * plain greedy decoding).
@@ -351,6 +383,15 @@ int dflash2_verify_accept(int batch, int block_size, const int32_t *path,
                           const int32_t *target, int32_t *accept_len,
                           int32_t *out_tok, int32_t *n_out, int32_t *next_anchor,
                           int32_t *seq_len, int64_t *counters, void *stream);
+
+/*
+ * dflash2_verify_accept for paths of n_draft[s] drafts (from the _ex
+ * selectors; nullable: B-1 each): a <= n_draft[s], and the counters add
+ * n_draft[s] drafted and n_draft[s] - a rolled-back tokens.
+ */
+int dflash2_verify_accept_ex(int batch, int block_size, const int32_t *path, const int32_t *n_draft,
+                             const int32_t *target, int32_t *accept_len, int32_t *out_tok, int32_t *n_out,
+                             int32_t *next_anchor, int32_t *seq_len, int64_t *counters, void *stream);
 
 /*
  * Instrumentation.  Number of kernel launches the library has issued since

@@ -35,7 +35,7 @@ __all__ = [
     "bf16_round", "Store", "rms_norm", "rope", "silu", "dynamic_conv",
     "project_features", "context_kv", "append_context", "block_attention",
     "draft_layer", "draft_block", "topk", "draft_step", "selector_factors",
-    "select_path", "brute_force_path", "path_score", "verify_accept",
+    "select_path", "select_path_knobs", "transition_logprobs", "brute_force_path", "path_score", "verify_accept",
     "Counters", "loss_decay_weights", "toy_target_next", "greedy_generate",
     "speculative_generate",
 ]
@@ -398,6 +398,44 @@ def select_path(cfg, W, anchor, cand_id, cand_z):
     return cand_id[np.arange(D), idx], idx, score
 
 
+def transition_logprobs(cfg, W, anchor, cand_id, cand_z, idx):
+    """T_i(prev, chosen) along one path, i = 1..len(idx): the log-probability
+    of each chosen transition (the selector's confidence in it)."""
+    cand_id = np.asarray(cand_id, dtype=np.int64)
+    z = _f64(cand_z)
+    out = []
+    prev_tok = int(anchor)
+    for i in range(len(idx)):
+        a_prev, _ = selector_factors(cfg, W, np.array([prev_tok]))
+        _, b_all = selector_factors(cfg, W, cand_id[i])
+        s = z[i] + b_all @ a_prev[0]
+        m = s.max()
+        out.append(s[idx[i]] - (m + math.log(np.exp(s - m).sum())))
+        prev_tok = int(cand_id[i, idx[i]])
+    return np.array(out)
+
+
+def select_path_knobs(cfg, W, anchor, cand_id, cand_z, n_max=0, p_min=0.0):
+    """The selector with the drafting knobs ([llama] "Configuration Notes":
+    draft_n_max bounds the drafts of a step; drafting stops at a transition
+    whose confidence is below draft_p_min).  (A reading where the pages are
+    silent.)
+
+    The max-score path over positions 1..n_max only (n_max = 0: all D), then
+    cut before the first position whose chosen transition has probability
+    exp(T_i) < p_min.  Returns (kept tokens, kept indices, the kept
+    positions' summed log-probability)."""
+    n = len(cand_id) if n_max == 0 else n_max
+    toks, idx, score = select_path(cfg, W, anchor, np.asarray(cand_id)[:n], np.asarray(cand_z)[:n])
+    if p_min <= 0.0:
+        return toks, idx, score
+    t = transition_logprobs(cfg, W, anchor, np.asarray(cand_id)[:n], np.asarray(cand_z)[:n], idx)
+    keep = 0
+    while keep < n and math.exp(t[keep]) >= p_min:
+        keep += 1
+    return toks[:keep], idx[:keep], float(np.sum(t[:keep]))
+
+
 def path_score(cfg, W, anchor, cand_id, cand_z, idx):
     """Sum of transition log-probabilities of one path, computed directly
     from its definition (used by the brute-force search)."""
@@ -476,11 +514,14 @@ class Counters:
         self.hist = np.zeros(n_spec + 1, dtype=np.int64)
         self.acc_pos = np.zeros(n_spec, dtype=np.int64)
 
-    def add(self, a):
+    def add(self, a, n_draft=None):
+        """One verified step with a accepted of n_draft drafted tokens (all
+        n_spec unless the drafting knobs kept fewer)."""
+        n = self.n_spec if n_draft is None else n_draft
         self.steps += 1
-        self.drafted += self.n_spec
+        self.drafted += n
         self.accepted += a
-        self.rollback += self.n_spec - a
+        self.rollback += n - a
         self.hist[a] += 1
         self.acc_pos[:a] += 1
 

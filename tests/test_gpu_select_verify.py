@@ -2,6 +2,8 @@
 factor table + Viterbi) and of greedy verify/accept/rollback with the oracle,
 on identical inputs."""
 
+import math
+
 import numpy as np
 import pytest
 
@@ -144,6 +146,95 @@ def test_selector_table_flags_bad_tokens():
     # without a workspace the call still runs (no status word to flag)
     B.dflash2_select_path_table(c, b, anchor, cand, z, table, path, None, None)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("kind", ["gemm", "table"])
+@pytest.mark.parametrize("n_max,p_min", [(3, 0.0), (7, 0.2), (5, 0.35), (1, 0.0), (7, 0.99), (0, 0.5)])
+def test_selector_drafting_knobs_match_oracle(kind, n_max, p_min):
+    """draft_n_max / draft_p_min: the walk over positions 1..n_max and the
+    cut at the first low-confidence transition, against the oracle on the
+    same lattice (paths, kept counts exactly; scores to 1e-3)."""
+    import torch
+    B = lib()
+    V, H, k, D, r, b = 1000, 128, 4, 7, 16, 16
+    cfg = sel_cfg("bf16", V, H, k, D, r)
+    # factors and logits of comparable size: the pairwise term moves every
+    # path off the per-position top-1, and chosen transitions span the
+    # thresholds (at p_min 0.35 / 0.5 / 0.99 the oracle cuts 6 / 16 / 16 of
+    # the 16 paths)
+    E = S._draw(31, "E", (V, H), 1.0 / np.sqrt(H), "bf16")
+    Wsel = S._draw(31, "sel", (2 * r, H), 0.3, "bf16")
+    g = np.random.default_rng(31)
+    cand = np.stack([np.stack([g.choice(V - 1, size=k, replace=False) for _ in range(D)]) for _ in range(b)])
+    z = -np.sort(-g.standard_normal((b, D, k)).astype(np.float32), axis=2)
+    anchor = g.integers(0, V - 1, size=b).astype(np.int32)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    w = B.WeightSet({"embed": S.to_torch(E), "sel": S.to_torch(Wsel), "lm_head": None, "fc": None,
+                     "hidden_norm": None, "final_norm": None, "layers": []})
+    c = B.make_config(cfg)
+    ws = torch.zeros(B.dflash2_workspace_size(c, b, 0, 16), dtype=torch.uint8, device="cuda")
+    path = torch.full((b, D), -5, dtype=torch.int32, device="cuda")
+    score = torch.zeros(b, dtype=torch.float32, device="cuda")
+    nd = torch.full((b,), -5, dtype=torch.int32, device="cuda")
+    args = (dev(anchor), dev(cand.astype(np.int32)), dev(z))
+    if kind == "table":
+        table = torch.empty(B.dflash2_selector_table_bytes(c) // 4, dtype=torch.float32, device="cuda")
+        B.dflash2_build_selector_table(c, w, table)
+        B.dflash2_select_path_table_ex(c, b, *args, table, n_max, p_min, path, score, nd, ws)
+    else:
+        B.dflash2_select_path_ex(c, w, b, *args, n_max, p_min, path, score, nd, ws)
+    torch.cuda.synchronize()
+    path, score, nd = path.cpu().numpy(), score.cpu().numpy(), nd.cpu().numpy()
+    Wo = {"embed": E.values, "sel": Wsel.values}
+    cut = 0
+    for s in range(b):
+        zs = z[s].astype(np.float64)
+        p, idx, sc = O.select_path_knobs(cfg, Wo, int(anchor[s]), cand[s], zs, n_max, p_min)
+        n = len(p)
+        t = O.transition_logprobs(cfg, Wo, int(anchor[s]), cand[s], zs, idx)
+        walk = O.select_path_knobs(cfg, Wo, int(anchor[s]), cand[s], zs, n_max)[1]   # before the cut
+        probs = np.exp(O.transition_logprobs(cfg, Wo, int(anchor[s]), cand[s], zs, walk))
+        if p_min > 0 and np.any(np.abs(probs - p_min) < 1e-4):
+            continue  # a transition on the threshold: fp32 and fp64 may decide it differently
+        assert nd[s] == n, (s, nd[s], n)
+        assert list(path[s, :n]) == list(p) and np.all(path[s, n:] == -1)
+        assert abs(score[s] - sc) < 1e-3 * max(1.0, abs(sc))
+        cut += int(n < (n_max or D))
+        assert np.all(t >= math.log(p_min) - 1e-9) if p_min > 0 else True
+    if p_min in (0.35, 0.5, 0.99):
+        assert cut > 0  # the lattice really exercises the cut
+
+
+def test_verify_with_fewer_drafts_matches_oracle():
+    import torch
+    B = lib()
+    g = np.random.default_rng(77)
+    b, B_ = 400, 8
+    D = B_ - 1
+    nd = g.integers(0, D + 1, b)
+    paths = g.integers(0, 3, (b, D))
+    paths = np.where(np.arange(D)[None, :] < nd[:, None], paths, -1)
+    targets = g.integers(0, 3, (b, B_))
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+    acc = torch.full((b,), -9, dtype=torch.int32, device="cuda")
+    out = torch.full((b, B_), -9, dtype=torch.int32, device="cuda")
+    n_out = torch.zeros(b, dtype=torch.int32, device="cuda")
+    nxt = torch.zeros(b, dtype=torch.int32, device="cuda")
+    seq = dev(np.zeros(b))
+    counters = torch.zeros(4 + 2 * B_ - 1, dtype=torch.int64, device="cuda")
+    B.dflash2_verify_accept_ex(b, B_, dev(paths), dev(nd), dev(targets), acc, out, n_out, nxt, seq, counters)
+    torch.cuda.synchronize()
+    acc, out, nxt, seq = acc.cpu().numpy(), out.cpu().numpy(), nxt.cpu().numpy(), seq.cpu().numpy()
+    cnt = O.Counters(D)
+    for s in range(b):
+        a, toks, na = O.verify_accept(paths[s, :nd[s]], targets[s])
+        cnt.add(a, int(nd[s]))
+        assert acc[s] == a and nxt[s] == na and seq[s] == a + 1
+        assert list(out[s, :a + 1]) == toks and np.all(out[s, a + 1:] == -1)
+    c = counters.cpu().numpy()
+    assert c[0] == cnt.steps and c[1] == cnt.drafted and c[2] == cnt.accepted and c[3] == cnt.rollback
+    np.testing.assert_array_equal(c[4:4 + B_], cnt.hist)
+    np.testing.assert_array_equal(c[4 + B_:], cnt.acc_pos)
 
 
 def _verify(paths, targets, B_, seq_len=None, counters=None):

@@ -382,6 +382,41 @@ def test_selector_ties_pick_smallest_indices():
     assert abs(s - 2 * math.log(1 / 3)) < 1e-14
 
 
+@pytest.mark.parametrize("k,D,n_max,seed", [(4, 7, 3, 6), (3, 5, 1, 7), (3, 6, 4, 8)])
+def test_draft_n_max_walks_the_shorter_lattice(k, D, n_max, seed):
+    # the path over positions 1..n_max is the brute-force optimum of that
+    # shorter lattice (not a prefix of the full-length path in general)
+    cfg, W, anchor, cand, z = _sel_case(k, D, seed, scale=3.0)
+    p, idx, s = O.select_path_knobs(cfg, W, anchor, cand, z, n_max=n_max)
+    pb, idxb, sb = O.brute_force_path(cfg, W, anchor, cand[:n_max], z[:n_max])
+    assert list(idx) == list(idxb) and abs(s - sb) < 1e-12 and len(p) == n_max
+
+
+def test_draft_p_min_cut_closed_form():
+    # no pairwise term: T_i(j) = log softmax(z_i)[j] and the path is the
+    # per-position top-1.  Rows whose entries are log-probabilities already
+    # (summing to 1) make exp(T_i) the printed probability exactly.
+    cfg = dict(selector_rank=1)
+    W = {"embed": np.zeros((50, 1)), "sel": np.zeros((2, 1))}
+    top1 = [0.9, 0.8, 0.4, 0.95, 0.7]   # the top-1 entry of each row is its first
+    z = np.array([[math.log(p), math.log((1 - p) / 2), math.log((1 - p) / 2)] for p in top1])
+    cand = np.arange(15).reshape(5, 3)
+    for p_min, keep in [(0.0, 5), (0.25, 5), (0.5, 2), (0.85, 1), (0.95, 0), (0.3, 5)]:
+        p, idx, s = O.select_path_knobs(cfg, W, 0, cand, z, p_min=p_min)
+        assert len(p) == keep and list(idx) == [0] * keep
+        assert abs(s - sum(math.log(x) for x in top1[:keep])) < 1e-12
+    # the cut and n_max together: at most n_max, then the cut
+    p, idx, s = O.select_path_knobs(cfg, W, 0, cand, z, n_max=4, p_min=0.5)
+    assert len(p) == 2
+
+
+def test_transition_logprobs_match_path_score():
+    cfg, W, anchor, cand, z = _sel_case(4, 6, 9, scale=2.0)
+    _, idx, s = O.select_path(cfg, W, anchor, cand, z)
+    t = O.transition_logprobs(cfg, W, anchor, cand, z, idx)
+    assert abs(float(np.sum(t)) - s) < 1e-12 and np.all(t <= 0)
+
+
 # ---------------------------------------------------------------------- verify
 
 def test_verify_golden_cases():
@@ -392,6 +427,15 @@ def test_verify_golden_cases():
         assert ga == int(a)
         assert gout == [int(x) for x in out.split()]
         assert gn == int(nxt)
+
+
+def test_counters_with_fewer_drafts():
+    # drafted counts the drafts kept; rollback = drafted - accepted
+    c = O.Counters(7)
+    for a, n in [(0, 0), (2, 3), (7, 7), (1, 4)]:
+        c.add(a, n)
+    assert c.drafted == 14 and c.accepted == 10 and c.rollback == 4 and c.steps == 4
+    assert list(c.hist[:8]) == [1, 1, 1, 0, 0, 0, 0, 1]
 
 
 def test_counter_identities():

@@ -36,7 +36,7 @@ class Config(ctypes.Structure):
         "top_k", "selector_rank", "page_size", "mask_token_id", "dtype")] + \
         [(n, ctypes.c_float) for n in (
             "rms_eps", "rope_theta", "input_embedding_scale", "output_multiplier",
-            "final_logit_softcap")]
+            "final_logit_softcap")] + [("sliding_window", ctypes.c_int)]
 
 
 _LAYER_FIELDS = ("attn_norm", "tapgen_attn", "qkv", "q_norm", "k_norm", "o", "mlp_norm",
@@ -116,6 +116,8 @@ def lib():
         L.dflash2_select_path_table_ex.argtypes = [F(Config), I, P, P, P, P, F(DraftOpts), P, P, P, P, P]
         L.dflash2_select_path_ex.restype = I
         L.dflash2_select_path_ex.argtypes = [F(Config), F(Weights), I, P, P, P, F(DraftOpts), P, P, P, P, S, P]
+        L.dflash2_select_top1.restype = I
+        L.dflash2_select_top1.argtypes = [F(Config), I, P, P, F(DraftOpts), P, P, P, P, P]
         L.dflash2_verify_accept_ex.restype = I
         L.dflash2_verify_accept_ex.argtypes = [I, I, P, P, P, P, P, P, P, P, P, P]
         L.dflash2_test_layout.restype = I
@@ -158,7 +160,7 @@ def make_config(d):
     """Config struct from a dict with the header's field names (extra keys ignored)."""
     c = Config()
     for name, _ in Config._fields_:
-        v = d[name]
+        v = d.get(name, 0) if name == "sliding_window" else d[name]
         if name == "dtype" and isinstance(v, str):
             v = {"f32": F32, "bf16": BF16, "fp8w": FP8W}[v]
         setattr(c, name, v)
@@ -269,6 +271,13 @@ def dflash2_select_path_table_ex(cfg, batch, anchor, cand_id, cand_logit, table,
     return _check("dflash2_select_path_table_ex", lib().dflash2_select_path_table_ex(
         ctypes.byref(cfg), batch, _ptr(anchor), _ptr(cand_id), _ptr(cand_logit), _ptr(table), _opts(n_max, p_min),
         _ptr(path), _ptr(path_score), _ptr(n_draft), _ptr(workspace), _stream(stream)))
+
+
+def dflash2_select_top1(cfg, batch, cand_id, cand_logit, n_max, p_min, path, path_score, n_draft, workspace=None,
+                        stream=None):
+    return _check("dflash2_select_top1", lib().dflash2_select_top1(
+        ctypes.byref(cfg), batch, _ptr(cand_id), _ptr(cand_logit), _opts(n_max, p_min), _ptr(path),
+        _ptr(path_score), _ptr(n_draft), _ptr(workspace), _stream(stream)))
 
 
 def dflash2_verify_accept_ex(batch, block_size, path, n_draft, target, accept_len, out_tok, n_out, next_anchor,

@@ -87,7 +87,8 @@ int check_config(const dflash2_config* c) {
     return DFLASH2_ERR_SHAPE;
   if (c->head_dim != 64 && c->head_dim != 128) return DFLASH2_ERR_SHAPE;
   if (c->n_q_heads % c->n_kv_heads) return DFLASH2_ERR_SHAPE;
-  if (c->conv_kernel_size != 2) return DFLASH2_ERR_SHAPE;
+  if (c->conv_kernel_size != 2 && c->conv_kernel_size != 0) return DFLASH2_ERR_SHAPE;  // DFlash 2, or v1 (none)
+  if (c->sliding_window < 0) return DFLASH2_ERR_SHAPE;
   if (c->conv_group_size <= 0 || c->hidden % c->conv_group_size) return DFLASH2_ERR_SHAPE;
   if (c->top_k < 1 || c->top_k > KMAX || c->top_k > c->vocab) return DFLASH2_ERR_SHAPE;
   if (c->selector_rank < 1 || c->selector_rank > 128) return DFLASH2_ERR_SHAPE;
@@ -298,16 +299,17 @@ int check_weights(const dflash2_config& c, const dflash2_weights* w) {
     return DFLASH2_ERR_INVALID_ARG;
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash2_layer_weights& L = w->layers[l];
-    if (!L.attn_norm || !L.tapgen_attn || !L.qkv || !L.q_norm || !L.k_norm || !L.o || !L.mlp_norm ||
-        !L.tapgen_mlp || !L.gate_up || !L.down)
+    if (!L.attn_norm || !L.qkv || !L.q_norm || !L.k_norm || !L.o || !L.mlp_norm || !L.gate_up || !L.down)
       return DFLASH2_ERR_INVALID_ARG;
+    if (c.conv_kernel_size > 0 && (!L.tapgen_attn || !L.tapgen_mlp)) return DFLASH2_ERR_INVALID_ARG;
   }
   if (c.dtype == DFLASH2_FP8W) {
     const dflash2_scales* s = w->scales;
     if (!s || !s->lm_head || !s->fc || !s->sel || !s->layers) return DFLASH2_ERR_INVALID_ARG;
     for (int l = 0; l < c.n_layers; ++l) {
       const dflash2_layer_scales& L = s->layers[l];
-      if (!L.tapgen_attn || !L.qkv || !L.o || !L.tapgen_mlp || !L.gate_up || !L.down) return DFLASH2_ERR_INVALID_ARG;
+      if (!L.qkv || !L.o || !L.gate_up || !L.down) return DFLASH2_ERR_INVALID_ARG;
+      if (c.conv_kernel_size > 0 && (!L.tapgen_attn || !L.tapgen_mlp)) return DFLASH2_ERR_INVALID_ARG;
     }
   }
   return DFLASH2_OK;
@@ -513,8 +515,12 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
   //    projects the appended rows' k/v into the cache (W_k and W_v read once
   //    per layer instead of twice).
   const int qkvM = (nq + 2 * nkv) * d;
+  // conv_kernel_size 0 (DFlash v1): no convolution, each sublayer reads its
+  // normed rows (u2 aliases u); the merged arrangement needs u2a next to f,
+  // so v1 runs the separate one
+  const bool conv = c.conv_kernel_size > 0;
   const bool merged =
-      c.n_layers > 1 && c.dtype == DFLASH2_BF16 && gemm_fusable(qkvM, rows + n_new, kEpiHeads);
+      conv && c.n_layers > 1 && c.dtype == DFLASH2_BF16 && gemm_fusable(qkvM, rows + n_new, kEpiHeads);
   std::unique_lock<std::mutex> side_lock(g_side_mu, std::defer_lock);
   SideStream side;
   const bool forked = n_new > 0;
@@ -522,7 +528,7 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
   // contraction bandwidth-bound, and neither fits an SM beside the other: a
   // forked step splits the SMs, kForkPrologueSMs for the prologue (on fewer,
   // wider CTAs) and the rest for the contraction, so the two overlap.
-  const bool fused = conv_prologue_fits(c.dtype, batch, B, H, G, ctx.nsm);
+  const bool fused = conv && conv_prologue_fits(c.dtype, batch, B, H, G, ctx.nsm);
   const bool split_sms = forked && fused && ctx.nsm > 2 * kForkPrologueSMs &&
                          conv_prologue_fits(c.dtype, batch, B, H, G, kForkPrologueSMs / 2);
   TRY(stage_event(0, ctx.stream));
@@ -550,9 +556,9 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
   float* Y = at<float>(workspace, L.Y);
   float* h = at<float>(workspace, L.h);
   void* u = at<char>(workspace, L.u);    // MLP sublayer: normed input
-  void* u2 = at<char>(workspace, L.u2);  // MLP sublayer: after the conv
+  void* u2 = conv ? at<char>(workspace, L.u2) : u;  // MLP sublayer: after the conv
   void* ua = at<char>(workspace, L.ua);   // attention sublayer: normed input
-  void* u2a = at<char>(workspace, L.u2a); // attention sublayer: after the conv
+  void* u2a = conv ? at<char>(workspace, L.u2a) : ua;  // attention sublayer: after the conv
   void* q = at<char>(workspace, L.q);
   void* kb = at<char>(workspace, L.kb);
   void* vb = at<char>(workspace, L.vb);
@@ -603,8 +609,10 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
                                  ctx));
     } else {
       if (l > 0) TRY(launch_rownorm(c.dtype, h, rows, H, Lw.attn_norm, c.rms_eps, ua, B, 0, ctx));
-      TRY(gemm(c, ctx, ws, L, Lw.tapgen_attn, 2 * G, H, ua, rows, Y, false, false, s_tap_a));
-      TRY(launch_dyn_conv(c.dtype, ua, Y, rows, H, c.conv_group_size, B, u2a, ctx));
+      if (conv) {
+        TRY(gemm(c, ctx, ws, L, Lw.tapgen_attn, 2 * G, H, ua, rows, Y, false, false, s_tap_a));
+        TRY(launch_dyn_conv(c.dtype, ua, Y, rows, H, c.conv_group_size, B, u2a, ctx));
+      }
     }
     // merged: the QKV contraction reads the appended rows' features, a full
     // dependency on the join
@@ -649,7 +657,8 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
     }
     TRY(launch_attention(c.dtype, q, kb, vb, elem_ptr(k_cache, l * layer_elems, c.dtype),
                          elem_ptr(v_cache, l * layer_elems, c.dtype), block_table, max_pages, c.page_size, n_pages,
-                         ctx_len, new_off, batch, B, nq, nkv, d, max_ctx, at<float>(workspace, L.attn), O, jctx));
+                         ctx_len, new_off, batch, B, nq, nkv, d, max_ctx, c.sliding_window, at<float>(workspace, L.attn),
+                         O, jctx));
     TRY(gemm(c, ctx, ws, L, Lw.o, H, nq * d, O, rows, h, true, false, s_o));
     // MLP sublayer: conv around the normed input, gate/up, SiLU*up, down (+= residual)
     if (fused) {
@@ -657,8 +666,10 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
                                batch, B, H, c.conv_group_size, nullptr, u, u2, RopeTab{}, ctx));
     } else {
       TRY(launch_rownorm(c.dtype, h, rows, H, Lw.mlp_norm, c.rms_eps, u, B, 0, ctx));
-      TRY(gemm(c, ctx, ws, L, Lw.tapgen_mlp, 2 * G, H, u, rows, Y, false, false, s_tap_m));
-      TRY(launch_dyn_conv(c.dtype, u, Y, rows, H, c.conv_group_size, B, u2, ctx));
+      if (conv) {
+        TRY(gemm(c, ctx, ws, L, Lw.tapgen_mlp, 2 * G, H, u, rows, Y, false, false, s_tap_m));
+        TRY(launch_dyn_conv(c.dtype, u, Y, rows, H, c.conv_group_size, B, u2, ctx));
+      }
     }
     if (c.dtype == DFLASH2_BF16 && gemm_fusable(2 * I, rows, kEpiSwiglu)) {
       GemmOp g = gemm_op(Lw.gate_up, 2 * I, H, u2, rows, s_gu);  // SiLU(gate) * up fused into the epilogue
@@ -774,6 +785,20 @@ int dflash2_select_path_table_ex(const dflash2_config* cfg, int batch, const int
   TRY(device_ctx(&ctx, stream, workspace));
   const dflash2_config& c = *cfg;
   return launch_viterbi(nullptr, table, anchor, c.vocab, cand_id, cand_logit, batch, c.block_size - 1, c.top_k,
+                        c.selector_rank, path, path_score, ctx, opts ? opts->n_max : 0, opts ? opts->p_min : 0.f,
+                        n_draft);
+}
+
+int dflash2_select_top1(const dflash2_config* cfg, int batch, const int32_t* cand_id, const float* cand_logit,
+                        const dflash2_draft_opts* opts, int32_t* path, float* path_score, int32_t* n_draft,
+                        void* workspace, void* stream) {
+  TRY(check_config(cfg));
+  if (batch <= 0) return DFLASH2_ERR_SHAPE;
+  if (!cand_id || !cand_logit || !path) return DFLASH2_ERR_INVALID_ARG;
+  Ctx ctx;
+  TRY(device_ctx(&ctx, stream, workspace));
+  const dflash2_config& c = *cfg;
+  return launch_viterbi(nullptr, nullptr, nullptr, c.vocab, cand_id, cand_logit, batch, c.block_size - 1, c.top_k,
                         c.selector_rank, path, path_score, ctx, opts ? opts->n_max : 0, opts ? opts->p_min : 0.f,
                         n_draft);
 }

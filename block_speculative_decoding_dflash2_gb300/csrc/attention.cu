@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(AT) attn_partial_kernel(
     const T* __restrict__ q, const T* __restrict__ kb, const T* __restrict__ vb, const T* __restrict__ kc,
     const T* __restrict__ vc, const int32_t* __restrict__ block_table, int max_pages, int page_size, int n_pages,
     const int32_t* __restrict__ ctx_len, const int32_t* __restrict__ new_off, int B, int nq, int nkv, int d, int CH,
-    int nsplit, float* __restrict__ part, unsigned* status) {
+    int nsplit, int window, float* __restrict__ part, unsigned* status) {
   extern __shared__ float sm[];
   pdl_launch_next();
   pdl_wait();
@@ -76,7 +76,8 @@ __global__ void __launch_bounds__(AT) attn_partial_kernel(
 
   const int P = ctx_len[s] + (new_off[s + 1] - new_off[s]);
   const int L = P + B;
-  const int k0 = sp * CH, k1 = min(k0 + CH, L);
+  const int w0 = window > 0 ? max(0, P - window) : 0;  // first context key read (sliding window)
+  const int k0 = w0 + sp * CH, k1 = min(k0 + CH, L);
   float* out = part + ((((size_t)s * nkv + g) * nsplit + sp) * R) * (d + 2);
   if (k0 >= L) {
     for (int r = threadIdx.x; r < R; r += blockDim.x) {
@@ -276,7 +277,7 @@ __global__ void __launch_bounds__(CLT, 1) attn_cluster_kernel(
     const bf16* __restrict__ q, const bf16* __restrict__ kb, const bf16* __restrict__ vb, const bf16* __restrict__ kc,
     const bf16* __restrict__ vc, const int32_t* __restrict__ block_table, int max_pages, int page_size, int n_pages,
     const int32_t* __restrict__ ctx_len, const int32_t* __restrict__ new_off, int B, int nq, int nkv, int npg,
-    bf16* __restrict__ o, unsigned* status) {
+    int window, bf16* __restrict__ o, unsigned* status) {
   constexpr int MCPW = 1;  // (row block, key share) combinations per warp
   constexpr int LD = DH + 8;  // padded smem row (elements): ldmatrix rows hit distinct banks
   constexpr int NT = DH / 8;  // n8 tiles across the head dimension
@@ -305,8 +306,9 @@ __global__ void __launch_bounds__(CLT, 1) attn_cluster_kernel(
   pdl_wait();
   const int P = ctx_len[s] + (new_off[s + 1] - new_off[s]);
   const int L = P + B;
-  const int CH = (((L + NS - 1) / NS) + 15) & ~15;
-  const int k0 = min(sp * CH, L), k1 = min(k0 + CH, L);
+  const int w0 = window > 0 ? max(0, P - window) : 0;  // first context key read (sliding window)
+  const int CH = (((L - w0 + NS - 1) / NS) + 15) & ~15;
+  const int k0 = w0 + min(sp * CH, L - w0), k1 = min(k0 + CH, L);
   if (P > max_pages * page_size && sp == 0 && threadIdx.x == 0) flag(status, DFLASH2_DEV_BAD_LENGTH);
   const float scale = rsqrtf((float)DH);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -671,7 +673,7 @@ template <int DH>
 int launch_cluster(int R, int max_ctx, int page_size, int batch, int nkv, const Ctx& c, const bf16* q,
                    const bf16* kb, const bf16* vb, const bf16* kc, const bf16* vc, const int32_t* block_table,
                    int max_pages, int n_pages, const int32_t* ctx_len, const int32_t* new_off, int B, int nq,
-                   bf16* o) {
+                   int window, bf16* o) {
   static bool attr = false;  // set once, before any capture
   if (!attr) {
     if (cudaFuncSetAttribute(attn_cluster_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024))
@@ -685,7 +687,7 @@ int launch_cluster(int R, int max_ctx, int page_size, int batch, int nkv, const 
   const size_t smem = attn_cl_smem<DH>(R, npg);
   if (smem > 200 * 1024) return DFLASH2_ERR_SHAPE;
   return launch_kx(attn_cluster_kernel<DH>, dim3(ns, nkv, batch), dim3(CLT), smem, c, ns, q, kb, vb, kc, vc,
-                   block_table, max_pages, page_size, n_pages, ctx_len, new_off, B, nq, nkv, npg, o, c.status);
+                   block_table, max_pages, page_size, n_pages, ctx_len, new_off, B, nq, nkv, npg, window, o, c.status);
 }
 
 }  // namespace
@@ -705,7 +707,7 @@ size_t attn_part_bytes(int max_batch, int B, int nq, int nkv, int d, int max_ctx
 int launch_attention(int dtype, const void* q, const void* kb, const void* vb, const void* kc, const void* vc,
                      const int32_t* block_table, int max_pages, int page_size, int n_pages,
                      const int32_t* ctx_len, const int32_t* new_off, int batch, int B, int nq, int nkv, int d,
-                     int max_ctx, float* part, void* o_out, const Ctx& c) {
+                     int max_ctx, int window, float* part, void* o_out, const Ctx& c) {
   const int R = (nq / nkv) * B;
   const int nrb = (R + 15) / 16;
   const int ncombo = nrb * attn_ksplit(nrb);
@@ -716,9 +718,9 @@ int launch_attention(int dtype, const void* q, const void* kb, const void* vb, c
     bf16* o_ = static_cast<bf16*>(o_out);
     if (d == 64)
       return launch_cluster<64>(R, max_ctx, page_size, batch, nkv, c, q_, kb_, vb_, kc_, vc_, block_table, max_pages,
-                                n_pages, ctx_len, new_off, B, nq, o_);
+                                n_pages, ctx_len, new_off, B, nq, window, o_);
     return launch_cluster<128>(R, max_ctx, page_size, batch, nkv, c, q_, kb_, vb_, kc_, vc_, block_table, max_pages,
-                               n_pages, ctx_len, new_off, B, nq, o_);
+                               n_pages, ctx_len, new_off, B, nq, window, o_);
   }
   // SIMT path (fp32 storage, or row counts beyond the tensor-core kernel):
   // key-chunk partials in global memory, then the combine kernel
@@ -741,12 +743,12 @@ int launch_attention(int dtype, const void* q, const void* kb, const void* vb, c
     rc = launch_k(attn_partial_kernel<bf16>, grid, dim3(AT), smem, c, static_cast<const bf16*>(q),
                   static_cast<const bf16*>(kb), static_cast<const bf16*>(vb), static_cast<const bf16*>(kc),
                   static_cast<const bf16*>(vc), block_table, max_pages, page_size, n_pages, ctx_len, new_off, B, nq,
-                  nkv, d, ch, nsplit, part, c.status);
+                  nkv, d, ch, nsplit, window, part, c.status);
   else
     rc = launch_k(attn_partial_kernel<float>, grid, dim3(AT), smem, c, static_cast<const float*>(q),
                   static_cast<const float*>(kb), static_cast<const float*>(vb), static_cast<const float*>(kc),
                   static_cast<const float*>(vc), block_table, max_pages, page_size, n_pages, ctx_len, new_off, B, nq,
-                  nkv, d, ch, nsplit, part, c.status);
+                  nkv, d, ch, nsplit, window, part, c.status);
   if (rc) return rc;
   Ctx cc = c;
   cc.pdl = true;  // same-stream successor of the partial kernel

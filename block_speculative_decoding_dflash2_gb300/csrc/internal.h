@@ -188,7 +188,7 @@ int launch_conv_prologue(int dtype, const float* h_in, const int32_t* anchor, in
 int launch_attention(int dtype, const void* q, const void* kb, const void* vb, const void* kc, const void* vc,
                      const int32_t* block_table, int max_pages, int page_size, int n_pages,
                      const int32_t* ctx_len, const int32_t* new_off, int batch, int B, int nq, int nkv, int d,
-                     int max_ctx, float* part, void* o_out, const Ctx& c);
+                     int max_ctx, int window, float* part, void* o_out, const Ctx& c);
 size_t attn_part_bytes(int batch, int B, int nq, int nkv, int d, int max_ctx);
 
 // top-k (topk.cu)

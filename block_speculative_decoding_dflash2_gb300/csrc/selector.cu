@@ -53,7 +53,8 @@ __global__ void __launch_bounds__(256) sel_gather_kernel(const int32_t* __restri
 }
 
 // Factors: Y [batch][nt][2r] rows in [anchor, candidates] order, or (Y
-// null) rows of `table` [V][2r] at those tokens.
+// null) rows of `table` [V][2r] at those tokens; neither (DFlash v1): no
+// pairwise term, so the walk is the per-position top-1.
 __global__ void __launch_bounds__(512) viterbi_kernel(const float* __restrict__ Y, const float* __restrict__ table,
                                                       const int32_t* __restrict__ anchor, int V,
                                                       const int32_t* __restrict__ cand_id,
@@ -81,7 +82,8 @@ __global__ void __launch_bounds__(512) viterbi_kernel(const float* __restrict__ 
   }
   // stage the factors: U vector loads in flight per thread
   constexpr int U = 8;
-  if (!Y) {
+  const bool pairwise = Y || table;
+  if (!Y && table) {
     if (threadIdx.x == 0) tok0 = anchor[s];
     __syncthreads();
     // row t of the sequence's lattice: the anchor, then candidate t-1
@@ -122,7 +124,7 @@ __global__ void __launch_bounds__(512) viterbi_kernel(const float* __restrict__ 
         F[t * ws + idx - t * w] = src ? src[idx - t * w] : 0.f;
       }
     }
-  } else if ((w & 3) == 0) {
+  } else if (Y && (w & 3) == 0) {
     const float4* y = reinterpret_cast<const float4*>(Y + (size_t)s * nt * w);
     const int w4 = w / 4, n4 = nt * w4;
     for (int base = threadIdx.x; base < n4; base += blockDim.x * U) {
@@ -143,7 +145,7 @@ __global__ void __launch_bounds__(512) viterbi_kernel(const float* __restrict__ 
         }
       }
     }
-  } else {
+  } else if (Y) {
     const float2* y = reinterpret_cast<const float2*>(Y + (size_t)s * nt * w);
     const int w2 = w / 2, n2 = nt * w2;
     for (int base = threadIdx.x; base < n2; base += blockDim.x * U) {
@@ -201,7 +203,9 @@ __global__ void __launch_bounds__(512) viterbi_kernel(const float* __restrict__ 
     for (int a = 0; a < 4; ++a)
 #pragma unroll
       for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
-    if ((r & 3) == 0) {
+    if (!pairwise) {
+      // no pairwise term: S = the candidate logits alone
+    } else if ((r & 3) == 0) {
       for (int c = 0; c < r; c += 4) {
         float4 x[4], y[4];
 #pragma unroll
@@ -331,7 +335,7 @@ int launch_sel_gather(int dtype, const int32_t* anchor, const int32_t* cand_id, 
 int launch_viterbi(const float* Y, const float* table, const int32_t* anchor, int V, const int32_t* cand_id,
                    const float* cand_logit, int batch, int D, int k, int r, int32_t* path, float* path_score,
                    const Ctx& c, int n_max, float p_min, int32_t* n_draft) {
-  if ((Y == nullptr) == (table == nullptr)) return DFLASH2_ERR_INVALID_ARG;
+  if (Y && table) return DFLASH2_ERR_INVALID_ARG;
   if (n_max < 0 || n_max > D || !(p_min >= 0.f) || p_min > 1.f) return DFLASH2_ERR_SHAPE;
   const int Dp = n_max == 0 ? D : n_max;
   const float log_p_min = p_min > 0.f ? logf(p_min) : -INFINITY;

@@ -88,7 +88,8 @@ extern "C" {
  *   n_layers               draft decoder layers (>= 1)
  *   n_taps                 T, number of target layers tapped (target_layer_ids)
  *   block_size             B = 1 anchor + (B-1) drafts, 2..32
- *   conv_kernel_size       taps of the in-block convolution; must be 2
+ *   conv_kernel_size       taps of the in-block convolution: 2 (DFlash 2), or 0 for
+ *                          DFlash (v1): no convolution, tapgen_* unused ("Variants")
  *   conv_group_size        channels sharing one set of dynamic taps; H % it == 0
  *   top_k                  selector_top_k, 1..16
  *   selector_rank          r, 1..128
@@ -100,6 +101,9 @@ extern "C" {
  *   input_embedding_scale  multiplies the embedded block (1 = identity)
  *   output_multiplier      multiplies the logits (1 = identity)
  *   final_logit_softcap    cap*tanh(z/cap) when > 0 (0 = off)
+ *   sliding_window         draft_sliding_window ("Key Config Fields"): when > 0 the
+ *                          block reads only the last sliding_window context
+ *                          positions (and all its own); 0 = the whole prefix
  */
 typedef struct dflash2_config {
     int hidden, n_q_heads, n_kv_heads, head_dim, intermediate, vocab;
@@ -107,6 +111,7 @@ typedef struct dflash2_config {
     int top_k, selector_rank, page_size, mask_token_id, dtype;
     float rms_eps, rope_theta, input_embedding_scale, output_multiplier,
           final_logit_softcap;
+    int sliding_window;
 } dflash2_config;
 
 /*
@@ -358,6 +363,19 @@ int dflash2_select_path_table_ex(const dflash2_config *cfg, int batch, const int
                                  const int32_t *cand_id, const float *cand_logit, const float *table,
                                  const dflash2_draft_opts *opts, int32_t *path, float *path_score,
                                  int32_t *n_draft, void *workspace, void *stream);
+
+/*
+ * DFlash (v1) selection ("Variants": DFlash 2 adds the pairwise selector to
+ * the block-parallel baseline, which takes each position's best candidate):
+ * path[s][i] = cand_id[s][i][0], the per-position top-1, with the same
+ * drafting knobs (opts nullable), whose transition probabilities are then
+ * the softmax of the k candidate logits.  Same outputs as the _ex selectors;
+ * needs no factors, no weights and no scratch (workspace nullable: its
+ * status word only).
+ */
+int dflash2_select_top1(const dflash2_config *cfg, int batch, const int32_t *cand_id, const float *cand_logit,
+                        const dflash2_draft_opts *opts, int32_t *path, float *path_score, int32_t *n_draft,
+                        void *workspace, void *stream);
 
 /*
  * Stage (d2): greedy verification ("Prerequisites": the target verifies

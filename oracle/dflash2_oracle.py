@@ -232,16 +232,28 @@ def draft_layer(cfg, Wl, h, ctxK, ctxV, pos, st):
 
     h [B, H] residual stream of one block (float64, never rounded);
     pos [B] absolute positions of the block.
+
+    conv_kernel_size 0 is DFlash (v1): no convolution, the sublayers read
+    the normed rows ([Train] "Variants": the convolution is what DFlash 2
+    adds to the block-parallel baseline).  sliding_window W > 0: the block
+    reads only the last W context positions ([Train] "Key Config Fields":
+    draft_sliding_window bounds how far back a block reads the context;
+    unset, it reads the whole prefix).  Reading taken: the window is counted
+    back from the first block position and the block's own keys are always
+    read.
     """
     H = cfg["hidden"]
     nq, nkv, d = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
     I = cfg["intermediate"]
     gs, kc, eps = cfg["conv_group_size"], cfg["conv_kernel_size"], cfg["rms_eps"]
     B = h.shape[0]
+    win = cfg.get("sliding_window", 0)
+    if win and win > 0:
+        ctxK, ctxV = ctxK[max(0, ctxK.shape[0] - win):], ctxV[max(0, ctxV.shape[0] - win):]
 
     # attention sublayer
     u = st(rms_norm(h, Wl["attn_norm"], eps))
-    u2 = st(u + dynamic_conv(u, Wl["tapgen_attn"], gs, kc))
+    u2 = st(u + dynamic_conv(u, Wl["tapgen_attn"], gs, kc)) if kc else u
     qkv = u2 @ _f64(Wl["qkv"]).T
     q = qkv[:, : nq * d].reshape(B, nq, d)
     k = qkv[:, nq * d: (nq + nkv) * d].reshape(B, nkv, d)
@@ -254,7 +266,7 @@ def draft_layer(cfg, Wl, h, ctxK, ctxV, pos, st):
 
     # MLP sublayer
     u = st(rms_norm(h, Wl["mlp_norm"], eps))
-    u2 = st(u + dynamic_conv(u, Wl["tapgen_mlp"], gs, kc))
+    u2 = st(u + dynamic_conv(u, Wl["tapgen_mlp"], gs, kc)) if kc else u
     gu = u2 @ _f64(Wl["gate_up"]).T
     act = st(silu(gu[:, :I]) * gu[:, I:])
     return h + act @ _f64(Wl["down"]).T

@@ -39,8 +39,8 @@ def test_every_declared_symbol_is_exported(B):
 
 
 def test_struct_sizes_match_header(B):
-    # 16 ints + 5 floats; 10 and 6+1+1 pointers; fp8 scales: 6 and 3+1
-    assert ctypes.sizeof(B.Config) == 21 * 4
+    # 16 ints + 5 floats + 1 int; 10 and 6+1+1 pointers; fp8 scales: 6 and 3+1
+    assert ctypes.sizeof(B.Config) == 22 * 4
     assert ctypes.sizeof(B.LayerWeights) == 10 * 8
     assert ctypes.sizeof(B.Weights) == 8 * 8
     assert ctypes.sizeof(B.LayerScales) == 6 * 8

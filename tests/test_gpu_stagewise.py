@@ -109,13 +109,15 @@ def run_stagewise(case):
     kb = R.get("kb", (rows, nkv, d))
     vb = R.get("vb", (rows, nkv, d))
     Og = R.get("O", (rows, nq * d))
+    kc = cfg["conv_kernel_size"]
+    win = cfg.get("sliding_window", 0)
     u_m = R.get("u", (rows, H))
-    u2_m = R.get("u2", (rows, H))
+    u2_m = R.get("u2", (rows, H)) if kc else u_m   # DFlash v1: no conv, u2 is u
     act = R.get("act", (rows, I))
     h = R.get("h", (rows, H), fp32=True)
     hn = R.get("hn", (b * D, H))
     ua = R.get("ua", (rows, H))
-    u2a = R.get("u2a", (rows, H))
+    u2a = R.get("u2a", (rows, H)) if kc else ua
     q_ref, k_ref, v_ref, O_ref, h_mid, ua_ref, u2a_ref = [], [], [], [], [], [], []
     for s in range(b):
         P = int(case.ctx_lens[s] + case.n_new[s])
@@ -123,7 +125,8 @@ def run_stagewise(case):
         toks = np.array([int(case.anchor[s])] + [cfg["mask_token_id"]] * D)
         h0 = cfg["input_embedding_scale"] * Wv["embed"][toks].astype(np.float64)
         ua_ref.append(st(O.rms_norm(h0, Wl["attn_norm"], eps)))
-        u2a_ref.append(st(ua[sl] + O.dynamic_conv(ua[sl], Wl["tapgen_attn"], cfg["conv_group_size"])))
+        u2a_ref.append(st(ua[sl] + O.dynamic_conv(ua[sl], Wl["tapgen_attn"], cfg["conv_group_size"])) if kc
+                       else ua[sl])
         qkv = u2a[sl] @ Wl["qkv"].astype(np.float64).T
         pos = P + np.arange(B_)
         q_ref.append(st(O.rope(O.rms_norm(qkv[:, :nq * d].reshape(B_, nq, d), Wl["q_norm"], eps), pos,
@@ -131,7 +134,7 @@ def run_stagewise(case):
         k_ref.append(st(O.rope(O.rms_norm(qkv[:, nq * d:(nq + nkv) * d].reshape(B_, nkv, d), Wl["k_norm"], eps),
                                pos, cfg["rope_theta"])))
         v_ref.append(st(qkv[:, (nq + nkv) * d:].reshape(B_, nkv, d)))
-        Kc, Vc = cache_rows(case, 0, s, np.arange(P))
+        Kc, Vc = cache_rows(case, 0, s, np.arange(max(0, P - win) if win else 0, P))
         O_ref.append(st(O.block_attention(q[sl], Kc, Vc, kb[sl], vb[sl])).reshape(B_, nq * d))
         h_mid.append(h0 + Og[sl] @ Wl["o"].astype(np.float64).T)
     check_ulps("u_attn", ua, np.concatenate(ua_ref), 2)
@@ -143,7 +146,8 @@ def run_stagewise(case):
     h_mid = np.concatenate(h_mid)
     check_ulps("u_mlp", u_m, st(O.rms_norm(h_mid, Wl["mlp_norm"], eps)), 2)
     u2_ref = np.concatenate([st(u_m[s * B_:(s + 1) * B_] + O.dynamic_conv(
-        u_m[s * B_:(s + 1) * B_], Wl["tapgen_mlp"], cfg["conv_group_size"])) for s in range(b)])
+        u_m[s * B_:(s + 1) * B_], Wl["tapgen_mlp"], cfg["conv_group_size"])) if kc else u_m[s * B_:(s + 1) * B_]
+        for s in range(b)])
     check_ulps("u2_mlp", u2_m, u2_ref, 2)
     Wgu = Wl["gate_up"].astype(np.float64)
     gu = u2_m @ Wgu.T

@@ -230,6 +230,43 @@ def test_draft_layer_residual_identity_when_outputs_zero():
     np.testing.assert_array_equal(out, h)
 
 
+def test_v1_layer_without_conv_mixes_rows_only_through_attention():
+    # conv_kernel_size 0 (DFlash v1): with the attention output switched off
+    # (W_o = 0) every row is processed alone, so changing row 1 leaves rows
+    # 0, 2, 3 unchanged; with the two-tap conv (DFlash 2) row 2 reads row 1
+    for kc, row2_moves in [(0, False), (2, True)]:
+        cfg = tiny_cfg(conv_kernel_size=kc)
+        W = tiny_weights(cfg)
+        Wl = dict(W["layers"][0]); Wl["o"] = np.zeros_like(Wl["o"])
+        h = np.random.default_rng(20).standard_normal((4, cfg["hidden"]))
+        h2 = h.copy(); h2[1] += 0.5
+        a = O.draft_layer(cfg, Wl, h, *empty_ctx(cfg)[0], np.arange(4), O.Store(False))
+        b = O.draft_layer(cfg, Wl, h2, *empty_ctx(cfg)[0], np.arange(4), O.Store(False))
+        np.testing.assert_array_equal(a[[0, 3]], b[[0, 3]])
+        assert np.any(a[1] != b[1])
+        assert bool(np.any(a[2] != b[2])) == row2_moves
+
+
+def test_sliding_window_reads_only_the_last_context_positions():
+    cfg = tiny_cfg()
+    W = tiny_weights(cfg)
+    taps = np.random.default_rng(21).standard_normal((12, cfg["n_taps"] * cfg["hidden"]))
+    st = O.Store(False)
+    ctx = O.append_context(cfg, W, empty_ctx(cfg), taps, 0, st)
+    full = O.draft_block(cfg, W, 7, ctx, st)
+    for win in (0, 12, 40):     # unset, or a window covering the whole context
+        np.testing.assert_array_equal(O.draft_block(dict(cfg, sliding_window=win), W, 7, ctx, st), full)
+    cw = dict(cfg, sliding_window=5)
+    z5 = O.draft_block(cw, W, 7, ctx, st)
+    assert np.max(np.abs(z5 - full)) > 1e-6
+    # keys and values older than the window do not matter; a key inside does
+    K, V = ctx[0]
+    old = [(np.concatenate([K[:7] * -3.0 + 1.0, K[7:]]), np.concatenate([V[:7] * 2.0, V[7:]]))]
+    np.testing.assert_array_equal(O.draft_block(cw, W, 7, old, st), z5)
+    inside = [(np.concatenate([K[:7], K[7:] * 1.5]), V)]
+    assert np.max(np.abs(O.draft_block(cw, W, 7, inside, st) - z5)) > 1e-9
+
+
 def test_draft_block_invariant_to_common_position_shift():
     # scores depend on relative positions only: shifting the context's and the
     # block's positions together leaves the logits unchanged (anchor at P).

@@ -118,6 +118,8 @@ def lib():
         L.dflash2_select_path_ex.argtypes = [F(Config), F(Weights), I, P, P, P, F(DraftOpts), P, P, P, P, S, P]
         L.dflash2_select_top1.restype = I
         L.dflash2_select_top1.argtypes = [F(Config), I, P, P, F(DraftOpts), P, P, P, P, P]
+        L.dflash2_verify_sampled.restype = I
+        L.dflash2_verify_sampled.argtypes = [I, I, I, P, P, P, P, P, P, P, P, P, P, P, P]
         L.dflash2_verify_accept_ex.restype = I
         L.dflash2_verify_accept_ex.argtypes = [I, I, P, P, P, P, P, P, P, P, P, P]
         L.dflash2_test_layout.restype = I
@@ -278,6 +280,14 @@ def dflash2_select_top1(cfg, batch, cand_id, cand_logit, n_max, p_min, path, pat
     return _check("dflash2_select_top1", lib().dflash2_select_top1(
         ctypes.byref(cfg), batch, _ptr(cand_id), _ptr(cand_logit), _opts(n_max, p_min), _ptr(path),
         _ptr(path_score), _ptr(n_draft), _ptr(workspace), _stream(stream)))
+
+
+def dflash2_verify_sampled(batch, block_size, vocab, path, n_draft, target_prob, u_accept, u_sample, accept_len,
+                           out_tok, n_out, next_anchor, seq_len=None, counters=None, stream=None):
+    return _check("dflash2_verify_sampled", lib().dflash2_verify_sampled(
+        batch, block_size, vocab, _ptr(path), _ptr(n_draft), _ptr(target_prob), _ptr(u_accept), _ptr(u_sample),
+        _ptr(accept_len), _ptr(out_tok), _ptr(n_out), _ptr(next_anchor), _ptr(seq_len), _ptr(counters),
+        _stream(stream)))
 
 
 def dflash2_verify_accept_ex(batch, block_size, path, n_draft, target, accept_len, out_tok, n_out, next_anchor,

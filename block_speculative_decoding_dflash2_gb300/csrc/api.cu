@@ -830,6 +830,18 @@ int dflash2_verify_accept_ex(int batch, int block_size, const int32_t* path, con
                        counters, static_cast<cudaStream_t>(stream));
 }
 
+int dflash2_verify_sampled(int batch, int block_size, int vocab, const int32_t* path, const int32_t* n_draft,
+                           const float* target_prob, const float* u_accept, const float* u_sample,
+                           int32_t* accept_len, int32_t* out_tok, int32_t* n_out, int32_t* next_anchor,
+                           int32_t* seq_len, int64_t* counters, void* stream) {
+  if (block_size < 2 || block_size > 32) return DFLASH2_ERR_BLOCK_SIZE;
+  if (batch <= 0 || vocab < 2) return DFLASH2_ERR_SHAPE;
+  if (!path || !target_prob || !u_accept || !u_sample || !accept_len || !out_tok || !n_out || !next_anchor)
+    return DFLASH2_ERR_INVALID_ARG;
+  return launch_verify_sampled(batch, block_size, vocab, path, n_draft, target_prob, u_accept, u_sample, accept_len,
+                               out_tok, n_out, next_anchor, seq_len, counters, static_cast<cudaStream_t>(stream));
+}
+
 int dflash2_read_device_status(void* workspace, size_t ws_bytes, void* stream) {
   if (!workspace || ws_bytes < 256) return DFLASH2_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -210,6 +210,10 @@ int launch_viterbi(const float* Y, const float* table, const int32_t* anchor, in
                    const float* cand_logit, int batch, int D, int k, int r, int32_t* path, float* path_score,
                    const Ctx& c, int n_max = 0, float p_min = 0.f, int32_t* n_draft = nullptr);
 size_t viterbi_smem_bytes(int D, int k, int r);
+int launch_verify_sampled(int batch, int B, int V, const int32_t* path, const int32_t* n_draft, const float* prob,
+                          const float* u_accept, const float* u_sample, int32_t* accept_len, int32_t* out_tok,
+                          int32_t* n_out, int32_t* next_anchor, int32_t* seq_len, int64_t* counters,
+                          cudaStream_t st);
 // n_draft: nullable [batch] drafts kept per sequence (B-1 when null).
 int launch_verify(int batch, int B, const int32_t* path, const int32_t* n_draft, const int32_t* target,
                   int32_t* accept_len, int32_t* out_tok, int32_t* n_out, int32_t* next_anchor, int32_t* seq_len,

@@ -284,6 +284,28 @@ def make_agreeing_target(path, cfg, p, seed=None, stream="agree"):
     return t
 
 
+def make_target_probs(n_rows, V, seed, stream="target_probs", temperature=1.0, top_p=0.95, top_k=20, scale=3.0):
+    """Synthetic target distributions for sampled verification: N(0, scale)
+    logits, temperature, then the target's own truncation (top-k, then the
+    smallest top-p nucleus in probability order), renormalised; float32
+    [n_rows, V] with zeros outside the kept tokens.  The settings default to
+    the ones the DFlash 2 evaluations quote (1.0, 0.95, 20)."""
+    z = _rng(seed, stream).standard_normal((n_rows, V)) * scale / temperature
+    order = np.argsort(-z, axis=1, kind="stable")
+    zs = np.take_along_axis(z, order, axis=1)
+    keep = np.zeros_like(zs, dtype=bool)
+    keep[:, :min(top_k, V)] = True
+    ps = np.exp(zs - zs[:, :1]) * keep
+    ps /= ps.sum(axis=1, keepdims=True)
+    cum = np.cumsum(ps, axis=1)
+    keep &= (cum - ps) < top_p               # a token is kept while the mass before it is below top_p
+    ps = ps * keep
+    ps /= ps.sum(axis=1, keepdims=True)
+    out = np.zeros_like(ps)
+    np.put_along_axis(out, order, ps, axis=1)
+    return out.astype(np.float32)
+
+
 def paged_layout(ctx_cap, page_size, batch, seed, spare_pages=0):
     """Block table [batch, max_pages] as a seeded random permutation of
     physical pages; returns (block_table int32, n_pages)."""

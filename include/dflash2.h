@@ -412,6 +412,32 @@ int dflash2_verify_accept_ex(int batch, int block_size, const int32_t *path, con
                              int32_t *next_anchor, int32_t *seq_len, int64_t *counters, void *stream);
 
 /*
+ * Sampled verification (temperature > 0): lossless speculative sampling
+ * against the target's distribution ([Train]: spec_generate's temperature,
+ * top_p and top_k truncate the TARGET's distribution, the one rejection
+ * sampling verifies against, so sampled decoding stays lossless with
+ * respect to the target sampling on its own).  The selector's proposal is
+ * deterministic (a point mass on its path), so draft i is accepted when
+ * u_accept[s][i] < p_i(path_i); at the first rejection the emitted token is
+ * drawn from p_i with path_i removed (renormalised), and when every kept
+ * draft is accepted the bonus token is drawn from the next position's p.
+ * A draw maps u_sample[s] to the first token, in id order, whose cumulative
+ * mass exceeds u_sample[s] times the total (inverse CDF).
+ *   target_prob  [batch, B, vocab] float: p_i for i = 0..B-1, the target's
+ *                distribution after [anchor, path_1..path_i] with its own
+ *                temperature / top-p / top-k applied (zeros outside)
+ *   u_accept     [batch, B-1] float in [0, 1): the acceptance draws
+ *   u_sample     [batch] float in [0, 1): the draw of the emitted token
+ *   n_draft      nullable [batch]: drafts kept per sequence (B-1 when null)
+ * Outputs, seq_len and counters as dflash2_verify_accept_ex.  Random numbers
+ * are inputs, so a call is deterministic.  DFLASH2_ERR_SHAPE for vocab < 2.
+ */
+int dflash2_verify_sampled(int batch, int block_size, int vocab, const int32_t *path, const int32_t *n_draft,
+                           const float *target_prob, const float *u_accept, const float *u_sample,
+                           int32_t *accept_len, int32_t *out_tok, int32_t *n_out, int32_t *next_anchor,
+                           int32_t *seq_len, int64_t *counters, void *stream);
+
+/*
  * Instrumentation.  Number of kernel launches the library has issued since
  * it was loaded (host-side counter; a launch recorded into a CUDA graph
  * counts once, at capture).

@@ -36,6 +36,7 @@ __all__ = [
     "project_features", "context_kv", "append_context", "block_attention",
     "draft_layer", "draft_block", "topk", "draft_step", "selector_factors",
     "select_path", "select_path_knobs", "transition_logprobs", "brute_force_path", "path_score", "verify_accept",
+    "verify_sampled",
     "Counters", "loss_decay_weights", "toy_target_next", "greedy_generate",
     "speculative_generate",
 ]
@@ -509,6 +510,40 @@ def verify_accept(path, target):
     while a < D and path[a] == target[a]:
         a += 1
     return a, path[:a] + [target[a]], target[a]
+
+
+def verify_sampled(path, prob, u_accept, u_sample):
+    """Sampled (temperature > 0) verification of one proposal.  (A reading
+    where the pages are silent on the mechanics.)
+
+    [Train] (spec_generate): temperature, top_p and top_k truncate the
+    target's distribution, the one rejection sampling verifies against, so
+    sampled decoding stays lossless with respect to the target sampling on
+    its own; [llama] "Configuration Notes": DFlash2 proposes through its
+    selector lattice, not by sampling the vocabulary.  Reading taken: the
+    proposal is a point mass on the selector's path, so the rejection rule
+    min(1, p/q) becomes "accept draft i when u_accept[i] < p_i(path_i)"; at
+    the first rejection the emitted token is drawn from p_i with path_i
+    removed and renormalised (the residual max(0, p - q)); when every draft
+    is accepted the bonus token is drawn from p_D.  A draw is the inverse
+    CDF in token-id order: the first token whose cumulative mass exceeds
+    u_sample times the total.
+    path [n] kept drafts; prob [>= n+1, V] rows p_0..p_n; u_accept [>= n];
+    u_sample scalar.  Returns (a, emitted tokens [a+1], next anchor).
+    """
+    path = [int(x) for x in path]
+    prob = np.asarray(prob, dtype=np.float64)
+    n = len(path)
+    a = 0
+    while a < n and float(u_accept[a]) < prob[a, path[a]]:
+        a += 1
+    row = prob[a].copy()
+    if a < n:
+        row[path[a]] = 0.0
+    cdf = np.cumsum(row)
+    v = int(np.searchsorted(cdf, float(u_sample) * cdf[-1], side="right"))
+    v = min(v, len(row) - 1)
+    return a, path[:a] + [v], v
 
 
 class Counters:

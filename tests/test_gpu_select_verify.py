@@ -237,6 +237,85 @@ def test_verify_with_fewer_drafts_matches_oracle():
     np.testing.assert_array_equal(c[4 + B_:], cnt.acc_pos)
 
 
+@pytest.mark.parametrize("V,B_,b", [(1000, 8, 64), (151936, 8, 16), (5000, 16, 32)])
+def test_sampled_verify_matches_oracle(V, B_, b):
+    """Sampled (temperature > 0) verification against the oracle on the same
+    target distributions and draws: accept lengths and counters exactly; the
+    emitted token exactly, or, where fp32 and fp64 cumulative sums straddle
+    the draw's threshold, a token the fp64 inverse CDF also admits."""
+    import torch
+    B = lib()
+    D = B_ - 1
+    g = np.random.default_rng(V + B_)
+    prob = S.make_target_probs(b * B_, V, seed=V + B_).reshape(b, B_, V)
+    # proposals: each position's most likely token, a kept token, or any token
+    pick = g.random((b, D))
+    best = prob[:, :D].argmax(axis=2)
+    kept = np.array([[g.choice(np.nonzero(prob[s, i])[0]) for i in range(D)] for s in range(b)])
+    paths = np.where(pick < 0.6, best, np.where(pick < 0.85, kept, g.integers(0, V, (b, D))))
+    nd = np.where(g.random(b) < 0.7, D, g.integers(0, D + 1, b))
+    paths = np.where(np.arange(D)[None, :] < nd[:, None], paths, -1)
+    ua = g.random((b, D)).astype(np.float32)
+    us = g.random(b).astype(np.float32)
+    dev = lambda a, dt=np.int32: torch.from_numpy(np.ascontiguousarray(a, dtype=dt)).cuda()
+    acc = torch.full((b,), -9, dtype=torch.int32, device="cuda")
+    out = torch.full((b, B_), -9, dtype=torch.int32, device="cuda")
+    n_out = torch.zeros(b, dtype=torch.int32, device="cuda")
+    nxt = torch.zeros(b, dtype=torch.int32, device="cuda")
+    seq = dev(np.zeros(b))
+    counters = torch.zeros(4 + 2 * B_ - 1, dtype=torch.int64, device="cuda")
+    B.dflash2_verify_sampled(b, B_, V, dev(paths), dev(nd), dev(prob, np.float32), dev(ua, np.float32),
+                             dev(us, np.float32), acc, out, n_out, nxt, seq, counters)
+    torch.cuda.synchronize()
+    acc, out, nxt, seq = acc.cpu().numpy(), out.cpu().numpy(), nxt.cpu().numpy(), seq.cpu().numpy()
+    cnt = O.Counters(D)
+    straddle = 0
+    for s in range(b):
+        a, toks, na = O.verify_sampled(paths[s, :nd[s]], prob[s], ua[s], us[s])
+        cnt.add(a, int(nd[s]))
+        assert acc[s] == a and seq[s] == a + 1
+        assert list(out[s, :a]) == toks[:a] and np.all(out[s, a + 1:] == -1) and out[s, a] == nxt[s]
+        if nxt[s] != na:
+            row = prob[s, a].astype(np.float64).copy()
+            if a < nd[s]:
+                row[paths[s, a]] = 0.0
+            cdf = np.cumsum(row)
+            thr = float(us[s]) * cdf[-1]
+            v = int(nxt[s])
+            lo = cdf[v - 1] if v > 0 else 0.0
+            assert row[v] > 0 and lo <= thr * (1 + 1e-5) + 1e-7 and cdf[v] >= thr * (1 - 1e-5) - 1e-7, (s, v, na)
+            straddle += 1
+    assert straddle <= max(1, b // 16)
+    c = counters.cpu().numpy()
+    assert c[0] == cnt.steps and c[1] == cnt.drafted and c[2] == cnt.accepted and c[3] == cnt.rollback
+    np.testing.assert_array_equal(c[4:4 + B_], cnt.hist)
+    np.testing.assert_array_equal(c[4 + B_:], cnt.acc_pos)
+    assert 0 < cnt.accepted < cnt.drafted  # both outcomes occur
+
+
+def test_sampled_verify_is_greedy_at_temperature_zero():
+    # one-hot target rows: the sampled rule reduces to the greedy one
+    import torch
+    B = lib()
+    g = np.random.default_rng(90)
+    b, B_, V = 128, 8, 300
+    D = B_ - 1
+    target = g.integers(0, V, (b, B_))
+    paths = np.where(g.random((b, D)) < 0.7, target[:, :D], g.integers(0, V, (b, D)))
+    prob = np.zeros((b, B_, V), dtype=np.float32)
+    np.put_along_axis(prob, target[:, :, None], 1.0, axis=2)
+    dev = lambda a, dt=np.int32: torch.from_numpy(np.ascontiguousarray(a, dtype=dt)).cuda()
+    outs = [torch.zeros(b, dtype=torch.int32, device="cuda"), torch.zeros((b, B_), dtype=torch.int32, device="cuda"),
+            torch.zeros(b, dtype=torch.int32, device="cuda"), torch.zeros(b, dtype=torch.int32, device="cuda")]
+    B.dflash2_verify_sampled(b, B_, V, dev(paths), None, dev(prob, np.float32),
+                             dev(g.random((b, D)), np.float32), dev(g.random(b), np.float32), *outs)
+    torch.cuda.synchronize()
+    acc, out, _, nxt = [t.cpu().numpy() for t in outs]
+    for s in range(b):
+        a, toks, na = O.verify_accept(paths[s], target[s])
+        assert acc[s] == a and nxt[s] == na and list(out[s, :a + 1]) == toks
+
+
 def _verify(paths, targets, B_, seq_len=None, counters=None):
     import torch
     B = lib()

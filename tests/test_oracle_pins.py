@@ -466,6 +466,46 @@ def test_verify_golden_cases():
         assert gn == int(nxt)
 
 
+def test_sampled_verify_at_temperature_zero_is_greedy():
+    # one-hot target rows (temperature 0): sampled verification equals the
+    # greedy rule for any draws
+    g = np.random.default_rng(40)
+    V, D = 6, 5
+    for _ in range(200):
+        target = g.integers(0, V, D + 1)
+        path = np.where(g.random(D) < 0.6, target[:D], g.integers(0, V, D))
+        prob = np.eye(V)[target]
+        got = O.verify_sampled(path, prob, g.random(D), g.random())
+        assert got == O.verify_accept(path, target)
+
+
+def test_sampled_verify_first_token_follows_the_target():
+    # losslessness: whatever the draft proposes, the first emitted token is
+    # distributed as the target's p_0 (chi-square over 40k draws, V = 6)
+    g = np.random.default_rng(41)
+    p0 = np.array([0.05, 0.3, 0.15, 0.25, 0.05, 0.2])
+    prob = np.stack([p0, np.full(6, 1 / 6)])
+    n = 40000
+    for draft in (1, 4):            # a likely and an unlikely proposal
+        counts = np.zeros(6)
+        for _ in range(n):
+            _, toks, _ = O.verify_sampled([draft], prob, [g.random()], g.random())
+            counts[toks[0]] += 1
+        chi2 = float(np.sum((counts - n * p0) ** 2 / (n * p0)))
+        assert chi2 < 25.0, (draft, chi2, counts / n)   # 5 dof: p < 1e-4
+
+
+def test_sampled_verify_hand_cases():
+    prob = np.array([[0.1, 0.6, 0.3], [0.2, 0.3, 0.5], [0.2, 0.3, 0.5]])
+    # both drafts accepted (u below p): the bonus draw from row 2, cdf 0.2, 0.5, 1.0
+    assert O.verify_sampled([1, 2], prob, [0.59, 0.49], 0.45) == (2, [1, 2, 1], 1)
+    assert O.verify_sampled([1, 2], prob, [0.59, 0.49], 0.1) == (2, [1, 2, 0], 0)
+    # first draft rejected (u = 0.6 is not below 0.6): residual [0.1, 0, 0.3]
+    # / 0.4, cdf 0.25, 0.25, 1.0: u 0.2 -> token 0, u 0.5 -> token 2
+    assert O.verify_sampled([1, 2], prob, [0.6, 0.0], 0.2) == (0, [0], 0)
+    assert O.verify_sampled([1, 2], prob, [0.6, 0.0], 0.5) == (0, [2], 2)
+
+
 def test_counters_with_fewer_drafts():
     # drafted counts the drafts kept; rollback = drafted - accepted
     c = O.Counters(7)

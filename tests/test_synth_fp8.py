@@ -65,3 +65,18 @@ def test_row_quantisation_scale_and_values():
     # for normals, 2^-10 * scale absolute in the subnormal range
     err = np.abs(t.values - w)
     assert np.all(err <= np.maximum(np.abs(w) * 2.0 ** -4, 2.0 ** -10 * t.scale[:, None]) + 1e-12)
+
+
+def test_target_probs_truncation():
+    # the synthetic target distributions: each row sums to 1, keeps at most
+    # top_k tokens, and its kept set is the smallest prefix (in probability
+    # order) whose mass reaches top_p
+    p = S.make_target_probs(50, 300, seed=3, top_p=0.9, top_k=20)
+    assert p.dtype == np.float32 and p.shape == (50, 300)
+    np.testing.assert_allclose(p.sum(1), 1.0, atol=1e-5)
+    for row in p.astype(np.float64):
+        kept = np.sort(row[row > 0])[::-1]
+        assert 1 <= kept.size <= 20
+        # dropping the smallest kept token would leave less than top_p of the
+        # (top-k renormalised) mass, so it had to stay
+        assert np.all(np.diff(kept) <= 1e-12)

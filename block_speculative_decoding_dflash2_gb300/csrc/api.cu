@@ -89,6 +89,8 @@ int check_config(const dflash2_config* c) {
   if (c->n_q_heads % c->n_kv_heads) return DFLASH2_ERR_SHAPE;
   if (c->conv_kernel_size != 2 && c->conv_kernel_size != 0) return DFLASH2_ERR_SHAPE;  // DFlash 2, or v1 (none)
   if (c->sliding_window < 0) return DFLASH2_ERR_SHAPE;
+  // fp8 weight rows are read in 16-byte units (TMA rows, staged tap rows)
+  if (c->dtype == DFLASH2_FP8W && (c->hidden % 16 || c->intermediate % 16)) return DFLASH2_ERR_SHAPE;
   if (c->conv_group_size <= 0 || c->hidden % c->conv_group_size) return DFLASH2_ERR_SHAPE;
   if (c->top_k < 1 || c->top_k > KMAX || c->top_k > c->vocab) return DFLASH2_ERR_SHAPE;
   if (c->selector_rank < 1 || c->selector_rank > 128) return DFLASH2_ERR_SHAPE;

@@ -318,6 +318,25 @@ __global__ void __launch_bounds__(RT) dyn_conv_kernel(const T* __restrict__ u, c
 constexpr int PT = 512;  // threads of the prologue kernel
 constexpr int PUB = 16;  // 4-element vectors per lane and round (bf16)
 
+// Bytes of a row of H elements of es bytes in the prologue's shared memory:
+// whole 16-byte units plus 16 bytes of padding.
+__host__ __device__ __forceinline__ int prologue_row_bytes(int H, int es) { return (H * es + 15) / 16 * 16 + 16; }
+
+// bf16 tensor-core helpers (mma.sync m16n8k16, ldmatrix), for the tap logits
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// four 8x8 b16 matrices, lane i supplying the address of row i % 8 of matrix i / 8
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+
 template <typename T>
 struct Vec4Raw;  // 4 elements as loaded, converted to float4 at use
 template <>
@@ -362,18 +381,26 @@ __global__ void __launch_bounds__(PT) conv_prologue_kernel(
   using XT = typename std::conditional<EMBED, T, float>::type;  // element type of the source rows
   const int s = blockIdx.y, G = H / gs;
   const int g0 = blockIdx.x * gpc, ng = min(gpc, G - g0);
-  T* us = reinterpret_cast<T*>(smraw);                 // [B][H] normed rows as stored
-  WT* wsm = reinterpret_cast<WT*>(us + (size_t)B * H); // [2 gpc][H] tap rows (stage_w)
-  float* rinv = reinterpret_cast<float*>(wsm + (stage_w ? (size_t)2 * gpc * H : 0));  // [B]
+  // rows are padded by 16 bytes (HP elements apart) so the 8 rows an
+  // ldmatrix reads start in different banks
+  const int HP = prologue_row_bytes(H, sizeof(T)) / (int)sizeof(T);
+  const int WP = prologue_row_bytes(H, sizeof(WT)) / (int)sizeof(WT);
+  T* us = reinterpret_cast<T*>(smraw);                 // [B][HP] normed rows as stored
+  WT* wsm = reinterpret_cast<WT*>(us + (size_t)B * HP); // [2 gpc][WP] tap rows (stage_w)
+  float* rinv = reinterpret_cast<float*>(wsm + (stage_w ? (size_t)2 * gpc * WP : 0));  // [B]
   float* lam = rinv + B;                               // [B][2 gpc] tap logits, then alpha
   float* red = lam + B * 2 * gpc;                      // [B][NW] partial sums of squares
+  float* red2 = red + B * NW;                          // [NW][2][16][8] tensor-core partial logits
   __shared__ int toks[32];
   pdl_launch_next();
   if (stage_w) {  // the weights are not written by any kernel of the stream
     constexpr int E16 = 16 / sizeof(WT);
     const WT* src = Wt + (size_t)2 * g0 * H;
-    for (int i = threadIdx.x; i < 2 * ng * H / E16; i += PT)
-      cp_async16(wsm + (size_t)i * E16, src + (size_t)i * E16, true);
+    const int per_row = H / E16;
+    for (int i = threadIdx.x; i < 2 * ng * per_row; i += PT) {
+      const int row = i / per_row, c = (i - row * per_row) * E16;
+      cp_async16(wsm + (size_t)row * WP + c, src + (size_t)row * H + c, true);
+    }
     cp_async_commit();
   }
   pdl_wait();
@@ -460,17 +487,66 @@ __global__ void __launch_bounds__(PT) conv_prologue_kernel(
           if (m0 + 128 * k < m1) {
             float4 v = x ? xv[k].f() : make_float4(0.f, 0.f, 0.f, 0.f);
             v = make_float4(xs * v.x, xs * v.y, xs * v.z, xs * v.w);
-            st4(us + (size_t)t * H + m0 + 128 * k, scale4(v, r, gv[k].f()));
+            st4(us + (size_t)t * HP + m0 + 128 * k, scale4(v, r, gv[k].f()));
           }
       }
     }
   }
   if (stage_w) cp_async_wait<0>();
   __syncthreads();
-  // 3. tap logits of this CTA's groups: one warp per (row, tap row)
+  // 3. tap logits of this CTA's groups.  bf16 rows staged in shared memory:
+  //    on the tensor cores, lambda[t][jj] = sum_h u[t][h] W[jj][h] as
+  //    m16n8k16 tiles (A = 16 block rows, B = 16 tap rows as two n8 tiles;
+  //    rows past the real ones repeat the last real row and their results
+  //    are dropped), the K range split across the warps and the partial
+  //    tiles summed through shared memory.  Otherwise one warp per (row,
+  //    tap row) on the CUDA cores.
+  constexpr bool MMA = std::is_same<T, bf16>::value && std::is_same<WT, bf16>::value;
+  const int mtiles = (B + 15) / 16, ntiles = (2 * ng + 15) / 16, tiles = mtiles * ntiles;
+  if (MMA && stage_w && H % 16 == 0 && tiles <= NW) {
+    const int ksplit = NW / tiles;  // warps per tile (the K range in slices)
+    const int tile = warp / ksplit, ks = warp % ksplit;
+    if (tile < tiles) {
+      const int mt = tile / ntiles, nt = tile % ntiles;
+      const int nk = H / 16, kb = ks * nk / ksplit, ke = (ks + 1) * nk / ksplit;
+      const int mi = lane >> 3;
+      const int ar = min(mt * 16 + (mi & 1) * 8 + (lane & 7), B - 1);            // A row (block row)
+      const int br = min(nt * 16 + (mi >> 1) * 8 + (lane & 7), 2 * ng - 1);      // B row (tap row)
+      const bf16* ap = reinterpret_cast<const bf16*>(us) + (size_t)ar * HP + (mi >> 1) * 8;
+      const bf16* bp = reinterpret_cast<const bf16*>(wsm) + (size_t)br * WP + (mi & 1) * 8;
+      float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int kk = kb; kk < ke; ++kk) {
+        uint32_t a[4], b[4];
+        ldmatrix_x4(a, ap + kk * 16);
+        ldmatrix_x4(b, bp + kk * 16);
+        mma_bf16_16816(c0, a, b[0], b[1]);
+        mma_bf16_16816(c1, a, b[2], b[3]);
+      }
+      // partial tile -> red2[warp]: [n8 tile][row 16][col 8]
+      float* o = red2 + (size_t)warp * 256;
+      const int r0 = lane >> 2, cc = (lane & 3) * 2;
+      o[r0 * 8 + cc] = c0[0];
+      o[r0 * 8 + cc + 1] = c0[1];
+      o[(r0 + 8) * 8 + cc] = c0[2];
+      o[(r0 + 8) * 8 + cc + 1] = c0[3];
+      o[128 + r0 * 8 + cc] = c1[0];
+      o[128 + r0 * 8 + cc + 1] = c1[1];
+      o[128 + (r0 + 8) * 8 + cc] = c1[2];
+      o[128 + (r0 + 8) * 8 + cc + 1] = c1[3];
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < B * 2 * ng; idx += PT) {
+      const int t = idx / (2 * ng), jj = idx % (2 * ng);
+      const int mt = t / 16, nt = jj / 16, tl = mt * ntiles + nt;
+      const int e = ((jj % 16) / 8) * 128 + (t % 16) * 8 + jj % 8;
+      float acc = 0.f;
+      for (int k2 = 0; k2 < ksplit; ++k2) acc += red2[(size_t)(tl * ksplit + k2) * 256 + e];
+      lam[t * 2 * gpc + jj] = wsc ? acc * wsc[2 * g0 + jj] : acc;
+    }
+  } else
   for (int p = warp; p < B * 2 * ng; p += NW) {
     const int t = p / (2 * ng), jj = p % (2 * ng);
-    const WT* w = stage_w ? wsm + (size_t)jj * H : Wt + (size_t)(2 * g0 + jj) * H;
+    const WT* w = stage_w ? wsm + (size_t)jj * WP : Wt + (size_t)(2 * g0 + jj) * H;
     float acc = 0.f;
     for (int m0 = lane * 4; m0 < H; m0 += 128 * PU) {
       Vec4Raw<WT> wv[PU];
@@ -480,7 +556,7 @@ __global__ void __launch_bounds__(PT) conv_prologue_kernel(
 #pragma unroll
       for (int k = 0; k < PU; ++k)
         if (m0 + 128 * k < H) {
-          const float4 wf = wv[k].f(), uv = ld4(us + (size_t)t * H + m0 + 128 * k);
+          const float4 wf = wv[k].f(), uv = ld4(us + (size_t)t * HP + m0 + 128 * k);
           acc += wf.x * uv.x + wf.y * uv.y + wf.z * uv.z + wf.w * uv.w;
         }
     }
@@ -505,8 +581,8 @@ __global__ void __launch_bounds__(PT) conv_prologue_kernel(
     const int t = idx / nc, cc = idx % nc, m = c0 + cc;
     const float* a = lam + t * 2 * gpc + 2 * (cc / gs);  // gs % 4 == 0: the 4 channels share a group
     const float a0 = a[0], a1 = a[1];
-    const float4 ut = ld4(us + (size_t)t * H + m);
-    const float4 up = t > 0 ? ld4(us + (size_t)(t - 1) * H + m) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 ut = ld4(us + (size_t)t * HP + m);
+    const float4 up = t > 0 ? ld4(us + (size_t)(t - 1) * HP + m) : make_float4(0.f, 0.f, 0.f, 0.f);
     const size_t o = ((size_t)s * B + t) * H + m;
     st4(u_out + o, ut);
     st4(u2_out + o, make_float4(ut.x + a0 * ut.x + a1 * up.x, ut.y + a0 * ut.y + a1 * up.y,
@@ -645,9 +721,9 @@ int launch_dyn_conv(int dtype, const void* u, const float* Y, int rows, int H, i
 // Shared memory of the prologue: the B normed rows, the CTA's tap rows when
 // staged, 1/rms, tap logits and the per-warp partial sums.
 size_t conv_prologue_smem(int dtype, int B, int H, int gpc, bool stage_w, bool w8) {
-  const size_t es = dtype == DFLASH2_BF16 ? 2 : 4;
-  return (size_t)B * H * es + (stage_w ? (size_t)2 * gpc * H * (w8 ? 1 : es) : 0) +
-         (size_t)B * (1 + 2 * gpc + PT / 32) * sizeof(float);
+  const int es = dtype == DFLASH2_BF16 ? 2 : 4, ws = w8 ? 1 : es;
+  return (size_t)B * prologue_row_bytes(H, es) + (stage_w ? (size_t)2 * gpc * prologue_row_bytes(H, ws) : 0) +
+         (size_t)B * (1 + 2 * gpc + PT / 32) * sizeof(float) + (size_t)(PT / 32) * 256 * sizeof(float);
 }
 
 int conv_prologue_groups(int G, int batch, int nsm) {

@@ -256,41 +256,46 @@ __global__ void __launch_bounds__(512) viterbi_kernel(const float* __restrict__ 
     }
   }
   __syncthreads();
-  // 3. the max-plus recurrence over positions and the backtrack, in one warp:
-  //    lane j holds delta[j]; ties keep the smaller predecessor (strict >,
-  //    predecessors in ascending order) and, at the end, the smaller index
-  //    over the first Dp positions (draft_n_max), then the cut at the first
-  //    chosen transition whose log-probability is below log(p_min)
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    float dl = lane < k ? Sm[lane] : -INFINITY;
+  // 3. the max-plus recurrence over the first Dp positions (draft_n_max):
+  //    thread (j, p) of the first 256 forms delta[p] + T_i(p, j), and each
+  //    half-warp (one j) reduces its 16 predecessors with shuffles, keeping
+  //    the larger value and, on a tie, the smaller predecessor; then the
+  //    backtrack and the cut at the first chosen transition whose
+  //    log-probability is below log(p_min)
+  __shared__ float dsm[2][16];
+  if (threadIdx.x < 256) {
+    const int j = threadIdx.x >> 4, p = threadIdx.x & 15;
+    const unsigned hmask = (threadIdx.x & 16) ? 0xffff0000u : 0x0000ffffu;
+    if (p == 0 && j < k) dsm[0][j] = Sm[j];
+    asm volatile("bar.sync 1, 256;" ::: "memory");
     for (int i = 1; i < Dp; ++i) {
       const float* T = Sm + (1 + (i - 1) * k) * k;  // [p][j]
-      float best = -INFINITY;
-      int arg = 0;
-      for (int p = 0; p < k; ++p) {
-        const float v = __shfl_sync(0xffffffffu, dl, p) + (lane < k ? T[p * k + lane] : 0.f);
-        if (v > best) {
-          best = v;
-          arg = p;
+      float v = (p < k && j < k) ? dsm[(i - 1) & 1][p] + T[p * k + j] : -INFINITY;
+      int arg = p;
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) {
+        const float v2 = __shfl_xor_sync(hmask, v, o);
+        const int a2 = __shfl_xor_sync(hmask, arg, o);
+        if (v2 > v || (v2 == v && a2 < arg)) {
+          v = v2;
+          arg = a2;
         }
       }
-      if (lane < k) {
-        dl = best;
-        bp[i * k + lane] = arg;
+      if (p == 0 && j < k) {
+        dsm[i & 1][j] = v;
+        bp[i * k + j] = arg;
       }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
     }
-    __syncwarp();
-    int jb = 0;
-    float vb = __shfl_sync(0xffffffffu, dl, 0);
-    for (int jj = 1; jj < k; ++jj) {
-      const float v = __shfl_sync(0xffffffffu, dl, jj);
-      if (v > vb) {
-        vb = v;
-        jb = jj;
-      }
-    }
-    if (lane == 0) {
+    if (threadIdx.x == 0) {
+      const float* dl = dsm[(Dp - 1) & 1];
+      int jb = 0;
+      float vb = dl[0];
+      for (int jj = 1; jj < k; ++jj)
+        if (dl[jj] > vb) {
+          vb = dl[jj];
+          jb = jj;
+        }
       int js[32];
       int j = jb;
       for (int i = Dp - 1; i >= 0; --i) {

@@ -323,17 +323,36 @@ def run_ours(a, rank, world):
         r.verify(d_target, seq)
         h_res.copy_(r.results, non_blocking=True)
 
+    # the caller captures the step, copies included, as one CUDA graph (the
+    # calls are graph-capturable) and replays it every step; the eager loop
+    # of the same calls is reported beside it
     for _ in range(3):
         e2e_step()
     torch.cuda.synchronize()
-    e2e_ms = []
+    ge = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        e2e_step()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(ge, stream=s):
+            e2e_step()
+    for _ in range(3):
+        ge.replay()
+    torch.cuda.synchronize()
+    e2e_ms, eager_ms = [], []
+    for _ in range(a.steps):
+        t0.record()
+        ge.replay()
+        t1.record()
+        t1.synchronize()
+        e2e_ms.append(t0.elapsed_time(t1))
     for _ in range(a.steps):
         t0.record()
         e2e_step()
         t1.record()
         t1.synchronize()
-        e2e_ms.append(t0.elapsed_time(t1))
+        eager_ms.append(t0.elapsed_time(t1))
     e2e_total = max_over_ranks(sum(e2e_ms), "cuda")
+    eager_total = max_over_ranks(sum(eager_ms), "cuda")
 
     pk, src = peaks()
     bytes_, flops, lm_bytes = work_model(cfg, [int(x) for x in ctx], [int(x) for x in n_new])
@@ -380,7 +399,9 @@ def run_ours(a, rank, world):
         "clocks": clocks,
         "e2e": {"value": whole_job_rate(a.steps, world, e2e_total), "unit": "draft steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "api": "dflash2_draft_step + dflash2_select_path_table + dflash2_verify_accept, eager"},
+                "api": "dflash2_draft_step + dflash2_select_path_table + dflash2_verify_accept with the "
+                       "H2D/D2H copies, captured once by the caller as a CUDA graph and replayed per step",
+                "eager_value": whole_job_rate(a.steps, world, eager_total)},
         "gpu_launches": launches_per_step * a.steps,
         "gpu_launches_per_step": launches_per_step,
     }

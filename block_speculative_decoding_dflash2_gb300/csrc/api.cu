@@ -212,6 +212,7 @@ int device_ctx(Ctx* ctx, void* stream, void* ws) {
 struct SideStream {
   cudaStream_t s;
   cudaEvent_t fork, join;
+  int prio = 0;  // the device's greatest stream priority
 };
 std::mutex g_side_mu;
 
@@ -222,7 +223,9 @@ int side_stream(SideStream* out) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DFLASH2_ERR_CUDA;
   if (!made[dev]) {
     SideStream sd;
-    if (cudaStreamCreateWithFlags(&sd.s, cudaStreamNonBlocking) != cudaSuccess ||
+    int least = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &sd.prio) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&sd.s, cudaStreamNonBlocking) != cudaSuccess ||
         cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming) != cudaSuccess)
       return DFLASH2_ERR_CUDA;
@@ -542,6 +545,7 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
     Ctx actx = ctx;
     actx.stream = side.s;
     actx.pdl = false;  // full dependency on the fork event
+    actx.prio = kSidePriority ? side.prio : 0;
     if (split_sms) actx.nsm = ctx.nsm - kForkPrologueSMs;
     if (merged)
       TRY(project_features(c, *w, sc, n_pages, block_table, max_pages, batch, ctx_len, n_new, new_taps, new_off,

@@ -14,6 +14,7 @@ struct Ctx {
   unsigned* status;  // device status word (workspace offset 0)
   int nsm;           // SMs of the current device
   bool pdl = true;   // launch with programmatic stream serialization
+  int prio = 0;      // launch priority (0: the stream's own; lower numbers run first)
 };
 
 // One dense contraction out[n][m] = sum_k W[m][k] * X[n][k]  (swap-AB: the
@@ -73,6 +74,10 @@ constexpr int kMaxSM = 256;  // CTAs of a stream-K launch, and its counter array
 // SMs left to the fused embedding prologue while the side stream's feature
 // contraction runs beside it (the contraction takes the rest).
 constexpr int kForkPrologueSMs = 32;
+// Whether the side stream's stage (a) kernels launch at the device's
+// greatest priority, so that the block scheduler places their CTAs before
+// the block branch's when SMs free up.
+constexpr bool kSidePriority = true;
 
 // Host-side count of kernel launches (instrumentation).
 void count_launch(int n = 1);
@@ -94,8 +99,13 @@ inline int launch_kx(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = c.stream;
-  cudaLaunchAttribute at[2];
+  cudaLaunchAttribute at[3];
   int n = 0;
+  if (c.prio != 0) {
+    at[n].id = cudaLaunchAttributePriority;
+    at[n].val.priority = c.prio;
+    ++n;
+  }
   if (c.pdl) {
     at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[n].val.programmaticStreamSerializationAllowed = 1;

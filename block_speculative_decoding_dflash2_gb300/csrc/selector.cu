@@ -167,56 +167,57 @@ __global__ void __launch_bounds__(512) viterbi_kernel(const float* __restrict__ 
   __syncthreads();
   // 1. every transition score at once (they do not depend on the DP): row 0 is
   //    position 1 after the anchor; row 1 + (i-1)k + p is position i+1 after
-  //    candidate p of position i.  A thread computes a 4 x 4 tile (4
-  //    predecessors x 4 candidates of one position): each factor it loads
-  //    serves 4 products, which keeps the shared-memory traffic at a quarter
-  //    of one dot product per score.
+  //    candidate p of position i.  A thread computes a TS x TS tile (TS
+  //    predecessors x TS candidates of one position): each factor it loads
+  //    serves TS products, and the tiles spread over most of the CTA's threads.
+  constexpr int TS = 2;
   const int nrow = 1 + (D - 1) * k;
-  const int k4 = (k + 3) / 4;
-  const int n_tiles = k4 + (D - 1) * k4 * k4;
+  const int kt = (k + TS - 1) / TS;
+  const int n_tiles = kt + (D - 1) * kt * kt;
   for (int tile = threadIdx.x; tile < n_tiles; tile += blockDim.x) {
     int i, p0, j0, np;
-    if (tile < k4) {  // position 1: the anchor is the only predecessor
+    if (tile < kt) {  // position 1: the anchor is the only predecessor
       i = 0;
       p0 = 0;
       np = 1;
-      j0 = 4 * tile;
+      j0 = TS * tile;
     } else {
-      const int t = tile - k4;
-      i = 1 + t / (k4 * k4);
-      const int rem = t % (k4 * k4);
-      p0 = 4 * (rem / k4);
-      j0 = 4 * (rem % k4);
-      np = min(4, k - p0);
+      const int t = tile - kt;
+      i = 1 + t / (kt * kt);
+      const int rem = t % (kt * kt);
+      p0 = TS * (rem / kt);
+      j0 = TS * (rem % kt);
+      np = min(TS, k - p0);
     }
-    const int nj = min(4, k - j0);
-    const float* arow[4];
-    const float* brow[4];
+    const int nj = min(TS, k - j0);
+    const float* arow[TS];
+    const float* brow[TS];
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
+    for (int a = 0; a < TS; ++a) {
       const int p = p0 + min(a, np - 1), j = j0 + min(a, nj - 1);  // clamped: spare lanes recompute an edge
       arow[a] = F + (size_t)(i == 0 ? 0 : 1 + (i - 1) * k + p) * ws;
       brow[a] = F + (size_t)(1 + i * k + j) * ws + r;
     }
-    float acc[4][4];
+    float acc[TS][TS];
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int a = 0; a < TS; ++a)
 #pragma unroll
-      for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+      for (int b = 0; b < TS; ++b) acc[a][b] = 0.f;
     if (!pairwise) {
       // no pairwise term: S = the candidate logits alone
     } else if ((r & 3) == 0) {
+#pragma unroll 4
       for (int c = 0; c < r; c += 4) {
-        float4 x[4], y[4];
+        float4 x[TS], y[TS];
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
+        for (int a = 0; a < TS; ++a) {
           x[a] = *reinterpret_cast<const float4*>(arow[a] + c);
           y[a] = *reinterpret_cast<const float4*>(brow[a] + c);
         }
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
+        for (int a = 0; a < TS; ++a)
 #pragma unroll
-          for (int b = 0; b < 4; ++b) {
+          for (int b = 0; b < TS; ++b) {
             acc[a][b] = fmaf(x[a].x, y[b].x, acc[a][b]);
             acc[a][b] = fmaf(x[a].y, y[b].y, acc[a][b]);
             acc[a][b] = fmaf(x[a].z, y[b].z, acc[a][b]);
@@ -226,15 +227,15 @@ __global__ void __launch_bounds__(512) viterbi_kernel(const float* __restrict__ 
     } else {
       for (int c = 0; c < r; ++c)
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
+        for (int a = 0; a < TS; ++a)
 #pragma unroll
-          for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(arow[a][c], brow[b][c], acc[a][b]);
+          for (int b = 0; b < TS; ++b) acc[a][b] = fmaf(arow[a][c], brow[b][c], acc[a][b]);
     }
     const int row0 = i == 0 ? 0 : 1 + (i - 1) * k + p0;
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int a = 0; a < TS; ++a)
 #pragma unroll
-      for (int b = 0; b < 4; ++b)
+      for (int b = 0; b < TS; ++b)
         if (a < np && b < nj) Sm[(row0 + a) * k + j0 + b] = zs[i * k + j0 + b] + acc[a][b];
   }
   __syncthreads();

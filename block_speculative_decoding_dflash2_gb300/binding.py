@@ -102,6 +102,8 @@ def lib():
         L.dflash2_test_gemm.restype = I
         L.dflash2_test_gemm.argtypes = [I, P, I, I, P, I, I, I, P, P, S, P]
         L.dflash2_test_gemm_fp8.restype = I
+        L.dflash2_test_force_cluster_split.restype = I
+        L.dflash2_test_force_cluster_split.argtypes = [I]
         L.dflash2_test_gemm_fp8.argtypes = [P, P, I, I, P, I, I, I, P, P, S, P]
         L.dflash2_select_path_static.restype = I
         L.dflash2_select_path_static.argtypes = [F(Config), F(Weights), I, P, P, P, P, P, P]
@@ -322,7 +324,8 @@ def dflash2_test_gemm_workspace(M, N):
 
 def dflash2_test_gemm(dtype, W, X, ctas, out, workspace, accumulate=False, stream=None):
     """ctas: 0 = the library's schedule, > 0 = stream-K over that many CTAs,
-    < 0 = whole tiles.  Returns the CTA count launched."""
+    -1 = whole tiles, -2..-8 = cluster split-K of -ctas slices per tile.
+    Returns the CTA count launched."""
     M, K = W.shape
     N = X.shape[0]
     rc = lib().dflash2_test_gemm(dtype, _ptr(W), M, K, _ptr(X), N, ctas, int(accumulate), _ptr(out),
@@ -330,6 +333,12 @@ def dflash2_test_gemm(dtype, W, X, ctas, out, workspace, accumulate=False, strea
     if rc < 0:
         _check("dflash2_test_gemm", rc)
     return rc
+
+
+def dflash2_test_force_cluster_split(cs):
+    """Force cluster split-K of cs slices on the library's own contractions
+    (0 = its own schedule)."""
+    _check("dflash2_test_force_cluster_split", lib().dflash2_test_force_cluster_split(int(cs)))
 
 
 def dflash2_test_gemm_fp8(W8, scale, X, ctas, out, workspace, accumulate=False, stream=None):

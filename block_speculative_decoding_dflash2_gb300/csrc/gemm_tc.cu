@@ -24,6 +24,11 @@
 // indexed by the tile's first CTA) sums them in CTA order, so the result is
 // deterministic and no CTA waits for another.  The top-k contraction (the
 // lm_head) needs whole tiles: its CTAs take whole tiles round-robin.
+// Contractions whose tiles fill the SMs a few times over in K slices run as
+// cluster split-K instead: one thread-block cluster per tile, CTA r of the
+// cluster takes K slice r, and the cluster's first CTA sums the slices'
+// partial tiles in rank order through distributed shared memory and runs the
+// epilogue (no partial leaves the SMs, no arrival counter).
 //
 // Epilogues: the plain fp32 output (stored or added to), the streaming top-k
 // of the lm_head, and two fused ones that remove a kernel each:
@@ -57,6 +62,7 @@
 #include <cmath>
 #include <cstring>
 #include <climits>
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -79,6 +85,7 @@ struct TcArgs {
   int n_chunks, m_tiles, n_tiles, tiles;
   long work;        // tiles * n_chunks
   int stream;       // 1: stream-K shares of the work; 0: whole tiles round-robin
+  int csplit;       // > 1: cluster split-K, csplit CTAs (one cluster) per tile
   float* out;       // final [N][M] fp32 (stored, or added to when accumulate)
   float* partial;   // stream: [gridDim.x][2][BN][BM] pieces of shared tiles
   int* counters;    // stream: [gridDim.x] arrival counters, zero between launches
@@ -160,7 +167,13 @@ __device__ __forceinline__ UnitIter unit_iter(const TcArgs& a) {
   UnitIter it;
   it.nc = a.n_chunks;
   it.stream = a.stream;
-  if (a.stream) {
+  if (a.csplit > 1) {  // one unit: K slice blockIdx.x % csplit of tile blockIdx.x / csplit
+    const long t = blockIdx.x / a.csplit, ks = blockIdx.x % a.csplit;
+    it.stream = 1;
+    it.c = t * a.n_chunks + ks * a.n_chunks / a.csplit;
+    it.cend = t * a.n_chunks + (ks + 1) * a.n_chunks / a.csplit;
+    it.step = 0;
+  } else if (a.stream) {
     it.c = share_start(a.work, gridDim.x, blockIdx.x);
     it.cend = share_start(a.work, gridDim.x, blockIdx.x + 1);
     it.step = 0;
@@ -339,6 +352,10 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
       }
     }
     __syncwarp();  // lanes 1..31 wait here for the producer lane: the warp reaches the final barrier whole
+    if (a.csplit > 1) {  // the two cluster barriers of the slice reduction (see the epilogue)
+      cluster_sync();
+      cluster_sync();
+    }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -385,6 +402,10 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
       mbar_wait(drain, 0, &never, WAIT_NS);
     }
     __syncwarp();  // as for the producer warp
+    if (a.csplit > 1) {
+      cluster_sync();
+      cluster_sync();
+    }
   } else if (FP8 && warp >= 6) {
     // ------------------------------------------------------------ fp8 converters
     // Slot s holds rows of 64 e4m3 bytes; thread ct rewrites 16-byte pieces
@@ -431,6 +452,10 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
         }
       }
     }
+    if (a.csplit > 1) {
+      cluster_sync();
+      cluster_sync();
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     pdl_wait();  // outputs, partials and counters may still be in use by the previous kernel
@@ -460,6 +485,7 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
       }
     };
 
+    bool cl_done = false;  // cluster split-K: this CTA took part in both cluster barriers
     UnitIter it = unit_iter(a);
     int t, k0, k1;
     while (it.next(t, k0, k1)) {
@@ -600,11 +626,18 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
             named_sync_epi();  // the exchange tile and column info are reused next
           }
         };
+        const bool clus = a.csplit > 1;
+        float* part_s = reinterpret_cast<float*>(stA);  // cluster split-K: this slice's partial [row][BN]
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 16) {
           float v[16];
           tmem_ld16(tbase + c0, v);
-          if (!direct) {
+          if (clus) {
+            // (the operand ring is idle: the MMAs of the CTA's only unit are done)
+#pragma unroll
+            for (int j = 0; j < 16; j += 4)
+              *reinterpret_cast<float4*>(part_s + row * BN + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+          } else if (!direct) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) pc[(c0 + j) * BM + row] = v[j];
           } else {
@@ -613,7 +646,33 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
         }
         tc_fence_before();
         mbar_arrive(tempty + acc);
-        if (!direct) {
+        if (clus) {
+          cluster_sync();  // every slice's partial is in its CTA's shared memory
+          if (blockIdx.x % a.csplit == 0) {
+            // the cluster's first CTA sums the slices in rank order and runs the epilogue
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 16) {
+              float v[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] = 0.f;
+              for (int qr = 0; qr < a.csplit; ++qr) {
+                float4 x[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) x[j] = ld_dsmem4(dsmem_addr(part_s + row * BN + c0 + 4 * j, (uint32_t)qr));
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  v[4 * j] += x[j].x;
+                  v[4 * j + 1] += x[j].y;
+                  v[4 * j + 2] += x[j].z;
+                  v[4 * j + 3] += x[j].w;
+                }
+              }
+              finish(v, c0, nullptr);
+            }
+          }
+          cluster_sync();  // the first CTA has read every partial
+          cl_done = true;
+        } else if (!direct) {
           // the piece is written; one thread publishes it (the barrier orders the
           // other threads' stores before its cumulative fence) and counts it
           named_sync_epi();
@@ -730,6 +789,10 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (a.csplit > 1 && !cl_done) {  // bailed out before the slice reduction: keep the cluster's barriers
+      cluster_sync();
+      cluster_sync();
+    }
     if constexpr (TOPK) {
       if (!named_sync_or(*abort_flag != 0)) {
         if (cur_nt >= 0) flush_lists(cur_nt, false);
@@ -808,16 +871,93 @@ int pick_bn(int M, int N) {
 }
 
 template <int BN, int EPI, bool FP8>
-int launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs& args, int grid, const Ctx& c) {
-  constexpr int smem = TcCfg<BN, FP8>::smem_bytes(EPI);
+int set_smem_attr() {
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(tc_gemm_kernel<BN, EPI, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(tc_gemm_kernel<BN, EPI, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             TcCfg<BN, FP8>::smem_bytes(EPI)) != cudaSuccess)
       return DFLASH2_ERR_CUDA;
     attr_set = true;
   }
-  return launch_k(tc_gemm_kernel<BN, EPI, FP8>, dim3(grid), dim3(threads_of(FP8)), smem, c, ma, mb, args);
+  return DFLASH2_OK;
+}
+
+template <int BN, int EPI, bool FP8>
+int launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs& args, int grid, const Ctx& c) {
+  constexpr int smem = TcCfg<BN, FP8>::smem_bytes(EPI);
+  const int rc = set_smem_attr<BN, EPI, FP8>();
+  if (rc) return rc;
+  return launch_kx(tc_gemm_kernel<BN, EPI, FP8>, dim3(grid), dim3(threads_of(FP8)), smem, c,
+                   args.csplit > 1 ? args.csplit : 1, ma, mb, args);
+}
+
+// Clusters of cs CTAs of this instantiation that fit the device at once
+// (0 when the query fails), cached per cluster size.
+template <int BN, int EPI, bool FP8>
+int max_clusters(int cs) {
+  static int cache[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
+  if (cs < 2 || cs > 8) return 0;
+  if (cache[cs] >= 0) return cache[cs];
+  if (set_smem_attr<BN, EPI, FP8>()) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs * 64);
+  cfg.blockDim = dim3(threads_of(FP8));
+  cfg.dynamicSmemBytes = TcCfg<BN, FP8>::smem_bytes(EPI);
+  cudaLaunchAttribute at;
+  at.id = cudaLaunchAttributeClusterDimension;
+  at.val.clusterDim.x = cs;
+  at.val.clusterDim.y = 1;
+  at.val.clusterDim.z = 1;
+  cfg.attrs = &at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<BN, EPI, FP8>, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  cache[cs] = n;
+  return n;
+}
+
+template <int BN, bool FP8>
+int max_clusters_epi(int epi, int cs) {
+  switch (epi) {
+    case EPI_SWIGLU:
+      if constexpr (BN <= 64) return max_clusters<BN, EPI_SWIGLU, FP8>(cs);
+      return 0;
+    case EPI_HEADS:
+      if constexpr (BN <= 64) return max_clusters<BN, EPI_HEADS, FP8>(cs);
+      return 0;
+    case EPI_PLAIN: return max_clusters<BN, EPI_PLAIN, FP8>(cs);
+    default: return 0;
+  }
+}
+
+int max_clusters_of(int bn, int epi, bool fp8, int cs) {
+  switch (bn) {
+    case 16: return fp8 ? max_clusters_epi<16, true>(epi, cs) : max_clusters_epi<16, false>(epi, cs);
+    case 32: return fp8 ? max_clusters_epi<32, true>(epi, cs) : max_clusters_epi<32, false>(epi, cs);
+    case 64: return fp8 ? max_clusters_epi<64, true>(epi, cs) : max_clusters_epi<64, false>(epi, cs);
+    default: return 0;
+  }
+}
+
+// Cluster split-K size for a contraction, or 1 (stream-K / whole tiles):
+// the largest cs in 2..8 (at most the K chunks) whose tiles x cs CTAs fill
+// at least three quarters of the SMs without exceeding them, when every
+// tile's cluster fits the device at once.  ctas <= -2 forces cs = -ctas.
+int pick_csplit(int tiles, int n_chunks, int bn, int epi, bool fp8, int nsm, int ctas) {
+  if (epi == EPI_TOPK || bn > 64) return 1;
+  if (ctas <= -2) {
+    const int cs = -ctas;
+    return cs <= 8 && cs <= n_chunks && max_clusters_of(bn, epi, fp8, cs) >= 1 ? cs : 1;
+  }
+  if (ctas != 0) return 1;
+  for (int cs = 8; cs >= 2; --cs) {
+    if (cs > n_chunks || (long)tiles * cs > nsm || (long)tiles * cs * 4 < (long)nsm * 3) continue;
+    if (max_clusters_of(bn, epi, fp8, cs) >= tiles) return cs;
+  }
+  return 1;
 }
 
 template <int BN, bool FP8>
@@ -866,6 +1006,11 @@ int gemm_topk_lists(int M, int N, int K, int nsm, int dtype) {
 
 int gemm_max_lists() { return std::max(kMaxSM, 0); }
 
+thread_local int g_last_grid = 0;
+int gemm_last_grid() { return g_last_grid; }
+std::atomic<int> g_force_csplit{0};
+void gemm_force_csplit(int cs) { g_force_csplit.store(cs); }
+
 int gemm_bf16(const GemmOp& g, const Ctx& c) {
   if (g.M <= 0 || g.N <= 0 || g.K <= 0) return DFLASH2_ERR_SHAPE;
   const int bn = pick_bn(g.M, g.N);
@@ -882,6 +1027,11 @@ int gemm_bf16(const GemmOp& g, const Ctx& c) {
   a.tiles = a.m_tiles * a.n_tiles;
   a.work = (long)a.tiles * a.n_chunks;
   a.stream = (!g.topk && g.ctas >= 0) ? 1 : 0;
+  const int fcs = g_force_csplit.load();
+  a.csplit = kClusterSplit && !g.topk ? pick_csplit(a.tiles, a.n_chunks, bn, epi, g.wscale != nullptr, c.nsm,
+                                                    fcs >= 2 && g.ctas == 0 ? -fcs : g.ctas)
+                                      : 1;
+  if (a.csplit > 1) a.stream = 0;
   a.out = g.out;
   a.partial = g.partial;
   a.counters = g.counters;
@@ -893,7 +1043,8 @@ int gemm_bf16(const GemmOp& g, const Ctx& c) {
   const long want = a.stream ? (g.ctas > 0 ? std::min(g.ctas, kMaxSM)
                                            : std::max(1L, std::min<long>(c.nsm, a.work / kMinChunks)))
                              : c.nsm;
-  const int grid = (int)std::min<long>(want, a.stream ? a.work : a.tiles);
+  const int grid = a.csplit > 1 ? a.tiles * a.csplit : (int)std::min<long>(want, a.stream ? a.work : a.tiles);
+  g_last_grid = grid;
   a.lists_v = g.lists_v;
   a.lists_i = g.lists_i;
   a.debug = g.debug;

@@ -78,6 +78,9 @@ constexpr int kForkPrologueSMs = 32;
 // greatest priority, so that the block scheduler places their CTAs before
 // the block branch's when SMs free up.
 constexpr bool kSidePriority = true;
+// Whether contractions whose tiles x K slices fill the SMs run as cluster
+// split-K (slices summed in distributed shared memory) instead of stream-K.
+constexpr bool kClusterSplit = true;
 
 // Host-side count of kernel launches (instrumentation).
 void count_launch(int n = 1);
@@ -134,6 +137,8 @@ inline int launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, 
 int workspace_offsets(const dflash2_config* c, int batch, int n_new, int max_ctx, size_t* out, int n);
 
 int gemm_bf16(const GemmOp& g, const Ctx& c);  // tcgen05 + TMA (sm_103a)
+int gemm_last_grid();  // CTAs of this thread's last gemm_bf16 launch
+void gemm_force_csplit(int cs);  // test hook: cluster split-K of cs slices where it applies (0 = off)
 int gemm_f32(const GemmOp& g, const Ctx& c);   // exact fp32 FMA, SIMT
 
 // Tiles (m_tiles * n_tiles) of a contraction, the size of its counter array.

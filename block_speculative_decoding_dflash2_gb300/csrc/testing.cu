@@ -72,13 +72,10 @@ int test_gemm(int dtype, const void* W, const float* wscale, int M, int K, const
     const int r = gemm_f32(g, c);
     return r ? r : 1;
   }
+  g.ctas = ctas <= -2 ? ctas : g.ctas;  // <= -2: cluster split-K of -ctas slices per tile
   const int r = gemm_bf16(g, c);
   if (r) return r;
-  // the CTA count gemm_bf16 launched
-  const long tiles = (long)gemm_tiles(M, N), work = tiles * ((K + 63) / 64);
-  if (g.ctas < 0) return (int)std::min<long>(tiles, c.nsm);
-  if (g.ctas > 0) return (int)std::min<long>(g.ctas, work);
-  return (int)std::min<long>(std::max(1L, std::min<long>(c.nsm, work / 8)), work);
+  return gemm_last_grid();  // the CTA count gemm_bf16 launched
 }
 
 }  // namespace
@@ -94,6 +91,12 @@ int dflash2_test_gemm_fp8(const void* W8, const float* scale, int M, int K, cons
                           int accumulate, float* out, void* workspace, size_t ws_bytes, void* stream) {
   if (!scale) return DFLASH2_ERR_INVALID_ARG;
   return test_gemm(DFLASH2_BF16, W8, scale, M, K, X, N, ctas, accumulate, out, workspace, ws_bytes, stream);
+}
+
+int dflash2_test_force_cluster_split(int cs) {
+  if (cs != 0 && (cs < 2 || cs > 8)) return DFLASH2_ERR_INVALID_ARG;
+  df2::gemm_force_csplit(cs);
+  return 0;
 }
 
 int dflash2_test_layout(const dflash2_config* cfg, int batch, int n_new, int max_ctx, size_t* offsets, int n) {

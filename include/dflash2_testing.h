@@ -26,13 +26,28 @@ extern "C" {
  *   ctas       bf16 work schedule: 0 = the library's own (stream-K shares of
  *              all tile x K-chunk work, one CTA per SM); > 0 = stream-K over
  *              that many CTAs (at most 256; tiles shared by several CTAs are
- *              summed by the last piece to arrive, in CTA order); < 0 =
- *              whole tiles, one CTA each, round-robin.  Ignored for f32.
+ *              summed by the last piece to arrive, in CTA order); -1 =
+ *              whole tiles, one CTA each, round-robin; -2..-8 = cluster
+ *              split-K, -ctas K slices per tile in one thread-block cluster,
+ *              summed in rank order through distributed shared memory (the
+ *              library's own schedule picks this for contractions whose
+ *              tiles x slices fill the SMs).  Ignored for f32.
  *   out        float [N][M]
  *   workspace  zeroed on first use, at least dflash2_test_gemm_workspace bytes
  * Returns the number of CTAs launched (>= 1) or a negative status.
  */
 size_t dflash2_test_gemm_workspace(int M, int N);
+
+/*
+ * From now on in this process, every bf16 / fp8-weight contraction that the
+ * library schedules itself (not the lm_head's top-k) takes cluster split-K
+ * with cs K slices where the shape allows it (at least cs K chunks of 64, an
+ * activation tile at most 64 wide), so the fused epilogues run after the
+ * distributed-shared-memory reduction at test sizes too.  cs = 0 restores the
+ * library's own schedule.  Returns 0, or DFLASH2_ERR_INVALID_ARG for cs
+ * outside {0, 2..8}.  Not thread-safe against concurrent draft steps.
+ */
+int dflash2_test_force_cluster_split(int cs);
 int dflash2_test_gemm(int dtype, const void *W, int M, int K, const void *X, int N, int ctas, int accumulate,
                       float *out, void *workspace, size_t ws_bytes, void *stream);
 

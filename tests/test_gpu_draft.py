@@ -100,6 +100,22 @@ def test_qwen3_8b_shape_batch1():
     check_case(case, tol=5e-2)
 
 
+@pytest.mark.parametrize("cs,dtype", [(2, "bf16"), (4, "bf16"), (3, "fp8w")])
+def test_cluster_split_epilogues(cs, dtype):
+    """Every contraction the shapes allow (feature projection, the context
+    K/V with the paged-store epilogue, the block QKV with q/k norm + RoPE,
+    O, gate/up with SiLU*up, down) forced onto cluster split-K: the fused
+    epilogues run on the rank-order sum of the slices."""
+    B = lib()
+    cfg = S.small_bf16_config(dtype=dtype, index=21 + cs)
+    B.dflash2_test_force_cluster_split(cs)
+    try:
+        case = Case(cfg, ctx_lens=[60, 7], n_new=[8, 3], seed=31 + cs).run_gpu()
+    finally:
+        B.dflash2_test_force_cluster_split(0)
+    check_case(case)
+
+
 def test_device_guards_flag_bad_page_and_token():
     import torch
     cfg = S.small_bf16_config(index=13)

@@ -30,6 +30,13 @@ def _mat(rows, cols, seed, std, dtype):
     (4096, 8, 4096, 256),    # 8 K chunks per CTA: 8 pieces per tile
     (4096, 8, 4096, 1),      # one CTA streams every tile whole
     (1000, 7, 256, -1),      # whole tiles round-robin
+    (1000, 7, 256, -2),      # cluster split-K: 2 slices of 2 K chunks, ragged M tile
+    (1000, 17, 520, -3),     # cluster split-K: 9 chunks in 3 slices, ragged K tail, 32-wide tile
+    (300, 40, 640, -8),      # cluster split-K: 8 slices, 64-wide ragged activation tile
+    (4096, 8, 4096, -8),     # 32 clusters x 8 CTAs > the SM count: clusters queue
+    (128, 16, 64, -2),       # one K chunk: too short to split, whole tiles instead
+    (384, 100, 1024, -4),    # 100 columns in 16-wide tiles (at most 4 row tiles): split
+    (640, 100, 1024, -4),    # 128-wide activation tile: no cluster split, whole tiles
 ])
 @pytest.mark.parametrize("accumulate", [False, True])
 def test_bf16_gemm_matches_float64_product(M, N, K, ctas, accumulate):
@@ -46,6 +53,13 @@ def test_bf16_gemm_matches_float64_product(M, N, K, ctas, accumulate):
         used = B.dflash2_test_gemm(B.BF16, S.to_torch(W), S.to_torch(X), ctas, out, ws, accumulate)
         torch.cuda.synchronize()
         assert 1 <= used <= 256 and (ctas <= 0 or used <= ctas)
+        if ctas <= -2:
+            # the cluster schedule ran where it applies (at least -ctas K chunks and
+            # an activation tile at most 64 wide, i.e. N <= 64 or at most 4 row
+            # tiles): -ctas CTAs for each whole tile, else one
+            tiles = B.dflash2_test_gemm(B.BF16, S.to_torch(W), S.to_torch(X), -1, torch.empty_like(out), ws)
+            split = (K + 63) // 64 >= -ctas and (N <= 64 or M <= 512)
+            assert used == tiles * (-ctas if split else 1)
         got = out.double().cpu().numpy() - (base if accumulate else 0.0)
         w64, x64 = W.values.astype(np.float64), X.values.astype(np.float64)
         ref = x64 @ w64.T
@@ -62,6 +76,8 @@ def test_bf16_gemm_matches_float64_product(M, N, K, ctas, accumulate):
     (384, 70, 1024, -1),     # 128-wide activation tile, whole tiles
     (2688, 7, 8064, 0),      # the 30B-A3B down / feature projection shape
     (5120, 14, 2688, 0),     # the 30B-A3B QKV shape with appended rows
+    (1000, 7, 512, -4),      # cluster split-K with the converter warps
+    (2688, 7, 8064, -8),     # 21 clusters x 8 slices
 ])
 @pytest.mark.parametrize("accumulate", [False, True])
 def test_fp8_gemm_matches_dequantised_product(M, N, K, ctas, accumulate):
@@ -79,6 +95,8 @@ def test_fp8_gemm_matches_dequantised_product(M, N, K, ctas, accumulate):
                                    ctas, out, ws, accumulate)
     torch.cuda.synchronize()
     assert 1 <= used <= 256
+    if ctas <= -2:
+        assert used == -(-M // 128) * -ctas
     got = out.double().cpu().numpy() - (base if accumulate else 0.0)
     x64 = X.values.astype(np.float64)
     ref = x64 @ W.values.T

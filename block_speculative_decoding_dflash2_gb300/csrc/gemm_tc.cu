@@ -566,21 +566,52 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
             named_sync_epi();
           } else if constexpr (EPI == EPI_HEADS) {
             const int tid = threadIdx.x - 64, wq = tid >> 5;
-            const int d = a.hd;
-            const int hg = m / d, di = m - hg * d;
+            const int d = a.hd, half = d / 2;
+            const int hg = m / d, di = m - hg * d, ip = di % half;
             const bool valid = m < a.M;
             const int kind = hg < a.n_qh ? 0 : (hg < a.n_qh + a.n_kh ? 1 : 2);  // q, k, v
-            // per-column sums of squares over this warp's 32 rows
-            float x[16];
+            const bool rot = kind < 2 && valid;
+            // every global value this epilogue reads, issued together up front:
+            // the norm weight, the RoPE angles of the 16 columns and, for
+            // appended rows, their cache offsets (issued after a global store
+            // they would each wait for it, the store may alias them)
+            const float gdi = rot ? ld((kind == 0 ? a.qn : a.kn) + di) : 1.f;
+            float2 cs[16];
+            long long dj[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) x[j] = warp_sum(valid ? v[j] * v[j] : 0.f);
-            if (lane == 0) {
+            for (int j = 0; j < 16; ++j) {
+              const int n = max(0, min(nb + j, a.N - 1));  // columns past N: clamped, unused
+              const bool blk = n < a.nblk;
+              const float2* src =
+                  blk ? a.rope + (size_t)n * half + ip : a.rope_app + (size_t)(n - a.nblk) * half + ip;
+              cs[j] = rot ? __ldcg(src) : make_float2(1.f, 0.f);
+              dj[j] = (valid && kind > 0 && !blk) ? __ldcg(a.dst + (n - a.nblk)) : -1;
+            }
+            // per-column sums of squares over this warp's 32 rows, by a
+            // transposing butterfly: each exchange halves the columns a lane
+            // keeps (16 shuffles instead of 16 x 5); lane L ends with column
+            // (L >> 1)'s sum
+            {
+              float t8[8], t4[4], t2[2];
+              const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
 #pragma unroll
-              for (int j = 0; j < 16; ++j) ssb[wq * 16 + j] = x[j];
+              for (int i = 0; i < 8; ++i) {
+                const float lo = valid ? v[i] * v[i] : 0.f, hi = valid ? v[8 + i] * v[8 + i] : 0.f;
+                t8[i] = (b4 ? hi : lo) + __shfl_xor_sync(0xffffffffu, b4 ? lo : hi, 16);
+              }
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                t4[i] = (b3 ? t8[4 + i] : t8[i]) + __shfl_xor_sync(0xffffffffu, b3 ? t8[i] : t8[4 + i], 8);
+#pragma unroll
+              for (int i = 0; i < 2; ++i)
+                t2[i] = (b2 ? t4[2 + i] : t4[i]) + __shfl_xor_sync(0xffffffffu, b2 ? t4[i] : t4[2 + i], 4);
+              float t1 = (b1 ? t2[1] : t2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? t2[0] : t2[1], 2);
+              t1 += __shfl_xor_sync(0xffffffffu, t1, 1);
+              if (!(lane & 1)) ssb[wq * 16 + (lane >> 1)] = t1;
             }
             named_sync_epi();
             // RMSNorm of q/k heads (a head spans all 128 rows, or a 64-row half)
-            const float gdi = (kind < 2 && valid) ? ld((kind == 0 ? a.qn : a.kn) + di) : 1.f;
+            float x[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const float ss = d == BM ? (ssb[j] + ssb[16 + j]) + (ssb[32 + j] + ssb[48 + j])
@@ -589,17 +620,9 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
               stg[j * BM + row] = x[j];
             }
             named_sync_epi();
-            // RoPE: rotate-half pairs (di, di + d/2), angles from the tables
-            if (kind < 2 && valid) {
-              const int half = d / 2, ip = di % half;
+            // RoPE: rotate-half pairs (di, di + d/2)
+            if (rot) {
               const float sgn = di < half ? -1.f : 1.f;
-              float2 cs[16];
-#pragma unroll
-              for (int j = 0; j < 16; ++j)
-                if (j < nj) {
-                  const int n = nb + j;
-                  cs[j] = n < a.nblk ? a.rope[(size_t)n * half + ip] : a.rope_app[(size_t)(n - a.nblk) * half + ip];
-                }
 #pragma unroll
               for (int j = 0; j < 16; ++j)
                 if (j < nj) x[j] = x[j] * cs[j].x + sgn * (stg[j * BM + (row ^ half)] * cs[j].y);
@@ -614,12 +637,9 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
                   if (kind == 0) a.q[(n * a.n_qh + hg) * d + di] = val;
                   else if (kind == 1) a.kb[(n * a.n_kh + (hg - a.n_qh)) * d + di] = val;
                   else a.vb[(n * a.n_kh + (hg - a.n_qh - a.n_kh)) * d + di] = val;
-                } else if (kind > 0) {
-                  const long long dj = a.dst[n - a.nblk];
-                  if (dj >= 0) {
-                    if (kind == 1) a.kc[dj + (size_t)(hg - a.n_qh) * d + di] = val;
-                    else if (kind == 2) a.vc[dj + (size_t)(hg - a.n_qh - a.n_kh) * d + di] = val;
-                  }
+                } else if (kind > 0 && dj[j] >= 0) {
+                  if (kind == 1) a.kc[dj[j] + (size_t)(hg - a.n_qh) * d + di] = val;
+                  else a.vc[dj[j] + (size_t)(hg - a.n_qh - a.n_kh) * d + di] = val;
                 }
               }
             }

@@ -72,16 +72,17 @@ __device__ __forceinline__ float key_value(unsigned long long key) {
 }
 __device__ __forceinline__ int key_id(unsigned long long key) { return 0x7fffffff - (int)(unsigned)key; }
 
-// Rank of key x at slot sx among keys[0..n): the keys above it, plus the
-// equal ones (padding entries) at smaller slots.  One warp: lanes split the
-// keys and the counts are summed across the warp.
-__device__ __forceinline__ int warp_rank_of(const unsigned long long* keys, int n, unsigned long long x, int sx) {
+// Rank of key x at slot sx among keys[0..n) in shared memory: the keys above
+// it, plus the equal ones (padding entries) at smaller slots.  One thread per
+// key ranked: the threads of a warp read the same key at once (a broadcast).
+__device__ __forceinline__ int rank_of(const unsigned long long* keys, int n, unsigned long long x, int sx) {
   int rank = 0;
-  for (int m = threadIdx.x & 31; m < n; m += 32) {
+#pragma unroll 8
+  for (int m = 0; m < n; ++m) {
     const unsigned long long y = keys[m];
     rank += (y > x) | ((y == x) & (m < sx));
   }
-  return __reduce_add_sync(0xffffffffu, rank);
+  return rank;
 }
 
 // One CTA per row.  The row's n_lists sorted lists are staged in shared
@@ -91,7 +92,8 @@ __device__ __forceinline__ int warp_rank_of(const unsigned long long* keys, int 
 // are rank counts over 64-bit order keys (a warp per element counts the
 // elements above it): tau is the head of rank KMAX-1, and a survivor of rank
 // q < k is output q.  The result is the exact top k under the strict
-// (value, id) order, whatever the vocabulary split.
+// (value, id) order, whatever the vocabulary split.  Each rank is counted by
+// one thread over keys read from shared memory as broadcasts.
 // dynamic shared memory: 2 * n_lists * KMAX * 8 bytes.
 constexpr int MT = 512;  // threads of the merge kernel
 
@@ -136,12 +138,10 @@ __global__ void __launch_bounds__(MT) topk_merge_kernel(const float* __restrict_
     tau = 0;  // fewer than KMAX lists: every entry survives
   }
   __syncthreads();
-  // tau: the list head of rank KMAX-1 (a warp per head)
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int NW = MT / 32;
+  // tau: the list head of rank KMAX-1
   if (n_lists >= KMAX)
-    for (int l = warp; l < n_lists; l += NW)
-      if (warp_rank_of(hk, n_lists, hk[l], l) == KMAX - 1 && lane == 0) tau = hk[l];
+    for (int l = threadIdx.x; l < n_lists; l += MT)
+      if (rank_of(hk, n_lists, hk[l], l) == KMAX - 1) tau = hk[l];
   __syncthreads();
   // survivors: entries whose key is at least tau's
   const unsigned long long t0 = tau;
@@ -157,10 +157,10 @@ __global__ void __launch_bounds__(MT) topk_merge_kernel(const float* __restrict_
     cand_id[(size_t)row * k + q] = -1;
     cand_logit[(size_t)row * k + q] = -INFINITY;
   }
-  for (int i = warp; i < ns; i += NW) {
+  for (int i = threadIdx.x; i < ns; i += MT) {
     const unsigned long long key = sk[i];
-    const int rank = warp_rank_of(sk, ns, key, i);
-    if (rank < k && lane == 0) {
+    const int rank = rank_of(sk, ns, key, i);
+    if (rank < k) {
       const int id = key_id(key);
       cand_id[(size_t)row * k + rank] = id == INT_MAX ? -1 : id;
       cand_logit[(size_t)row * k + rank] = key_value(key);

@@ -430,7 +430,8 @@ int dflash2_verify_accept_ex(int batch, int block_size, const int32_t *path, con
  *   u_sample     [batch] float in [0, 1): the draw of the emitted token
  *   n_draft      nullable [batch]: drafts kept per sequence (B-1 when null)
  * Outputs, seq_len and counters as dflash2_verify_accept_ex.  Random numbers
- * are inputs, so a call is deterministic.  DFLASH2_ERR_SHAPE for vocab < 2.
+ * are inputs, so a call is deterministic.  DFLASH2_ERR_SHAPE for vocab < 2
+ * or vocab > 1,536,000.
  */
 int dflash2_verify_sampled(int batch, int block_size, int vocab, const int32_t *path, const int32_t *n_draft,
                            const float *target_prob, const float *u_accept, const float *u_sample,

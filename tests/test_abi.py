@@ -138,3 +138,20 @@ def test_host_side_error_paths_return_before_cuda(B):
     assert L.dflash2_select_path(ctypes.byref(c), ctypes.byref(w), 1, 1, 1, 1, 1, None, 1, 1 << 30,
                                  None) == -1
     assert L.dflash2_read_device_status(None, 0, None) == -5
+
+
+def test_sampled_verify_and_cluster_switch_host_checks(B):
+    L = B.lib()
+    # sampled verification: block size, vocabulary bounds and null pointers are
+    # checked on the host, before any launch (dummy non-null pointers are never
+    # dereferenced)
+    args = (1, 1, 1, 1, 1, 1, 1, 1, 1, None, None, None)
+    assert L.dflash2_verify_sampled(1, 40, 1000, *args) == -3
+    assert L.dflash2_verify_sampled(1, 8, 1, *args) == -2
+    assert L.dflash2_verify_sampled(1, 8, 1_536_001, *args) == -2  # segment sums exceed shared memory
+    assert L.dflash2_verify_sampled(1, 8, 1000, None, *args[1:]) == -1
+    # the test switch of cluster split-K: 0 or 2..8 slices, nothing else
+    for cs in (1, 9, -2):
+        assert L.dflash2_test_force_cluster_split(cs) == -1
+    for cs in (2, 8, 0):
+        assert L.dflash2_test_force_cluster_split(cs) == 0

@@ -181,7 +181,7 @@ Layout plan(const dflash2_config& c0, int batch, int n_new, int max_ctx) {
   return L;
 }
 
-// Per-device facts: SM count and whether it is the sm_103 part this build targets.
+// Per-device facts: SM count and whether it is the sm_103 part this library targets.
 int device_ctx(Ctx* ctx, void* stream, void* ws) {
   static int nsm_cache[64] = {0};
   static int ok_cache[64] = {0};
@@ -444,7 +444,7 @@ const char* dflash2_status_string(int s) {
     case DFLASH2_ERR_DTYPE: return "unsupported dtype";
     case DFLASH2_ERR_WORKSPACE: return "workspace missing or too small";
     case DFLASH2_ERR_CUDA: return "a CUDA call failed";
-    case DFLASH2_ERR_UNSUPPORTED: return "unsupported device or request (this build targets sm_103a)";
+    case DFLASH2_ERR_UNSUPPORTED: return "unsupported device or request (this library targets sm_103a)";
     default: return "unknown status";
   }
 }

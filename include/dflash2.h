@@ -60,7 +60,7 @@ extern "C" {
 #define DFLASH2_ERR_DTYPE            -4  /* unsupported dtype */
 #define DFLASH2_ERR_WORKSPACE        -5  /* workspace null or smaller than required */
 #define DFLASH2_ERR_CUDA             -6  /* a CUDA runtime/driver call failed */
-#define DFLASH2_ERR_UNSUPPORTED      -7  /* valid request this build does not serve (e.g. not sm_103a) */
+#define DFLASH2_ERR_UNSUPPORTED      -7  /* valid request this library does not serve (e.g. not sm_103a) */
 
 /* device status word bits (dflash2_read_device_status) */
 #define DFLASH2_DEV_BAD_PAGE        0x1  /* block_table entry outside [0, n_pages) */
@@ -187,7 +187,7 @@ const char *dflash2_status_string(int status);
 int dflash2_version(void);
 
 /*
- * Checks a configuration against what this build serves.  Returns
+ * Checks a configuration against what this library serves.  Returns
  * DFLASH2_OK, DFLASH2_ERR_INVALID_ARG (null), DFLASH2_ERR_SHAPE,
  * DFLASH2_ERR_BLOCK_SIZE or DFLASH2_ERR_DTYPE.  Host only, no CUDA call.
  */

@@ -360,7 +360,8 @@ int project_features(const dflash2_config& c, const dflash2_weights& w, const Sc
 // its shape allows).
 int run_append(const dflash2_config& c, const dflash2_weights& w, const Scales& sc, void* kc, void* vc, int n_pages,
                const int32_t* block_table, int max_pages, int batch, const int32_t* ctx_len, int n_new,
-               const void* taps, const int32_t* new_off, void* ws, const Layout& L, const Ctx& ctx) {
+               const void* taps, const int32_t* new_off, void* ws, const Layout& L, const Ctx& ctx,
+               int kv_nsm = 0) {
   if (n_new == 0) return DFLASH2_OK;
   const int H = c.hidden, nq = c.n_q_heads, nkv = c.n_kv_heads, d = c.head_dim;
   float* Y = at<float>(ws, L.Ya);
@@ -369,6 +370,7 @@ int run_append(const dflash2_config& c, const dflash2_weights& w, const Scales& 
   Ctx rest;
   TRY(project_features(c, w, sc, n_pages, block_table, max_pages, batch, ctx_len, n_new, taps, new_off, ws, L,
                        fused_kv, ctx, &rest));
+  if (kv_nsm > 0) rest.nsm = kv_nsm;  // the K/V contractions fit the SMs the block branch leaves free
   const size_t layer_elems = (size_t)n_pages * c.page_size * nkv * d;
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash2_layer_weights& Lw = w.layers[l];
@@ -536,6 +538,10 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
   const bool fused = conv && conv_prologue_fits(c.dtype, batch, B, H, G, ctx.nsm);
   const bool split_sms = forked && fused && ctx.nsm > 2 * kForkPrologueSMs &&
                          conv_prologue_fits(c.dtype, batch, B, H, G, kForkPrologueSMs / 2);
+  // separate arrangement: the block's first QKV contraction leaves kForkKvSMs
+  // SMs free, where the side stream's K/V contraction runs beside it instead
+  // of waiting for the QKV's CTAs to exit
+  const bool kv_split = split_sms && !merged && kForkKvSMs > 0 && ctx.nsm > 2 * kForkKvSMs;
   TRY(stage_event(0, ctx.stream));
   if (forked) {
     side_lock.lock();
@@ -552,7 +558,7 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
                            workspace, L, true, actx, nullptr));
     else
       TRY(run_append(c, *w, sc, k_cache, v_cache, n_pages, block_table, max_pages, batch, ctx_len, n_new, new_taps,
-                     new_off, workspace, L, actx));
+                     new_off, workspace, L, actx, kv_split ? kForkKvSMs : 0));
     TRY(stage_event(1, side.s));
     if (cudaEventRecord(side.join, side.s) != cudaSuccess) return DFLASH2_ERR_CUDA;
   } else {
@@ -623,6 +629,7 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
     // merged: the QKV contraction reads the appended rows' features, a full
     // dependency on the join
     Ctx qctx = ctx;
+    if (kv_split && l == 0) qctx.nsm = ctx.nsm - kForkKvSMs;
     if (forked && merged && l == 0) {
       if (cudaStreamWaitEvent(ctx.stream, side.join, 0) != cudaSuccess) return DFLASH2_ERR_CUDA;
       qctx.pdl = false;

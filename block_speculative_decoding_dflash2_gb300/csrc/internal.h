@@ -74,6 +74,9 @@ constexpr int kMaxSM = 256;  // CTAs of a stream-K launch, and its counter array
 // SMs left to the fused embedding prologue while the side stream's feature
 // contraction runs beside it (the contraction takes the rest).
 constexpr int kForkPrologueSMs = 32;
+// SMs the block's first QKV contraction leaves to the side stream's K/V
+// contraction when the two run side by side (0: the QKV takes every SM).
+constexpr int kForkKvSMs = 32;
 // Whether the side stream's stage (a) kernels launch at the device's
 // greatest priority, so that the block scheduler places their CTAs before
 // the block branch's when SMs free up.

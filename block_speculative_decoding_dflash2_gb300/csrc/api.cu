@@ -538,10 +538,15 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
   const bool fused = conv && conv_prologue_fits(c.dtype, batch, B, H, G, ctx.nsm);
   const bool split_sms = forked && fused && ctx.nsm > 2 * kForkPrologueSMs &&
                          conv_prologue_fits(c.dtype, batch, B, H, G, kForkPrologueSMs / 2);
-  // separate arrangement: the block's first QKV contraction leaves kForkKvSMs
-  // SMs free, where the side stream's K/V contraction runs beside it instead
-  // of waiting for the QKV's CTAs to exit
-  const bool kv_split = split_sms && !merged && kForkKvSMs > 0 && ctx.nsm > 2 * kForkKvSMs;
+  // sublayer prologues: one fused kernel (norm, tap logits, conv) when the
+  // sequence's B rows fit its shared memory, else norm + tap GEMM + conv;
+  // the QKV contraction with its q/k-norm + RoPE epilogue when its
+  // activation tile allows
+  const bool fused_qkv = merged || (c.dtype == DFLASH2_BF16 && gemm_fusable(qkvM, rows, kEpiHeads));
+  // separate arrangement with the fused QKV: the block's first QKV
+  // contraction leaves kForkKvSMs SMs free, where the side stream's K/V
+  // contraction runs beside it instead of waiting for the QKV's CTAs to exit
+  const bool kv_split = split_sms && !merged && fused_qkv && kForkKvSMs > 0 && ctx.nsm > 2 * kForkKvSMs;
   TRY(stage_event(0, ctx.stream));
   if (forked) {
     side_lock.lock();
@@ -580,9 +585,6 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
   const size_t layer_elems = (size_t)n_pages * c.page_size * nkv * d;
   void* ws = workspace;
 
-  // sublayer prologues: one fused kernel (norm, tap logits, conv) when the
-  // sequence's B rows fit its shared memory, else norm + tap GEMM + conv
-  const bool fused_qkv = merged || (c.dtype == DFLASH2_BF16 && gemm_fusable(qkvM, rows, kEpiHeads));
   RopeTab rt;  // the block rows' RoPE angles, left by the first kernel for the fused QKV epilogues
   std::memset(&rt, 0, sizeof(rt));
   if (fused_qkv) {

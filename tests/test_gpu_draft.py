@@ -72,6 +72,15 @@ def test_small_bf16_wide_batch():
     check_case(case)
 
 
+def test_small_bf16_one_layer_kv_beside_qkv():
+    # one layer (the separate arrangement) with a fused QKV: the block's QKV
+    # contraction runs on all but 32 SMs and the side stream's K/V contraction
+    # on those 32, side by side (the 8B bench step's schedule, at small size)
+    cfg = S.small_bf16_config(n_layers=1, index=27)
+    case = Case(cfg, ctx_lens=[60, 7, 33], n_new=[8, 3, 5], seed=27).run_gpu()
+    check_case(case)
+
+
 def test_small_bf16_block16_and_groups():
     cfg = S.small_bf16_config(block_size=16, n_q_heads=8, n_kv_heads=2, head_dim=128, top_k=16,
                               conv_group_size=64, index=12)

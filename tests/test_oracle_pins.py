@@ -230,6 +230,117 @@ def test_draft_layer_residual_identity_when_outputs_zero():
     np.testing.assert_array_equal(out, h)
 
 
+def _rms_rows(x, gamma, eps):
+    # RMSNorm written out row by row for the closed forms below
+    return np.stack([r / math.sqrt(float(np.dot(r, r)) / r.size + eps) for r in x]) * gamma
+
+
+def _left_avg_conv_input(u):
+    # a zero tap generator gives the taps 1/2, 1/2, so the sublayer reads
+    # u_t + (u_t + u_{t-1}) / 2 with nothing left of the anchor
+    prev = np.vstack([np.zeros_like(u[:1]), u[:-1]])
+    return 1.5 * u + 0.5 * prev
+
+
+@pytest.mark.parametrize("which", ["q", "k"])
+def test_draft_layer_qk_norm_makes_head_scale_irrelevant(which):
+    # draft_layer ([Train] "What is DFlash?", the draft's own norms; Qwen3
+    # layer: per-head q/k RMSNorm before RoPE): scaling the projection rows of
+    # one query head, or of one key head, by c > 0 leaves the layer output
+    # unchanged, because that head's norm divides the scale out.  A dropped
+    # q_norm / k_norm, or one taken over all heads together, fails this.
+    cfg = tiny_cfg(rms_eps=0.0)
+    W = tiny_weights(cfg, seed=3)
+    nq, nkv, d = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
+    g = np.random.default_rng(30)
+    h = g.standard_normal((4, cfg["hidden"]))
+    ctxK = g.standard_normal((5, nkv, d))
+    ctxV = g.standard_normal((5, nkv, d))
+    pos = np.arange(5, 9)
+    st = O.Store(False)
+    base = O.draft_layer(cfg, W["layers"][0], h, ctxK, ctxV, pos, st)
+    head_row0 = 1 * d if which == "q" else (nq + 1) * d     # q head 1, or kv head 1
+    for c in (3.7, 0.25):
+        Wl = dict(W["layers"][0])
+        Wl["qkv"] = Wl["qkv"].copy()
+        Wl["qkv"][head_row0:head_row0 + d] *= c
+        out = O.draft_layer(cfg, Wl, h, ctxK, ctxV, pos, st)
+        np.testing.assert_allclose(out, base, rtol=1e-11, atol=1e-11)
+    # the pin has teeth: the same scaling of a v head does change the output
+    Wl = dict(W["layers"][0])
+    Wl["qkv"] = Wl["qkv"].copy()
+    Wl["qkv"][(nq + nkv + 1) * d:(nq + nkv + 2) * d] *= 3.7
+    assert np.max(np.abs(O.draft_layer(cfg, Wl, h, ctxK, ctxV, pos, st) - base)) > 1e-3
+
+
+def test_draft_layer_attention_reads_u_plus_conv_closed_form():
+    # draft_layer, attention sublayer ([Train] "Variants": the convolution is
+    # added around the sublayer): with W_k = 0 every block key normalises to
+    # 0, so (no context) each row attends uniformly to the B block values.
+    # With W_v copying the first nkv*d channels of the sublayer input and W_o
+    # copying head 0's output back into channels [0, d), every row gains
+    # mean_t(u'_t)[0:d] with u' = u + (u + u_prev)/2.  Reading c alone (not
+    # u + c), a causal mask, or a wrong V / O wiring fails this.
+    cfg = tiny_cfg()
+    W = tiny_weights(cfg, seed=4)
+    H, nq, nkv, d, I = (cfg[k] for k in ("hidden", "n_q_heads", "n_kv_heads", "head_dim", "intermediate"))
+    Wl = dict(W["layers"][0])
+    Wl["tapgen_attn"] = np.zeros_like(Wl["tapgen_attn"])
+    qkv = Wl["qkv"].copy()
+    qkv[nq * d:(nq + nkv) * d] = 0.0
+    qkv[(nq + nkv) * d:] = np.eye(nkv * d, H)
+    Wl["qkv"] = qkv
+    Wl["o"] = np.eye(H, nq * d) * (np.arange(H) < d)[:, None]
+    Wl["gate_up"] = np.zeros((2 * I, H))
+    h = np.random.default_rng(31).standard_normal((4, H))
+    out = O.draft_layer(cfg, Wl, h, *empty_ctx(cfg)[0], np.arange(4), O.Store(False))
+    u2 = _left_avg_conv_input(_rms_rows(h, Wl["attn_norm"], cfg["rms_eps"]))
+    want = h.copy()
+    want[:, :d] += u2[:, :d].mean(axis=0)
+    np.testing.assert_allclose(out, want, rtol=1e-12, atol=1e-12)
+
+
+def test_draft_layer_mlp_is_silu_gate_times_up_on_post_attention_rows():
+    # draft_layer, MLP sublayer (Qwen3 MLP: down(SiLU(gate x) * up x)) with
+    # the additive two-tap conv: one gate row e_i, one up row e_j and one down
+    # column e_m give out[:, m] = h1[:, m] + SiLU(u'_i) * u'_j, where h1 is the
+    # residual after the attention sublayer and u' = u + (u + u_prev)/2 of
+    # RMSNorm(h1).  Swapping gate and up (SiLU(u'_j) * u'_i), norming the
+    # pre-attention rows, or feeding c instead of u + c fails this.
+    cfg = tiny_cfg()
+    W = tiny_weights(cfg, seed=5)
+    H, nq, nkv, d, I = (cfg[k] for k in ("hidden", "n_q_heads", "n_kv_heads", "head_dim", "intermediate"))
+    i, j, m = 3, 11, 7
+    Wl = dict(W["layers"][0])
+    Wl["tapgen_attn"] = np.zeros_like(Wl["tapgen_attn"])
+    Wl["tapgen_mlp"] = np.zeros_like(Wl["tapgen_mlp"])
+    qkv = Wl["qkv"].copy()
+    qkv[nq * d:(nq + nkv) * d] = 0.0
+    qkv[(nq + nkv) * d:] = np.eye(nkv * d, H)
+    Wl["qkv"] = qkv
+    Wl["o"] = 0.7 * np.eye(H, nq * d) * (np.arange(H) < d)[:, None]
+    gu = np.zeros((2 * I, H))
+    gu[0, i] = 1.0          # gate row 0 reads channel i
+    gu[I, j] = 1.0          # up row 0 reads channel j
+    Wl["gate_up"] = gu
+    down = np.zeros((H, I))
+    down[m, 0] = 1.0
+    Wl["down"] = down
+    h = np.random.default_rng(32).standard_normal((4, H))
+    out = O.draft_layer(cfg, Wl, h, *empty_ctx(cfg)[0], np.arange(4), O.Store(False))
+    eps = cfg["rms_eps"]
+    ua = _left_avg_conv_input(_rms_rows(h, Wl["attn_norm"], eps))
+    h1 = h.copy()
+    h1[:, :d] += 0.7 * ua[:, :d].mean(axis=0)
+    um = _left_avg_conv_input(_rms_rows(h1, Wl["mlp_norm"], eps))
+    want = h1.copy()
+    want[:, m] += um[:, i] / (1.0 + np.exp(-um[:, i])) * um[:, j]
+    np.testing.assert_allclose(out, want, rtol=1e-12, atol=1e-12)
+    swapped = h1.copy()
+    swapped[:, m] += um[:, j] / (1.0 + np.exp(-um[:, j])) * um[:, i]
+    assert np.max(np.abs(swapped - want)) > 1e-3
+
+
 def test_v1_layer_without_conv_mixes_rows_only_through_attention():
     # conv_kernel_size 0 (DFlash v1): with the attention output switched off
     # (W_o = 0) every row is processed alone, so changing row 1 leaves rows

@@ -97,6 +97,8 @@ def lib():
         L.dflash2_verify_accept.argtypes = [I, I, P, P, P, P, P, P, P, P, P]
         L.dflash2_read_device_status.restype = I
         L.dflash2_read_device_status.argtypes = [P, S, P]
+        L.dflash2_test_last_schedule.restype = I
+        L.dflash2_test_last_schedule.argtypes = []
         L.dflash2_test_gemm_workspace.restype = S
         L.dflash2_test_gemm_workspace.argtypes = [I, I]
         L.dflash2_test_gemm.restype = I
@@ -108,6 +110,8 @@ def lib():
         L.dflash2_select_path_static.restype = I
         L.dflash2_select_path_static.argtypes = [F(Config), F(Weights), I, P, P, P, P, P, P]
         L.dflash2_select_path_static_capacity.restype = S
+        L.dflash2_select_path_static_read_status.restype = I
+        L.dflash2_select_path_static_read_status.argtypes = [P]
         L.dflash2_selector_table_bytes.restype = S
         L.dflash2_selector_table_bytes.argtypes = [F(Config)]
         L.dflash2_build_selector_table.restype = I
@@ -372,6 +376,14 @@ def dflash2_test_layout(cfg, batch, n_new, max_ctx):
                     list(out)))
 
 
+SCHED_FUSED_PROLOGUE, SCHED_SPLIT_SMS, SCHED_FUSED_QKV, SCHED_KV_BESIDE_QKV, SCHED_MERGED = 1, 2, 4, 8, 16
+
+
+def dflash2_test_last_schedule():
+    """Schedule bits (SCHED_*) of the last draft step in this process."""
+    return lib().dflash2_test_last_schedule()
+
+
 def dflash2_launch_count():
     return lib().dflash2_launch_count()
 
@@ -401,3 +413,12 @@ def dflash2_select_path_static(cfg, w, batch, anchor, cand_id, cand_logit, path,
 
 def dflash2_select_path_static_capacity():
     return lib().dflash2_select_path_static_capacity()
+
+
+def dflash2_select_path_static_read_status(stream=None):
+    """Device status word (DFLASH2_DEV_* bits) of the last static selector
+    call on the current device, read and cleared; synchronises the stream."""
+    rc = lib().dflash2_select_path_static_read_status(_stream(stream))
+    if rc < 0:
+        _check("dflash2_select_path_static_read_status", rc)
+    return rc

@@ -26,6 +26,7 @@ namespace {
 constexpr int kVersion = 10000;
 
 std::atomic<long long> g_launches{0};
+std::atomic<int> g_last_schedule{0};
 void* volatile g_stage_events[DFLASH2_N_STAGE_EVENTS] = {nullptr};
 std::atomic<int> g_stage_on{0};
 
@@ -106,8 +107,11 @@ int check_config(const dflash2_config* c) {
   return DFLASH2_OK;
 }
 
+// Most lm_head rows (batch * drafts) a draft step takes.
+constexpr int kMaxTopkRows = 32 * 256;
+
 struct Layout {
-  size_t status, cnt, cnta, f, Y, P, Ya, Pa, h, u, u2, ua, u2a, q, kb, vb, attn, O, act, hn, logits, lv, li, selx,
+  size_t status, cnt, cnta, thr, f, Y, P, Ya, Pa, h, u, u2, ua, u2a, q, kb, vb, attn, O, act, hn, logits, lv, li, selx,
       rope, ropea, dsta, total;
 };
 
@@ -151,6 +155,7 @@ Layout plan(const dflash2_config& c0, int batch, int n_new, int max_ctx) {
   L.status = take(256);
   L.cnt = take(kMaxSM * sizeof(int));
   L.cnta = take(kMaxSM * sizeof(int));
+  L.thr = take(kMaxTopkRows * sizeof(unsigned long long));  // the lm_head's shared top-k thresholds
   L.Y = take(Yb);
   L.P = take(P);
   L.Ya = take(Yba);
@@ -370,10 +375,13 @@ int run_append(const dflash2_config& c, const dflash2_weights& w, const Scales& 
   Ctx rest;
   TRY(project_features(c, w, sc, n_pages, block_table, max_pages, batch, ctx_len, n_new, taps, new_off, ws, L,
                        fused_kv, ctx, &rest));
-  if (kv_nsm > 0) rest.nsm = kv_nsm;  // the K/V contractions fit the SMs the block branch leaves free
   const size_t layer_elems = (size_t)n_pages * c.page_size * nkv * d;
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash2_layer_weights& Lw = w.layers[l];
+    // layer 0's K/V contraction fits the SMs the block's first QKV
+    // contraction leaves free; later layers run beside nothing and take all
+    Ctx lrest = rest;
+    if (kv_nsm > 0 && l == 0) lrest.nsm = kv_nsm;
     // the k and v rows of the qkv matrix (fp8: bytes, and their scales)
     const float* skv = sc.layers ? sc.layers[l].qkv + (size_t)nq * d : nullptr;
     const void* wkv = skv ? static_cast<const void*>(static_cast<const uint8_t*>(Lw.qkv) + (size_t)nq * d * H)
@@ -393,11 +401,11 @@ int run_append(const dflash2_config& c, const dflash2_weights& w, const Scales& 
       g.dst = at<long long>(ws, L.dsta);
       g.kc = kcl;
       g.vc = vcl;
-      TRY(gemm_fused(g, rest, ws, L, true));
+      TRY(gemm_fused(g, lrest, ws, L, true));
     } else {
-      TRY(gemm(c, rest, ws, L, wkv, 2 * nkv * d, H, f, n_new, Y, false, true, skv));
+      TRY(gemm(c, lrest, ws, L, wkv, 2 * nkv * d, H, f, n_new, Y, false, true, skv));
       TRY(launch_kv_append(c.dtype, Y, n_new, nkv, d, Lw.k_norm, c.rms_eps, c.rope_theta, ctx_len, new_off, batch,
-                           block_table, max_pages, c.page_size, n_pages, kcl, vcl, rest));
+                           block_table, max_pages, c.page_size, n_pages, kcl, vcl, lrest));
     }
   }
   return DFLASH2_OK;
@@ -421,6 +429,8 @@ RopeFreq rope_freq(int d, float theta) {
 }
 
 void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+int draft_last_schedule() { return g_last_schedule.load(); }
 
 int workspace_offsets(const dflash2_config* c, int batch, int n_new, int max_ctx, size_t* out, int n) {
   if (check_config(c) != DFLASH2_OK) return DFLASH2_ERR_SHAPE;
@@ -502,7 +512,7 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
   const int max_ctx = max_pages * c.page_size;
   const Layout L = plan(c, batch, n_new, max_ctx);
   if (ws_bytes < L.total) return DFLASH2_ERR_WORKSPACE;
-  if ((long long)batch * (c.block_size - 1) > 32 * 256) return DFLASH2_ERR_SHAPE;
+  if ((long long)batch * (c.block_size - 1) > kMaxTopkRows) return DFLASH2_ERR_SHAPE;
   Ctx ctx;
   TRY(device_ctx(&ctx, stream, workspace));
 
@@ -547,6 +557,9 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
   // contraction leaves kForkKvSMs SMs free, where the side stream's K/V
   // contraction runs beside it instead of waiting for the QKV's CTAs to exit
   const bool kv_split = split_sms && !merged && fused_qkv && kForkKvSMs > 0 && ctx.nsm > 2 * kForkKvSMs;
+  g_last_schedule.store((fused ? kSchedFusedPrologue : 0) | (split_sms ? kSchedSplitSMs : 0) |
+                        (fused_qkv ? kSchedFusedQKV : 0) | (kv_split ? kSchedKvBesideQKV : 0) |
+                        (merged ? kSchedMerged : 0));
   TRY(stage_event(0, ctx.stream));
   if (forked) {
     side_lock.lock();
@@ -697,7 +710,8 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
     }
     TRY(gemm(c, ctx, ws, L, Lw.down, H, I, act, rows, h, true, false, s_down));
   }
-  TRY(launch_rownorm(c.dtype, h, rows, H, w->final_norm, c.rms_eps, hn, B, 1, ctx));
+  TRY(launch_rownorm(c.dtype, h, rows, H, w->final_norm, c.rms_eps, hn, B, 1, ctx,
+                     at<unsigned long long>(workspace, L.thr)));
 
   TRY(stage_event(2, ctx.stream));
   // (c) lm_head over block positions 1..B-1 with the streaming top-k
@@ -719,6 +733,7 @@ int dflash2_draft_step(const dflash2_config* cfg, const dflash2_weights* w, void
     g.topk = true;
     g.lists_v = lv;
     g.lists_i = li;
+    g.thr = at<unsigned long long>(workspace, L.thr);
     g.debug = debug_logits;
     g.mult = c.output_multiplier;
     g.cap = c.final_logit_softcap;

@@ -90,6 +90,64 @@ __device__ __forceinline__ void warp_list_offer(float& lv, int& li, float& tv, i
   ti = __shfl_sync(0xffffffffu, li, KMAX - 1);
 }
 
+// 64-bit order key of a candidate: a larger key is a better candidate under
+// the (value descending, id ascending) order, so one integer compare replaces
+// the two-field one.  Value bits are mapped to an unsigned order (negative
+// zero first folded onto zero, which compares equal to it).  Key 0 is below
+// every candidate with a non-NaN value: it marks an empty list slot.
+__device__ __forceinline__ unsigned long long order_key(float v, int id) {
+  unsigned u = __float_as_uint(v + 0.f);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)u << 32) | (unsigned)(0x7fffffff - id);
+}
+__device__ __forceinline__ float key_value(unsigned long long key) {
+  const unsigned u = (unsigned)(key >> 32);
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
+}
+__device__ __forceinline__ int key_id(unsigned long long key) { return 0x7fffffff - (int)(unsigned)key; }
+
+// Offer key ck to a warp-held sorted list of keys: lanes 0..15 hold entry
+// `lane` (best first, 0 = empty), lanes 16..31 hold 0; tk is entry 15, kept
+// current.  Called by all 32 lanes with the same ck.
+__device__ __forceinline__ void warp_key_offer(unsigned long long& lk, unsigned long long& tk,
+                                               unsigned long long ck) {
+  if (ck <= tk) return;  // uniform across the warp
+  const int lane = threadIdx.x & 31;
+  const int pos = __popc(__ballot_sync(0xffffffffu, lane < KMAX && lk > ck) & 0xffffu);
+  const unsigned long long pk = __shfl_up_sync(0xffffffffu, lk, 1);
+  if (lane < KMAX && lane > pos) lk = pk;
+  if (lane == pos) lk = ck;
+  tk = __shfl_sync(0xffffffffu, lk, KMAX - 1);
+}
+
+// Merge one key per lane (0 = none) into the warp-held list above in one
+// pass: a bitonic sort of the 32 offered keys (descending), then a bitonic
+// merge of the list with the best 16 of them (the list descending in lanes
+// 0..15, the offers ascending in lanes 16..31 form one bitonic sequence).
+__device__ __forceinline__ void warp_key_merge(unsigned long long& lk, unsigned long long& tk,
+                                               unsigned long long ck) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long x = ck;
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const unsigned long long y = __shfl_xor_sync(0xffffffffu, x, j);
+      // blocks with (lane & k) == 0 sort descending (the whole warp at k = 32)
+      const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
+      x = keep_max ? (x > y ? x : y) : (x < y ? x : y);
+    }
+  const unsigned long long rev = __shfl_sync(0xffffffffu, x, 31 - lane);
+  x = lane < KMAX ? lk : rev;
+#pragma unroll
+  for (int j = 16; j > 0; j >>= 1) {
+    const unsigned long long y = __shfl_xor_sync(0xffffffffu, x, j);
+    x = (lane & j) == 0 ? (x > y ? x : y) : (x < y ? x : y);
+  }
+  lk = lane < KMAX ? x : 0ull;
+  tk = __shfl_sync(0xffffffffu, lk, KMAX - 1);
+}
+
 // ----------------------------------------------------------------- PTX: smem
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

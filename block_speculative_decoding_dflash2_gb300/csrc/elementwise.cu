@@ -247,10 +247,13 @@ __global__ void __launch_bounds__(RT) embed_norm_kernel(const int32_t* __restric
 }
 
 // u = RMSNorm_gamma(h[row]).  With skip_anchor, block slot 0 is not written
-// and the other rows are packed as [batch, B-1, H] (the lm_head input).
+// and the other rows are packed as [batch, B-1, H] (the lm_head input); then
+// zero_key (nullable) receives a 0 at each packed row: the lm_head's shared
+// top-k thresholds start from nothing.
 template <typename T>
 __global__ void __launch_bounds__(RT) rownorm_kernel(const float* __restrict__ h, int H, const T* __restrict__ gamma,
-                                                     float eps, T* __restrict__ u, int B, int skip_anchor) {
+                                                     float eps, T* __restrict__ u, int B, int skip_anchor,
+                                                     unsigned long long* __restrict__ zero_key) {
   extern __shared__ float xs[];
   __shared__ float red[32];
   pdl_launch_next();
@@ -261,6 +264,7 @@ __global__ void __launch_bounds__(RT) rownorm_kernel(const float* __restrict__ h
     const int s = row / B, i = row % B;
     if (i == 0) return;  // the whole CTA leaves together
     orow = s * (B - 1) + i - 1;
+    if (zero_key && threadIdx.x == 0) zero_key[orow] = 0ull;
   }
   for (int m = threadIdx.x * 4; m < H; m += blockDim.x * 4)
     *reinterpret_cast<float4*>(xs + m) = *reinterpret_cast<const float4*>(h + (size_t)row * H + m);
@@ -702,10 +706,11 @@ int launch_embed_norm(int dtype, const int32_t* anchor, int mask_id, int batch, 
 }
 
 int launch_rownorm(int dtype, const float* h, int rows, int H, const void* gamma, float eps, void* u_out, int B,
-                   int skip_anchor, const Ctx& c) {
+                   int skip_anchor, const Ctx& c, unsigned long long* zero_key) {
   int rc;
   DF2_DISPATCH(dtype, rc = launch_k(rownorm_kernel<T>, dim3(rows), dim3(RT), H * sizeof(float), c, h, H,
-                                    static_cast<const T*>(gamma), eps, static_cast<T*>(u_out), B, skip_anchor));
+                                    static_cast<const T*>(gamma), eps, static_cast<T*>(u_out), B, skip_anchor,
+                                    zero_key));
   return rc;
 }
 
@@ -735,7 +740,10 @@ int conv_prologue_groups(int G, int batch, int nsm) {
 constexpr size_t kPrologueSmem = 200 * 1024;
 
 bool conv_prologue_fits(int dtype, int batch, int B, int H, int G, int nsm) {
-  return B <= 32 && conv_prologue_smem(dtype, B, H, conv_prologue_groups(G, batch, nsm), false, false) <= kPrologueSmem;
+  // the fused kernel pays off only with its CTA's tap rows staged in shared
+  // memory (tensor-core tap logits); past that (wide batches, where a CTA
+  // would take many groups) the rownorm + tap contraction + conv kernels run
+  return B <= 32 && conv_prologue_smem(dtype, B, H, conv_prologue_groups(G, batch, nsm), true, false) <= kPrologueSmem;
 }
 
 int launch_conv_prologue(int dtype, const float* h_in, const int32_t* anchor, int mask_id, const void* embed, int V,

@@ -92,6 +92,7 @@ struct TcArgs {
   int accumulate;
   float* lists_v;
   int* lists_i;
+  unsigned long long* thr;  // [N] order key every CTA's candidates must beat (0 at launch)
   float* debug;
   float mult, cap;
   unsigned* status;
@@ -123,7 +124,7 @@ struct TcCfg {
   static constexpr int A8_BYTES = FP8 ? BM * BK : 0;  // e4m3 staging of a weight tile
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE = A_BYTES + A8_BYTES + B_BYTES;
-  static constexpr int TOPK_EXTRA = 16 * BM * 4 + BN * KMAX * 8;
+  static constexpr int TOPK_EXTRA = 16 * BM * 4 + BN * KMAX * 8 + 2 * BN * 8;  // staging, lists, thresholds
   static constexpr int FUSE_EXTRA = 16 * BM * 4 + 4 * 16 * 4;  // exchange tile, column sums
   static constexpr int FIXED = 1024 /* alignment slack */ + 1024 /* barriers */;
   __host__ __device__ static constexpr int extra(int epi) {
@@ -234,8 +235,8 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
   uint64_t* full8 = drain + 4;
   uint64_t* tma_full = FP8 ? full8 : full;
   float* stg = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 1024);  // [16][BM]
-  float* lv_s = stg + 16 * BM;                                                       // [BN][KMAX]
-  int* li_s = reinterpret_cast<int*>(lv_s + BN * KMAX);                              // [BN][KMAX]
+  unsigned long long* lk_s = reinterpret_cast<unsigned long long*>(stg + 16 * BM);  // [BN][KMAX] list keys
+  unsigned long long* thr_s = lk_s + BN * KMAX;                                       // [2][BN] thresholds
   float* ssb = stg + 16 * BM;  // fused: [4 warps][16 columns] sums
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -468,10 +469,7 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
     uint32_t touched = 0;
 
     auto reset_lists = [&]() {
-      for (int i = threadIdx.x - 64; i < BN * KMAX; i += 128) {
-        lv_s[i] = -INFINITY;
-        li_s[i] = INT_MAX;
-      }
+      for (int i = threadIdx.x - 64; i < BN * KMAX; i += 128) lk_s[i] = 0ull;
     };
     auto flush_lists = [&](int nt, bool sentinel) {
       for (int i = threadIdx.x - 64; i < BN * KMAX; i += 128) {
@@ -479,8 +477,9 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
         const int n = nt * BN + c;
         if (n < a.N) {
           const size_t o = ((size_t)blockIdx.x * a.N + n) * KMAX + e;
-          a.lists_v[o] = sentinel ? -INFINITY : lv_s[i];
-          a.lists_i[o] = sentinel ? INT_MAX : li_s[i];
+          const unsigned long long key = sentinel ? 0ull : lk_s[i];
+          a.lists_v[o] = key ? key_value(key) : -INFINITY;  // empty slots: the (-inf, INT_MAX) sentinel
+          a.lists_i[o] = key ? key_id(key) : INT_MAX;
         }
       }
     };
@@ -750,10 +749,31 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
           touched |= 1u << nt;
           named_sync_epi();
         }
+        // The shared per-column thresholds of this tile's columns, read once
+        // per tile into the buffer of this accumulator's parity (the other
+        // buffer may still be read by a warp scanning the previous tile).
+        // Each is the order key of some CTA's 16th-best entry of that column,
+        // so at least 16 entries beat it: an entry that does not beat it is
+        // not in the column's top 16 and is not offered.  The first chunk's
+        // barriers order these stores before the scans read them.
+        unsigned long long* thr_t = thr_s + acc * BN;
+        unsigned long long gl[(BN + 127) / 128];  // loaded now, stored after the first TMEM read
+#pragma unroll
+        for (int i = 0; i < (BN + 127) / 128; ++i) {
+          const int c = threadIdx.x - 64 + i * 128, n = nt * BN + c;
+          gl[i] = (c < BN && n < a.N) ? __ldcg(a.thr + n) : ~0ull;
+        }
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 16) {
           float v[16];
           tmem_ld16(tbase + c0, v);
+          if (c0 == 0) {
+#pragma unroll
+            for (int i = 0; i < (BN + 127) / 128; ++i) {
+              const int c = threadIdx.x - 64 + i * 128;
+              if (c < BN) thr_t[c] = gl[i];
+            }
+          }
           if (c0 + 16 >= BN) {
             tc_fence_before();
             mbar_arrive(tempty + acc);
@@ -777,31 +797,32 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
           named_sync_epi();
           for (int jj = ew; jj < 16; jj += 4) {
             const int c = c0 + jj;
-            if (nt * BN + c >= a.N) continue;
-            float* Lv = lv_s + c * KMAX;
-            int* Li = li_s + c * KMAX;
-            float lv = lane < KMAX ? Lv[lane] : -INFINITY;
-            int li = lane < KMAX ? Li[lane] : INT_MAX;
-            float tv = __shfl_sync(0xffffffffu, lv, KMAX - 1);
-            int ti = __shfl_sync(0xffffffffu, li, KMAX - 1);
+            const int n = nt * BN + c;
+            if (n >= a.N) continue;
+            unsigned long long* Lk = lk_s + c * KMAX;
+            unsigned long long lk = lane < KMAX ? Lk[lane] : 0ull;
+            unsigned long long tk = __shfl_sync(0xffffffffu, lk, KMAX - 1);
+            const unsigned long long gk = thr_t[c];
 #pragma unroll 1
             for (int r = 0; r < 4; ++r) {
               const int rr = r * 32 + lane;
               const int mm = mt * BM + rr;
-              const float x = stg[jj * BM + rr];
-              const bool pass = (mm < a.M) && beats(x, mm, tv, ti);
+              const unsigned long long key = mm < a.M ? order_key(stg[jj * BM + rr], mm) : 0ull;
+              const bool pass = key > tk && key > gk;
               unsigned mask = __ballot_sync(0xffffffffu, pass);
-              while (mask) {
-                const int src = __ffs(mask) - 1;
-                mask &= mask - 1;
-                const float cv = __shfl_sync(0xffffffffu, x, src);
-                warp_list_offer(lv, li, tv, ti, cv, mt * BM + r * 32 + src);
+              if (__popc(mask) > 3) {
+                // many at once (a column's first rows): one sort + merge pass
+                warp_key_merge(lk, tk, pass ? key : 0ull);
+              } else {
+                while (mask) {
+                  const int src = __ffs(mask) - 1;
+                  mask &= mask - 1;
+                  warp_key_offer(lk, tk, __shfl_sync(0xffffffffu, key, src));
+                }
               }
             }
-            if (lane < KMAX) {
-              Lv[lane] = lv;
-              Li[lane] = li;
-            }
+            if (lane < KMAX) Lk[lane] = lk;
+            if (lane == 0 && tk > gk) atomicMax(a.thr + n, tk);  // a full list tightens the shared bound
             __syncwarp();
           }
         }
@@ -1067,6 +1088,8 @@ int gemm_bf16(const GemmOp& g, const Ctx& c) {
   g_last_grid = grid;
   a.lists_v = g.lists_v;
   a.lists_i = g.lists_i;
+  a.thr = g.thr;
+  if (g.topk && !g.thr) return DFLASH2_ERR_INVALID_ARG;
   a.debug = g.debug;
   a.mult = g.mult;
   a.cap = g.cap;

@@ -39,6 +39,7 @@ struct GemmOp {
   bool topk;
   float* lists_v;  // [n_lists][N][KMAX]
   int* lists_i;
+  unsigned long long* thr;  // [N] per-row threshold keys shared by the CTAs, zero at launch
   float* debug;  // nullable [N][M] logits after the transform
   float mult, cap;
   // fused epilogues (bf16 path, activation tiles of at most 64 rows; see
@@ -140,6 +141,15 @@ inline int launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, 
 int workspace_offsets(const dflash2_config* c, int batch, int n_new, int max_ctx, size_t* out, int n);
 
 int gemm_bf16(const GemmOp& g, const Ctx& c);  // tcgen05 + TMA (sm_103a)
+// Schedule bits of the last dflash2_draft_step call (test hook)
+enum {
+  kSchedFusedPrologue = 1,  // sublayer prologue fused (norm + tap logits + conv)
+  kSchedSplitSMs = 2,       // embedding prologue beside the feature contraction on split SMs
+  kSchedFusedQKV = 4,       // QKV contraction with the q/k-norm + RoPE epilogue
+  kSchedKvBesideQKV = 8,    // layer 0's context K/V contraction on the SMs the QKV leaves free
+  kSchedMerged = 16,        // appended rows ride in the QKV contractions
+};
+int draft_last_schedule();
 int gemm_last_grid();  // CTAs of this thread's last gemm_bf16 launch
 void gemm_force_csplit(int cs);  // test hook: cluster split-K of cs slices where it applies (0 = off)
 int gemm_f32(const GemmOp& g, const Ctx& c);   // exact fp32 FMA, SIMT
@@ -181,7 +191,7 @@ int launch_embed_norm(int dtype, const int32_t* anchor, int mask_id, int batch, 
                       float scale, const void* gamma, float eps, float* h_out, void* u_out, const RopeTab& rt,
                       const Ctx& c);
 int launch_rownorm(int dtype, const float* h, int rows, int H, const void* gamma, float eps, void* u_out, int B,
-                   int skip_anchor, const Ctx& c);
+                   int skip_anchor, const Ctx& c, unsigned long long* zero_key = nullptr);
 int launch_dyn_conv(int dtype, const void* u, const float* Y, int rows, int H, int group_size, int B, void* u2_out,
                     const Ctx& c);
 int launch_qkv_epilogue(int dtype, const float* Y, int rows, int B, int nq, int nkv, int d, const void* q_norm,
@@ -192,8 +202,8 @@ int launch_act(int dtype, const float* Y, int rows, int I, void* act, const Ctx&
 // sequence's B rows: from the residual h_in, or, with h_in == nullptr, from
 // the block embedding [anchor, mask...] (then h_out receives it).  Writes u
 // (normed, as stored) and u2 (after the conv).  conv_prologue_fits says
-// whether the B rows fit its shared memory; otherwise the caller runs
-// rownorm + tap GEMM + dyn_conv.
+// whether the B rows and the CTA's tap rows fit its shared memory;
+// otherwise the caller runs rownorm + tap GEMM + dyn_conv.
 bool conv_prologue_fits(int dtype, int batch, int B, int H, int G, int nsm);
 // w_tap: [2G, H] of dtype, or (tap_scale != nullptr, bf16 activations) e4m3
 // codes whose row r is scaled by tap_scale[r].

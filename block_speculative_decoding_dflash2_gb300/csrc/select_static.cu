@@ -63,6 +63,21 @@ extern "C" {
 
 size_t dflash2_select_path_static_capacity(void) { return kStaticScratchBytes; }
 
+// The device status word of the last dflash2_select_path_static call on the
+// current device (the first word of the fixed array): read, then cleared,
+// ordered after the work already on `stream`, which this call synchronises.
+int dflash2_select_path_static_read_status(void* stream) {
+  int err = DFLASH2_OK;
+  void* base = scratch_address(&err);
+  if (!base) return err;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned v = 0;
+  if (cudaMemcpyAsync(&v, base, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess) return DFLASH2_ERR_CUDA;
+  if (cudaMemsetAsync(base, 0, sizeof(v), st) != cudaSuccess) return DFLASH2_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return DFLASH2_ERR_CUDA;
+  return (int)(v & 0x7fffffffu);
+}
+
 int dflash2_select_path_static(const dflash2_config* cfg, const dflash2_weights* w, int batch, const int32_t* anchor,
                                const int32_t* cand_id, const float* cand_logit, int32_t* path, float* path_score,
                                void* stream) {
@@ -77,6 +92,10 @@ int dflash2_select_path_static(const dflash2_config* cfg, const dflash2_weights*
   if (fp8) c.dtype = DFLASH2_BF16;  // bf16 embedding rows; e4m3 selector weights with row scales
   const int D = c.block_size - 1, k = c.top_k, r = c.selector_rank, H = c.hidden;
   const int es = c.dtype == DFLASH2_BF16 ? 2 : 4;
+  // bound the batch before any int product: one sequence's gathered rows
+  // alone take (D*k+1)*H*es bytes, so a batch past this cannot fit
+  const size_t per_seq = (size_t)(D * k + 1) * ((size_t)H * es + 2 * (size_t)r * sizeof(float));
+  if ((size_t)batch > kStaticScratchBytes / per_seq) return DFLASH2_ERR_WORKSPACE;
   const int nsel = batch * (D * k + 1);
   // scratch layout: status word | tile counters | gathered rows | factors | split partials
   int dev = 0, nsm = 0, maj = 0, mi = 0;

@@ -33,6 +33,8 @@ using namespace df2;
 
 extern "C" {
 
+int dflash2_test_last_schedule(void) { return draft_last_schedule(); }
+
 size_t dflash2_test_gemm_workspace(int M, int N) {
   if (M <= 0 || N <= 0) return 0;
   return al((size_t)kMaxSM * sizeof(int)) + al(gemm_partial_bytes(M, N));
@@ -105,7 +107,7 @@ int dflash2_test_layout(const dflash2_config* cfg, int batch, int n_new, int max
 
 size_t dflash2_test_topk_workspace(int dtype, int M, int N) {
   const int n_lists = std::max(kMaxSM, topk_scan_lists(M));
-  size_t t = al(256) + 2 * al((size_t)n_lists * N * KMAX * 4);
+  size_t t = al(256) + 2 * al((size_t)n_lists * N * KMAX * 4) + al((size_t)N * 8);
   if (dtype == DFLASH2_F32) t += al((size_t)N * M * 4);
   return t;
 }
@@ -137,15 +139,22 @@ int dflash2_test_gemm_topk(int dtype, const void* W, int M, int K, const void* X
   g.mult = mult;
   g.cap = cap;
   if (dtype == DFLASH2_BF16) {
+    // the shared per-row thresholds start at zero (a memset node; the draft
+    // step zeroes them in the kernel before the lm_head instead)
+    unsigned long long* thr =
+        reinterpret_cast<unsigned long long*>(base + al(256) + 2 * al((size_t)n_lists_cap * N * KMAX * 4));
+    if (cudaMemsetAsync(thr, 0, (size_t)N * 8, c.stream) != cudaSuccess) return DFLASH2_ERR_CUDA;
     g.topk = true;
     g.lists_v = lv;
     g.lists_i = li;
+    g.thr = thr;
     g.debug = debug;
     rc = gemm_bf16(g, c);
     if (rc) return rc;
     n_lists = gemm_topk_lists(M, N, K, c.nsm, dtype);
   } else {
-    float* logits = reinterpret_cast<float*>(base + al(256) + 2 * al((size_t)n_lists_cap * N * KMAX * 4));
+    float* logits = reinterpret_cast<float*>(base + al(256) + 2 * al((size_t)n_lists_cap * N * KMAX * 4) +
+                                             al((size_t)N * 8));
     g.out = logits;
     rc = gemm_f32(g, c);
     if (rc) return rc;

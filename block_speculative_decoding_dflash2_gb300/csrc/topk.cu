@@ -56,22 +56,6 @@ __global__ void __launch_bounds__(128) topk_scan_kernel(const float* __restrict_
   }
 }
 
-// 64-bit key of a candidate: a larger key is a better candidate under the
-// (value descending, id ascending) order, so one integer compare replaces
-// the two-field one.  Value bits are mapped to an unsigned order (negative
-// zero first folded onto zero, which compares equal to it).
-__device__ __forceinline__ unsigned long long order_key(float v, int id) {
-  unsigned u = __float_as_uint(v + 0.f);
-  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  return ((unsigned long long)u << 32) | (unsigned)(0x7fffffff - id);
-}
-
-__device__ __forceinline__ float key_value(unsigned long long key) {
-  const unsigned u = (unsigned)(key >> 32);
-  return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
-}
-__device__ __forceinline__ int key_id(unsigned long long key) { return 0x7fffffff - (int)(unsigned)key; }
-
 // Rank of key x at slot sx among keys[0..n) in shared memory: the keys above
 // it, plus the equal ones (padding entries) at smaller slots.  One thread per
 // key ranked: the threads of a warp read the same key at once (a broadcast).

@@ -32,6 +32,8 @@ def main():
     p = argparse.ArgumentParser()
     p.add_argument("--kernel", default="lm_head", choices=sorted(SHAPES) + ["select"])
     p.add_argument("--launches", type=int, default=3)
+    p.add_argument("--rows", type=int, default=0,
+                   help="activation rows (N); 0 = the batch-1 block's rows of the 8B-shaped step")
     p.add_argument("--ctas", type=int, default=0,
                    help="contraction schedule: 0 = the library's, >0 = stream-K over that many CTAs, <0 = whole tiles")
     a = p.parse_args()
@@ -39,6 +41,7 @@ def main():
     if a.kernel == "select":
         return bench_select(a)
     M, K, N = SHAPES[a.kernel]
+    N = a.rows or N
     g = torch.Generator(device="cuda")
     g.manual_seed(1234)
     W = (torch.randn((M, K), generator=g, device="cuda") * 0.02).to(torch.bfloat16)

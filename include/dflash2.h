@@ -275,8 +275,11 @@ int dflash2_select_path(const dflash2_config *cfg, const dflash2_weights *w,
  * and hands the library only its inputs and outputs.  The pages have no
  * counterpart of this entry point; it exists only for such callers.
  *
- * Same arguments, results and status codes as dflash2_select_path, minus the
- * workspace.  Its scratch is one fixed device array inside the library
+ * Same arguments, results and return codes as dflash2_select_path, minus the
+ * workspace.  Device-side flags (DFLASH2_DEV_BAD_TOKEN for a candidate or
+ * anchor id outside [0, vocab), DFLASH2_DEV_WAIT_TIMEOUT) land in the fixed
+ * array's own status word, which the next call clears: read them with
+ * dflash2_select_path_static_read_status before the next call.  Its scratch is one fixed device array inside the library
  * (dflash2_select_path_static_capacity() bytes, 8 MiB), which every GPU that
  * loads the library keeps until the process exits.  A call whose batch needs
  * more scratch than that returns DFLASH2_ERR_WORKSPACE without launching
@@ -297,6 +300,15 @@ int dflash2_select_path_static(const dflash2_config *cfg, const dflash2_weights 
 
 /* Bytes of the fixed scratch array dflash2_select_path_static uses. */
 size_t dflash2_select_path_static_capacity(void);
+
+/*
+ * Device status word of the last dflash2_select_path_static call on the
+ * current device: a bitwise OR of DFLASH2_DEV_* codes (>= 0), read after the
+ * work already queued on `stream` and then cleared.  Synchronises `stream`.
+ * Returns DFLASH2_ERR_CUDA on a failed copy or a failed address lookup.
+ * Allocates nothing.
+ */
+int dflash2_select_path_static_read_status(void *stream);
 
 /*
  * The selector's factors of a token depend on nothing but the frozen

@@ -36,6 +36,17 @@ extern "C" {
  *   workspace  zeroed on first use, at least dflash2_test_gemm_workspace bytes
  * Returns the number of CTAs launched (>= 1) or a negative status.
  */
+/*
+ * Schedule the last dflash2_draft_step call in this process took, as bits:
+ *   1  fused sublayer prologue (norm + tap logits + conv in one kernel)
+ *   2  embedding prologue beside the feature contraction on split SMs
+ *   4  QKV contraction with the fused q/k-norm + RoPE epilogue
+ *   8  layer 0's context K/V contraction on the SMs the QKV leaves free
+ *  16  appended rows carried by the QKV contractions (merged arrangement)
+ * Host only; not synchronised with concurrent draft steps.
+ */
+int dflash2_test_last_schedule(void);
+
 size_t dflash2_test_gemm_workspace(int M, int N);
 
 /*

@@ -78,6 +78,8 @@ def test_small_bf16_one_layer_kv_beside_qkv():
     # on those 32, side by side (the 8B bench step's schedule, at small size)
     cfg = S.small_bf16_config(n_layers=1, index=27)
     case = Case(cfg, ctx_lens=[60, 7, 33], n_new=[8, 3, 5], seed=27).run_gpu()
+    sched = lib().dflash2_test_last_schedule()
+    assert sched & lib().SCHED_KV_BESIDE_QKV, f"the K/V-beside-QKV schedule was not taken (bits {sched:#x})"
     check_case(case)
 
 

@@ -66,3 +66,29 @@ def test_static_selector_refuses_batches_beyond_its_scratch():
     with pytest.raises(B.DFlash2Error) as e:
         B.dflash2_select_path_static(c, w, b, dev(anchor), dev(cand), dev(z), path, None)
     assert e.value.status == -5
+
+
+def test_static_selector_reports_a_bad_token_id():
+    # an anchor outside the vocabulary is flagged in the fixed array's status
+    # word (its gathered row reads as zeros); the read clears it, and a clean
+    # call afterwards reports nothing
+    import torch
+    B = lib()
+    cfg = S.config_of("tiny_fp32")
+    W = S.make_weights(cfg)
+    w = B.WeightSet({"embed": S.to_torch(W["embed"]), "sel": S.to_torch(W["sel"]), "lm_head": None, "fc": None,
+                     "hidden_norm": None, "final_norm": None, "layers": []})
+    c = B.make_config(cfg)
+    b, D = 2, cfg["block_size"] - 1
+    anchor, cand, z = _inputs(cfg, b, seed=11)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    path = torch.zeros((b, D), dtype=torch.int32, device="cuda")
+    score = torch.zeros(b, dtype=torch.float32, device="cuda")
+    B.dflash2_select_path_static_read_status()
+    bad = anchor.copy()
+    bad[1] = cfg["vocab"] + 5
+    B.dflash2_select_path_static(c, w, b, dev(bad), dev(cand), dev(z), path, score)
+    assert B.dflash2_select_path_static_read_status() == 0x2   # DFLASH2_DEV_BAD_TOKEN
+    assert B.dflash2_select_path_static_read_status() == 0
+    B.dflash2_select_path_static(c, w, b, dev(anchor), dev(cand), dev(z), path, score)
+    assert B.dflash2_select_path_static_read_status() == 0

@@ -155,7 +155,7 @@ Layout plan(const dflash2_config& c0, int batch, int n_new, int max_ctx) {
   L.status = take(256);
   L.cnt = take(kMaxSM * sizeof(int));
   L.cnta = take(kMaxSM * sizeof(int));
-  L.thr = take(kMaxTopkRows * sizeof(unsigned long long));  // the lm_head's shared top-k thresholds
+  L.thr = take((size_t)kMaxTopkRows * kTopkSlots * sizeof(unsigned long long));  // the lm_head's shared top-k bounds
   L.Y = take(Yb);
   L.P = take(P);
   L.Ya = take(Yba);

@@ -248,8 +248,8 @@ __global__ void __launch_bounds__(RT) embed_norm_kernel(const int32_t* __restric
 
 // u = RMSNorm_gamma(h[row]).  With skip_anchor, block slot 0 is not written
 // and the other rows are packed as [batch, B-1, H] (the lm_head input); then
-// zero_key (nullable) receives a 0 at each packed row: the lm_head's shared
-// top-k thresholds start from nothing.
+// zero_key (nullable, [rows][kTopkSlots]) receives zeros at each packed row:
+// the lm_head's shared top-k bounds start from nothing.
 template <typename T>
 __global__ void __launch_bounds__(RT) rownorm_kernel(const float* __restrict__ h, int H, const T* __restrict__ gamma,
                                                      float eps, T* __restrict__ u, int B, int skip_anchor,
@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(RT) rownorm_kernel(const float* __restrict__ h
     const int s = row / B, i = row % B;
     if (i == 0) return;  // the whole CTA leaves together
     orow = s * (B - 1) + i - 1;
-    if (zero_key && threadIdx.x == 0) zero_key[orow] = 0ull;
+    if (zero_key && threadIdx.x < kTopkSlots) zero_key[(size_t)orow * kTopkSlots + threadIdx.x] = 0ull;
   }
   for (int m = threadIdx.x * 4; m < H; m += blockDim.x * 4)
     *reinterpret_cast<float4*>(xs + m) = *reinterpret_cast<const float4*>(h + (size_t)row * H + m);

@@ -40,12 +40,14 @@
 //           RoPE of q and k and stores bf16 q, k, v: to the block's q/k/v
 //           buffers, or, for appended context rows, into the paged cache.
 //
-// Warp roles (192 threads; 320 with fp8 weights):
+// Warp roles (192 threads; 320 for the top-k of tiles wider than 16; 64
+// more with fp8 weights):
 //   warp 0      TMA producer (one lane): weight + activation tiles -> ring
 //   warp 1      MMA issuer (one lane) and TMEM owner
 //   warps 2..5  epilogue: TMEM -> registers -> the output tile, a partial
-//               piece (coalesced over m), or the streaming top-k.
-//   warps 6..9  fp8 weights only: converters.  The weight tile arrives as
+//               piece (coalesced over m), or the streaming top-k (wide top-k
+//               tiles: warps 2..9, two sets of four on alternate chunks).
+//   next 2      fp8 weights only: converters.  The weight tile arrives as
 //               e4m3 bytes in a staging slot (half the bytes of bf16); the
 //               converters rewrite it as bf16 in the MMA operand layout
 //               (exact: every e4m3 value is a bf16 value), and the epilogue
@@ -76,9 +78,19 @@ constexpr int BM = 128;     // MMA M: weight rows per tile
 constexpr int BK = 64;      // K elements per ring stage (128 bytes of bf16)
 constexpr int SMEM_BUDGET = 227 * 1024;
 constexpr uint64_t WAIT_NS = 1000000000ull;
-constexpr int THREADS = 192;
-constexpr int THREADS_FP8 = THREADS + 128;  // + 4 converter warps
-__host__ __device__ constexpr int threads_of(bool fp8) { return fp8 ? THREADS_FP8 : THREADS; }
+enum { EPI_PLAIN = 0, EPI_TOPK = 1, EPI_SWIGLU = 2, EPI_HEADS = 3 };
+// Epilogue warps: 4 (one per TMEM lane quarter), or 8 (two sets of 4, each
+// taking every other 16-column chunk) for the top-k epilogue of wide tiles.
+__host__ __device__ constexpr int epi_warps(int epi, int bn) { return (epi == EPI_TOPK && bn > 16) ? 8 : 4; }
+// fp8 weights: threads of the converter warps, four warps, or two for the
+// q/k-norm + RoPE epilogue (its registers: the block stays at 256 threads,
+// so every role may use up to 255 registers)
+__host__ __device__ constexpr int conv_threads(int epi) { return epi == EPI_HEADS ? 64 : 128; }
+// producer + MMA warps, the epilogue warps, and (fp8 weights) the converters
+__host__ __device__ constexpr int threads_of(int epi, int bn, bool fp8) {
+  return 64 + 32 * epi_warps(epi, bn) + (fp8 ? conv_threads(epi) : 0);
+}
+constexpr int TOPK_SLOTS = kTopkSlots;  // shared bound slots per lm_head row (see the top-k epilogue)
 
 struct TcArgs {
   int M, N, K;
@@ -92,7 +104,7 @@ struct TcArgs {
   int accumulate;
   float* lists_v;
   int* lists_i;
-  unsigned long long* thr;  // [N] order key every CTA's candidates must beat (0 at launch)
+  unsigned long long* thr;  // [N][TOPK_SLOTS] shared bound slots of the top-k (0 at launch)
   float* debug;
   float mult, cap;
   unsigned* status;
@@ -116,15 +128,17 @@ struct TcArgs {
   bf16 *kc, *vc;      // appended rows: paged cache [pages][page_size][n_kh][hd]
 };
 
-enum { EPI_PLAIN = 0, EPI_TOPK = 1, EPI_SWIGLU = 2, EPI_HEADS = 3 };
-
 template <int BN, bool FP8 = false>
 struct TcCfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int A8_BYTES = FP8 ? BM * BK : 0;  // e4m3 staging of a weight tile
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE = A_BYTES + A8_BYTES + B_BYTES;
-  static constexpr int TOPK_EXTRA = 16 * BM * 4 + BN * KMAX * 8 + 2 * BN * 8;  // staging, lists, thresholds
+  // top-k: 16-column staging (narrow tiles) or the candidate queues of each
+  // warp set (wide tiles), the lists, the per-column thresholds, queue counts
+  static constexpr int TOPK_SETS = epi_warps(EPI_TOPK, BN) / 4;
+  static constexpr int TOPK_EXTRA = (BN > 16 ? TOPK_SETS * 16 * BM * 8 : 16 * BM * 4) + BN * KMAX * 8 + BN * 8 +
+                                    TOPK_SETS * 16 * 4;
   static constexpr int FUSE_EXTRA = 16 * BM * 4 + 4 * 16 * 4;  // exchange tile, column sums
   static constexpr int FIXED = 1024 /* alignment slack */ + 1024 /* barriers */;
   __host__ __device__ static constexpr int extra(int epi) {
@@ -189,29 +203,38 @@ __device__ __forceinline__ UnitIter unit_iter(const TcArgs& a) {
 // CTA whose share holds chunk c: the largest g with share_start(g) <= c.
 __device__ __forceinline__ int share_of(long c, long work, int G) { return (int)(((c + 1) * G - 1) / work); }
 
-__device__ __forceinline__ void named_sync_epi() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Named barrier 1 over the NT epilogue threads; barriers 2, 3 over one set of
+// 4 epilogue warps (the top-k epilogue of wide tiles).
+template <int NT = 128>
+__device__ __forceinline__ void named_sync_epi() { asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); }
+__device__ __forceinline__ void named_sync_set(int set) { asm volatile("bar.sync %0, 128;" ::"r"(2 + set) : "memory"); }
 
 // Named barrier over the 4 epilogue warps that also ORs a predicate, so the
 // warps take the same branch after it (no warp left waiting on a barrier
 // the others skipped).
+template <int NT = 128>
 __device__ __forceinline__ bool named_sync_or(bool pred) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 q, %1, 0;\n\t"
-      "bar.red.or.pred p, 1, 128, q;\n\t"
+      "bar.red.or.pred p, 1, %2, q;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(r)
-      : "r"((uint32_t)pred)
+      : "r"((uint32_t)pred), "n"(NT)
       : "memory");
   return r != 0;
 }
 
 template <int BN, int EPI, bool FP8>
-__global__ void __launch_bounds__(threads_of(FP8), 1)
+__global__ void __launch_bounds__(threads_of(EPI, BN, FP8), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcArgs a) {
   using C = TcCfg<BN, FP8>;
   constexpr bool TOPK = EPI == EPI_TOPK;
+  constexpr int EW = epi_warps(EPI, BN);  // epilogue warps
+  constexpr int EPT = 32 * EW;            // epilogue threads
+  constexpr int SETS = EW / 4;
+  constexpr int CONV_THREADS = conv_threads(EPI);
   constexpr int STAGES = C::stages(EPI);
   constexpr int A_BYTES = C::A_BYTES, B_BYTES = C::B_BYTES, A8_BYTES = C::A8_BYTES;
   static_assert(STAGES >= 2, "ring too small");
@@ -235,22 +258,27 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
   uint64_t* full8 = drain + 4;
   uint64_t* tma_full = FP8 ? full8 : full;
   float* stg = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 1024);  // [16][BM]
-  unsigned long long* lk_s = reinterpret_cast<unsigned long long*>(stg + 16 * BM);  // [BN][KMAX] list keys
-  unsigned long long* thr_s = lk_s + BN * KMAX;                                       // [2][BN] thresholds
   float* ssb = stg + 16 * BM;  // fused: [4 warps][16 columns] sums
+  // top-k: per-set queues [SETS][16][BM] keys (wide tiles; narrow ones stage
+  // values in stg), lists [BN][KMAX], thresholds [BN], queue counts [SETS][16]
+  unsigned long long* q_s = reinterpret_cast<unsigned long long*>(stg);
+  unsigned long long* lk_s =
+      reinterpret_cast<unsigned long long*>(reinterpret_cast<uint8_t*>(stg) + (BN > 16 ? SETS * 16 * BM * 8 : 16 * BM * 4));
+  unsigned long long* thr_s = lk_s + BN * KMAX;
+  int* qn_s = reinterpret_cast<int*>(thr_s + BN);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_launch_next();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full + s, FP8 ? 128 : 1);  // fp8: every converter thread arrives
+      mbar_init(full + s, FP8 ? CONV_THREADS : 1);  // fp8: every converter thread arrives
       mbar_init(empty + s, 1);
       if (FP8) mbar_init(full8 + s, 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(tfull + i, 1);
-      mbar_init(tempty + i, 128);
+      mbar_init(tempty + i, EPT);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -407,12 +435,12 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
       cluster_sync();
       cluster_sync();
     }
-  } else if (FP8 && warp >= 6) {
+  } else if (FP8 && warp >= 2 + EW) {
     // ------------------------------------------------------------ fp8 converters
     // Slot s holds rows of 64 e4m3 bytes; thread ct rewrites 16-byte pieces
     // (16 elements of row r) as two 16-byte bf16 chunks of the 128-byte
     // swizzled operand row (chunk c of row r lives at chunk c ^ (r & 7)).
-    const int ct = threadIdx.x - THREADS;
+    const int ct = threadIdx.x - (64 + EPT);
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -428,8 +456,8 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
         const uint8_t* src = stA8 + stage * A8_BYTES;
         uint8_t* dst = stA + stage * A_BYTES;
 #pragma unroll
-        for (int i = 0; i < A8_BYTES / 16 / 128; ++i) {
-          const int piece = ct + i * 128;
+        for (int i = 0; i < A8_BYTES / 16 / CONV_THREADS; ++i) {
+          const int piece = ct + i * CONV_THREADS;
           const int r = piece >> 2, c0 = (piece & 3) * 2;
           const uint4 q = *reinterpret_cast<const uint4*>(src + piece * 16);
           const uint32_t w[4] = {q.x, q.y, q.z, q.w};
@@ -469,10 +497,12 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
     uint32_t touched = 0;
 
     auto reset_lists = [&]() {
-      for (int i = threadIdx.x - 64; i < BN * KMAX; i += 128) lk_s[i] = 0ull;
+      for (int i = threadIdx.x - 64; i < BN * KMAX; i += EPT) lk_s[i] = 0ull;
+      for (int i = threadIdx.x - 64; i < BN; i += EPT) thr_s[i] = 0ull;
+      for (int i = threadIdx.x - 64; i < SETS * 16; i += EPT) qn_s[i] = 0;
     };
     auto flush_lists = [&](int nt, bool sentinel) {
-      for (int i = threadIdx.x - 64; i < BN * KMAX; i += 128) {
+      for (int i = threadIdx.x - 64; i < BN * KMAX; i += EPT) {
         const int c = i / KMAX, e = i % KMAX;
         const int n = nt * BN + c;
         if (n < a.N) {
@@ -491,7 +521,7 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
       const int mt = t % a.m_tiles, nt = t / a.m_tiles;
       const bool got = mbar_wait(tfull + acc, acc_phase, abort_flag, WAIT_NS);
       if (!got) fail();
-      if (named_sync_or(!got || *abort_flag)) break;
+      if (named_sync_or<EPT>(!got || *abort_flag)) break;
       tc_fence_after();
       const int m = mt * BM + row;
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
@@ -646,7 +676,12 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
           }
         };
         const bool clus = a.csplit > 1;
-        float* part_s = reinterpret_cast<float*>(stA);  // cluster split-K: this slice's partial [row][BN]
+        // cluster split-K: this slice's partial tile in the idle operand ring,
+        // as float4 groups [BN / 4][BM][4] (a warp's 16-byte accesses of one
+        // column group are consecutive: no bank conflicts at any BN)
+        float* part_s = reinterpret_cast<float*>(stA);
+        static_assert(EPI == EPI_TOPK || STAGES * (A_BYTES + B_BYTES + A8_BYTES) >= BM * BN * 4,
+                      "the operand ring must hold a partial tile");
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 16) {
           float v[16];
@@ -655,7 +690,8 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
             // (the operand ring is idle: the MMAs of the CTA's only unit are done)
 #pragma unroll
             for (int j = 0; j < 16; j += 4)
-              *reinterpret_cast<float4*>(part_s + row * BN + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+              *reinterpret_cast<float4*>(part_s + ((size_t)((c0 + j) >> 2) * BM + row) * 4) =
+                  make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
           } else if (!direct) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) pc[(c0 + j) * BM + row] = v[j];
@@ -667,29 +703,41 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
         mbar_arrive(tempty + acc);
         if (clus) {
           cluster_sync();  // every slice's partial is in its CTA's shared memory
-          if (blockIdx.x % a.csplit == 0) {
-            // the cluster's first CTA sums the slices in rank order and runs the epilogue
+          // The cluster's CTAs share the reduction and the epilogue: CTA r sums
+          // the slices of column chunks r, r + cs, ... in rank order (the same
+          // order whichever CTA sums) and finishes them.
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 16) {
-              float v[16];
+          for (int c0 = (int)(blockIdx.x % a.csplit) * 16; c0 < BN; c0 += 16 * a.csplit) {
+            float v[16];
 #pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] = 0.f;
-              for (int qr = 0; qr < a.csplit; ++qr) {
-                float4 x[4];
+            for (int j = 0; j < 16; ++j) v[j] = 0.f;
+#pragma unroll 1
+            constexpr int QF = FP8 ? 1 : 2;  // slices whose loads are in flight at once (registers)
+            for (int q0 = 0; q0 < a.csplit; q0 += QF) {
+              float4 x[QF][4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) x[j] = ld_dsmem4(dsmem_addr(part_s + row * BN + c0 + 4 * j, (uint32_t)qr));
+              for (int qq = 0; qq < QF; ++qq)
+                if (q0 + qq < a.csplit) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  v[4 * j] += x[j].x;
-                  v[4 * j + 1] += x[j].y;
-                  v[4 * j + 2] += x[j].z;
-                  v[4 * j + 3] += x[j].w;
+                  for (int j = 0; j < 4; ++j)
+                    x[qq][j] = ld_dsmem4(dsmem_addr(part_s + ((size_t)((c0 >> 2) + j) * BM + row) * 4,
+                                                    (uint32_t)(q0 + qq)));
                 }
-              }
-              finish(v, c0, nullptr);
+#pragma unroll
+              for (int qq = 0; qq < QF; ++qq)
+                if (q0 + qq < a.csplit) {
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    v[4 * j] += x[qq][j].x;
+                    v[4 * j + 1] += x[qq][j].y;
+                    v[4 * j + 2] += x[qq][j].z;
+                    v[4 * j + 3] += x[qq][j].w;
+                  }
+                }
             }
+            finish(v, c0, nullptr);
           }
-          cluster_sync();  // the first CTA has read every partial
+          cluster_sync();  // every partial has been read
           cl_done = true;
         } else if (!direct) {
           // the piece is written; one thread publishes it (the barrier orders the
@@ -717,7 +765,7 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
 #pragma unroll
                 for (int j = 0; j < 16; ++j) old[j] = j < nj ? p0[(size_t)j * a.M] : 0.f;
               }
-              constexpr int PB = (EPI == EPI_HEADS || FP8) ? 4 : 8;  // pieces per round of loads (registers)
+              constexpr int PB = FP8 ? 2 : (EPI == EPI_HEADS ? 4 : 8);  // pieces per round of loads (registers)
               for (int g0 = g_first; g0 <= g_last; g0 += PB) {
                 float v[PB][16];
 #pragma unroll
@@ -740,44 +788,62 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
           }
         }
       } else {
+        // ---------------------------------------------- streaming top-k
+        // Each CTA keeps, per column (lm_head row) of its current column
+        // tile, a sorted list of its best KMAX (vocabulary id, logit) entries
+        // as 64-bit order keys in shared memory.  An entry is offered only
+        // when it beats the column's threshold: the larger of the list's
+        // KMAX-th key and a bound shared by all CTAs through global memory.
+        // That bound is the smallest of TOPK_SLOTS slots; CTA g raises slot
+        // g % TOPK_SLOTS to its list's best key, so the slots hold the keys
+        // of TOPK_SLOTS distinct entries (one per slot, from distinct CTAs),
+        // and an entry below their minimum has KMAX better ones: it is not in
+        // the column's top KMAX.  The slots start at zero (no bound).
+        const int ewq = ew & 3;                 // warp within its set
+        const int set = SETS > 1 ? ew >> 2 : 0;  // which chunks its set takes
         if (nt != cur_nt) {
-          named_sync_epi();
+          named_sync_epi<EPT>();
           if (cur_nt >= 0) flush_lists(cur_nt, false);
-          named_sync_epi();
+          named_sync_epi<EPT>();
           reset_lists();
           cur_nt = nt;
           touched |= 1u << nt;
-          named_sync_epi();
+          named_sync_epi<EPT>();
         }
-        // The shared per-column thresholds of this tile's columns, read once
-        // per tile into the buffer of this accumulator's parity (the other
-        // buffer may still be read by a warp scanning the previous tile).
-        // Each is the order key of some CTA's 16th-best entry of that column,
-        // so at least 16 entries beat it: an entry that does not beat it is
-        // not in the column's top 16 and is not offered.  The first chunk's
-        // barriers order these stores before the scans read them.
-        unsigned long long* thr_t = thr_s + acc * BN;
-        unsigned long long gl[(BN + 127) / 128];  // loaded now, stored after the first TMEM read
+        // the shared bound slots of the 4 columns this warp merges in a chunk
+        // (columns ewq + 4i, i = 0..3), lane l holding slot l % 16 of column
+        // i = 2r + l / 16, loaded ahead of their use in the merge step
+        auto slots_load = [&](int c0, unsigned long long (&gs)[2]) {
 #pragma unroll
-        for (int i = 0; i < (BN + 127) / 128; ++i) {
-          const int c = threadIdx.x - 64 + i * 128, n = nt * BN + c;
-          gl[i] = (c < BN && n < a.N) ? __ldcg(a.thr + n) : ~0ull;
-        }
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 16) {
+          for (int r2 = 0; r2 < 2; ++r2) {
+            const int n = nt * BN + c0 + ewq + 4 * (2 * r2 + (lane >> 4));
+            gs[r2] = n < a.N ? __ldcg(a.thr + (size_t)n * TOPK_SLOTS + (lane & 15)) : ~0ull;
+          }
+        };
+        // the minimum of column i's slots, on every lane
+        auto slots_min = [&](const unsigned long long (&gs)[2], int i) {
+          unsigned long long x = (i & 2) ? gs[1] : gs[0];
+#pragma unroll
+          for (int o = 1; o < 16; o <<= 1) {
+            const unsigned long long y = __shfl_xor_sync(0xffffffffu, x, o);
+            x = y < x ? y : x;
+          }
+          return __shfl_sync(0xffffffffu, x, (i & 1) * 16);
+        };
+        auto publish = [&](int n, unsigned long long top_before, unsigned long long lk) {
+          const unsigned long long top = __shfl_sync(0xffffffffu, lk, 0);
+          if (lane == 0 && top > top_before) atomicMax(a.thr + (size_t)n * TOPK_SLOTS + (blockIdx.x % TOPK_SLOTS), top);
+        };
+        if constexpr (BN <= 16) {
+          // narrow tiles (a few rows, the batch-1 step): one chunk per tile,
+          // staged in shared memory; warp ew scans columns ew, ew + 4, ...
+          // over the 128 rows, 32 at a time
+          unsigned long long gs[2];
+          slots_load(0, gs);
           float v[16];
-          tmem_ld16(tbase + c0, v);
-          if (c0 == 0) {
-#pragma unroll
-            for (int i = 0; i < (BN + 127) / 128; ++i) {
-              const int c = threadIdx.x - 64 + i * 128;
-              if (c < BN) thr_t[c] = gl[i];
-            }
-          }
-          if (c0 + 16 >= BN) {
-            tc_fence_before();
-            mbar_arrive(tempty + acc);
-          }
+          tmem_ld16(tbase, v);
+          tc_fence_before();
+          mbar_arrive(tempty + acc);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             float z = a.mult * (FP8 ? wsc * v[j] : v[j]);
@@ -787,31 +853,32 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
           if (a.debug != nullptr && m < a.M) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const int n = nt * BN + c0 + j;
+              const int n = nt * BN + j;
               if (n < a.N) a.debug[(size_t)n * a.M + m] = v[j];
             }
           }
-          named_sync_epi();  // previous chunk's scans are done with the staging tile
+          named_sync_epi();  // previous tile's scans are done with the staging tile
 #pragma unroll
           for (int j = 0; j < 16; ++j) stg[j * BM + row] = v[j];
           named_sync_epi();
-          for (int jj = ew; jj < 16; jj += 4) {
-            const int c = c0 + jj;
+#pragma unroll 1
+          for (int i = 0; i < 4; ++i) {
+            const int c = ewq + 4 * i;
             const int n = nt * BN + c;
+            const unsigned long long gk = slots_min(gs, i);  // every lane takes part
             if (n >= a.N) continue;
             unsigned long long* Lk = lk_s + c * KMAX;
             unsigned long long lk = lane < KMAX ? Lk[lane] : 0ull;
             unsigned long long tk = __shfl_sync(0xffffffffu, lk, KMAX - 1);
-            const unsigned long long gk = thr_t[c];
+            const unsigned long long top_before = __shfl_sync(0xffffffffu, lk, 0);
 #pragma unroll 1
             for (int r = 0; r < 4; ++r) {
               const int rr = r * 32 + lane;
               const int mm = mt * BM + rr;
-              const unsigned long long key = mm < a.M ? order_key(stg[jj * BM + rr], mm) : 0ull;
+              const unsigned long long key = mm < a.M ? order_key(stg[c * BM + rr], mm) : 0ull;
               const bool pass = key > tk && key > gk;
               unsigned mask = __ballot_sync(0xffffffffu, pass);
               if (__popc(mask) > 3) {
-                // many at once (a column's first rows): one sort + merge pass
                 warp_key_merge(lk, tk, pass ? key : 0ull);
               } else {
                 while (mask) {
@@ -822,8 +889,86 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
               }
             }
             if (lane < KMAX) Lk[lane] = lk;
-            if (lane == 0 && tk > gk) atomicMax(a.thr + n, tk);  // a full list tightens the shared bound
+            publish(n, top_before, lk);
             __syncwarp();
+          }
+        } else {
+          // wide tiles: the two warp sets take alternate 16-column chunks.  Each
+          // thread filters its own row's 16 values against the columns'
+          // thresholds (kept current in shared memory) and appends the few
+          // that pass to the column's queue; after the set's barrier warp ewq
+          // merges the queues of columns ewq + 4i into their lists and renews
+          // their thresholds.
+          unsigned long long* qset = q_s + (size_t)set * 16 * BM;
+          int* qn = qn_s + set * 16;
+          const unsigned idk = (unsigned)(0x7fffffff - m);  // low half of this row's keys
+#pragma unroll 1
+          for (int c0 = set * 16; c0 < BN; c0 += 16 * SETS) {
+            unsigned long long gs[2];
+            slots_load(c0, gs);
+            float v[16];
+            tmem_ld16(tbase + c0, v);
+            if (c0 + 16 * SETS >= BN) {  // this set's last chunk of the tile
+              tc_fence_before();
+              mbar_arrive(tempty + acc);
+            }
+            const int nj = min(16, a.N - (nt * BN + c0));  // valid columns of the chunk
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              float z = a.mult * (FP8 ? wsc * v[j] : v[j]);
+              if (a.cap > 0.f) z = a.cap * tanhf(z / a.cap);
+              v[j] = z;
+            }
+            if (a.debug != nullptr && m < a.M) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (j < nj) a.debug[(size_t)(nt * BN + c0 + j) * a.M + m] = v[j];
+            }
+            if (m < a.M) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                unsigned u = __float_as_uint(v[j] + 0.f);
+                u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+                const unsigned long long key = ((unsigned long long)u << 32) | idk;
+                if (j < nj && key > thr_s[c0 + j]) qset[j * BM + atomicAdd(qn + j, 1)] = key;
+              }
+            }
+            named_sync_set(set);
+#pragma unroll 1
+            for (int i = 0; i < 4; ++i) {
+              const int jj = ewq + 4 * i, c = c0 + jj, n = nt * BN + c;
+              const unsigned long long gk = slots_min(gs, i);  // every lane takes part
+              if (jj >= nj) continue;
+              const int cnt = qn[jj];
+              unsigned long long* Lk = lk_s + c * KMAX;
+              unsigned long long lk = lane < KMAX ? Lk[lane] : 0ull;
+              unsigned long long tk = __shfl_sync(0xffffffffu, lk, KMAX - 1);
+              if (cnt > 0) {
+                const unsigned long long top_before = __shfl_sync(0xffffffffu, lk, 0);
+#pragma unroll 1
+                for (int b0 = 0; b0 < cnt; b0 += 32) {
+                  unsigned long long ck = b0 + lane < cnt ? qset[jj * BM + b0 + lane] : 0ull;
+                  if (ck <= tk || ck <= gk) ck = 0ull;  // no longer beats the list or the shared bound
+                  unsigned mask = __ballot_sync(0xffffffffu, ck != 0ull);
+                  if (__popc(mask) > 3) {
+                    warp_key_merge(lk, tk, ck);
+                  } else {
+                    while (mask) {
+                      const int src = __ffs(mask) - 1;
+                      mask &= mask - 1;
+                      warp_key_offer(lk, tk, __shfl_sync(0xffffffffu, ck, src));
+                    }
+                  }
+                }
+                if (lane < KMAX) Lk[lane] = lk;
+                publish(n, top_before, lk);
+              }
+              if (lane == 0) {
+                thr_s[c] = tk > gk ? tk : gk;
+                qn[jj] = 0;
+              }
+            }
+            named_sync_set(set);  // queues emptied and thresholds renewed before the next chunk's filter
           }
         }
       }
@@ -835,7 +980,7 @@ __global__ void __launch_bounds__(threads_of(FP8), 1)
       cluster_sync();
     }
     if constexpr (TOPK) {
-      if (!named_sync_or(*abort_flag != 0)) {
+      if (!named_sync_or<EPT>(*abort_flag != 0)) {
         if (cur_nt >= 0) flush_lists(cur_nt, false);
         for (int nt = 0; nt < a.n_tiles; ++nt)
           if (!(touched & (1u << nt))) flush_lists(nt, true);
@@ -928,7 +1073,7 @@ int launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, const TcArgs& args, 
   constexpr int smem = TcCfg<BN, FP8>::smem_bytes(EPI);
   const int rc = set_smem_attr<BN, EPI, FP8>();
   if (rc) return rc;
-  return launch_kx(tc_gemm_kernel<BN, EPI, FP8>, dim3(grid), dim3(threads_of(FP8)), smem, c,
+  return launch_kx(tc_gemm_kernel<BN, EPI, FP8>, dim3(grid), dim3(threads_of(EPI, BN, FP8)), smem, c,
                    args.csplit > 1 ? args.csplit : 1, ma, mb, args);
 }
 
@@ -942,7 +1087,7 @@ int max_clusters(int cs) {
   if (set_smem_attr<BN, EPI, FP8>()) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cs * 64);
-  cfg.blockDim = dim3(threads_of(FP8));
+  cfg.blockDim = dim3(threads_of(EPI, BN, FP8));
   cfg.dynamicSmemBytes = TcCfg<BN, FP8>::smem_bytes(EPI);
   cudaLaunchAttribute at;
   at.id = cudaLaunchAttributeClusterDimension;
@@ -964,11 +1109,9 @@ template <int BN, bool FP8>
 int max_clusters_epi(int epi, int cs) {
   switch (epi) {
     case EPI_SWIGLU:
-      if constexpr (BN <= 64) return max_clusters<BN, EPI_SWIGLU, FP8>(cs);
-      return 0;
+      return max_clusters<BN, EPI_SWIGLU, FP8>(cs);
     case EPI_HEADS:
-      if constexpr (BN <= 64) return max_clusters<BN, EPI_HEADS, FP8>(cs);
-      return 0;
+      return max_clusters<BN, EPI_HEADS, FP8>(cs);
     case EPI_PLAIN: return max_clusters<BN, EPI_PLAIN, FP8>(cs);
     default: return 0;
   }
@@ -979,6 +1122,8 @@ int max_clusters_of(int bn, int epi, bool fp8, int cs) {
     case 16: return fp8 ? max_clusters_epi<16, true>(epi, cs) : max_clusters_epi<16, false>(epi, cs);
     case 32: return fp8 ? max_clusters_epi<32, true>(epi, cs) : max_clusters_epi<32, false>(epi, cs);
     case 64: return fp8 ? max_clusters_epi<64, true>(epi, cs) : max_clusters_epi<64, false>(epi, cs);
+    case 128: return fp8 ? max_clusters_epi<128, true>(epi, cs) : max_clusters_epi<128, false>(epi, cs);
+    case 256: return fp8 ? max_clusters_epi<256, true>(epi, cs) : max_clusters_epi<256, false>(epi, cs);
     default: return 0;
   }
 }
@@ -988,7 +1133,7 @@ int max_clusters_of(int bn, int epi, bool fp8, int cs) {
 // at least three quarters of the SMs without exceeding them, when every
 // tile's cluster fits the device at once.  ctas <= -2 forces cs = -ctas.
 int pick_csplit(int tiles, int n_chunks, int bn, int epi, bool fp8, int nsm, int ctas) {
-  if (epi == EPI_TOPK || bn > 64) return 1;
+  if (epi == EPI_TOPK) return 1;
   if (ctas <= -2) {
     const int cs = -ctas;
     return cs <= 8 && cs <= n_chunks && max_clusters_of(bn, epi, fp8, cs) >= 1 ? cs : 1;
@@ -1006,11 +1151,9 @@ int launch_epi(int epi, const CUtensorMap& ma, const CUtensorMap& mb, const TcAr
   switch (epi) {
     case EPI_TOPK: return launch_bn<BN, EPI_TOPK, FP8>(ma, mb, args, grid, c);
     case EPI_SWIGLU:
-      if constexpr (BN <= 64) return launch_bn<BN, EPI_SWIGLU, FP8>(ma, mb, args, grid, c);
-      return DFLASH2_ERR_SHAPE;
+      return launch_bn<BN, EPI_SWIGLU, FP8>(ma, mb, args, grid, c);
     case EPI_HEADS:
-      if constexpr (BN <= 64) return launch_bn<BN, EPI_HEADS, FP8>(ma, mb, args, grid, c);
-      return DFLASH2_ERR_SHAPE;
+      return launch_bn<BN, EPI_HEADS, FP8>(ma, mb, args, grid, c);
     default: return launch_bn<BN, EPI_PLAIN, FP8>(ma, mb, args, grid, c);
   }
 }
@@ -1024,7 +1167,7 @@ int launch_epi(int epi, bool fp8, const CUtensorMap& ma, const CUtensorMap& mb, 
 }  // namespace
 
 bool gemm_fusable(int M, int N, int epi) {
-  if (pick_bn(M, N) > 64) return false;
+  (void)N;
   return epi != kEpiSwiglu || M % BM == 0;
 }
 

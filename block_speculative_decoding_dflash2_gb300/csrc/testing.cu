@@ -107,7 +107,7 @@ int dflash2_test_layout(const dflash2_config* cfg, int batch, int n_new, int max
 
 size_t dflash2_test_topk_workspace(int dtype, int M, int N) {
   const int n_lists = std::max(kMaxSM, topk_scan_lists(M));
-  size_t t = al(256) + 2 * al((size_t)n_lists * N * KMAX * 4) + al((size_t)N * 8);
+  size_t t = al(256) + 2 * al((size_t)n_lists * N * KMAX * 4) + al((size_t)N * kTopkSlots * 8);
   if (dtype == DFLASH2_F32) t += al((size_t)N * M * 4);
   return t;
 }
@@ -143,7 +143,7 @@ int dflash2_test_gemm_topk(int dtype, const void* W, int M, int K, const void* X
     // step zeroes them in the kernel before the lm_head instead)
     unsigned long long* thr =
         reinterpret_cast<unsigned long long*>(base + al(256) + 2 * al((size_t)n_lists_cap * N * KMAX * 4));
-    if (cudaMemsetAsync(thr, 0, (size_t)N * 8, c.stream) != cudaSuccess) return DFLASH2_ERR_CUDA;
+    if (cudaMemsetAsync(thr, 0, (size_t)N * kTopkSlots * 8, c.stream) != cudaSuccess) return DFLASH2_ERR_CUDA;
     g.topk = true;
     g.lists_v = lv;
     g.lists_i = li;
@@ -154,7 +154,7 @@ int dflash2_test_gemm_topk(int dtype, const void* W, int M, int K, const void* X
     n_lists = gemm_topk_lists(M, N, K, c.nsm, dtype);
   } else {
     float* logits = reinterpret_cast<float*>(base + al(256) + 2 * al((size_t)n_lists_cap * N * KMAX * 4) +
-                                             al((size_t)N * 8));
+                                             al((size_t)N * kTopkSlots * 8));
     g.out = logits;
     rc = gemm_f32(g, c);
     if (rc) return rc;

@@ -9,6 +9,25 @@ import oracle as O
 TOL = {"f32": 1e-4, "bf16": 2e-2, "fp8w": 2e-2}
 
 
+def e2e_tol(case):
+    """End-to-end logit bound of a full-size case: max(2e-2, 1.6 x the
+    oracle's own bf16 rounding-chaos floor at that case), the floor measured
+    by tests/golden/make_bf16_chaos_floor.py (oracle only) and stored in
+    tests/golden/bf16_chaos_floor.txt."""
+    from tests.conftest import read_golden
+    floors = {k: float(v) for k, v in read_golden("bf16_chaos_floor.txt")}
+    return max(2e-2, 1.6 * floors[case])
+
+
+# Near-ties allowed by the discrete checks, recorded per case and written to
+# tests/near_tie_counts.txt when the session ends (tests/conftest.py).
+NEAR_TIES = {}
+
+
+def record_near_ties(case, kind, count, total):
+    NEAR_TIES[(case, kind)] = (count, total)
+
+
 def lib():
     from block_speculative_decoding_dflash2_gb300 import build as bld
     bld.build()

@@ -7,12 +7,12 @@ import pytest
 
 import dflash2_synth as S
 import oracle as O
-from tests.helpers import TOL, Case, lib, topk_compare
+from tests.helpers import TOL, Case, e2e_tol, lib, record_near_ties, topk_compare
 
 pytestmark = pytest.mark.gpu
 
 
-def check_case(case, tol=None):
+def check_case(case, tol=None, name=None):
     cfg = case.cfg
     tol = TOL[cfg["dtype"]] if tol is None else tol
     k = cfg["top_k"]
@@ -31,6 +31,8 @@ def check_case(case, tol=None):
     # end-to-end: against the oracle's logits, near-ties counted
     near = topk_compare(cid, z, k, tol)
     print(f"[parity] {cfg['dtype']} b={case.b} max|dlogit|={err:.3e} near-tie rows={near}/{cid.shape[0] * cid.shape[1]}")
+    if name:
+        record_near_ties(name, "top-k rows", near, cid.shape[0] * cid.shape[1])
     return err, near
 
 
@@ -102,13 +104,14 @@ def test_small_bf16_gqa5_block16():
 @pytest.mark.slow
 def test_qwen3_8b_shape_batch1():
     # End to end at this shape the bf16 pipeline is rounding-chaotic: the
-    # oracle's own bf16-storage logits move by 0.0305 (max abs) when its
+    # oracle's own bf16-storage logits move by about 0.03 (max abs) when its
     # weights are nudged by 1e-6 relative, the size of fp32-vs-fp64
-    # accumulation noise.  The end-to-end bound is therefore 5e-2 (1.6x that
-    # floor); every stage is held to ~1 bf16 ulp in test_gpu_stagewise.py.
+    # accumulation noise (measured per case, tests/golden/bf16_chaos_floor.txt).
+    # The end-to-end bound is max(2e-2, 1.6 x that floor); every stage is held
+    # to ~1 bf16 ulp in test_gpu_stagewise.py.
     cfg = S.config_of("qwen3_8b_b1")
     case = Case(cfg, ctx_lens=[2040], n_new=[8], seed=21).run_gpu()
-    check_case(case, tol=5e-2)
+    check_case(case, tol=e2e_tol("qwen3_8b_b1"), name="qwen3_8b_b1")
 
 
 @pytest.mark.parametrize("cs,dtype", [(2, "bf16"), (4, "bf16"), (3, "fp8w")])

@@ -11,7 +11,7 @@ import pytest
 
 import dflash2_synth as S
 import oracle as O
-from tests.helpers import TOL, Case, lib, topk_compare
+from tests.helpers import TOL, Case, e2e_tol, lib, record_near_ties, topk_compare
 from tests.test_gpu_draft import check_case
 from tests.test_gpu_full_configs import check_select_and_verify
 from tests.test_gpu_stagewise import run_stagewise
@@ -35,7 +35,7 @@ def test_fp8_small_two_layers_ragged_batch():
     cfg = small_fp8(index=22)
     case = Case(cfg, ctx_lens=[40, 0, 200], n_new=[1, 8, 3], seed=22).run_gpu()
     check_case(case)
-    check_select_and_verify(case, [0, 1, 2], None)
+    check_select_and_verify(case, [0, 1, 2], None, "fp8 small, two layers")
 
 
 def test_fp8_small_wide_batch_unfused_paths():
@@ -123,10 +123,11 @@ def test_a3b_30b_fp8_sweep_point(batch, context):
         z.append(O.draft_block(cfg, Wv, int(anchor[s]), ctx, st))
     z = np.stack(z)
     err = np.max(np.abs(dbg - z))
-    tol = 5e-2  # the bf16 pipeline's rounding-chaos floor at full size
-    assert err <= tol, f"max |logit - oracle| = {err}"
+    tol = e2e_tol(f"a3b_30b_fp8_ctx{context}")  # the bf16 pipeline's rounding-chaos floor, measured
+    assert err <= tol, f"max |logit - oracle| = {err} (bound {tol})"
     near = topk_compare(cid[seqs], z, k, tol)
     print(f"[parity] fp8w b={batch} ctx={context} sampled {seqs}: max|dlogit|={err:.3e} near-tie rows={near}")
+    record_near_ties(f"a3b_30b_fp8 b={batch} ctx={context}", "top-k rows", near, len(seqs) * (B_ - 1))
     # selector (factor table) and verify on the GPU's lattice, every sequence
     r.build_selector_table()
     r.select(dev(anchor))
@@ -139,6 +140,7 @@ def test_a3b_30b_fp8_sweep_point(batch, context):
             gi = [list(cid[s, i]).index(path[s, i]) for i in range(B_ - 1)]
             assert sc - O.path_score(cfg, Wv, int(anchor[s]), cid[s], cz[s], gi) < 1e-4
             near += 1
+    record_near_ties(f"a3b_30b_fp8 b={batch} ctx={context}", "selector paths", near, batch)
     assert near <= max(1, batch // 8)
     target = S.make_agreeing_target(path, cfg, 0.7)
     seq = dev(np.full(batch, context))

@@ -36,7 +36,10 @@ def _mat(rows, cols, seed, std, dtype):
     (4096, 8, 4096, -8),     # 32 clusters x 8 CTAs > the SM count: clusters queue
     (128, 16, 64, -2),       # one K chunk: too short to split, whole tiles instead
     (384, 100, 1024, -4),    # 100 columns in 16-wide tiles (at most 4 row tiles): split
-    (640, 100, 1024, -4),    # 128-wide activation tile: no cluster split, whole tiles
+    (640, 100, 1024, -4),    # 128-wide activation tile: 4-slice cluster split of wide partial tiles
+    (512, 256, 2048, -4),    # 256-wide activation tile: 4 slices summed through distributed shared memory
+    (4096, 256, 12288, 0),   # the down / feature shape at 256 rows (batch 32): the library's cluster schedule
+    (6144, 256, 4096, 0),    # the QKV shape at 256 rows
 ])
 @pytest.mark.parametrize("accumulate", [False, True])
 def test_bf16_gemm_matches_float64_product(M, N, K, ctas, accumulate):
@@ -54,11 +57,10 @@ def test_bf16_gemm_matches_float64_product(M, N, K, ctas, accumulate):
         torch.cuda.synchronize()
         assert 1 <= used <= 256 and (ctas <= 0 or used <= ctas)
         if ctas <= -2:
-            # the cluster schedule ran where it applies (at least -ctas K chunks and
-            # an activation tile at most 64 wide, i.e. N <= 64 or at most 4 row
-            # tiles): -ctas CTAs for each whole tile, else one
+            # the cluster schedule ran where it applies (at least -ctas K chunks):
+            # -ctas CTAs for each whole tile, else one
             tiles = B.dflash2_test_gemm(B.BF16, S.to_torch(W), S.to_torch(X), -1, torch.empty_like(out), ws)
-            split = (K + 63) // 64 >= -ctas and (N <= 64 or M <= 512)
+            split = (K + 63) // 64 >= -ctas
             assert used == tiles * (-ctas if split else 1)
         got = out.double().cpu().numpy() - (base if accumulate else 0.0)
         w64, x64 = W.values.astype(np.float64), X.values.astype(np.float64)

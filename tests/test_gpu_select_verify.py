@@ -10,7 +10,7 @@ import pytest
 import dflash2_synth as S
 import oracle as O
 from tests.conftest import read_golden
-from tests.helpers import lib
+from tests.helpers import lib, record_near_ties
 
 pytestmark = pytest.mark.gpu
 
@@ -72,6 +72,7 @@ def test_selector_matches_oracle_viterbi(dtype, V, H, k, D, r, b, kind):
             alt = O.path_score(cfg, W, int(anchor[s]), cand[s], z[s].astype(np.float64), gi)
             assert sc - alt < 1e-4, (s, list(path[s]), list(p))
             near += 1
+    record_near_ties(f"selector {dtype} V={V} H={H} k={k} D={D} r={r} b={b} ({kind})", "selector paths", near, b)
     assert near <= max(1, b // 4)
 
 

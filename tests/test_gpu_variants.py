@@ -8,7 +8,7 @@ import pytest
 
 import dflash2_synth as S
 import oracle as O
-from tests.helpers import Case, lib
+from tests.helpers import Case, e2e_tol, lib
 from tests.test_gpu_draft import check_case
 from tests.test_gpu_stagewise import run_stagewise
 
@@ -51,7 +51,7 @@ def test_sliding_window_qwen3_8b_shape():
     cfg = S.config_of("qwen3_8b_b1", sliding_window=512)
     case = Case(cfg, ctx_lens=[2040], n_new=[8], seed=32).run_gpu()
     run_stagewise(case)
-    check_case(case, tol=5e-2)
+    check_case(case, tol=e2e_tol("qwen3_8b_b1_window512"), name="qwen3_8b_b1_window512")
 
 
 @pytest.mark.parametrize("n_max,p_min", [(0, 0.0), (4, 0.0), (0, 0.3), (7, 0.6)])

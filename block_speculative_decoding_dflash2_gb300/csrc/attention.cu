@@ -238,38 +238,39 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-constexpr int MKT = 128;         // keys per tile
-constexpr int KST = 2;           // K/V tile stages
+constexpr int kMaxStages = 4;    // K/V tile stages at most
 constexpr int kMaxCluster = 8;   // CTAs per cluster (portable)
 constexpr int CLW = 16;          // warps per CTA
 constexpr int CLT = 32 * CLW;    // threads
 constexpr int kMaxShares = 8;    // key shares per 16-row block (16 keys each per tile)
+constexpr size_t kAttnSmem = 227 * 1024;
 
-// Key shares per 16-row block: a power of two, so each share is a whole
-// number of 16-key steps, and enough (row block, share) combinations to give
-// most warps one (at most CLW combinations for 16 row blocks or fewer).
-__host__ __device__ inline int attn_ksplit(int nrb) {
+// Key shares per 16-row block: a power of two, so each share of an mkt-key
+// tile is a whole number of 16-key steps, and enough (row block, share)
+// combinations to give most warps one (at most CLW combinations for 16 row
+// blocks or fewer).
+__host__ __device__ inline int attn_ksplit(int nrb, int mkt) {
   int k = 1;
-  while (k < kMaxShares && nrb * 2 * k <= CLW) k *= 2;
+  while (k < kMaxShares && nrb * 2 * k <= CLW && mkt / (2 * k) >= 16) k *= 2;
   return k;
 }
 
-// Shared memory: Q rows; the K/V stages, which after the key loop hold the
-// per-combination partial states (read by the whole cluster); the merge
-// weights of this CTA's rows; the page ids of its key chunk (npg of them).
+// Shared memory: Q rows; the kst K/V stages of mkt keys, which after the key
+// loop hold the per-combination partial states (read by the whole cluster);
+// the merge weights of this CTA's rows; the page ids of its key chunk (npg).
 template <int DH>
-__host__ __device__ inline size_t attn_kv_bytes(int R) {
+__host__ __device__ inline size_t attn_kv_bytes(int R, int mkt, int kst) {
   const int nrb = (R + 15) / 16;
-  const size_t kvb = (size_t)KST * 2 * MKT * (DH + 8) * 2;
-  const size_t comb = (size_t)nrb * attn_ksplit(nrb) * 16 * (DH + 2) * 4;
+  const size_t kvb = (size_t)kst * 2 * mkt * (DH + 8) * 2;
+  const size_t comb = (size_t)nrb * attn_ksplit(nrb, mkt) * 16 * (DH + 2) * 4;
   return kvb > comb ? kvb : comb;
 }
 template <int DH>
-size_t attn_cl_smem(int R, int npg) {
+size_t attn_cl_smem(int R, int npg, int mkt, int kst) {
   const int nrb = (R + 15) / 16;
   const size_t qb = (size_t)nrb * 16 * (DH + 8) * 2;
-  return qb + attn_kv_bytes<DH>(R) + (size_t)(R + kMaxCluster) * kMaxShares * 2 * 4 + (size_t)npg * 4 + 8 +
-         KST * sizeof(uint64_t);
+  return qb + attn_kv_bytes<DH>(R, mkt, kst) + (size_t)(R + kMaxCluster) * kMaxShares * 2 * 4 + (size_t)npg * 4 +
+         8 + kMaxStages * sizeof(uint64_t);
 }
 
 template <int DH>
@@ -277,7 +278,9 @@ __global__ void __launch_bounds__(CLT, 1) attn_cluster_kernel(
     const bf16* __restrict__ q, const bf16* __restrict__ kb, const bf16* __restrict__ vb, const bf16* __restrict__ kc,
     const bf16* __restrict__ vc, const int32_t* __restrict__ block_table, int max_pages, int page_size, int n_pages,
     const int32_t* __restrict__ ctx_len, const int32_t* __restrict__ new_off, int B, int nq, int nkv, int npg,
-    int window, bf16* __restrict__ o, unsigned* status) {
+    int window, int MKT, int KST, bf16* __restrict__ o, unsigned* status) {
+  // MKT keys per K/V tile, KST tile stages (KST - 1 tiles in flight while one
+  // is consumed)
   constexpr int MCPW = 1;  // (row block, key share) combinations per warp
   constexpr int LD = DH + 8;  // padded smem row (elements): ldmatrix rows hit distinct banks
   constexpr int NT = DH / 8;  // n8 tiles across the head dimension
@@ -289,13 +292,12 @@ __global__ void __launch_bounds__(CLT, 1) attn_cluster_kernel(
   const int sp = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
   const int grp = nq / nkv, R = grp * B;
   const int nrb = (R + 15) / 16;
-  const int ksplit = attn_ksplit(nrb);
+  const int ksplit = attn_ksplit(nrb, MKT);
   const int ncombo = nrb * ksplit;
-  const int np = NS * ksplit;  // partials per row across the cluster
   bf16* Qs = reinterpret_cast<bf16*>(smraw);
   bf16* KV = Qs + nrb * 16 * LD;                        // [KST][K, V][MKT][LD]
   float* comb = reinterpret_cast<float*>(KV);            // [ncombo][16][FS], after the key loop
-  float* wts = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(KV) + attn_kv_bytes<DH>(R));  // merge weights
+  float* wts = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(KV) + attn_kv_bytes<DH>(R, MKT, KST));  // merge weights
   int* pg = reinterpret_cast<int*>(wts + (size_t)(R + kMaxCluster) * kMaxShares * 2);  // page ids of the chunk
   uint64_t* kvbar = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(pg + npg) + 7) & ~uintptr_t(7));
   if (threadIdx.x == 0) {  // one K/V stage completes when its 2*MKT row copies have landed
@@ -310,7 +312,10 @@ __global__ void __launch_bounds__(CLT, 1) attn_cluster_kernel(
   const int CH = (((L - w0 + NS - 1) / NS) + 15) & ~15;
   const int k0 = w0 + min(sp * CH, L - w0), k1 = min(k0 + CH, L);
   if (P > max_pages * page_size && sp == 0 && threadIdx.x == 0) flag(status, DFLASH2_DEV_BAD_LENGTH);
-  const float scale = rsqrtf((float)DH);
+  // scores are kept in base-2 units (1/sqrt(d) times log2(e)), so each
+  // exponential is one exp2 and the softmax is unchanged: 2^(x log2 e) = e^x
+  constexpr float kLog2e = 1.4426950408889634f;
+  const float scale = rsqrtf((float)DH) * kLog2e;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // page ids of the chunk's context keys, once (-1: past the table)
@@ -363,7 +368,7 @@ __global__ void __launch_bounds__(CLT, 1) attn_cluster_kernel(
   };
   const int ntiles = (k1 - k0 + MKT - 1) / MKT;  // 0 for an empty chunk
   cp_async_commit();  // the Q rows
-  if (ntiles > 0) issue(k0, 0);
+  for (int i = 0; i < KST && i < ntiles; ++i) issue(k0 + i * MKT, i);  // every stage starts filling
   volatile int never = 0;
 
   // per-combination online-softmax state: rows lane/4 and lane/4 + 8 of the block
@@ -376,12 +381,11 @@ __global__ void __launch_bounds__(CLT, 1) attn_cluster_kernel(
     for (int n = 0; n < NT; ++n) acc[c][n][0] = acc[c][n][1] = acc[c][n][2] = acc[c][n][3] = 0.f;
   }
   cp_async_wait<0>();
+  __syncthreads();  // the Q rows and the zero-filled rows of the first tiles are visible to every warp
   for (int t = 0; t < ntiles; ++t) {
-    if (t + 1 < ntiles) issue(k0 + (t + 1) * MKT, (t + 1) % KST);
     // tile t has landed (bounded wait: on a timeout the status says so)
     if (!mbar_wait(kvbar + t % KST, (uint32_t)((t / KST) & 1), &never, 1000000000ull) && threadIdx.x == 0)
       flag(status, DFLASH2_DEV_WAIT_TIMEOUT);
-    __syncthreads();
     const bf16* Ks = KV + (size_t)(t % KST) * 2 * MKT * LD;
     const bf16* Vs = Ks + MKT * LD;
     const int nk = min(MKT, k1 - (k0 + t * MKT));
@@ -420,27 +424,29 @@ __global__ void __launch_bounds__(CLT, 1) attn_cluster_kernel(
           mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
         }
         const float mn0 = fmaxf(m_st[slot][0], mx0), mn1 = fmaxf(m_st[slot][1], mx1);
-        const float f0 = expf(m_st[slot][0] - mn0), f1 = expf(m_st[slot][1] - mn1);
-        m_st[slot][0] = mn0;
-        m_st[slot][1] = mn1;
+        // the accumulators are rescaled only when a row's running max grew
+        // (after the first keys it rarely does)
+        if (__any_sync(0xffffffffu, mn0 > m_st[slot][0] || mn1 > m_st[slot][1])) {
+          const float f0 = exp2f(m_st[slot][0] - mn0), f1 = exp2f(m_st[slot][1] - mn1);
+          l_st[slot][0] *= f0;
+          l_st[slot][1] *= f1;
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            acc[slot][n][0] *= f0;
+            acc[slot][n][1] *= f0;
+            acc[slot][n][2] *= f1;
+            acc[slot][n][3] *= f1;
+          }
+          m_st[slot][0] = mn0;
+          m_st[slot][1] = mn1;
+        }
         float p[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) p[e] = expf(sv[e] - ((e & 2) ? mn1 : mn0));
-        float s0 = p[0] + p[1] + p[4] + p[5], s1 = p[2] + p[3] + p[6] + p[7];
-#pragma unroll
-        for (int o2 = 1; o2 <= 2; o2 <<= 1) {
-          s0 += __shfl_xor_sync(0xffffffffu, s0, o2);
-          s1 += __shfl_xor_sync(0xffffffffu, s1, o2);
-        }
-        l_st[slot][0] = l_st[slot][0] * f0 + s0;
-        l_st[slot][1] = l_st[slot][1] * f1 + s1;
-#pragma unroll
-        for (int n = 0; n < NT; ++n) {
-          acc[slot][n][0] *= f0;
-          acc[slot][n][1] *= f0;
-          acc[slot][n][2] *= f1;
-          acc[slot][n][3] *= f1;
-        }
+        for (int e = 0; e < 8; ++e) p[e] = exp2f(sv[e] - ((e & 2) ? mn1 : mn0));
+        // each lane keeps the sum of its own keys' weights; the four lanes of
+        // a row are summed once, after the key loop
+        l_st[slot][0] += (p[0] + p[1]) + (p[4] + p[5]);
+        l_st[slot][1] += (p[2] + p[3]) + (p[6] + p[7]);
         // P as the A operand, split hi + lo
         float lo[8];
         uint32_t ph[4], pl[4];
@@ -465,14 +471,21 @@ __global__ void __launch_bounds__(CLT, 1) attn_cluster_kernel(
         }
       }
     }
-    __syncthreads();  // this stage is refilled two tiles later
+    __syncthreads();  // tile t is consumed: its stage takes tile t + KST
+    if (t + KST < ntiles) issue(k0 + (t + KST) * MKT, t % KST);
   }
-  __syncthreads();  // the K/V stages now hold the partial states
+  // (the last iteration's barrier: every warp is done with the K/V stages,
+  // which now hold the partial states)
   // each combination's partial state -> shared memory (empty ones: m = -inf, l = 0)
 #pragma unroll
   for (int slot = 0; slot < MCPW; ++slot) {
     const int combo = warp + slot * CLW;
     if (combo >= ncombo) break;
+#pragma unroll
+    for (int o2 = 1; o2 <= 2; o2 <<= 1) {  // a row's weight sum over its four lanes
+      l_st[slot][0] += __shfl_xor_sync(0xffffffffu, l_st[slot][0], o2);
+      l_st[slot][1] += __shfl_xor_sync(0xffffffffu, l_st[slot][1], o2);
+    }
     float* cb = comb + (size_t)combo * 16 * FS;
     const int r0 = lane >> 2, c0 = (lane & 3) * 2;
 #pragma unroll
@@ -503,7 +516,7 @@ __global__ void __launch_bounds__(CLT, 1) attn_cluster_kernel(
     float l = 0.f;
     for (int ks = 0; ks < ksplit; ++ks) {
       const float* b = base + (size_t)ks * 16 * FS;
-      const float w = b[1] > 0.f ? expf(b[0] - M) : 0.f;
+      const float w = b[1] > 0.f ? exp2f(b[0] - M) : 0.f;  // base-2 maxima
       wk[r * ksplit + ks] = w;
       l += b[1] * w;
     }
@@ -548,7 +561,7 @@ __global__ void __launch_bounds__(CLT, 1) attn_cluster_kernel(
 #pragma unroll
     for (int p = 0; p < kMaxCluster; ++p)
       if (p < NS) {
-        ml[p].x = ml[p].y > 0.f ? expf(ml[p].x - M) : 0.f;
+        ml[p].x = ml[p].y > 0.f ? exp2f(ml[p].x - M) : 0.f;  // base-2 maxima
         den += ml[p].y * ml[p].x;
       }
     const float inv = den > 0.f ? 1.f / den : 0.f;
@@ -661,12 +674,15 @@ int chunk_of(int max_ctx, int B, int batch, int nkv, int nsm) {
   return (int)std::max(64L, std::min(1024L, ch));
 }
 
-// CTAs per cluster: one per 64 keys of the longest sequence, at most 16, and
-// no more than it takes to give the SMs about two CTAs each.
+// CTAs per cluster: at most kMaxCluster and one per 64 keys of the longest
+// sequence.  A CTA takes a whole SM, so while the (kv head, sequence) pairs
+// fit the SMs the clusters fill one wave; beyond that, enough CTAs for about
+// two per SM, finer pieces for the scheduler to balance ragged contexts.
 int attn_cluster_ctas(int max_ctx, int B, int batch, int nkv, int nsm) {
   const long L = (long)max_ctx + B;
-  const long fill = std::max(1L, (2L * nsm + (long)nkv * batch - 1) / ((long)nkv * batch));
-  return (int)std::max(1L, std::min<long>({(long)kMaxCluster, (L + MKT - 1) / MKT, fill}));
+  const long pairs = (long)nkv * batch;
+  const long fill = pairs <= nsm ? nsm / pairs : (2L * nsm + pairs - 1) / pairs;
+  return (int)std::max(1L, std::min<long>({(long)kMaxCluster, (L + 63) / 64, fill}));
 }
 
 template <int DH>
@@ -676,7 +692,7 @@ int launch_cluster(int R, int max_ctx, int page_size, int batch, int nkv, const 
                    int window, bf16* o) {
   static bool attr = false;  // set once, before any capture
   if (!attr) {
-    if (cudaFuncSetAttribute(attn_cluster_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024))
+    if (cudaFuncSetAttribute(attn_cluster_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAttnSmem))
       return DFLASH2_ERR_CUDA;
     attr = true;
   }
@@ -684,10 +700,24 @@ int launch_cluster(int R, int max_ctx, int page_size, int batch, int nkv, const 
   // chunk length bound (keys), then its pages
   const long ch = ((((long)max_ctx + B + ns - 1) / ns) + 15) & ~15L;
   const int npg = (int)((ch + page_size - 1) / page_size + 1);
-  const size_t smem = attn_cl_smem<DH>(R, npg);
-  if (smem > 200 * 1024) return DFLASH2_ERR_SHAPE;
+  // K/V ring: three stages of 128 keys for up to 32 query rows per kv head
+  // (every share of a tile still a whole 16-key step for 8 shares), four of
+  // 64 keys for more rows (their Q tile and partials take more space);
+  // shallower when the chunk's page list does not leave room
+  const int nrb = (R + 15) / 16;
+  const int geo[4][2] = {{nrb <= 2 ? 128 : 64, nrb <= 2 ? 3 : 4}, {64, 4}, {64, 3}, {64, 2}};
+  int mkt = 0, kst = 0;
+  size_t smem = 0;
+  for (const auto& gk : geo) {
+    mkt = gk[0];
+    kst = gk[1];
+    smem = attn_cl_smem<DH>(R, npg, mkt, kst);
+    if (smem <= kAttnSmem) break;
+  }
+  if (smem > kAttnSmem) return DFLASH2_ERR_SHAPE;
   return launch_kx(attn_cluster_kernel<DH>, dim3(ns, nkv, batch), dim3(CLT), smem, c, ns, q, kb, vb, kc, vc,
-                   block_table, max_pages, page_size, n_pages, ctx_len, new_off, B, nq, nkv, npg, window, o, c.status);
+                   block_table, max_pages, page_size, n_pages, ctx_len, new_off, B, nq, nkv, npg, window, mkt, kst, o,
+                   c.status);
 }
 
 }  // namespace
@@ -710,8 +740,7 @@ int launch_attention(int dtype, const void* q, const void* kb, const void* vb, c
                      int max_ctx, int window, float* part, void* o_out, const Ctx& c) {
   const int R = (nq / nkv) * B;
   const int nrb = (R + 15) / 16;
-  const int ncombo = nrb * attn_ksplit(nrb);
-  if (dtype == DFLASH2_BF16 && (d == 64 || d == 128) && ncombo <= CLW) {
+  if (dtype == DFLASH2_BF16 && (d == 64 || d == 128) && nrb <= CLW) {  // a warp per (row block, key share)
     const bf16 *q_ = static_cast<const bf16*>(q), *kb_ = static_cast<const bf16*>(kb),
                *vb_ = static_cast<const bf16*>(vb), *kc_ = static_cast<const bf16*>(kc),
                *vc_ = static_cast<const bf16*>(vc);

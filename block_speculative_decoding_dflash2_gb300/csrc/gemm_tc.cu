@@ -1109,9 +1109,11 @@ template <int BN, bool FP8>
 int max_clusters_epi(int epi, int cs) {
   switch (epi) {
     case EPI_SWIGLU:
-      return max_clusters<BN, EPI_SWIGLU, FP8>(cs);
+      if constexpr (BN <= 64) return max_clusters<BN, EPI_SWIGLU, FP8>(cs);
+      return 0;
     case EPI_HEADS:
-      return max_clusters<BN, EPI_HEADS, FP8>(cs);
+      if constexpr (BN <= 64) return max_clusters<BN, EPI_HEADS, FP8>(cs);
+      return 0;
     case EPI_PLAIN: return max_clusters<BN, EPI_PLAIN, FP8>(cs);
     default: return 0;
   }
@@ -1151,9 +1153,11 @@ int launch_epi(int epi, const CUtensorMap& ma, const CUtensorMap& mb, const TcAr
   switch (epi) {
     case EPI_TOPK: return launch_bn<BN, EPI_TOPK, FP8>(ma, mb, args, grid, c);
     case EPI_SWIGLU:
-      return launch_bn<BN, EPI_SWIGLU, FP8>(ma, mb, args, grid, c);
+      if constexpr (BN <= 64) return launch_bn<BN, EPI_SWIGLU, FP8>(ma, mb, args, grid, c);
+      return DFLASH2_ERR_SHAPE;
     case EPI_HEADS:
-      return launch_bn<BN, EPI_HEADS, FP8>(ma, mb, args, grid, c);
+      if constexpr (BN <= 64) return launch_bn<BN, EPI_HEADS, FP8>(ma, mb, args, grid, c);
+      return DFLASH2_ERR_SHAPE;
     default: return launch_bn<BN, EPI_PLAIN, FP8>(ma, mb, args, grid, c);
   }
 }
@@ -1167,7 +1171,10 @@ int launch_epi(int epi, bool fp8, const CUtensorMap& ma, const CUtensorMap& mb, 
 }  // namespace
 
 bool gemm_fusable(int M, int N, int epi) {
-  (void)N;
+  // wider activation tiles run the plain epilogue and a row kernel: their
+  // fused epilogues (16 columns per step, each step's norm/RoPE loads and
+  // barriers in series) measured slower than the two kernels at 128 and 256
+  if (pick_bn(M, N) > 64) return false;
   return epi != kEpiSwiglu || M % BM == 0;
 }
 

@@ -42,7 +42,8 @@ struct GemmOp {
   unsigned long long* thr;  // [N][kTopkSlots] bound slots shared by the CTAs, zero at launch
   float* debug;  // nullable [N][M] logits after the transform
   float mult, cap;
-  // fused epilogues (bf16 path; see gemm_fusable): 0 = plain fp32 out; kEpiSwiglu = gate/up rows [0, M/2) and
+  // fused epilogues (bf16 path, activation tiles of at most 64 rows; see
+  // gemm_fusable): 0 = plain fp32 out; kEpiSwiglu = gate/up rows [0, M/2) and
   // [M/2, M) -> act [N][M/2] bf16 = SiLU(gate) * up; kEpiHeads = per-head
   // RMSNorm + RoPE of q/k heads and copy of v heads, to q/kb/vb (block rows)
   // or to the paged cache (appended rows).
@@ -61,8 +62,8 @@ struct GemmOp {
 constexpr int kEpiSwiglu = 2, kEpiHeads = 3;
 constexpr int kTopkSlots = 16;  // shared top-k bound slots per lm_head row
 
-// Whether an M x N contraction can take a fused epilogue (the gate/up
-// pairing needs M % 128 == 0).
+// Whether an M x N contraction can take a fused epilogue (activation tiles of
+// at most 64 rows; the gate/up pairing also needs M % 128 == 0).
 bool gemm_fusable(int M, int N, int epi);
 
 // Bytes of stream-K partial pieces an M x N contraction can need (any SM count).

@@ -41,7 +41,9 @@ def check_ulps(name, gpu, ref, max_ulp, frac_over_1=0.01, slack=None):
     if slack is not None:
         ulp_ref = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 7)
         bad &= np.abs(gpu - ref) > slack + ulp_ref
-    print(f"[stage] {name:8s} max {u.max():.2f} ulp, >1ulp {over:.2e}, beyond bound {int(bad.sum())}, n={u.size}")
+    w = int(np.argmax(u))
+    print(f"[stage] {name:8s} max {u.max():.2f} ulp (at |ref| {abs(ref.flat[w]):.3e}, |diff| "
+          f"{abs(gpu.flat[w] - ref.flat[w]):.3e}), >1ulp {over:.2e}, beyond bound {int(bad.sum())}, n={u.size}")
     assert not bad.any(), (name, float(u.max()))
     assert over <= frac_over_1, (name, over)
 
@@ -119,6 +121,7 @@ def run_stagewise(case):
     ua = R.get("ua", (rows, H))
     u2a = R.get("u2a", (rows, H)) if kc else ua
     q_ref, k_ref, v_ref, O_ref, h_mid, ua_ref, u2a_ref = [], [], [], [], [], [], []
+    O_slack = []
     for s in range(b):
         P = int(case.ctx_lens[s] + case.n_new[s])
         sl = slice(s * B_, (s + 1) * B_)
@@ -136,13 +139,20 @@ def run_stagewise(case):
         v_ref.append(st(qkv[:, (nq + nkv) * d:].reshape(B_, nkv, d)))
         Kc, Vc = cache_rows(case, 0, s, np.arange(max(0, P - win) if win else 0, P))
         O_ref.append(st(O.block_attention(q[sl], Kc, Vc, kb[sl], vb[sl])).reshape(B_, nq * d))
+        # fp32 (tensor-core) accumulation of the P.V sums over the L keys read:
+        # a random-walk bound, 32 * 2^-24 * sqrt(L) * sum_j p_j |v_j|, the
+        # magnitude sum being the same attention over |V|.  Outputs that are a
+        # small remainder of large terms carry this absolute error.
+        L = Kc.shape[0] + B_
+        O_abs = O.block_attention(q[sl], Kc, np.abs(Vc), kb[sl], np.abs(vb[sl])).reshape(B_, nq * d)
+        O_slack.append(32.0 * 2.0 ** -24 * np.sqrt(L) * O_abs)
         h_mid.append(h0 + Og[sl] @ Wl["o"].astype(np.float64).T)
     check_ulps("u_attn", ua, np.concatenate(ua_ref), 2)
     check_ulps("u2_attn", u2a, np.concatenate(u2a_ref), 2)
     check_ulps("q", q, np.concatenate(q_ref), 2)
     check_ulps("k_blk", kb, np.concatenate(k_ref), 2)
     check_ulps("v_blk", vb, np.concatenate(v_ref), 2)
-    check_ulps("attn_O", Og, np.concatenate(O_ref), 2)
+    check_ulps("attn_O", Og, np.concatenate(O_ref), 2, slack=np.concatenate(O_slack))
     h_mid = np.concatenate(h_mid)
     check_ulps("u_mlp", u_m, st(O.rms_norm(h_mid, Wl["mlp_norm"], eps)), 2)
     u2_ref = np.concatenate([st(u_m[s * B_:(s + 1) * B_] + O.dynamic_conv(

@@ -219,7 +219,7 @@ def whole_job_rate(steps, world, max_total_ms):
 
 # ---------------------------------------------------------------- our arm
 
-LM_PROFILE = os.path.join(ROOT, "profiles", "lm_head_topk_qwen3_8b_b1.txt")
+LM_PROFILE = os.path.join(ROOT, "profiles", "lm_head_topk_qwen3_8b_b1.md")
 LM_SOURCES = [os.path.join(ROOT, "block_speculative_decoding_dflash2_gb300", "csrc", f)
               for f in ("gemm_tc.cu", "common.cuh")]
 

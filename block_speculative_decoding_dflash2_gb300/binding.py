@@ -13,6 +13,7 @@ import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libdflash2.so")
+TEST_LIB_PATH = os.path.join(_PKG, "libdflash2_testing.so")
 
 F32 = 0
 BF16 = 1
@@ -68,6 +69,38 @@ class Weights(ctypes.Structure):
 
 
 _lib = None
+_tlib = None
+
+
+def testing_lib():
+    """The test-hook library (include/dflash2_testing.h), loaded after the
+    product library it links against."""
+    global _tlib
+    if _tlib is None:
+        lib()
+        if not os.path.exists(TEST_LIB_PATH):
+            raise ImportError(f"{TEST_LIB_PATH} is missing: build it with __graft_entry__.build()")
+        T = ctypes.CDLL(TEST_LIB_PATH)
+        P, I, S, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.POINTER
+        T.dflash2_test_last_schedule.restype = I
+        T.dflash2_test_last_schedule.argtypes = []
+        T.dflash2_test_gemm_workspace.restype = S
+        T.dflash2_test_gemm_workspace.argtypes = [I, I]
+        T.dflash2_test_gemm.restype = I
+        T.dflash2_test_gemm.argtypes = [I, P, I, I, P, I, I, I, P, P, S, P]
+        T.dflash2_test_gemm_fp8.restype = I
+        T.dflash2_test_force_cluster_split.restype = I
+        T.dflash2_test_force_cluster_split.argtypes = [I]
+        T.dflash2_test_gemm_fp8.argtypes = [P, P, I, I, P, I, I, I, P, P, S, P]
+        T.dflash2_test_layout.restype = I
+        T.dflash2_test_layout.argtypes = [F(Config), I, I, I, F(ctypes.c_size_t), I]
+        T.dflash2_test_topk_workspace.restype = S
+        T.dflash2_test_topk_workspace.argtypes = [I, I, I]
+        T.dflash2_test_gemm_topk.restype = I
+        T.dflash2_test_gemm_topk.argtypes = [I, P, I, I, P, I, I, ctypes.c_float, ctypes.c_float, P, P, P,
+                                             P, S, P]
+        _tlib = T
+    return _tlib
 
 
 def lib():
@@ -97,16 +130,6 @@ def lib():
         L.dflash2_verify_accept.argtypes = [I, I, P, P, P, P, P, P, P, P, P]
         L.dflash2_read_device_status.restype = I
         L.dflash2_read_device_status.argtypes = [P, S, P]
-        L.dflash2_test_last_schedule.restype = I
-        L.dflash2_test_last_schedule.argtypes = []
-        L.dflash2_test_gemm_workspace.restype = S
-        L.dflash2_test_gemm_workspace.argtypes = [I, I]
-        L.dflash2_test_gemm.restype = I
-        L.dflash2_test_gemm.argtypes = [I, P, I, I, P, I, I, I, P, P, S, P]
-        L.dflash2_test_gemm_fp8.restype = I
-        L.dflash2_test_force_cluster_split.restype = I
-        L.dflash2_test_force_cluster_split.argtypes = [I]
-        L.dflash2_test_gemm_fp8.argtypes = [P, P, I, I, P, I, I, I, P, P, S, P]
         L.dflash2_select_path_static.restype = I
         L.dflash2_select_path_static.argtypes = [F(Config), F(Weights), I, P, P, P, P, P, P]
         L.dflash2_select_path_static_capacity.restype = S
@@ -128,16 +151,9 @@ def lib():
         L.dflash2_verify_sampled.argtypes = [I, I, I, P, P, P, P, P, P, P, P, P, P, P, P]
         L.dflash2_verify_accept_ex.restype = I
         L.dflash2_verify_accept_ex.argtypes = [I, I, P, P, P, P, P, P, P, P, P, P]
-        L.dflash2_test_layout.restype = I
-        L.dflash2_test_layout.argtypes = [F(Config), I, I, I, F(ctypes.c_size_t), I]
         L.dflash2_launch_count.restype = ctypes.c_int64
         L.dflash2_set_stage_events.restype = None
         L.dflash2_set_stage_events.argtypes = [P]
-        L.dflash2_test_topk_workspace.restype = S
-        L.dflash2_test_topk_workspace.argtypes = [I, I, I]
-        L.dflash2_test_gemm_topk.restype = I
-        L.dflash2_test_gemm_topk.argtypes = [I, P, I, I, P, I, I, ctypes.c_float, ctypes.c_float, P, P, P,
-                                             P, S, P]
         _lib = L
     return _lib
 
@@ -323,7 +339,7 @@ def dflash2_read_device_status(workspace, stream=None):
 # path on their own, for parity tests)
 
 def dflash2_test_gemm_workspace(M, N):
-    return lib().dflash2_test_gemm_workspace(M, N)
+    return testing_lib().dflash2_test_gemm_workspace(M, N)
 
 
 def dflash2_test_gemm(dtype, W, X, ctas, out, workspace, accumulate=False, stream=None):
@@ -332,7 +348,7 @@ def dflash2_test_gemm(dtype, W, X, ctas, out, workspace, accumulate=False, strea
     Returns the CTA count launched."""
     M, K = W.shape
     N = X.shape[0]
-    rc = lib().dflash2_test_gemm(dtype, _ptr(W), M, K, _ptr(X), N, ctas, int(accumulate), _ptr(out),
+    rc = testing_lib().dflash2_test_gemm(dtype, _ptr(W), M, K, _ptr(X), N, ctas, int(accumulate), _ptr(out),
                                  _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     if rc < 0:
         _check("dflash2_test_gemm", rc)
@@ -342,14 +358,14 @@ def dflash2_test_gemm(dtype, W, X, ctas, out, workspace, accumulate=False, strea
 def dflash2_test_force_cluster_split(cs):
     """Force cluster split-K of cs slices on the library's own contractions
     (0 = its own schedule)."""
-    _check("dflash2_test_force_cluster_split", lib().dflash2_test_force_cluster_split(int(cs)))
+    _check("dflash2_test_force_cluster_split", testing_lib().dflash2_test_force_cluster_split(int(cs)))
 
 
 def dflash2_test_gemm_fp8(W8, scale, X, ctas, out, workspace, accumulate=False, stream=None):
     """W8: uint8 e4m3 codes [M, K]; scale: float32 [M]; X: bf16 [N, K]."""
     M, K = W8.shape
     N = X.shape[0]
-    rc = lib().dflash2_test_gemm_fp8(_ptr(W8), _ptr(scale), M, K, _ptr(X), N, ctas, int(accumulate), _ptr(out),
+    rc = testing_lib().dflash2_test_gemm_fp8(_ptr(W8), _ptr(scale), M, K, _ptr(X), N, ctas, int(accumulate), _ptr(out),
                                      _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     if rc < 0:
         _check("dflash2_test_gemm_fp8", rc)
@@ -357,13 +373,13 @@ def dflash2_test_gemm_fp8(W8, scale, X, ctas, out, workspace, accumulate=False, 
 
 
 def dflash2_test_topk_workspace(dtype, M, N):
-    return lib().dflash2_test_topk_workspace(dtype, M, N)
+    return testing_lib().dflash2_test_topk_workspace(dtype, M, N)
 
 
 def dflash2_test_gemm_topk(dtype, W, X, k, mult, cap, cand_id, cand_logit, debug, workspace, stream=None):
     M, K = W.shape
     N = X.shape[0]
-    return _check("dflash2_test_gemm_topk", lib().dflash2_test_gemm_topk(
+    return _check("dflash2_test_gemm_topk", testing_lib().dflash2_test_gemm_topk(
         dtype, _ptr(W), M, K, _ptr(X), N, k, mult, cap, _ptr(cand_id), _ptr(cand_logit), _ptr(debug),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
@@ -371,7 +387,7 @@ def dflash2_test_gemm_topk(dtype, W, X, k, mult, cap, cand_id, cand_logit, debug
 def dflash2_test_layout(cfg, batch, n_new, max_ctx):
     """Workspace byte offsets of {f, h, u, u2, q, kb, vb, O, act, hn, ua, u2a, cnt, cnta}."""
     out = (ctypes.c_size_t * 14)()
-    _check("dflash2_test_layout", lib().dflash2_test_layout(ctypes.byref(cfg), batch, n_new, max_ctx, out, 14))
+    _check("dflash2_test_layout", testing_lib().dflash2_test_layout(ctypes.byref(cfg), batch, n_new, max_ctx, out, 14))
     return dict(zip(("f", "h", "u", "u2", "q", "kb", "vb", "O", "act", "hn", "ua", "u2a", "cnt", "cnta"),
                     list(out)))
 
@@ -381,7 +397,7 @@ SCHED_FUSED_PROLOGUE, SCHED_SPLIT_SMS, SCHED_FUSED_QKV, SCHED_KV_BESIDE_QKV, SCH
 
 def dflash2_test_last_schedule():
     """Schedule bits (SCHED_*) of the last draft step in this process."""
-    return lib().dflash2_test_last_schedule()
+    return testing_lib().dflash2_test_last_schedule()
 
 
 def dflash2_launch_count():

@@ -1,7 +1,8 @@
-"""Builds libdflash2.so in-tree with nvcc for sm_103a.
+"""Builds libdflash2.so (and the test-hook library libdflash2_testing.so,
+linked against it) in-tree with nvcc for sm_103a.
 
 The translation units compile in parallel into ``_build/`` next to this file
-and link into ``libdflash2.so`` beside it.  A unit is rebuilt when it or any
+and link into the two libraries beside it.  A unit is rebuilt when it or any
 header is newer than its object.
 """
 
@@ -17,7 +18,11 @@ OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdflash2.so")
 
 SOURCES = ["api.cu", "gemm_tc.cu", "gemm_simt.cu", "elementwise.cu", "attention.cu",
-           "topk.cu", "selector.cu", "verify.cu", "testing.cu", "select_static.cu"]
+           "topk.cu", "selector.cu", "verify.cu", "select_static.cu"]
+# the test hooks (include/dflash2_testing.h) live in a library of their own,
+# linked against libdflash2.so, so the product library exports only dflash2.h
+TEST_SOURCES = ["testing.cu"]
+TEST_LIB = os.path.join(PKG, "libdflash2_testing.so")
 HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "internal.h"),
            os.path.join(ROOT, "include", "dflash2.h"), os.path.join(ROOT, "include", "dflash2_testing.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -57,22 +62,31 @@ def _compile(src, verbose):
     return obj, True
 
 
-def build(verbose=False, jobs=None):
-    """Compile and link; returns the path of libdflash2.so."""
-    os.makedirs(OBJ, exist_ok=True)
-    srcs = [os.path.join(CSRC, s) for s in SOURCES]
-    jobs = jobs or min(len(srcs), max(2, os.cpu_count() or 2))
-    with concurrent.futures.ThreadPoolExecutor(jobs) as ex:
-        results = list(ex.map(lambda s: _compile(s, verbose), srcs))
-    objs = [o for o, _ in results]
-    rebuilt = any(b for _, b in results)
-    if rebuilt or not os.path.exists(LIB) or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
-        tmp = LIB + ".tmp"
-        cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs
+def _link(lib, objs, rebuilt, extra=()):
+    if rebuilt or not os.path.exists(lib) or any(os.path.getmtime(o) > os.path.getmtime(lib) for o in objs):
+        tmp = lib + ".tmp"
+        cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs + list(extra)
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
+        os.replace(tmp, lib)
+
+
+def build(verbose=False, jobs=None):
+    """Compile and link libdflash2.so and the test-hook library beside it;
+    returns the path of libdflash2.so."""
+    os.makedirs(OBJ, exist_ok=True)
+    srcs = [os.path.join(CSRC, s) for s in SOURCES + TEST_SOURCES]
+    jobs = jobs or min(len(srcs), max(2, os.cpu_count() or 2))
+    with concurrent.futures.ThreadPoolExecutor(jobs) as ex:
+        results = list(ex.map(lambda s: _compile(s, verbose), srcs))
+    n = len(SOURCES)
+    objs = [o for o, _ in results[:n]]
+    _link(LIB, objs, any(b for _, b in results[:n]))
+    tobjs = [o for o, _ in results[n:]]
+    _link(TEST_LIB, tobjs, any(b for _, b in results[n:]) or os.path.getmtime(LIB) > os.path.getmtime(TEST_LIB)
+          if os.path.exists(TEST_LIB) else True,
+          ["-L" + PKG, "-ldflash2", "-Xlinker", "-rpath=$ORIGIN"])
     return LIB
 
 

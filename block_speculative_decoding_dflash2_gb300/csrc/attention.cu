@@ -14,6 +14,7 @@
 // chunks.  No CTA waits on another.  Keys are gathered row by row (one page
 // lookup per key, then 16-byte loads of its d contiguous elements).
 #include <algorithm>
+#include <cstring>
 
 #include "common.cuh"
 #include "internal.h"
@@ -269,8 +270,8 @@ template <int DH>
 size_t attn_cl_smem(int R, int npg, int mkt, int kst) {
   const int nrb = (R + 15) / 16;
   const size_t qb = (size_t)nrb * 16 * (DH + 8) * 2;
-  return qb + attn_kv_bytes<DH>(R, mkt, kst) + (size_t)(R + kMaxCluster) * kMaxShares * 2 * 4 + (size_t)npg * 4 +
-         8 + kMaxStages * sizeof(uint64_t);
+  return qb + 128 /* K/V ring alignment */ + attn_kv_bytes<DH>(R, mkt, kst) +
+         (size_t)(R + kMaxCluster) * kMaxShares * 2 * 4 + (size_t)npg * 4 + 8 + kMaxStages * sizeof(uint64_t);
 }
 
 template <int DH>
@@ -278,7 +279,8 @@ __global__ void __launch_bounds__(CLT, 1) attn_cluster_kernel(
     const bf16* __restrict__ q, const bf16* __restrict__ kb, const bf16* __restrict__ vb, const bf16* __restrict__ kc,
     const bf16* __restrict__ vc, const int32_t* __restrict__ block_table, int max_pages, int page_size, int n_pages,
     const int32_t* __restrict__ ctx_len, const int32_t* __restrict__ new_off, int B, int nq, int nkv, int npg,
-    int window, int MKT, int KST, bf16* __restrict__ o, unsigned* status) {
+    int window, int MKT, int KST, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+    int page_tma, bf16* __restrict__ o, unsigned* status) {
   // MKT keys per K/V tile, KST tile stages (KST - 1 tiles in flight while one
   // is consumed)
   constexpr int MCPW = 1;  // (row block, key share) combinations per warp
@@ -295,7 +297,8 @@ __global__ void __launch_bounds__(CLT, 1) attn_cluster_kernel(
   const int ksplit = attn_ksplit(nrb, MKT);
   const int ncombo = nrb * ksplit;
   bf16* Qs = reinterpret_cast<bf16*>(smraw);
-  bf16* KV = Qs + nrb * 16 * LD;                        // [KST][K, V][MKT][LD]
+  // [KST][K, V][MKT][LD], 128-byte aligned: a page of rows is one TMA box
+  bf16* KV = reinterpret_cast<bf16*>((reinterpret_cast<uintptr_t>(Qs + nrb * 16 * LD) + 127) & ~uintptr_t(127));
   float* comb = reinterpret_cast<float*>(KV);            // [ncombo][16][FS], after the key loop
   float* wts = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(KV) + attn_kv_bytes<DH>(R, MKT, KST));  // merge weights
   int* pg = reinterpret_cast<int*>(wts + (size_t)(R + kMaxCluster) * kMaxShares * 2);  // page ids of the chunk
@@ -334,16 +337,50 @@ __global__ void __launch_bounds__(CLT, 1) attn_cluster_kernel(
     if (r < R) src = q + (((size_t)s * B + r / grp) * nq + g * grp + r % grp) * DH + c;
     cp_async16(Qs + r * LD + c, src, r < R);
   }
-  // K/V rows of keys t0 .. t0 + MKT - 1 into stage stg: thread kk copies the
-  // K row of key kk, thread MKT + kk its V row, each one 16-byte-aligned bulk
-  // copy of DH elements, and arrives on the stage barrier with its byte
-  // count.  Keys past k1, and keys whose page is invalid (flagged), are
-  // written as zeros instead.
+  // K/V rows of keys t0 .. t0 + MKT - 1 into stage stg.  With page_tma (16-key
+  // pages and a page-aligned chunk start), each whole context page of the
+  // tile is one TMA box per K and V (16 rows of DH + 8 elements from the
+  // cache viewed as [pages * 16][nkv * DH]: the row's DH values of this kv
+  // head plus 8 ignored ones, which lands them at the padded row pitch);
+  // threads 0 .. 2p-1 issue those.  The other rows (the tile's last partial
+  // context page, the block's own keys, keys past k1) are copied one row per
+  // thread, one 16-byte-aligned bulk copy of DH elements each.  Each of the
+  // first 2*MKT threads arrives once per tile on the stage barrier with the
+  // bytes it issued (0 when it has none); keys past k1, and rows of an
+  // invalid page (flagged), are written as zeros instead.
+  const bool tma_ok = page_tma && (k0 % 16) == 0;
   auto issue = [&](int t0, int stg) {
     if (threadIdx.x >= 2 * MKT) return;
-    const bool is_v = threadIdx.x >= MKT;
-    const int kk = threadIdx.x - (is_v ? MKT : 0);
-    bf16* dst = KV + (size_t)stg * 2 * MKT * LD + (is_v ? MKT * LD : 0) + (size_t)kk * LD;
+    bf16* sbase = KV + (size_t)stg * 2 * MKT * LD;
+    const int cend = min(min(t0 + MKT, k1), P);  // context keys of this tile end here
+    const int nfull = tma_ok ? max(0, (cend - t0) / 16) : 0;  // whole pages by TMA
+    const int nrow = MKT - 16 * nfull;                         // rows copied one by one
+    const int tid = threadIdx.x;
+    if (tid < 2 * nfull) {
+      const bool is_v = tid >= nfull;
+      const int pi = is_v ? tid - nfull : tid;
+      bf16* dst = sbase + (is_v ? MKT * LD : 0) + (size_t)pi * 16 * LD;
+      const int li = (t0 + pi * 16) / 16 - pbase;
+      const int page = li < npg ? pg[li] : -1;
+      if (page >= 0 && page < n_pages) {
+        mbar_arrive_expect_tx(kvbar + stg, 16 * LD * 2);
+        fence_proxy_async_smem();
+        tma_load_2d(dst, is_v ? &tmV : &tmK, kvbar + stg, g * DH, page * 16, policy_evict_first());
+      } else {
+        if (!is_v) flag(status, DFLASH2_DEV_BAD_PAGE);
+        mbar_arrive_expect_tx(kvbar + stg, 0);
+        for (int c = 0; c < 16 * LD / 8; ++c) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0, 0, 0, 0);
+      }
+      return;
+    }
+    const int tr = tid - 2 * nfull;
+    if (tr >= 2 * nrow) {  // nothing left for this thread this tile
+      mbar_arrive_expect_tx(kvbar + stg, 0);
+      return;
+    }
+    const bool is_v = tr >= nrow;
+    const int kk = 16 * nfull + (is_v ? tr - nrow : tr);
+    bf16* dst = sbase + (is_v ? MKT * LD : 0) + (size_t)kk * LD;
     const int j = t0 + kk;
     const bf16* src = nullptr;
     if (j < k1) {
@@ -715,9 +752,18 @@ int launch_cluster(int R, int max_ctx, int page_size, int batch, int nkv, const 
     if (smem <= kAttnSmem) break;
   }
   if (smem > kAttnSmem) return DFLASH2_ERR_SHAPE;
+  // whole 16-key pages of the cache by TMA: the cache viewed as
+  // [n_pages * 16 rows][nkv * DH], a box of 16 rows x (DH + 8) elements
+  CUtensorMap tmK, tmV;
+  std::memset(&tmK, 0, sizeof(tmK));
+  std::memset(&tmV, 0, sizeof(tmV));
+  int page_tma = page_size == 16 && (long long)n_pages * 16 < (1LL << 31);
+  if (page_tma)
+    page_tma = make_rows_map(&tmK, kc, (long long)n_pages * 16, nkv * DH, (long long)nkv * DH, DH + 8, 16) == 0 &&
+               make_rows_map(&tmV, vc, (long long)n_pages * 16, nkv * DH, (long long)nkv * DH, DH + 8, 16) == 0;
   return launch_kx(attn_cluster_kernel<DH>, dim3(ns, nkv, batch), dim3(CLT), smem, c, ns, q, kb, vb, kc, vc,
-                   block_table, max_pages, page_size, n_pages, ctx_len, new_off, B, nq, nkv, npg, window, mkt, kst, o,
-                   c.status);
+                   block_table, max_pages, page_size, n_pages, ctx_len, new_off, B, nq, nkv, npg, window, mkt, kst, tmK,
+                   tmV, page_tma, o, c.status);
 }
 
 }  // namespace

@@ -138,7 +138,7 @@ struct TcCfg {
   // warp set (wide tiles), the lists, the per-column thresholds, queue counts
   static constexpr int TOPK_SETS = epi_warps(EPI_TOPK, BN) / 4;
   static constexpr int TOPK_EXTRA = (BN > 16 ? TOPK_SETS * 16 * BM * 8 : 16 * BM * 4) + BN * KMAX * 8 + BN * 8 +
-                                    TOPK_SETS * 16 * 4;
+                                    TOPK_SETS * 16 * 4 + TOPK_SETS * 4 * 16 * 4;
   static constexpr int FUSE_EXTRA = 16 * BM * 4 + 4 * 16 * 4;  // exchange tile, column sums
   static constexpr int FIXED = 1024 /* alignment slack */ + 1024 /* barriers */;
   __host__ __device__ static constexpr int extra(int epi) {
@@ -266,6 +266,7 @@ __global__ void __launch_bounds__(threads_of(EPI, BN, FP8), 1)
       reinterpret_cast<unsigned long long*>(reinterpret_cast<uint8_t*>(stg) + (BN > 16 ? SETS * 16 * BM * 8 : 16 * BM * 4));
   unsigned long long* thr_s = lk_s + BN * KMAX;
   int* qn_s = reinterpret_cast<int*>(thr_s + BN);
+  float* tau_s = reinterpret_cast<float*>(qn_s + SETS * 16);  // [SETS][4 warps][16] first-tile bounds
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_launch_next();
@@ -801,6 +802,7 @@ __global__ void __launch_bounds__(threads_of(EPI, BN, FP8), 1)
         // the column's top KMAX.  The slots start at zero (no bound).
         const int ewq = ew & 3;                 // warp within its set
         const int set = SETS > 1 ? ew >> 2 : 0;  // which chunks its set takes
+        const bool fresh = nt != cur_nt;        // the lists start empty at this tile
         if (nt != cur_nt) {
           named_sync_epi<EPT>();
           if (cur_nt >= 0) flush_lists(cur_nt, false);
@@ -924,13 +926,39 @@ __global__ void __launch_bounds__(threads_of(EPI, BN, FP8), 1)
               for (int j = 0; j < 16; ++j)
                 if (j < nj) a.debug[(size_t)(nt * BN + c0 + j) * a.M + m] = v[j];
             }
+            // First tile (empty lists): a lower bound of each column's 16th
+            // largest value in this tile, the smallest of its 16 group
+            // maxima (8 consecutive rows each: every group maximum is a
+            // distinct row at least that large).  Only values at least this
+            // bound can be in the tile's top 16, so the rest are not queued.
+            float tau[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) tau[j] = -INFINITY;
+            if (fresh) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                float x = m < a.M ? v[j] : -INFINITY;
+                x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
+                x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
+                x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 4));
+                x = fminf(x, __shfl_xor_sync(0xffffffffu, x, 8));
+                x = fminf(x, __shfl_xor_sync(0xffffffffu, x, 16));
+                if (lane == 0) tau_s[(set * 4 + ewq) * 16 + j] = x;
+              }
+              named_sync_set(set);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float* tw = tau_s + set * 64 + j;
+                tau[j] = fminf(fminf(tw[0], tw[16]), fminf(tw[32], tw[48]));
+              }
+            }
             if (m < a.M) {
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 unsigned u = __float_as_uint(v[j] + 0.f);
                 u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
                 const unsigned long long key = ((unsigned long long)u << 32) | idk;
-                if (j < nj && key > thr_s[c0 + j]) qset[j * BM + atomicAdd(qn + j, 1)] = key;
+                if (j < nj && v[j] >= tau[j] && key > thr_s[c0 + j]) qset[j * BM + atomicAdd(qn + j, 1)] = key;
               }
             }
             named_sync_set(set);
@@ -1169,6 +1197,21 @@ int launch_epi(int epi, bool fp8, const CUtensorMap& ma, const CUtensorMap& mb, 
 }
 
 }  // namespace
+
+int make_rows_map(CUtensorMap* map, const void* base, long long rows, int cols, long long ld_elems, int box_cols,
+                  int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return DFLASH2_ERR_CUDA;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || (ld_elems * 2) % 16 || (box_cols * 2) % 16) return DFLASH2_ERR_SHAPE;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld_elems * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+}
 
 bool gemm_fusable(int M, int N, int epi) {
   // wider activation tiles run the plain epilogue and a row kernel: their

@@ -1,6 +1,7 @@
 // Host-side interfaces between the C ABI layer and the kernel launchers.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -142,6 +143,11 @@ inline int launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, 
 int workspace_offsets(const dflash2_config* c, int batch, int n_new, int max_ctx, size_t* out, int n);
 
 int gemm_bf16(const GemmOp& g, const Ctx& c);  // tcgen05 + TMA (sm_103a)
+// 2-D bf16 tensor map over rows x cols (row stride ld_elems elements), box of
+// box_cols x box_rows, no swizzle, zero fill past the edges (the attention's
+// page loads); DFLASH2_ERR_SHAPE for unaligned bases or strides.
+int make_rows_map(CUtensorMap* map, const void* base, long long rows, int cols, long long ld_elems, int box_cols,
+                  int box_rows);
 // Schedule bits of the last dflash2_draft_step call (test hook)
 enum {
   kSchedFusedPrologue = 1,  // sublayer prologue fused (norm + tap logits + conv)

@@ -30,12 +30,18 @@ def declared(header):
 
 
 def test_every_declared_symbol_is_exported(B):
-    names = declared("dflash2.h") + declared("dflash2_testing.h")
+    names = declared("dflash2.h")
     assert "dflash2_draft_step" in names and "dflash2_select_path" in names
     assert "dflash2_verify_accept" in names
     lib = ctypes.CDLL(B.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
+    # the test hooks come from their own library, not the product one
+    hooks = declared("dflash2_testing.h")
+    tlib = ctypes.CDLL(B.TEST_LIB_PATH)
+    for n in hooks:
+        assert hasattr(tlib, n), n
+        assert not hasattr(lib, n), n
 
 
 def test_struct_sizes_match_header(B):
@@ -151,7 +157,8 @@ def test_sampled_verify_and_cluster_switch_host_checks(B):
     assert L.dflash2_verify_sampled(1, 8, 1_536_001, *args) == -2  # segment sums exceed shared memory
     assert L.dflash2_verify_sampled(1, 8, 1000, None, *args[1:]) == -1
     # the test switch of cluster split-K: 0 or 2..8 slices, nothing else
+    T = B.testing_lib()
     for cs in (1, 9, -2):
-        assert L.dflash2_test_force_cluster_split(cs) == -1
+        assert T.dflash2_test_force_cluster_split(cs) == -1
     for cs in (2, 8, 0):
-        assert L.dflash2_test_force_cluster_split(cs) == 0
+        assert T.dflash2_test_force_cluster_split(cs) == 0

@@ -246,31 +246,32 @@ constexpr int CLT = 32 * CLW;    // threads
 constexpr int kMaxShares = 8;    // key shares per 16-row block (16 keys each per tile)
 constexpr size_t kAttnSmem = 227 * 1024;
 
-// Key shares per 16-row block: a power of two, so each share of an mkt-key
-// tile is a whole number of 16-key steps, and enough (row block, share)
-// combinations to give most warps one (at most CLW combinations for 16 row
-// blocks or fewer).
-__host__ __device__ inline int attn_ksplit(int nrb, int mkt) {
-  int k = 1;
-  while (k < kMaxShares && nrb * 2 * k <= CLW && mkt / (2 * k) >= 16) k *= 2;
-  return k;
+// Key shares per 16-row block: enough (row block, share) combinations to
+// give nearly every warp one (at most CLW combinations, at most kMaxShares
+// shares).  The tile takes mkt = shares x 16 x steps keys, steps the fewest
+// 16-key steps per share that make the tile at least 64 keys, so every share
+// is a whole number of steps.
+inline int attn_ksplit(int nrb) { return std::max(1, std::min(kMaxShares, CLW / nrb)); }
+inline int attn_tile_keys(int ksplit) {
+  const int unit = 16 * ksplit;
+  return unit * ((64 + unit - 1) / unit);
 }
 
 // Shared memory: Q rows; the kst K/V stages of mkt keys, which after the key
 // loop hold the per-combination partial states (read by the whole cluster);
 // the merge weights of this CTA's rows; the page ids of its key chunk (npg).
 template <int DH>
-__host__ __device__ inline size_t attn_kv_bytes(int R, int mkt, int kst) {
+__host__ __device__ inline size_t attn_kv_bytes(int R, int mkt, int kst, int ksplit) {
   const int nrb = (R + 15) / 16;
   const size_t kvb = (size_t)kst * 2 * mkt * (DH + 8) * 2;
-  const size_t comb = (size_t)nrb * attn_ksplit(nrb, mkt) * 16 * (DH + 2) * 4;
+  const size_t comb = (size_t)nrb * ksplit * 16 * (DH + 2) * 4;
   return kvb > comb ? kvb : comb;
 }
 template <int DH>
-size_t attn_cl_smem(int R, int npg, int mkt, int kst) {
+size_t attn_cl_smem(int R, int npg, int mkt, int kst, int ksplit) {
   const int nrb = (R + 15) / 16;
   const size_t qb = (size_t)nrb * 16 * (DH + 8) * 2;
-  return qb + 128 /* K/V ring alignment */ + attn_kv_bytes<DH>(R, mkt, kst) +
+  return qb + 128 /* K/V ring alignment */ + attn_kv_bytes<DH>(R, mkt, kst, ksplit) +
          (size_t)(R + kMaxCluster) * kMaxShares * 2 * 4 + (size_t)npg * 4 + 8 + kMaxStages * sizeof(uint64_t);
 }
 
@@ -279,10 +280,10 @@ __global__ void __launch_bounds__(CLT, 1) attn_cluster_kernel(
     const bf16* __restrict__ q, const bf16* __restrict__ kb, const bf16* __restrict__ vb, const bf16* __restrict__ kc,
     const bf16* __restrict__ vc, const int32_t* __restrict__ block_table, int max_pages, int page_size, int n_pages,
     const int32_t* __restrict__ ctx_len, const int32_t* __restrict__ new_off, int B, int nq, int nkv, int npg,
-    int window, int MKT, int KST, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-    int page_tma, bf16* __restrict__ o, unsigned* status) {
+    int window, int MKT, int KST, int ksplit, const __grid_constant__ CUtensorMap tmK,
+    const __grid_constant__ CUtensorMap tmV, int page_tma, bf16* __restrict__ o, unsigned* status) {
   // MKT keys per K/V tile, KST tile stages (KST - 1 tiles in flight while one
-  // is consumed)
+  // is consumed), ksplit key shares of MKT / ksplit keys per 16-row block
   constexpr int MCPW = 1;  // (row block, key share) combinations per warp
   constexpr int LD = DH + 8;  // padded smem row (elements): ldmatrix rows hit distinct banks
   constexpr int NT = DH / 8;  // n8 tiles across the head dimension
@@ -294,13 +295,12 @@ __global__ void __launch_bounds__(CLT, 1) attn_cluster_kernel(
   const int sp = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
   const int grp = nq / nkv, R = grp * B;
   const int nrb = (R + 15) / 16;
-  const int ksplit = attn_ksplit(nrb, MKT);
   const int ncombo = nrb * ksplit;
   bf16* Qs = reinterpret_cast<bf16*>(smraw);
   // [KST][K, V][MKT][LD], 128-byte aligned: a page of rows is one TMA box
   bf16* KV = reinterpret_cast<bf16*>((reinterpret_cast<uintptr_t>(Qs + nrb * 16 * LD) + 127) & ~uintptr_t(127));
   float* comb = reinterpret_cast<float*>(KV);            // [ncombo][16][FS], after the key loop
-  float* wts = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(KV) + attn_kv_bytes<DH>(R, MKT, KST));  // merge weights
+  float* wts = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(KV) + attn_kv_bytes<DH>(R, MKT, KST, ksplit));  // merge weights
   int* pg = reinterpret_cast<int*>(wts + (size_t)(R + kMaxCluster) * kMaxShares * 2);  // page ids of the chunk
   uint64_t* kvbar = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(pg + npg) + 7) & ~uintptr_t(7));
   if (threadIdx.x == 0) {  // one K/V stage completes when its 2*MKT row copies have landed
@@ -737,20 +737,13 @@ int launch_cluster(int R, int max_ctx, int page_size, int batch, int nkv, const 
   // chunk length bound (keys), then its pages
   const long ch = ((((long)max_ctx + B + ns - 1) / ns) + 15) & ~15L;
   const int npg = (int)((ch + page_size - 1) / page_size + 1);
-  // K/V ring: three stages of 128 keys for up to 32 query rows per kv head
-  // (every share of a tile still a whole 16-key step for 8 shares), four of
-  // 64 keys for more rows (their Q tile and partials take more space);
-  // shallower when the chunk's page list does not leave room
+  // K/V ring: tiles of mkt keys (the share geometry above), as many stages
+  // (up to four) as the shared memory holds beside the Q tile and page list
   const int nrb = (R + 15) / 16;
-  const int geo[4][2] = {{nrb <= 2 ? 128 : 64, nrb <= 2 ? 3 : 4}, {64, 4}, {64, 3}, {64, 2}};
-  int mkt = 0, kst = 0;
-  size_t smem = 0;
-  for (const auto& gk : geo) {
-    mkt = gk[0];
-    kst = gk[1];
-    smem = attn_cl_smem<DH>(R, npg, mkt, kst);
-    if (smem <= kAttnSmem) break;
-  }
+  const int ksplit = attn_ksplit(nrb), mkt = attn_tile_keys(ksplit);
+  int kst = kMaxStages;
+  size_t smem = attn_cl_smem<DH>(R, npg, mkt, kst, ksplit);
+  while (smem > kAttnSmem && kst > 2) smem = attn_cl_smem<DH>(R, npg, mkt, --kst, ksplit);
   if (smem > kAttnSmem) return DFLASH2_ERR_SHAPE;
   // whole 16-key pages of the cache by TMA: the cache viewed as
   // [n_pages * 16 rows][nkv * DH], a box of 16 rows x (DH + 8) elements
@@ -762,8 +755,8 @@ int launch_cluster(int R, int max_ctx, int page_size, int batch, int nkv, const 
     page_tma = make_rows_map(&tmK, kc, (long long)n_pages * 16, nkv * DH, (long long)nkv * DH, DH + 8, 16) == 0 &&
                make_rows_map(&tmV, vc, (long long)n_pages * 16, nkv * DH, (long long)nkv * DH, DH + 8, 16) == 0;
   return launch_kx(attn_cluster_kernel<DH>, dim3(ns, nkv, batch), dim3(CLT), smem, c, ns, q, kb, vb, kc, vc,
-                   block_table, max_pages, page_size, n_pages, ctx_len, new_off, B, nq, nkv, npg, window, mkt, kst, tmK,
-                   tmV, page_tma, o, c.status);
+                   block_table, max_pages, page_size, n_pages, ctx_len, new_off, B, nq, nkv, npg, window, mkt, kst,
+                   ksplit, tmK, tmV, page_tma, o, c.status);
 }
 
 }  // namespace

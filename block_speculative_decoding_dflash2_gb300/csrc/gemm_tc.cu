@@ -1158,10 +1158,18 @@ int max_clusters_of(int bn, int epi, bool fp8, int cs) {
   }
 }
 
-// Cluster split-K size for a contraction, or 1 (stream-K / whole tiles):
+// Cluster split-K size for a contraction, or 1 (stream-K / whole tiles).
+// Activation tiles up to 64 wide stream weights with a short MMA per chunk:
 // the largest cs in 2..8 (at most the K chunks) whose tiles x cs CTAs fill
-// at least three quarters of the SMs without exceeding them, when every
-// tile's cluster fits the device at once.  ctas <= -2 forces cs = -ctas.
+// at least three quarters of the SMs without exceeding them.  At 128 and 256
+// wide, a chunk's MMA is 8-16x longer than at 16 and each slice hands a
+// 64-128 KB fp32 partial through distributed shared memory: the largest cs in 2..4
+// whose tiles x cs CTAs fit the SMs in one wave, however few (measured at
+// 128 and 256 rows: a 16-tile K/V contraction takes 20-24 us in 4 slices,
+// 30-34 us in 8 and 32-33 us as whole tiles; a 48-56-tile QKV contraction
+// 27-28 us in 2 slices against 35-38 us whole and 41-54 us stream-K).
+// Either way every tile's cluster must fit the device at once.  ctas <= -2
+// forces cs = -ctas.
 int pick_csplit(int tiles, int n_chunks, int bn, int epi, bool fp8, int nsm, int ctas) {
   if (epi == EPI_TOPK) return 1;
   if (ctas <= -2) {
@@ -1169,8 +1177,10 @@ int pick_csplit(int tiles, int n_chunks, int bn, int epi, bool fp8, int nsm, int
     return cs <= 8 && cs <= n_chunks && max_clusters_of(bn, epi, fp8, cs) >= 1 ? cs : 1;
   }
   if (ctas != 0) return 1;
-  for (int cs = 8; cs >= 2; --cs) {
-    if (cs > n_chunks || (long)tiles * cs > nsm || (long)tiles * cs * 4 < (long)nsm * 3) continue;
+  const bool narrow = bn <= 64;
+  for (int cs = narrow ? 8 : 4; cs >= 2; --cs) {
+    if (cs > n_chunks || (long)tiles * cs > nsm) continue;
+    if (narrow && (long)tiles * cs * 4 < (long)nsm * 3) continue;
     if (max_clusters_of(bn, epi, fp8, cs) >= tiles) return cs;
   }
   return 1;
@@ -1265,7 +1275,11 @@ int gemm_bf16(const GemmOp& g, const Ctx& c) {
   a.csplit = kClusterSplit && !g.topk ? pick_csplit(a.tiles, a.n_chunks, bn, epi, g.wscale != nullptr, c.nsm,
                                                     fcs >= 2 && g.ctas == 0 ? -fcs : g.ctas)
                                       : 1;
-  if (a.csplit > 1) a.stream = 0;
+  // 128- and 256-wide tiles without a cluster split run whole: the fix-up of
+  // a stream-K piece reads a 64-128 KB fp32 partial serially, which costs
+  // more than the SMs it fills (at 192-272 tiles: 64-72 us whole against
+  // 74-83 us stream-K)
+  if (a.csplit > 1 || (g.ctas == 0 && bn >= 128)) a.stream = 0;
   a.out = g.out;
   a.partial = g.partial;
   a.counters = g.counters;

@@ -8,7 +8,9 @@ Kernels:
             (vocab 151936 x hidden 4096 bf16, 7 block rows, top-16) through
             the dflash2_test_gemm_topk hook, then the top-k merge;
   gate_up   the MLP gate/up contraction (24576 x 4096, 8 rows);
-  fc, qkv, down, o   the other contractions of the 8B-shaped draft step;
+  fc, qkv, kv, down, o   the other contractions of the 8B-shaped draft step;
+  fc27, kv27, qkv27, o27, gate_up27, down27   the 27B-shaped step's contractions
+            at 128 rows (batch 8 x block 16);
   select    the selector on a factor table (vocab 151936, rank 64, 7
             positions x top-16, one sequence) through
             dflash2_select_path_table.
@@ -25,7 +27,11 @@ from . import binding as B
 from .build import build
 
 SHAPES = {"lm_head": (151936, 4096, 7), "gate_up": (24576, 4096, 8), "fc": (4096, 12288, 8),
-          "qkv": (6144, 4096, 8), "down": (4096, 12288, 8), "o": (4096, 4096, 8)}
+          "qkv": (6144, 4096, 8), "down": (4096, 12288, 8), "o": (4096, 4096, 8),
+          "kv": (2048, 4096, 8),
+          # the 27B-shaped draft at batch 8 x block 16 (128 rows)
+          "fc27": (5120, 15360, 128), "kv27": (2048, 5120, 128), "qkv27": (7168, 5120, 128),
+          "gate_up27": (34816, 5120, 128), "down27": (5120, 17408, 128), "o27": (5120, 5120, 128)}
 
 
 def main():

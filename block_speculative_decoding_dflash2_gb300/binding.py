@@ -91,6 +91,8 @@ def testing_lib():
         T.dflash2_test_gemm_fp8.restype = I
         T.dflash2_test_force_cluster_split.restype = I
         T.dflash2_test_force_cluster_split.argtypes = [I]
+        T.dflash2_test_force_attention.restype = I
+        T.dflash2_test_force_attention.argtypes = [I]
         T.dflash2_test_gemm_fp8.argtypes = [P, P, I, I, P, I, I, I, P, P, S, P]
         T.dflash2_test_layout.restype = I
         T.dflash2_test_layout.argtypes = [F(Config), I, I, I, F(ctypes.c_size_t), I]
@@ -359,6 +361,12 @@ def dflash2_test_force_cluster_split(cs):
     """Force cluster split-K of cs slices on the library's own contractions
     (0 = its own schedule)."""
     _check("dflash2_test_force_cluster_split", testing_lib().dflash2_test_force_cluster_split(int(cs)))
+
+
+def dflash2_test_force_attention(mode):
+    """Attention kernel of later draft steps: 0 the library's choice, 1 the
+    mma.sync cluster kernel, 2 the tcgen05 kernel wherever it applies."""
+    _check("dflash2_test_force_attention", testing_lib().dflash2_test_force_attention(int(mode)))
 
 
 def dflash2_test_gemm_fp8(W8, scale, X, ctas, out, workspace, accumulate=False, stream=None):

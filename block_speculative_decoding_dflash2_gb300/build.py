@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdflash2.so")
 
-SOURCES = ["api.cu", "gemm_tc.cu", "gemm_simt.cu", "elementwise.cu", "attention.cu",
+SOURCES = ["api.cu", "gemm_tc.cu", "gemm_simt.cu", "elementwise.cu", "attention.cu", "attention_tc.cu",
            "topk.cu", "selector.cu", "verify.cu", "select_static.cu"]
 # the test hooks (include/dflash2_testing.h) live in a library of their own,
 # linked against libdflash2.so, so the product library exports only dflash2.h

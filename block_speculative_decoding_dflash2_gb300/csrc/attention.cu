@@ -14,6 +14,7 @@
 // chunks.  No CTA waits on another.  Keys are gathered row by row (one page
 // lookup per key, then 16-byte loads of its d contiguous elements).
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 
 #include "common.cuh"
@@ -711,17 +712,6 @@ int chunk_of(int max_ctx, int B, int batch, int nkv, int nsm) {
   return (int)std::max(64L, std::min(1024L, ch));
 }
 
-// CTAs per cluster: at most kMaxCluster and one per 64 keys of the longest
-// sequence.  A CTA takes a whole SM, so while the (kv head, sequence) pairs
-// fit the SMs the clusters fill one wave; beyond that, enough CTAs for about
-// two per SM, finer pieces for the scheduler to balance ragged contexts.
-int attn_cluster_ctas(int max_ctx, int B, int batch, int nkv, int nsm) {
-  const long L = (long)max_ctx + B;
-  const long pairs = (long)nkv * batch;
-  const long fill = pairs <= nsm ? nsm / pairs : (2L * nsm + pairs - 1) / pairs;
-  return (int)std::max(1L, std::min<long>({(long)kMaxCluster, (L + 63) / 64, fill}));
-}
-
 template <int DH>
 int launch_cluster(int R, int max_ctx, int page_size, int batch, int nkv, const Ctx& c, const bf16* q,
                    const bf16* kb, const bf16* vb, const bf16* kc, const bf16* vc, const int32_t* block_table,
@@ -761,6 +751,21 @@ int launch_cluster(int R, int max_ctx, int page_size, int batch, int nkv, const 
 
 }  // namespace
 
+// CTAs per cluster: at most 8 (the portable cluster size) and one per 64
+// keys of the longest sequence.  A CTA takes a whole SM, so while the (kv
+// head, sequence) pairs fit the SMs the clusters fill one wave; beyond that,
+// enough CTAs for about two per SM, finer pieces for the scheduler to
+// balance ragged contexts.
+int attn_cluster_ctas(int max_ctx, int B, int batch, int nkv, int nsm) {
+  const long L = (long)max_ctx + B;
+  const long pairs = (long)nkv * batch;
+  const long fill = pairs <= nsm ? nsm / pairs : (2L * nsm + pairs - 1) / pairs;
+  return (int)std::max(1L, std::min<long>({8L, (L + 63) / 64, fill}));
+}
+
+std::atomic<int> g_attn_mode{0};
+void attention_force_mode(int mode) { g_attn_mode.store(mode); }
+
 // Upper bound over every batch <= max_batch and SM count <= kMaxSM (the
 // chunk grows with the SM count's inverse, so kMaxSM gives the most chunks).
 size_t attn_part_bytes(int max_batch, int B, int nq, int nkv, int d, int max_ctx) {
@@ -779,6 +784,13 @@ int launch_attention(int dtype, const void* q, const void* kb, const void* vb, c
                      int max_ctx, int window, float* part, void* o_out, const Ctx& c) {
   const int R = (nq / nkv) * B;
   const int nrb = (R + 15) / 16;
+  const int mode = g_attn_mode.load();
+  if (mode != 1 && attention_tc_fits(dtype, d, page_size, R)) {
+    // (a page list too long for its shared memory: the cluster kernel below)
+    const int rc = launch_attention_tc(q, kb, vb, kc, vc, block_table, max_pages, page_size, n_pages, ctx_len,
+                                       new_off, batch, B, nq, nkv, max_ctx, window, o_out, c);
+    if (rc != DFLASH2_ERR_SHAPE) return rc;
+  }
   if (dtype == DFLASH2_BF16 && (d == 64 || d == 128) && nrb <= CLW) {  // a warp per (row block, key share)
     const bf16 *q_ = static_cast<const bf16*>(q), *kb_ = static_cast<const bf16*>(kb),
                *vb_ = static_cast<const bf16*>(vb), *kc_ = static_cast<const bf16*>(kc),

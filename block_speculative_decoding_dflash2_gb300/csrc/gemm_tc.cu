@@ -1223,6 +1223,20 @@ int make_rows_map(CUtensorMap* map, const void* base, long long rows, int cols, 
   return r == CUDA_SUCCESS ? DFLASH2_OK : DFLASH2_ERR_CUDA;
 }
 
+int make_sw128_map(CUtensorMap* map, const void* base, long long rows, int cols, long long ld_elems, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return DFLASH2_ERR_CUDA;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || (ld_elems * 2) % 16) return DFLASH2_ERR_SHAPE;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld_elems * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+}
+
 bool gemm_fusable(int M, int N, int epi) {
   // wider activation tiles run the plain epilogue and a row kernel: their
   // fused epilogues (16 columns per step, each step's norm/RoPE loads and

@@ -148,6 +148,9 @@ int gemm_bf16(const GemmOp& g, const Ctx& c);  // tcgen05 + TMA (sm_103a)
 // page loads); DFLASH2_ERR_SHAPE for unaligned bases or strides.
 int make_rows_map(CUtensorMap* map, const void* base, long long rows, int cols, long long ld_elems, int box_cols,
                   int box_rows);
+// The same view with a box of 64 columns x box_rows rows and the 128-byte
+// swizzle (tiles that tcgen05.mma reads as K-major or MN-major operands).
+int make_sw128_map(CUtensorMap* map, const void* base, long long rows, int cols, long long ld_elems, int box_rows);
 // Schedule bits of the last dflash2_draft_step call (test hook)
 enum {
   kSchedFusedPrologue = 1,  // sublayer prologue fused (norm + tap logits + conv)
@@ -225,6 +228,18 @@ int launch_attention(int dtype, const void* q, const void* kb, const void* vb, c
                      const int32_t* ctx_len, const int32_t* new_off, int batch, int B, int nq, int nkv, int d,
                      int max_ctx, int window, float* part, void* o_out, const Ctx& c);
 size_t attn_part_bytes(int batch, int B, int nq, int nkv, int d, int max_ctx);
+// CTAs per cluster (key chunks per (kv head, sequence)) of the cluster kernels
+int attn_cluster_ctas(int max_ctx, int B, int batch, int nkv, int nsm);
+// test hook: 0 = the library's choice, 1 = the mma.sync cluster kernel,
+// 2 = the tcgen05 kernel wherever it applies
+void attention_force_mode(int mode);
+// tcgen05 attention (attention_tc.cu): bf16 storage, head dimension 128,
+// 16-key pages, at most 80 query rows per kv head
+bool attention_tc_fits(int dtype, int d, int page_size, int R);
+int launch_attention_tc(const void* q, const void* kb, const void* vb, const void* kc, const void* vc,
+                        const int32_t* block_table, int max_pages, int page_size, int n_pages,
+                        const int32_t* ctx_len, const int32_t* new_off, int batch, int B, int nq, int nkv,
+                        int max_ctx, int window, void* o, const Ctx& c);
 
 // top-k (topk.cu)
 int launch_topk_scan(const float* logits, int rows, int V, float mult, float cap, float* debug, float* lists_v,

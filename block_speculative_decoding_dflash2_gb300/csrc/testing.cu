@@ -101,6 +101,12 @@ int dflash2_test_force_cluster_split(int cs) {
   return 0;
 }
 
+int dflash2_test_force_attention(int mode) {
+  if (mode < 0 || mode > 2) return DFLASH2_ERR_INVALID_ARG;
+  df2::attention_force_mode(mode);
+  return 0;
+}
+
 int dflash2_test_layout(const dflash2_config* cfg, int batch, int n_new, int max_ctx, size_t* offsets, int n) {
   return workspace_offsets(cfg, batch, n_new, max_ctx, offsets, n);
 }

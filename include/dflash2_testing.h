@@ -59,6 +59,16 @@ size_t dflash2_test_gemm_workspace(int M, int N);
  * outside {0, 2..8}.  Not thread-safe against concurrent draft steps.
  */
 int dflash2_test_force_cluster_split(int cs);
+
+/*
+ * From now on in this process, the block attention of every bf16 draft step
+ * runs on: mode 0, the library's choice; 1, the mma.sync cluster kernel; 2,
+ * the tcgen05 kernel wherever it applies (head dimension 128, 16-key pages,
+ * at most 80 query rows per kv head; elsewhere the library's choice).
+ * Returns 0, or DFLASH2_ERR_INVALID_ARG for another mode.  Not thread-safe
+ * against concurrent draft steps.
+ */
+int dflash2_test_force_attention(int mode);
 int dflash2_test_gemm(int dtype, const void *W, int M, int K, const void *X, int N, int ctas, int accumulate,
                       float *out, void *workspace, size_t ws_bytes, void *stream);
 

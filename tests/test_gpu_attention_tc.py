@@ -1,0 +1,66 @@
+"""The tcgen05 block attention (head dimension 128, 16-key pages) against the
+oracle, stage by stage, next to the mma.sync cluster kernel on the same
+inputs: every query-row count it is built for (16 .. 80 rows per kv head,
+the 56-row shape padded to 64), contexts that span several 128-key tiles per
+CTA and end mid-page, an empty context, sliding windows whose first key is
+not on a page boundary (every row then takes the cp.async path), and the
+end-to-end step."""
+
+import pytest
+
+import dflash2_synth as S
+from tests.helpers import Case, lib
+from tests.test_gpu_draft import check_case
+from tests.test_gpu_stagewise import run_stagewise
+
+pytestmark = pytest.mark.gpu
+
+# query rows per kv head = (n_q_heads / n_kv_heads) x block_size
+SHAPES = {
+    "r16": dict(n_q_heads=4, n_kv_heads=2, block_size=8),
+    "r32": dict(n_q_heads=8, n_kv_heads=2, block_size=8),
+    "r48": dict(n_q_heads=12, n_kv_heads=2, block_size=8),
+    "r56": dict(n_q_heads=16, n_kv_heads=2, block_size=7),
+    "r80": dict(n_q_heads=10, n_kv_heads=2, block_size=16),
+}
+
+
+def _cfg(name, i, **over):
+    return S.small_bf16_config(head_dim=128, hidden=512, n_layers=1, top_k=8, index=40 + i, **SHAPES[name],
+                               **over)
+
+
+def _run(cfg, mode, ctx_lens, n_new, seed):
+    B = lib()
+    B.dflash2_test_force_attention(mode)
+    try:
+        case = Case(cfg, ctx_lens=ctx_lens, n_new=n_new, seed=seed).run_gpu()
+    finally:
+        B.dflash2_test_force_attention(0)
+    assert case.status == 0
+    return case
+
+
+@pytest.mark.parametrize("mode", [2, 1])
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_attention_kernels_stagewise(name, mode):
+    # 3000 + 8 keys in 8 chunks of 384: three 128-key tiles per CTA; 1234
+    # ends mid-page; the empty context reads the block's own keys only
+    i = list(SHAPES).index(name)
+    B_ = SHAPES[name]["block_size"]
+    case = _run(_cfg(name, i), mode, [3000, 0, 333, 1234], [B_, 3, 1, 5], 60 + i)
+    run_stagewise(case)
+
+
+@pytest.mark.parametrize("window", [37, 200, 1000])
+@pytest.mark.parametrize("name", ["r56", "r80"])
+def test_tc_attention_sliding_window(name, window):
+    i = list(SHAPES).index(name)
+    case = _run(_cfg(name, i, sliding_window=window), 2, [3000, 60, 0, 777], [4, 2, 8, 1], 70 + i)
+    run_stagewise(case)
+
+
+def test_tc_attention_end_to_end():
+    case = _run(_cfg("r80", 4), 2, [2047, 16, 500], [16, 1, 7], 80)
+    run_stagewise(case)
+    check_case(case)

@@ -785,7 +785,10 @@ int launch_attention(int dtype, const void* q, const void* kb, const void* vb, c
   const int R = (nq / nkv) * B;
   const int nrb = (R + 15) / 16;
   const int mode = g_attn_mode.load();
-  if (mode != 1 && attention_tc_fits(dtype, d, page_size, R)) {
+  // the tcgen05 kernel where it was measured faster: more than 32 query rows
+  // per kv head (the 27B and 30B-A3B shapes: +8% and +7..37% per step); at
+  // 32 rows (the 8B shapes) the mma.sync cluster kernel is as fast or faster
+  if ((mode == 2 || (mode == 0 && R > 32)) && attention_tc_fits(dtype, d, page_size, R)) {
     // (a page list too long for its shared memory: the cluster kernel below)
     const int rc = launch_attention_tc(q, kb, vb, kc, vc, block_table, max_pages, page_size, n_pages, ctx_len,
                                        new_off, batch, B, nq, nkv, max_ctx, window, o_out, c);

@@ -12,12 +12,15 @@
 // head dimension take the 128-row M side:
 //
 //   S^T = K Q^T     M = 128 keys, N = the query rows, K = 128 dims
-//   O^T += V^T P^T  M = 128 dims, N = the query rows, K = 128 keys
+//   O^T += V^T P^T  M = 128 dims, N = 2 x the query rows, K = 128 keys
 //
-// K, Q and P^T are K-major operands; V^T is read MN-major straight from the
-// V tile (each key a 128-byte row of 64 dims).  P is split into bf16 hi + lo
-// parts (two MMAs), so the probabilities keep ~16 bits as in the mma.sync
-// kernel.  Roles by warp:
+// K and Q are K-major operands; V^T is read MN-major straight from the V
+// tile (each key a 128-byte row of 64 dims), and P^T MN-major as the softmax
+// threads write it (each key a 128-byte row of 64 columns, so a thread
+// stores its key's probabilities as 16-byte vectors).  P is split into bf16
+// hi + lo parts, side by side along N (one MMA per 16 keys reads V once),
+// so the probabilities keep ~16 bits as in the mma.sync kernel; the two
+// halves of O^T are added at the end.  Roles by warp:
 //   warp 0      K/V tiles of 128 keys into a two-stage ring: whole 16-key
 //               cache pages by TMA (128-byte swizzle, one box per page, half
 //               head and K or V), the rest (a partial last page, the block's
@@ -61,12 +64,18 @@ template <int NP>
 struct TcSmem {
   static constexpr int KV = 0;                         // [TST][K, V][2 halves][TK][128 B]
   static constexpr int Q = TST * KV_STAGE;             // [2 halves][NP][128 B]
-  static constexpr int P = Q + 2 * NP * 128;           // [hi, lo][2 key halves][NP][128 B]
-  static constexpr int RED = P + 4 * NP * 128;         // float [4 lane quarters][NP]
+  // P^T of a tile: the hi parts as columns 0 .. NP-1 and the lo parts as
+  // NP .. 2NP-1 of one N = 2NP operand, in 64-column blocks
+  static constexpr int NB = (2 * NP + 63) / 64;
+  static constexpr int P = Q + 2 * NP * 128;           // [PB][NB][TK keys][128 B]
+  // two P buffers (the softmax of a tile overlaps the PV of the one before)
+  // where they fit beside two K/V stages
+  static constexpr int PB = P + 2 * NB * TK * 128 + 8 * 1024 <= 227 * 1024 ? 2 : 1;
+  static constexpr int RED = P + PB * NB * TK * 128;   // float [4 lane quarters][NP]
   static constexpr int MS = RED + 4 * NP * 4;          // float [NP] reference maxima of the rows
   static constexpr int CW = MS + NP * 4;               // float [rows of this CTA][TNS] merge weights
   static constexpr int PG = CW + (NP + TNS) * TNS * 4;  // int page ids of the chunk
-  static size_t bytes(int npg) { return 1024 + PG + (size_t)npg * 4 + 16 * 8 + 16; }
+  static size_t bytes(int npg) { return 1024 + PG + (size_t)npg * 4 + 8 + 18 * 8 + 16; }
 };
 
 __device__ __forceinline__ void sm_bar_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
@@ -83,15 +92,12 @@ __device__ __forceinline__ bool sm_bar_or(bool pred) {
   return r != 0;
 }
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
+// 2^x by the special-function unit (ex2.approx: relative error near 2^-22,
+// far below the 2^-16 the hi + lo split of P keeps; 2^-inf = 0)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 template <int NP>
@@ -103,6 +109,9 @@ __global__ void __launch_bounds__(TT, 1) attn_tc_kernel(
     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, int page_tma,
     bf16* __restrict__ o, unsigned* status) {
   using L = TcSmem<NP>;
+  constexpr int PB = L::PB;
+  // TMEM columns: O^T (hi, lo halves: 2NP) at 0, the two S^T buffers at 256
+  constexpr uint32_t kOCol = 0, kSCol = 256;
   constexpr int HC = NP / 2;  // query rows (TMEM columns) per softmax thread
   constexpr int FS = TD + 2;  // partial row: acc[TD], m, l
   static_assert(NP % 16 == 0 && NP <= kTcMaxRows, "query rows");
@@ -113,14 +122,19 @@ __global__ void __launch_bounds__(TT, 1) attn_tc_kernel(
   float* cw = reinterpret_cast<float*>(sm + L::CW);
   int* pg = reinterpret_cast<int*>(sm + L::PG);
   uint64_t* bars = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(pg + npg) + 7) & ~uintptr_t(7));
-  uint64_t* kvfull = bars;       // [TST] a tile landed (1 arrival + TMA bytes)
-  uint64_t* kvempty = bars + 2;  // [TST] its PV MMAs completed (commit)
-  uint64_t* sfull = bars + 4;    // [2] S^T of a tile in TMEM (commit)
-  uint64_t* sempty = bars + 6;   // [2] S^T read by the softmax warps (8 arrivals)
-  uint64_t* pready = bars + 8;   // P of a tile in shared memory (8 arrivals)
-  uint64_t* odone = bars + 9;    // a tile's PV MMAs completed (commit)
-  uint64_t* qready = bars + 10;  // Q rows in shared memory (8 arrivals)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
+  uint64_t* kfull = bars;        // [TST] a K tile landed (1 arrival + TMA bytes)
+  uint64_t* kempty = bars + 2;   // [TST] its S^T MMAs completed (commit)
+  uint64_t* vfull = bars + 4;    // [TST] a V tile landed
+  uint64_t* vempty = bars + 6;   // [TST] its PV MMAs completed (commit)
+  uint64_t* sfull = bars + 8;    // [2] S^T of a tile in TMEM (commit)
+  uint64_t* sempty = bars + 10;  // [2] S^T read by the softmax warps (8 arrivals)
+  // P buffer b = t % PB has a barrier pair of its own: with two buffers the
+  // softmax may finish tile t + 1 before the MMA thread has seen tile t's
+  // phase, which one shared barrier would then have passed
+  uint64_t* pready = bars + 12;  // [PB] P of tile t in buffer t % PB (8 arrivals)
+  uint64_t* odone = bars + 14;   // [PB] the PV MMAs reading buffer t % PB completed (commit)
+  uint64_t* qready = bars + 16;  // Q rows in shared memory (8 arrivals)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* comb = reinterpret_cast<float*>(sm + L::KV);  // [R][FS] after the key loop (aliases the ring)
 
@@ -130,21 +144,25 @@ __global__ void __launch_bounds__(TT, 1) attn_tc_kernel(
   pdl_launch_next();
   if (threadIdx.x == 0) {
     for (int i = 0; i < TST; ++i) {
-      mbar_init(kvfull + i, 1);
-      mbar_init(kvempty + i, 1);
+      mbar_init(kfull + i, 1);
+      mbar_init(kempty + i, 1);
+      mbar_init(vfull + i, 1);
+      mbar_init(vempty + i, 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(sfull + i, 1);
       mbar_init(sempty + i, TSW);
     }
     mbar_init(pready, TSW);
+    mbar_init(pready + 1, TSW);
     mbar_init(odone, 1);
+    mbar_init(odone + 1, 1);
     mbar_init(qready, TSW);
     *abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 256);
+    tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
 
@@ -174,82 +192,90 @@ __global__ void __launch_bounds__(TT, 1) attn_tc_kernel(
 
   if (warp == 0) {
     // ---------------------------------------------------------------- K/V loads
-    // Lane c < 16 moves 16-byte chunk c of a key's K row, lane 16 + c the
-    // same chunk of its V row; chunk c lands in half c / 8, at position
-    // (c % 8) ^ (row % 8) of the row's 128 bytes (the TMA's 128-byte swizzle).
+    // K and V of a tile have stages (and barriers) of their own: K(t + 2)
+    // loads as soon as S^T(t) is done, V(t + 2) once PV(t) is, so the K
+    // load overlaps the softmax of the tiles in between.  Whole context
+    // pages with a valid id go by TMA (one box per 64-dim half); the other
+    // rows by cp.async, chunk c of a row in half c / 8 at position
+    // (c % 8) ^ (row % 8) of its 128 bytes (the TMA's 128-byte swizzle).
     const bool tma_ok = page_tma && (k0 % 16) == 0;
     const uint64_t pol = policy_evict_first();
-    const bool isv = lane >= 16;
-    const int c = lane & 15;
     int issued = 0;
-    for (int t = 0; t < ntiles; ++t) {
+    bool stop = false;
+    for (int t = 0; t < ntiles && !stop; ++t) {
       const int st = t % TST;
-      if (t >= TST) {
-        const bool free_ = __all_sync(0xffffffffu, mbar_wait(kvempty + st, (uint32_t)(((t / TST) - 1) & 1),
-                                                             abort_flag, kTcWaitNs));
-        if (!free_) {
-          if (lane == 0) fail();
-          break;
-        }
-      }
       const int t0 = k0 + t * TK;
-      uint8_t* Kst = sm + L::KV + st * KV_STAGE;
-      uint8_t* Vst = Kst + KV_STAGE / 2;
-      // whole context pages of the tile: TMA boxes where the page id is valid
+      // (worked out before the stages are free: lane i < 8 checks page i)
       const int cend = max(t0, min(min(t0 + TK, k1), P));
       const int nfull = tma_ok ? (cend - t0) / 16 : 0;
-      uint32_t vmask = 0;
-      for (int i = 0; i < nfull; ++i) {
-        const int li = (t0 + 16 * i) / 16 - pbase;
-        const int page = li < npg ? pg[li] : -1;
-        if (page >= 0 && page < n_pages) vmask |= 1u << i;
+      int my_page = -1;
+      if (lane < nfull) {
+        const int li = (t0 + 16 * lane) / 16 - pbase;
+        my_page = li < npg ? pg[li] : -1;
       }
-      // every other row by cp.async (zero-filled where nothing is read)
-      bool manual = false;
-      for (int r = 0; r < TK; ++r) {
-        if ((r >> 4) < nfull && ((vmask >> (r >> 4)) & 1)) continue;
-        manual = true;
-        const int j = t0 + r;
-        const bf16* src = kc;
-        bool ok = false;
-        if (j < k1) {
-          if (j < P) {
-            const int li = j / page_size - pbase;
-            const int page = li < npg ? pg[li] : -1;
-            if (page >= 0 && page < n_pages) {
-              src = (isv ? vc : kc) + (((size_t)page * page_size + j % page_size) * nkv + g) * TD + c * 8;
-              ok = true;
-            } else if (lane == 0) {
-              flag(status, DFLASH2_DEV_BAD_PAGE);
-            }
-          } else {
-            src = (isv ? vb : kb) + (((size_t)s * B + (j - P)) * nkv + g) * TD + c * 8;
-            ok = true;
+      const uint32_t vmask = __ballot_sync(0xffffffffu, my_page >= 0 && my_page < n_pages) & 0xffu;
+      const uint32_t full_mask = (1u << nfull) - 1u;
+      const bool manual = vmask != full_mask || nfull * 16 < TK;
+      const int box_page = __shfl_sync(0xffffffffu, my_page, (lane >> 1) & 7);
+      for (int part = 0; part < 2; ++part) {  // K, then V
+        uint64_t* full = (part ? vfull : kfull) + st;
+        if (t >= TST) {
+          const bool free_ = __all_sync(0xffffffffu, mbar_wait((part ? vempty : kempty) + st,
+                                                               (uint32_t)(((t / TST) - 1) & 1), abort_flag,
+                                                               kTcWaitNs));
+          if (!free_) {
+            if (lane == 0) fail();
+            stop = true;
+            break;
           }
         }
-        cp_async16((isv ? Vst : Kst) + (c >> 3) * HALF + r * 128 + (((c & 7) ^ (r & 7)) << 4), src, ok);
+        uint8_t* dstb = sm + L::KV + st * KV_STAGE + part * (KV_STAGE / 2);
+        if (manual) {
+          // the pages with an invalid id, then the rows past the whole pages
+          for (int idx = (vmask == full_mask ? nfull * 256 : 0) + lane; idx < TK * 16; idx += 32) {
+            const int r = idx >> 4, c = idx & 15;
+            if ((r >> 4) < nfull && ((vmask >> (r >> 4)) & 1)) continue;
+            const int j = t0 + r;
+            const bf16* src = kc;
+            bool ok = false;
+            if (j < k1) {
+              if (j < P) {
+                const int li = j / page_size - pbase;
+                const int page = li < npg ? pg[li] : -1;
+                if (page >= 0 && page < n_pages) {
+                  src = (part ? vc : kc) + (((size_t)page * page_size + j % page_size) * nkv + g) * TD + c * 8;
+                  ok = true;
+                } else if (c == 0 && part == 0) {
+                  flag(status, DFLASH2_DEV_BAD_PAGE);
+                }
+              } else {
+                src = (part ? vb : kb) + (((size_t)s * B + (j - P)) * nkv + g) * TD + c * 8;
+                ok = true;
+              }
+            }
+            cp_async16(dstb + (c >> 3) * HALF + r * 128 + (((c & 7) ^ (r & 7)) << 4), src, ok);
+          }
+          cp_async_commit();
+          cp_async_wait<0>();
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)__popc(vmask) * 2u * 2048u);
+        __syncwarp();
+        // lane 2i + hh: page i, half hh
+        if (lane < 2 * nfull && ((vmask >> (lane >> 1)) & 1)) {
+          const int i = lane >> 1, hh = lane & 1;
+          tma_load_2d(dstb + hh * HALF + i * 16 * 128, part ? &tmV : &tmK, full, g * TD + hh * 64, box_page * 16,
+                      pol);
+        }
       }
-      if (manual) {
-        cp_async_commit();
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(kvfull + st, (uint32_t)__popc(vmask) * 4u * 2048u);
-      __syncwarp();
-      // lane 4i + w: page i, box w (K half 0, K half 1, V half 0, V half 1)
-      if (lane < 4 * nfull && ((vmask >> (lane >> 2)) & 1)) {
-        const int i = lane >> 2, w = lane & 3;
-        const int page = pg[(t0 + 16 * i) / 16 - pbase];
-        uint8_t* dst = (w < 2 ? Kst : Vst) + (w & 1) * HALF + i * 16 * 128;
-        tma_load_2d(dst, w < 2 ? &tmK : &tmV, kvfull + st, g * TD + (w & 1) * 64, page * 16, pol);
-      }
-      ++issued;
+      if (!stop) ++issued;
     }
     // copies still in flight (after an abort) land before the CTA moves on
     for (int t = max(0, issued - TST); t < issued; ++t) {
       volatile int never = 0;
-      mbar_wait(kvfull + t % TST, (uint32_t)((t / TST) & 1), &never, kTcWaitNs);
+      mbar_wait(kfull + t % TST, (uint32_t)((t / TST) & 1), &never, kTcWaitNs);
+      mbar_wait(vfull + t % TST, (uint32_t)((t / TST) & 1), &never, kTcWaitNs);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issue
@@ -258,52 +284,58 @@ __global__ void __launch_bounds__(TT, 1) attn_tc_kernel(
     // can go, PV first, so a PV never waits behind a load.
     if (lane == 0 && ntiles > 0) {
       const uint32_t id_s = idesc_bf16_f32(TK, NP);
-      const uint32_t id_o = idesc_bf16_f32(TD, NP) | (1u << 15);  // A = V^T read MN-major
-      const uint32_t q_base = smem_u32(sm + L::Q), p_base = smem_u32(sm + L::P);
+      // A = V^T and B = P^T both read MN-major; N = hi and lo columns
+      const uint32_t id_o = idesc_bf16_f32(TD, 2 * NP) | (1u << 15) | (1u << 16);
+      // operand descriptors of the stage / buffer bases; a k step adds its
+      // offset in 16-byte units to the start-address field (no carry: shared
+      // addresses stay below 2^18 bytes)
+      const uint32_t kv0 = smem_u32(sm + L::KV), p_base = smem_u32(sm + L::P);
+      const uint64_t q_desc = sdesc_sw128(smem_u32(sm + L::Q));
+      // (stage / buffer 1 is stage / buffer 0 plus a fixed offset)
+      const uint64_t k_desc = sdesc_sw128(kv0), v_desc = sdesc_mn_sw128(kv0 + KV_STAGE / 2, HALF, 1024);
+      const uint64_t p_desc = sdesc_mn_sw128(p_base, HALF, 1024);
+      constexpr uint64_t kStageStep = KV_STAGE >> 4, kBufStep = (L::NB * HALF) >> 4;
       bool ok = mbar_wait(qready, 0, abort_flag, kTcWaitNs);
       tc_fence_after();
       int ns_ = 0, npv = 0;
       uint64_t t_last = globaltimer();
       while (ok && npv < ntiles) {
         bool did = false;
-        if (npv < ns_ && mbar_try_wait(smem_u32(pready), (uint32_t)(npv & 1))) {
+        if (npv < ns_ && mbar_test_wait(smem_u32(pready + npv % PB), (uint32_t)((npv / PB) & 1)) &&
+            mbar_test_wait(smem_u32(vfull + npv % TST), (uint32_t)((npv / TST) & 1))) {
           tc_fence_after();
-          const int st = npv % TST;
-          const uint32_t v_base = smem_u32(sm + L::KV + st * KV_STAGE + KV_STAGE / 2);
-          const uint32_t od = tmem + 2 * NP;
+          const int st = npv % TST, pb = npv % PB;
+          const uint64_t vd = v_desc + (uint64_t)st * kStageStep;
+          const uint64_t pd = p_desc + (uint64_t)pb * kBufStep;
 #pragma unroll
-          for (int part = 0; part < 2; ++part) {  // P hi, then P lo
-#pragma unroll
-            for (int j = 0; j < TK / 16; ++j) {
-              const uint64_t ad = sdesc_mn_sw128(v_base + j * 2048, HALF, 1024);
-              const uint64_t bd = sdesc_sw128(p_base + part * 2 * NP * 128 + (j >> 2) * NP * 128 + (j & 3) * 32);
-              umma_bf16(od, ad, bd, id_o, (npv > 0 || part > 0 || j > 0) ? 1u : 0u);
-            }
-          }
-          umma_commit(odone);
-          umma_commit(kvempty + st);
+          for (int j = 0; j < TK / 16; ++j)  // 16 keys = two 1024-byte atoms
+            umma_bf16(tmem + kOCol, vd + (uint64_t)(j * 128), pd + (uint64_t)(j * 128), id_o,
+                      (npv > 0 || j > 0) ? 1u : 0u);
+          umma_commit(odone + npv % PB);
+          umma_commit(vempty + st);
           ++npv;
           did = true;
         } else if (ns_ < ntiles && ns_ < npv + 2 &&
-                   mbar_try_wait(smem_u32(kvfull + ns_ % TST), (uint32_t)((ns_ / TST) & 1)) &&
-                   (ns_ < 2 || mbar_try_wait(smem_u32(sempty + (ns_ & 1)), (uint32_t)(((ns_ >> 1) - 1) & 1)))) {
+                   mbar_test_wait(smem_u32(kfull + ns_ % TST), (uint32_t)((ns_ / TST) & 1)) &&
+                   (ns_ < 2 || mbar_test_wait(smem_u32(sempty + (ns_ & 1)), (uint32_t)(((ns_ >> 1) - 1) & 1)))) {
           tc_fence_after();
-          const uint32_t k_base = smem_u32(sm + L::KV + (ns_ % TST) * KV_STAGE);
-          const uint32_t sd = tmem + (uint32_t)((ns_ & 1) * NP);
+          const uint32_t sd = tmem + (uint32_t)(kSCol + (ns_ & 1) * NP);
+          const uint64_t kd = k_desc + (uint64_t)(ns_ % TST) * kStageStep;
 #pragma unroll
-          for (int kk = 0; kk < TD / 16; ++kk) {
-            const uint64_t ad = sdesc_sw128(k_base + (kk >> 2) * HALF + (kk & 3) * 32);
-            const uint64_t bd = sdesc_sw128(q_base + (kk >> 2) * NP * 128 + (kk & 3) * 32);
-            umma_bf16(sd, ad, bd, id_s, kk > 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < TD / 16; ++kk)  // 16 dims: 32 bytes within the half's 128-byte rows
+            umma_bf16(sd, kd + (uint64_t)((kk >> 2) * (HALF >> 4) + (kk & 3) * 2),
+                      q_desc + (uint64_t)((kk >> 2) * (NP * 8) + (kk & 3) * 2), id_s, kk > 0 ? 1u : 0u);
           umma_commit(sfull + (ns_ & 1));
+          umma_commit(kempty + ns_ % TST);
           ++ns_;
           did = true;
         }
         if (did) {
           t_last = globaltimer();
-        } else if (*abort_flag || globaltimer() - t_last > kTcWaitNs) {
-          ok = false;
+        } else {
+          // back off: this warp shares its scheduler with two softmax warps
+          __nanosleep(40);
+          if (*abort_flag || globaltimer() - t_last > kTcWaitNs) ok = false;
         }
       }
       if (!ok) fail();
@@ -339,11 +371,10 @@ __global__ void __launch_bounds__(TT, 1) attn_tc_kernel(
     if (qd == 0 && lane == 0)
       for (int i = 0; i < HC; ++i) msh[n0 + i] = -INFINITY;
     sm_bar_sync();
-    // this thread's P^T element (row n, key kl): key half kl / 64, 16-byte
-    // chunk (kl % 64) / 8 swizzled by the row, element kl % 8
-    uint8_t* p_hi = sm + L::P + (kl >> 6) * NP * 128 + (kl & 7) * 2;
-    uint8_t* p_lo = p_hi + 2 * NP * 128;
-    const int pchunk = (kl & 63) >> 3;
+    // this thread's row of P^T: key kl, query rows n0 .. n0 + HC - 1 in
+    // 16-byte chunks of 8 rows (chunk c of a 64-row block at position
+    // c ^ (kl % 8) of the key's 128-byte row)
+    uint8_t* p_row = sm + L::P + kl * 128;
     // ok stays uniform over the 256 softmax threads: a failed wait only
     // clears it, and the threads leave the key loop together, at the vote at
     // the top of the next tile, so every named barrier sees all of them
@@ -362,7 +393,7 @@ __global__ void __launch_bounds__(TT, 1) attn_tc_kernel(
         uint32_t r[HC];
 #pragma unroll
         for (int c8 = 0; c8 < HC / 8; ++c8)
-          tmem_ld8_nowait(lane_base + (uint32_t)((t & 1) * NP + n0 + c8 * 8),
+          tmem_ld8_nowait(lane_base + (uint32_t)(kSCol + (t & 1) * NP + n0 + c8 * 8),
                           *reinterpret_cast<uint32_t(*)[8]>(&r[c8 * 8]));
         tmem_ld_wait();
 #pragma unroll
@@ -371,29 +402,36 @@ __global__ void __launch_bounds__(TT, 1) attn_tc_kernel(
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(sempty + (t & 1));
+      // rescale test: a score passes its row's reference maximum by more
+      // than the headroom (valid keys only; the key is this thread's)
       bool need = false;
+      if (valid) {
 #pragma unroll
-      for (int i = 0; i < HC; ++i) {
-        x[i] = valid ? x[i] * scale : -INFINITY;
-        need |= x[i] > msh[n0 + i] + kRescaleAt;
+        for (int i = 0; i < HC; i += 4) {
+          const float4 m4 = *reinterpret_cast<const float4*>(msh + n0 + i);
+          need |= fmaf(x[i], scale, -m4.x) > kRescaleAt;
+          need |= fmaf(x[i + 1], scale, -m4.y) > kRescaleAt;
+          need |= fmaf(x[i + 2], scale, -m4.z) > kRescaleAt;
+          need |= fmaf(x[i + 3], scale, -m4.w) > kRescaleAt;
+        }
       }
       bool have_o = false;  // waited for the previous tile's PV
       if (sm_bar_or(need)) {
         // new reference maxima: the tile's column maxima over its 128 keys
 #pragma unroll
         for (int i = 0; i < HC; ++i) {
-          const float v = warp_max(x[i]);
+          const float v = warp_max(valid ? x[i] * scale : -INFINITY);
           if (lane == 0) red[qd * NP + n0 + i] = v;
         }
         sm_bar_sync();
         if (t > 0) {  // O^T holds the earlier tiles: rescale it once their PV is done
-          if (!mbar_wait(odone, (uint32_t)((t - 1) & 1), abort_flag, kTcWaitNs)) {
+          if (!mbar_wait(odone + (t - 1) % PB, (uint32_t)(((t - 1) / PB) & 1), abort_flag, kTcWaitNs)) {
             fail();
             ok = false;
           }
           ok = __all_sync(0xffffffffu, ok);
           tc_fence_after();
-          have_o = true;
+          have_o = PB == 1;
         }
 #pragma unroll
         for (int c8 = 0; c8 < HC / 8; ++c8) {
@@ -406,14 +444,17 @@ __global__ void __launch_bounds__(TT, 1) attn_tc_kernel(
             f[e] = mo == -INFINITY ? 0.f : exp2f(mo - mn);
             l[i] *= f[e];
           }
-          if (t > 0 && ok) {
-            uint32_t r8[8];
-            const uint32_t ta = lane_base + (uint32_t)(2 * NP + n0 + c8 * 8);
-            tmem_ld8_nowait(ta, r8);
-            tmem_ld_wait();
+          if (t > 0 && ok) {  // the hi and the lo columns of these rows
 #pragma unroll
-            for (int e = 0; e < 8; ++e) r8[e] = __float_as_uint(__uint_as_float(r8[e]) * f[e]);
-            tmem_st8(ta, r8);
+            for (int part = 0; part < 2; ++part) {
+              uint32_t r8[8];
+              const uint32_t ta = lane_base + (uint32_t)(kOCol + part * NP + n0 + c8 * 8);
+              tmem_ld8_nowait(ta, r8);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 8; ++e) r8[e] = __float_as_uint(__uint_as_float(r8[e]) * f[e]);
+              tmem_st8(ta, r8);
+            }
           }
         }
         if (t > 0 && ok) tmem_st_wait();
@@ -425,34 +466,59 @@ __global__ void __launch_bounds__(TT, 1) attn_tc_kernel(
           }
         sm_bar_sync();
       }
-      if (t > 0 && !have_o) {  // P of the previous tile read by its PV before it is overwritten
-        if (!mbar_wait(odone, (uint32_t)((t - 1) & 1), abort_flag, kTcWaitNs)) {
+      // P buffer t % PB is free once the PV of tile t - PB is done
+      if (t >= PB && !have_o) {
+        if (!mbar_wait(odone + t % PB, (uint32_t)(((t - PB) / PB) & 1), abort_flag, kTcWaitNs)) {
           fail();
           ok = false;
         }
         tc_fence_after();
       }
-      // P = 2^(x - m), split hi + lo, into P^T (row n, key kl)
+      // P = 2^(x - m), split hi + lo, into P^T (key kl, rows n0 ..)
+      uint8_t* pb = p_row + (t % PB) * (L::NB * HALF);
 #pragma unroll
-      for (int i = 0; i < HC; ++i) {
-        const int n = n0 + i;
-        const float p = x[i] == -INFINITY ? 0.f : exp2f(x[i] - msh[n]);
-        l[i] += p;
-        const __nv_bfloat16 hi = __float2bfloat16_rn(p);
-        const __nv_bfloat16 lo = __float2bfloat16_rn(p - __bfloat162float(hi));
-        const int off = n * 128 + ((pchunk ^ (n & 7)) << 4);
-        *reinterpret_cast<__nv_bfloat16*>(p_hi + off) = hi;
-        *reinterpret_cast<__nv_bfloat16*>(p_lo + off) = lo;
+      for (int c8 = 0; c8 < HC / 8; ++c8) {
+        const int nc = n0 + c8 * 8;
+        uint32_t hi[4], lo[4];
+        if (valid) {
+          const float4 ma = *reinterpret_cast<const float4*>(msh + nc);
+          const float4 mb = *reinterpret_cast<const float4*>(msh + nc + 4);
+          const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const int i = c8 * 8 + e;
+            const float p0 = ex2_approx(fmaf(x[i], scale, -mm[e]));
+            const float p1 = ex2_approx(fmaf(x[i + 1], scale, -mm[e + 1]));
+            l[i] += p0;
+            l[i + 1] += p1;
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+            const uint32_t hb = *reinterpret_cast<const uint32_t*>(&h2);
+            const __nv_bfloat162 l2 =
+                __floats2bfloat162_rn(p0 - __uint_as_float(hb << 16), p1 - __uint_as_float(hb & 0xffff0000u));
+            hi[e >> 1] = hb;
+            lo[e >> 1] = *reinterpret_cast<const uint32_t*>(&l2);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) hi[e] = lo[e] = 0u;
+        }
+        // column nc (hi) and NP + nc (lo): block c / 64, chunk (c % 64) / 8
+        const int ch = nc, cl = NP + nc;
+        *reinterpret_cast<uint4*>(pb + (ch >> 6) * HALF + ((((ch & 63) >> 3) ^ (kl & 7)) << 4)) =
+            make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(pb + (cl >> 6) * HALF + ((((cl & 63) >> 3) ^ (kl & 7)) << 4)) =
+            make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(pready);
+      if (lane == 0) mbar_arrive(pready + t % PB);
     }
     // the last PV, then this CTA's partial rows: O^T columns, m and the
     // weight sums (over the 32 keys of a warp, then the 4 lane quarters)
     if (ntiles > 0 && ok) {
-      if (!mbar_wait(odone, (uint32_t)((ntiles - 1) & 1), abort_flag, kTcWaitNs)) fail();
+      if (!mbar_wait(odone + (ntiles - 1) % PB, (uint32_t)(((ntiles - 1) / PB) & 1), abort_flag, kTcWaitNs))
+        fail();
       tc_fence_after();
     }
     sm_bar_sync();  // every read of red by the last tile is done
@@ -465,12 +531,13 @@ __global__ void __launch_bounds__(TT, 1) attn_tc_kernel(
 #pragma unroll
     for (int c8 = 0; c8 < HC / 8; ++c8) {
       float ov[8];
-      if (ntiles > 0) {
-        uint32_t r8[8];
-        tmem_ld8_nowait(lane_base + (uint32_t)(2 * NP + n0 + c8 * 8), r8);
+      if (ntiles > 0) {  // hi + lo halves
+        uint32_t rh[8], rl[8];
+        tmem_ld8_nowait(lane_base + (uint32_t)(kOCol + n0 + c8 * 8), rh);
+        tmem_ld8_nowait(lane_base + (uint32_t)(kOCol + NP + n0 + c8 * 8), rl);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 8; ++e) ov[e] = __uint_as_float(r8[e]);
+        for (int e = 0; e < 8; ++e) ov[e] = __uint_as_float(rh[e]) + __uint_as_float(rl[e]);
       } else {
 #pragma unroll
         for (int e = 0; e < 8; ++e) ov[e] = 0.f;
@@ -549,7 +616,7 @@ __global__ void __launch_bounds__(TT, 1) attn_tc_kernel(
   cluster_sync();  // the other CTAs may still be reading this CTA's partials
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 

@@ -2,7 +2,7 @@
 oracle, stage by stage, next to the mma.sync cluster kernel on the same
 inputs: every query-row count it is built for (16 .. 80 rows per kv head,
 the 56-row shape padded to 64), contexts that span several 128-key tiles per
-CTA and end mid-page, an empty context, sliding windows whose first key is
+CTA (up to eight) and end mid-page, an empty context, sliding windows whose first key is
 not on a page boundary (every row then takes the cp.async path), and the
 end-to-end step."""
 
@@ -57,6 +57,16 @@ def test_attention_kernels_stagewise(name, mode):
 def test_tc_attention_sliding_window(name, window):
     i = list(SHAPES).index(name)
     case = _run(_cfg(name, i, sliding_window=window), 2, [3000, 60, 0, 777], [4, 2, 8, 1], 70 + i)
+    run_stagewise(case)
+
+
+@pytest.mark.parametrize("name", ["r32", "r56", "r80"])
+def test_tc_attention_long_chunks(name):
+    # one long sequence and a shorter one: 8 chunks of ~1000 keys, eight
+    # 128-key tiles per CTA, so the double-buffered P and the K/V stages
+    # each go round several times
+    i = list(SHAPES).index(name)
+    case = _run(_cfg(name, i), 2, [8000, 5100], [3, 2], 90 + i)
     run_stagewise(case)
 
 

@@ -18,10 +18,11 @@
 // tile (each key a 128-byte row of 64 dims), and P^T MN-major as the softmax
 // threads write it (each key a 128-byte row of 64 columns, so a thread
 // stores its key's probabilities as 16-byte vectors).  P is split into bf16
-// hi + lo parts, side by side along N (one MMA per 16 keys reads V once),
-// so the probabilities keep ~16 bits as in the mma.sync kernel; the two
-// halves of O^T are added at the end.  Roles by warp:
-//   warp 0      K/V tiles of 128 keys into a two-stage ring: whole 16-key
+// hi + lo parts (hi the top 16 bits of p, lo the remainder rounded), side by
+// side along N (one MMA per 16 keys reads V once), so the probabilities keep
+// ~15 bits; the two halves of O^T are added at the end.  Roles by warp:
+//   warp 0      K and V tiles of 128 keys, each into a two-stage ring of its
+//               own (K reloads once its S^T is done, V once its PV is): whole 16-key
 //               cache pages by TMA (128-byte swizzle, one box per page, half
 //               head and K or V), the rest (a partial last page, the block's
 //               own keys, zero rows past the chunk, every row when the chunk
@@ -491,11 +492,12 @@ __global__ void __launch_bounds__(TT, 1) attn_tc_kernel(
             const float p1 = ex2_approx(fmaf(x[i + 1], scale, -mm[e + 1]));
             l[i] += p0;
             l[i + 1] += p1;
-            const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-            const uint32_t hb = *reinterpret_cast<const uint32_t*>(&h2);
-            const __nv_bfloat162 l2 =
-                __floats2bfloat162_rn(p0 - __uint_as_float(hb << 16), p1 - __uint_as_float(hb & 0xffff0000u));
-            hi[e >> 1] = hb;
+            // hi = p truncated to bf16 (its top 16 bits), lo = the exact
+            // remainder rounded to bf16: hi + lo keeps ~15 bits of p
+            const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+            const __nv_bfloat162 l2 = __floats2bfloat162_rn(p0 - __uint_as_float(b0 & 0xffff0000u),
+                                                            p1 - __uint_as_float(b1 & 0xffff0000u));
+            hi[e >> 1] = __byte_perm(b0, b1, 0x7632);
             lo[e >> 1] = *reinterpret_cast<const uint32_t*>(&l2);
           }
         } else {

@@ -66,6 +66,9 @@ def args_(argv=None):
     p.add_argument("--context", type=int, default=0, help="context override (30B-A3B sweep points)")
     p.add_argument("--sweep", action="store_true", help="one line per workload and sweep point")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--attention", choices=["auto", "cluster", "tc"], default="auto",
+                   help="attention kernel (a diagnostic switch through the test library): the library's "
+                        "choice, the mma.sync cluster kernel, or the tcgen05 kernel wherever it applies")
     p.add_argument("--profile-steps", type=int, default=0,
                    help="for profiler captures: run this many eager steps after two warm-up steps, each inside "
                         "an NVTX range named 'step', and exit (no timing, no JSON line)")
@@ -673,6 +676,9 @@ def main():
         import torch
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         torch.distributed.init_process_group("nccl")
+    if a.attention != "auto":
+        from block_speculative_decoding_dflash2_gb300 import binding as B
+        B.dflash2_test_force_attention({"cluster": 1, "tc": 2}[a.attention])
     points = sweep_points() if a.sweep else [(a.workload, a.batch, a.context)]
     if a.sweep and "--steps" not in sys.argv:
         a.steps = SWEEP_STEPS

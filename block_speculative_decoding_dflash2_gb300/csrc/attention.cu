@@ -786,9 +786,14 @@ int launch_attention(int dtype, const void* q, const void* kb, const void* vb, c
   const int nrb = (R + 15) / 16;
   const int mode = g_attn_mode.load();
   // the tcgen05 kernel where it was measured faster: more than 32 query rows
-  // per kv head (the 27B and 30B-A3B shapes: +8% and +7..37% per step); at
-  // 32 rows (the 8B shapes) the mma.sync cluster kernel is as fast or faster
-  if ((mode == 2 || (mode == 0 && R > 32)) && attention_tc_fits(dtype, d, page_size, R)) {
+  // per kv head and chunks of at least 1024 keys per CTA (27B b=8 ctx 8192:
+  // +8% per step; 30B-A3B ctx 8192: +2% at b=1, +8% at b=8, +27% at b=64,
+  // +37% at b=256).  With shorter chunks (every 1k-context point, 258-516
+  // keys per CTA) and at 32 rows (the 8B shapes) the mma.sync cluster kernel
+  // is 1-4% faster: its per-CTA start-up is shorter.
+  const long ns = attn_cluster_ctas(max_ctx, B, batch, nkv, c.nsm);
+  const long chunk = ((long)max_ctx + B + ns - 1) / ns;
+  if ((mode == 2 || (mode == 0 && R > 32 && chunk >= 1024)) && attention_tc_fits(dtype, d, page_size, R)) {
     // (a page list too long for its shared memory: the cluster kernel below)
     const int rc = launch_attention_tc(q, kb, vb, kc, vc, block_table, max_pages, page_size, n_pages, ctx_len,
                                        new_off, batch, B, nq, nkv, max_ctx, window, o_out, c);

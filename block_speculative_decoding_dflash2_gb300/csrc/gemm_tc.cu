@@ -1183,6 +1183,12 @@ int pick_csplit(int tiles, int n_chunks, int bn, int epi, bool fp8, int nsm, int
     if (narrow && (long)tiles * cs * 4 < (long)nsm * 3) continue;
     if (max_clusters_of(bn, epi, fp8, cs) >= tiles) return cs;
   }
+  // so few narrow tiles that no split fills three quarters of the SMs (at
+  // most 18 tiles): the widest split with at least two K chunks per slice
+  // still beats stream-K, whose pieces meet through global memory
+  if (narrow)
+    for (int cs = std::min(8, n_chunks / 2); cs >= 2; --cs)
+      if ((long)tiles * cs <= nsm && max_clusters_of(bn, epi, fp8, cs) >= tiles) return cs;
   return 1;
 }
 

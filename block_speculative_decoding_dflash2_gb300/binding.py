@@ -93,6 +93,8 @@ def testing_lib():
         T.dflash2_test_force_cluster_split.argtypes = [I]
         T.dflash2_test_force_attention.restype = I
         T.dflash2_test_force_attention.argtypes = [I]
+        T.dflash2_test_last_attention.restype = I
+        T.dflash2_test_last_attention.argtypes = []
         T.dflash2_test_gemm_fp8.argtypes = [P, P, I, I, P, I, I, I, P, P, S, P]
         T.dflash2_test_layout.restype = I
         T.dflash2_test_layout.argtypes = [F(Config), I, I, I, F(ctypes.c_size_t), I]
@@ -367,6 +369,12 @@ def dflash2_test_force_attention(mode):
     """Attention kernel of later draft steps: 0 the library's choice, 1 the
     mma.sync cluster kernel, 2 the tcgen05 kernel wherever it applies."""
     _check("dflash2_test_force_attention", testing_lib().dflash2_test_force_attention(int(mode)))
+
+
+def dflash2_test_last_attention():
+    """Attention kernel of the last draft step: 1 mma.sync cluster, 2
+    tcgen05, 3 SIMT (0 before any)."""
+    return int(testing_lib().dflash2_test_last_attention())
 
 
 def dflash2_test_gemm_fp8(W8, scale, X, ctas, out, workspace, accumulate=False, stream=None):

@@ -764,7 +764,9 @@ int attn_cluster_ctas(int max_ctx, int B, int batch, int nkv, int nsm) {
 }
 
 std::atomic<int> g_attn_mode{0};
+std::atomic<int> g_attn_last{0};
 void attention_force_mode(int mode) { g_attn_mode.store(mode); }
+int attention_last_kernel() { return g_attn_last.load(); }
 
 // Upper bound over every batch <= max_batch and SM count <= kMaxSM (the
 // chunk grows with the SM count's inverse, so kMaxSM gives the most chunks).
@@ -797,9 +799,13 @@ int launch_attention(int dtype, const void* q, const void* kb, const void* vb, c
     // (a page list too long for its shared memory: the cluster kernel below)
     const int rc = launch_attention_tc(q, kb, vb, kc, vc, block_table, max_pages, page_size, n_pages, ctx_len,
                                        new_off, batch, B, nq, nkv, max_ctx, window, o_out, c);
-    if (rc != DFLASH2_ERR_SHAPE) return rc;
+    if (rc != DFLASH2_ERR_SHAPE) {
+      g_attn_last.store(2);
+      return rc;
+    }
   }
   if (dtype == DFLASH2_BF16 && (d == 64 || d == 128) && nrb <= CLW) {  // a warp per (row block, key share)
+    g_attn_last.store(1);
     const bf16 *q_ = static_cast<const bf16*>(q), *kb_ = static_cast<const bf16*>(kb),
                *vb_ = static_cast<const bf16*>(vb), *kc_ = static_cast<const bf16*>(kc),
                *vc_ = static_cast<const bf16*>(vc);
@@ -812,6 +818,7 @@ int launch_attention(int dtype, const void* q, const void* kb, const void* vb, c
   }
   // SIMT path (fp32 storage, or row counts beyond the tensor-core kernel):
   // key-chunk partials in global memory, then the combine kernel
+  g_attn_last.store(3);
   const int ch = chunk_of(max_ctx, B, batch, nkv, c.nsm);
   const int nsplit = (max_ctx + B + ch - 1) / ch;
   const size_t smem = attn_smem(R, d);

@@ -233,6 +233,7 @@ int attn_cluster_ctas(int max_ctx, int B, int batch, int nkv, int nsm);
 // test hook: 0 = the library's choice, 1 = the mma.sync cluster kernel,
 // 2 = the tcgen05 kernel wherever it applies
 void attention_force_mode(int mode);
+int attention_last_kernel();  // test hook: 1 mma.sync cluster, 2 tcgen05, 3 SIMT (0 before any launch)
 // tcgen05 attention (attention_tc.cu): bf16 storage, head dimension 128,
 // 16-key pages, at most 80 query rows per kv head
 bool attention_tc_fits(int dtype, int d, int page_size, int R);

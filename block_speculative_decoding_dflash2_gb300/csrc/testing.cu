@@ -107,6 +107,8 @@ int dflash2_test_force_attention(int mode) {
   return 0;
 }
 
+int dflash2_test_last_attention(void) { return df2::attention_last_kernel(); }
+
 int dflash2_test_layout(const dflash2_config* cfg, int batch, int n_new, int max_ctx, size_t* offsets, int n) {
   return workspace_offsets(cfg, batch, n_new, max_ctx, offsets, n);
 }

@@ -69,6 +69,13 @@ int dflash2_test_force_cluster_split(int cs);
  * against concurrent draft steps.
  */
 int dflash2_test_force_attention(int mode);
+
+/*
+ * The attention kernel the last bf16 or fp32 draft step of this process
+ * launched: 1 the mma.sync cluster kernel, 2 the tcgen05 kernel, 3 the SIMT
+ * partial + combine kernels; 0 before any.
+ */
+int dflash2_test_last_attention(void);
 int dflash2_test_gemm(int dtype, const void *W, int M, int K, const void *X, int N, int ctas, int accumulate,
                       float *out, void *workspace, size_t ws_bytes, void *stream);
 

@@ -70,6 +70,22 @@ def test_tc_attention_long_chunks(name):
     run_stagewise(case)
 
 
+def test_library_attention_choice():
+    """The library's own choice: tcgen05 for more than 32 rows per kv head
+    and chunks of at least 1024 keys per CTA, else the mma.sync kernel."""
+    B = lib()
+    # 80 rows, one 9000-key sequence (8 chunks of ~1130 keys): tcgen05
+    case = Case(_cfg("r80", 4), ctx_lens=[9000], n_new=[2], seed=95).run_gpu()
+    assert case.status == 0 and B.dflash2_test_last_attention() == 2
+    run_stagewise(case)
+    # 80 rows, short context (chunks of ~130 keys): mma.sync
+    case = Case(_cfg("r80", 4), ctx_lens=[1000], n_new=[2], seed=96).run_gpu()
+    assert case.status == 0 and B.dflash2_test_last_attention() == 1
+    # 32 rows, long context: mma.sync
+    case = Case(_cfg("r32", 1), ctx_lens=[9000], n_new=[2], seed=97).run_gpu()
+    assert case.status == 0 and B.dflash2_test_last_attention() == 1
+
+
 def test_tc_attention_end_to_end():
     case = _run(_cfg("r80", 4), 2, [2047, 16, 500], [16, 1, 7], 80)
     run_stagewise(case)

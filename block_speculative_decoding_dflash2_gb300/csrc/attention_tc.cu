@@ -94,7 +94,7 @@ __device__ __forceinline__ bool sm_bar_or(bool pred) {
 }
 
 // 2^x by the special-function unit (ex2.approx: relative error near 2^-22,
-// far below the 2^-16 the hi + lo split of P keeps; 2^-inf = 0)
+// far below the ~2^-15 the hi + lo split of P keeps; 2^-inf = 0)
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -177,9 +177,13 @@ def _topk_run(dtype, W, X, k, mult=1.0, cap=0.0):
 @pytest.mark.parametrize("dtype,M,N,k", [
     ("bf16", 1000, 7, 4), ("bf16", 1000, 16, 16), ("bf16", 4096 + 50, 40, 16), ("bf16", 2000, 300, 8),
     ("bf16", 151936, 7, 16), ("f32", 4096, 7, 4), ("f32", 3000, 9, 16),
+    # 209..224 rows in one 256-wide tile (224 = the 8B batch-32 block; 209
+    # ragged), K = 1024: 16 chunks a tile, so the ring wraps within a tile;
+    # 20000 rows: 157 tiles, some CTAs take two
+    ("bf16", 20000, 224, 16), ("bf16", 2500, 209, 8),
 ])
 def test_lm_head_topk_component_parity(dtype, M, N, k):
-    K = 256
+    K = 1024 if N > 208 else 256
     W = _mat(M, K, 5, 0.05, dtype)
     X = _mat(N, K, 6, 1.0, dtype)
     cid, cz, dbg = _topk_run(1 if dtype == "bf16" else 0, W, X, k)

@@ -70,6 +70,27 @@ def test_tc_attention_long_chunks(name):
     run_stagewise(case)
 
 
+def test_tc_attention_flags_bad_page():
+    """A block-table entry outside [0, n_pages) is flagged, not read: a whole
+    page inside a chunk (the TMA path) and the last, partial page (the row
+    path); the kernel zero-fills those rows and the step completes."""
+    import torch
+    B = lib()
+    B.dflash2_test_force_attention(2)
+    try:
+        case = Case(_cfg("r80", 4), ctx_lens=[700, 300], n_new=[2, 2], seed=98)
+        case.run_gpu()
+        assert case.status == 0
+        r = case.runner
+        r.block_table[0, 3] = r.n_pages + 5  # keys 48..63 of sequence 0
+        r.block_table[1, 18] = -7             # keys 288..303 of sequence 1 (its last page)
+        case.run_gpu()
+        assert case.status & B.DEV_BAD_PAGE
+        torch.cuda.synchronize()
+    finally:
+        B.dflash2_test_force_attention(0)
+
+
 def test_library_attention_choice():
     """The library's own choice: tcgen05 for more than 32 rows per kv head
     and chunks of at least 1024 keys per CTA, else the mma.sync kernel."""

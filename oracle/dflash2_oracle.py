@@ -156,8 +156,8 @@ def project_features(cfg, W, taps, st):
     [Train] "What is DFlash?": the draft reads hidden states tapped from the
     frozen target at target_layer_ids, mapped by a trained projection;
     [vLLM] "DFlash2 inference": dflash_config carries target_layer_ids.  taps [n, T*H] is the concatenation of the T tapped
-    hidden states in target_layer_ids order.  Parity unpinned beyond the
-    special cases in the pin tests (identity blocks select one tap).
+    hidden states in target_layer_ids order.  Pinned by identity and
+    permutation blocks (which tap, which orientation, which gain).
     """
     x = _f64(taps) @ _f64(W["fc"]).T
     return st(rms_norm(x, W["hidden_norm"], cfg["rms_eps"]))

@@ -204,6 +204,29 @@ def test_feature_projection_identity_blocks_select_taps():
                                    rtol=1e-12)
 
 
+def test_feature_projection_permutation_block_fixes_orientation():
+    """project_features: W_fc holding a non-symmetric permutation P in tap
+    block t gives x = tap_t P^T, i.e. x[:, i] = tap_t[:, pi(i)], then the
+    hidden_norm gain.  A transposed operand would read pi^-1 instead (pi
+    below has no fixed points and is not an involution), a wrong block
+    offset another tap, and the final norm's gain a different scale."""
+    cfg = tiny_cfg()
+    W = tiny_weights(cfg)
+    H, T = cfg["hidden"], cfg["n_taps"]
+    pi = np.roll(np.arange(H), 3)  # i -> i - 3 (mod H)
+    g = np.random.default_rng(18)
+    taps = g.standard_normal((4, T * H))
+    st = O.Store(False)
+    for t in range(T):
+        W["fc"] = np.zeros((H, T * H))
+        W["fc"][np.arange(H), t * H + pi] = 1.0
+        f = O.project_features(cfg, W, taps, st)
+        want = O.rms_norm(taps[:, t * H:(t + 1) * H][:, pi], W["hidden_norm"], 1e-6)
+        np.testing.assert_allclose(f, want, rtol=1e-12)
+        wrong = O.rms_norm(taps[:, t * H:(t + 1) * H][:, np.argsort(pi)], W["hidden_norm"], 1e-6)
+        assert not np.allclose(f, wrong)
+
+
 def test_context_kv_identity_projection():
     cfg = tiny_cfg(hidden=32, n_q_heads=2, n_kv_heads=1, head_dim=16)
     H, d = 32, 16
@@ -415,6 +438,27 @@ def test_draft_block_softcap_and_multiplier():
     z3 = O.draft_block(dict(cfg, final_logit_softcap=0.5), W, 3, ctx, st)
     np.testing.assert_allclose(z3, 0.5 * np.tanh(z / 0.5), rtol=1e-13)
     assert np.all(np.abs(z3) < 0.5)
+
+
+def test_draft_block_readout_rows_and_gain():
+    """draft_block's readout z[v] = mult * sum_i lm_head[v, i] * hn[i], hn the
+    final-normed rows: permuting the rows of lm_head permutes the logits the
+    same way (vocab index = row index), the readout is additive in lm_head,
+    and scaling final_norm's gain by c scales every logit by c."""
+    cfg = tiny_cfg()
+    W = tiny_weights(cfg)
+    st = O.Store(False)
+    ctx = O.append_context(cfg, W, empty_ctx(cfg), np.ones((2, cfg["n_taps"] * cfg["hidden"])), 0, st)
+    z = O.draft_block(cfg, W, 3, ctx, st)
+    perm = np.random.default_rng(19).permutation(cfg["vocab"])
+    zp = O.draft_block(cfg, dict(W, lm_head=W["lm_head"][perm]), 3, ctx, st)
+    np.testing.assert_allclose(zp, z[:, perm], rtol=1e-12, atol=1e-14)
+    L2 = np.random.default_rng(20).standard_normal(W["lm_head"].shape)
+    za = O.draft_block(cfg, dict(W, lm_head=L2), 3, ctx, st)
+    zs = O.draft_block(cfg, dict(W, lm_head=W["lm_head"] + L2), 3, ctx, st)
+    np.testing.assert_allclose(zs, z + za, rtol=1e-10, atol=1e-12)
+    zc = O.draft_block(cfg, dict(W, final_norm=3.0 * W["final_norm"]), 3, ctx, st)
+    np.testing.assert_allclose(zc, 3.0 * z, rtol=1e-12, atol=1e-14)
 
 
 def test_draft_block_anchor_is_the_only_non_mask_token():

@@ -242,6 +242,25 @@ def test_context_kv_identity_projection():
                                                cfg["rope_theta"])[:, 0], rtol=1e-12)
 
 
+def test_context_kv_permutation_blocks_fix_orientation():
+    """context_kv: permutation blocks in W_k and W_v (no fixed points, not
+    involutions) give V = f[:, d + pi] and K = RoPE(RMSNorm_k(f[:, pi])): a
+    transposed projection would read pi^-1."""
+    cfg = tiny_cfg(hidden=32, n_q_heads=2, n_kv_heads=1, head_dim=16)
+    H, d = 32, 16
+    pi = np.roll(np.arange(d), 5)
+    Wl = {"qkv": np.zeros((4 * d, H)), "k_norm": 0.5 + np.arange(d) / d}
+    Wl["qkv"][2 * d + np.arange(d), pi] = 1.0       # W_k reads f[:, pi]
+    Wl["qkv"][3 * d + np.arange(d), d + pi] = 1.0   # W_v reads f[:, 16 + pi]
+    f = np.random.default_rng(29).standard_normal((5, H))
+    pos = np.array([0, 1, 7, 64, 1000])
+    k, v = O.context_kv(cfg, Wl, f, pos, O.Store(False))
+    np.testing.assert_allclose(v[:, 0], f[:, d + pi], rtol=1e-15)
+    want = O.rope(O.rms_norm(f[:, None, pi], Wl["k_norm"], 1e-6), pos, cfg["rope_theta"])[:, 0]
+    np.testing.assert_allclose(k[:, 0], want, rtol=1e-12)
+    assert not np.allclose(v[:, 0], f[:, d + np.argsort(pi)])
+
+
 # ---------------------------------------------------------------- draft block
 
 def test_draft_layer_residual_identity_when_outputs_zero():

@@ -584,6 +584,24 @@ def test_selector_two_position_hand_example():
     assert abs(s - (l1 + l2)) < 1e-14
 
 
+def test_selector_factor_roles_are_not_swapped():
+    """selector_factors: rows 0..r-1 of W_sel (W_a) factor the predecessor and
+    rows r..2r-1 (W_b) the candidate.  With E[t] = [t, 1], W_a = [1, 0] and
+    W_b = [0, 1] the pairwise term is the predecessor's value p, the same for
+    every candidate of a position, so the path is the per-position argmax of
+    the logits; with the roles swapped it would be the candidate's value and
+    the larger ids would win."""
+    cfg = dict(selector_rank=1)
+    W = {"embed": np.stack([np.arange(10.0), np.ones(10)], 1), "sel": np.array([[1.0, 0.0], [0.0, 1.0]])}
+    cand = np.array([[2, 9], [5, 8]])
+    z = np.array([[1.0, 0.0], [1.0, 0.0]])
+    p, idx, s = O.select_path(cfg, W, 3, cand, z)
+    assert list(p) == [2, 5]
+    assert abs(s - 2 * (1.0 - math.log(math.e + 1.0))) < 1e-14
+    a, b = O.selector_factors(cfg, W, np.array([7]))
+    assert a[0, 0] == 7.0 and b[0, 0] == 1.0
+
+
 def test_selector_ties_pick_smallest_indices():
     cfg = dict(selector_rank=1)
     W = {"embed": np.zeros((10, 1)), "sel": np.zeros((2, 1))}

@@ -99,6 +99,17 @@ def test_rope_d2_is_a_plane_rotation_by_pos_radians():
         np.testing.assert_allclose(y, [0.3 * c + 1.2 * s, -1.2 * c + 0.3 * s], rtol=1e-12, atol=1e-15)
 
 
+def test_rope_pair_frequencies_follow_theta_power():
+    """rope: pair i rotates by pos * theta^(-2i/d).  At d = 4, theta = 100:
+    pair (0, 2) by pos radians, pair (1, 3) by pos / 10 radians; a unit
+    vector in x1 shows that second angle directly."""
+    e1 = np.zeros((1, 1, 4)); e1[0, 0, 1] = 1.0
+    for pos in (1, 3, 40):
+        y = O.rope(e1, np.array([pos]), 100.0)[0, 0]
+        a = pos / 10.0
+        np.testing.assert_allclose(y, [0.0, math.cos(a), 0.0, math.sin(a)], rtol=1e-12, atol=1e-15)
+
+
 def test_rope_relative_position_and_norm():
     g = np.random.default_rng(3)
     q = g.standard_normal((1, 1, 64))
@@ -383,6 +394,44 @@ def test_draft_layer_mlp_is_silu_gate_times_up_on_post_attention_rows():
     assert np.max(np.abs(swapped - want)) > 1e-3
 
 
+def test_draft_layer_each_sublayer_uses_its_own_tap_generator():
+    """draft_layer: the attention sublayer's conv reads tapgen_attn and the
+    MLP's tapgen_mlp.  With a random attention generator and a zero MLP
+    generator, the MLP pin above still holds with the attention rows formed
+    by dynamic_conv(u, tapgen_attn) (pinned on its own) and the MLP rows by
+    the two-tap average; using one generator for both sublayers fails it."""
+    cfg = tiny_cfg()
+    W = tiny_weights(cfg, seed=6)
+    H, nq, nkv, d, I = (cfg[k] for k in ("hidden", "n_q_heads", "n_kv_heads", "head_dim", "intermediate"))
+    i, j, m = 5, 2, 9
+    Wl = dict(W["layers"][0])
+    Wl["tapgen_attn"] = 2.0 * np.random.default_rng(40).standard_normal(Wl["tapgen_attn"].shape)
+    Wl["tapgen_mlp"] = np.zeros_like(Wl["tapgen_mlp"])
+    qkv = Wl["qkv"].copy()
+    qkv[nq * d:(nq + nkv) * d] = 0.0
+    qkv[(nq + nkv) * d:] = np.eye(nkv * d, H)
+    Wl["qkv"] = qkv
+    Wl["o"] = 0.7 * np.eye(H, nq * d) * (np.arange(H) < d)[:, None]
+    gu = np.zeros((2 * I, H))
+    gu[0, i] = 1.0
+    gu[I, j] = 1.0
+    Wl["gate_up"] = gu
+    down = np.zeros((H, I))
+    down[m, 0] = 1.0
+    Wl["down"] = down
+    h = np.random.default_rng(41).standard_normal((4, H))
+    out = O.draft_layer(cfg, Wl, h, *empty_ctx(cfg)[0], np.arange(4), O.Store(False))
+    eps = cfg["rms_eps"]
+    u = _rms_rows(h, Wl["attn_norm"], eps)
+    ua = u + O.dynamic_conv(u, Wl["tapgen_attn"], cfg["conv_group_size"], cfg["conv_kernel_size"])
+    h1 = h.copy()
+    h1[:, :d] += 0.7 * ua[:, :d].mean(axis=0)
+    um = _left_avg_conv_input(_rms_rows(h1, Wl["mlp_norm"], eps))
+    want = h1.copy()
+    want[:, m] += um[:, i] / (1.0 + np.exp(-um[:, i])) * um[:, j]
+    np.testing.assert_allclose(out, want, rtol=1e-12, atol=1e-12)
+
+
 def test_v1_layer_without_conv_mixes_rows_only_through_attention():
     # conv_kernel_size 0 (DFlash v1): with the attention output switched off
     # (W_o = 0) every row is processed alone, so changing row 1 leaves rows
@@ -478,6 +527,20 @@ def test_draft_block_readout_rows_and_gain():
     np.testing.assert_allclose(zs, z + za, rtol=1e-10, atol=1e-12)
     zc = O.draft_block(cfg, dict(W, final_norm=3.0 * W["final_norm"]), 3, ctx, st)
     np.testing.assert_allclose(zc, 3.0 * z, rtol=1e-12, atol=1e-14)
+
+
+def test_draft_block_input_embedding_scale_scales_the_embedded_rows():
+    """draft_block: input_embedding_scale c multiplies the embedded block rows,
+    so the logits equal those of a table of c-scaled embeddings at scale 1
+    (the residual stream carries the scale; dropping it changes the logits)."""
+    cfg = tiny_cfg()
+    W = tiny_weights(cfg)
+    st = O.Store(False)
+    ctx = O.append_context(cfg, W, empty_ctx(cfg), np.ones((2, cfg["n_taps"] * cfg["hidden"])), 0, st)
+    zc = O.draft_block(dict(cfg, input_embedding_scale=3.0), W, 3, ctx, st)
+    ze = O.draft_block(cfg, dict(W, embed=3.0 * W["embed"]), 3, ctx, st)
+    np.testing.assert_allclose(zc, ze, rtol=1e-12, atol=1e-13)
+    assert not np.allclose(zc, O.draft_block(cfg, W, 3, ctx, st))
 
 
 def test_draft_block_anchor_is_the_only_non_mask_token():
@@ -637,6 +700,20 @@ def test_draft_p_min_cut_closed_form():
     # the cut and n_max together: at most n_max, then the cut
     p, idx, s = O.select_path_knobs(cfg, W, 0, cand, z, n_max=4, p_min=0.5)
     assert len(p) == 2
+
+
+def test_draft_p_min_keeps_a_transition_at_the_threshold():
+    """select_path_knobs: drafting stops at a transition whose probability is
+    below draft_p_min, so one exactly at it is kept.  Two equal candidates
+    per position make each transition exactly 1/2."""
+    cfg = dict(selector_rank=1)
+    W = {"embed": np.zeros((20, 1)), "sel": np.zeros((2, 1))}
+    cand = np.arange(8).reshape(4, 2)
+    z = np.zeros((4, 2))
+    p, idx, s = O.select_path_knobs(cfg, W, 0, cand, z, p_min=0.5)
+    assert len(p) == 4 and list(idx) == [0] * 4
+    p, idx, s = O.select_path_knobs(cfg, W, 0, cand, z, p_min=0.5 + 1e-9)
+    assert len(p) == 0
 
 
 def test_transition_logprobs_match_path_score():

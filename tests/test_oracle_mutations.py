@@ -51,9 +51,9 @@ MUTATIONS = [
     ("k_and_v_rows_swapped",
      "k = qkv[:, nq * d: (nq + nkv) * d].reshape(B, nkv, d)\n    v = qkv[:, (nq + nkv) * d:].reshape(B, nkv, d)",
      "v = qkv[:, nq * d: (nq + nkv) * d].reshape(B, nkv, d)\n    k = qkv[:, (nq + nkv) * d:].reshape(B, nkv, d)"),
-    ("values_rotated", "    v = st(v)\n", '    v = st(rope(v, pos, cfg["rope_theta"]))\n'),
-    ("q_norm_dropped", 'rms_norm(q, Wl["q_norm"], eps)', "(q)"),
-    ("k_norm_dropped", 'rms_norm(k, Wl["k_norm"], eps)', "(k)"),
+    ('values_rotated', '    v = st(v)\n', '    v = st(rope(v, pos, cfg["rope_theta"]))\n'),
+    ('q_norm_dropped', 'rms_norm(q, Wl["q_norm"], eps)', '(q)'),
+    ('k_norm_dropped', 'rms_norm(k, Wl["k_norm"], eps)', '(k)'),
     ("conv_correction_without_input", 'u2 = st(u + dynamic_conv(u, Wl["tapgen_attn"]',
      'u2 = st(0 * u + dynamic_conv(u, Wl["tapgen_attn"]'),
     ("attention_conv_reads_mlp_generator", 'u2 = st(u + dynamic_conv(u, Wl["tapgen_attn"], gs, kc)) if kc else u',
@@ -63,7 +63,7 @@ MUTATIONS = [
     ("mlp_norm_before_attention", '    u = st(rms_norm(h, Wl["mlp_norm"], eps))',
      '    u = st(rms_norm(h - O @ _f64(Wl["o"]).T, Wl["mlp_norm"], eps))'),
     ("gate_and_up_swapped", "act = st(silu(gu[:, :I]) * gu[:, I:])", "act = st(silu(gu[:, I:]) * gu[:, :I])"),
-    ("mlp_residual_dropped", 'return h + act @ _f64(Wl["down"]).T', 'return act @ _f64(Wl["down"]).T'),
+    ('mlp_residual_dropped', 'return h + act @ _f64(Wl["down"]).T', 'return act @ _f64(Wl["down"]).T'),
     ("window_off_by_one", "ctxK[max(0, ctxK.shape[0] - win):], ctxV[max(0, ctxV.shape[0] - win):]",
      "ctxK[max(0, ctxK.shape[0] - win + 1):], ctxV[max(0, ctxV.shape[0] - win + 1):]"),
     ("block_positions_from_zero", "pos = P + np.arange(B)", "pos = np.arange(B)"),
@@ -93,6 +93,67 @@ MUTATIONS = [
     ("rollback_count", "self.rollback += n - a", "self.rollback += n - a - 1"),
     ("mean_acceptance_without_bonus", "return 1.0 + self.accepted / self.steps if self.steps else 0.0",
      "return self.accepted / self.steps if self.steps else 0.0"),
+    ("bf16_truncates", "np.rint(np.ldexp(x, 8 - e))", "np.trunc(np.ldexp(x, 8 - e))"),
+    ("bf16_one_bit_short", "np.rint(np.ldexp(x, 8 - e)), e - 8", "np.rint(np.ldexp(x, 7 - e)), e - 7"),
+    ("bf16_subnormal_floor", "e = np.maximum(e, -125)", "e = np.maximum(e, -140)"),
+    ("silu_sign", "return x / (1.0 + np.exp(-x))", "return x / (1.0 + np.exp(x))"),
+    ("rms_over_rows", "ms = np.mean(x * x, axis=-1, keepdims=True)", "ms = np.mean(x * x, axis=0, keepdims=True)"),
+    ("conv_softmax_over_groups", "alpha = e / e.sum(axis=-1, keepdims=True)",
+     "alpha = e / e.sum(axis=1, keepdims=True)"),
+    ('features_unnormed', 'return st(rms_norm(x, W["hidden_norm"], cfg["rms_eps"]))', 'return st(x)'),
+    ("context_keys_with_q_norm",
+     'k = rope(rms_norm(k, Wl["k_norm"], cfg["rms_eps"]), np.asarray(pos), cfg["rope_theta"])',
+     'k = rope(rms_norm(k, Wl["q_norm"], cfg["rms_eps"]), np.asarray(pos), cfg["rope_theta"])'),
+    ("context_keys_unrotated",
+     'k = rope(rms_norm(k, Wl["k_norm"], cfg["rms_eps"]), np.asarray(pos), cfg["rope_theta"])',
+     'k = rms_norm(k, Wl["k_norm"], cfg["rms_eps"])'),
+    ("context_keys_unnormed", 'k = rope(rms_norm(k, Wl["k_norm"], cfg["rms_eps"]), np.asarray(pos), cfg["rope_theta"])',
+     'k = rope(k, np.asarray(pos), cfg["rope_theta"])'),
+    ("context_new_rows_prepended", "out.append((np.concatenate([K0, k], 0), np.concatenate([V0, v], 0)))",
+     "out.append((np.concatenate([k, K0], 0), np.concatenate([v, V0], 0)))"),
+    ("attention_reads_keys_as_values", "O[:, h, :] = p @ V[:, g, :]", "O[:, h, :] = p @ K[:, g, :]"),
+    ("block_keys_one_position_late", 'k = st(rope(rms_norm(k, Wl["k_norm"], eps), pos, cfg["rope_theta"]))',
+     'k = st(rope(rms_norm(k, Wl["k_norm"], eps), pos + 1, cfg["rope_theta"]))'),
+    ("queries_unrotated", 'q = st(rope(rms_norm(q, Wl["q_norm"], eps), pos, cfg["rope_theta"]))',
+     'q = st(rms_norm(q, Wl["q_norm"], eps))'),
+    ("block_all_anchor", 'toks = np.array([anchor] + [cfg["mask_token_id"]] * (B - 1), dtype=np.int64)',
+     "toks = np.array([anchor] * B, dtype=np.int64)"),
+    ("block_anchor_masked", 'toks = np.array([anchor] + [cfg["mask_token_id"]] * (B - 1), dtype=np.int64)',
+     'toks = np.array([cfg["mask_token_id"]] * B, dtype=np.int64)'),
+    ("softcap_unscaled", "z = cap * np.tanh(z / cap)", "z = np.tanh(z / cap)"),
+    ("softcap_inner_unscaled", "z = cap * np.tanh(z / cap)", "z = cap * np.tanh(z)"),
+    ("multiplier_after_cap",
+     'z = cfg["output_multiplier"] * (hn @ _f64(W["lm_head"]).T)\n    cap = cfg["final_logit_softcap"]\n'
+     '    if cap and cap > 0:\n        z = cap * np.tanh(z / cap)',
+     'z = (hn @ _f64(W["lm_head"]).T)\n    cap = cfg["final_logit_softcap"]\n'
+     '    if cap and cap > 0:\n        z = cap * np.tanh(z / cap)\n    z = cfg["output_multiplier"] * z'),
+    ("topk_skips_the_best", "ids[r] = order[:k]", "ids[r] = order[1:k + 1]"),
+    ("draft_step_appends_at_zero", "c = append_context(cfg, W, c, new_taps[s], P0, st)",
+     "c = append_context(cfg, W, c, new_taps[s], 0, st)"),
+    ("selector_first_unnormalised", "delta = S1 - _logsumexp(S1, 0)", "delta = S1"),
+    ("selector_pred_factor_wrong_position", "S = z[i][None, :] + Ac[i - 1] @ Bc[i].T",
+     "S = z[i][None, :] + Ac[i] @ Bc[i].T"),
+    ("selector_without_unary", "S = z[i][None, :] + Ac[i - 1] @ Bc[i].T", "S = Ac[i - 1] @ Bc[i].T"),
+    ("transitions_keep_anchor", "        prev_tok = int(cand_id[i, idx[i]])\n    return np.array(out)",
+     "        pass\n    return np.array(out)"),
+    ("path_score_keep_anchor", "        prev_tok = int(cand_id[i, idx[i]])\n    return total",
+     "        pass\n    return total"),
+    ("sampled_inverse_cdf_left", 'v = int(np.searchsorted(cdf, float(u_sample) * cdf[-1], side="right"))',
+     'v = int(np.searchsorted(cdf, float(u_sample) * cdf[-1], side="left"))'),
+    ("sampled_residual_unrenormalised", 'v = int(np.searchsorted(cdf, float(u_sample) * cdf[-1], side="right"))',
+     'v = int(np.searchsorted(cdf, float(u_sample), side="right"))'),
+    ("sampled_bonus_from_previous_row", "row = prob[a].copy()", "row = prob[max(a - 1, 0)].copy()"),
+    ("acceptance_by_position_off_by_one", "self.acc_pos[:a] += 1",
+     "self.acc_pos[:a + 1 if a < self.n_spec else a] += 1"),
+    ("histogram_counts_drafts", "self.hist[a] += 1", "self.hist[n - a] += 1"),
+    ("acceptance_rate_over_steps", "return self.accepted / self.drafted if self.drafted else 0.0",
+     "return self.accepted / self.steps if self.steps else 0.0"),
+    ("knobs_n_max_off_by_one", "n = len(cand_id) if n_max == 0 else n_max",
+     "n = len(cand_id) if n_max == 0 else n_max + 1"),
+    ("knobs_cut_after", "return toks[:keep], idx[:keep], float(np.sum(t[:keep]))",
+     "return toks[:keep + 1], idx[:keep + 1], float(np.sum(t[:keep + 1]))"),
+    ("spec_loop_anchor_not_next", "t = [toy_target_next(table, anchor)] + [toy_target_next(table, p) for p in path]",
+     "t = [toy_target_next(table, p) for p in path] + [toy_target_next(table, path[-1])]"),
 ]
 
 

@@ -469,6 +469,51 @@ def test_sliding_window_reads_only_the_last_context_positions():
     assert np.max(np.abs(O.draft_block(cw, W, 7, inside, st) - z5)) > 1e-9
 
 
+def test_context_appended_in_two_steps_equals_one_append():
+    """append_context, draft_step: committing positions 0..4 and then 5..11
+    leaves every layer's context rows in position order, the same as
+    committing 0..11 at once (the second append starts at the context's
+    length), and the step after it reads the same logits."""
+    cfg = tiny_cfg(n_layers=2)
+    W = tiny_weights(cfg)
+    taps = np.random.default_rng(23).standard_normal((12, cfg["n_taps"] * cfg["hidden"]))
+    st = O.Store(False)
+    once = O.append_context(cfg, W, empty_ctx(cfg), taps, 0, st)
+    first = O.append_context(cfg, W, empty_ctx(cfg), taps[:5], 0, st)
+    twice = O.append_context(cfg, W, first, taps[5:], 5, st)
+    c1, _, _, _ = O.draft_step(cfg, W, [empty_ctx(cfg)], [7], [taps[:5]], st)
+    c2, z2, _, _ = O.draft_step(cfg, W, c1, [7], [taps[5:]], st)
+    for l in range(cfg["n_layers"]):
+        for i in range(2):
+            np.testing.assert_allclose(twice[l][i], once[l][i], rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(c2[0][l][i], once[l][i], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(z2[0], O.draft_block(cfg, W, 7, once, st), rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("kc", [0, 2])
+def test_block_keys_sit_where_context_keys_at_the_same_positions_would(kc):
+    """draft_layer, context_kv: the block's own keys and values are the
+    context's projection, norm and rotation applied to the attention input.
+    Context rows built by context_kv from that input at the block's own
+    positions repeat the block's keys and values exactly; every key then
+    appears twice with the same value, which leaves each query's attention
+    output unchanged, so the layer equals the one with an empty context.  The
+    same rows one position later do change it."""
+    cfg = tiny_cfg(conv_kernel_size=kc)
+    W = tiny_weights(cfg)
+    Wl = W["layers"][0]
+    h = np.random.default_rng(24).standard_normal((cfg["block_size"], cfg["hidden"]))
+    pos = 9 + np.arange(cfg["block_size"])
+    st = O.Store(False)
+    u = O.rms_norm(h, Wl["attn_norm"], cfg["rms_eps"])
+    u2 = u + O.dynamic_conv(u, Wl["tapgen_attn"], cfg["conv_group_size"], kc) if kc else u
+    alone = O.draft_layer(cfg, Wl, h, *empty_ctx(cfg)[0], pos, st)
+    K, V = O.context_kv(cfg, Wl, u2, pos, st)
+    np.testing.assert_allclose(O.draft_layer(cfg, Wl, h, K, V, pos, st), alone, rtol=1e-10, atol=1e-12)
+    K1, V1 = O.context_kv(cfg, Wl, u2, pos + 1, st)
+    assert np.max(np.abs(O.draft_layer(cfg, Wl, h, K1, V1, pos, st) - alone)) > 1e-6
+
+
 def test_draft_block_invariant_to_common_position_shift():
     # scores depend on relative positions only: shifting the context's and the
     # block's positions together leaves the logits unchanged (anchor at P).
@@ -506,6 +551,11 @@ def test_draft_block_softcap_and_multiplier():
     z3 = O.draft_block(dict(cfg, final_logit_softcap=0.5), W, 3, ctx, st)
     np.testing.assert_allclose(z3, 0.5 * np.tanh(z / 0.5), rtol=1e-13)
     assert np.all(np.abs(z3) < 0.5)
+    # both set: the multiplier scales the raw logits and the cap bounds the
+    # product (a cap applied first and scaled after would exceed the cap)
+    z4 = O.draft_block(dict(cfg, output_multiplier=2.5, final_logit_softcap=0.5), W, 3, ctx, st)
+    np.testing.assert_allclose(z4, 0.5 * np.tanh(2.5 * z / 0.5), rtol=1e-13)
+    assert np.all(np.abs(z4) <= 0.5)
 
 
 def test_draft_block_readout_rows_and_gain():
@@ -775,6 +825,19 @@ def test_sampled_verify_hand_cases():
     assert O.verify_sampled([1, 2], prob, [0.6, 0.0], 0.5) == (0, [2], 2)
 
 
+def test_sampled_verify_never_draws_a_zero_probability_token():
+    """verify_sampled: the draw is the first token whose cumulative mass
+    exceeds u times the total, so a token with no mass is never emitted, not
+    even at u = 0, in a residual row and in a bonus row alike."""
+    prob = np.array([[0.0, 0.0, 0.5, 0.5, 0.0], [0.0, 0.25, 0.0, 0.75, 0.0]])
+    # draft 2 rejected (0.9 is not below 0.5): residual [0, 0, 0, 0.5, 0]
+    assert O.verify_sampled([2], prob, [0.9], 0.0) == (0, [3], 3)
+    # draft 2 accepted: the bonus from row 1, whose first token with mass is 1
+    assert O.verify_sampled([2], prob, [0.1], 0.0) == (1, [2, 1], 1)
+    # u just below 1 draws the last token with mass
+    assert O.verify_sampled([2], prob, [0.1], 1.0 - 1e-12) == (1, [2, 3], 3)
+
+
 def test_counters_with_fewer_drafts():
     # drafted counts the drafts kept; rollback = drafted - accepted
     c = O.Counters(7)
@@ -782,6 +845,11 @@ def test_counters_with_fewer_drafts():
         c.add(a, n)
     assert c.drafted == 14 and c.accepted == 10 and c.rollback == 4 and c.steps == 4
     assert list(c.hist[:8]) == [1, 1, 1, 0, 0, 0, 0, 1]
+    # acceptance rate = accepted / drafted ([NIM] "Observe Acceptance");
+    # mean acceptance length counts the target's own token: 1 + 10 / 4
+    assert c.acceptance_rate == 10 / 14
+    assert c.mean_acceptance_length == 3.5
+    assert list(c.acc_pos) == [3, 2, 1, 1, 1, 1, 1]
 
 
 def test_counter_identities():

@@ -2,7 +2,8 @@
 
 Each case plants one single-point mistake in a copy of the oracle's source
 (a dropped term or gain, a wrong sign, index, axis or offset, a transposed or
-swapped operand, swapped roles, an off-by-one, a boundary moved), builds the
+swapped operand, swapped roles, an off-by-one, a boundary moved, a bf16
+storage point dropped or added), builds the
 copy as a module on the CPU, and runs every pin of tests/test_oracle_pins.py
 against it: at least one pin must fail.  The oracle itself is untouched.
 """
@@ -154,6 +155,19 @@ MUTATIONS = [
      "return toks[:keep + 1], idx[:keep + 1], float(np.sum(t[:keep + 1]))"),
     ("spec_loop_anchor_not_next", "t = [toy_target_next(table, anchor)] + [toy_target_next(table, p) for p in path]",
      "t = [toy_target_next(table, p) for p in path] + [toy_target_next(table, path[-1])]"),
+    ("values_not_stored", "    v = st(v)\n", ""),
+    ("activation_not_stored", "act = st(silu(gu[:, :I]) * gu[:, I:])", "act = silu(gu[:, :I]) * gu[:, I:]"),
+    ("readout_rows_not_stored", 'hn = st(rms_norm(h[1:], W["final_norm"], cfg["rms_eps"]))',
+     'hn = rms_norm(h[1:], W["final_norm"], cfg["rms_eps"])'),
+    ("residual_stored", 'h = h + O @ _f64(Wl["o"]).T', 'h = st(h + O @ _f64(Wl["o"]).T)'),
+    ("features_not_stored", 'return st(rms_norm(x, W["hidden_norm"], cfg["rms_eps"]))',
+     'return rms_norm(x, W["hidden_norm"], cfg["rms_eps"])'),
+    ("attention_output_not_stored", "O = st(block_attention(q, ctxK, ctxV, k, v)).reshape(B, nq * d)",
+     "O = block_attention(q, ctxK, ctxV, k, v).reshape(B, nq * d)"),
+    ("logits_stored", 'z = cfg["output_multiplier"] * (hn @ _f64(W["lm_head"]).T)',
+     'z = st(cfg["output_multiplier"] * (hn @ _f64(W["lm_head"]).T))'),
+    ("mlp_input_not_stored", '    u = st(rms_norm(h, Wl["mlp_norm"], eps))', '    u = rms_norm(h, Wl["mlp_norm"], eps)'),
+    ("context_values_not_stored", "    return st(k), st(v)", "    return st(k), v"),
 ]
 
 

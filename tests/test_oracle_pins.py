@@ -943,3 +943,32 @@ def test_bf16_storage_mode_rounds_block_outputs():
     z64 = O.draft_block(cfg, W, 5, O.append_context(cfg, W, empty_ctx(cfg), taps, 0, O.Store(False)),
                         O.Store(False))
     assert 0 < np.max(np.abs(z16 - z64)) < 0.2
+
+
+@pytest.mark.parametrize("kc", [0, 2])
+def test_storage_points_are_the_listed_tensors(kc):
+    """Store: in bf16 mode the oracle rounds exactly the tensors that the
+    precision reading lists, in the order the step makes them, and nothing
+    else (the residual stream and the logits stay float64): the features;
+    each layer's context K and V; per layer the attention input u and, with
+    the conv, u'; q, k, v; the attention output; the MLP input u and u'; the
+    MLP activation; then the final-normed rows."""
+    shapes = []
+
+    class Spy(O.Store):
+        def __call__(self, x):
+            shapes.append(np.shape(x))
+            return O.Store.__call__(self, x)
+
+    cfg = tiny_cfg(n_layers=2, conv_kernel_size=kc)
+    W = tiny_weights(cfg)
+    H, I, B = cfg["hidden"], cfg["intermediate"], cfg["block_size"]
+    nq, nkv, d = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
+    taps = O.bf16_round(np.random.default_rng(25).standard_normal((5, cfg["n_taps"] * H)))
+    ctx = O.append_context(cfg, W, empty_ctx(cfg), taps, 0, Spy(True))
+    assert shapes == [(5, H)] + [(5, nkv, d), (5, nkv, d)] * 2
+    shapes.clear()
+    O.draft_block(cfg, W, 5, ctx, Spy(True))
+    conv = [(B, H)] if kc else []
+    layer = [(B, H)] + conv + [(B, nq, d), (B, nkv, d), (B, nkv, d), (B, nq, d)] + [(B, H)] + conv + [(B, I)]
+    assert shapes == layer * 2 + [(B - 1, H)]

@@ -166,8 +166,45 @@ MUTATIONS = [
      "O = block_attention(q, ctxK, ctxV, k, v).reshape(B, nq * d)"),
     ("logits_stored", 'z = cfg["output_multiplier"] * (hn @ _f64(W["lm_head"]).T)',
      'z = st(cfg["output_multiplier"] * (hn @ _f64(W["lm_head"]).T))'),
-    ("mlp_input_not_stored", '    u = st(rms_norm(h, Wl["mlp_norm"], eps))', '    u = rms_norm(h, Wl["mlp_norm"], eps)'),
+    ("mlp_input_not_stored", '    u = st(rms_norm(h, Wl["mlp_norm"], eps))',
+     '    u = rms_norm(h, Wl["mlp_norm"], eps)'),
     ("context_values_not_stored", "    return st(k), st(v)", "    return st(k), v"),
+    ("topk_values_of_wrong_ids", "vals = np.take_along_axis(flat, ids, axis=1)",
+     "vals = -np.sort(-flat, axis=1)[:, ::-1][:, :k]"),
+    ("greedy_skips_first", "        t = toy_target_next(table, t)\n        out.append(t)",
+     "        out.append(t)\n        t = toy_target_next(table, t)"),
+    ("spec_loop_first_anchor_is_prompt", "    anchor = toy_target_next(table, prompt_last)\n    out.append(anchor)",
+     "    anchor = int(prompt_last)\n    out.append(anchor)"),
+    ("verify_all_accepted_no_bonus",
+     "    while a < D and path[a] == target[a]:\n        a += 1\n    return a, path[:a] + [target[a]], target[a]",
+     "    while a < D and path[a] == target[a]:\n"
+     "        a += 1\n"
+     "    if a == D:\n"
+     "        return a, path[:a], path[-1]\n"
+     "    return a, path[:a] + [target[a]], target[a]"),
+    ("knobs_ignore_p_min_sign", "    if p_min <= 0.0:\n        return toks, idx, score",
+     "    if p_min <= 0.5:\n        return toks, idx, score"),
+    ("knobs_score_not_kept", "return toks[:keep], idx[:keep], float(np.sum(t[:keep]))",
+     "return toks[:keep], idx[:keep], float(np.sum(t))"),
+    ("counters_fewer_drafts_ignored", "        n = self.n_spec if n_draft is None else n_draft",
+     "        n = self.n_spec"),
+    ("draft_step_ctx_not_updated",
+     "            c = append_context(cfg, W, c, new_taps[s], P0, st)\n        out_ctx.append(c)",
+     "            append_context(cfg, W, c, new_taps[s], P0, st)\n        out_ctx.append(c)"),
+    ("draft_step_anchor_of_next_seq", "        logits.append(draft_block(cfg, W, int(anchor), c, st))",
+     "        logits.append(draft_block(cfg, W, int(anchors[(s + 1) % len(anchors)]), c, st))"),
+    ("selector_final_argmin", "    j = int(np.argmax(delta))",
+     "    j = int(np.argmax(delta[::-1]))\n    j = len(delta) - 1 - j"),
+    ("selector_backtrack_off_by_one", "    for bp in reversed(back):\n        j = int(bp[j])",
+     "    for bp in back:\n        j = int(bp[j])"),
+    ("conv_kernel_size_ignored", "    for j in range(kernel_size):", "    for j in range(2):"),
+    ("rope_theta_ignored", "inv_freq = float(theta) ** (", "inv_freq = float(10000.0) ** ("),
+    ("loss_decay_gamma_inverted", "return np.exp(-(k - 1.0) / gamma)", "return np.exp(-(k - 1.0) * gamma / 49.0)"),
+    ("window_counts_block", "ctxK[max(0, ctxK.shape[0] - win):], ctxV[max(0, ctxV.shape[0] - win):]",
+     "ctxK[max(0, ctxK.shape[0] - max(0, win - B)):], ctxV[max(0, ctxV.shape[0] - max(0, win - B)):]"),
+    ("features_taps_reversed", '    x = _f64(taps) @ _f64(W["fc"]).T', '    x = _f64(taps)[:, ::-1] @ _f64(W["fc"]).T'),
+    ("sampled_accept_le", "while a < n and float(u_accept[a]) < prob[a, path[a]]:",
+     "while a < n and float(u_accept[a]) <= prob[a, path[a]]:"),
 ]
 
 

@@ -163,6 +163,24 @@ def test_dynamic_conv_is_left_looking_and_grouped():
     np.testing.assert_allclose(c[:, 0:8], 0.5 * (u + prev)[:, 0:8], atol=1e-12)
 
 
+def test_dynamic_conv_wider_window_reads_further_back():
+    # conv_kernel_size counts the taps: with three, a generator sending every
+    # group hard to tap 2 returns the row two positions back (zero before the
+    # block), and a zero generator the three-row average
+    g = np.random.default_rng(26)
+    H, gs, Kc = 16, 8, 3
+    u = g.standard_normal((6, H))
+    w = np.zeros((Kc * (H // gs), H))
+    w[Kc * 0 + 2] = w[Kc * 1 + 2] = 100.0
+    c = O.dynamic_conv(np.abs(u) + 0.5, w, gs, kernel_size=Kc)
+    back2 = np.vstack([np.zeros((2, H)), (np.abs(u) + 0.5)[:-2]])
+    np.testing.assert_allclose(c, back2, atol=1e-12)
+    c0 = O.dynamic_conv(u, np.zeros_like(w), gs, kernel_size=Kc)
+    p1 = np.vstack([np.zeros((1, H)), u[:-1]])
+    p2 = np.vstack([np.zeros((2, H)), u[:-2]])
+    np.testing.assert_allclose(c0, (u + p1 + p2) / 3.0, atol=1e-15)
+
+
 # ------------------------------------------------------------------ attention
 
 def test_block_attention_special_cases():
@@ -488,6 +506,26 @@ def test_context_appended_in_two_steps_equals_one_append():
             np.testing.assert_allclose(twice[l][i], once[l][i], rtol=1e-12, atol=1e-13)
             np.testing.assert_allclose(c2[0][l][i], once[l][i], rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(z2[0], O.draft_block(cfg, W, 7, once, st), rtol=1e-10, atol=1e-12)
+
+
+def test_draft_step_sequences_are_independent():
+    """draft_step: a batch of sequences gives, row for row, what each
+    sequence gives alone (its own anchor, context and new taps)."""
+    cfg = tiny_cfg()
+    W = tiny_weights(cfg)
+    st = O.Store(False)
+    g = np.random.default_rng(27)
+    TH = cfg["n_taps"] * cfg["hidden"]
+    ctxs = [O.append_context(cfg, W, empty_ctx(cfg), g.standard_normal((n, TH)), 0, st) for n in (3, 6)]
+    new = [g.standard_normal((2, TH)), g.standard_normal((1, TH))]
+    anchors = [7, 11]
+    _, z, ids, vals = O.draft_step(cfg, W, ctxs, anchors, new, st)
+    for s in range(2):
+        _, z1, ids1, vals1 = O.draft_step(cfg, W, [ctxs[s]], [anchors[s]], [new[s]], st)
+        np.testing.assert_array_equal(z[s], z1[0])
+        np.testing.assert_array_equal(ids[s], ids1[0])
+        np.testing.assert_array_equal(vals[s], vals1[0])
+    assert not np.allclose(z[0], z[1])
 
 
 @pytest.mark.parametrize("kc", [0, 2])

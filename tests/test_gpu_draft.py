@@ -54,6 +54,16 @@ def test_small_bf16_paged_ragged_batch():
     check_case(case)
 
 
+@pytest.mark.parametrize("block_size,top_k", [(2, 8), (8, 1), (2, 1)])
+def test_degenerate_block_and_candidate_counts(block_size, top_k):
+    # the method's degenerate cases: one draft per step (block 2, so the
+    # lm_head reads one row per sequence) and one candidate per position
+    # (top-k 1); ragged appends including none
+    cfg = S.small_bf16_config(block_size=block_size, top_k=top_k, index=51)
+    case = Case(cfg, ctx_lens=[40, 0, 131], n_new=[block_size, 1, 0], seed=51).run_gpu()
+    check_case(case)
+
+
 def test_fp32_rows_beyond_fused_prologue():
     # 32 block rows x 2048 fp32 channels (256 KiB) exceed the fused sublayer
     # prologue's shared memory: norm, tap GEMM and conv run as three kernels

@@ -59,6 +59,11 @@ def run_select(dtype, V, H, k, D, r, b, seed, emb_std=1.0, sel_std=0.3, logit_st
     ("bf16", 151936, 4096, 16, 7, 64, 2),
     ("bf16", 5000, 512, 16, 15, 64, 2),
     ("f32", 4096, 256, 4, 7, 16, 3),
+    # degenerate lattices: one candidate per position (the single path), one
+    # draft position (the anchor's transitions only), both
+    ("bf16", 1000, 128, 1, 7, 16, 3),
+    ("bf16", 1000, 128, 4, 1, 16, 3),
+    ("bf16", 1000, 128, 1, 1, 16, 3),
 ])
 def test_selector_matches_oracle_viterbi(dtype, V, H, k, D, r, b, kind):
     cfg, W, anchor, cand, z, path, score = run_select(dtype, V, H, k, D, r, b, seed=V + k, kind=kind)

@@ -64,6 +64,14 @@ def test_degenerate_block_and_candidate_counts(block_size, top_k):
     check_case(case)
 
 
+def test_bf16_largest_block():
+    # block 32 (31 drafts), the largest the library takes: 64 query rows per
+    # kv head in the attention, 31 lm_head rows per sequence
+    cfg = S.small_bf16_config(block_size=32, index=52)
+    case = Case(cfg, ctx_lens=[100, 7], n_new=[32, 5], seed=52).run_gpu()
+    check_case(case)
+
+
 def test_fp32_rows_beyond_fused_prologue():
     # 32 block rows x 2048 fp32 channels (256 KiB) exceed the fused sublayer
     # prologue's shared memory: norm, tap GEMM and conv run as three kernels

@@ -64,6 +64,9 @@ def run_select(dtype, V, H, k, D, r, b, seed, emb_std=1.0, sel_std=0.3, logit_st
     ("bf16", 1000, 128, 1, 7, 16, 3),
     ("bf16", 1000, 128, 4, 1, 16, 3),
     ("bf16", 1000, 128, 1, 1, 16, 3),
+    # the largest rank (128) and the largest block (31 positions)
+    ("bf16", 5000, 512, 16, 7, 128, 2),
+    ("bf16", 2000, 128, 8, 31, 32, 2),
 ])
 def test_selector_matches_oracle_viterbi(dtype, V, H, k, D, r, b, kind):
     cfg, W, anchor, cand, z, path, score = run_select(dtype, V, H, k, D, r, b, seed=V + k, kind=kind)

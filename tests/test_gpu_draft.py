@@ -64,6 +64,13 @@ def test_degenerate_block_and_candidate_counts(block_size, top_k):
     check_case(case)
 
 
+def test_small_bf16_empty_batch_context():
+    # no sequence has context or appends anything: stage (a) is skipped and
+    # every block attends to its own keys only
+    cfg = S.small_bf16_config(index=53)
+    check_case(Case(cfg, ctx_lens=[0, 0, 0], n_new=[0, 0, 0], seed=53).run_gpu())
+
+
 def test_bf16_largest_block():
     # block 32 (31 drafts), the largest the library takes: 64 query rows per
     # kv head in the attention, 31 lm_head rows per sequence

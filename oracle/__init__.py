@@ -2,8 +2,8 @@
 
 TEST INFRASTRUCTURE ONLY.  Nothing in the product path (the CUDA library and
 its Python binding) may import, call or execute anything in this package.
-Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
-``bench.py`` use it.  It shares no code with the CUDA path.
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline and
+reference legs of ``bench.py`` use it.  It shares no code with the CUDA path.
 
 The oracle is plain numpy in float64.  Each function cites the passage of
 the source pages it follows, by page title and section:

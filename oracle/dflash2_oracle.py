@@ -1,7 +1,8 @@
 """Plain, slow, float64 reference of the DFlash2 draft step, selector and verify.
 
 TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
-and the CPU-baseline leg of ``bench.py``, never by the product path.  It shares
+and the CPU-baseline and reference legs of ``bench.py``, never by the product
+path.  It shares
 no code with the CUDA library.
 
 Pages cited (title, then section):

@@ -2,8 +2,7 @@
 
 TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
 and the CPU-baseline and reference legs of ``bench.py``, never by the product
-path.  It shares
-no code with the CUDA library.
+path.  It shares no code with the CUDA library.
 
 Pages cited (title, then section):
   [Train]  "Train a DFlash Drafter for Speculative Decoding"

@@ -342,8 +342,10 @@ int launch_viterbi(const float* Y, const float* table, const int32_t* anchor, in
                    const float* cand_logit, int batch, int D, int k, int r, int32_t* path, float* path_score,
                    const Ctx& c, int n_max, float p_min, int32_t* n_draft) {
   if (Y && table) return DFLASH2_ERR_INVALID_ARG;
-  if (n_max < 0 || n_max > D || !(p_min >= 0.f) || p_min > 1.f) return DFLASH2_ERR_SHAPE;
-  const int Dp = n_max == 0 ? D : n_max;
+  if (n_max < 0 || !(p_min >= 0.f) || p_min > 1.f) return DFLASH2_ERR_SHAPE;
+  // a request past the block is clamped to its B - 1 drafts ("DFlash2
+  // Speculative Decoding" (llama-cpp-python wiki), "Configuration Notes")
+  const int Dp = (n_max == 0 || n_max > D) ? D : n_max;
   const float log_p_min = p_min > 0.f ? logf(p_min) : -INFINITY;
   const size_t smem = viterbi_smem_bytes(D, k, r);
   static bool attr = false;

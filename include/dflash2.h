@@ -349,8 +349,10 @@ int dflash2_select_path_table(const dflash2_config *cfg, int batch, const int32_
  * "Configuration Notes": draft_n_max bounds the tokens drafted per step;
  * drafting stops early at a low-confidence selector transition,
  * draft_p_min).  Host struct.
- *   n_max  drafts per step, 1..B-1 (0 = B-1): the selector walks positions
- *          1..n_max only (the max-score path over that shorter lattice)
+ *   n_max  drafts per step (0 = B-1; a request above B-1 is clamped to B-1,
+ *          as the same section says the engine does): the selector walks
+ *          positions 1..n_max only (the max-score path over that shorter
+ *          lattice)
  *   p_min  in [0, 1]: the path is cut before the first position whose chosen
  *          transition has probability exp(T_i(prev, chosen)) < p_min
  *          (0 = never cut)
@@ -364,8 +366,8 @@ typedef struct dflash2_draft_opts {
  * dflash2_select_path / dflash2_select_path_table with drafting knobs (opts
  * nullable: no knobs).  n_draft: nullable [batch] int32 out, the drafts kept
  * (0..n_max); path slots from n_draft on are -1; path_score is the kept
- * positions' summed log-probability.  DFLASH2_ERR_SHAPE for n_max outside
- * 0..B-1 or p_min outside [0, 1].
+ * positions' summed log-probability.  DFLASH2_ERR_SHAPE for a negative n_max
+ * or p_min outside [0, 1].
  */
 int dflash2_select_path_ex(const dflash2_config *cfg, const dflash2_weights *w, int batch,
                            const int32_t *anchor, const int32_t *cand_id, const float *cand_logit,

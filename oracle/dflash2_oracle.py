@@ -434,11 +434,13 @@ def select_path_knobs(cfg, W, anchor, cand_id, cand_z, n_max=0, p_min=0.0):
     whose confidence is below draft_p_min).  (A reading where the pages are
     silent.)
 
-    The max-score path over positions 1..n_max only (n_max = 0: all D), then
-    cut before the first position whose chosen transition has probability
-    exp(T_i) < p_min.  Returns (kept tokens, kept indices, the kept
-    positions' summed log-probability)."""
-    n = len(cand_id) if n_max == 0 else n_max
+    The max-score path over positions 1..n_max only (n_max = 0: all D; a
+    request above D is clamped to D, as the same section says the engine
+    clamps draft_n_max to block_size - 1), then cut before the first
+    position whose chosen transition has probability exp(T_i) < p_min.
+    Returns (kept tokens, kept indices, the kept positions' summed
+    log-probability)."""
+    n = len(cand_id) if n_max == 0 else min(n_max, len(cand_id))
     toks, idx, score = select_path(cfg, W, anchor, np.asarray(cand_id)[:n], np.asarray(cand_z)[:n])
     if p_min <= 0.0:
         return toks, idx, score

@@ -158,11 +158,13 @@ def test_selector_table_flags_bad_tokens():
 
 
 @pytest.mark.parametrize("kind", ["gemm", "table"])
-@pytest.mark.parametrize("n_max,p_min", [(3, 0.0), (7, 0.2), (5, 0.35), (1, 0.0), (7, 0.99), (0, 0.5)])
+@pytest.mark.parametrize("n_max,p_min", [(3, 0.0), (7, 0.2), (5, 0.35), (1, 0.0), (7, 0.99), (0, 0.5),
+                                         (12, 0.35)])
 def test_selector_drafting_knobs_match_oracle(kind, n_max, p_min):
     """draft_n_max / draft_p_min: the walk over positions 1..n_max and the
     cut at the first low-confidence transition, against the oracle on the
-    same lattice (paths, kept counts exactly; scores to 1e-3)."""
+    same lattice (paths, kept counts exactly; scores to 1e-3).  A request
+    above B-1 drafts is clamped to B-1."""
     import torch
     B = lib()
     V, H, k, D, r, b = 1000, 128, 4, 7, 16, 16
@@ -208,7 +210,7 @@ def test_selector_drafting_knobs_match_oracle(kind, n_max, p_min):
         assert nd[s] == n, (s, nd[s], n)
         assert list(path[s, :n]) == list(p) and np.all(path[s, n:] == -1)
         assert abs(score[s] - sc) < 1e-3 * max(1.0, abs(sc))
-        cut += int(n < (n_max or D))
+        cut += int(n < (min(n_max, D) or D))
         assert np.all(t >= math.log(p_min) - 1e-9) if p_min > 0 else True
     if p_min in (0.35, 0.5, 0.99):
         assert cut > 0  # the lattice really exercises the cut

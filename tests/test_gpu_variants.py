@@ -54,7 +54,7 @@ def test_sliding_window_qwen3_8b_shape():
     check_case(case, tol=e2e_tol("qwen3_8b_b1_window512"), name="qwen3_8b_b1_window512")
 
 
-@pytest.mark.parametrize("n_max,p_min", [(0, 0.0), (4, 0.0), (0, 0.3), (7, 0.6)])
+@pytest.mark.parametrize("n_max,p_min", [(0, 0.0), (4, 0.0), (0, 0.3), (7, 0.6), (10, 0.3)])
 def test_top1_selection_with_knobs(n_max, p_min):
     """dflash2_select_top1: the per-position top-1 path, cut by the softmax
     of the candidate logits (the oracle's selector without its pairwise

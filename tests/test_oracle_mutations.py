@@ -149,8 +149,10 @@ MUTATIONS = [
     ("histogram_counts_drafts", "self.hist[a] += 1", "self.hist[n - a] += 1"),
     ("acceptance_rate_over_steps", "return self.accepted / self.drafted if self.drafted else 0.0",
      "return self.accepted / self.steps if self.steps else 0.0"),
-    ("knobs_n_max_off_by_one", "n = len(cand_id) if n_max == 0 else n_max",
-     "n = len(cand_id) if n_max == 0 else n_max + 1"),
+    ("knobs_n_max_off_by_one", "n = len(cand_id) if n_max == 0 else min(n_max, len(cand_id))",
+     "n = len(cand_id) if n_max == 0 else min(n_max + 1, len(cand_id))"),
+    ("knobs_n_max_not_clamped", "n = len(cand_id) if n_max == 0 else min(n_max, len(cand_id))",
+     "n = len(cand_id) if n_max == 0 else n_max"),
     ("knobs_cut_after", "return toks[:keep], idx[:keep], float(np.sum(t[:keep]))",
      "return toks[:keep + 1], idx[:keep + 1], float(np.sum(t[:keep + 1]))"),
     ("spec_loop_anchor_not_next", "t = [toy_target_next(table, anchor)] + [toy_target_next(table, p) for p in path]",

@@ -772,6 +772,22 @@ def test_draft_n_max_walks_the_shorter_lattice(k, D, n_max, seed):
     assert list(idx) == list(idxb) and abs(s - sb) < 1e-12 and len(p) == n_max
 
 
+@pytest.mark.parametrize("p_min", [0.0, 0.2])
+def test_draft_n_max_above_the_block_is_clamped(p_min):
+    # [llama] "Configuration Notes": the engine clamps draft_n_max to
+    # block_size - 1, so any request from D up walks the whole lattice
+    cfg = tiny_cfg(top_k=3, selector_rank=4)
+    W = tiny_weights(cfg, seed=28)
+    g = np.random.default_rng(28)
+    D = 5
+    cand = np.stack([g.choice(cfg["vocab"] - 1, 3, replace=False) for _ in range(D)])
+    z = -np.sort(-g.standard_normal((D, 3)), axis=1) + 2.0   # confident rows: few cuts
+    whole = O.select_path_knobs(cfg, W, 1, cand, z, n_max=0, p_min=p_min)
+    for n_max in (D, D + 1, D + 9):
+        got = O.select_path_knobs(cfg, W, 1, cand, z, n_max=n_max, p_min=p_min)
+        assert list(got[1]) == list(whole[1]) and got[2] == whole[2]
+
+
 def test_draft_p_min_cut_closed_form():
     # no pairwise term: T_i(j) = log softmax(z_i)[j] and the path is the
     # per-position top-1.  Rows whose entries are log-probabilities already

@@ -6,8 +6,9 @@
  *   dflash2_draft_step     stages (a)-(c): feature projection + context K/V
  *                          append, one non-causal block forward, lm_head with
  *                          a fused streaming top-k (the candidate lattice);
- *   dflash2_select_path    stage (d1): pairwise low-rank selector (Viterbi);
- *   dflash2_verify_accept  stage (d2): greedy verify, accept, rollback and
+ *   dflash2_select_path    stage (d): pairwise low-rank selector (factors +
+ *                          Viterbi);
+ *   dflash2_verify_accept  stage (d): greedy verify, accept, rollback and
  *                          counters.
  *
  * dflash2_append_context runs stage (a) alone (e.g. to prefill a prompt).
@@ -100,7 +101,8 @@ extern "C" {
  *   rope_theta             rotary base
  *   input_embedding_scale  multiplies the embedded block (1 = identity)
  *   output_multiplier      multiplies the logits (1 = identity)
- *   final_logit_softcap    cap*tanh(z/cap) when > 0 (0 = off)
+ *   final_logit_softcap    cap*tanh(z/cap) when > 0, on the multiplied logits
+ *                          (0 = off)
  *   sliding_window         draft_sliding_window ("Key Config Fields"): when > 0 the
  *                          block reads only the last sliding_window context
  *                          positions (and all its own); 0 = the whole prefix
